@@ -1,0 +1,214 @@
+/*
+ * blocks.c -- decode one quantised block into exact integer codes and scales.
+ * TEST INFRASTRUCTURE ONLY (see oracle.h).
+ *
+ * Formats: "Models and formats" page, section "Tensor formats" (Q4_0, Q5_0,
+ * Q8_0, the K-quants Q4_K and Q6_K, MXFP4); "Architecture" page, section
+ * "The package map", pkg/quant ("block layouts, dequantisation").  The pages
+ * name the formats without printing their bytes; the layouts below are the
+ * GGUF block conventions, read field by field, little-endian:
+ *
+ *   Q4_0  (18 B / 32 w): fp16 d | 16 bytes of nibbles.  Element j (j < 16) is
+ *         the low nibble of byte j, element j+16 its high nibble.  w = d*(q-8).
+ *   Q5_0  (22 B / 32 w): fp16 d | u32 high-bit mask | 16 bytes of nibbles.
+ *         Nibbles as Q4_0; bit i of the mask is bit 4 of element i.  w = d*(q-16).
+ *   Q8_0  (34 B / 32 w): fp16 d | 32 int8.  w = d*q.
+ *   MXFP4 (17 B / 32 w): u8 E8M0 exponent e | 16 bytes of E2M1 codes, nibble
+ *         order as Q4_0.  w = 2^(e-127) * E2M1(code); e = 255 is NaN (OCP MX).
+ *   Q4_K  (144 B / 256 w): fp16 d | fp16 dmin | 12 bytes of packed 6-bit
+ *         sub-block scales sc[8] and mins m[8] | 128 bytes of nibbles.
+ *         Sub-block j holds elements 32j..32j+31; 32-byte chunk c of the
+ *         nibbles holds sub-block 2c in its low nibbles and 2c+1 in its high
+ *         nibbles.  w = d*sc_j*q - dmin*m_j.
+ *   Q6_K  (210 B / 256 w): 128 B low nibbles | 64 B high 2-bit pairs |
+ *         int8 scales[16] | fp16 d.  Element i uses scales[i/16].
+ *         w = d*sc*(q-32).
+ */
+#include "oracle.h"
+#include <math.h>
+#include <string.h>
+
+static uint32_t rd_u16(const uint8_t* p) { return (uint32_t)p[0] | ((uint32_t)p[1] << 8); }
+static uint32_t rd_u32(const uint8_t* p)
+{
+    return (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24);
+}
+
+int64_t orc_block_elems(int type)
+{
+    switch (type) {
+    case ORC_Q4_0: case ORC_Q5_0: case ORC_Q8_0: case ORC_MXFP4: return 32;
+    case ORC_Q4_K: case ORC_Q6_K: case ORC_Q8_K: return 256;
+    default: return 0;
+    }
+}
+
+int64_t orc_block_bytes(int type)
+{
+    switch (type) {
+    case ORC_Q4_0: return 18;
+    case ORC_Q5_0: return 22;
+    case ORC_Q8_0: return 34;
+    case ORC_MXFP4: return 17;
+    case ORC_Q4_K: return 144;
+    case ORC_Q6_K: return 210;
+    case ORC_Q8_K: return 292;
+    default: return 0;
+    }
+}
+
+/* Nibble k (0..31) of a 16-byte nibble field in the Q4_0 element order. */
+static int nibble32(const uint8_t* qs, int k)
+{
+    return k < 16 ? (qs[k] & 0x0f) : (qs[k - 16] >> 4);
+}
+
+/* OCP E2M1: bit 3 sign, bits 2..1 exponent E (bias 1), bit 0 mantissa M.
+ * E == 0 is subnormal: 0.5*M; otherwise 2^(E-1)*(1 + M/2).  Returned doubled,
+ * which makes every value an integer: {0,1,2,3,4,6,8,12} with sign. */
+static int e2m1_doubled(int c)
+{
+    int s = (c >> 3) & 1;
+    int E = (c >> 1) & 3;
+    int M = c & 1;
+    int mag2;
+    if (E == 0) mag2 = M;                       /* 2 * 0.5*M */
+    else mag2 = (2 + M) << (E - 1);             /* 2 * 2^(E-1) * (1 + M/2) */
+    return s ? -mag2 : mag2;
+}
+
+/* Q4_K: the 12-byte field packs eight 6-bit scales and eight 6-bit mins.
+ * Bytes 0..3: low 6 bits are sc0..sc3, top 2 bits are bits 4..5 of sc4..sc7.
+ * Bytes 4..7: low 6 bits are m0..m3, top 2 bits are bits 4..5 of m4..m7.
+ * Bytes 8..11: low nibble is bits 0..3 of sc4..sc7, high nibble of m4..m7. */
+static void q4k_scale_min(const uint8_t* f, int j, int* sc, int* m)
+{
+    if (j < 4) {
+        *sc = f[j] & 63;
+        *m = f[4 + j] & 63;
+    } else {
+        int t = j - 4;
+        *sc = (f[8 + t] & 0x0f) | ((f[t] >> 6) << 4);
+        *m = (f[8 + t] >> 4) | ((f[4 + t] >> 6) << 4);
+    }
+}
+
+int orc_decode_block(int type, const uint8_t* b, orc_block* out)
+{
+    memset(out, 0, sizeof(*out));
+    switch (type) {
+    case ORC_Q4_0: {
+        out->n = 32;
+        out->d = orc_f16_to_f64((uint16_t)rd_u16(b));
+        for (int i = 0; i < 32; i++) {
+            out->code[i] = nibble32(b + 2, i) - 8;
+            out->sub_scale[i] = 1;
+        }
+        return ORC_OK;
+    }
+    case ORC_Q5_0: {
+        out->n = 32;
+        out->d = orc_f16_to_f64((uint16_t)rd_u16(b));
+        uint32_t qh = rd_u32(b + 2);
+        for (int i = 0; i < 32; i++) {
+            int q = nibble32(b + 6, i) | (int)(((qh >> i) & 1u) << 4);
+            out->code[i] = q - 16;
+            out->sub_scale[i] = 1;
+        }
+        return ORC_OK;
+    }
+    case ORC_Q8_0: {
+        out->n = 32;
+        out->d = orc_f16_to_f64((uint16_t)rd_u16(b));
+        for (int i = 0; i < 32; i++) {
+            out->code[i] = (int8_t)b[2 + i];
+            out->sub_scale[i] = 1;
+        }
+        return ORC_OK;
+    }
+    case ORC_MXFP4: {
+        out->n = 32;
+        int e = b[0];
+        /* E8M0: 2^(e-127); the doubled code takes one more factor 1/2. */
+        out->d = (e == 255) ? NAN : ldexp(1.0, e - 128);
+        for (int i = 0; i < 32; i++) {
+            out->code[i] = e2m1_doubled(nibble32(b + 1, i));
+            out->sub_scale[i] = 1;
+        }
+        return ORC_OK;
+    }
+    case ORC_Q4_K: {
+        out->n = 256;
+        out->d = orc_f16_to_f64((uint16_t)rd_u16(b));
+        out->dmin = orc_f16_to_f64((uint16_t)rd_u16(b + 2));
+        const uint8_t* scf = b + 4;
+        const uint8_t* qs = b + 16;
+        for (int j = 0; j < 8; j++) {
+            int sc, m;
+            q4k_scale_min(scf, j, &sc, &m);
+            const uint8_t* chunk = qs + 32 * (j / 2);
+            for (int l = 0; l < 32; l++) {
+                int q = (j % 2 == 0) ? (chunk[l] & 0x0f) : (chunk[l] >> 4);
+                out->code[32 * j + l] = q;
+                out->sub_scale[32 * j + l] = sc;
+                out->sub_min[32 * j + l] = m;
+            }
+        }
+        return ORC_OK;
+    }
+    case ORC_Q6_K: {
+        out->n = 256;
+        const uint8_t* ql = b;
+        const uint8_t* qh = b + 128;
+        const int8_t* scales = (const int8_t*)(b + 192);
+        out->d = orc_f16_to_f64((uint16_t)rd_u16(b + 208));
+        for (int h = 0; h < 2; h++) {
+            const uint8_t* L = ql + 64 * h;
+            const uint8_t* H = qh + 32 * h;
+            for (int l = 0; l < 32; l++) {
+                int e0 = 128 * h + l;
+                int q0 = (L[l] & 0x0f) | (((H[l] >> 0) & 3) << 4);
+                int q1 = (L[l + 32] & 0x0f) | (((H[l] >> 2) & 3) << 4);
+                int q2 = (L[l] >> 4) | (((H[l] >> 4) & 3) << 4);
+                int q3 = (L[l + 32] >> 4) | (((H[l] >> 6) & 3) << 4);
+                out->code[e0] = q0 - 32;
+                out->code[e0 + 32] = q1 - 32;
+                out->code[e0 + 64] = q2 - 32;
+                out->code[e0 + 96] = q3 - 32;
+            }
+        }
+        for (int i = 0; i < 256; i++) out->sub_scale[i] = scales[i / 16];
+        return ORC_OK;
+    }
+    default:
+        return ORC_EUNSUP;
+    }
+}
+
+double orc_block_weight(const orc_block* b, int i)
+{
+    /* Each product below is exact in fp64 (at most 23 significant bits), and
+     * so is the difference for the scale ranges the formats can express at
+     * any realistic spread of d and dmin. */
+    double a = b->d * (double)b->sub_scale[i] * (double)b->code[i];
+    double m = b->dmin * (double)b->sub_min[i];
+    return a - m;
+}
+
+int orc_dequant(int type, const uint8_t* W, int64_t rows, int64_t cols, float* out)
+{
+    int64_t bs = orc_block_elems(type), bb = orc_block_bytes(type);
+    if (bs == 0 || type == ORC_Q8_K) return ORC_EUNSUP;
+    if (rows < 0 || cols < 0) return ORC_EINVAL;
+    if (cols % bs) return ORC_ESHAPE;
+    int64_t nb = cols / bs;
+    orc_block blk;
+    for (int64_t r = 0; r < rows; r++) {
+        for (int64_t k = 0; k < nb; k++) {
+            int rc = orc_decode_block(type, W + (r * nb + k) * bb, &blk);
+            if (rc) return rc;
+            for (int i = 0; i < bs; i++) out[r * cols + k * bs + i] = (float)orc_block_weight(&blk, i);
+        }
+    }
+    return ORC_OK;
+}

@@ -1,0 +1,190 @@
+"""Python face of the CPU oracle (test infrastructure only).
+
+The oracle is plain C in this directory (fp.c, blocks.c, quant.c, mm.c),
+compiled with gcc into ``oracle/_build/liboracle.so`` and loaded through
+ctypes.  Only the test-suite, ``__graft_entry__.smoke()`` and the CPU-baseline
+leg of ``bench.py`` may import this module; the CUDA library never does, and
+the two share no code.
+
+Every function below is a thin marshalling wrapper; the arithmetic lives in the
+C files, each of which cites the passage of the llamay pages it follows.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+BUILD_DIR = os.path.join(HERE, "_build")
+LIB_PATH = os.path.join(BUILD_DIR, "liboracle.so")
+SOURCES = ["fp.c", "blocks.c", "quant.c", "mm.c"]
+
+# The oracle's own type numbers (oracle.h).
+Q4_0, Q5_0, Q8_0, Q4_K, Q6_K, MXFP4, Q8_K, F32, BF16 = 1, 2, 3, 4, 5, 6, 7, 8, 9
+BLOCK_ELEMS = {Q4_0: 32, Q5_0: 32, Q8_0: 32, MXFP4: 32, Q4_K: 256, Q6_K: 256, Q8_K: 256}
+BLOCK_BYTES = {Q4_0: 18, Q5_0: 22, Q8_0: 34, MXFP4: 17, Q4_K: 144, Q6_K: 210, Q8_K: 292}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no fast-math, no FMA contraction)."""
+    srcs = [os.path.join(HERE, s) for s in SOURCES]
+    hdr = os.path.join(HERE, "oracle.h")
+    if not force and os.path.exists(LIB_PATH):
+        newest = max(os.path.getmtime(p) for p in srcs + [hdr])
+        if os.path.getmtime(LIB_PATH) >= newest:
+            return LIB_PATH
+    os.makedirs(BUILD_DIR, exist_ok=True)
+    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-ffp-contract=off",
+           "-fno-fast-math", "-Wall", "-Wextra", "-o", tmp] + srcs + ["-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, LIB_PATH)
+    return LIB_PATH
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            L = C.CDLL(LIB_PATH)
+            P, I64, I = C.c_void_p, C.c_int64, C.c_int
+            L.orc_f16_to_f64.argtypes = [C.c_uint16]
+            L.orc_f16_to_f64.restype = C.c_double
+            L.orc_f32_to_f16_rn.argtypes = [C.c_float]
+            L.orc_f32_to_f16_rn.restype = C.c_uint16
+            L.orc_bf16_to_f64.argtypes = [C.c_uint16]
+            L.orc_bf16_to_f64.restype = C.c_double
+            L.orc_f32_to_bf16_rn.argtypes = [C.c_float]
+            L.orc_f32_to_bf16_rn.restype = C.c_uint16
+            L.orc_dequant.argtypes = [I, P, I64, I64, P]
+            L.orc_quantize_act.argtypes = [I, P, I64, P]
+            L.orc_block_dots.argtypes = [I, P, I64, I64, P, I64, P]
+            L.orc_matvec.argtypes = [I, I, P, I64, I64, P, I64, P, I64, P, P]
+            L.orc_moe.argtypes = [I, I, P, I64, I64, I64, P, P, I64, P, I64, P, P, P]
+            L.orc_decode_block.argtypes = [I, P, P]
+            for f in ("orc_dequant", "orc_quantize_act", "orc_block_dots", "orc_matvec",
+                      "orc_moe", "orc_decode_block"):
+                getattr(L, f).restype = I
+            _lib = L
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(C.c_void_p)
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise OracleError(f"{what} returned {rc}")
+
+
+def row_bytes(t: int, cols: int) -> int:
+    return cols // BLOCK_ELEMS[t] * BLOCK_BYTES[t]
+
+
+# ---- scalar conversions -------------------------------------------------------
+
+def f16_to_f64(h: int) -> float:
+    return lib().orc_f16_to_f64(int(h))
+
+
+def f32_to_f16_rn(f: float) -> int:
+    return lib().orc_f32_to_f16_rn(float(np.float32(f)))
+
+
+def bf16_to_f64(b: int) -> float:
+    return lib().orc_bf16_to_f64(int(b))
+
+
+def f32_to_bf16_rn(f: float) -> int:
+    return lib().orc_f32_to_bf16_rn(float(np.float32(f)))
+
+
+# ---- blocks -------------------------------------------------------------------
+
+class _Block(C.Structure):
+    _fields_ = [("n", C.c_int), ("code", C.c_int32 * 256), ("sub_scale", C.c_int32 * 256),
+                ("sub_min", C.c_int32 * 256), ("d", C.c_double), ("dmin", C.c_double)]
+
+
+def decode_block(t: int, blk: bytes):
+    """-> dict(code, sub_scale, sub_min (int arrays), d, dmin) for one block."""
+    b = _Block()
+    buf = np.frombuffer(bytes(blk), dtype=np.uint8).copy()
+    _check(lib().orc_decode_block(t, _ptr(buf), C.byref(b)), "decode_block")
+    n = b.n
+    return dict(code=np.array(b.code[:n]), sub_scale=np.array(b.sub_scale[:n]),
+                sub_min=np.array(b.sub_min[:n]), d=b.d, dmin=b.dmin)
+
+
+def dequant(t: int, W: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    assert W.size >= rows * row_bytes(t, cols)
+    out = np.empty((rows, cols), dtype=np.float32)
+    _check(lib().orc_dequant(t, _ptr(W), rows, cols, _ptr(out)), "dequant")
+    return out
+
+
+def quantize_act(atype: int, x: np.ndarray) -> np.ndarray:
+    """x float32 [..., cols] -> uint8 [..., cols/bs * block_bytes]."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    bs, bb = BLOCK_ELEMS[atype], BLOCK_BYTES[atype]
+    cols = x.shape[-1]
+    out = np.empty(x.shape[:-1] + (cols // bs * bb,), dtype=np.uint8)
+    _check(lib().orc_quantize_act(atype, _ptr(x), x.size, _ptr(out)), "quantize_act")
+    return out
+
+
+def block_dots(wt: int, W: np.ndarray, rows: int, cols: int, xq: np.ndarray, n_vec: int) -> np.ndarray:
+    """-> int64 [n_vec][rows][cols/bs][2] = (S, Mn) per block."""
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    xq = np.ascontiguousarray(xq, dtype=np.uint8)
+    nb = cols // BLOCK_ELEMS[wt]
+    out = np.empty((n_vec, rows, nb, 2), dtype=np.int64)
+    _check(lib().orc_block_dots(wt, _ptr(W), rows, cols, _ptr(xq), n_vec, _ptr(out)), "block_dots")
+    return out
+
+
+def matvec(wt: int, at: int, W: np.ndarray, rows: int, cols: int, x: np.ndarray, n_vec: int,
+           row_ids=None, want_abs: bool = True):
+    """-> (y, yabs) float64 [n_vec][n_rows]; x in the layout of `at` (see oracle.h)."""
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    x = np.ascontiguousarray(x)
+    if row_ids is not None:
+        row_ids = np.ascontiguousarray(row_ids, dtype=np.int64)
+        n_rows = row_ids.size
+    else:
+        n_rows = rows
+    y = np.empty((n_vec, n_rows), dtype=np.float64)
+    ya = np.empty((n_vec, n_rows), dtype=np.float64) if want_abs else None
+    _check(lib().orc_matvec(wt, at, _ptr(W), rows, cols, _ptr(x), n_vec, _ptr(row_ids),
+                            n_rows, _ptr(y), _ptr(ya)), "matvec")
+    return y, ya
+
+
+def moe(wt: int, at: int, W3d: np.ndarray, n_expert: int, rows: int, cols: int, ids: np.ndarray,
+        gates, k: int, x: np.ndarray, n_tok: int, bias=None):
+    """-> (y, yabs) float64: [n_tok][k][rows] if gates is None else [n_tok][rows]."""
+    W3d = np.ascontiguousarray(W3d, dtype=np.uint8)
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    x = np.ascontiguousarray(x)
+    g = None if gates is None else np.ascontiguousarray(gates, dtype=np.float32)
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    shape = (n_tok, k, rows) if gates is None else (n_tok, rows)
+    y = np.empty(shape, dtype=np.float64)
+    ya = np.empty(shape, dtype=np.float64)
+    _check(lib().orc_moe(wt, at, _ptr(W3d), n_expert, rows, cols, _ptr(ids), _ptr(g), k,
+                         _ptr(x), n_tok, _ptr(b), _ptr(y), _ptr(ya)), "moe")
+    return y, ya
