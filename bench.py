@@ -1,0 +1,383 @@
+#!/usr/bin/env python
+"""Benchmark of the block-quantised decode path on GB300.
+
+Workload (one step): a Qwen2.5-0.5B-shaped decode step through the W4A8 path
+-- for each of 24 layers, the fp32 activations are quantised to Q8_0 blocks
+and multiplied by q 896x896, k 128x896, v 128x896, o 896x896, gate 4864x896,
+up 4864x896 and down 896x4864 weights in Q5_0; then the lm_head 151936x896 in
+Q8_0.  169 matvecs and 97 activation quantisations; 390,648,832 weight bytes
+per step (372.55 MiB), synthetic weights and N(0,1) activations, batch 1.
+The weights (> 3x the 129 MB L2) are streamed cold every step.
+
+Metric: weight GB/s = weight bytes of the step / step time (higher is
+better), reported against the HBM roofline.  The step is captured once in a
+CUDA graph and replayed; timing uses CUDA events on the replay stream.
+
+Also reported: batch-8 decode of the same step, the lm_head matvec alone
+(the dominant kernel, for the roofline), end-to-end through host buffers, and
+the CPU oracle on a bounded sample (cpu_baseline).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gguf_block_quantised_gb300 import synth  # noqa: E402
+
+Q4_0, Q5_0, Q8_0, Q4_K, Q6_K, MXFP4, Q8_K, F32, BF16 = 1, 2, 3, 4, 5, 6, 7, 8, 9
+LAYERS = 24
+HID, FFN, KV, VOCAB = 896, 4864, 128, 151936
+# (name, rows, cols, input index) per layer; inputs: 0 attn-in, 1 o-in, 2 ffn-in, 3 down-in
+LAYER_MATS = [("q", HID, HID, 0), ("k", KV, HID, 0), ("v", KV, HID, 0), ("o", HID, HID, 1),
+              ("gate", FFN, HID, 2), ("up", FFN, HID, 2), ("down", HID, FFN, 3)]
+IN_COLS = [HID, HID, HID, FFN]
+
+
+def row_bytes(t, cols):
+    return synth.row_bytes(t, cols)
+
+
+STEP_WEIGHT_BYTES = LAYERS * sum(r * row_bytes(Q5_0, c) for _, r, c, _ in LAYER_MATS) + VOCAB * row_bytes(Q8_0, HID)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            hbm = d.get("hbm_gbs") or d.get("hbm_GBps")
+            if hbm:
+                return float(hbm), "measured"
+        except Exception:
+            pass
+    return 6800.0, "fallback"
+
+
+# ---- clocks sampled during the timed region -----------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---- the decode step ---------------------------------------------------------------------
+class DecodeStep:
+    """Weights and buffers of the Qwen2.5-0.5B-shaped decode step on one device."""
+
+    def __init__(self, q, torch, n_vec, seed=1):
+        self.q, self.torch, self.n_vec = q, torch, n_vec
+        dev = torch.device("cuda")
+        self.W = []
+        tid = 0
+        for layer in range(LAYERS):
+            mats = []
+            for name, rows, cols, inp in LAYER_MATS:
+                mats.append((torch.from_numpy(synth.weights(Q5_0, rows, cols, seed=seed, tensor_id=tid)).to(dev),
+                             rows, cols, inp))
+                tid += 1
+            self.W.append(mats)
+        self.lm = torch.from_numpy(synth.weights(Q8_0, VOCAB, HID, seed=seed, tensor_id=tid)).to(dev)
+        # activations: 4 inputs per layer + the final hidden state
+        self.x_host = [synth.activations(n_vec, IN_COLS[i], seed=seed, tensor_id=10000 + 4 * l + i)
+                       for l in range(LAYERS) for i in range(4)] + [synth.activations(n_vec, HID, seed=seed,
+                                                                                       tensor_id=20000)]
+        self.x = [torch.from_numpy(a).to(dev) for a in self.x_host]
+        self.xq = [torch.empty(n_vec * q.qmv_row_bytes(Q8_0, a.shape[1]), dtype=torch.uint8, device=dev)
+                   for a in self.x_host]
+        self.y = [[torch.empty((n_vec, r), dtype=torch.float32, device=dev) for _, r, _, _ in LAYER_MATS]
+                  for _ in range(LAYERS)]
+        self.logits = torch.empty((n_vec, VOCAB), dtype=torch.float32, device=dev)
+        self.launches = LAYERS * (4 + 7) + 2
+
+    def run(self, stream):
+        q, n = self.q, self.n_vec
+        s = stream.cuda_stream
+        for l in range(LAYERS):
+            for i in range(4):
+                j = 4 * l + i
+                q.qmv_quantize_act(Q8_0, self.x[j], self.xq[j], n * IN_COLS[i], s)
+            for m, (W, rows, cols, inp) in enumerate(self.W[l]):
+                q.qmv_matvec(q.FMT(Q5_0, Q8_0), W, rows, cols, self.xq[4 * l + inp], self.y[l][m], n, s)
+        q.qmv_quantize_act(Q8_0, self.x[-1], self.xq[-1], n * HID, s)
+        q.qmv_matvec(q.FMT(Q8_0, Q8_0), self.lm, VOCAB, HID, self.xq[-1], self.logits, n, s)
+
+
+def time_graph(torch, fn, stream, steps, warmup, sampler_index=None):
+    """Capture fn(stream) once, replay warmup + steps times; returns (ms/step, clocks)."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn(stream)                      # build-time set-up outside the capture
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            fn(stream)
+    for _ in range(warmup):
+        g.replay()
+    stream.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = None
+    sampler = ClockSampler(sampler_index) if sampler_index is not None else None
+    if sampler:
+        sampler.__enter__()
+        time.sleep(0.3)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(steps):
+            g.replay()
+        end.record(stream)
+    end.synchronize()
+    if sampler:
+        sampler.__exit__(None, None, None)
+        clocks = sampler.summary()
+    return start.elapsed_time(end) / steps, clocks
+
+
+def cpu_baseline(n_steps=4):
+    """The oracle (single thread) on a bounded sample: n_steps full decode steps."""
+    from oracle import oracle as O
+    rng_w = []
+    tid = 0
+    for layer in range(LAYERS):
+        for name, rows, cols, inp in LAYER_MATS:
+            rng_w.append((synth.weights(Q5_0, rows, cols, seed=1, tensor_id=tid), rows, cols, inp, Q5_0))
+            tid += 1
+    lm = synth.weights(Q8_0, VOCAB, HID, seed=1, tensor_id=tid)
+    xs = [synth.activations(1, IN_COLS[i], seed=1, tensor_id=10000 + 4 * l + i) for l in range(LAYERS)
+          for i in range(4)]
+    xf = synth.activations(1, HID, seed=1, tensor_id=20000)
+    t0 = time.perf_counter()
+    for _ in range(n_steps):
+        xq = [O.quantize_act(O.Q8_0, a) for a in xs]
+        for k, (W, rows, cols, inp, t) in enumerate(rng_w):
+            O.matvec(t, O.Q8_0, W, rows, cols, xq[4 * (k // 7) + inp], 1, want_abs=False)
+        O.matvec(O.Q8_0, O.Q8_0, lm, VOCAB, HID, O.quantize_act(O.Q8_0, xf), 1, want_abs=False)
+    dt = time.perf_counter() - t0
+    return {"value": STEP_WEIGHT_BYTES * n_steps / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n_steps} full decode steps (batch 1, W4A8), single-threaded C oracle, {dt:.1f} s"}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from oracle import oracle as O  # noqa: F401
+    per = []
+    for _ in range(args.warmup):
+        cpu_baseline(1)
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        cpu_baseline(1)
+        per.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(per) / len(per)
+    value = STEP_WEIGHT_BYTES / (ms / 1e3) / 1e9
+    line = {"impl": "reference", "metric": "quant GEMV weight GB/s (decode step, W4A8)", "value": value,
+            "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8xint4->fp32",
+            "data": "synthetic",
+            "config": {"workload": "qwen2.5-0.5b-shaped decode step (24 layers Q5_0 + lm_head Q8_0), batch 1",
+                       "l2": "weights 390.6 MB > L2, streamed cold each step"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": "one full decode step per timed step, single-threaded C oracle"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import gguf_block_quantised_gb300 as q
+    from gguf_block_quantised_gb300 import build as B
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    if rank == 0 or ws == 1:
+        B.build()
+    if ws > 1:
+        torch.distributed.barrier()
+    q.load()
+    stream = torch.cuda.Stream()
+
+    # --- the step at batch 1 (the headline) and batch 8
+    step1 = DecodeStep(q, torch, 1)
+    step8 = DecodeStep(q, torch, 8)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ms1, clocks = time_graph(torch, step1.run, stream, args.steps, args.warmup, sampler_index=local)
+    ms8, _ = time_graph(torch, step8.run, stream, max(args.steps // 4, 10), args.warmup)
+    q.qmv_get_status(stream)
+    if ws > 1:
+        t = torch.tensor([ms1, ms8], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms1, ms8 = t.tolist()
+
+    # --- the dominant kernel alone: lm_head matvec (144.6 MB per launch, > L2)
+    lm_bytes = VOCAB * row_bytes(Q8_0, HID)
+    def lm_only(s):
+        q.qmv_matvec(q.FMT(Q8_0, Q8_0), step1.lm, VOCAB, HID, step1.xq[-1], step1.logits, 1, s.cuda_stream)
+    lm_reps = 200
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        lm_only(stream)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(lm_reps):
+                lm_only(stream)
+    g.replay()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+    e1.synchronize()
+    lm_ms = e0.elapsed_time(e1) / lm_reps
+    lm_gbs = lm_bytes / (lm_ms / 1e3) / 1e9
+
+    # --- end to end through host buffers: pinned activations in, logits out, per step
+    host_x = [torch.from_numpy(a).pin_memory() for a in step1.x_host]
+    host_logits = torch.empty((1, VOCAB), dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * 4 for t in host_x)
+    d2h = host_logits.numel() * 4
+
+    def e2e_step(s):
+        with torch.cuda.stream(s):
+            for dst, src in zip(step1.x, host_x):
+                dst.copy_(src, non_blocking=True)
+            step1.run(s)
+            host_logits.copy_(step1.logits, non_blocking=True)
+    e2e_steps = max(args.steps // 4, 10)
+    e2e_ms, _ = time_graph(torch, e2e_step, stream, e2e_steps, args.warmup)
+
+    hbm, peak_kind = load_peaks()
+    value = ws * STEP_WEIGHT_BYTES / (ms1 / 1e3) / 1e9
+    if rank != 0:
+        if ws > 1:
+            torch.distributed.barrier()
+        return 0
+    cpu = None if args.no_cpu_baseline else cpu_baseline(4)
+    launches_per_step = step1.launches
+    line = {
+        "metric": "quant GEMV weight GB/s (decode step, W4A8)",
+        "value": value,
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms1,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int8xint4->fp32",
+        "data": "synthetic",
+        "config": {"workload": "qwen2.5-0.5b-shaped decode step (24 layers q/k/v/o/gate/up/down Q5_0 + lm_head "
+                               "151936x896 Q8_0; activations quantised to Q8_0), batch 1",
+                   "weight_bytes_per_step": STEP_WEIGHT_BYTES, "parallelism": f"replicas x{ws}",
+                   "l2": "weights 390.6 MB > 129 MB L2, streamed cold every step (no flush needed)",
+                   "graph": "step captured once as a CUDA graph and replayed"},
+        "frac_of_hbm": value / ws / hbm,
+        "batch8": {"ms_per_step": ms8, "value": ws * STEP_WEIGHT_BYTES / (ms8 / 1e3) / 1e9, "unit": "GB/s",
+                   "vector_rate_tok_s": ws * 8 / (ms8 / 1e3)},
+        "roofline": {"bound": "hbm", "kernel": "k_gemv<Q8_0,A8,1> lm_head 151936x896",
+                     "achieved": lm_gbs, "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": lm_gbs / hbm, "traffic": None,
+                     "algorithmic_bytes_per_launch": lm_bytes, "launch_ms": lm_ms},
+        "clocks": clocks,
+        "e2e": {"value": ws * STEP_WEIGHT_BYTES / (e2e_ms / 1e3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "how": "pinned host activations copied in and logits copied out every step, all in one replayed "
+                       "CUDA graph on the caller's stream"},
+        "gpu_launches": launches_per_step * args.steps,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+    if ws > 1:
+        torch.distributed.barrier()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

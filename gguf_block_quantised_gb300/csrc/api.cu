@@ -1,0 +1,313 @@
+// api.cu -- the extern "C" boundary of libqmv (declared in include/qmv.h).
+//
+// Every entry point validates its arguments on the host, returns a negative
+// qmv_status without launching anything when they are wrong, and otherwise
+// only enqueues kernels on the caller's stream.  Unsupported input is refused
+// with a message naming what is supported ("Models and formats" page: anything
+// outside the supported set "is refused at load with a message naming what
+// does work"; "Tensor formats": rows that are not a multiple of 256 cannot be
+// K-quants).  Nothing here allocates device memory.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "common.cuh"
+#include "runtime.cuh"
+
+// Launchers defined in the kernel translation units.
+int qmv_launch_quantize(int atype, const float* x, void* xq, int64_t n, cudaStream_t st);
+int qmv_launch_dequant(int t, const void* W, int64_t rows, int64_t cols, float* out, cudaStream_t st);
+int qmv_launch_block_dots(int t, const void* W, int64_t rows, int64_t cols, const void* xq, int n_vec,
+                          int32_t* out, cudaStream_t st);
+int qmv_gemv_q4_0(bool, const void*, int64_t, int64_t, const void*, float*, int, cudaStream_t);
+int qmv_gemv_q5_0(bool, const void*, int64_t, int64_t, const void*, float*, int, cudaStream_t);
+int qmv_gemv_q8_0(bool, const void*, int64_t, int64_t, const void*, float*, int, cudaStream_t);
+int qmv_gemv_mxfp4(bool, const void*, int64_t, int64_t, const void*, float*, int, cudaStream_t);
+int qmv_gemv_q4_k(bool, const void*, int64_t, int64_t, const void*, float*, int, cudaStream_t);
+int qmv_gemv_q6_k(bool, const void*, int64_t, int64_t, const void*, float*, int, cudaStream_t);
+
+// The device status word: kernels OR fault bits into it (QMV_DEV_*).
+__device__ unsigned g_qmv_status;
+
+namespace qmv {
+
+unsigned* status_word()
+{
+    static std::atomic<unsigned*> cache[kMaxDevices];
+    const int d = current_device();
+    unsigned* p = (d >= 0 && d < kMaxDevices) ? cache[d].load(std::memory_order_acquire) : nullptr;
+    if (!p) {
+        void* a = nullptr;
+        if (cudaGetSymbolAddress(&a, g_qmv_status) != cudaSuccess) return nullptr;
+        p = static_cast<unsigned*>(a);
+        if (d >= 0 && d < kMaxDevices) cache[d].store(p, std::memory_order_release);
+    }
+    return p;
+}
+
+}  // namespace qmv
+
+namespace {
+
+thread_local std::string t_err;
+
+int fail(int code, const char* fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_err = buf;
+    return code;
+}
+
+int ok()
+{
+    t_err.clear();
+    return QMV_OK;
+}
+
+const char* type_name(int t)
+{
+    switch (t) {
+    case QMV_Q4_0: return "Q4_0";
+    case QMV_Q5_0: return "Q5_0";
+    case QMV_Q8_0: return "Q8_0";
+    case QMV_Q4_K: return "Q4_K";
+    case QMV_Q6_K: return "Q6_K";
+    case QMV_MXFP4: return "MXFP4";
+    case QMV_Q8_K: return "Q8_K";
+    case QMV_F32: return "F32";
+    case QMV_BF16: return "BF16";
+    default: return "unknown";
+    }
+}
+
+bool is_weight_type(int t)
+{
+    return t == QMV_Q4_0 || t == QMV_Q5_0 || t == QMV_Q8_0 || t == QMV_MXFP4 || t == QMV_Q4_K || t == QMV_Q6_K;
+}
+
+bool is_kquant(int t) { return t == QMV_Q4_K || t == QMV_Q6_K; }
+
+int paired_act(int wtype) { return is_kquant(wtype) ? QMV_Q8_K : QMV_Q8_0; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+const char* kWeightList = "Q4_0, Q5_0, Q8_0, MXFP4 (32-element blocks) and Q4_K, Q6_K (256-element blocks)";
+
+int check_weights(int wtype, const void* W, int64_t rows, int64_t cols)
+{
+    if (!is_weight_type(wtype))
+        return fail(QMV_ERR_UNSUPPORTED, "weight type %d (%s) is not supported; supported: %s", wtype,
+                    type_name(wtype), kWeightList);
+    if (rows < 0 || cols <= 0) return fail(QMV_ERR_INVALID_ARG, "rows must be >= 0 and cols > 0 (got %lld x %lld)",
+                                           (long long)rows, (long long)cols);
+    const int bs = qmv_block_elems(wtype);
+    if (cols % bs)
+        return fail(QMV_ERR_SHAPE,
+                    "%s rows hold %d-element blocks; cols = %lld is not a multiple of %d%s", type_name(wtype), bs,
+                    (long long)cols, bs,
+                    is_kquant(wtype) ? " (rows whose length is not a multiple of 256 are stored as Q4_0/Q5_0/Q8_0)"
+                                     : "");
+    if (cols > (int64_t)1 << 24) return fail(QMV_ERR_SHAPE, "cols = %lld is over the limit of 16777216", (long long)cols);
+    if (rows > 0 && !W) return fail(QMV_ERR_INVALID_ARG, "W is NULL");
+    if (W && !aligned(W, 16)) return fail(QMV_ERR_ALIGN, "W must start on a 16-byte boundary");
+    return QMV_OK;
+}
+
+int cuda_fail(const char* where)
+{
+    const cudaError_t e = cudaGetLastError();
+    return fail(QMV_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+struct Workspace {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+};
+std::mutex g_ws_mu;
+Workspace g_ws[qmv::kMaxDevices];
+
+}  // namespace
+
+extern "C" {
+
+int qmv_version(void) { return QMV_VERSION; }
+
+const char* qmv_strerror(int err)
+{
+    switch (err) {
+    case QMV_OK: return "ok";
+    case QMV_ERR_INVALID_ARG: return "invalid argument";
+    case QMV_ERR_SHAPE: return "unsupported shape";
+    case QMV_ERR_UNSUPPORTED: return "unsupported format";
+    case QMV_ERR_ALIGN: return "misaligned pointer";
+    case QMV_ERR_WORKSPACE: return "workspace missing or too small";
+    case QMV_ERR_CUDA: return "CUDA error";
+    case QMV_ERR_DEVICE_STATUS: return "fault reported by a kernel";
+    default: return "unknown error";
+    }
+}
+
+const char* qmv_last_error(void) { return t_err.c_str(); }
+
+int qmv_block_elems(int type)
+{
+    switch (type) {
+    case QMV_Q4_0: case QMV_Q5_0: case QMV_Q8_0: case QMV_MXFP4: return 32;
+    case QMV_Q4_K: case QMV_Q6_K: case QMV_Q8_K: return 256;
+    case QMV_F32: case QMV_BF16: return 1;
+    default: return 0;
+    }
+}
+
+size_t qmv_block_bytes(int type)
+{
+    switch (type) {
+    case QMV_Q4_0: return 18;
+    case QMV_Q5_0: return 22;
+    case QMV_Q8_0: return 34;
+    case QMV_MXFP4: return 17;
+    case QMV_Q4_K: return 144;
+    case QMV_Q6_K: return 210;
+    case QMV_Q8_K: return 292;
+    case QMV_F32: return 4;
+    case QMV_BF16: return 2;
+    default: return 0;
+    }
+}
+
+size_t qmv_row_bytes(int type, int64_t cols)
+{
+    const int bs = qmv_block_elems(type);
+    if (bs == 0 || cols < 0 || cols % bs) return 0;
+    return (size_t)(cols / bs) * qmv_block_bytes(type);
+}
+
+int qmv_quantize_act(int fmt, const float* x, void* xq, int64_t n, void* stream)
+{
+    if (fmt != QMV_Q8_0 && fmt != QMV_Q8_K)
+        return fail(QMV_ERR_UNSUPPORTED, "activation format %d (%s) is not supported; supported: Q8_0, Q8_K", fmt,
+                    type_name(fmt));
+    const int bs = qmv_block_elems(fmt);
+    if (n < 0) return fail(QMV_ERR_INVALID_ARG, "n must be >= 0");
+    if (n % bs) return fail(QMV_ERR_SHAPE, "%s quantises %d-element blocks; n = %lld is not a multiple of %d",
+                            type_name(fmt), bs, (long long)n, bs);
+    if (n == 0) return ok();
+    if (!x || !xq) return fail(QMV_ERR_INVALID_ARG, "x and xq must not be NULL");
+    if (!aligned(x, fmt == QMV_Q8_K ? 16 : 4)) return fail(QMV_ERR_ALIGN, "x must be %d-byte aligned", fmt == QMV_Q8_K ? 16 : 4);
+    if (!aligned(xq, fmt == QMV_Q8_K ? 4 : 2)) return fail(QMV_ERR_ALIGN, "xq must be %d-byte aligned", fmt == QMV_Q8_K ? 4 : 2);
+    if (qmv_launch_quantize(fmt, x, xq, n, static_cast<cudaStream_t>(stream))) return cuda_fail("qmv_quantize_act");
+    return ok();
+}
+
+int qmv_dequantize(int type, const void* W, int64_t rows, int64_t cols, float* out, void* stream)
+{
+    int rc = check_weights(type, W, rows, cols);
+    if (rc) return rc;
+    if (rows == 0) return ok();
+    if (!out) return fail(QMV_ERR_INVALID_ARG, "out is NULL");
+    if (qmv_launch_dequant(type, W, rows, cols, out, static_cast<cudaStream_t>(stream))) return cuda_fail("qmv_dequantize");
+    return ok();
+}
+
+int qmv_block_dots(int type, const void* W, int64_t rows, int64_t cols, const void* xq, int n_vec, int32_t* out,
+                   void* stream)
+{
+    int rc = check_weights(type, W, rows, cols);
+    if (rc) return rc;
+    if (n_vec < 0) return fail(QMV_ERR_INVALID_ARG, "n_vec must be >= 0");
+    if (rows == 0 || n_vec == 0) return ok();
+    if (!xq || !out) return fail(QMV_ERR_INVALID_ARG, "xq and out must not be NULL");
+    if (qmv_launch_block_dots(type, W, rows, cols, xq, n_vec, out, static_cast<cudaStream_t>(stream)))
+        return cuda_fail("qmv_block_dots");
+    return ok();
+}
+
+int qmv_matvec(int fmt, const void* W, int64_t rows, int64_t cols, const void* x, float* y, int n_vec, void* stream)
+{
+    const int wtype = fmt & 0xff, atype = (fmt >> 8) & 0xff;
+    int rc = check_weights(wtype, W, rows, cols);
+    if (rc) return rc;
+    if (atype != QMV_F32 && atype != paired_act(wtype))
+        return fail(QMV_ERR_UNSUPPORTED,
+                    "%s weights take F32 or %s activations in qmv_matvec (got %s); 32-element formats pair with "
+                    "Q8_0, K-quants with Q8_K",
+                    type_name(wtype), type_name(paired_act(wtype)), type_name(atype));
+    if (n_vec < 0 || n_vec > 64) return fail(QMV_ERR_INVALID_ARG, "n_vec must be in 0..64 (got %d)", n_vec);
+    if (rows == 0 || n_vec == 0) return ok();
+    if (!x || !y) return fail(QMV_ERR_INVALID_ARG, "x and y must not be NULL");
+    const bool a8 = atype != QMV_F32;
+    if (!aligned(x, a8 ? 4 : 16)) return fail(QMV_ERR_ALIGN, "x must be %d-byte aligned", a8 ? 4 : 16);
+    if (!aligned(y, 4)) return fail(QMV_ERR_ALIGN, "y must be 4-byte aligned");
+    if (!qmv::status_word()) return cuda_fail("qmv_matvec (status word)");
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    switch (wtype) {
+    case QMV_Q4_0: rc = qmv_gemv_q4_0(a8, W, rows, cols, x, y, n_vec, st); break;
+    case QMV_Q5_0: rc = qmv_gemv_q5_0(a8, W, rows, cols, x, y, n_vec, st); break;
+    case QMV_Q8_0: rc = qmv_gemv_q8_0(a8, W, rows, cols, x, y, n_vec, st); break;
+    case QMV_MXFP4: rc = qmv_gemv_mxfp4(a8, W, rows, cols, x, y, n_vec, st); break;
+    case QMV_Q4_K: rc = qmv_gemv_q4_k(a8, W, rows, cols, x, y, n_vec, st); break;
+    case QMV_Q6_K: rc = qmv_gemv_q6_k(a8, W, rows, cols, x, y, n_vec, st); break;
+    }
+    if (rc == -2) return fail(QMV_ERR_SHAPE, "cols = %lld needs more shared memory than one SM has", (long long)cols);
+    if (rc) return cuda_fail("qmv_matvec");
+    return ok();
+}
+
+int qmv_matmul(int fmt, const void* W, int64_t rows, int64_t cols, const void* X, float* Y, int64_t m, void* stream)
+{
+    (void)W; (void)rows; (void)cols; (void)X; (void)Y; (void)m; (void)stream;
+    return fail(QMV_ERR_UNSUPPORTED, "qmv_matmul: format 0x%x is not supported; supported: QMV_FMT(Q4_K, BF16), "
+                                     "QMV_FMT(Q4_K, Q8_K)", fmt);
+}
+
+int qmv_moe_matvec(int fmt, const void* W3d, int n_expert, int64_t rows, int64_t cols, const int32_t* ids,
+                   const float* gates, int k, const void* x, float* y, int64_t n_tok, const float* bias, void* stream)
+{
+    (void)W3d; (void)n_expert; (void)rows; (void)cols; (void)ids; (void)gates; (void)k; (void)x; (void)y;
+    (void)n_tok; (void)bias; (void)stream;
+    return fail(QMV_ERR_UNSUPPORTED, "qmv_moe_matvec: format 0x%x is not supported yet", fmt);
+}
+
+size_t qmv_workspace_size(int op, int fmt, int64_t rows, int64_t cols, int64_t n)
+{
+    (void)op; (void)fmt; (void)rows; (void)cols; (void)n;
+    return 0;
+}
+
+int qmv_set_workspace(void* ptr, size_t bytes)
+{
+    if (ptr && !aligned(ptr, 256)) return fail(QMV_ERR_ALIGN, "workspace must be 256-byte aligned");
+    const int d = qmv::current_device();
+    if (d < 0 || d >= qmv::kMaxDevices) return fail(QMV_ERR_INVALID_ARG, "device %d out of range", d);
+    std::lock_guard<std::mutex> lock(g_ws_mu);
+    g_ws[d].ptr = ptr;
+    g_ws[d].bytes = ptr ? bytes : 0;
+    return ok();
+}
+
+int qmv_get_status(void* stream)
+{
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return cuda_fail("qmv_get_status (synchronize)");
+    unsigned v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_qmv_status, sizeof v) != cudaSuccess) return cuda_fail("qmv_get_status (read)");
+    if (v == 0) return ok();
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_qmv_status, &zero, sizeof zero) != cudaSuccess) return cuda_fail("qmv_get_status (clear)");
+    std::string what;
+    if (v & QMV_DEV_BAD_EXPERT) what += "an expert id was out of range; ";
+    if (v & QMV_DEV_WAIT_TIMEOUT) what += "a pipeline wait gave up (a copy never landed); ";
+    if (v & QMV_DEV_BAD_ARG) what += "a kernel saw an inconsistent argument; ";
+    return fail(QMV_ERR_DEVICE_STATUS, "device status 0x%x: %s", v, what.c_str());
+}
+
+}  // extern "C"

@@ -1,0 +1,181 @@
+// common.cuh -- device helpers shared by the libqmv kernels (sm_103a).
+//
+// Inline PTX for the Blackwell data movers (mbarrier, cp.async.bulk), integer
+// dot products (dp4a) and a bounded-wait discipline: every spin on an
+// mbarrier gives up after a time limit, records a fault in the device status
+// word and lets the kernel return, so a stuck copy can never hang the GPU.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/qmv.h"
+
+// Device status word bits (read and cleared by qmv_get_status).
+#define QMV_DEV_BAD_EXPERT 1u
+#define QMV_DEV_WAIT_TIMEOUT 2u
+#define QMV_DEV_BAD_ARG 4u
+
+#define QMV_WAIT_LIMIT_NS 2000000000ull   // 2 s: a copy that has not landed by then never will
+
+namespace qmv {
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---- mbarrier ---------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+// Make initialised barriers visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_barrier_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for phase `parity` of `bar` to complete; false (and the status word
+// flagged) if it has not after QMV_WAIT_LIMIT_NS.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, unsigned* status,
+                                                  uint64_t limit_ns = QMV_WAIT_LIMIT_NS)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            atomicOr(status, QMV_DEV_WAIT_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// ---- bulk copy global -> shared (TMA, 1-D) ------------------------------------
+// dst and src 16-byte aligned, bytes a multiple of 16.  Completion is signalled
+// as transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Hint the L2 to start fetching [src, src+bytes) (16-byte aligned, multiple of 16).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// ---- integer dot products ---------------------------------------------------------
+// Four unsigned bytes of a times four signed bytes of b, plus c.
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c)
+{
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+// Four signed bytes times four signed bytes, plus c.
+__device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c)
+{
+    int d;
+    asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// ---- byte-addressed reads of shared memory -------------------------------------------
+// K little-endian 32-bit words starting at any byte address p (shared memory,
+// with at least 4 readable bytes after the last word's end).
+template <int K>
+__device__ __forceinline__ void load_words(const uint8_t* p, uint32_t (&w)[K])
+{
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    const uint32_t* base = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
+    const uint32_t sh = static_cast<uint32_t>(a & 3) * 8u;
+    uint32_t prev = base[0];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const uint32_t next = base[k + 1];
+        w[k] = __funnelshift_r(prev, next, sh);
+        prev = next;
+    }
+}
+
+__device__ __forceinline__ float half_bits_to_float(uint32_t h16)
+{
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(h16 & 0xffffu)));
+}
+
+__device__ __forceinline__ uint32_t ld_u16(const uint8_t* p)   // 2-byte aligned
+{
+    return *reinterpret_cast<const uint16_t*>(p);
+}
+
+// Four unsigned bytes of w -> the float value of byte k minus `off`, exactly:
+// 0x4B0000xx is the float 2^23 + xx, and 2^23 + off is exact below 2^24.
+__device__ __forceinline__ float ubyte_to_float_minus(uint32_t w, int k, float two23_plus_off)
+{
+    return __int_as_float(static_cast<int>(__byte_perm(w, 0x4B000000u, 0x7650u + k))) - two23_plus_off;
+}
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ int warp_sum_int(int v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+}  // namespace qmv

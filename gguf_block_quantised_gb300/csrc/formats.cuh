@@ -1,0 +1,561 @@
+// formats.cuh -- per-format decoding of weight "units" and their fused dot
+// products with staged activations.
+//
+// Formats ("Models and formats" page, "Tensor formats"; GGUF block layouts):
+//   Q4_0  18 B / 32 w   fp16 d | 16 B nibbles              w = d*(q-8)
+//   Q5_0  22 B / 32 w   fp16 d | u32 fifth bits | 16 B     w = d*(q-16)
+//   Q8_0  34 B / 32 w   fp16 d | int8[32]                  w = d*q
+//   MXFP4 17 B / 32 w   E8M0 e | 16 B E2M1 codes           w = 2^(e-127)*E2M1(q)
+//   Q4_K 144 B / 256 w  fp16 d | fp16 dmin | 12 B six-bit sc/m | 128 B nibbles
+//                                                          w = d*sc_j*q - dmin*m_j
+//   Q6_K 210 B / 256 w  128 B low nibbles | 64 B high pairs | int8 sc[16] | fp16 d
+//                                                          w = d*sc*(q-32)
+// Nibble order: element j of a 32-run is the low nibble of byte j, element
+// j+16 its high nibble; Q4_K 32-byte chunk c holds sub-block 2c (low) and
+// 2c+1 (high); Q6_K element i uses scales[i/16].
+//
+// A unit is the piece of a row one lane handles at a time: one block (32 w)
+// for the 32-element formats, 64 weights for the K-quants (Q4_K: one 32-byte
+// nibble chunk = two sub-blocks; Q6_K: the l-half lh of half h, i.e. the 16
+// consecutive elements at offsets 32g + 16lh, g = 0..3, of that half).
+//
+// The W4A8 ("fused W4A8 kernels", "Architecture" page, pkg/quant) product of a
+// unit is exact in integers: codes are laid out as bytes that line up with the
+// staged int8 activations and summed with dp4a; offsets (q-8, q-16, q-32) are
+// applied through the exact activation sums.  The scales enter once per unit
+// through fixed fp32 fused multiply-adds, so the reduction order of an output
+// depends only on the row, never on how many vectors share the pass.
+#pragma once
+
+#include "common.cuh"
+
+namespace qmv {
+
+// ---- staged activations -------------------------------------------------------
+// Layout in shared memory for G vectors (all arrays 16-byte aligned):
+//   A8:  codes int8 [G][cols] (MXFP4: each 32-run interleaved as x0,x16,x1,x17,..)
+//        d     f32  [G][nb]         (activation block scale)
+//        sum32 i32  [G][nb]         (32-element formats: sum of the block's codes)
+//        bsum  i16  [G][nb][16]     (K-quants: sums of each run of 16 codes)
+//   A32: xf    f32  [G][cols]       (MXFP4 runs interleaved as above)
+//        xs32  f32  [G][cols/32]    (Q4_K: sum of each 32-run, fixed order)
+struct XView {
+    const uint8_t* codes;
+    const float* d;
+    const int* sum32;
+    const int16_t* bsum;
+    const float* xf;
+    const float* xs32;
+    int cols;
+    int nb;   // activation blocks per vector (= weight blocks per row)
+};
+
+template <int T>
+struct Fmt;
+
+// ------------------------------------------------------------------------------
+// The 32-element formats share one shape: 8 code words + one scale per unit.
+// ------------------------------------------------------------------------------
+struct W32 {
+    uint32_t c[8];   // 32 code bytes in staged-activation order
+    float d;         // w = d * (code - OFF)
+};
+
+template <int T>
+struct Fmt32Base {
+    static constexpr int BS = 32, UE = 32, UPB = 1;
+
+    struct XA8 {
+        uint32_t w[8];
+        float d;
+        int sum;
+    };
+
+    static __device__ __forceinline__ void load_x_a8(const XView& X, int v, int b, int /*sub*/, XA8& x)
+    {
+        const uint4* p = reinterpret_cast<const uint4*>(X.codes + (size_t)v * X.cols + (size_t)b * 32);
+        const uint4 a = p[0], c = p[1];
+        x.w[0] = a.x; x.w[1] = a.y; x.w[2] = a.z; x.w[3] = a.w;
+        x.w[4] = c.x; x.w[5] = c.y; x.w[6] = c.z; x.w[7] = c.w;
+        x.d = X.d[v * X.nb + b];
+        x.sum = X.sum32[v * X.nb + b];
+    }
+};
+
+template <>
+struct Fmt<QMV_Q4_0> : Fmt32Base<QMV_Q4_0> {
+    static constexpr int BB = 18, OFF = 8;
+    static constexpr bool SIGNED = false;
+    using W = W32;
+    static __device__ __forceinline__ void load(const uint8_t* blk, int, W& w)
+    {
+        uint32_t q[4];
+        load_words<4>(blk + 2, q);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            w.c[k] = q[k] & 0x0f0f0f0fu;
+            w.c[4 + k] = (q[k] >> 4) & 0x0f0f0f0fu;
+        }
+        w.d = half_bits_to_float(ld_u16(blk));
+    }
+};
+
+template <>
+struct Fmt<QMV_Q5_0> : Fmt32Base<QMV_Q5_0> {
+    static constexpr int BB = 22, OFF = 16;
+    static constexpr bool SIGNED = false;
+    using W = W32;
+    // Four bits of the mask -> bit 4 of four bytes.  t * 0x00204081 places bit
+    // j of t at bit 8j (and elsewhere, never overlapping bits 0, 8, 16, 24).
+    static __device__ __forceinline__ uint32_t spread4(uint32_t t)
+    {
+        return ((t * 0x00204081u) & 0x01010101u) << 4;
+    }
+    static __device__ __forceinline__ void load(const uint8_t* blk, int, W& w)
+    {
+        uint32_t q[5];
+        load_words<5>(blk + 2, q);   // q[0] = fifth-bit mask, q[1..4] = nibbles
+        const uint32_t qh = q[0];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            w.c[k] = (q[1 + k] & 0x0f0f0f0fu) | spread4((qh >> (4 * k)) & 15u);
+            w.c[4 + k] = ((q[1 + k] >> 4) & 0x0f0f0f0fu) | spread4((qh >> (16 + 4 * k)) & 15u);
+        }
+        w.d = half_bits_to_float(ld_u16(blk));
+    }
+};
+
+template <>
+struct Fmt<QMV_Q8_0> : Fmt32Base<QMV_Q8_0> {
+    static constexpr int BB = 34, OFF = 0;
+    static constexpr bool SIGNED = true;
+    using W = W32;
+    static __device__ __forceinline__ void load(const uint8_t* blk, int, W& w)
+    {
+        load_words<8>(blk + 2, w.c);
+        w.d = half_bits_to_float(ld_u16(blk));
+    }
+};
+
+// MXFP4: E2M1 codes become the doubled values {0,1,2,3,4,6,8,12} (exact
+// integers) with their sign, through byte-permute tables; the doubling is
+// undone by using 2^(e-128) as the block scale.
+template <>
+struct Fmt<QMV_MXFP4> : Fmt32Base<QMV_MXFP4> {
+    static constexpr int BB = 17, OFF = 0;
+    static constexpr bool SIGNED = true;
+    using W = W32;
+    // Four nibbles (16 bits) -> four signed bytes.
+    static __device__ __forceinline__ uint32_t lut4(uint32_t s)
+    {
+        const uint32_t sel = s & 0x7777u;
+        const uint32_t pos = __byte_perm(0x03020100u, 0x0c080604u, sel);   // 0,1,2,3 | 4,6,8,12
+        const uint32_t neg = __byte_perm(0xfdfeff00u, 0xf4f8fafcu, sel);   // 0,-1,-2,-3 | -4,-6,-8,-12
+        // 0xff in the bytes whose nibble has its sign bit (bit 3) set: the
+        // sign-replicate mode of PRMT copies bit 7 of the selected byte.
+        const uint32_t m = __byte_perm(s << 4, s, 0xd9c8u);
+        return (pos & ~m) | (neg & m);
+    }
+    static __device__ __forceinline__ float e8m0_half(uint32_t e)   // 2^(e-128)
+    {
+        if (e == 255u) return __int_as_float(0x7fc00000);
+        if (e >= 2u) return __int_as_float(static_cast<int>((e - 1u) << 23));
+        return __int_as_float(static_cast<int>(0x00400000u >> (1u - e)));
+    }
+    static __device__ __forceinline__ void load(const uint8_t* blk, int, W& w)
+    {
+        uint32_t q[4];
+        load_words<4>(blk + 1, q);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            w.c[2 * k] = lut4(q[k] & 0xffffu);
+            w.c[2 * k + 1] = lut4(q[k] >> 16);
+        }
+        w.d = e8m0_half(blk[0]);
+    }
+};
+
+// ------------------------------------------------------------------------------
+// Q4_K: unit = 32-byte nibble chunk c of a super-block (sub-blocks 2c, 2c+1).
+// ------------------------------------------------------------------------------
+template <>
+struct Fmt<QMV_Q4_K> {
+    static constexpr int BS = 256, BB = 144, UE = 64, UPB = 4;
+    struct W {
+        uint32_t lo[8], hi[8];
+        int sc0, sc1, m0, m1;
+        float d, dmin;
+    };
+    static __device__ __forceinline__ uint32_t fbyte(uint32_t f0, uint32_t f1, uint32_t f2, int i)
+    {
+        const uint32_t w = i < 4 ? f0 : (i < 8 ? f1 : f2);
+        return (w >> (8 * (i & 3))) & 0xffu;
+    }
+    // Six-bit scale and min of sub-block j from the 12-byte field.
+    static __device__ __forceinline__ void scale_min(uint32_t f0, uint32_t f1, uint32_t f2, int j, int& sc, int& m)
+    {
+        if (j < 4) {
+            sc = fbyte(f0, f1, f2, j) & 63;
+            m = fbyte(f0, f1, f2, j + 4) & 63;
+        } else {
+            const uint32_t lo4 = fbyte(f0, f1, f2, j + 4);
+            sc = (lo4 & 15) | ((fbyte(f0, f1, f2, j - 4) >> 6) << 4);
+            m = (lo4 >> 4) | ((fbyte(f0, f1, f2, j) >> 6) << 4);
+        }
+    }
+    // blk is 16-byte aligned (144-byte blocks in a 16-byte aligned staging slot).
+    static __device__ __forceinline__ void load(const uint8_t* blk, int c, W& w)
+    {
+        const uint4 h = *reinterpret_cast<const uint4*>(blk);   // d, dmin, field[0..11]
+        const uint4* qp = reinterpret_cast<const uint4*>(blk + 16 + 32 * c);
+        const uint4 a = qp[0], b = qp[1];
+        const uint32_t q[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            w.lo[k] = q[k] & 0x0f0f0f0fu;
+            w.hi[k] = (q[k] >> 4) & 0x0f0f0f0fu;
+        }
+        scale_min(h.y, h.z, h.w, 2 * c, w.sc0, w.m0);
+        scale_min(h.y, h.z, h.w, 2 * c + 1, w.sc1, w.m1);
+        w.d = half_bits_to_float(h.x & 0xffffu);
+        w.dmin = half_bits_to_float(h.x >> 16);
+    }
+    struct XA8 {
+        uint32_t lo[8], hi[8];
+        float d;
+        int s0, s1;   // sums of the codes of sub-blocks 2c and 2c+1
+    };
+    static __device__ __forceinline__ void load_x_a8(const XView& X, int v, int b, int c, XA8& x)
+    {
+        const uint4* p = reinterpret_cast<const uint4*>(X.codes + (size_t)v * X.cols + (size_t)b * 256 + 64 * c);
+        const uint4 a0 = p[0], a1 = p[1], a2 = p[2], a3 = p[3];
+        x.lo[0] = a0.x; x.lo[1] = a0.y; x.lo[2] = a0.z; x.lo[3] = a0.w;
+        x.lo[4] = a1.x; x.lo[5] = a1.y; x.lo[6] = a1.z; x.lo[7] = a1.w;
+        x.hi[0] = a2.x; x.hi[1] = a2.y; x.hi[2] = a2.z; x.hi[3] = a2.w;
+        x.hi[4] = a3.x; x.hi[5] = a3.y; x.hi[6] = a3.z; x.hi[7] = a3.w;
+        x.d = X.d[v * X.nb + b];
+        const uint2 bs = *reinterpret_cast<const uint2*>(X.bsum + ((size_t)v * X.nb + b) * 16 + 4 * c);
+        x.s0 = (int)(int16_t)(bs.x & 0xffffu) + (int)(int16_t)(bs.x >> 16);
+        x.s1 = (int)(int16_t)(bs.y & 0xffffu) + (int)(int16_t)(bs.y >> 16);
+    }
+    static __device__ __forceinline__ void ints(const W& w, const XA8& x, int& S, int& Mn)
+    {
+        int i0 = 0, i1 = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            i0 = dp4a_us(w.lo[k], x.lo[k], i0);
+            i1 = dp4a_us(w.hi[k], x.hi[k], i1);
+        }
+        S = w.sc0 * i0 + w.sc1 * i1;
+        Mn = w.m0 * x.s0 + w.m1 * x.s1;
+    }
+    static __device__ __forceinline__ void acc_a8(const W& w, const XA8& x, float& acc)
+    {
+        int S, Mn;
+        ints(w, x, S, Mn);
+        acc = __fmaf_rn((float)S, w.d * x.d, acc);
+        acc = __fmaf_rn(-(float)Mn, w.dmin * x.d, acc);
+    }
+    static __device__ __forceinline__ void acc_a32(const W& w, const XView& X, int v, int b, int c, float& acc)
+    {
+        const float4* xp = reinterpret_cast<const float4*>(X.xf + (size_t)v * X.cols + (size_t)b * 256 + 64 * c);
+        float p0 = 0.f, p1 = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float4 xa = xp[k], xb = xp[8 + k];
+            p0 = __fmaf_rn(ubyte_to_float_minus(w.lo[k], 0, 8388608.f), xa.x, p0);
+            p0 = __fmaf_rn(ubyte_to_float_minus(w.lo[k], 1, 8388608.f), xa.y, p0);
+            p0 = __fmaf_rn(ubyte_to_float_minus(w.lo[k], 2, 8388608.f), xa.z, p0);
+            p0 = __fmaf_rn(ubyte_to_float_minus(w.lo[k], 3, 8388608.f), xa.w, p0);
+            p1 = __fmaf_rn(ubyte_to_float_minus(w.hi[k], 0, 8388608.f), xb.x, p1);
+            p1 = __fmaf_rn(ubyte_to_float_minus(w.hi[k], 1, 8388608.f), xb.y, p1);
+            p1 = __fmaf_rn(ubyte_to_float_minus(w.hi[k], 2, 8388608.f), xb.z, p1);
+            p1 = __fmaf_rn(ubyte_to_float_minus(w.hi[k], 3, 8388608.f), xb.w, p1);
+        }
+        const float* xs = X.xs32 + (size_t)v * (X.cols / 32) + (size_t)b * 8 + 2 * c;
+        acc = __fmaf_rn(p0, w.d * (float)w.sc0, acc);
+        acc = __fmaf_rn(p1, w.d * (float)w.sc1, acc);
+        acc = __fmaf_rn(-xs[0], w.dmin * (float)w.m0, acc);
+        acc = __fmaf_rn(-xs[1], w.dmin * (float)w.m1, acc);
+    }
+};
+
+// ------------------------------------------------------------------------------
+// Q6_K: unit (h, lh) = elements 128h + 32g + 16lh + [0,16) for g = 0..3.
+// ------------------------------------------------------------------------------
+template <>
+struct Fmt<QMV_Q6_K> {
+    static constexpr int BS = 256, BB = 210, UE = 64, UPB = 4;
+    struct W {
+        uint32_t g[4][4];   // 6-bit codes (0..63) of group g, 16 elements as 4 words
+        int sc[4];          // scale of group g: scales[8h + 2g + lh]
+        float d;
+    };
+    static __device__ __forceinline__ void load(const uint8_t* blk, int sub, W& w)
+    {
+        const int h = sub >> 1, lh = sub & 1;
+        uint32_t L0[4], L1[4], H[4], S[2];
+        load_words<4>(blk + 64 * h + 16 * lh, L0);        // ql[l],    l = 16lh..16lh+15
+        load_words<4>(blk + 64 * h + 32 + 16 * lh, L1);   // ql[l+32]
+        load_words<4>(blk + 128 + 32 * h + 16 * lh, H);   // qh[l]
+        load_words<2>(blk + 192 + 8 * h, S);              // this half's 8 int8 scales
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            w.g[0][k] = (L0[k] & 0x0f0f0f0fu) | ((H[k] & 0x03030303u) << 4);
+            w.g[1][k] = (L1[k] & 0x0f0f0f0fu) | ((H[k] & 0x0c0c0c0cu) << 2);
+            w.g[2][k] = ((L0[k] >> 4) & 0x0f0f0f0fu) | (H[k] & 0x30303030u);
+            w.g[3][k] = ((L1[k] >> 4) & 0x0f0f0f0fu) | ((H[k] & 0xc0c0c0c0u) >> 2);
+        }
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const int idx = 2 * g + lh;   // 0..7 within the half
+            const uint32_t word = idx < 4 ? S[0] : S[1];
+            w.sc[g] = (int)(int8_t)((word >> (8 * (idx & 3))) & 0xffu);
+        }
+        w.d = half_bits_to_float(ld_u16(blk + 208));
+    }
+    struct XA8 {
+        uint32_t g[4][4];
+        float d;
+        int s[4];   // sums of the 16 codes of each group
+    };
+    static __device__ __forceinline__ void load_x_a8(const XView& X, int v, int b, int sub, XA8& x)
+    {
+        const int h = sub >> 1, lh = sub & 1;
+        const uint8_t* base = X.codes + (size_t)v * X.cols + (size_t)b * 256 + 128 * h + 16 * lh;
+        const int16_t* bs = X.bsum + ((size_t)v * X.nb + b) * 16 + 8 * h + lh;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const uint4 a = *reinterpret_cast<const uint4*>(base + 32 * g);
+            x.g[g][0] = a.x; x.g[g][1] = a.y; x.g[g][2] = a.z; x.g[g][3] = a.w;
+            x.s[g] = bs[2 * g];
+        }
+        x.d = X.d[v * X.nb + b];
+    }
+    static __device__ __forceinline__ void ints(const W& w, const XA8& x, int& S, int& Mn)
+    {
+        S = 0;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            int dot = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) dot = dp4a_us(w.g[g][k], x.g[g][k], dot);
+            S += w.sc[g] * (dot - 32 * x.s[g]);
+        }
+        Mn = 0;
+    }
+    static __device__ __forceinline__ void acc_a8(const W& w, const XA8& x, float& acc)
+    {
+        int S, Mn;
+        ints(w, x, S, Mn);
+        acc = __fmaf_rn((float)S, w.d * x.d, acc);
+    }
+    static __device__ __forceinline__ void acc_a32(const W& w, const XView& X, int v, int b, int sub, float& acc)
+    {
+        const int h = sub >> 1, lh = sub & 1;
+        const float* xb = X.xf + (size_t)v * X.cols + (size_t)b * 256 + 128 * h + 16 * lh;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const float4* xp = reinterpret_cast<const float4*>(xb + 32 * g);
+            float p = 0.f;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float4 xa = xp[k];
+                p = __fmaf_rn(ubyte_to_float_minus(w.g[g][k], 0, 8388640.f), xa.x, p);
+                p = __fmaf_rn(ubyte_to_float_minus(w.g[g][k], 1, 8388640.f), xa.y, p);
+                p = __fmaf_rn(ubyte_to_float_minus(w.g[g][k], 2, 8388640.f), xa.z, p);
+                p = __fmaf_rn(ubyte_to_float_minus(w.g[g][k], 3, 8388640.f), xa.w, p);
+            }
+            acc = __fmaf_rn(p, w.d * (float)w.sc[g], acc);
+        }
+    }
+};
+
+// ---- the 32-element formats' products ------------------------------------------
+template <int T>
+__device__ __forceinline__ void ints32(const W32& w, const typename Fmt<T>::XA8& x, int& S, int& Mn)
+{
+    int dot = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        dot = Fmt<T>::SIGNED ? dp4a_ss(w.c[k], x.w[k], dot) : dp4a_us(w.c[k], x.w[k], dot);
+    S = dot - Fmt<T>::OFF * x.sum;
+    Mn = 0;
+}
+
+template <int T>
+__device__ __forceinline__ void acc32_a8(const W32& w, const typename Fmt<T>::XA8& x, float& acc)
+{
+    int S, Mn;
+    ints32<T>(w, x, S, Mn);
+    acc = __fmaf_rn((float)S, w.d * x.d, acc);
+}
+
+template <int T>
+__device__ __forceinline__ void acc32_a32(const W32& w, const XView& X, int v, int b, float& acc)
+{
+    // Unsigned codes minus OFF; signed codes are biased by 128 first.
+    constexpr float kOff = 8388608.f + (Fmt<T>::SIGNED ? 128.f : (float)Fmt<T>::OFF);
+    const float4* xp = reinterpret_cast<const float4*>(X.xf + (size_t)v * X.cols + (size_t)b * 32);
+    float p = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint32_t c = Fmt<T>::SIGNED ? (w.c[k] ^ 0x80808080u) : w.c[k];
+        const float4 xa = xp[k];
+        p = __fmaf_rn(ubyte_to_float_minus(c, 0, kOff), xa.x, p);
+        p = __fmaf_rn(ubyte_to_float_minus(c, 1, kOff), xa.y, p);
+        p = __fmaf_rn(ubyte_to_float_minus(c, 2, kOff), xa.z, p);
+        p = __fmaf_rn(ubyte_to_float_minus(c, 3, kOff), xa.w, p);
+    }
+    acc = __fmaf_rn(p, w.d, acc);
+}
+
+// Uniform entry points over all formats.
+template <int T>
+struct Ops {
+    using F = Fmt<T>;
+    using W = typename F::W;
+    using XA8 = typename F::XA8;
+    static __device__ __forceinline__ void ints(const W& w, const XA8& x, int& S, int& Mn)
+    {
+        if constexpr (F::BS == 32) ints32<T>(w, x, S, Mn);
+        else F::ints(w, x, S, Mn);
+    }
+    static __device__ __forceinline__ void acc_a8(const W& w, const XA8& x, float& acc)
+    {
+        if constexpr (F::BS == 32) acc32_a8<T>(w, x, acc);
+        else F::acc_a8(w, x, acc);
+    }
+    static __device__ __forceinline__ void acc_a32(const W& w, const XView& X, int v, int b, int sub, float& acc)
+    {
+        if constexpr (F::BS == 32) acc32_a32<T>(w, X, v, b, acc);
+        else F::acc_a32(w, X, v, b, sub, acc);
+    }
+};
+
+// ---- staging activations into shared memory -----------------------------------------
+// Position of element i (0..31) of a 32-run in the staged order of format T.
+template <int T>
+__device__ __forceinline__ int staged_pos(int i)
+{
+    if constexpr (T == QMV_MXFP4) return i < 16 ? 2 * i : 2 * (i - 16) + 1;
+    else return i;
+}
+
+// Bytes of staged activations for g vectors of `cols` elements.
+__host__ __device__ inline size_t xhat_bytes(int T, bool a8, int g, int cols)
+{
+    const int bs = (T == QMV_Q4_K || T == QMV_Q6_K) ? 256 : 32;
+    const size_t nb = (size_t)cols / bs;
+    auto r16 = [](size_t v) { return (v + 15) & ~size_t(15); };
+    if (a8) {
+        size_t s = r16((size_t)g * cols) + r16((size_t)g * nb * 4);
+        s += (bs == 32) ? r16((size_t)g * nb * 4) : r16((size_t)g * nb * 32);
+        return s;
+    }
+    size_t s = r16((size_t)g * cols * 4);
+    if (T == QMV_Q4_K) s += r16((size_t)g * (cols / 32) * 4);
+    return s;
+}
+
+template <int T>
+__device__ __forceinline__ XView carve_xview(uint8_t* base, bool a8, int g, int cols)
+{
+    constexpr int bs = Fmt<T>::BS;
+    const int nb = cols / bs;
+    auto r16 = [](size_t v) { return (v + 15) & ~size_t(15); };
+    XView X{};
+    X.cols = cols;
+    X.nb = nb;
+    if (a8) {
+        X.codes = base;
+        uint8_t* p = base + r16((size_t)g * cols);
+        X.d = reinterpret_cast<const float*>(p);
+        p += r16((size_t)g * nb * 4);
+        if (bs == 32) X.sum32 = reinterpret_cast<const int*>(p);
+        else X.bsum = reinterpret_cast<const int16_t*>(p);
+    } else {
+        X.xf = reinterpret_cast<const float*>(base);
+        X.xs32 = reinterpret_cast<const float*>(base + r16((size_t)g * cols * 4));
+    }
+    return X;
+}
+
+// Stage g vectors of activations, starting at global vector v0, with all
+// threads of the block.  x points at the caller's activations: fp32
+// [n][cols] (A32) or Q8_0/Q8_K blocks [n][nb] (A8).  Ends with __syncthreads.
+template <int T>
+__device__ void stage_xhat(uint8_t* base, bool a8, const void* x, int g, int cols)
+{
+    constexpr int bs = Fmt<T>::BS;
+    const int nb = cols / bs;
+    auto r16 = [](size_t v) { return (v + 15) & ~size_t(15); };
+    const int tid = threadIdx.x, nth = blockDim.x;
+    if (a8) {
+        uint8_t* codes = base;
+        float* d = reinterpret_cast<float*>(base + r16((size_t)g * cols));
+        uint8_t* tail = base + r16((size_t)g * cols) + r16((size_t)g * nb * 4);
+        if constexpr (bs == 32) {
+            // Q8_0 blocks: fp16 d | int8[32], 34 bytes, 2-byte aligned.
+            int* sum = reinterpret_cast<int*>(tail);
+            const uint8_t* src = static_cast<const uint8_t*>(x);
+            for (int i = tid; i < g * nb; i += nth) {
+                const uint8_t* blk = src + (size_t)i * 34;
+                const uint16_t* h = reinterpret_cast<const uint16_t*>(blk);
+                uint8_t q[32];
+                int s = 0;
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const uint32_t two = h[1 + k];
+                    q[2 * k] = two & 0xffu;
+                    q[2 * k + 1] = two >> 8;
+                    s += (int)(int8_t)(two & 0xffu) + (int)(int8_t)(two >> 8);
+                }
+                uint8_t* dst = codes + (size_t)i * 32;   // vector v, block b: i = v*nb + b
+#pragma unroll
+                for (int k = 0; k < 32; ++k) dst[staged_pos<T>(k)] = q[k];
+                d[i] = half_bits_to_float(h[0]);
+                sum[i] = s;
+            }
+        } else {
+            // Q8_K blocks: f32 d | int8[256] | int16 bsums[16], 292 bytes, 4-byte aligned.
+            int16_t* bsum = reinterpret_cast<int16_t*>(tail);
+            const uint32_t* src = static_cast<const uint32_t*>(x);
+            for (int i = tid; i < g * nb * 73; i += nth) {
+                const int blkno = i / 73, wd = i % 73;
+                const uint32_t val = src[i];
+                if (wd == 0) d[blkno] = __uint_as_float(val);
+                else if (wd <= 64) reinterpret_cast<uint32_t*>(codes + (size_t)blkno * 256)[wd - 1] = val;
+                else reinterpret_cast<uint32_t*>(bsum + (size_t)blkno * 16)[wd - 65] = val;
+            }
+        }
+    } else {
+        float* xf = reinterpret_cast<float*>(base);
+        const float4* src = static_cast<const float4*>(x);
+        const int n4 = g * cols / 4;
+        for (int i = tid; i < n4; i += nth) {
+            const float4 v = src[i];
+            if constexpr (T == QMV_MXFP4) {
+                const int e = 4 * i, run = e & ~31;
+                xf[run + staged_pos<T>((e + 0) & 31)] = v.x;
+                xf[run + staged_pos<T>((e + 1) & 31)] = v.y;
+                xf[run + staged_pos<T>((e + 2) & 31)] = v.z;
+                xf[run + staged_pos<T>((e + 3) & 31)] = v.w;
+            } else {
+                reinterpret_cast<float4*>(xf)[i] = v;
+            }
+        }
+        if constexpr (T == QMV_Q4_K) {
+            __syncthreads();
+            float* xs32 = reinterpret_cast<float*>(base + r16((size_t)g * cols * 4));
+            for (int i = tid; i < g * cols / 32; i += nth) {
+                float s = 0.f;
+                for (int k = 0; k < 32; ++k) s += xf[(size_t)i * 32 + k];
+                xs32[i] = s;
+            }
+        }
+    }
+    __syncthreads();
+}
+
+}  // namespace qmv

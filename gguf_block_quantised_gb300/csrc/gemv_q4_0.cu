@@ -1,0 +1,5 @@
+// gemv_q4_0.cu -- decode matvec kernels for Q4_0 weights (one translation unit
+// per format so the kernels compile in parallel).
+#include "gemv_launch.cuh"
+
+QMV_GEMV_INSTANTIATE(QMV_Q4_0, qmv_gemv_q4_0)

@@ -1,0 +1,5 @@
+// gemv_q6_k.cu -- decode matvec kernels for Q6_K weights (one translation unit
+// per format so the kernels compile in parallel).
+#include "gemv_launch.cuh"
+
+QMV_GEMV_INSTANTIATE(QMV_Q6_K, qmv_gemv_q6_k)

@@ -1,0 +1,88 @@
+// quant_act.cu -- fp32 activations -> Q8_0 / Q8_K blocks (the "A8" of the
+// fused W4A8 kernels, "Architecture" page, "The package map", pkg/quant).
+//
+// Per block: amax = max|x|; d = amax/127; id = 1/d (0 when d = 0);
+// q = round-half-away-from-zero(x*id) clamped to +-127.  Every step is one
+// IEEE fp32 rounding (__fdiv_rn, __fmul_rn, roundf), so the codes are
+// bit-identical to the plain definition whatever the thread layout.  Q8_0
+// stores fp16(d) (round to nearest even); Q8_K stores the fp32 d and the
+// int16 sums of each run of 16 codes.
+//
+// One warp per block.  This kernel moves ~5 bytes per element in total and is
+// a small fraction of any multiply it feeds.
+#include "common.cuh"
+
+namespace qmv {
+
+__device__ __forceinline__ int8_t quant1(float v, float id)
+{
+    float r = roundf(__fmul_rn(v, id));
+    r = fminf(fmaxf(r, -127.f), 127.f);
+    return (int8_t)(int)r;
+}
+
+// Q8_0: lane i owns element i of the block.
+__global__ void k_quant_q8_0(const float* __restrict__ x, uint8_t* __restrict__ out, int64_t nblk)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t b = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (b >= nblk) return;
+    const float v = x[b * 32 + lane];
+    const float amax = warp_max(fabsf(v));
+    const float d = __fdiv_rn(amax, 127.f);
+    const float id = d == 0.f ? 0.f : __fdiv_rn(1.f, d);
+    const int8_t q = quant1(v, id);
+    uint8_t* o = out + b * 34;
+    o[2 + lane] = (uint8_t)q;
+    if (lane == 0) *reinterpret_cast<__half*>(o) = __float2half_rn(d);
+}
+
+// Q8_K: lane i owns elements 8i..8i+7.
+__global__ void k_quant_q8_k(const float* __restrict__ x, uint8_t* __restrict__ out, int64_t nblk)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t b = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (b >= nblk) return;
+    const float4* xp = reinterpret_cast<const float4*>(x + b * 256 + lane * 8);
+    const float4 a = xp[0], c = xp[1];
+    const float v[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+    float m = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(v[k]));
+    const float amax = warp_max(m);
+    const float d = __fdiv_rn(amax, 127.f);
+    const float id = d == 0.f ? 0.f : __fdiv_rn(1.f, d);
+    uint32_t w0 = 0, w1 = 0;
+    int s = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int8_t q = quant1(v[k], id);
+        s += q;
+        if (k < 4) w0 |= (uint32_t)(uint8_t)q << (8 * k);
+        else w1 |= (uint32_t)(uint8_t)q << (8 * (k - 4));
+    }
+    uint8_t* o = out + b * 292;
+    uint32_t* qw = reinterpret_cast<uint32_t*>(o + 4 + lane * 8);
+    qw[0] = w0;
+    qw[1] = w1;
+    const int pair = s + __shfl_xor_sync(0xffffffffu, s, 1);   // lanes 2g, 2g+1 cover run g of 16
+    if ((lane & 1) == 0) reinterpret_cast<int16_t*>(o + 260)[lane >> 1] = (int16_t)pair;
+    if (lane == 0) *reinterpret_cast<float*>(o) = d;
+}
+
+}  // namespace qmv
+
+int qmv_launch_quantize(int atype, const float* x, void* xq, int64_t n, cudaStream_t st)
+{
+    using namespace qmv;
+    const int bs = atype == QMV_Q8_0 ? 32 : 256;
+    const int64_t nblk = n / bs;
+    if (nblk == 0) return 0;
+    const int warps = 8;
+    const int64_t grid = (nblk + warps - 1) / warps;
+    if (atype == QMV_Q8_0)
+        k_quant_q8_0<<<(unsigned)grid, warps * 32, 0, st>>>(x, static_cast<uint8_t*>(xq), nblk);
+    else
+        k_quant_q8_k<<<(unsigned)grid, warps * 32, 0, st>>>(x, static_cast<uint8_t*>(xq), nblk);
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}

@@ -1,0 +1,65 @@
+// runtime.cuh -- host-side device facts and per-kernel launch set-up, cached.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <atomic>
+#include <mutex>
+
+namespace qmv {
+
+constexpr int kMaxDevices = 64;
+
+inline int current_device()
+{
+    int d = 0;
+    cudaGetDevice(&d);
+    return d;
+}
+
+inline int num_sms()
+{
+    static std::atomic<int> cache[kMaxDevices];
+    const int d = current_device();
+    int v = (d >= 0 && d < kMaxDevices) ? cache[d].load(std::memory_order_relaxed) : 0;
+    if (v == 0) {
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, d);
+        if (v <= 0) v = 1;
+        if (d >= 0 && d < kMaxDevices) cache[d].store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
+// Device address of the library's status word (defined in api.cu).
+unsigned* status_word();
+
+// Opt a kernel into `bytes` of dynamic shared memory (once per kernel and
+// device) and return how many of its blocks fit on one SM with that much.
+template <typename K>
+inline int prepare_kernel(K* kernel, int threads, size_t bytes)
+{
+    struct Entry {
+        const void* fn;
+        int dev;
+        int threads;
+        size_t bytes;
+        int occ;
+    };
+    static std::mutex mu;
+    static Entry cache[64];
+    static int n = 0;
+    const int dev = current_device();
+    const void* fn = reinterpret_cast<const void*>(kernel);
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n; ++i)
+        if (cache[i].fn == fn && cache[i].dev == dev && cache[i].threads == threads && cache[i].bytes == bytes)
+            return cache[i].occ;
+    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, threads, bytes) != cudaSuccess || occ < 1) occ = 1;
+    Entry e{fn, dev, threads, bytes, occ};
+    if (n < 64) cache[n++] = e;
+    else cache[(reinterpret_cast<uintptr_t>(fn) >> 4) % 64] = e;
+    return occ;
+}
+
+}  // namespace qmv

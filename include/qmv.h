@@ -1,0 +1,217 @@
+/*
+ * qmv.h -- C ABI of the GB300 block-quantised matrix multiply library (libqmv).
+ *
+ * The library multiplies by weights stored in GGUF quantised blocks, unpacking
+ * and scaling them inside the dot product.  The operations are those named on
+ * the llamay documentation pages:
+ *   "Architecture" page, "The package map": pkg/quant owns the block layouts,
+ *     dequantisation and the fused W4A8 kernels (4-bit weights, 8-bit
+ *     activations); pkg/tensor owns MatVec (decode) and MatMul (prefill).
+ *   "Architecture" page, "The two phases": decode is bound by memory, prefill
+ *     by arithmetic, so the two get different kernels.
+ *   "Architecture" page, "A request, end to end": decode is batched across
+ *     sequences so that the weights are read once for N of them.
+ *   "Models and formats" page, "Tensor formats": the block formats.
+ *   "Models and formats" page, "Architectures": mixture-of-experts models keep
+ *     experts as stacked 3-D tensors, a router picks k of n per token, and
+ *     gpt-oss carries a bias on every expert projection.
+ *
+ * Conventions shared by every call
+ * ---------------------------------
+ *  - A weight matrix W has `rows` outputs and `cols` inputs.  Each row is
+ *    cols/bs consecutive blocks, rows are consecutive (the GGUF layout).  W must
+ *    start on a 16-byte boundary.
+ *  - Every pointer argument named W, x, xq, X, y, Y, ids, gates, bias, out is a
+ *    DEVICE pointer owned by the caller; the library never frees or keeps it.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Every call only enqueues work on that stream and returns; none
+ *    synchronises.  Inputs must stay valid, and outputs must not be read, until
+ *    the stream reaches the call.  Outputs must not alias inputs.
+ *  - Calls allocate no device memory.  The mixture-of-experts call needs
+ *    scratch, given once through qmv_set_workspace().
+ *  - Errors: every call validates its arguments on the host before launching
+ *    and returns a negative qmv_status without launching anything on failure;
+ *    qmv_last_error() then names what is supported (the pages' convention of
+ *    refusing with a message that names what does work).  A launch failure
+ *    returns QMV_ERR_CUDA.  Faults found on the device (an expert id out of
+ *    range, a pipeline wait that gave up) set a device status word that
+ *    qmv_get_status() reads; kernels never trap.
+ *  - Results are deterministic: the same inputs give bit-identical outputs,
+ *    and output row r of vector v does not depend on the other vectors of the
+ *    batch (decode is batch-invariant, as the pages' determinism claim asks).
+ */
+#ifndef QMV_H
+#define QMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QMV_VERSION 10000   /* 1.0.0 */
+
+/* Block and element types. */
+typedef enum {
+    QMV_Q4_0 = 1,   /* 32 w, 18 B: fp16 d | 16 B nibbles;                 w = d*(q-8)            */
+    QMV_Q5_0 = 2,   /* 32 w, 22 B: fp16 d | u32 5th bits | 16 B nibbles;  w = d*(q-16)           */
+    QMV_Q8_0 = 3,   /* 32 w, 34 B: fp16 d | int8[32];                     w = d*q                */
+    QMV_Q4_K = 4,   /* 256 w, 144 B: fp16 d | fp16 dmin | 12 B 6-bit sc/m | 128 B nibbles;
+                                                                         w = d*sc*q - dmin*m    */
+    QMV_Q6_K = 5,   /* 256 w, 210 B: 128 B low 4 bits | 64 B high 2 bits | int8 sc[16] | fp16 d;
+                                                                         w = d*sc*(q-32)        */
+    QMV_MXFP4 = 6,  /* 32 w, 17 B: E8M0 e | 16 B E2M1 codes;             w = 2^(e-127)*E2M1(q)  */
+    QMV_Q8_K = 7,   /* activations only, 256 w, 292 B: fp32 d | int8[256] | int16 bsums[16]      */
+    QMV_F32 = 8,    /* plain fp32 */
+    QMV_BF16 = 9    /* plain bfloat16 */
+} qmv_type;
+
+/* A multiply's format is the weight type plus the activation type. */
+#define QMV_FMT(wtype, atype) ((int)(wtype) | ((int)(atype) << 8))
+
+typedef enum {
+    QMV_OK = 0,
+    QMV_ERR_INVALID_ARG = -1,   /* null pointer, negative size                              */
+    QMV_ERR_SHAPE = -2,         /* cols not a multiple of the block length, or over a limit */
+    QMV_ERR_UNSUPPORTED = -3,   /* format / activation pair not provided                    */
+    QMV_ERR_ALIGN = -4,         /* a pointer is not aligned as the call requires            */
+    QMV_ERR_WORKSPACE = -5,     /* workspace missing or too small                           */
+    QMV_ERR_CUDA = -6,          /* a CUDA call failed (the message has the CUDA string)     */
+    QMV_ERR_DEVICE_STATUS = -7  /* a kernel reported a fault through the status word        */
+} qmv_status;
+
+/* Library version, QMV_VERSION of the build. */
+int qmv_version(void);
+/* Static text for a qmv_status code. */
+const char* qmv_strerror(int err);
+/* Detail of the last failed call on this host thread ("" if none). */
+const char* qmv_last_error(void);
+
+/* Block geometry: elements per block (32 or 256; 1 for F32/BF16; 0 if unknown),
+ * bytes per block, bytes of one row of `cols` elements (0 if cols is not a
+ * multiple of the block length). */
+int    qmv_block_elems(int type);
+size_t qmv_block_bytes(int type);
+size_t qmv_row_bytes(int type, int64_t cols);
+
+/* ---------------------------------------------------------------------------
+ * qmv_quantize_act -- fp32 activations to 8-bit blocks (the "A8" of W4A8;
+ * "Architecture" page, "The package map", pkg/quant).
+ *   fmt : QMV_Q8_0 (32-element blocks, fp16 scale, 34 B) or
+ *         QMV_Q8_K (256-element blocks, fp32 scale, int16 sums of each run of
+ *         16 codes, 292 B).
+ *   x   : n fp32 values, 4-byte aligned; several vectors may be laid end to end
+ *         as long as each vector's length is a multiple of the block length.
+ *   xq  : n/bs blocks out.
+ *   n   : multiple of 32 (Q8_0) or 256 (Q8_K); 0 is a no-op.
+ * Per block: amax = max|x|, d = amax/127, q = round-half-away(x * (1/d))
+ * clamped to +-127 (q = 0 when amax = 0); fp32 arithmetic, one rounding per
+ * operation.  Q8_0 stores d rounded to fp16, Q8_K the fp32 d.
+ * ------------------------------------------------------------------------- */
+int qmv_quantize_act(int fmt, const float* x, void* xq, int64_t n, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * qmv_dequantize -- weights to fp32 ("The package map", pkg/quant:
+ * dequantisation).  out is rows x cols fp32, row-major.  Bit-exact: every
+ * format's weight is an fp32 value, except Q4_K whose weight is the single
+ * rounding of d*sc*q - dmin*m.
+ * ------------------------------------------------------------------------- */
+int qmv_dequantize(int type, const void* W, int64_t rows, int64_t cols, float* out, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * qmv_block_dots -- the integers of the fused W4A8 dot product, exposed for
+ * verification.  For weight block b of row r against activation block b of
+ * vector v:
+ *   out[((v*rows + r)*nb + b)*2 + 0] = S  = sum_i sub_scale_i * code_i * xq_i
+ *   out[((v*rows + r)*nb + b)*2 + 1] = Mn = sum_i sub_min_i * xq_i  (Q4_K; else 0)
+ * with code = q-8 (Q4_0), q-16 (Q5_0), q (Q8_0, Q4_K), q-32 (Q6_K), twice the
+ * E2M1 value (MXFP4); sub_scale = the 6-bit (Q4_K) or int8 (Q6_K) sub-block
+ * scale, else 1; sub_min = the Q4_K 6-bit min.  xq is Q8_0 for the 32-element
+ * formats and Q8_K for Q4_K/Q6_K, [n_vec][cols/bs] blocks.  out is int32,
+ * [n_vec][rows][cols/bs][2].  These are the same device routines the matvec
+ * kernels use.
+ * ------------------------------------------------------------------------- */
+int qmv_block_dots(int type, const void* W, int64_t rows, int64_t cols,
+                   const void* xq, int n_vec, int32_t* out, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * qmv_matvec -- decode: y[v][r] = sum_c w[r][c] * xhat[v][c] for n_vec
+ * vectors sharing one pass over the weights ("The package map", pkg/tensor
+ * MatVec; "A request, end to end": N sequences read the weights once).
+ *   fmt : QMV_FMT(wtype, atype), wtype in {Q4_0, Q5_0, Q8_0, MXFP4} with atype
+ *         in {F32, Q8_0}, or wtype in {Q4_K, Q6_K} with atype in {F32, Q8_K}.
+ *   x   : F32: fp32 [n_vec][cols], 16-byte aligned, xhat = x.
+ *         Q8_0/Q8_K: [n_vec][cols/bs] blocks from qmv_quantize_act,
+ *         4-byte aligned, xhat = d_x*q (the W4A8 product: integer dot per
+ *         block, then the two scales, fp32 accumulation).
+ *   y   : fp32 [n_vec][rows], overwritten.
+ *   n_vec : 0..64 (0 is a no-op).
+ * Accuracy: |y - exact| <= 1e-4 * sum_c |w*xhat| per output (in practice
+ * ~1e-6).  Batch-invariant: row r of vector v is bit-identical whatever
+ * n_vec is and whatever the other vectors hold.
+ * ------------------------------------------------------------------------- */
+int qmv_matvec(int fmt, const void* W, int64_t rows, int64_t cols,
+               const void* x, float* y, int n_vec, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * qmv_matmul -- prefill: Y[m][r] = sum_c w[r][c] * xhat[m][c]
+ * ("The package map", pkg/tensor MatMul; "The two phases": prefill is
+ * arithmetic-bound).  Batched prefill must agree with sequential decode
+ * ("The forward pass").
+ *   fmt : QMV_FMT(QMV_Q4_K, QMV_BF16): X bf16 [m][cols]; the weights are
+ *         dequantised to bf16 tiles (w rounded once from its fp32 value) and
+ *         multiplied on the tensor cores with fp32 accumulation.
+ *         QMV_FMT(QMV_Q4_K, QMV_Q8_K): X Q8_K blocks [m][cols/256] (W4A8).
+ *   X   : 16-byte aligned.   Y : fp32 [m][rows], overwritten.
+ *   m   : >= 0.
+ * ------------------------------------------------------------------------- */
+int qmv_matmul(int fmt, const void* W, int64_t rows, int64_t cols,
+               const void* X, float* Y, int64_t m, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * qmv_moe_matvec -- mixture of experts over a stacked 3-D weight tensor
+ * W3d[n_expert][rows][cols] ("Models and formats", "Architectures": k of n
+ * experts per token, stacked 3-D expert tensors, a bias on every expert
+ * projection).  (token, slot) pairs are grouped by expert with a stable
+ * counting sort so that each expert's weights are read once per call.
+ *   ids   : int32 [n_tok][k], expert of each slot (0 <= id < n_expert; an id
+ *           out of range sets the device status word and its slot is skipped).
+ *   gates : NULL -> the up/gate form: x is [n_tok][cols], shared by the k
+ *                   slots, and y[t][s][r] = (W[ids[t][s]] x_t)[r] + bias.
+ *           non-NULL fp32 [n_tok][k] -> the down form: x is [n_tok][k][cols],
+ *                   one input per slot, and
+ *                   y[t][r] = sum_s gates[t][s] * ((W[ids[t][s]] x_{t,s})[r] + bias),
+ *                   summed in slot order.
+ *   bias  : fp32 [n_expert][rows], or NULL for none.
+ *   fmt   : QMV_FMT(wtype, atype) with the pairs of qmv_matvec (activations
+ *           F32 or 8-bit blocks, one block row per input vector), or
+ *           atype = BF16 (x bf16) for weight types whose values are exact in
+ *           bf16 (MXFP4, Q4_0, Q5_0).
+ *   Workspace: qmv_workspace_size(QMV_OP_MOE, ...) bytes set by
+ *           qmv_set_workspace(); calls that share the workspace must be
+ *           ordered on one stream.
+ * ------------------------------------------------------------------------- */
+int qmv_moe_matvec(int fmt, const void* W3d, int n_expert, int64_t rows, int64_t cols,
+                   const int32_t* ids, const float* gates, int k,
+                   const void* x, float* y, int64_t n_tok, const float* bias,
+                   void* stream);
+
+/* Workspace for the calls that need scratch. */
+enum { QMV_OP_MATVEC = 1, QMV_OP_MATMUL = 2, QMV_OP_MOE = 3 };
+/* Bytes of workspace `op` needs for these sizes (n = n_tok*k for MoE).  0 if none. */
+size_t qmv_workspace_size(int op, int fmt, int64_t rows, int64_t cols, int64_t n);
+/* Register a caller-owned device buffer (256-byte aligned) as the workspace of
+ * the current device; NULL/0 clears it.  The library keeps the pointer only. */
+int qmv_set_workspace(void* ptr, size_t bytes);
+
+/* Synchronise `stream`, read and clear the device status word of the current
+ * device.  Returns QMV_OK, or QMV_ERR_DEVICE_STATUS with qmv_last_error()
+ * describing the fault, or QMV_ERR_CUDA. */
+int qmv_get_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMV_H */

@@ -1,0 +1,28 @@
+"""Helpers for the GPU parity tests: device copies and the tolerance of the
+multiply (per output |y - y_oracle| <= 1e-4 * sum_c |w * xhat|; an output
+whose sum of magnitudes is 0 must be exactly 0)."""
+import numpy as np
+import torch
+
+TOL = 1e-4
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def assert_close(y, yref, yabs, tol=TOL, what=""):
+    y = np.asarray(y, dtype=np.float64)
+    err = np.abs(y - yref)
+    bound = tol * yabs
+    bad = err > bound
+    if bad.any():
+        i = np.argwhere(bad)[0]
+        raise AssertionError(f"{what}: {bad.sum()} outputs out of tolerance; first at {tuple(i)}: "
+                             f"y={y[tuple(i)]!r} ref={yref[tuple(i)]!r} sum|wx|={yabs[tuple(i)]!r}")
+    return float((err / np.maximum(yabs, 1e-300)).max()) if err.size else 0.0

@@ -1,0 +1,92 @@
+"""Host-side tests of the C ABI (no GPU needed): the library builds and loads,
+exports every entry point include/qmv.h declares, and refuses bad arguments
+with the documented codes before any CUDA work."""
+import os
+import re
+
+import pytest
+
+import gguf_block_quantised_gb300 as q
+from gguf_block_quantised_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return q.load()
+
+
+def header_symbols():
+    src = open(os.path.join(ROOT, "include", "qmv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(qmv_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    syms = header_symbols()
+    assert len(syms) >= 15
+    for s in syms:
+        assert hasattr(lib, s), s
+    assert set(syms) == set(q.EXPORTS)
+
+
+def test_geometry(lib):
+    assert q.qmv_version() == 10000
+    expect = {q.Q4_0: (32, 18), q.Q5_0: (32, 22), q.Q8_0: (32, 34), q.MXFP4: (32, 17),
+              q.Q4_K: (256, 144), q.Q6_K: (256, 210), q.Q8_K: (256, 292)}
+    for t, (bs, bb) in expect.items():
+        assert q.qmv_block_elems(t) == bs and q.qmv_block_bytes(t) == bb
+    assert q.qmv_row_bytes(q.Q5_0, 896) == 616
+    assert q.qmv_row_bytes(q.Q4_K, 14336) == 8064
+    assert q.qmv_row_bytes(q.Q4_K, 300) == 0
+    assert q.qmv_block_elems(99) == 0
+
+
+def rc(lib, name, *args):
+    return getattr(lib, name)(*args)
+
+
+def test_refusals(lib):
+    F = q.FMT
+    # shape: K-quant rows must be multiples of 256 (and the message says what to use)
+    assert rc(lib, "qmv_matvec", F(q.Q4_K, q.F32), 4096, 8, 300, 4096, 4096, 1, None) == q.ERR_SHAPE
+    assert "256" in q.qmv_last_error()
+    assert rc(lib, "qmv_matvec", F(q.Q4_0, q.F32), 4096, 8, 40, 4096, 4096, 1, None) == q.ERR_SHAPE
+    # unsupported weight type / pairing
+    assert rc(lib, "qmv_matvec", F(q.Q8_K, q.F32), 4096, 8, 256, 4096, 4096, 1, None) == q.ERR_UNSUPPORTED
+    assert "Q4_0" in q.qmv_last_error()
+    assert rc(lib, "qmv_matvec", F(q.Q4_K, q.Q8_0), 4096, 8, 256, 4096, 4096, 1, None) == q.ERR_UNSUPPORTED
+    assert rc(lib, "qmv_matvec", F(q.Q4_0, q.BF16), 4096, 8, 256, 4096, 4096, 1, None) == q.ERR_UNSUPPORTED
+    # null / negative / alignment
+    assert rc(lib, "qmv_matvec", F(q.Q4_0, q.F32), None, 8, 256, 4096, 4096, 1, None) == q.ERR_INVALID_ARG
+    assert rc(lib, "qmv_matvec", F(q.Q4_0, q.F32), 4096, -1, 256, 4096, 4096, 1, None) == q.ERR_INVALID_ARG
+    assert rc(lib, "qmv_matvec", F(q.Q4_0, q.F32), 4096, 8, 256, 4096, 4096, 65, None) == q.ERR_INVALID_ARG
+    assert rc(lib, "qmv_matvec", F(q.Q4_0, q.F32), 4104, 8, 256, 4096, 4096, 1, None) == q.ERR_ALIGN
+    assert rc(lib, "qmv_matvec", F(q.Q4_0, q.F32), 4096, 8, 256, 4100, 4096, 1, None) == q.ERR_ALIGN
+    # empty work is a no-op, even without pointers
+    assert rc(lib, "qmv_matvec", F(q.Q4_0, q.F32), None, 0, 256, None, None, 1, None) == q.OK
+    assert rc(lib, "qmv_matvec", F(q.Q4_0, q.Q8_0), 4096, 8, 256, None, None, 0, None) == q.OK
+    # quantiser
+    assert rc(lib, "qmv_quantize_act", q.Q4_0, 4096, 4096, 32, None) == q.ERR_UNSUPPORTED
+    assert rc(lib, "qmv_quantize_act", q.Q8_K, 4096, 4096, 32, None) == q.ERR_SHAPE
+    assert rc(lib, "qmv_quantize_act", q.Q8_0, 4096, 4096, 0, None) == q.OK
+    assert rc(lib, "qmv_quantize_act", q.Q8_0, None, 4096, 32, None) == q.ERR_INVALID_ARG
+    # verification calls
+    assert rc(lib, "qmv_dequantize", q.Q6_K, 4096, 2, 200, 4096, None) == q.ERR_SHAPE
+    assert rc(lib, "qmv_block_dots", q.Q8_0, 4096, 2, 64, 4096, -1, 4096, None) == q.ERR_INVALID_ARG
+    # workspace alignment
+    assert rc(lib, "qmv_set_workspace", 4100, 1024) == q.ERR_ALIGN
+
+
+def test_error_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5, -6, -7):
+        assert q.qmv_strerror(code)
+    assert q.qmv_strerror(-99) == "unknown error"
+
+
+def test_binding_raises_with_message(lib):
+    with pytest.raises(q.QmvError) as e:
+        q.qmv_matvec(q.FMT(q.Q4_K, q.F32), 4096, 8, 300, 4096, 4096, 1, stream=0)
+    assert e.value.code == q.ERR_SHAPE and "multiple of 256" in str(e.value)

@@ -1,0 +1,186 @@
+"""GPU parity of the activation quantiser, dequantisation, the W4A8 integer
+block dots and the decode matvec against the CPU oracle, through the C ABI.
+
+Bars: bit-exact for quantised activations, dequantised weights and integer
+dots; |y - y_oracle| <= 1e-4 * sum|w*xhat| for every matvec output; decode
+bit-identical whatever n_vec (batch invariance)."""
+import numpy as np
+import pytest
+import torch
+
+from gguf_block_quantised_gb300 import synth
+from gpu_util import assert_close, dev, host
+
+pytestmark = pytest.mark.gpu
+
+W32 = [1, 2, 3, 6]          # Q4_0, Q5_0, Q8_0, MXFP4
+WK = [4, 5]                 # Q4_K, Q6_K
+ALLW = W32 + WK
+
+
+def act_for(t):
+    return 3 if t in W32 else 7   # Q8_0 / Q8_K
+
+
+def shapes_for(t):
+    if t in W32:
+        # ragged tile (37 rows), C1/C2 width, several K-chunks with a ragged last chunk
+        return [(1, 32), (37, 96), (300, 896), (45, 8288)]
+    return [(1, 256), (37, 512), (70, 4096), (19, 14336)]
+
+
+@pytest.mark.parametrize("atype", [3, 7])
+@pytest.mark.parametrize("n", [32 * 7, 256 * 3, 256 * 64])
+def test_quantize_act_bit_exact(qmv, orc, atype, n):
+    if n % (32 if atype == 3 else 256):
+        pytest.skip("n not a multiple of the block")
+    g = np.random.default_rng(n + atype)
+    x = (g.standard_normal(n) * np.exp2(g.integers(-6, 6, n // 32).repeat(32))).astype(np.float32)
+    x[:32] = 0.0                      # an all-zero block
+    x[32:64] = np.float32(2.5)        # ties of x*id
+    ref = orc.quantize_act(atype, x)
+    xq = torch.zeros(ref.size, dtype=torch.uint8, device="cuda")
+    qmv.qmv_quantize_act(atype, dev(x), xq, n)
+    assert np.array_equal(host(xq), ref)
+
+
+@pytest.mark.parametrize("t", ALLW)
+def test_dequantize_bit_exact(qmv, orc, t):
+    for rows, cols in shapes_for(t)[:3]:
+        W = synth.weights(t, rows, cols, seed=1, tensor_id=t)
+        ref = orc.dequant(t, W, rows, cols)
+        out = torch.empty((rows, cols), dtype=torch.float32, device="cuda")
+        qmv.qmv_dequantize(t, dev(W), rows, cols, out)
+        assert np.array_equal(host(out).view(np.uint32), ref.view(np.uint32)), (t, rows, cols)
+
+
+@pytest.mark.parametrize("t", ALLW)
+def test_block_dots_bit_exact(qmv, orc, t):
+    rows, cols = shapes_for(t)[1]
+    n_vec = 3
+    W = synth.weights(t, rows, cols, seed=2, tensor_id=t)
+    x = synth.activations(n_vec, cols, seed=2)
+    xq = orc.quantize_act(act_for(t), x)
+    ref = orc.block_dots(t, W, rows, cols, xq, n_vec)
+    assert np.abs(ref).max() < 2 ** 31
+    out = torch.empty(ref.shape, dtype=torch.int32, device="cuda")
+    qmv.qmv_block_dots(t, dev(W), rows, cols, dev(xq), n_vec, out)
+    assert np.array_equal(host(out).astype(np.int64), ref)
+
+
+@pytest.mark.parametrize("a8", [True, False], ids=["A8", "A32"])
+@pytest.mark.parametrize("t", ALLW)
+def test_matvec_parity(qmv, orc, t, a8):
+    at = act_for(t) if a8 else 8
+    for rows, cols in shapes_for(t):
+        for n_vec in (1, 3, 16):
+            W = synth.weights(t, rows, cols, seed=3, tensor_id=rows)
+            x = synth.activations(n_vec, cols, seed=3, tensor_id=cols)
+            xin = orc.quantize_act(at, x) if a8 else x
+            yref, yabs = orc.matvec(t, at, W, rows, cols, xin, n_vec)
+            y = torch.full((n_vec, rows), float("nan"), dtype=torch.float32, device="cuda")
+            qmv.qmv_matvec(qmv.FMT(t, at), dev(W), rows, cols, dev(xin), y, n_vec)
+            assert_close(host(y), yref, yabs, what=f"t={t} a8={a8} {rows}x{cols} n_vec={n_vec}")
+    qmv.qmv_get_status()
+
+
+@pytest.mark.parametrize("a8", [True, False], ids=["A8", "A32"])
+@pytest.mark.parametrize("t", ALLW)
+def test_matvec_batch_invariance(qmv, orc, t, a8):
+    """Output (v, r) is bit-identical whether v is decoded alone or with others
+    (the pages' determinism claim: "regardless of ... batch composition")."""
+    at = act_for(t) if a8 else 8
+    rows, cols = shapes_for(t)[2]
+    n_vec = 20
+    W = dev(synth.weights(t, rows, cols, seed=4))
+    x = synth.activations(n_vec, cols, seed=4)
+    xin = orc.quantize_act(at, x) if a8 else x
+    xd = dev(xin)
+    y = torch.empty((n_vec, rows), dtype=torch.float32, device="cuda")
+    qmv.qmv_matvec(qmv.FMT(t, at), W, rows, cols, xd, y, n_vec)
+    ys = host(y)
+    for v in (0, 7, 19):
+        y1 = torch.empty((1, rows), dtype=torch.float32, device="cuda")
+        qmv.qmv_matvec(qmv.FMT(t, at), W, rows, cols, xd[v], y1, 1)
+        assert np.array_equal(host(y1)[0].view(np.uint32), ys[v].view(np.uint32)), v
+    # and across vector groups of a different composition
+    y5 = torch.empty((5, rows), dtype=torch.float32, device="cuda")
+    qmv.qmv_matvec(qmv.FMT(t, at), W, rows, cols, xd[3:8], y5, 5)
+    assert np.array_equal(host(y5).view(np.uint32), ys[3:8].view(np.uint32))
+
+
+def test_matvec_quantised_pipeline(qmv, orc):
+    """fp32 x -> qmv_quantize_act -> qmv_matvec on the device equals the oracle's
+    quantise-then-multiply (the W4A8 hot path end to end)."""
+    t, rows, cols, n_vec = 2, 256, 896, 8
+    W = synth.weights(t, rows, cols, seed=5)
+    x = synth.activations(n_vec, cols, seed=5)
+    xq = torch.empty(n_vec * 28 * 34, dtype=torch.uint8, device="cuda")
+    qmv.qmv_quantize_act(3, dev(x), xq, n_vec * cols)
+    y = torch.empty((n_vec, rows), dtype=torch.float32, device="cuda")
+    qmv.qmv_matvec(qmv.FMT(t, 3), dev(W), rows, cols, xq, y, n_vec)
+    yref, yabs = orc.matvec(t, 3, W, rows, cols, orc.quantize_act(3, x), n_vec)
+    assert_close(host(y), yref, yabs)
+
+
+def test_matvec_edge_cases(qmv, orc):
+    # odd MXFP4 rows: the matrix ends off a 16-byte boundary (ragged tail path)
+    for rows in (1, 15, 17, 33):
+        t, cols = 6, 32
+        W = synth.weights(t, rows, cols, seed=rows)
+        x = synth.activations(2, cols, seed=rows)
+        yref, yabs = orc.matvec(t, 8, W, rows, cols, x, 2)
+        y = torch.empty((2, rows), dtype=torch.float32, device="cuda")
+        qmv.qmv_matvec(qmv.FMT(t, 8), dev(W), rows, cols, dev(x), y, 2)
+        assert_close(host(y), yref, yabs, what=f"mxfp4 rows={rows}")
+    # zero activations give exact zeros
+    t, rows, cols = 4, 40, 512
+    W = dev(synth.weights(t, rows, cols, seed=9))
+    xq = dev(orc.quantize_act(7, np.zeros((2, cols), np.float32)))
+    y = torch.full((2, rows), 7.0, dtype=torch.float32, device="cuda")
+    qmv.qmv_matvec(qmv.FMT(t, 7), W, rows, cols, xq, y, 2)
+    assert (host(y) == 0).all()
+    # n_vec = 0 and rows = 0 are no-ops that leave y alone
+    y = torch.full((1, rows), 7.0, dtype=torch.float32, device="cuda")
+    qmv.qmv_matvec(qmv.FMT(t, 7), W, rows, cols, xq, y, 0)
+    qmv.qmv_matvec(qmv.FMT(t, 7), W, 0, cols, xq, y, 1)
+    assert (host(y) == 7).all()
+    # misaligned weights are refused, not read
+    buf = torch.zeros(100000, dtype=torch.uint8, device="cuda")
+    with pytest.raises(qmv.QmvError) as e:
+        qmv.qmv_matvec(qmv.FMT(1, 8), buf.data_ptr() + 8, 4, 32, dev(np.zeros(32, np.float32)), y, 1)
+    assert e.value.code == qmv.ERR_ALIGN
+    qmv.qmv_get_status()
+
+
+# ---- the configurations' full shapes, checked on sampled rows ----------------------
+
+CONFIG_SHAPES = [
+    # single Q4_0 GEMV 896x896 (A32 and A8)
+    (1, 896, 896, (1,)),
+    # Qwen2.5-0.5B-shaped decode: q/o, k/v, gate/up, down in Q5_0; lm_head in Q8_0
+    (2, 896, 896, (1, 8)), (2, 128, 896, (1, 8)), (2, 4864, 896, (1, 8)), (2, 896, 4864, (1, 8)),
+    (3, 151936, 896, (1, 8)),
+    # Llama-3-8B-shaped decode in K-quants
+    (4, 4096, 4096, (1, 4, 16)), (4, 1024, 4096, (1, 16)), (4, 14336, 4096, (1, 16)),
+    (4, 4096, 14336, (1, 4, 16)), (5, 128256, 4096, (1, 4, 16)),
+]
+
+
+@pytest.mark.parametrize("cfg", CONFIG_SHAPES, ids=lambda c: f"t{c[0]}_{c[1]}x{c[2]}")
+def test_config_shapes_sampled(qmv, orc, cfg):
+    t, rows, cols, nvecs = cfg
+    W = synth.weights(t, rows, cols, seed=1, tensor_id=rows * 7 + cols)
+    Wd = dev(W)
+    g = np.random.default_rng(rows + cols)
+    ids = np.unique(np.concatenate([[0, rows - 1], g.integers(0, rows, 48)]))
+    for a8 in (True, False):
+        at = act_for(t) if a8 else 8
+        for n_vec in nvecs:
+            x = synth.activations(n_vec, cols, seed=1)
+            xin = orc.quantize_act(at, x) if a8 else x
+            y = torch.empty((n_vec, rows), dtype=torch.float32, device="cuda")
+            qmv.qmv_matvec(qmv.FMT(t, at), Wd, rows, cols, dev(xin), y, n_vec)
+            yref, yabs = orc.matvec(t, at, W, rows, cols, xin, n_vec, row_ids=ids)
+            assert_close(host(y)[:, ids], yref, yabs, what=f"{cfg} a8={a8} n_vec={n_vec}")
+    qmv.qmv_get_status()
