@@ -151,9 +151,12 @@ struct Fmt<QMV_MXFP4> : Fmt32Base<QMV_MXFP4> {
         const uint32_t sel = s & 0x7777u;
         const uint32_t pos = __byte_perm(0x03020100u, 0x0c080604u, sel);   // 0,1,2,3 | 4,6,8,12
         const uint32_t neg = __byte_perm(0xfdfeff00u, 0xf4f8fafcu, sel);   // 0,-1,-2,-3 | -4,-6,-8,-12
-        // 0xff in the bytes whose nibble has its sign bit (bit 3) set: the
-        // sign-replicate mode of PRMT copies bit 7 of the selected byte.
-        const uint32_t m = __byte_perm(s << 4, s, 0xd9c8u);
+        // 0xff in the bytes whose nibble has its sign bit (bit 3) set: with
+        // bit 3 of a selector nibble set, prmt.b32 replicates bit 7 of the
+        // selected byte.  (The __byte_perm intrinsic only honours 3-bit
+        // selectors, so this one is written in PTX.)
+        uint32_t m;
+        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(m) : "r"(s << 4), "r"(s), "r"(0xd9c8u));
         return (pos & ~m) | (neg & m);
     }
     static __device__ __forceinline__ float e8m0_half(uint32_t e)   // 2^(e-128)
