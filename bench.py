@@ -5,8 +5,9 @@ Workload (one step): a Qwen2.5-0.5B-shaped decode step through the W4A8 path
 -- for each of 24 layers, the fp32 activations are quantised to Q8_0 blocks
 and multiplied by q 896x896, k 128x896, v 128x896, o 896x896, gate 4864x896,
 up 4864x896 and down 896x4864 weights in Q5_0; then the lm_head 151936x896 in
-Q8_0.  169 matvecs and 97 activation quantisations; 390,648,832 weight bytes
-per step (372.55 MiB), synthetic weights and N(0,1) activations, batch 1.
+Q8_0.  169 matvec launches, each quantising its own input, chained with
+programmatic dependent launch; 390,648,832 weight bytes per step
+(372.55 MiB), synthetic weights and N(0,1) activations, batch 1.
 The weights (> 3x the 129 MB L2) are streamed cold every step.
 
 Metric: weight GB/s = weight bytes of the step / step time (higher is
@@ -124,10 +125,15 @@ class ClockSampler:
 
 # ---- the decode step ---------------------------------------------------------------------
 class DecodeStep:
-    """Weights and buffers of the Qwen2.5-0.5B-shaped decode step on one device."""
+    """Weights and buffers of the Qwen2.5-0.5B-shaped decode step on one device.
 
-    def __init__(self, q, torch, n_vec, seed=1):
-        self.q, self.torch, self.n_vec = q, torch, n_vec
+    fused=True: each matvec quantises its fp32 activations itself
+    (QMV_FLAG_QUANTIZE_X) and is launched as a programmatic dependent of the
+    one before (QMV_FLAG_PDL): 169 launches per step.  fused=False: separate
+    qmv_quantize_act launches, plain stream order: 266 launches per step."""
+
+    def __init__(self, q, torch, n_vec, seed=1, fused=True):
+        self.q, self.torch, self.n_vec, self.fused = q, torch, n_vec, fused
         dev = torch.device("cuda")
         self.W = []
         tid = 0
@@ -149,11 +155,18 @@ class DecodeStep:
         self.y = [[torch.empty((n_vec, r), dtype=torch.float32, device=dev) for _, r, _, _ in LAYER_MATS]
                   for _ in range(LAYERS)]
         self.logits = torch.empty((n_vec, VOCAB), dtype=torch.float32, device=dev)
-        self.launches = LAYERS * (4 + 7) + 2
+        self.launches = LAYERS * 7 + 1 if fused else LAYERS * (4 + 7) + 2
 
     def run(self, stream):
         q, n = self.q, self.n_vec
         s = stream.cuda_stream
+        if self.fused:
+            fl = q.FLAG_QUANTIZE_X | q.FLAG_PDL
+            for l in range(LAYERS):
+                for m, (W, rows, cols, inp) in enumerate(self.W[l]):
+                    q.qmv_matvec(q.FMT(Q5_0, Q8_0) | fl, W, rows, cols, self.x[4 * l + inp], self.y[l][m], n, s)
+            q.qmv_matvec(q.FMT(Q8_0, Q8_0) | fl, self.lm, VOCAB, HID, self.x[-1], self.logits, n, s)
+            return
         for l in range(LAYERS):
             for i in range(4):
                 j = 4 * l + i
@@ -280,32 +293,39 @@ def main():
     q.load()
     stream = torch.cuda.Stream()
 
-    # --- the step at batch 1 (the headline) and batch 8
+    # --- the step at batch 1 (the headline) and batch 8; the two-launch form for comparison
     step1 = DecodeStep(q, torch, 1)
     step8 = DecodeStep(q, torch, 8)
+    step1u = DecodeStep(q, torch, 1, fused=False)
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     ms1, clocks = time_graph(torch, step1.run, stream, args.steps, args.warmup, sampler_index=local)
     ms8, _ = time_graph(torch, step8.run, stream, max(args.steps // 4, 10), args.warmup)
+    ms1u, _ = time_graph(torch, step1u.run, stream, max(args.steps // 4, 10), args.warmup)
     q.qmv_get_status(stream)
     if ws > 1:
         t = torch.tensor([ms1, ms8], device="cuda")
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms1, ms8 = t.tolist()
 
-    # --- the dominant kernel alone: lm_head matvec (144.6 MB per launch, > L2)
+    # --- the dominant kernel alone: lm_head matvec (144.6 MB per launch).  Four
+    # copies of the weights are rotated (578 MB > 4x L2), so every launch reads
+    # its weights from HBM.
     lm_bytes = VOCAB * row_bytes(Q8_0, HID)
-    def lm_only(s):
-        q.qmv_matvec(q.FMT(Q8_0, Q8_0), step1.lm, VOCAB, HID, step1.xq[-1], step1.logits, 1, s.cuda_stream)
+    lm_copies = [step1.lm] + [step1.lm.clone() for _ in range(3)]
+
+    def lm_only(s, Wl):
+        q.qmv_matvec(q.FMT(Q8_0, Q8_0) | q.FLAG_QUANTIZE_X, Wl, VOCAB, HID, step1.x[-1], step1.logits, 1,
+                     s.cuda_stream)
     lm_reps = 200
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
-        lm_only(stream)
+        lm_only(stream, lm_copies[0])
         stream.synchronize()
         with torch.cuda.graph(g, stream=stream):
-            for _ in range(lm_reps):
-                lm_only(stream)
+            for i in range(lm_reps):
+                lm_only(stream, lm_copies[i % 4])
     g.replay()
     stream.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -354,17 +374,22 @@ def main():
         "dtype": "int8xint4->fp32",
         "data": "synthetic",
         "config": {"workload": "qwen2.5-0.5b-shaped decode step (24 layers q/k/v/o/gate/up/down Q5_0 + lm_head "
-                               "151936x896 Q8_0; activations quantised to Q8_0), batch 1",
+                               "151936x896 Q8_0; fp32 activations quantised to Q8_0 inside each matvec), batch 1",
+                   "launches_per_step": step1.launches,
                    "weight_bytes_per_step": STEP_WEIGHT_BYTES, "parallelism": f"replicas x{ws}",
                    "l2": "weights 390.6 MB > 129 MB L2, streamed cold every step (no flush needed)",
                    "graph": "step captured once as a CUDA graph and replayed"},
         "frac_of_hbm": value / ws / hbm,
         "batch8": {"ms_per_step": ms8, "value": ws * STEP_WEIGHT_BYTES / (ms8 / 1e3) / 1e9, "unit": "GB/s",
                    "vector_rate_tok_s": ws * 8 / (ms8 / 1e3)},
-        "roofline": {"bound": "hbm", "kernel": "k_gemv<Q8_0,A8,1> lm_head 151936x896",
+        "unfused_batch1": {"ms_per_step": ms1u, "value": ws * STEP_WEIGHT_BYTES / (ms1u / 1e3) / 1e9,
+                           "unit": "GB/s", "launches_per_step": step1u.launches,
+                           "how": "qmv_quantize_act + qmv_matvec as separate launches, no PDL"},
+        "roofline": {"bound": "hbm", "kernel": "k_gemv<Q8_0,A8,NV=1> lm_head 151936x896 (quantising its fp32 input)",
                      "achieved": lm_gbs, "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": lm_gbs / hbm, "traffic": None,
-                     "algorithmic_bytes_per_launch": lm_bytes, "launch_ms": lm_ms},
+                     "algorithmic_bytes_per_launch": lm_bytes, "launch_ms": lm_ms,
+                     "l2": "4 weight copies rotated, each launch reads cold"},
         "clocks": clocks,
         "e2e": {"value": ws * STEP_WEIGHT_BYTES / (e2e_ms / 1e3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,

@@ -24,6 +24,10 @@ OK, ERR_INVALID_ARG, ERR_SHAPE, ERR_UNSUPPORTED, ERR_ALIGN, ERR_WORKSPACE, ERR_C
     0, -1, -2, -3, -4, -5, -6, -7
 
 
+FLAG_QUANTIZE_X = 1 << 16
+FLAG_PDL = 1 << 17
+
+
 def FMT(wtype: int, atype: int) -> int:
     return int(wtype) | (int(atype) << 8)
 

@@ -20,16 +20,18 @@
 #include "runtime.cuh"
 
 // Launchers defined in the kernel translation units.
-int qmv_launch_quantize(int atype, const float* x, void* xq, int64_t n, cudaStream_t st);
+int qmv_launch_quantize(int atype, const float* x, void* xq, int64_t n, bool pdl, cudaStream_t st);
 int qmv_launch_dequant(int t, const void* W, int64_t rows, int64_t cols, float* out, cudaStream_t st);
 int qmv_launch_block_dots(int t, const void* W, int64_t rows, int64_t cols, const void* xq, int n_vec,
                           int32_t* out, cudaStream_t st);
-int qmv_gemv_q4_0(bool, const void*, int64_t, int64_t, const void*, float*, int, cudaStream_t);
-int qmv_gemv_q5_0(bool, const void*, int64_t, int64_t, const void*, float*, int, cudaStream_t);
-int qmv_gemv_q8_0(bool, const void*, int64_t, int64_t, const void*, float*, int, cudaStream_t);
-int qmv_gemv_mxfp4(bool, const void*, int64_t, int64_t, const void*, float*, int, cudaStream_t);
-int qmv_gemv_q4_k(bool, const void*, int64_t, int64_t, const void*, float*, int, cudaStream_t);
-int qmv_gemv_q6_k(bool, const void*, int64_t, int64_t, const void*, float*, int, cudaStream_t);
+#define QMV_GEMV_DECL(NAME) \
+    int NAME(bool a8, bool quant_x, bool pdl, const void*, int64_t, int64_t, const void*, float*, int, cudaStream_t);
+QMV_GEMV_DECL(qmv_gemv_q4_0)
+QMV_GEMV_DECL(qmv_gemv_q5_0)
+QMV_GEMV_DECL(qmv_gemv_q8_0)
+QMV_GEMV_DECL(qmv_gemv_mxfp4)
+QMV_GEMV_DECL(qmv_gemv_q4_k)
+QMV_GEMV_DECL(qmv_gemv_q6_k)
 
 // The device status word: kernels OR fault bits into it (QMV_DEV_*).
 __device__ unsigned g_qmv_status;
@@ -193,6 +195,9 @@ size_t qmv_row_bytes(int type, int64_t cols)
 
 int qmv_quantize_act(int fmt, const float* x, void* xq, int64_t n, void* stream)
 {
+    const bool pdl = (fmt & QMV_FLAG_PDL) != 0;
+    if (fmt & ~(0xffff | QMV_FLAG_PDL)) return fail(QMV_ERR_INVALID_ARG, "unknown flags 0x%x", fmt & ~0xffff);
+    fmt &= 0xffff;
     if (fmt != QMV_Q8_0 && fmt != QMV_Q8_K)
         return fail(QMV_ERR_UNSUPPORTED, "activation format %d (%s) is not supported; supported: Q8_0, Q8_K", fmt,
                     type_name(fmt));
@@ -204,7 +209,7 @@ int qmv_quantize_act(int fmt, const float* x, void* xq, int64_t n, void* stream)
     if (!x || !xq) return fail(QMV_ERR_INVALID_ARG, "x and xq must not be NULL");
     if (!aligned(x, fmt == QMV_Q8_K ? 16 : 4)) return fail(QMV_ERR_ALIGN, "x must be %d-byte aligned", fmt == QMV_Q8_K ? 16 : 4);
     if (!aligned(xq, fmt == QMV_Q8_K ? 4 : 2)) return fail(QMV_ERR_ALIGN, "xq must be %d-byte aligned", fmt == QMV_Q8_K ? 4 : 2);
-    if (qmv_launch_quantize(fmt, x, xq, n, static_cast<cudaStream_t>(stream))) return cuda_fail("qmv_quantize_act");
+    if (qmv_launch_quantize(fmt, x, xq, n, pdl, static_cast<cudaStream_t>(stream))) return cuda_fail("qmv_quantize_act");
     return ok();
 }
 
@@ -233,29 +238,35 @@ int qmv_block_dots(int type, const void* W, int64_t rows, int64_t cols, const vo
 
 int qmv_matvec(int fmt, const void* W, int64_t rows, int64_t cols, const void* x, float* y, int n_vec, void* stream)
 {
+    if (fmt & ~(0xffff | QMV_FLAG_QUANTIZE_X | QMV_FLAG_PDL))
+        return fail(QMV_ERR_INVALID_ARG, "unknown flags 0x%x", fmt & ~0xffff);
+    const bool quant_x = (fmt & QMV_FLAG_QUANTIZE_X) != 0, pdl = (fmt & QMV_FLAG_PDL) != 0;
     const int wtype = fmt & 0xff, atype = (fmt >> 8) & 0xff;
-    int rc = check_weights(wtype, W, rows, cols);
-    if (rc) return rc;
-    if (atype != QMV_F32 && atype != paired_act(wtype))
+    if (atype != QMV_F32 && atype != paired_act(wtype) && is_weight_type(wtype))
         return fail(QMV_ERR_UNSUPPORTED,
                     "%s weights take F32 or %s activations in qmv_matvec (got %s); 32-element formats pair with "
                     "Q8_0, K-quants with Q8_K",
                     type_name(wtype), type_name(paired_act(wtype)), type_name(atype));
+    int rc = check_weights(wtype, W, rows, cols);
+    if (rc) return rc;
+    if (quant_x && atype == QMV_F32)
+        return fail(QMV_ERR_INVALID_ARG, "QMV_FLAG_QUANTIZE_X needs an 8-bit activation type (Q8_0 or Q8_K)");
     if (n_vec < 0 || n_vec > 64) return fail(QMV_ERR_INVALID_ARG, "n_vec must be in 0..64 (got %d)", n_vec);
     if (rows == 0 || n_vec == 0) return ok();
     if (!x || !y) return fail(QMV_ERR_INVALID_ARG, "x and y must not be NULL");
     const bool a8 = atype != QMV_F32;
-    if (!aligned(x, a8 ? 4 : 16)) return fail(QMV_ERR_ALIGN, "x must be %d-byte aligned", a8 ? 4 : 16);
+    const int xal = (a8 && !quant_x) ? 4 : 16;
+    if (!aligned(x, xal)) return fail(QMV_ERR_ALIGN, "x must be %d-byte aligned", xal);
     if (!aligned(y, 4)) return fail(QMV_ERR_ALIGN, "y must be 4-byte aligned");
     if (!qmv::status_word()) return cuda_fail("qmv_matvec (status word)");
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (wtype) {
-    case QMV_Q4_0: rc = qmv_gemv_q4_0(a8, W, rows, cols, x, y, n_vec, st); break;
-    case QMV_Q5_0: rc = qmv_gemv_q5_0(a8, W, rows, cols, x, y, n_vec, st); break;
-    case QMV_Q8_0: rc = qmv_gemv_q8_0(a8, W, rows, cols, x, y, n_vec, st); break;
-    case QMV_MXFP4: rc = qmv_gemv_mxfp4(a8, W, rows, cols, x, y, n_vec, st); break;
-    case QMV_Q4_K: rc = qmv_gemv_q4_k(a8, W, rows, cols, x, y, n_vec, st); break;
-    case QMV_Q6_K: rc = qmv_gemv_q6_k(a8, W, rows, cols, x, y, n_vec, st); break;
+    case QMV_Q4_0: rc = qmv_gemv_q4_0(a8, quant_x, pdl, W, rows, cols, x, y, n_vec, st); break;
+    case QMV_Q5_0: rc = qmv_gemv_q5_0(a8, quant_x, pdl, W, rows, cols, x, y, n_vec, st); break;
+    case QMV_Q8_0: rc = qmv_gemv_q8_0(a8, quant_x, pdl, W, rows, cols, x, y, n_vec, st); break;
+    case QMV_MXFP4: rc = qmv_gemv_mxfp4(a8, quant_x, pdl, W, rows, cols, x, y, n_vec, st); break;
+    case QMV_Q4_K: rc = qmv_gemv_q4_k(a8, quant_x, pdl, W, rows, cols, x, y, n_vec, st); break;
+    case QMV_Q6_K: rc = qmv_gemv_q6_k(a8, quant_x, pdl, W, rows, cols, x, y, n_vec, st); break;
     }
     if (rc == -2) return fail(QMV_ERR_SHAPE, "cols = %lld needs more shared memory than one SM has", (long long)cols);
     if (rc) return cuda_fail("qmv_matvec");

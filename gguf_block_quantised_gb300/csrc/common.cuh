@@ -157,6 +157,30 @@ __device__ __forceinline__ float ubyte_to_float_minus(uint32_t w, int k, float t
     return __int_as_float(static_cast<int>(__byte_perm(w, 0x4B000000u, 0x7650u + k))) - two23_plus_off;
 }
 
+// ---- the 8-bit activation quantiser step (shared by the quantise kernels and
+// the matvec kernels that quantise their activations while staging them) ----
+// d = amax/127 and id = 1/d (0 when d = 0), each one IEEE fp32 rounding.
+__device__ __forceinline__ void act_scale(float amax, float& d, float& id)
+{
+    d = __fdiv_rn(amax, 127.f);
+    id = d == 0.f ? 0.f : __fdiv_rn(1.f, d);
+}
+// q = round-half-away-from-zero(v * id), clamped to +-127.
+__device__ __forceinline__ int8_t quant1(float v, float id)
+{
+    float r = roundf(__fmul_rn(v, id));
+    r = fminf(fmaxf(r, -127.f), 127.f);
+    return (int8_t)(int)r;
+}
+
+// ---- programmatic dependent launch ----------------------------------------------
+// Wait until the grids this one depends on have finished and their writes are
+// visible (a no-op when the kernel was not launched as a dependent).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the next grid on the stream be scheduled (its own pdl_wait still waits
+// for this grid to finish).
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ float warp_sum(float v)
 {
 #pragma unroll

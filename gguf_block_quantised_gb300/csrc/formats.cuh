@@ -484,17 +484,66 @@ __device__ __forceinline__ XView carve_xview(uint8_t* base, bool a8, int g, int 
     return X;
 }
 
-// Stage g vectors of activations, starting at global vector v0, with all
-// threads of the block.  x points at the caller's activations: fp32
-// [n][cols] (A32) or Q8_0/Q8_K blocks [n][nb] (A8).  Ends with __syncthreads.
+// Stage g vectors of activations with all threads of the block.  x points at
+// the caller's activations: fp32 [g][cols] (A32, or A8 with quant_x) or
+// Q8_0/Q8_K blocks [g][nb] (A8).  With quant_x the fp32 activations are
+// quantised here with the exact steps of the activation quantiser, so the
+// staged bytes equal those staged from qmv_quantize_act's output.  Ends with
+// __syncthreads.
 template <int T>
-__device__ void stage_xhat(uint8_t* base, bool a8, const void* x, int g, int cols)
+__device__ void stage_xhat(uint8_t* base, bool a8, bool quant_x, const void* x, int g, int cols)
 {
     constexpr int bs = Fmt<T>::BS;
     const int nb = cols / bs;
     auto r16 = [](size_t v) { return (v + 15) & ~size_t(15); };
     const int tid = threadIdx.x, nth = blockDim.x;
-    if (a8) {
+    if (a8 && quant_x) {
+        uint8_t* codes = base;
+        float* d = reinterpret_cast<float*>(base + r16((size_t)g * cols));
+        uint8_t* tail = base + r16((size_t)g * cols) + r16((size_t)g * nb * 4);
+        const float4* src = static_cast<const float4*>(x);
+        for (int i = tid; i < g * nb; i += nth) {       // one activation block per thread
+            const float4* xp = src + (size_t)i * (bs / 4);
+            float amax = 0.f;
+            for (int k = 0; k < bs / 4; ++k) {
+                const float4 v = xp[k];
+                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+            }
+            float dd, id;
+            act_scale(amax, dd, id);
+            uint8_t* dst = codes + (size_t)i * bs;
+            if constexpr (bs == 32) {
+                int s = 0;
+                for (int k = 0; k < 8; ++k) {
+                    const float4 v = xp[k];
+                    const int8_t q0 = quant1(v.x, id), q1 = quant1(v.y, id), q2 = quant1(v.z, id), q3 = quant1(v.w, id);
+                    dst[staged_pos<T>(4 * k + 0)] = (uint8_t)q0;
+                    dst[staged_pos<T>(4 * k + 1)] = (uint8_t)q1;
+                    dst[staged_pos<T>(4 * k + 2)] = (uint8_t)q2;
+                    dst[staged_pos<T>(4 * k + 3)] = (uint8_t)q3;
+                    s += q0 + q1 + q2 + q3;
+                }
+                d[i] = __half2float(__float2half_rn(dd));   // Q8_0 keeps its scale in fp16
+                reinterpret_cast<int*>(tail)[i] = s;
+            } else {
+                int16_t* bsum = reinterpret_cast<int16_t*>(tail) + (size_t)i * 16;
+                for (int r = 0; r < 16; ++r) {
+                    int s = 0;
+                    for (int k = 0; k < 4; ++k) {
+                        const float4 v = xp[4 * r + k];
+                        const int8_t q0 = quant1(v.x, id), q1 = quant1(v.y, id), q2 = quant1(v.z, id),
+                                     q3 = quant1(v.w, id);
+                        reinterpret_cast<uint32_t*>(dst)[4 * r + k] =
+                            (uint32_t)(uint8_t)q0 | ((uint32_t)(uint8_t)q1 << 8) | ((uint32_t)(uint8_t)q2 << 16) |
+                            ((uint32_t)(uint8_t)q3 << 24);
+                        s += q0 + q1 + q2 + q3;
+                    }
+                    bsum[r] = (int16_t)s;
+                }
+                d[i] = dd;
+            }
+        }
+    } else if (a8) {
         uint8_t* codes = base;
         float* d = reinterpret_cast<float*>(base + r16((size_t)g * cols));
         uint8_t* tail = base + r16((size_t)g * cols) + r16((size_t)g * nb * 4);

@@ -16,6 +16,21 @@ inline int act_block_bytes(int wtype)
     return (wtype == QMV_Q4_K || wtype == QMV_Q6_K) ? 292 : 34;
 }
 
+// Rows a consumer warp decodes at once: fewer as the vector count (and with
+// it the accumulator count RIF x NV) grows.
+template <int T, int NV>
+constexpr int rows_in_flight()
+{
+    return Fmt<T>::BS == 32 ? (NV <= 2 ? 4 : 2) : (NV <= 4 ? 2 : 1);
+}
+
+inline int rows_in_flight_rt(int T, int nv)
+{
+    const bool b32 = !(T == QMV_Q4_K || T == QMV_Q6_K);
+    const int NV = nv <= 1 ? 1 : nv <= 2 ? 2 : nv <= 4 ? 4 : nv <= 8 ? 8 : 16;
+    return b32 ? (NV <= 2 ? 4 : 2) : (NV <= 4 ? 2 : 1);
+}
+
 template <int T>
 inline bool plan_gemv(bool a8, int64_t rows, int64_t cols, int n_vec, GemvPlan& pl)
 {
@@ -30,53 +45,77 @@ inline bool plan_gemv(bool a8, int64_t rows, int64_t cols, int n_vec, GemvPlan& 
     }
     pl.n_chunks = (nb + pl.kb - 1) / pl.kb;
     pl.seg_cap = (uint32_t)(((size_t)pl.kb * F::BB + 48 + 15) & ~size_t(15));
-    const size_t stage = (size_t)pl.seg_cap * kGemvRows;
+    // Largest vector group whose staged activations fit next to at least two
+    // stages (three when two CTAs share an SM); then fewer rows per warp.
     int g = n_vec < 16 ? n_vec : 16;
     if (g < 1) g = 1;
-    while (g > 1 && xhat_bytes(T, a8, g, (int)cols) > kXhatMaxBytes) --g;
-    pl.group = g;
-    pl.xhat_bytes = (uint32_t)xhat_bytes(T, a8, g, (int)cols);
-    const size_t base = 128 + ((pl.xhat_bytes + 127) & ~size_t(127));
-    int S = base < kSmemTwoPerSm ? (int)((kSmemTwoPerSm - base) / stage) : 0;
-    if (S < 3) S = base < kSmemOnePerSm ? (int)((kSmemOnePerSm - base) / stage) : 0;
-    if (S < 2) return false;
-    if (S > kMaxStages) S = kMaxStages;
-    pl.stages = S;
-    pl.smem = (uint32_t)(base + S * stage);
-    return true;
+    for (;;) {
+        // Accumulators stay in registers across K-chunks only for one row
+        // group, so a multi-chunk row gives each warp as many rows as this
+        // group's kernel decodes at once (smaller groups decode at least as many).
+        const int rif = rows_in_flight_rt(T, g);
+        for (int rpw = pl.n_chunks > 1 ? rif : 4; rpw >= 1; rpw /= 2) {
+            if (pl.n_chunks > 1 && rpw != rif) break;
+            const size_t xb = xhat_bytes(T, a8, g, (int)cols);
+            if (xb > kXhatMaxBytes && g > 1) break;
+            const size_t stage = (size_t)pl.seg_cap * kConsumerWarps * rpw;
+            const size_t base = 256 + ((xb + 127) & ~size_t(127));
+            int S = base < kSmemTwoPerSm ? (int)((kSmemTwoPerSm - base) / stage) : 0;
+            if (S < 3) S = base < kSmemOnePerSm ? (int)((kSmemOnePerSm - base) / stage) : 0;
+            if (S >= 2) {
+                if (S > kMaxStages) S = kMaxStages;
+                pl.group = g;
+                pl.rpw = rpw;
+                pl.xhat_bytes = (uint32_t)xb;
+                pl.stages = S;
+                pl.smem = (uint32_t)(base + S * stage);
+                return true;
+            }
+        }
+        if (g == 1) return false;
+        --g;
+    }
+
 }
 
 template <int T, bool A8, int NV>
-inline int launch_gemv_nv(const GemvParams& p, const GemvPlan& pl, cudaStream_t st)
+inline int launch_gemv_nv(GemvParams p, const GemvPlan& pl, bool pdl, cudaStream_t st)
 {
-    auto* k = &k_gemv<T, A8, NV>;
+    auto* k = &k_gemv<T, A8, NV, rows_in_flight<T, NV>()>;
     const int occ = prepare_kernel(k, kGemvThreads, pl.smem);
-    const int64_t n_tiles = (p.rows + kGemvRows - 1) / kGemvRows;
+    const int64_t tr = kConsumerWarps * pl.rpw;
+    const int64_t n_tiles = (p.rows + tr - 1) / tr;
     int64_t grid = (int64_t)num_sms() * occ;
     if (grid > n_tiles) grid = n_tiles;
-    k<<<(unsigned)grid, kGemvThreads, pl.smem, st>>>(p);
-    return cudaGetLastError() == cudaSuccess ? 0 : -6;
+    return launch_ex(k, dim3((unsigned)grid), dim3(kGemvThreads), pl.smem, st, pdl, p) == cudaSuccess ? 0 : -6;
 }
 
 template <int T, bool A8>
-inline int launch_gemv_group(const GemvParams& p, const GemvPlan& pl, cudaStream_t st)
+inline int launch_gemv_group(const GemvParams& p, const GemvPlan& pl, bool pdl, cudaStream_t st)
 {
-    if (p.nv <= 1) return launch_gemv_nv<T, A8, 1>(p, pl, st);
-    if (p.nv <= 2) return launch_gemv_nv<T, A8, 2>(p, pl, st);
-    if (p.nv <= 4) return launch_gemv_nv<T, A8, 4>(p, pl, st);
-    if (p.nv <= 8) return launch_gemv_nv<T, A8, 8>(p, pl, st);
-    return launch_gemv_nv<T, A8, 16>(p, pl, st);
+    if (p.nv <= 1) return launch_gemv_nv<T, A8, 1>(p, pl, pdl, st);
+    if (p.nv <= 2) return launch_gemv_nv<T, A8, 2>(p, pl, pdl, st);
+    if (p.nv <= 4) return launch_gemv_nv<T, A8, 4>(p, pl, pdl, st);
+    if (p.nv <= 8) return launch_gemv_nv<T, A8, 8>(p, pl, pdl, st);
+    return launch_gemv_nv<T, A8, 16>(p, pl, pdl, st);
 }
 
 // Returns 0, -2 (shape beyond the shared-memory plan) or -6 (launch failure).
+// quant_x: A8 from fp32 activations quantised in the kernel.  pdl: launch as a
+// programmatic dependent of the previous kernel on the stream.
 template <int T>
-inline int launch_gemv_t(bool a8, const void* W, int64_t rows, int64_t cols, const void* x, float* y, int n_vec,
-                         cudaStream_t st)
+inline int launch_gemv_t(bool a8, bool quant_x, bool pdl, const void* W, int64_t rows, int64_t cols, const void* x,
+                         float* y, int n_vec, cudaStream_t st)
 {
     using F = Fmt<T>;
     if (rows == 0 || n_vec == 0) return 0;
     GemvPlan pl;
     if (!plan_gemv<T>(a8, rows, cols, n_vec, pl)) return -2;
+    // Small matrices: shorter tiles so that more SMs take part (the tile shape
+    // does not enter the arithmetic of any output).
+    if (pl.n_chunks == 1)
+        while (pl.rpw > 1 && (rows + kConsumerWarps * pl.rpw - 1) / (kConsumerWarps * pl.rpw) < 2 * num_sms())
+            pl.rpw /= 2;
     GemvParams p{};
     p.W = static_cast<const uint8_t*>(W);
     p.rows = rows;
@@ -88,14 +127,16 @@ inline int launch_gemv_t(bool a8, const void* W, int64_t rows, int64_t cols, con
     p.n_chunks = pl.n_chunks;
     p.stages = pl.stages;
     p.seg_cap = pl.seg_cap;
+    p.rpw = pl.rpw;
+    p.quant_x = quant_x ? 1 : 0;
     p.xhat_bytes = pl.xhat_bytes;
     p.status = status_word();
-    const size_t xrow = a8 ? (size_t)p.nb * act_block_bytes(T) : (size_t)cols * 4;
+    const size_t xrow = (a8 && !quant_x) ? (size_t)p.nb * act_block_bytes(T) : (size_t)cols * 4;
     for (int v0 = 0; v0 < n_vec; v0 += pl.group) {
         p.nv = min(pl.group, n_vec - v0);
         p.x = static_cast<const uint8_t*>(x) + (size_t)v0 * xrow;
         p.y = y + (int64_t)v0 * rows;
-        const int rc = a8 ? launch_gemv_group<T, true>(p, pl, st) : launch_gemv_group<T, false>(p, pl, st);
+        const int rc = a8 ? launch_gemv_group<T, true>(p, pl, pdl, st) : launch_gemv_group<T, false>(p, pl, pdl, st);
         if (rc) return rc;
     }
     return 0;
@@ -104,8 +145,8 @@ inline int launch_gemv_t(bool a8, const void* W, int64_t rows, int64_t cols, con
 }  // namespace qmv
 
 #define QMV_GEMV_INSTANTIATE(T, NAME)                                                                     \
-    int NAME(bool a8, const void* W, int64_t rows, int64_t cols, const void* x, float* y, int n_vec,      \
-             cudaStream_t st)                                                                              \
+    int NAME(bool a8, bool quant_x, bool pdl, const void* W, int64_t rows, int64_t cols, const void* x,   \
+             float* y, int n_vec, cudaStream_t st)                                                         \
     {                                                                                                      \
-        return qmv::launch_gemv_t<T>(a8, W, rows, cols, x, y, n_vec, st);                                  \
+        return qmv::launch_gemv_t<T>(a8, quant_x, pdl, W, rows, cols, x, y, n_vec, st);                    \
     }

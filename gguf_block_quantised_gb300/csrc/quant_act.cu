@@ -14,23 +14,18 @@
 
 namespace qmv {
 
-__device__ __forceinline__ int8_t quant1(float v, float id)
-{
-    float r = roundf(__fmul_rn(v, id));
-    r = fminf(fmaxf(r, -127.f), 127.f);
-    return (int8_t)(int)r;
-}
-
 // Q8_0: lane i owns element i of the block.
 __global__ void k_quant_q8_0(const float* __restrict__ x, uint8_t* __restrict__ out, int64_t nblk)
 {
     const int lane = threadIdx.x & 31;
     const int64_t b = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    pdl_trigger();
+    pdl_wait();
     if (b >= nblk) return;
     const float v = x[b * 32 + lane];
     const float amax = warp_max(fabsf(v));
-    const float d = __fdiv_rn(amax, 127.f);
-    const float id = d == 0.f ? 0.f : __fdiv_rn(1.f, d);
+    float d, id;
+    act_scale(amax, d, id);
     const int8_t q = quant1(v, id);
     uint8_t* o = out + b * 34;
     o[2 + lane] = (uint8_t)q;
@@ -42,6 +37,8 @@ __global__ void k_quant_q8_k(const float* __restrict__ x, uint8_t* __restrict__ 
 {
     const int lane = threadIdx.x & 31;
     const int64_t b = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    pdl_trigger();
+    pdl_wait();
     if (b >= nblk) return;
     const float4* xp = reinterpret_cast<const float4*>(x + b * 256 + lane * 8);
     const float4 a = xp[0], c = xp[1];
@@ -50,8 +47,8 @@ __global__ void k_quant_q8_k(const float* __restrict__ x, uint8_t* __restrict__ 
 #pragma unroll
     for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(v[k]));
     const float amax = warp_max(m);
-    const float d = __fdiv_rn(amax, 127.f);
-    const float id = d == 0.f ? 0.f : __fdiv_rn(1.f, d);
+    float d, id;
+    act_scale(amax, d, id);
     uint32_t w0 = 0, w1 = 0;
     int s = 0;
 #pragma unroll
@@ -72,17 +69,24 @@ __global__ void k_quant_q8_k(const float* __restrict__ x, uint8_t* __restrict__ 
 
 }  // namespace qmv
 
-int qmv_launch_quantize(int atype, const float* x, void* xq, int64_t n, cudaStream_t st)
+int qmv_launch_quantize(int atype, const float* x, void* xq, int64_t n, bool pdl, cudaStream_t st)
 {
     using namespace qmv;
     const int bs = atype == QMV_Q8_0 ? 32 : 256;
     const int64_t nblk = n / bs;
     if (nblk == 0) return 0;
     const int warps = 8;
-    const int64_t grid = (nblk + warps - 1) / warps;
-    if (atype == QMV_Q8_0)
-        k_quant_q8_0<<<(unsigned)grid, warps * 32, 0, st>>>(x, static_cast<uint8_t*>(xq), nblk);
-    else
-        k_quant_q8_k<<<(unsigned)grid, warps * 32, 0, st>>>(x, static_cast<uint8_t*>(xq), nblk);
-    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)((nblk + warps - 1) / warps));
+    cfg.blockDim = dim3(warps * 32);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    uint8_t* out = static_cast<uint8_t*>(xq);
+    const cudaError_t e = atype == QMV_Q8_0 ? cudaLaunchKernelEx(&cfg, k_quant_q8_0, x, out, nblk)
+                                            : cudaLaunchKernelEx(&cfg, k_quant_q8_k, x, out, nblk);
+    return e == cudaSuccess ? 0 : -1;
 }

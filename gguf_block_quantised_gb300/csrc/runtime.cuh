@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <atomic>
 #include <mutex>
+#include <utility>
 
 namespace qmv {
 
@@ -53,13 +54,38 @@ inline int prepare_kernel(K* kernel, int threads, size_t bytes)
     for (int i = 0; i < n; ++i)
         if (cache[i].fn == fn && cache[i].dev == dev && cache[i].threads == threads && cache[i].bytes == bytes)
             return cache[i].occ;
-    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    // The limit is per kernel, not per launch: raise it to the device's opt-in
+    // maximum once, so launches of the same kernel with other sizes stay valid.
+    int max_optin = 0;
+    cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         max_optin > (int)bytes ? max_optin : (int)bytes);
+    // Prefer shared memory over L1 so that two ~100 KB blocks fit on one SM.
+    cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     int occ = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, threads, bytes) != cudaSuccess || occ < 1) occ = 1;
     Entry e{fn, dev, threads, bytes, occ};
     if (n < 64) cache[n++] = e;
     else cache[(reinterpret_cast<uintptr_t>(fn) >> 4) % 64] = e;
     return occ;
+}
+
+// Launch `kernel` with an optional programmatic-dependent-launch attribute.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             bool pdl, Args&&... args)
+{
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 }  // namespace qmv

@@ -70,6 +70,19 @@ typedef enum {
 /* A multiply's format is the weight type plus the activation type. */
 #define QMV_FMT(wtype, atype) ((int)(wtype) | ((int)(atype) << 8))
 
+/* Flags OR-ed into fmt.
+ * QMV_FLAG_QUANTIZE_X: qmv_matvec with an 8-bit activation type (Q8_0/Q8_K)
+ *   takes x as fp32 [n_vec][cols] (16-byte aligned) and quantises it inside the
+ *   kernel, with results bit-identical to qmv_quantize_act followed by
+ *   qmv_matvec (one launch instead of two).
+ * QMV_FLAG_PDL: launch as a programmatic dependent of the kernel before it on
+ *   the stream.  The kernel may start streaming W before that kernel has
+ *   finished; it still waits for it before reading x or writing y.  Only for
+ *   weights that the immediately preceding kernels do not write.  Accepted by
+ *   qmv_quantize_act and qmv_matvec. */
+#define QMV_FLAG_QUANTIZE_X (1 << 16)
+#define QMV_FLAG_PDL (1 << 17)
+
 typedef enum {
     QMV_OK = 0,
     QMV_ERR_INVALID_ARG = -1,   /* null pointer, negative size                              */
@@ -100,7 +113,7 @@ size_t qmv_row_bytes(int type, int64_t cols);
  * "Architecture" page, "The package map", pkg/quant).
  *   fmt : QMV_Q8_0 (32-element blocks, fp16 scale, 34 B) or
  *         QMV_Q8_K (256-element blocks, fp32 scale, int16 sums of each run of
- *         16 codes, 292 B).
+ *         16 codes, 292 B), optionally | QMV_FLAG_PDL.
  *   x   : n fp32 values, 4-byte aligned; several vectors may be laid end to end
  *         as long as each vector's length is a multiple of the block length.
  *   xq  : n/bs blocks out.
@@ -140,7 +153,8 @@ int qmv_block_dots(int type, const void* W, int64_t rows, int64_t cols,
  * vectors sharing one pass over the weights ("The package map", pkg/tensor
  * MatVec; "A request, end to end": N sequences read the weights once).
  *   fmt : QMV_FMT(wtype, atype), wtype in {Q4_0, Q5_0, Q8_0, MXFP4} with atype
- *         in {F32, Q8_0}, or wtype in {Q4_K, Q6_K} with atype in {F32, Q8_K}.
+ *         in {F32, Q8_0}, or wtype in {Q4_K, Q6_K} with atype in {F32, Q8_K};
+ *         optionally | QMV_FLAG_QUANTIZE_X (8-bit atype only) | QMV_FLAG_PDL.
  *   x   : F32: fp32 [n_vec][cols], 16-byte aligned, xhat = x.
  *         Q8_0/Q8_K: [n_vec][cols/bs] blocks from qmv_quantize_act,
  *         4-byte aligned, xhat = d_x*q (the W4A8 product: integer dot per

@@ -184,3 +184,47 @@ def test_config_shapes_sampled(qmv, orc, cfg):
             yref, yabs = orc.matvec(t, at, W, rows, cols, xin, n_vec, row_ids=ids)
             assert_close(host(y)[:, ids], yref, yabs, what=f"{cfg} a8={a8} n_vec={n_vec}")
     qmv.qmv_get_status()
+
+
+@pytest.mark.parametrize("t", ALLW)
+def test_quantize_x_flag_bit_identical(qmv, orc, t):
+    """QMV_FLAG_QUANTIZE_X (quantise fp32 activations inside the matvec) gives
+    the same bits as qmv_quantize_act followed by qmv_matvec."""
+    at = act_for(t)
+    for rows, cols in shapes_for(t)[1:]:
+        n_vec = 5
+        W = dev(synth.weights(t, rows, cols, seed=6))
+        x = synth.activations(n_vec, cols, seed=6)
+        x[1, :64] = 0.0
+        xd = dev(x)
+        xq = torch.empty(n_vec * qmv.qmv_row_bytes(at, cols), dtype=torch.uint8, device="cuda")
+        qmv.qmv_quantize_act(at, xd, xq, n_vec * cols)
+        y1 = torch.empty((n_vec, rows), dtype=torch.float32, device="cuda")
+        y2 = torch.empty((n_vec, rows), dtype=torch.float32, device="cuda")
+        qmv.qmv_matvec(qmv.FMT(t, at), W, rows, cols, xq, y1, n_vec)
+        qmv.qmv_matvec(qmv.FMT(t, at) | qmv.FLAG_QUANTIZE_X, W, rows, cols, xd, y2, n_vec)
+        assert np.array_equal(host(y1).view(np.uint32), host(y2).view(np.uint32)), (t, rows, cols)
+
+
+def test_pdl_flag_same_results(qmv, orc):
+    """Programmatic dependent launch changes scheduling only: a chain of
+    dependent quantise + matvec launches gives the same bits with and without
+    it, including when each matvec reads the previous one's output."""
+    t, at, n = 2, 3, 896
+    Ws = [dev(synth.weights(t, n, n, seed=10 + i)) for i in range(6)]
+    x0 = dev(synth.activations(1, n, seed=10))
+
+    def chain(flags):
+        x = x0.clone()
+        for W in Ws:
+            y = torch.empty((1, n), dtype=torch.float32, device="cuda")
+            xq = torch.empty(qmv.qmv_row_bytes(at, n), dtype=torch.uint8, device="cuda")
+            qmv.qmv_quantize_act(at | flags, x, xq, n)
+            qmv.qmv_matvec(qmv.FMT(t, at) | flags, W, n, n, xq, y, 1)
+            x = y * 0.05
+        return host(x)
+
+    a = chain(0)
+    b = chain(qmv.FLAG_PDL)
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    qmv.qmv_get_status()
