@@ -32,6 +32,8 @@ QMV_GEMV_DECL(qmv_gemv_q8_0)
 QMV_GEMV_DECL(qmv_gemv_mxfp4)
 QMV_GEMV_DECL(qmv_gemv_q4_k)
 QMV_GEMV_DECL(qmv_gemv_q6_k)
+int qmv_launch_gemm_q4k_bf16(const void* W, int64_t rows, int64_t cols, const void* X, float* Y, int64_t m, bool pdl,
+                             cudaStream_t st);
 
 // The device status word: kernels OR fault bits into it (QMV_DEV_*).
 __device__ unsigned g_qmv_status;
@@ -275,9 +277,27 @@ int qmv_matvec(int fmt, const void* W, int64_t rows, int64_t cols, const void* x
 
 int qmv_matmul(int fmt, const void* W, int64_t rows, int64_t cols, const void* X, float* Y, int64_t m, void* stream)
 {
-    (void)W; (void)rows; (void)cols; (void)X; (void)Y; (void)m; (void)stream;
-    return fail(QMV_ERR_UNSUPPORTED, "qmv_matmul: format 0x%x is not supported; supported: QMV_FMT(Q4_K, BF16), "
-                                     "QMV_FMT(Q4_K, Q8_K)", fmt);
+    if (fmt & ~(0xffff | QMV_FLAG_PDL)) return fail(QMV_ERR_INVALID_ARG, "unknown flags 0x%x", fmt & ~0xffff);
+    const bool pdl = (fmt & QMV_FLAG_PDL) != 0;
+    const int wtype = fmt & 0xff, atype = (fmt >> 8) & 0xff;
+    if (wtype != QMV_Q4_K || atype != QMV_BF16)
+        return fail(QMV_ERR_UNSUPPORTED,
+                    "qmv_matmul: %s weights with %s activations are not provided; supported: QMV_FMT(Q4_K, BF16) "
+                    "(other formats: qmv_matvec with n_vec <= 64)",
+                    type_name(wtype), type_name(atype));
+    int rc = check_weights(wtype, W, rows, cols);
+    if (rc) return rc;
+    if (m < 0) return fail(QMV_ERR_INVALID_ARG, "m must be >= 0");
+    if (m > (int64_t)1 << 30 || rows > (int64_t)1 << 30) return fail(QMV_ERR_SHAPE, "m and rows must be below 2^30");
+    if (rows == 0 || m == 0) return ok();
+    if (!X || !Y) return fail(QMV_ERR_INVALID_ARG, "X and Y must not be NULL");
+    if (!aligned(X, 16)) return fail(QMV_ERR_ALIGN, "X must be 16-byte aligned");
+    if (!aligned(Y, 4)) return fail(QMV_ERR_ALIGN, "Y must be 4-byte aligned");
+    if (!qmv::status_word()) return cuda_fail("qmv_matmul (status word)");
+    rc = qmv_launch_gemm_q4k_bf16(W, rows, cols, X, Y, m, pdl, static_cast<cudaStream_t>(stream));
+    if (rc == -8) return fail(QMV_ERR_CUDA, "qmv_matmul: could not build a TMA tensor map");
+    if (rc) return cuda_fail("qmv_matmul");
+    return ok();
 }
 
 int qmv_moe_matvec(int fmt, const void* W3d, int n_expert, int64_t rows, int64_t cols, const int32_t* ids,

@@ -1,0 +1,331 @@
+// gemm_q4k.cu -- prefill GEMM with Q4_K weights on the 5th-generation tensor
+// cores (tcgen05, sm_103a).
+//
+// "Architecture" page, "The package map": pkg/tensor MatMul is the prefill
+// multiply; "The two phases": prefill is bound by arithmetic, so it runs on
+// the tensor cores.  Y[m][r] = sum_k X[m][k] * bf16(w[r][k]): the Q4_K weights
+// are dequantised to bf16 tiles in shared memory (w = d*sc*q - dmin*m in fp32,
+// one rounding, then rounded to bf16) and multiplied with bf16 activations,
+// accumulating in fp32.
+//
+// One persistent CTA per SM, 12 warps, warp-specialised:
+//   warp 0      TMA producer of activation tiles X[256 tokens][64 k] (bf16,
+//               128-byte swizzle, the UMMA K-major canonical layout)
+//   warp 1      TMEM owner (alloc/free) and the single-thread MMA issuer
+//   warp 2      TMA producer of raw Q4_K super-block tiles W[128 rows][144 B]
+//   warps 4-7   dequantisers: raw super-block -> four bf16 A tiles
+//               [128 rows][64 k] written in the 128-byte swizzled layout
+//   warps 8-11  epilogue: TMEM -> registers -> Y, one 128-byte row segment
+//               per column, so every store is coalesced
+// MMA: M = 128 weight rows, N = 256 tokens, K = 16 per instruction, fp32
+// accumulator in TMEM, double-buffered (2 x 256 columns) so the epilogue of
+// one tile overlaps the MMAs of the next.  Every mbarrier wait is bounded;
+// on a timeout the kernel flags the status word, unwinds and frees its TMEM.
+#include <cuda.h>
+
+#include "formats.cuh"
+#include "runtime.cuh"
+#include "tc.cuh"
+
+namespace qmv {
+
+namespace gq {
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int SX = 4, SA = 3, SR = 2;
+constexpr int X_BYTES = BN * BK * 2;    // 32768
+constexpr int A_BYTES = BM * BK * 2;    // 16384
+constexpr int R_BYTES = BM * 144;       // 18432
+constexpr int OFF_X = 0;
+constexpr int OFF_A = OFF_X + SX * X_BYTES;
+constexpr int OFF_R = OFF_A + SA * A_BYTES;
+constexpr int OFF_BAR = OFF_R + SR * R_BYTES;
+constexpr int N_BARS = 2 * SX + 2 * SR + 2 * SA + 4;
+constexpr int SMEM = OFF_BAR + N_BARS * 8 + 16 + 1024;   // + alignment slack
+constexpr int THREADS = 384;
+constexpr uint32_t TMEM_COLS = 512;
+}  // namespace gq
+
+struct GemmArgs {
+    int64_t rows;      // weight rows (outputs per token)
+    int cols;          // K
+    int m;             // tokens
+    float* Y;          // [m][rows]
+    unsigned* status;
+};
+
+// Dequantise sub-blocks 2c, 2c+1 of the raw super-block tile into a bf16 A
+// tile (128 rows x 64 k, K-major, 128-byte swizzle).  128 threads; thread t
+// handles rows r = t and 8-k groups jj = 0..3 of both sub-blocks.
+__device__ __forceinline__ void dequant_q4k_tile(const uint8_t* raw, uint8_t* A, int c, int t)
+{
+    const int r = t;
+    const uint8_t* rp = raw + r * 144;
+    const uint4 h = *reinterpret_cast<const uint4*>(rp);
+    int sc0, m0, sc1, m1;
+    Fmt<QMV_Q4_K>::scale_min(h.y, h.z, h.w, 2 * c, sc0, m0);
+    Fmt<QMV_Q4_K>::scale_min(h.y, h.z, h.w, 2 * c + 1, sc1, m1);
+    const float d = half_bits_to_float(h.x & 0xffffu), dmin = half_bits_to_float(h.x >> 16);
+    const float D0 = d * (float)sc0, M0 = dmin * (float)m0;   // exact
+    const float D1 = d * (float)sc1, M1 = dmin * (float)m1;
+    uint8_t* rowA = A + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+        const uint2 q = *reinterpret_cast<const uint2*>(rp + 16 + 32 * c + 8 * jj);
+        const uint32_t qw[2] = {q.x, q.y};
+        uint32_t lo[4], hi[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t w = qw[k >> 1];
+            const int sh = (k & 1) * 16;
+            // bytes 2k', 2k'+1 of the 8: low nibbles -> sub-block 2c, high -> 2c+1
+            const uint32_t b0 = (w >> sh) & 0xffu, b1 = (w >> (sh + 8)) & 0xffu;
+            const float l0 = __int_as_float(0x4B000000 | (b0 & 15u)) - 8388608.f;
+            const float l1 = __int_as_float(0x4B000000 | (b1 & 15u)) - 8388608.f;
+            const float g0 = __int_as_float(0x4B000000 | (b0 >> 4)) - 8388608.f;
+            const float g1 = __int_as_float(0x4B000000 | (b1 >> 4)) - 8388608.f;
+            const __nv_bfloat162 pl = __floats2bfloat162_rn(__fmaf_rn(D0, l0, -M0), __fmaf_rn(D0, l1, -M0));
+            const __nv_bfloat162 ph = __floats2bfloat162_rn(__fmaf_rn(D1, g0, -M1), __fmaf_rn(D1, g1, -M1));
+            lo[k] = *reinterpret_cast<const uint32_t*>(&pl);
+            hi[k] = *reinterpret_cast<const uint32_t*>(&ph);
+        }
+        const int jl = jj, jh = 4 + jj;   // 16-byte chunks of the 128-byte row
+        *reinterpret_cast<uint4*>(rowA + ((jl ^ (r & 7)) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        *reinterpret_cast<uint4*>(rowA + ((jh ^ (r & 7)) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    }
+}
+
+__global__ void __launch_bounds__(gq::THREADS, 1)
+    k_gemm_q4k_bf16(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, const GemmArgs a)
+{
+    using namespace gq;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+    uint64_t* xf = bars;
+    uint64_t* xe = xf + SX;
+    uint64_t* rf = xe + SX;
+    uint64_t* re = rf + SR;
+    uint64_t* af = re + SR;
+    uint64_t* ae = af + SA;
+    uint64_t* accf = ae + SA;
+    uint64_t* acce = accf + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 2);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n_rt = (int)((a.rows + BM - 1) / BM);
+    const int n_nt = (a.m + BN - 1) / BN;
+    const int n_tiles = n_rt * n_nt;
+    const int nk = a.cols / BK;
+    const int nsb = a.cols / 256;
+
+    if (tid == 0) {
+        for (int i = 0; i < SX; ++i) { mbar_init(&xf[i], 1); mbar_init(&xe[i], 1); }
+        for (int i = 0; i < SR; ++i) { mbar_init(&rf[i], 1); mbar_init(&re[i], 4); }
+        for (int i = 0; i < SA; ++i) { mbar_init(&af[i], 4); mbar_init(&ae[i], 1); }
+        for (int i = 0; i < 2; ++i) { mbar_init(&accf[i], 1); mbar_init(&acce[i], 4); }
+        *abort_flag = 0;
+        fence_barrier_init();
+        prefetch_tmap(&tmX);
+        prefetch_tmap(&tmW);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    pdl_trigger();
+    pdl_wait();
+
+    auto fail = [&]() { *abort_flag = 1; };
+
+    if (warp == 0) {
+        // ---- activation tiles
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 1;
+            for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x) {
+                const int nt = t / n_rt;
+                for (int kk = 0; kk < nk; ++kk) {
+                    if (!mbar_wait_bounded(&xe[s], ph, a.status)) { fail(); break; }
+                    mbar_arrive_expect_tx(&xf[s], X_BYTES);
+                    tma_load_2d(smem + OFF_X + s * X_BYTES, &tmX, kk * BK, nt * BN, &xf[s]);
+                    if (++s == SX) { s = 0; ph ^= 1; }
+                }
+            }
+        }
+    } else if (warp == 2) {
+        // ---- raw weight super-block tiles
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 1;
+            for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x) {
+                const int rt = t % n_rt;
+                for (int sb = 0; sb < nsb; ++sb) {
+                    if (!mbar_wait_bounded(&re[s], ph, a.status)) { fail(); break; }
+                    mbar_arrive_expect_tx(&rf[s], R_BYTES);
+                    tma_load_2d(smem + OFF_R + s * R_BYTES, &tmW, sb * 144, rt * BM, &rf[s]);
+                    if (++s == SR) { s = 0; ph ^= 1; }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16(BM, BN);
+            int sx = 0, sa = 0;
+            uint32_t pxf = 0, paf = 0;
+            int local = 0;
+            for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x, ++local) {
+                const int buf = local & 1;
+                const uint32_t use = (uint32_t)(local >> 1);
+                if (!mbar_wait_bounded(&acce[buf], (use & 1) ^ 1, a.status)) { fail(); break; }
+                tc_fence_after();
+                const uint32_t d = tmem + buf * BN;
+                bool bad = false;
+                for (int kk = 0; kk < nk; ++kk) {
+                    if (!mbar_wait_bounded(&af[sa], paf, a.status) || !mbar_wait_bounded(&xf[sx], pxf, a.status)) {
+                        bad = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t adesc = smem_desc_sw128(smem + OFF_A + sa * A_BYTES);
+                    const uint64_t bdesc = smem_desc_sw128(smem + OFF_X + sx * X_BYTES);
+#pragma unroll
+                    for (int k4 = 0; k4 < BK / 16; ++k4)   // 32 bytes per K = 16 step, inside the swizzle atom
+                        mma_f16(d, adesc + 2 * k4, bdesc + 2 * k4, idesc, (kk | k4) != 0);
+                    mma_commit(&ae[sa]);
+                    mma_commit(&xe[sx]);
+                    if (++sa == SA) { sa = 0; paf ^= 1; }
+                    if (++sx == SX) { sx = 0; pxf ^= 1; }
+                }
+                if (bad) { fail(); break; }
+                mma_commit(&accf[buf]);
+            }
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ---- dequantisers
+        const int t0 = tid - 128;
+        int sr = 0, sa = 0;
+        uint32_t prf = 0, pae = 1;
+        for (int t = blockIdx.x; t < n_tiles && !__any_sync(0xffffffffu, *abort_flag); t += gridDim.x) {
+            bool bad = false;
+            for (int sb = 0; sb < nsb && !bad; ++sb) {
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&rf[sr], prf, a.status))) { bad = true; break; }
+                const uint8_t* raw = smem + OFF_R + sr * R_BYTES;
+                for (int c = 0; c < 4; ++c) {
+                    if (!__all_sync(0xffffffffu, mbar_wait_bounded(&ae[sa], pae, a.status))) { bad = true; break; }
+                    dequant_q4k_tile(raw, smem + OFF_A + sa * A_BYTES, c, t0);
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // make the tile visible to the MMA
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&af[sa]);
+                    if (++sa == SA) { sa = 0; pae ^= 1; }
+                }
+                if (bad) break;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&re[sr]);
+                if (++sr == SR) { sr = 0; prf ^= 1; }
+            }
+            if (bad) { fail(); break; }
+        }
+    } else if (warp >= 8) {
+        // ---- epilogue: lane quarter (warp % 4) of the 128 TMEM lanes
+        const int q = warp & 3;
+        int local = 0;
+        for (int t = blockIdx.x; t < n_tiles && !__any_sync(0xffffffffu, *abort_flag); t += gridDim.x, ++local) {
+            const int rt = t % n_rt, nt = t / n_rt;
+            const int buf = local & 1;
+            const uint32_t use = (uint32_t)(local >> 1);
+            // warp-uniform: every lane must take part in the tcgen05.ld below
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&accf[buf], use & 1, a.status))) { fail(); break; }
+            tc_fence_after();
+            const int64_t row = (int64_t)rt * BM + 32 * q + lane;
+            const bool row_ok = row < a.rows;
+            for (int c16 = 0; c16 < BN / 16; ++c16) {
+                float v[16];
+                tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + buf * BN + c16 * 16, v);
+                const int tok0 = nt * BN + c16 * 16;
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    if (row_ok && tok0 + i < a.m) a.Y[(int64_t)(tok0 + i) * a.rows + row] = v[i];
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acce[buf]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// ---- host --------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D tensor map: dims {inner, outer} elements, row pitch in bytes.
+bool make_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                  uint64_t pitch, uint32_t box_in, uint32_t box_out, CUtensorMapSwizzle sw)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {pitch};
+    const cuuint32_t box[2] = {box_in, box_out};
+    const cuuint32_t es[2] = {1, 1};
+    return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace qmv
+
+// Returns 0, -6 (launch failure) or -8 (tensor map could not be built).
+int qmv_launch_gemm_q4k_bf16(const void* W, int64_t rows, int64_t cols, const void* X, float* Y, int64_t m,
+                             bool pdl, cudaStream_t st)
+{
+    using namespace qmv;
+    if (rows == 0 || m == 0) return 0;
+    const uint64_t rb = (uint64_t)(cols / 256) * 144;
+    CUtensorMap tmX, tmW;
+    if (!make_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, (uint64_t)cols, (uint64_t)m, (uint64_t)cols * 2,
+                      gq::BK, gq::BN, CU_TENSOR_MAP_SWIZZLE_128B))
+        return -8;
+    if (!make_tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, rb, (uint64_t)rows, rb, 144, gq::BM,
+                      CU_TENSOR_MAP_SWIZZLE_NONE))
+        return -8;
+    GemmArgs a;
+    a.rows = rows;
+    a.cols = (int)cols;
+    a.m = (int)m;
+    a.Y = Y;
+    a.status = status_word();
+    auto* k = &k_gemm_q4k_bf16;
+    prepare_kernel(k, gq::THREADS, gq::SMEM);
+    const int64_t n_tiles = ((rows + gq::BM - 1) / gq::BM) * ((m + gq::BN - 1) / gq::BN);
+    const int grid = (int)std::min<int64_t>(n_tiles, num_sms());
+    return launch_ex(k, dim3(grid), dim3(gq::THREADS), gq::SMEM, st, pdl, tmX, tmW, a) == cudaSuccess ? 0 : -6;
+}

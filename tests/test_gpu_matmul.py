@@ -1,0 +1,95 @@
+"""GPU parity of the prefill GEMM (Q4_K weights, bf16 activations, tcgen05)
+against the CPU oracle, which multiplies bf16(w) by the bf16 activations in
+fp64.  Bar: |Y - Y_oracle| <= 1e-4 * sum|bf16(w) x| for every output checked.
+Invariant: prefill equals row-by-row decode ("Architecture" page, "The forward
+pass") within the bf16 rounding of the weights."""
+import numpy as np
+import pytest
+import torch
+
+from gguf_block_quantised_gb300 import synth
+from gpu_util import assert_close, dev, host
+
+pytestmark = pytest.mark.gpu
+
+Q4_K, F32, BF16 = 4, 8, 9
+
+
+def bf16_x(m, cols, seed):
+    x = synth.activations(m, cols, seed=seed, tensor_id=m + cols)
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    return xb, xb.view(torch.int16).numpy()
+
+
+def run_matmul(qmv, Wd, rows, cols, xb, m):
+    Y = torch.full((m, rows), float("nan"), dtype=torch.float32, device="cuda")
+    qmv.qmv_matmul(qmv.FMT(Q4_K, BF16), Wd, rows, cols, xb.cuda(), Y, m)
+    return host(Y)
+
+
+@pytest.mark.parametrize("rows,cols,m", [(128, 256, 256), (300, 512, 1), (256, 1024, 100), (130, 768, 300),
+                                         (512, 2048, 513)])
+def test_matmul_bf16_parity(qmv, orc, rows, cols, m):
+    """Small shapes covering ragged row tiles (130, 300), ragged token tiles
+    (1, 100, 300, 513) and several super-blocks per row; every output checked."""
+    W = synth.weights(Q4_K, rows, cols, seed=7, tensor_id=rows)
+    xb, xbits = bf16_x(m, cols, 7)
+    Y = run_matmul(qmv, dev(W), rows, cols, xb, m)
+    yref, yabs = orc.matvec(Q4_K, BF16, W, rows, cols, xbits, m)
+    assert_close(Y, yref, yabs, what=f"{rows}x{cols} m={m}")
+    qmv.qmv_get_status()
+
+
+@pytest.mark.parametrize("rows,cols,m", [(14336, 4096, 512), (4096, 14336, 512), (14336, 4096, 2048),
+                                         (4096, 14336, 2048)])
+def test_matmul_config_shapes_sampled(qmv, orc, rows, cols, m):
+    """The prefill configuration's shapes at full size; the oracle checks 40
+    sampled rows for 64 sampled tokens (first and last of each included)."""
+    W = synth.weights(Q4_K, rows, cols, seed=3, tensor_id=rows * 3 + cols)
+    xb, xbits = bf16_x(m, cols, 3)
+    Y = run_matmul(qmv, dev(W), rows, cols, xb, m)
+    assert np.isfinite(Y).all()
+    g = np.random.default_rng(rows + m)
+    rids = np.unique(np.concatenate([[0, rows - 1], g.integers(0, rows, 38)]))
+    toks = np.unique(np.concatenate([[0, m - 1], g.integers(0, m, 62)]))
+    yref, yabs = orc.matvec(Q4_K, BF16, W, rows, cols, xbits[toks], len(toks), row_ids=rids)
+    assert_close(Y[np.ix_(toks, rids)], yref, yabs, what=f"{rows}x{cols} m={m}")
+    qmv.qmv_get_status()
+
+
+def test_matmul_equals_rowwise_decode(qmv, orc):
+    """Prefill vs sequential decode of the same bf16 token values: the GEMM
+    multiplies bf16-rounded weights, the A32 matvec exact ones, so they may
+    differ by at most the weight rounding, 2^-9 * sum|w x| (plus fp32 noise)."""
+    rows, cols, m = 512, 2048, 64
+    W = synth.weights(Q4_K, rows, cols, seed=11)
+    Wd = dev(W)
+    xb, _ = bf16_x(m, cols, 11)
+    Y = run_matmul(qmv, Wd, rows, cols, xb, m)
+    xf = xb.float().cuda()
+    yv = torch.empty((m, rows), dtype=torch.float32, device="cuda")
+    for t in range(m):   # one token at a time, as decode runs
+        qmv.qmv_matvec(qmv.FMT(Q4_K, F32), Wd, rows, cols, xf[t], yv[t], 1)
+    yv = host(yv)
+    _, yabs = orc.matvec(Q4_K, F32, W, rows, cols, xf.cpu().numpy(), m)
+    assert (np.abs(Y - yv) <= (2.0 ** -9 + 2e-6) * yabs).all()
+
+
+def test_matmul_edge_cases(qmv, orc):
+    rows, cols = 128, 256
+    W = dev(synth.weights(Q4_K, rows, cols, seed=1))
+    # m = 0 and rows = 0 do nothing
+    Y = torch.full((1, rows), 5.0, device="cuda")
+    qmv.qmv_matmul(qmv.FMT(Q4_K, BF16), W, rows, cols, torch.zeros((1, cols), dtype=torch.bfloat16, device="cuda"), Y, 0)
+    qmv.qmv_matmul(qmv.FMT(Q4_K, BF16), W, 0, cols, torch.zeros((1, cols), dtype=torch.bfloat16, device="cuda"), Y, 1)
+    assert (host(Y) == 5).all()
+    # zero activations give exact zeros
+    assert (run_matmul(qmv, W, rows, cols, torch.zeros((3, cols), dtype=torch.bfloat16), 3) == 0).all()
+    # unsupported pairs and shapes are refused before any launch
+    with pytest.raises(qmv.QmvError) as e:
+        qmv.qmv_matmul(qmv.FMT(2, BF16), W, rows, cols, W, Y, 1)
+    assert e.value.code == qmv.ERR_UNSUPPORTED
+    with pytest.raises(qmv.QmvError) as e:
+        qmv.qmv_matmul(qmv.FMT(Q4_K, BF16), W, rows, 300, W, Y, 1)
+    assert e.value.code == qmv.ERR_SHAPE
+    qmv.qmv_get_status()
