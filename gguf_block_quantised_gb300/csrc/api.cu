@@ -32,6 +32,10 @@ QMV_GEMV_DECL(qmv_gemv_q8_0)
 QMV_GEMV_DECL(qmv_gemv_mxfp4)
 QMV_GEMV_DECL(qmv_gemv_q4_k)
 QMV_GEMV_DECL(qmv_gemv_q6_k)
+size_t qmv_moe_workspace_bytes(int64_t rows, int64_t n_pairs);
+int qmv_launch_moe(int wtype, bool a8, bool quant_x, size_t act_block_bytes, const void* W3d, int n_expert,
+                   int64_t rows, int64_t cols, const int32_t* ids, const float* gates, int k, const void* x, float* y,
+                   int64_t n_tok, const float* bias, void* ws, cudaStream_t st);
 int qmv_launch_gemm_q4k_bf16(const void* W, int64_t rows, int64_t cols, const void* X, float* Y, int64_t m, bool pdl,
                              cudaStream_t st);
 
@@ -303,14 +307,54 @@ int qmv_matmul(int fmt, const void* W, int64_t rows, int64_t cols, const void* X
 int qmv_moe_matvec(int fmt, const void* W3d, int n_expert, int64_t rows, int64_t cols, const int32_t* ids,
                    const float* gates, int k, const void* x, float* y, int64_t n_tok, const float* bias, void* stream)
 {
-    (void)W3d; (void)n_expert; (void)rows; (void)cols; (void)ids; (void)gates; (void)k; (void)x; (void)y;
-    (void)n_tok; (void)bias; (void)stream;
-    return fail(QMV_ERR_UNSUPPORTED, "qmv_moe_matvec: format 0x%x is not supported yet", fmt);
+    if (fmt & ~(0xffff | QMV_FLAG_QUANTIZE_X)) return fail(QMV_ERR_INVALID_ARG, "unknown flags 0x%x", fmt & ~0xffff);
+    const bool quant_x = (fmt & QMV_FLAG_QUANTIZE_X) != 0;
+    const int wtype = fmt & 0xff, atype = (fmt >> 8) & 0xff;
+    if (is_weight_type(wtype) && atype != QMV_F32 && atype != paired_act(wtype))
+        return fail(QMV_ERR_UNSUPPORTED,
+                    "qmv_moe_matvec: %s experts take F32 or %s activations (got %s)", type_name(wtype),
+                    type_name(paired_act(wtype)), type_name(atype));
+    int rc = check_weights(wtype, W3d, rows, cols);
+    if (rc) return rc;
+    if (quant_x && atype == QMV_F32)
+        return fail(QMV_ERR_INVALID_ARG, "QMV_FLAG_QUANTIZE_X needs an 8-bit activation type (Q8_0 or Q8_K)");
+    if (n_expert < 1 || n_expert > 1024) return fail(QMV_ERR_INVALID_ARG, "n_expert must be in 1..1024 (got %d)", n_expert);
+    if (k < 1 || k > 64) return fail(QMV_ERR_INVALID_ARG, "k must be in 1..64 (got %d)", k);
+    if (n_tok < 0 || n_tok * k > (int64_t)1 << 24)
+        return fail(QMV_ERR_INVALID_ARG, "n_tok must be >= 0 with n_tok*k <= 16777216");
+    if (n_tok == 0 || rows == 0) return ok();
+    if (!ids || !x || !y) return fail(QMV_ERR_INVALID_ARG, "ids, x and y must not be NULL");
+    const bool a8 = atype != QMV_F32;
+    const int xal = (a8 && !quant_x) ? 4 : 16;
+    if (!aligned(x, xal)) return fail(QMV_ERR_ALIGN, "x must be %d-byte aligned", xal);
+    if (!aligned(ids, 4) || !aligned(y, 4) || (gates && !aligned(gates, 4)) || (bias && !aligned(bias, 4)))
+        return fail(QMV_ERR_ALIGN, "ids, gates, bias and y must be 4-byte aligned");
+    const size_t need = qmv_moe_workspace_bytes(rows, n_tok * k);
+    const int d = qmv::current_device();
+    void* ws = nullptr;
+    size_t have = 0;
+    if (d >= 0 && d < qmv::kMaxDevices) {
+        std::lock_guard<std::mutex> lock(g_ws_mu);
+        ws = g_ws[d].ptr;
+        have = g_ws[d].bytes;
+    }
+    if (!ws || have < need)
+        return fail(QMV_ERR_WORKSPACE,
+                    "qmv_moe_matvec needs %zu bytes of workspace (qmv_workspace_size(QMV_OP_MOE, ...)); %zu set",
+                    need, have);
+    if (!qmv::status_word()) return cuda_fail("qmv_moe_matvec (status word)");
+    rc = qmv_launch_moe(wtype, a8, quant_x, qmv_block_bytes(paired_act(wtype)), W3d, n_expert, rows, cols, ids, gates,
+                        k, x, y, n_tok, bias, ws, static_cast<cudaStream_t>(stream));
+    if (rc == -2) return fail(QMV_ERR_SHAPE, "cols = %lld needs more shared memory than one SM has", (long long)cols);
+    if (rc) return cuda_fail("qmv_moe_matvec");
+    return ok();
 }
 
 size_t qmv_workspace_size(int op, int fmt, int64_t rows, int64_t cols, int64_t n)
 {
-    (void)op; (void)fmt; (void)rows; (void)cols; (void)n;
+    (void)fmt;
+    (void)cols;
+    if (op == QMV_OP_MOE && rows > 0 && n > 0) return qmv_moe_workspace_bytes(rows, n);
     return 0;
 }
 

@@ -484,30 +484,33 @@ __device__ __forceinline__ XView carve_xview(uint8_t* base, bool a8, int g, int 
     return X;
 }
 
-// Stage g vectors of activations with all threads of the block.  x points at
-// the caller's activations: fp32 [g][cols] (A32, or A8 with quant_x) or
-// Q8_0/Q8_K blocks [g][nb] (A8).  With quant_x the fp32 activations are
-// quantised here with the exact steps of the activation quantiser, so the
-// staged bytes equal those staged from qmv_quantize_act's output.  Ends with
-// __syncthreads.
+// Stage g activation vectors with threads tid = 0..nth-1 of the block (the
+// caller synchronises afterwards).  Vector v is row idx[v] (v when idx is
+// NULL) of the caller's activations, whose rows are xrow bytes apart: fp32
+// [cols] (A32, or A8 with quant_x) or Q8_0/Q8_K blocks [nb] (A8).  With
+// quant_x the fp32 activations are quantised here with the exact steps of the
+// activation quantiser, so the staged bytes equal those staged from
+// qmv_quantize_act's output.
 template <int T>
-__device__ void stage_xhat(uint8_t* base, bool a8, bool quant_x, const void* x, int g, int cols)
+__device__ void stage_xhat(uint8_t* base, bool a8, bool quant_x, const void* x, size_t xrow, const int* idx, int g,
+                           int cols, int tid, int nth)
 {
     constexpr int bs = Fmt<T>::BS;
     const int nb = cols / bs;
     auto r16 = [](size_t v) { return (v + 15) & ~size_t(15); };
-    const int tid = threadIdx.x, nth = blockDim.x;
+    const uint8_t* xb = static_cast<const uint8_t*>(x);
+    auto row = [&](int v) { return xb + (size_t)(idx ? idx[v] : v) * xrow; };
     if (a8 && quant_x) {
         uint8_t* codes = base;
         float* d = reinterpret_cast<float*>(base + r16((size_t)g * cols));
         uint8_t* tail = base + r16((size_t)g * cols) + r16((size_t)g * nb * 4);
-        const float4* src = static_cast<const float4*>(x);
         for (int i = tid; i < g * nb; i += nth) {       // one activation block per thread
-            const float4* xp = src + (size_t)i * (bs / 4);
+            const int v = i / nb, b = i % nb;
+            const float4* xp = reinterpret_cast<const float4*>(row(v)) + (size_t)b * (bs / 4);
             float amax = 0.f;
             for (int k = 0; k < bs / 4; ++k) {
-                const float4 v = xp[k];
-                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+                const float4 w = xp[k];
+                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(w.x), fabsf(w.y)), fmaxf(fabsf(w.z), fabsf(w.w))));
             }
             float dd, id;
             act_scale(amax, dd, id);
@@ -515,8 +518,8 @@ __device__ void stage_xhat(uint8_t* base, bool a8, bool quant_x, const void* x, 
             if constexpr (bs == 32) {
                 int s = 0;
                 for (int k = 0; k < 8; ++k) {
-                    const float4 v = xp[k];
-                    const int8_t q0 = quant1(v.x, id), q1 = quant1(v.y, id), q2 = quant1(v.z, id), q3 = quant1(v.w, id);
+                    const float4 w = xp[k];
+                    const int8_t q0 = quant1(w.x, id), q1 = quant1(w.y, id), q2 = quant1(w.z, id), q3 = quant1(w.w, id);
                     dst[staged_pos<T>(4 * k + 0)] = (uint8_t)q0;
                     dst[staged_pos<T>(4 * k + 1)] = (uint8_t)q1;
                     dst[staged_pos<T>(4 * k + 2)] = (uint8_t)q2;
@@ -530,9 +533,9 @@ __device__ void stage_xhat(uint8_t* base, bool a8, bool quant_x, const void* x, 
                 for (int r = 0; r < 16; ++r) {
                     int s = 0;
                     for (int k = 0; k < 4; ++k) {
-                        const float4 v = xp[4 * r + k];
-                        const int8_t q0 = quant1(v.x, id), q1 = quant1(v.y, id), q2 = quant1(v.z, id),
-                                     q3 = quant1(v.w, id);
+                        const float4 w = xp[4 * r + k];
+                        const int8_t q0 = quant1(w.x, id), q1 = quant1(w.y, id), q2 = quant1(w.z, id),
+                                     q3 = quant1(w.w, id);
                         reinterpret_cast<uint32_t*>(dst)[4 * r + k] =
                             (uint32_t)(uint8_t)q0 | ((uint32_t)(uint8_t)q1 << 8) | ((uint32_t)(uint8_t)q2 << 16) |
                             ((uint32_t)(uint8_t)q3 << 24);
@@ -550,10 +553,9 @@ __device__ void stage_xhat(uint8_t* base, bool a8, bool quant_x, const void* x, 
         if constexpr (bs == 32) {
             // Q8_0 blocks: fp16 d | int8[32], 34 bytes, 2-byte aligned.
             int* sum = reinterpret_cast<int*>(tail);
-            const uint8_t* src = static_cast<const uint8_t*>(x);
             for (int i = tid; i < g * nb; i += nth) {
-                const uint8_t* blk = src + (size_t)i * 34;
-                const uint16_t* h = reinterpret_cast<const uint16_t*>(blk);
+                const int v = i / nb, b = i % nb;
+                const uint16_t* h = reinterpret_cast<const uint16_t*>(row(v) + (size_t)b * 34);
                 uint8_t q[32];
                 int s = 0;
 #pragma unroll
@@ -572,10 +574,10 @@ __device__ void stage_xhat(uint8_t* base, bool a8, bool quant_x, const void* x, 
         } else {
             // Q8_K blocks: f32 d | int8[256] | int16 bsums[16], 292 bytes, 4-byte aligned.
             int16_t* bsum = reinterpret_cast<int16_t*>(tail);
-            const uint32_t* src = static_cast<const uint32_t*>(x);
             for (int i = tid; i < g * nb * 73; i += nth) {
                 const int blkno = i / 73, wd = i % 73;
-                const uint32_t val = src[i];
+                const int v = blkno / nb, b = blkno % nb;
+                const uint32_t val = reinterpret_cast<const uint32_t*>(row(v) + (size_t)b * 292)[wd];
                 if (wd == 0) d[blkno] = __uint_as_float(val);
                 else if (wd <= 64) reinterpret_cast<uint32_t*>(codes + (size_t)blkno * 256)[wd - 1] = val;
                 else reinterpret_cast<uint32_t*>(bsum + (size_t)blkno * 16)[wd - 65] = val;
@@ -583,31 +585,38 @@ __device__ void stage_xhat(uint8_t* base, bool a8, bool quant_x, const void* x, 
         }
     } else {
         float* xf = reinterpret_cast<float*>(base);
-        const float4* src = static_cast<const float4*>(x);
-        const int n4 = g * cols / 4;
-        for (int i = tid; i < n4; i += nth) {
-            const float4 v = src[i];
+        const int c4 = cols / 4;
+        for (int i = tid; i < g * c4; i += nth) {
+            const int v = i / c4, j = i % c4;
+            const float4 w = reinterpret_cast<const float4*>(row(v))[j];
             if constexpr (T == QMV_MXFP4) {
                 const int e = 4 * i, run = e & ~31;
-                xf[run + staged_pos<T>((e + 0) & 31)] = v.x;
-                xf[run + staged_pos<T>((e + 1) & 31)] = v.y;
-                xf[run + staged_pos<T>((e + 2) & 31)] = v.z;
-                xf[run + staged_pos<T>((e + 3) & 31)] = v.w;
+                xf[run + staged_pos<T>((e + 0) & 31)] = w.x;
+                xf[run + staged_pos<T>((e + 1) & 31)] = w.y;
+                xf[run + staged_pos<T>((e + 2) & 31)] = w.z;
+                xf[run + staged_pos<T>((e + 3) & 31)] = w.w;
             } else {
-                reinterpret_cast<float4*>(xf)[i] = v;
-            }
-        }
-        if constexpr (T == QMV_Q4_K) {
-            __syncthreads();
-            float* xs32 = reinterpret_cast<float*>(base + r16((size_t)g * cols * 4));
-            for (int i = tid; i < g * cols / 32; i += nth) {
-                float s = 0.f;
-                for (int k = 0; k < 32; ++k) s += xf[(size_t)i * 32 + k];
-                xs32[i] = s;
+                reinterpret_cast<float4*>(xf)[i] = w;
             }
         }
     }
-    __syncthreads();
+}
+
+// Per-32 sums of staged fp32 activations (A32 Q4_K), in a fixed order; run
+// after the staging is visible to these threads.
+template <int T>
+__device__ void stage_xsum32(uint8_t* base, int g, int cols, int tid, int nth)
+{
+    if constexpr (T == QMV_Q4_K) {
+        auto r16 = [](size_t v) { return (v + 15) & ~size_t(15); };
+        const float* xf = reinterpret_cast<const float*>(base);
+        float* xs32 = reinterpret_cast<float*>(base + r16((size_t)g * cols * 4));
+        for (int i = tid; i < g * cols / 32; i += nth) {
+            float s = 0.f;
+            for (int k = 0; k < 32; ++k) s += xf[(size_t)i * 32 + k];
+            xs32[i] = s;
+        }
+    }
 }
 
 }  // namespace qmv

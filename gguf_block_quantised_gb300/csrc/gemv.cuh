@@ -215,7 +215,15 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_gemv(const GemvParams p)
         }
     }
     pdl_wait();
-    stage_xhat<T>(xs, A8, p.quant_x != 0, p.x, p.nv, p.cols);   // ends with a barrier
+    {
+        const size_t xrow = (A8 && !p.quant_x) ? (size_t)p.nb * (F::BS == 32 ? 34 : 292) : (size_t)p.cols * 4;
+        stage_xhat<T>(xs, A8, p.quant_x != 0, p.x, xrow, nullptr, p.nv, p.cols, tid, kGemvThreads);
+        __syncthreads();
+        if (!A8) {
+            stage_xsum32<T>(xs, p.nv, p.cols, tid, kGemvThreads);
+            __syncthreads();
+        }
+    }
 
     if (producer) {
         int64_t tile = blockIdx.x + (int64_t)(S / p.n_chunks) * gridDim.x;

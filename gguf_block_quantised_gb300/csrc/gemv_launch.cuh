@@ -2,6 +2,7 @@
 #pragma once
 
 #include "gemv.cuh"
+#include "moe.cuh"
 #include "runtime.cuh"
 
 namespace qmv {
@@ -142,7 +143,87 @@ inline int launch_gemv_t(bool a8, bool quant_x, bool pdl, const void* W, int64_t
     return 0;
 }
 
+// ---- mixture of experts -----------------------------------------------------------
+template <int T, bool A8, int NV>
+inline int launch_moe_nv(const MoeParams& mp, const GemvPlan& pl, int n_expert, int active, cudaStream_t st)
+{
+    auto* k = &k_moe_gemv<T, A8, NV, rows_in_flight<T, NV>()>;
+    const size_t smem = pl.smem + 256;
+    const int occ = prepare_kernel(k, kGemvThreads, smem);
+    const int64_t tr = kConsumerWarps * pl.rpw;
+    const int64_t n_tiles = (mp.g.rows + tr - 1) / tr;
+    int64_t gx = ((int64_t)num_sms() * occ * 2 + active - 1) / active;
+    if (gx > n_tiles) gx = n_tiles;
+    if (gx < 1) gx = 1;
+    return launch_ex(k, dim3((unsigned)gx, (unsigned)n_expert), dim3(kGemvThreads), smem, st, false, mp) ==
+                   cudaSuccess
+               ? 0
+               : -6;
+}
+
+// Expert matvecs for grouped (token, slot) pairs.  x rows are xrow bytes
+// apart; pair p reads row p / kdiv and writes out[p*rows ..].
+template <int T>
+inline int launch_moe_t(bool a8, bool quant_x, const void* W3d, int n_expert, int64_t rows, int64_t cols,
+                        const int* offsets, const int* perm, int n_pairs, const void* x, size_t xrow, int kdiv,
+                        float* out, const float* bias, cudaStream_t st)
+{
+    using F = Fmt<T>;
+    if (rows == 0 || n_pairs == 0) return 0;
+    GemvPlan pl;
+    if (!plan_gemv<T>(a8, rows, cols, n_pairs < 16 ? n_pairs : 16, pl)) return -2;
+    if (pl.n_chunks == 1) pl.rpw = 1;   // many small tiles: an expert's rows spread over many SMs
+    MoeParams mp{};
+    GemvParams& p = mp.g;
+    p.W = static_cast<const uint8_t*>(W3d);
+    p.rows = rows;
+    p.nb = (int)(cols / F::BS);
+    p.rb = (int64_t)p.nb * F::BB;
+    p.total = rows * p.rb;
+    p.cols = (int)cols;
+    p.kb = pl.kb;
+    p.n_chunks = pl.n_chunks;
+    p.stages = pl.stages;
+    p.seg_cap = pl.seg_cap;
+    p.rpw = pl.rpw;
+    p.quant_x = quant_x ? 1 : 0;
+    p.xhat_bytes = pl.xhat_bytes;
+    p.status = status_word();
+    p.x = x;
+    mp.expert_bytes = p.total;
+    mp.offsets = offsets;
+    mp.perm = perm;
+    mp.xrow = xrow;
+    mp.kdiv = kdiv;
+    mp.out = out;
+    mp.bias = bias;
+    mp.group = pl.group;
+    const int active = n_pairs < n_expert ? n_pairs : n_expert;
+    const int g = pl.group;
+    if (a8) {
+        if (g <= 1) return launch_moe_nv<T, true, 1>(mp, pl, n_expert, active, st);
+        if (g <= 2) return launch_moe_nv<T, true, 2>(mp, pl, n_expert, active, st);
+        if (g <= 4) return launch_moe_nv<T, true, 4>(mp, pl, n_expert, active, st);
+        if (g <= 8) return launch_moe_nv<T, true, 8>(mp, pl, n_expert, active, st);
+        return launch_moe_nv<T, true, 16>(mp, pl, n_expert, active, st);
+    }
+    if (g <= 1) return launch_moe_nv<T, false, 1>(mp, pl, n_expert, active, st);
+    if (g <= 2) return launch_moe_nv<T, false, 2>(mp, pl, n_expert, active, st);
+    if (g <= 4) return launch_moe_nv<T, false, 4>(mp, pl, n_expert, active, st);
+    if (g <= 8) return launch_moe_nv<T, false, 8>(mp, pl, n_expert, active, st);
+    return launch_moe_nv<T, false, 16>(mp, pl, n_expert, active, st);
+}
+
 }  // namespace qmv
+
+#define QMV_MOE_INSTANTIATE(T, NAME)                                                                        \
+    int NAME(bool a8, bool quant_x, const void* W3d, int n_expert, int64_t rows, int64_t cols,                 \
+             const int* offsets, const int* perm, int n_pairs, const void* x, size_t xrow, int kdiv,            \
+             float* out, const float* bias, cudaStream_t st)                                                    \
+    {                                                                                                           \
+        return qmv::launch_moe_t<T>(a8, quant_x, W3d, n_expert, rows, cols, offsets, perm, n_pairs, x, xrow,   \
+                                    kdiv, out, bias, st);                                                       \
+    }
 
 #define QMV_GEMV_INSTANTIATE(T, NAME)                                                                     \
     int NAME(bool a8, bool quant_x, bool pdl, const void* W, int64_t rows, int64_t cols, const void* x,   \

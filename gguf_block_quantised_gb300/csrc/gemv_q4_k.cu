@@ -1,5 +1,6 @@
-// gemv_q4_k.cu -- decode matvec kernels for Q4_K weights (one translation unit
+// gemv_q4_k.cu -- decode matvec and expert matvec kernels for Q4_K weights (one translation unit
 // per format so the kernels compile in parallel).
 #include "gemv_launch.cuh"
 
 QMV_GEMV_INSTANTIATE(QMV_Q4_K, qmv_gemv_q4_k)
+QMV_MOE_INSTANTIATE(QMV_Q4_K, qmv_moe_q4_k)

@@ -1,5 +1,6 @@
-// gemv_q6_k.cu -- decode matvec kernels for Q6_K weights (one translation unit
+// gemv_q6_k.cu -- decode matvec and expert matvec kernels for Q6_K weights (one translation unit
 // per format so the kernels compile in parallel).
 #include "gemv_launch.cuh"
 
 QMV_GEMV_INSTANTIATE(QMV_Q6_K, qmv_gemv_q6_k)
+QMV_MOE_INSTANTIATE(QMV_Q6_K, qmv_moe_q6_k)

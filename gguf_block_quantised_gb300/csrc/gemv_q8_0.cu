@@ -1,5 +1,6 @@
-// gemv_q8_0.cu -- decode matvec kernels for Q8_0 weights (one translation unit
+// gemv_q8_0.cu -- decode matvec and expert matvec kernels for Q8_0 weights (one translation unit
 // per format so the kernels compile in parallel).
 #include "gemv_launch.cuh"
 
 QMV_GEMV_INSTANTIATE(QMV_Q8_0, qmv_gemv_q8_0)
+QMV_MOE_INSTANTIATE(QMV_Q8_0, qmv_moe_q8_0)

@@ -1,0 +1,142 @@
+// moe.cu -- grouping and combining for the mixture-of-experts matvec.
+//
+// "Models and formats" page, "Architectures": a router picks k of n experts
+// per token (here: the ids and gates are inputs), experts are stacked 3-D
+// tensors, and gpt-oss adds a bias on every expert projection.
+//
+//  k_moe_group    one block: validates the ids and sorts the n_tok*k (token,
+//                 slot) pairs by expert with a stable counting sort (one warp
+//                 per expert, ballots over the pairs in order), writing
+//                 offsets[n_expert+1] and perm[n_pairs] to the workspace.
+//  k_moe_gemv     (moe.cuh) the expert matvecs over grouped pairs.
+//  k_moe_combine  down form only: y[t][r] = sum over slots s, in slot order, of
+//                 gates[t][s] * (part[t*k+s][r] + bias[e][r]).
+// Nothing here uses atomics on data, so results are deterministic.
+#include "common.cuh"
+#include "runtime.cuh"
+
+namespace qmv {
+
+__global__ void __launch_bounds__(1024) k_moe_group(const int32_t* __restrict__ ids, int n_pairs, int n_expert,
+                                                    int* __restrict__ offsets, int* __restrict__ perm,
+                                                    unsigned* status)
+{
+    __shared__ int base[1025];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
+    pdl_wait();
+    for (int p = tid; p < n_pairs; p += blockDim.x) {
+        const int e = ids[p];
+        if (e < 0 || e >= n_expert) atomicOr(status, QMV_DEV_BAD_EXPERT);
+    }
+    for (int e = warp; e < n_expert; e += nw) {
+        int c = 0;
+        for (int b = 0; b < n_pairs; b += 32) {
+            const int p = b + lane;
+            c += __popc(__ballot_sync(0xffffffffu, p < n_pairs && ids[p] == e));
+        }
+        if (lane == 0) base[e] = c;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int run = 0;
+        for (int e = 0; e < n_expert; ++e) {
+            const int c = base[e];
+            base[e] = run;
+            offsets[e] = run;
+            run += c;
+        }
+        offsets[n_expert] = run;   // pairs with a valid expert
+    }
+    __syncthreads();
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int e = warp; e < n_expert; e += nw) {
+        int pos = base[e];
+        for (int b = 0; b < n_pairs; b += 32) {
+            const int p = b + lane;
+            const bool m = p < n_pairs && ids[p] == e;
+            const uint32_t mask = __ballot_sync(0xffffffffu, m);
+            if (m) perm[pos + __popc(mask & lt)] = p;
+            pos += __popc(mask);
+        }
+    }
+}
+
+__global__ void k_moe_combine(const float* __restrict__ part, const int32_t* __restrict__ ids,
+                              const float* __restrict__ gates, const float* __restrict__ bias, int k, int64_t rows,
+                              int64_t n_tok, int n_expert, float* __restrict__ y)
+{
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n_tok * rows) return;
+    const int64_t t = i / rows, r = i % rows;
+    float acc = 0.f;
+    for (int s = 0; s < k; ++s) {
+        const int64_t pr = t * k + s;
+        const int e = ids[pr];
+        if (e < 0 || e >= n_expert) continue;
+        float v = part[pr * rows + r];
+        if (bias) v += bias[(int64_t)e * rows + r];
+        acc = __fmaf_rn(gates[pr], v, acc);
+    }
+    y[i] = acc;
+}
+
+inline size_t r256(size_t v) { return (v + 255) & ~size_t(255); }
+
+}  // namespace qmv
+
+#define QMV_MOE_DECL(NAME)                                                                                      \
+    int NAME(bool a8, bool quant_x, const void* W3d, int n_expert, int64_t rows, int64_t cols, const int* offsets, \
+             const int* perm, int n_pairs, const void* x, size_t xrow, int kdiv, float* out, const float* bias,    \
+             cudaStream_t st);
+QMV_MOE_DECL(qmv_moe_q4_0)
+QMV_MOE_DECL(qmv_moe_q5_0)
+QMV_MOE_DECL(qmv_moe_q8_0)
+QMV_MOE_DECL(qmv_moe_mxfp4)
+QMV_MOE_DECL(qmv_moe_q4_k)
+QMV_MOE_DECL(qmv_moe_q6_k)
+
+size_t qmv_moe_workspace_bytes(int64_t rows, int64_t n_pairs)
+{
+    using qmv::r256;
+    return r256(1025 * 4) + r256((size_t)n_pairs * 4) + (size_t)n_pairs * (size_t)rows * 4;
+}
+
+// Returns 0, -2 (shape beyond the plan), -6 (launch failure).
+int qmv_launch_moe(int wtype, bool a8, bool quant_x, size_t act_block_bytes, const void* W3d, int n_expert,
+                   int64_t rows, int64_t cols, const int32_t* ids, const float* gates, int k, const void* x, float* y,
+                   int64_t n_tok, const float* bias, void* ws, cudaStream_t st)
+{
+    using namespace qmv;
+    const int64_t n_pairs = n_tok * k;
+    if (n_pairs == 0 || rows == 0) return 0;
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    int* offsets = reinterpret_cast<int*>(w);
+    int* perm = reinterpret_cast<int*>(w + r256(1025 * 4));
+    float* part = reinterpret_cast<float*>(w + r256(1025 * 4) + r256((size_t)n_pairs * 4));
+    k_moe_group<<<1, 1024, 0, st>>>(ids, (int)n_pairs, n_expert, offsets, perm, status_word());
+    if (cudaGetLastError() != cudaSuccess) return -6;
+    const size_t xrow = (a8 && !quant_x) ? (size_t)(cols / (wtype == QMV_Q4_K || wtype == QMV_Q6_K ? 256 : 32)) *
+                                               act_block_bytes
+                                         : (size_t)cols * 4;
+    const int kdiv = gates ? 1 : k;
+    float* out = gates ? part : y;
+    const float* b = gates ? nullptr : bias;
+    int rc = -3;
+#define QMV_MOE_CALL(NAME) NAME(a8, quant_x, W3d, n_expert, rows, cols, offsets, perm, (int)n_pairs, x, xrow, kdiv, out, b, st)
+    switch (wtype) {
+    case QMV_Q4_0: rc = QMV_MOE_CALL(qmv_moe_q4_0); break;
+    case QMV_Q5_0: rc = QMV_MOE_CALL(qmv_moe_q5_0); break;
+    case QMV_Q8_0: rc = QMV_MOE_CALL(qmv_moe_q8_0); break;
+    case QMV_MXFP4: rc = QMV_MOE_CALL(qmv_moe_mxfp4); break;
+    case QMV_Q4_K: rc = QMV_MOE_CALL(qmv_moe_q4_k); break;
+    case QMV_Q6_K: rc = QMV_MOE_CALL(qmv_moe_q6_k); break;
+    }
+#undef QMV_MOE_CALL
+    if (rc) return rc;
+    if (gates) {
+        const int64_t n = n_tok * rows;
+        k_moe_combine<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(part, ids, gates, bias, k, rows, n_tok, n_expert, y);
+        if (cudaGetLastError() != cudaSuccess) return -6;
+    }
+    return 0;
+}

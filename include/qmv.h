@@ -198,10 +198,14 @@ int qmv_matmul(int fmt, const void* W, int64_t rows, int64_t cols,
  *                   y[t][r] = sum_s gates[t][s] * ((W[ids[t][s]] x_{t,s})[r] + bias),
  *                   summed in slot order.
  *   bias  : fp32 [n_expert][rows], or NULL for none.
- *   fmt   : QMV_FMT(wtype, atype) with the pairs of qmv_matvec (activations
- *           F32 or 8-bit blocks, one block row per input vector), or
- *           atype = BF16 (x bf16) for weight types whose values are exact in
- *           bf16 (MXFP4, Q4_0, Q5_0).
+ *   fmt   : QMV_FMT(wtype, atype) with the pairs of qmv_matvec: activations
+ *           F32 (fp32 rows, 16-byte aligned) or the paired 8-bit blocks (one
+ *           block row per input vector, 4-byte aligned), optionally
+ *           | QMV_FLAG_QUANTIZE_X (fp32 rows quantised inside the kernel).
+ *   n_expert in 1..1024, k in 1..64, n_tok*k <= 2^24.
+ *   Results per (token, slot) are those of qmv_matvec on that expert's
+ *   matrix (same arithmetic and reduction order), plus the bias; the down
+ *   form's gate-weighted sum runs in fp32 in slot order.
  *   Workspace: qmv_workspace_size(QMV_OP_MOE, ...) bytes set by
  *           qmv_set_workspace(); calls that share the workspace must be
  *           ordered on one stream.
@@ -213,7 +217,8 @@ int qmv_moe_matvec(int fmt, const void* W3d, int n_expert, int64_t rows, int64_t
 
 /* Workspace for the calls that need scratch. */
 enum { QMV_OP_MATVEC = 1, QMV_OP_MATMUL = 2, QMV_OP_MOE = 3 };
-/* Bytes of workspace `op` needs for these sizes (n = n_tok*k for MoE).  0 if none. */
+/* Bytes of workspace `op` needs for these sizes (n = n_tok*k for MoE: the
+ * grouping, 1025 + n ints, and n*rows fp32 slot outputs).  0 if none. */
 size_t qmv_workspace_size(int op, int fmt, int64_t rows, int64_t cols, int64_t n);
 /* Register a caller-owned device buffer (256-byte aligned) as the workspace of
  * the current device; NULL/0 clears it.  The library keeps the pointer only. */

@@ -1,0 +1,153 @@
+"""GPU parity of the mixture-of-experts matvec against the CPU oracle.
+
+Bar (per output): |y - y_oracle| <= 1e-4 * sum_s g_s (sum|w*xhat| + |b|)
+(gates taken as 1 in the up form)."""
+import numpy as np
+import pytest
+import torch
+
+from gguf_block_quantised_gb300 import synth
+from gpu_util import assert_close, dev, host
+
+pytestmark = pytest.mark.gpu
+
+MXFP4, Q8_0, F32, Q4_K, Q8_K = 6, 3, 8, 4, 7
+
+
+@pytest.fixture(scope="module")
+def workspace(qmv):
+    buf = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")   # 256 MB
+    qmv.qmv_set_workspace(buf, buf.numel())
+    yield buf
+    qmv.qmv_set_workspace(None, 0)
+
+
+def moe_inputs(t, E, rows, cols, n_tok, k, seed):
+    W3 = synth.weights(t, E * rows, cols, seed=seed, tensor_id=1)
+    ids, gates = synth.router(n_tok, E, k, seed=seed)
+    b = synth.bias(E, rows, seed=seed)
+    return W3, ids, gates, b
+
+
+def run_moe(qmv, fmt, W3d, E, rows, cols, ids, gates, k, x, n_tok, bias):
+    shape = (n_tok, k, rows) if gates is None else (n_tok, rows)
+    y = torch.full(shape, float("nan"), dtype=torch.float32, device="cuda")
+    qmv.qmv_moe_matvec(fmt, W3d, E, rows, cols, dev(ids), None if gates is None else dev(gates), k, x, y, n_tok,
+                       None if bias is None else dev(bias))
+    return host(y)
+
+
+@pytest.mark.parametrize("t", [MXFP4, Q4_K])
+@pytest.mark.parametrize("mode", ["A32", "A8", "A8q"])
+def test_moe_small_parity(qmv, orc, workspace, t, mode):
+    E, rows, k, n_tok = 6, 48, 3, 9
+    cols = 256 if t == Q4_K else 128
+    at = {"A32": F32, "A8": Q8_0 if t == MXFP4 else Q8_K, "A8q": Q8_0 if t == MXFP4 else Q8_K}[mode]
+    flags = qmv.FLAG_QUANTIZE_X if mode == "A8q" else 0
+    W3, ids, gates, b = moe_inputs(t, E, rows, cols, n_tok, k, 5)
+    W3d = dev(W3)
+    # up form: x shared by the slots of a token
+    x = synth.activations(n_tok, cols, seed=5)
+    xin_o = orc.quantize_act(at, x) if at != F32 else x
+    xin_g = dev(x) if (at == F32 or flags) else dev(xin_o)
+    y = run_moe(qmv, qmv.FMT(t, at) | flags, W3d, E, rows, cols, ids, None, k, xin_g, n_tok, b)
+    yref, yabs = orc.moe(t, at, W3, E, rows, cols, ids, None, k, xin_o, n_tok, bias=b)
+    assert_close(y, yref, yabs, what=f"up {mode}")
+    # down form: one input per slot, gate-weighted
+    h = synth.activations(n_tok * k, cols, seed=6).reshape(n_tok, k, cols)
+    hin_o = orc.quantize_act(at, h) if at != F32 else h
+    hin_g = dev(h) if (at == F32 or flags) else dev(hin_o)
+    y = run_moe(qmv, qmv.FMT(t, at) | flags, W3d, E, rows, cols, ids, gates, k, hin_g, n_tok, b)
+    yref, yabs = orc.moe(t, at, W3, E, rows, cols, ids, gates, k, hin_o, n_tok, bias=b)
+    assert_close(y, yref, yabs, what=f"down {mode}")
+    qmv.qmv_get_status()
+
+
+def oracle_sampled(orc, t, at, W3, E, rows, cols, ids, gates, k, x_o, toks, rids, bias, down):
+    """Expected values for sampled tokens and rows, composed from the oracle's
+    matvec on each routed expert's slice of the stacked tensor."""
+    rb = orc.row_bytes(t, cols)
+    outs, absd = [], []
+    for tok in toks:
+        per, pera = [], []
+        for s in range(k):
+            e = int(ids[tok, s])
+            We = W3[e * rows * rb:(e + 1) * rows * rb]
+            xv = x_o[tok, s:s + 1] if down else x_o[tok:tok + 1]
+            yv, ya = orc.matvec(t, at, We, rows, cols, xv, 1, row_ids=rids)
+            per.append(yv[0] + bias[e, rids])
+            pera.append(ya[0] + np.abs(bias[e, rids]))
+        if down:
+            g = gates[tok].astype(np.float64)
+            outs.append(sum(g[s] * per[s] for s in range(k)))
+            absd.append(sum(abs(g[s]) * pera[s] for s in range(k)))
+        else:
+            outs.append(np.stack(per))
+            absd.append(np.stack(pera))
+    return np.stack(outs), np.stack(absd)
+
+
+@pytest.mark.parametrize("n_tok", [1, 64, 1024])
+def test_moe_gpt_oss_shapes_sampled(qmv, orc, workspace, n_tok):
+    """gpt-oss-20B-shaped experts: 32 MXFP4 experts, gate_up 5760x2880 and
+    down 2880x2880 with biases, top-4 routing; W4A8 with the activations
+    quantised inside the kernels.  Sampled tokens and rows are checked."""
+    E, k, t, at = 32, 4, MXFP4, Q8_0
+    fl = qmv.FLAG_QUANTIZE_X
+    g = np.random.default_rng(n_tok)
+    for rows, cols, down in ((5760, 2880, False), (2880, 2880, True)):
+        W3, ids, gates, b = moe_inputs(t, E, rows, cols, n_tok, k, 20 + rows)
+        x = synth.activations(n_tok * (k if down else 1), cols, seed=21)
+        x = x.reshape(n_tok, k, cols) if down else x
+        y = run_moe(qmv, qmv.FMT(t, at) | fl, dev(W3), E, rows, cols, ids, gates if down else None, k, dev(x),
+                    n_tok, b)
+        toks = np.unique(np.concatenate([[0, n_tok - 1], g.integers(0, n_tok, 4)]))
+        rids = np.unique(np.concatenate([[0, rows - 1], g.integers(0, rows, 30)]))
+        x_o = orc.quantize_act(at, x)
+        yref, yabs = oracle_sampled(orc, t, at, W3, E, rows, cols, ids, gates, k, x_o, toks, rids, b, down)
+        ysel = y[toks][..., rids]
+        assert_close(ysel, yref, yabs, what=f"n_tok={n_tok} down={down}")
+    qmv.qmv_get_status()
+
+
+def test_moe_routing_invariance(qmv, orc, workspace):
+    """A token's expert outputs do not depend on which other tokens were routed
+    with it: the 16-token call equals 16 single-token calls bit for bit."""
+    E, rows, cols, k, n_tok, t = 8, 96, 256, 2, 16, MXFP4
+    W3, ids, gates, b = moe_inputs(t, E, rows, cols, n_tok, k, 9)
+    W3d = dev(W3)
+    x = synth.activations(n_tok, cols, seed=9)
+    fmt = qmv.FMT(t, Q8_0) | qmv.FLAG_QUANTIZE_X
+    y = run_moe(qmv, fmt, W3d, E, rows, cols, ids, None, k, dev(x), n_tok, b)
+    for tok in (0, 5, 15):
+        y1 = run_moe(qmv, fmt, W3d, E, rows, cols, ids[tok:tok + 1], None, k, dev(x[tok:tok + 1]), 1, b)
+        assert np.array_equal(y1[0].view(np.uint32), y[tok].view(np.uint32))
+
+
+def test_moe_bad_expert_and_workspace(qmv, orc, workspace):
+    E, rows, cols, k, n_tok, t = 4, 32, 64, 2, 3, MXFP4
+    W3, ids, gates, b = moe_inputs(t, E, rows, cols, n_tok, k, 4)
+    W3d = dev(W3)
+    x = synth.activations(n_tok, cols, seed=4)
+    bad = ids.copy()
+    bad[1, 0] = 7   # out of range
+    y = run_moe(qmv, qmv.FMT(t, F32), W3d, E, rows, cols, bad, None, k, dev(x), n_tok, b)
+    with pytest.raises(qmv.QmvError) as e:
+        qmv.qmv_get_status()
+    assert e.value.code == qmv.ERR_DEVICE_STATUS and "expert id" in str(e.value)
+    yref, yabs = orc.moe(t, F32, W3, E, rows, cols, ids, None, k, x, n_tok, bias=b)
+    ok = [(0, 0), (0, 1), (1, 1), (2, 0), (2, 1)]   # every slot but the bad one
+    for tok, s in ok:
+        assert_close(y[tok, s], yref[tok, s], yabs[tok, s])
+    qmv.qmv_get_status()   # cleared
+    # a workspace that is too small is refused before launching
+    need = qmv.qmv_workspace_size(qmv.OP_MOE, qmv.FMT(t, F32), rows, cols, n_tok * k)
+    assert need > 0
+    small = torch.empty(1024, dtype=torch.uint8, device="cuda")
+    qmv.qmv_set_workspace(small, small.numel())
+    try:
+        with pytest.raises(qmv.QmvError) as e:
+            run_moe(qmv, qmv.FMT(t, F32), W3d, E, rows, cols, ids, None, k, dev(x), n_tok, b)
+        assert e.value.code == qmv.ERR_WORKSPACE
+    finally:
+        qmv.qmv_set_workspace(workspace, workspace.numel())
