@@ -56,6 +56,7 @@ _SIGS = {
     "qmv_matvec": (_I, [_I, _P, _I64, _I64, _P, _P, _I, _P]),
     "qmv_matmul": (_I, [_I, _P, _I64, _I64, _P, _P, _I64, _P]),
     "qmv_moe_matvec": (_I, [_I, _P, _I, _I64, _I64, _P, _P, _I, _P, _P, _I64, _P, _P]),
+    "qmv_moe_matvec_noalloc": (_I, [_I, _P, _I, _I64, _I64, _P, _P, _I, _P, _P, _I64, _P, _P]),
     "qmv_workspace_size": (_SZ, [_I, _I, _I64, _I64, _I64]),
     "qmv_set_workspace": (_I, [_P, _SZ]),
     "qmv_get_status": (_I, [_P]),
@@ -153,6 +154,15 @@ def qmv_matmul(fmt, W, rows, cols, X, Y, m, stream=None):
 def qmv_moe_matvec(fmt, W3d, n_expert, rows, cols, ids, gates, k, x, y, n_tok, bias=None, stream=None):
     return _call("qmv_moe_matvec", fmt, _ptr(W3d), n_expert, rows, cols, _ptr(ids), _ptr(gates), k,
                  _ptr(x), _ptr(y), n_tok, _ptr(bias), _stream(stream))
+
+
+def qmv_moe_matvec_noalloc(fmt, W3d, n_expert, rows, cols, ids, gates, k, x, y, n_tok, bias=None, stream=None):
+    """qmv_moe_matvec with the library's built-in scratch (no workspace)."""
+    return _call("qmv_moe_matvec_noalloc", fmt, _ptr(W3d), n_expert, rows, cols, _ptr(ids), _ptr(gates), k,
+                 _ptr(x), _ptr(y), n_tok, _ptr(bias), _stream(stream))
+
+
+MOE_NOALLOC_MAX_BYTES = 4 << 20
 
 
 def qmv_workspace_size(op, fmt, rows, cols, n) -> int:

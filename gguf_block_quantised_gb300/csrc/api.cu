@@ -42,6 +42,12 @@ int qmv_launch_gemm_q4k_bf16(const void* W, int64_t rows, int64_t cols, const vo
 // The device status word: kernels OR fault bits into it (QMV_DEV_*).
 __device__ unsigned g_qmv_status;
 
+// Built-in scratch of qmv_moe_matvec_noalloc: a fixed array in the library's
+// device image, present on every GPU that loads the library until the process
+// exits.  Host code must not use this name as an address; see
+// moe_noalloc_scratch() below.
+static __device__ __align__(256) uint8_t g_moe_noalloc_scratch[QMV_MOE_NOALLOC_MAX_BYTES];
+
 namespace qmv {
 
 unsigned* status_word()
@@ -383,6 +389,75 @@ int qmv_get_status(void* stream)
     if (v & QMV_DEV_WAIT_TIMEOUT) what += "a pipeline wait gave up (a copy never landed); ";
     if (v & QMV_DEV_BAD_ARG) what += "a kernel saw an inconsistent argument; ";
     return fail(QMV_ERR_DEVICE_STATUS, "device status 0x%x: %s", v, what.c_str());
+}
+
+// ---- the MoE call that allocates nothing ------------------------------------------
+}  // extern "C"
+
+namespace {
+
+// Device address of g_moe_noalloc_scratch on the current device, looked up
+// once per device (with that device current) and cached.  In host code the
+// array's name is only a stand-in for the symbol, never a device pointer.
+void* moe_noalloc_scratch()
+{
+    static std::atomic<void*> cache[qmv::kMaxDevices];
+    const int d = qmv::current_device();
+    if (d < 0 || d >= qmv::kMaxDevices) return nullptr;
+    void* p = cache[d].load(std::memory_order_acquire);
+    if (!p) {
+        void* a = nullptr;
+        if (cudaGetSymbolAddress(&a, g_moe_noalloc_scratch) != cudaSuccess || !a) return nullptr;
+        cache[d].store(a, std::memory_order_release);
+        p = a;
+    }
+    return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+int qmv_moe_matvec_noalloc(int fmt, const void* W3d, int n_expert, int64_t rows, int64_t cols, const int32_t* ids,
+                           const float* gates, int k, const void* x, float* y, int64_t n_tok, const float* bias,
+                           void* stream)
+{
+    if (fmt & ~(0xffff | QMV_FLAG_QUANTIZE_X)) return fail(QMV_ERR_INVALID_ARG, "unknown flags 0x%x", fmt & ~0xffff);
+    const bool quant_x = (fmt & QMV_FLAG_QUANTIZE_X) != 0;
+    const int wtype = fmt & 0xff, atype = (fmt >> 8) & 0xff;
+    if (is_weight_type(wtype) && atype != QMV_F32 && atype != paired_act(wtype))
+        return fail(QMV_ERR_UNSUPPORTED, "qmv_moe_matvec_noalloc: %s experts take F32 or %s activations (got %s)",
+                    type_name(wtype), type_name(paired_act(wtype)), type_name(atype));
+    int rc = check_weights(wtype, W3d, rows, cols);
+    if (rc) return rc;
+    if (quant_x && atype == QMV_F32)
+        return fail(QMV_ERR_INVALID_ARG, "QMV_FLAG_QUANTIZE_X needs an 8-bit activation type (Q8_0 or Q8_K)");
+    if (n_expert < 1 || n_expert > 1024) return fail(QMV_ERR_INVALID_ARG, "n_expert must be in 1..1024 (got %d)", n_expert);
+    if (k < 1 || k > 64) return fail(QMV_ERR_INVALID_ARG, "k must be in 1..64 (got %d)", k);
+    if (n_tok < 0 || n_tok * k > (int64_t)1 << 24)
+        return fail(QMV_ERR_INVALID_ARG, "n_tok must be >= 0 with n_tok*k <= 16777216");
+    if (n_tok == 0 || rows == 0) return ok();
+    const size_t need = qmv_moe_workspace_bytes(rows, n_tok * k);
+    if (need > QMV_MOE_NOALLOC_MAX_BYTES)
+        return fail(QMV_ERR_SHAPE,
+                    "qmv_moe_matvec_noalloc: %lld (token, slot) pairs x %lld rows need %zu bytes of scratch; the "
+                    "built-in scratch holds %zu (about n_tok*k*rows*4 bytes are needed); use qmv_moe_matvec with a "
+                    "workspace for larger calls",
+                    (long long)(n_tok * k), (long long)rows, need, (size_t)QMV_MOE_NOALLOC_MAX_BYTES);
+    if (!ids || !x || !y) return fail(QMV_ERR_INVALID_ARG, "ids, x and y must not be NULL");
+    const bool a8 = atype != QMV_F32;
+    const int xal = (a8 && !quant_x) ? 4 : 16;
+    if (!aligned(x, xal)) return fail(QMV_ERR_ALIGN, "x must be %d-byte aligned", xal);
+    if (!aligned(ids, 4) || !aligned(y, 4) || (gates && !aligned(gates, 4)) || (bias && !aligned(bias, 4)))
+        return fail(QMV_ERR_ALIGN, "ids, gates, bias and y must be 4-byte aligned");
+    void* ws = moe_noalloc_scratch();
+    if (!ws) return cuda_fail("qmv_moe_matvec_noalloc (scratch address)");
+    if (!qmv::status_word()) return cuda_fail("qmv_moe_matvec_noalloc (status word)");
+    rc = qmv_launch_moe(wtype, a8, quant_x, qmv_block_bytes(paired_act(wtype)), W3d, n_expert, rows, cols, ids, gates,
+                        k, x, y, n_tok, bias, ws, static_cast<cudaStream_t>(stream));
+    if (rc == -2) return fail(QMV_ERR_SHAPE, "cols = %lld needs more shared memory than one SM has", (long long)cols);
+    if (rc) return cuda_fail("qmv_moe_matvec_noalloc");
+    return ok();
 }
 
 }  // extern "C"

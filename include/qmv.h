@@ -215,6 +215,38 @@ int qmv_moe_matvec(int fmt, const void* W3d, int n_expert, int64_t rows, int64_t
                    const void* x, float* y, int64_t n_tok, const float* bias,
                    void* stream);
 
+/* ---------------------------------------------------------------------------
+ * qmv_moe_matvec_noalloc -- qmv_moe_matvec for callers that cannot allocate
+ * device memory.  (This entry point has no counterpart on the llamay pages;
+ * it is a property of this library's interface.)
+ *
+ * Some callers can't call cudaMalloc or hand the library a buffer: a plugin
+ * inside a host program that owns all device memory through its own pool, a
+ * latency-critical loop where an allocation (which may synchronise the
+ * device) is not allowed, or code that runs before the host's allocator
+ * exists.  This call takes exactly the arguments of qmv_moe_matvec and gives
+ * the same results, but its scratch (the expert grouping and the per-slot
+ * outputs) lives in a fixed array inside the library's device image instead
+ * of a registered workspace.  It allocates nothing and needs no
+ * qmv_set_workspace().
+ *   Limit: the scratch holds QMV_MOE_NOALLOC_MAX_BYTES (4 MiB); a call needs
+ *   qmv_workspace_size(QMV_OP_MOE, fmt, rows, cols, n_tok*k) bytes (about
+ *   n_tok*k*rows*4), and a larger one is refused with QMV_ERR_SHAPE.  Every
+ *   GPU that loads the library holds these 4 MiB until the process exits.
+ *   Set-up: the first call on each device looks up the array's device address
+ *   (with that device current); make that first call before any stream
+ *   capture.
+ *   Sharing: every call uses the same array, which keeps the last call's
+ *   contents (each call overwrites what it reads, so nothing needs clearing).
+ *   Calls that can overlap on the GPU -- on different streams, or from
+ *   different host threads -- race on the array; order them on one stream.
+ * ------------------------------------------------------------------------- */
+#define QMV_MOE_NOALLOC_MAX_BYTES ((size_t)4 << 20)
+int qmv_moe_matvec_noalloc(int fmt, const void* W3d, int n_expert, int64_t rows, int64_t cols,
+                           const int32_t* ids, const float* gates, int k,
+                           const void* x, float* y, int64_t n_tok, const float* bias,
+                           void* stream);
+
 /* Workspace for the calls that need scratch. */
 enum { QMV_OP_MATVEC = 1, QMV_OP_MATMUL = 2, QMV_OP_MOE = 3 };
 /* Bytes of workspace `op` needs for these sizes (n = n_tok*k for MoE: the
