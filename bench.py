@@ -67,6 +67,15 @@ def load_peaks():
     return 6800.0, "fallback"
 
 
+def load_tflops_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d.get("bf16_tflops") or 1900.0)
+    except Exception:
+        return 1900.0
+
+
 # ---- clocks sampled during the timed region -----------------------------------------
 class ClockSampler:
     FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
@@ -231,6 +240,104 @@ def cpu_baseline(n_steps=4):
             "sample": f"{n_steps} full decode steps (batch 1, W4A8), single-threaded C oracle, {dt:.1f} s"}
 
 
+def time_rotating(torch, stream, calls, reps):
+    """Time `calls` (a list of closures taking a stream, each on its own input
+    copy so consecutive launches do not hit in L2) replayed round robin from a
+    CUDA graph; returns ms per call."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for c in calls:
+            c(stream)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(reps):
+                calls[i % len(calls)](stream)
+    g.replay()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def prefill_leg(q, torch, stream, tflops_peak):
+    """Q4_K prefill GEMMs (bf16 activations, tcgen05): 14336x4096 and 4096x14336
+    at M = 512 and 2048.  Four (W, X) copies rotate so that every launch reads
+    its operands from HBM (> L2 in total)."""
+    out = {}
+    tot_flop, tot_ms = 0.0, 0.0
+    for rows, cols in ((14336, 4096), (4096, 14336)):
+        Ws = [torch.from_numpy(synth.weights(Q4_K, rows, cols, seed=4, tensor_id=rows + i)).cuda() for i in range(4)]
+        for m in (512, 2048):
+            Xs = [torch.randn(m, cols, device="cuda").to(torch.bfloat16) for _ in range(4)]
+            Y = torch.empty(m, rows, device="cuda")
+            calls = [(lambda s, W=W, X=X: q.qmv_matmul(q.FMT(Q4_K, BF16), W, rows, cols, X, Y, m, s.cuda_stream))
+                     for W, X in zip(Ws, Xs)]
+            ms = time_rotating(torch, stream, calls, 40)
+            flop = 2.0 * m * rows * cols
+            out[f"{rows}x{cols}_m{m}"] = {"ms": ms, "tflops": flop / (ms / 1e3) / 1e12,
+                                         "frac_of_peak": flop / (ms / 1e3) / 1e12 / tflops_peak}
+            tot_flop += flop
+            tot_ms += ms
+            del Xs, Y
+        del Ws
+    q.qmv_get_status(stream)
+    return {"metric": "prefill GEMM TFLOP/s (Q4_K x bf16, fp32 accumulate)", "unit": "TFLOP/s",
+            "value": tot_flop / (tot_ms / 1e3) / 1e12, "peak": tflops_peak,
+            "frac": tot_flop / (tot_ms / 1e3) / 1e12 / tflops_peak, "shapes": out,
+            "kernel": "k_gemm_q4k_bf16 (tcgen05.mma kind::f16, M=128 rows x N=256 tokens, TMEM accumulator)"}
+
+
+def moe_leg(q, torch, stream, hbm):
+    """gpt-oss-20B-shaped MoE layer: 32 MXFP4 experts, gate_up 5760x2880 (up
+    form, x shared by the 4 slots) then down 2880x2880 (per-slot inputs,
+    gate-weighted), fp32 biases, top-4 of N(0,1) router logits, activations
+    quantised to Q8_0 in the kernels.  Metric: distinct expert weight bytes
+    read per layer / time."""
+    E, k = 32, 4
+    Wgu = torch.from_numpy(synth.weights(MXFP4, E * 5760, 2880, seed=5, tensor_id=1)).cuda()
+    Wd = torch.from_numpy(synth.weights(MXFP4, E * 2880, 2880, seed=5, tensor_id=2)).cuda()
+    bgu = torch.from_numpy(synth.bias(E, 5760, seed=5)).cuda()
+    bd = torch.from_numpy(synth.bias(E, 2880, seed=5, tensor_id=2001)).cuda()
+    fmt = q.FMT(MXFP4, Q8_0) | q.FLAG_QUANTIZE_X
+    res = {}
+    ws = None
+    for n_tok in (1, 64, 1024):
+        # four routings rotate, so the experts one launch reads were not just read
+        routes = [synth.router(n_tok, E, k, seed=6 + r) for r in range(4)]
+        x = torch.randn(n_tok, 2880, device="cuda")
+        h = torch.randn(n_tok, k, 2880, device="cuda")
+        y1 = torch.empty(n_tok, k, 5760, device="cuda")
+        y2 = torch.empty(n_tok, 2880, device="cuda")
+        need = q.qmv_workspace_size(q.OP_MOE, fmt, 5760, 2880, n_tok * k)
+        if ws is None or ws.numel() < need:
+            ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+        q.qmv_set_workspace(ws, ws.numel())
+        calls = []
+        for ids_np, gates_np in routes:
+            ids, gates = torch.from_numpy(ids_np).cuda(), torch.from_numpy(gates_np).cuda()
+
+            def layer(s, ids=ids, gates=gates):
+                q.qmv_moe_matvec(fmt, Wgu, E, 5760, 2880, ids, None, k, x, y1, n_tok, bgu, s.cuda_stream)
+                q.qmv_moe_matvec(fmt, Wd, E, 2880, 2880, ids, gates, k, h, y2, n_tok, bd, s.cuda_stream)
+            calls.append(layer)
+        reps = 20 if n_tok >= 1024 else 100
+        ms = time_rotating(torch, stream, calls, reps)
+        used = float(np.mean([len(np.unique(r[0])) for r in routes]))
+        wbytes = used * (5760 + 2880) * synth.row_bytes(MXFP4, 2880)
+        flop = 2.0 * n_tok * k * (5760 + 2880) * 2880
+        res[f"tok{n_tok}"] = {"ms": ms, "experts_used": used, "weight_bytes": int(wbytes),
+                              "weight_gbs": wbytes / (ms / 1e3) / 1e9, "frac_of_hbm": wbytes / (ms / 1e3) / 1e9 / hbm,
+                              "tflops": flop / (ms / 1e3) / 1e12}
+    q.qmv_set_workspace(None, 0)
+    q.qmv_get_status(stream)
+    return {"metric": "MoE layer (gate_up + down) expert weight GB/s", "unit": "GB/s", "by_tokens": res,
+            "path": "grouped per-expert matvec (k_moe_group + k_moe_gemv + k_moe_combine) for every token count"}
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -272,6 +379,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the prefill and MoE legs")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
@@ -353,6 +461,9 @@ def main():
     e2e_ms, _ = time_graph(torch, e2e_step, stream, e2e_steps, args.warmup)
 
     hbm, peak_kind = load_peaks()
+    tflops_peak = 1900.0 if peak_kind == "fallback" else load_tflops_peak()
+    prefill = None if args.no_extra else prefill_leg(q, torch, stream, tflops_peak)
+    moe = None if args.no_extra else moe_leg(q, torch, stream, hbm)
     value = ws * STEP_WEIGHT_BYTES / (ms1 / 1e3) / 1e9
     if rank != 0:
         if ws > 1:
@@ -397,6 +508,8 @@ def main():
                        "CUDA graph on the caller's stream"},
         "gpu_launches": launches_per_step * args.steps,
         "cpu_baseline": cpu,
+        "prefill": prefill,
+        "moe": moe,
     }
     print(json.dumps(line))
     if ws > 1:
