@@ -338,6 +338,90 @@ def moe_leg(q, torch, stream, hbm):
             "path": "grouped per-expert matvec (k_moe_group + k_moe_gemv + k_moe_combine) for every token count"}
 
 
+def run_probe(spec):
+    """Single-kernel runs for profiling (ncu captures).  Specs:
+      gemv:T:rows:cols:atype:n_vec   qmv_matvec on synthetic weights (atype 8 = fp32)
+      gemm:rows:cols:m               qmv_matmul, Q4_K x bf16
+      moe:n_tok                      one gpt-oss-shaped MoE layer (gate_up + down)
+    Each runs its call five times and prints the event-timed mean of the last three."""
+    import torch
+    import gguf_block_quantised_gb300 as q
+    from gguf_block_quantised_gb300 import build as B
+    B.build()
+    q.load()
+    parts = spec.split(":")
+    kind, a = parts[0], [int(v) for v in parts[1:]]
+    if kind == "gemv":
+        t, rows, cols, at, nv = a
+        W = torch.from_numpy(synth.weights(t, rows, cols, seed=1)).cuda()
+        x = torch.from_numpy(synth.activations(nv, cols)).cuda()
+        if at != F32:
+            xq = torch.empty(nv * q.qmv_row_bytes(at, cols), dtype=torch.uint8, device="cuda")
+            q.qmv_quantize_act(at, x, xq, nv * cols)
+            x = xq
+        y = torch.empty((nv, rows), dtype=torch.float32, device="cuda")
+        call = lambda: q.qmv_matvec(q.FMT(t, at), W, rows, cols, x, y, nv)
+        nbytes, what = W.numel(), "weight GB/s"
+    elif kind == "gemm":
+        rows, cols, m = a
+        W = torch.from_numpy(synth.weights(Q4_K, rows, cols, seed=1)).cuda()
+        X = torch.randn(m, cols, device="cuda").to(torch.bfloat16)
+        Y = torch.empty(m, rows, device="cuda")
+        call = lambda: q.qmv_matmul(q.FMT(Q4_K, BF16), W, rows, cols, X, Y, m)
+        nbytes, what = 2 * m * rows * cols / 1e3, "TFLOP/s"
+    elif kind == "moe":
+        (n_tok,) = a
+        E, k = 32, 4
+        Wgu = torch.from_numpy(synth.weights(MXFP4, E * 5760, 2880, seed=5, tensor_id=1)).cuda()
+        Wd = torch.from_numpy(synth.weights(MXFP4, E * 2880, 2880, seed=5, tensor_id=2)).cuda()
+        bgu = torch.from_numpy(synth.bias(E, 5760, seed=5)).cuda()
+        bd = torch.from_numpy(synth.bias(E, 2880, seed=5, tensor_id=2001)).cuda()
+        ids_np, gates_np = synth.router(n_tok, E, k, seed=6)
+        ids, gates = torch.from_numpy(ids_np).cuda(), torch.from_numpy(gates_np).cuda()
+        x = torch.randn(n_tok, 2880, device="cuda")
+        h = torch.randn(n_tok, k, 2880, device="cuda")
+        y1 = torch.empty(n_tok, k, 5760, device="cuda")
+        y2 = torch.empty(n_tok, 2880, device="cuda")
+        fmt = q.FMT(MXFP4, Q8_0) | q.FLAG_QUANTIZE_X
+        ws = torch.empty(q.qmv_workspace_size(q.OP_MOE, fmt, 5760, 2880, n_tok * k), dtype=torch.uint8, device="cuda")
+        q.qmv_set_workspace(ws, ws.numel())
+
+        def call():
+            q.qmv_moe_matvec(fmt, Wgu, E, 5760, 2880, ids, None, k, x, y1, n_tok, bgu)
+            q.qmv_moe_matvec(fmt, Wd, E, 2880, 2880, ids, gates, k, h, y2, n_tok, bd)
+        nbytes = len(np.unique(ids_np)) * (5760 + 2880) * synth.row_bytes(MXFP4, 2880)
+        what = "expert weight GB/s"
+    else:
+        raise SystemExit(f"unknown probe {spec}")
+    for _ in range(2):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(3):
+        call()
+    e1.record()
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / 3
+    q.qmv_get_status()
+    print(json.dumps({"probe": spec, "ms": ms, what: nbytes / (ms / 1e3) / 1e9}))
+    return 0
+
+
+def traffic_for(kernel):
+    """DRAM bytes per launch from the committed ncu record, if the kernel's
+    source is unchanged since that capture; else None."""
+    import hashlib
+    try:
+        rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))[kernel]
+        src = os.path.join(ROOT, "gguf_block_quantised_gb300", "csrc")
+        h = hashlib.sha1(b"".join(open(os.path.join(src, f), "rb").read()
+                                  for f in ["common.cuh", "formats.cuh", "gemv.cuh", "gemv_launch.cuh"])).hexdigest()
+        return rec["dram_bytes"] if h == rec["source_sha1"] else None
+    except Exception:
+        return None
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -380,7 +464,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the prefill and MoE legs")
+    ap.add_argument("--probe", default=None, help="run one kernel for profiling (see run_probe)")
     args = ap.parse_args()
+    if args.probe:
+        return run_probe(args.probe)
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
         return run_reference(args)
@@ -498,7 +585,7 @@ def main():
                            "how": "qmv_quantize_act + qmv_matvec as separate launches, no PDL"},
         "roofline": {"bound": "hbm", "kernel": "k_gemv<Q8_0,A8,NV=1> lm_head 151936x896 (quantising its fp32 input)",
                      "achieved": lm_gbs, "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": lm_gbs / hbm, "traffic": None,
+                     "frac": lm_gbs / hbm, "traffic": traffic_for("k_gemv<Q8_0,A8,NV=1> lm_head 151936x896"),
                      "algorithmic_bytes_per_launch": lm_bytes, "launch_ms": lm_ms,
                      "l2": "4 weight copies rotated, each launch reads cold"},
         "clocks": clocks,
