@@ -240,10 +240,46 @@ def cpu_baseline(n_steps=4):
             "sample": f"{n_steps} full decode steps (batch 1, W4A8), single-threaded C oracle, {dt:.1f} s"}
 
 
-def time_rotating(torch, stream, calls, reps):
-    """Time `calls` (a list of closures taking a stream, each on its own input
-    copy so consecutive launches do not hit in L2) replayed round robin from a
-    CUDA graph; returns ms per call."""
+def lm_roofline(q, torch, stream, step, dev_index):
+    """The dominant kernel alone: the lm_head matvec (144.6 MB per launch).
+    Four copies of the weights rotate (578 MB > 4x L2), so every launch reads
+    its weights from HBM; 200 launches replay from one CUDA graph."""
+    lm_copies = [step.lm] + [step.lm.clone() for _ in range(3)]
+
+    def lm_only(s, Wl):
+        q.qmv_matvec(q.FMT(Q8_0, Q8_0) | q.FLAG_QUANTIZE_X, Wl, VOCAB, HID, step.x[-1], step.logits, 1,
+                     s.cuda_stream)
+    lm_reps = 200
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        lm_only(stream, lm_copies[0])
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(lm_reps):
+                lm_only(stream, lm_copies[i % 4])
+    g.replay()
+    stream.synchronize()
+    sampler = ClockSampler(dev_index)
+    sampler.__enter__()
+    time.sleep(0.2)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(5):
+            g.replay()
+        e1.record(stream)
+    e1.synchronize()
+    sampler.__exit__(None, None, None)
+    del g, lm_copies
+    return e0.elapsed_time(e1) / (5 * lm_reps), sampler.summary()
+
+
+def time_rotating(torch, stream, calls, reps, warmup=3, timed=3):
+    """Time `calls` (closures taking a stream, each on its own input copy so
+    consecutive launches do not hit in L2) replayed round robin from one CUDA
+    graph of `reps` calls: at least `warmup` replays and 20 ms of warm-up (so
+    the clocks have ramped after the idle capture), then `timed` replays
+    between CUDA events.  Returns ms per call."""
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         for c in calls:
@@ -252,15 +288,23 @@ def time_rotating(torch, stream, calls, reps):
         with torch.cuda.graph(g, stream=stream):
             for i in range(reps):
                 calls[i % len(calls)](stream)
-    g.replay()
-    stream.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    spent, n = 0.0, 0
+    while n < warmup or spent < 20.0:
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        e1.synchronize()
+        spent += e0.elapsed_time(e1)
+        n += 1
     with torch.cuda.stream(stream):
         e0.record(stream)
-        g.replay()
+        for _ in range(timed):
+            g.replay()
         e1.record(stream)
     e1.synchronize()
-    return e0.elapsed_time(e1) / reps
+    return e0.elapsed_time(e1) / (timed * reps)
 
 
 def prefill_leg(q, torch, stream, tflops_peak):
@@ -284,8 +328,20 @@ def prefill_leg(q, torch, stream, tflops_peak):
             tot_ms += ms
             del Xs, Y
         del Ws
+    # W4A8 (Q8_K activations): exact integer path, one shape
+    rows, cols, m = 14336, 4096, 512
+    Ws = [torch.from_numpy(synth.weights(Q4_K, rows, cols, seed=4, tensor_id=rows + i)).cuda() for i in range(4)]
+    x = torch.randn(m, cols, device="cuda")
+    Xq = torch.empty(m * q.qmv_row_bytes(Q8_K, cols), dtype=torch.uint8, device="cuda")
+    q.qmv_quantize_act(Q8_K, x, Xq, m * cols)
+    Y = torch.empty(m, rows, device="cuda")
+    calls = [(lambda s, W=W: q.qmv_matmul(q.FMT(Q4_K, Q8_K), W, rows, cols, Xq, Y, m, s.cuda_stream)) for W in Ws]
+    ms = time_rotating(torch, stream, calls, 8)
+    w4a8 = {"shape": f"{rows}x{cols}_m{m}", "ms": ms, "tflops": 2.0 * m * rows * cols / (ms / 1e3) / 1e12,
+            "path": "exact int8 dp4a block dots (the decode engine over token groups of 16)"}
+    del Ws, Xq, Y
     q.qmv_get_status(stream)
-    return {"metric": "prefill GEMM TFLOP/s (Q4_K x bf16, fp32 accumulate)", "unit": "TFLOP/s",
+    return {"metric": "prefill GEMM TFLOP/s (Q4_K x bf16, fp32 accumulate)", "unit": "TFLOP/s", "w4a8": w4a8,
             "value": tot_flop / (tot_ms / 1e3) / 1e12, "peak": tflops_peak,
             "frac": tot_flop / (tot_ms / 1e3) / 1e12 / tflops_peak, "shapes": out,
             "kernel": "k_gemm_q4k_bf16 (tcgen05.mma kind::f16, M=128 rows x N=256 tokens, TMEM accumulator)"}
@@ -490,6 +546,7 @@ def main():
 
     # --- the step at batch 1 (the headline) and batch 8; the two-launch form for comparison
     step1 = DecodeStep(q, torch, 1)
+    lm_ms_first, _ = lm_roofline(q, torch, stream, step1, local)
     step8 = DecodeStep(q, torch, 8)
     step1u = DecodeStep(q, torch, 1, fused=False)
     if ws > 1:
@@ -504,32 +561,8 @@ def main():
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms1, ms8 = t.tolist()
 
-    # --- the dominant kernel alone: lm_head matvec (144.6 MB per launch).  Four
-    # copies of the weights are rotated (578 MB > 4x L2), so every launch reads
-    # its weights from HBM.
+    lm_ms, lm_clocks = lm_roofline(q, torch, stream, step1, local)
     lm_bytes = VOCAB * row_bytes(Q8_0, HID)
-    lm_copies = [step1.lm] + [step1.lm.clone() for _ in range(3)]
-
-    def lm_only(s, Wl):
-        q.qmv_matvec(q.FMT(Q8_0, Q8_0) | q.FLAG_QUANTIZE_X, Wl, VOCAB, HID, step1.x[-1], step1.logits, 1,
-                     s.cuda_stream)
-    lm_reps = 200
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        lm_only(stream, lm_copies[0])
-        stream.synchronize()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(lm_reps):
-                lm_only(stream, lm_copies[i % 4])
-    g.replay()
-    stream.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        g.replay()
-        e1.record(stream)
-    e1.synchronize()
-    lm_ms = e0.elapsed_time(e1) / lm_reps
     lm_gbs = lm_bytes / (lm_ms / 1e3) / 1e9
 
     # --- end to end through host buffers: pinned activations in, logits out, per step
@@ -587,6 +620,7 @@ def main():
                      "achieved": lm_gbs, "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": lm_gbs / hbm, "traffic": traffic_for("k_gemv<Q8_0,A8,NV=1> lm_head 151936x896"),
                      "algorithmic_bytes_per_launch": lm_bytes, "launch_ms": lm_ms,
+                     "launch_ms_before_step_graphs": lm_ms_first, "clocks": lm_clocks,
                      "l2": "4 weight copies rotated, each launch reads cold"},
         "clocks": clocks,
         "e2e": {"value": ws * STEP_WEIGHT_BYTES / (e2e_ms / 1e3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,

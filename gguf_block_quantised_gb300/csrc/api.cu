@@ -290,10 +290,10 @@ int qmv_matmul(int fmt, const void* W, int64_t rows, int64_t cols, const void* X
     if (fmt & ~(0xffff | QMV_FLAG_PDL)) return fail(QMV_ERR_INVALID_ARG, "unknown flags 0x%x", fmt & ~0xffff);
     const bool pdl = (fmt & QMV_FLAG_PDL) != 0;
     const int wtype = fmt & 0xff, atype = (fmt >> 8) & 0xff;
-    if (wtype != QMV_Q4_K || atype != QMV_BF16)
+    if (wtype != QMV_Q4_K || (atype != QMV_BF16 && atype != QMV_Q8_K))
         return fail(QMV_ERR_UNSUPPORTED,
-                    "qmv_matmul: %s weights with %s activations are not provided; supported: QMV_FMT(Q4_K, BF16) "
-                    "(other formats: qmv_matvec with n_vec <= 64)",
+                    "qmv_matmul: %s weights with %s activations are not provided; supported: QMV_FMT(Q4_K, BF16), "
+                    "QMV_FMT(Q4_K, Q8_K) (other formats: qmv_matvec with n_vec <= 64)",
                     type_name(wtype), type_name(atype));
     int rc = check_weights(wtype, W, rows, cols);
     if (rc) return rc;
@@ -304,6 +304,14 @@ int qmv_matmul(int fmt, const void* W, int64_t rows, int64_t cols, const void* X
     if (!aligned(X, 16)) return fail(QMV_ERR_ALIGN, "X must be 16-byte aligned");
     if (!aligned(Y, 4)) return fail(QMV_ERR_ALIGN, "Y must be 4-byte aligned");
     if (!qmv::status_word()) return cuda_fail("qmv_matmul (status word)");
+    if (atype == QMV_Q8_K) {
+        // W4A8: the exact integer block dots of the decode engine over every
+        // token (Y[m][rows] has the matvec's y[v][rows] layout).
+        rc = qmv_gemv_q4_k(true, false, pdl, W, rows, cols, X, Y, (int)m, static_cast<cudaStream_t>(stream));
+        if (rc == -2) return fail(QMV_ERR_SHAPE, "cols = %lld needs more shared memory than one SM has", (long long)cols);
+        if (rc) return cuda_fail("qmv_matmul");
+        return ok();
+    }
     rc = qmv_launch_gemm_q4k_bf16(W, rows, cols, X, Y, m, pdl, static_cast<cudaStream_t>(stream));
     if (rc == -8) return fail(QMV_ERR_CUDA, "qmv_matmul: could not build a TMA tensor map");
     if (rc) return cuda_fail("qmv_matmul");

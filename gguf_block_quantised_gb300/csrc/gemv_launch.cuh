@@ -33,7 +33,7 @@ inline int rows_in_flight_rt(int T, int nv)
 }
 
 template <int T>
-inline bool plan_gemv(bool a8, int64_t rows, int64_t cols, int n_vec, GemvPlan& pl)
+inline bool plan_gemv(bool a8, int64_t rows, int64_t cols, int n_vec, GemvPlan& pl, int max_rpw = 4)
 {
     using F = Fmt<T>;
     const int nb = (int)(cols / F::BS);
@@ -55,7 +55,7 @@ inline bool plan_gemv(bool a8, int64_t rows, int64_t cols, int n_vec, GemvPlan& 
         // group, so a multi-chunk row gives each warp as many rows as this
         // group's kernel decodes at once (smaller groups decode at least as many).
         const int rif = rows_in_flight_rt(T, g);
-        for (int rpw = pl.n_chunks > 1 ? rif : 4; rpw >= 1; rpw /= 2) {
+        for (int rpw = pl.n_chunks > 1 ? rif : max_rpw; rpw >= 1; rpw /= 2) {
             if (pl.n_chunks > 1 && rpw != rif) break;
             const size_t xb = xhat_bytes(T, a8, g, (int)cols);
             if (xb > kXhatMaxBytes && g > 1) break;
@@ -145,7 +145,7 @@ inline int launch_gemv_t(bool a8, bool quant_x, bool pdl, const void* W, int64_t
 
 // ---- mixture of experts -----------------------------------------------------------
 template <int T, bool A8, int NV>
-inline int launch_moe_nv(const MoeParams& mp, const GemvPlan& pl, int n_expert, int active, cudaStream_t st)
+inline int launch_moe_nv(const MoeParams& mp, const GemvPlan& pl, int grid_y, int active, cudaStream_t st)
 {
     auto* k = &k_moe_gemv<T, A8, NV, rows_in_flight<T, NV>()>;
     const size_t smem = pl.smem + 256;
@@ -155,7 +155,7 @@ inline int launch_moe_nv(const MoeParams& mp, const GemvPlan& pl, int n_expert, 
     int64_t gx = ((int64_t)num_sms() * occ * 2 + active - 1) / active;
     if (gx > n_tiles) gx = n_tiles;
     if (gx < 1) gx = 1;
-    return launch_ex(k, dim3((unsigned)gx, (unsigned)n_expert), dim3(kGemvThreads), smem, st, false, mp) ==
+    return launch_ex(k, dim3((unsigned)gx, (unsigned)grid_y), dim3(kGemvThreads), smem, st, false, mp) ==
                    cudaSuccess
                ? 0
                : -6;
@@ -165,14 +165,15 @@ inline int launch_moe_nv(const MoeParams& mp, const GemvPlan& pl, int n_expert, 
 // apart; pair p reads row p / kdiv and writes out[p*rows ..].
 template <int T>
 inline int launch_moe_t(bool a8, bool quant_x, const void* W3d, int n_expert, int64_t rows, int64_t cols,
-                        const int* offsets, const int* perm, int n_pairs, const void* x, size_t xrow, int kdiv,
-                        float* out, const float* bias, cudaStream_t st)
+                        const int* offsets, const int* active_list, const int* perm, int n_pairs, const void* x,
+                        size_t xrow, int kdiv, float* out, const float* bias, cudaStream_t st)
 {
     using F = Fmt<T>;
     if (rows == 0 || n_pairs == 0) return 0;
     GemvPlan pl;
-    if (!plan_gemv<T>(a8, rows, cols, n_pairs < 16 ? n_pairs : 16, pl)) return -2;
-    if (pl.n_chunks == 1) pl.rpw = 1;   // many small tiles: an expert's rows spread over many SMs
+    // Many small tiles (one row per warp) so an expert's rows spread over many
+    // SMs; the stage ring is sized for that tile.
+    if (!plan_gemv<T>(a8, rows, cols, n_pairs < 16 ? n_pairs : 16, pl, 1)) return -2;
     MoeParams mp{};
     GemvParams& p = mp.g;
     p.W = static_cast<const uint8_t*>(W3d);
@@ -192,37 +193,39 @@ inline int launch_moe_t(bool a8, bool quant_x, const void* W3d, int n_expert, in
     p.x = x;
     mp.expert_bytes = p.total;
     mp.offsets = offsets;
+    mp.active = active_list;
     mp.perm = perm;
     mp.xrow = xrow;
     mp.kdiv = kdiv;
     mp.out = out;
     mp.bias = bias;
     mp.group = pl.group;
+    // Grid rows map onto the experts that received pairs (at most this many).
     const int active = n_pairs < n_expert ? n_pairs : n_expert;
     const int g = pl.group;
     if (a8) {
-        if (g <= 1) return launch_moe_nv<T, true, 1>(mp, pl, n_expert, active, st);
-        if (g <= 2) return launch_moe_nv<T, true, 2>(mp, pl, n_expert, active, st);
-        if (g <= 4) return launch_moe_nv<T, true, 4>(mp, pl, n_expert, active, st);
-        if (g <= 8) return launch_moe_nv<T, true, 8>(mp, pl, n_expert, active, st);
-        return launch_moe_nv<T, true, 16>(mp, pl, n_expert, active, st);
+        if (g <= 1) return launch_moe_nv<T, true, 1>(mp, pl, active, active, st);
+        if (g <= 2) return launch_moe_nv<T, true, 2>(mp, pl, active, active, st);
+        if (g <= 4) return launch_moe_nv<T, true, 4>(mp, pl, active, active, st);
+        if (g <= 8) return launch_moe_nv<T, true, 8>(mp, pl, active, active, st);
+        return launch_moe_nv<T, true, 16>(mp, pl, active, active, st);
     }
-    if (g <= 1) return launch_moe_nv<T, false, 1>(mp, pl, n_expert, active, st);
-    if (g <= 2) return launch_moe_nv<T, false, 2>(mp, pl, n_expert, active, st);
-    if (g <= 4) return launch_moe_nv<T, false, 4>(mp, pl, n_expert, active, st);
-    if (g <= 8) return launch_moe_nv<T, false, 8>(mp, pl, n_expert, active, st);
-    return launch_moe_nv<T, false, 16>(mp, pl, n_expert, active, st);
+    if (g <= 1) return launch_moe_nv<T, false, 1>(mp, pl, active, active, st);
+    if (g <= 2) return launch_moe_nv<T, false, 2>(mp, pl, active, active, st);
+    if (g <= 4) return launch_moe_nv<T, false, 4>(mp, pl, active, active, st);
+    if (g <= 8) return launch_moe_nv<T, false, 8>(mp, pl, active, active, st);
+    return launch_moe_nv<T, false, 16>(mp, pl, active, active, st);
 }
 
 }  // namespace qmv
 
 #define QMV_MOE_INSTANTIATE(T, NAME)                                                                        \
     int NAME(bool a8, bool quant_x, const void* W3d, int n_expert, int64_t rows, int64_t cols,                 \
-             const int* offsets, const int* perm, int n_pairs, const void* x, size_t xrow, int kdiv,            \
-             float* out, const float* bias, cudaStream_t st)                                                    \
+             const int* offsets, const int* active, const int* perm, int n_pairs, const void* x, size_t xrow,  \
+             int kdiv, float* out, const float* bias, cudaStream_t st)                                          \
     {                                                                                                           \
-        return qmv::launch_moe_t<T>(a8, quant_x, W3d, n_expert, rows, cols, offsets, perm, n_pairs, x, xrow,   \
-                                    kdiv, out, bias, st);                                                       \
+        return qmv::launch_moe_t<T>(a8, quant_x, W3d, n_expert, rows, cols, offsets, active, perm, n_pairs, x, \
+                                    xrow, kdiv, out, bias, st);                                                 \
     }
 
 #define QMV_GEMV_INSTANTIATE(T, NAME)                                                                     \

@@ -7,7 +7,9 @@
 //  k_moe_group    one block: validates the ids and sorts the n_tok*k (token,
 //                 slot) pairs by expert with a stable counting sort (one warp
 //                 per expert, ballots over the pairs in order), writing
-//                 offsets[n_expert+1] and perm[n_pairs] to the workspace.
+//                 offsets[n_expert+1], the experts that received pairs
+//                 (active[], in id order, and their count) and perm[n_pairs]
+//                 to the workspace.
 //  k_moe_gemv     (moe.cuh) the expert matvecs over grouped pairs.
 //  k_moe_combine  down form only: y[t][r] = sum over slots s, in slot order, of
 //                 gates[t][s] * (part[t*k+s][r] + bias[e][r]).
@@ -18,8 +20,8 @@
 namespace qmv {
 
 __global__ void __launch_bounds__(1024) k_moe_group(const int32_t* __restrict__ ids, int n_pairs, int n_expert,
-                                                    int* __restrict__ offsets, int* __restrict__ perm,
-                                                    unsigned* status)
+                                                    int* __restrict__ offsets, int* __restrict__ active,
+                                                    int* __restrict__ perm, unsigned* status)
 {
     __shared__ int base[1025];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
@@ -38,14 +40,16 @@ __global__ void __launch_bounds__(1024) k_moe_group(const int32_t* __restrict__ 
     }
     __syncthreads();
     if (tid == 0) {
-        int run = 0;
+        int run = 0, na = 0;
         for (int e = 0; e < n_expert; ++e) {
             const int c = base[e];
             base[e] = run;
             offsets[e] = run;
             run += c;
+            if (c > 0) active[1 + na++] = e;
         }
         offsets[n_expert] = run;   // pairs with a valid expert
+        active[0] = na;
     }
     __syncthreads();
     const uint32_t lt = (1u << lane) - 1u;
@@ -86,8 +90,8 @@ inline size_t r256(size_t v) { return (v + 255) & ~size_t(255); }
 
 #define QMV_MOE_DECL(NAME)                                                                                      \
     int NAME(bool a8, bool quant_x, const void* W3d, int n_expert, int64_t rows, int64_t cols, const int* offsets, \
-             const int* perm, int n_pairs, const void* x, size_t xrow, int kdiv, float* out, const float* bias,    \
-             cudaStream_t st);
+             const int* active, const int* perm, int n_pairs, const void* x, size_t xrow, int kdiv, float* out,     \
+             const float* bias, cudaStream_t st);
 QMV_MOE_DECL(qmv_moe_q4_0)
 QMV_MOE_DECL(qmv_moe_q5_0)
 QMV_MOE_DECL(qmv_moe_q8_0)
@@ -98,7 +102,7 @@ QMV_MOE_DECL(qmv_moe_q6_k)
 size_t qmv_moe_workspace_bytes(int64_t rows, int64_t n_pairs)
 {
     using qmv::r256;
-    return r256(1025 * 4) + r256((size_t)n_pairs * 4) + (size_t)n_pairs * (size_t)rows * 4;
+    return r256(2050 * 4) + r256((size_t)n_pairs * 4) + (size_t)n_pairs * (size_t)rows * 4;
 }
 
 // Returns 0, -2 (shape beyond the plan), -6 (launch failure).
@@ -110,10 +114,11 @@ int qmv_launch_moe(int wtype, bool a8, bool quant_x, size_t act_block_bytes, con
     const int64_t n_pairs = n_tok * k;
     if (n_pairs == 0 || rows == 0) return 0;
     uint8_t* w = static_cast<uint8_t*>(ws);
-    int* offsets = reinterpret_cast<int*>(w);
-    int* perm = reinterpret_cast<int*>(w + r256(1025 * 4));
-    float* part = reinterpret_cast<float*>(w + r256(1025 * 4) + r256((size_t)n_pairs * 4));
-    k_moe_group<<<1, 1024, 0, st>>>(ids, (int)n_pairs, n_expert, offsets, perm, status_word());
+    int* offsets = reinterpret_cast<int*>(w);            // [n_expert + 1]
+    int* active = offsets + 1025;                         // [0] = count, [1..] = expert ids
+    int* perm = reinterpret_cast<int*>(w + r256(2050 * 4));
+    float* part = reinterpret_cast<float*>(w + r256(2050 * 4) + r256((size_t)n_pairs * 4));
+    k_moe_group<<<1, 1024, 0, st>>>(ids, (int)n_pairs, n_expert, offsets, active, perm, status_word());
     if (cudaGetLastError() != cudaSuccess) return -6;
     const size_t xrow = (a8 && !quant_x) ? (size_t)(cols / (wtype == QMV_Q4_K || wtype == QMV_Q6_K ? 256 : 32)) *
                                                act_block_bytes
@@ -122,7 +127,8 @@ int qmv_launch_moe(int wtype, bool a8, bool quant_x, size_t act_block_bytes, con
     float* out = gates ? part : y;
     const float* b = gates ? nullptr : bias;
     int rc = -3;
-#define QMV_MOE_CALL(NAME) NAME(a8, quant_x, W3d, n_expert, rows, cols, offsets, perm, (int)n_pairs, x, xrow, kdiv, out, b, st)
+#define QMV_MOE_CALL(NAME) \
+    NAME(a8, quant_x, W3d, n_expert, rows, cols, offsets, active, perm, (int)n_pairs, x, xrow, kdiv, out, b, st)
     switch (wtype) {
     case QMV_Q4_0: rc = QMV_MOE_CALL(qmv_moe_q4_0); break;
     case QMV_Q5_0: rc = QMV_MOE_CALL(qmv_moe_q5_0); break;

@@ -19,6 +19,7 @@ struct MoeParams {
     GemvParams g;            // geometry of one expert's matrix; g.W = expert 0
     int64_t expert_bytes;    // rows * rb
     const int* offsets;      // [n_expert + 1] pair ranges per expert
+    const int* active;       // [0] = number of experts with pairs, [1..] their ids (grid row y -> active[1 + y])
     const int* perm;         // pair indices (t*k + s) grouped by expert, stable
     size_t xrow;             // bytes between activation rows
     int kdiv;                // activation row of pair p = p / kdiv (k: shared per token, 1: per slot)
@@ -33,7 +34,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_moe_gemv(const MoeParams mp
     using F = Fmt<T>;
     extern __shared__ __align__(128) uint8_t smem[];
     pdl_wait();   // the grouping comes from the kernel before this one
-    const int e = blockIdx.y;
+    if ((int)blockIdx.y >= mp.active[0]) return;   // uniform for the whole block
+    const int e = mp.active[1 + blockIdx.y];
     const int o0 = mp.offsets[e];
     const int cnt = mp.offsets[e + 1] - o0;
     GemvParams p = mp.g;

@@ -176,7 +176,10 @@ int qmv_matvec(int fmt, const void* W, int64_t rows, int64_t cols,
  *   fmt : QMV_FMT(QMV_Q4_K, QMV_BF16): X bf16 [m][cols]; the weights are
  *         dequantised to bf16 tiles (w rounded once from its fp32 value) and
  *         multiplied on the tensor cores with fp32 accumulation.
- *         QMV_FMT(QMV_Q4_K, QMV_Q8_K): X Q8_K blocks [m][cols/256] (W4A8).
+ *         QMV_FMT(QMV_Q4_K, QMV_Q8_K): X Q8_K blocks [m][cols/256] (W4A8):
+ *         exact per-super-block integer dots scaled in fp32, the arithmetic of
+ *         qmv_matvec, so every token's row equals its decode result bit for bit.
+ *         (The int8 tensor-core instruction kind::i8 does not exist on sm_103a.)
  *   X   : 16-byte aligned.   Y : fp32 [m][rows], overwritten.
  *   m   : >= 0.
  * ------------------------------------------------------------------------- */
@@ -250,7 +253,7 @@ int qmv_moe_matvec_noalloc(int fmt, const void* W3d, int n_expert, int64_t rows,
 /* Workspace for the calls that need scratch. */
 enum { QMV_OP_MATVEC = 1, QMV_OP_MATMUL = 2, QMV_OP_MOE = 3 };
 /* Bytes of workspace `op` needs for these sizes (n = n_tok*k for MoE: the
- * grouping, 1025 + n ints, and n*rows fp32 slot outputs).  0 if none. */
+ * grouping, 2050 + n ints, and n*rows fp32 slot outputs).  0 if none. */
 size_t qmv_workspace_size(int op, int fmt, int64_t rows, int64_t cols, int64_t n);
 /* Register a caller-owned device buffer (256-byte aligned) as the workspace of
  * the current device; NULL/0 clears it.  The library keeps the pointer only. */

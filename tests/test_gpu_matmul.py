@@ -93,3 +93,30 @@ def test_matmul_edge_cases(qmv, orc):
         qmv.qmv_matmul(qmv.FMT(Q4_K, BF16), W, rows, 300, W, Y, 1)
     assert e.value.code == qmv.ERR_SHAPE
     qmv.qmv_get_status()
+
+
+Q8_K = 7
+
+
+@pytest.mark.parametrize("rows,cols,m", [(128, 256, 1), (300, 1024, 37), (14336, 4096, 512)])
+def test_matmul_w4a8_parity(qmv, orc, rows, cols, m):
+    """W4A8 prefill (Q4_K x Q8_K): within 1e-4 of the oracle's exact integer
+    dots, and every token's row equal bit for bit to its own decode matvec."""
+    W = synth.weights(Q4_K, rows, cols, seed=12, tensor_id=rows)
+    Wd = dev(W)
+    x = synth.activations(m, cols, seed=12)
+    xq = orc.quantize_act(Q8_K, x)
+    Y = torch.full((m, rows), float("nan"), dtype=torch.float32, device="cuda")
+    qmv.qmv_matmul(qmv.FMT(Q4_K, Q8_K), Wd, rows, cols, dev(xq), Y, m)
+    Y = host(Y)
+    g = np.random.default_rng(rows)
+    rids = np.unique(np.concatenate([[0, rows - 1], g.integers(0, rows, 30)])) if rows > 512 else np.arange(rows)
+    toks = np.unique(np.concatenate([[0, m - 1], g.integers(0, m, 14)])) if m > 64 else np.arange(m)
+    yref, yabs = orc.matvec(Q4_K, Q8_K, W, rows, cols, xq[toks], len(toks), row_ids=rids)
+    assert_close(Y[np.ix_(toks, rids)], yref, yabs, what=f"w4a8 {rows}x{cols} m={m}")
+    xqd = dev(xq)
+    for t in toks[:3]:
+        y1 = torch.empty((1, rows), dtype=torch.float32, device="cuda")
+        qmv.qmv_matvec(qmv.FMT(Q4_K, Q8_K), Wd, rows, cols, xqd[t], y1, 1)
+        assert np.array_equal(host(y1)[0].view(np.uint32), Y[t].view(np.uint32))
+    qmv.qmv_get_status()
