@@ -32,6 +32,7 @@ QMV_GEMV_DECL(qmv_gemv_q8_0)
 QMV_GEMV_DECL(qmv_gemv_mxfp4)
 QMV_GEMV_DECL(qmv_gemv_q4_k)
 QMV_GEMV_DECL(qmv_gemv_q6_k)
+int qmv_gemm_mma_q4_k(bool pdl, const void* W, int64_t rows, int64_t cols, const void* X, float* Y, int m, cudaStream_t st);
 size_t qmv_moe_workspace_bytes(int64_t rows, int64_t n_pairs);
 int qmv_launch_moe(int wtype, bool a8, bool quant_x, size_t act_block_bytes, const void* W3d, int n_expert,
                    int64_t rows, int64_t cols, const int32_t* ids, const float* gates, int k, const void* x, float* y,
@@ -305,9 +306,9 @@ int qmv_matmul(int fmt, const void* W, int64_t rows, int64_t cols, const void* X
     if (!aligned(Y, 4)) return fail(QMV_ERR_ALIGN, "Y must be 4-byte aligned");
     if (!qmv::status_word()) return cuda_fail("qmv_matmul (status word)");
     if (atype == QMV_Q8_K) {
-        // W4A8: the exact integer block dots of the decode engine over every
-        // token (Y[m][rows] has the matvec's y[v][rows] layout).
-        rc = qmv_gemv_q4_k(true, false, pdl, W, rows, cols, X, Y, (int)m, static_cast<cudaStream_t>(stream));
+        // W4A8: exact per-super-block integer dots on the int8 tensor path
+        // (mma.sync), token groups of 16 (Y[m][rows] has the matvec's layout).
+        rc = qmv_gemm_mma_q4_k(pdl, W, rows, cols, X, Y, (int)m, static_cast<cudaStream_t>(stream));
         if (rc == -2) return fail(QMV_ERR_SHAPE, "cols = %lld needs more shared memory than one SM has", (long long)cols);
         if (rc) return cuda_fail("qmv_matmul");
         return ok();

@@ -491,7 +491,7 @@ __device__ __forceinline__ XView carve_xview(uint8_t* base, bool a8, int g, int 
 // quant_x the fp32 activations are quantised here with the exact steps of the
 // activation quantiser, so the staged bytes equal those staged from
 // qmv_quantize_act's output.
-template <int T>
+template <int T, bool NATURAL = false>
 __device__ void stage_xhat(uint8_t* base, bool a8, bool quant_x, const void* x, size_t xrow, const int* idx, int g,
                            int cols, int tid, int nth)
 {
@@ -520,10 +520,10 @@ __device__ void stage_xhat(uint8_t* base, bool a8, bool quant_x, const void* x, 
                 for (int k = 0; k < 8; ++k) {
                     const float4 w = xp[k];
                     const int8_t q0 = quant1(w.x, id), q1 = quant1(w.y, id), q2 = quant1(w.z, id), q3 = quant1(w.w, id);
-                    dst[staged_pos<T>(4 * k + 0)] = (uint8_t)q0;
-                    dst[staged_pos<T>(4 * k + 1)] = (uint8_t)q1;
-                    dst[staged_pos<T>(4 * k + 2)] = (uint8_t)q2;
-                    dst[staged_pos<T>(4 * k + 3)] = (uint8_t)q3;
+                    dst[NATURAL ? 4 * k + 0 : staged_pos<T>(4 * k + 0)] = (uint8_t)q0;
+                    dst[NATURAL ? 4 * k + 1 : staged_pos<T>(4 * k + 1)] = (uint8_t)q1;
+                    dst[NATURAL ? 4 * k + 2 : staged_pos<T>(4 * k + 2)] = (uint8_t)q2;
+                    dst[NATURAL ? 4 * k + 3 : staged_pos<T>(4 * k + 3)] = (uint8_t)q3;
                     s += q0 + q1 + q2 + q3;
                 }
                 d[i] = __half2float(__float2half_rn(dd));   // Q8_0 keeps its scale in fp16
@@ -567,7 +567,7 @@ __device__ void stage_xhat(uint8_t* base, bool a8, bool quant_x, const void* x, 
                 }
                 uint8_t* dst = codes + (size_t)i * 32;   // vector v, block b: i = v*nb + b
 #pragma unroll
-                for (int k = 0; k < 32; ++k) dst[staged_pos<T>(k)] = q[k];
+                for (int k = 0; k < 32; ++k) dst[NATURAL ? k : staged_pos<T>(k)] = q[k];
                 d[i] = half_bits_to_float(h[0]);
                 sum[i] = s;
             }
@@ -600,6 +600,14 @@ __device__ void stage_xhat(uint8_t* base, bool a8, bool quant_x, const void* x, 
             }
         }
     }
+}
+
+// A8 staging in natural element order (the tensor-core engine's B fragments).
+template <int T>
+__device__ __forceinline__ void stage_xhat_a8_natural(uint8_t* base, bool quant_x, const void* x, size_t xrow, int g,
+                                                      int cols, int tid, int nth)
+{
+    stage_xhat<T, true>(base, true, quant_x, x, xrow, nullptr, g, cols, tid, nth);
 }
 
 // Per-32 sums of staged fp32 activations (A32 Q4_K), in a fixed order; run

@@ -55,6 +55,9 @@ struct GemvParams {
     int n_chunks;
     int stages;
     int rpw;            // rows per consumer warp per tile (1, 2 or 4)
+    int wk;             // tensor-core engine: K-splits per 16-row group (1, 2, 4 or 8)
+    int contig;         // whole rows per stage: one bulk copy moves the tile's consecutive rows
+    uint32_t stage_bytes;
     int quant_x;        // A8 only: x is fp32, quantised while staging
     uint32_t seg_cap;   // bytes per row slot of a stage
     uint32_t xhat_bytes;
@@ -71,26 +74,48 @@ __device__ __forceinline__ int64_t ceil16(int64_t v) { return (v + 15) & ~int64_
 // the consumers.
 template <int BB>
 __device__ __forceinline__ void gemv_produce(const GemvParams& p, int64_t tile, int chunk, uint8_t* buf,
-                                             uint64_t* bar)
+                                             uint64_t* bar, int tr = 0)
 {
     const int lane = threadIdx.x & 31;
-    const int tr = kConsumerWarps * p.rpw;
-    const int64_t r = tile * tr + lane;
+    if (tr == 0) tr = kConsumerWarps * p.rpw;
     const int64_t lim = floor16(p.total);
+    if (p.contig) {
+        // Rows r0 .. r1-1 are one byte range: copy its 16-byte aligned superset
+        // at once (the ragged end of the matrix with plain loads).
+        if (lane == 0) {
+            const int64_t r0 = tile * tr;
+            const int64_t r1 = min(p.rows, r0 + tr);
+            const int64_t s0 = r0 * p.rb, e = r1 * p.rb;
+            const int64_t a0 = floor16(s0);
+            const int64_t ea = min(ceil16(e), lim);
+            const uint32_t bytes = ea > a0 ? (uint32_t)(ea - a0) : 0u;
+            for (int64_t k = max(lim, a0); k < e; ++k) buf[k - a0] = p.W[k];
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive_expect_tx(bar, bytes);
+            if (bytes) bulk_g2s(buf, p.W + a0, bytes, bar);
+        }
+        __syncwarp();
+        return;
+    }
     const int c0 = chunk * p.kb;
     const int c1 = min(p.nb, c0 + p.kb);
-    uint32_t bytes = 0;
-    int64_t a = 0;
-    uint8_t* slot = buf + (size_t)lane * p.seg_cap;
-    if (lane < tr && r < p.rows) {
-        const int64_t s = r * p.rb + (int64_t)c0 * BB;
-        const int64_t e = r * p.rb + (int64_t)c1 * BB;
-        a = floor16(s);
-        const int64_t ea = min(ceil16(e), lim);
-        if (ea > a) bytes = (uint32_t)(ea - a);
-        for (int64_t i = max(lim, a); i < e; ++i) slot[i - a] = p.W[i];   // only the matrix's last row
+    uint32_t bytes[4] = {0, 0, 0, 0};   // up to 128 rows: 4 per lane
+    int64_t a[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int i = lane + 32 * j;
+        const int64_t r = tile * tr + i;
+        if (i < tr && r < p.rows) {
+            const int64_t s = r * p.rb + (int64_t)c0 * BB;
+            const int64_t e = r * p.rb + (int64_t)c1 * BB;
+            a[j] = floor16(s);
+            const int64_t ea = min(ceil16(e), lim);
+            if (ea > a[j]) bytes[j] = (uint32_t)(ea - a[j]);
+            uint8_t* slot = buf + (size_t)i * p.seg_cap;
+            for (int64_t k = max(lim, a[j]); k < e; ++k) slot[k - a[j]] = p.W[k];   // only the matrix's last row
+        }
     }
-    uint32_t total = bytes;
+    uint32_t total = bytes[0] + bytes[1] + bytes[2] + bytes[3];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
     // Order this buffer's earlier generic-proxy accesses (consumer reads,
@@ -99,7 +124,9 @@ __device__ __forceinline__ void gemv_produce(const GemvParams& p, int64_t tile, 
     __syncwarp();
     if (lane == 0) mbar_arrive_expect_tx(bar, total);
     __syncwarp();
-    if (bytes) bulk_g2s(slot, p.W + a, bytes, bar);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        if (bytes[j]) bulk_g2s(buf + (size_t)(lane + 32 * j) * p.seg_cap, p.W + a[j], bytes[j], bar);
 }
 
 // Consumer: rows r0 + j (j < RIF) of one warp, one K-chunk, all vectors.
@@ -113,8 +140,9 @@ __device__ __forceinline__ void gemv_rows(const GemvParams& p, const XView& X, c
     const uint8_t* rowp[RIF];
 #pragma unroll
     for (int j = 0; j < RIF; ++j)
-        rowp[j] = slot0 + (size_t)j * p.seg_cap +
-                  (((uint32_t)(r0 + j) * (uint32_t)p.rb + (uint32_t)c0 * (uint32_t)F::BB) & 15u);
+        rowp[j] = p.contig ? slot0 + (size_t)j * p.rb
+                           : slot0 + (size_t)j * p.seg_cap +
+                                 (((uint32_t)(r0 + j) * (uint32_t)p.rb + (uint32_t)c0 * (uint32_t)F::BB) & 15u);
     const int u0 = c0 * F::UPB, u1 = c1 * F::UPB;
 #pragma unroll 1
     for (int u = u0 + lane; u < u1; u += 32) {
@@ -187,7 +215,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_gemv(const GemvParams p)
     uint8_t* xs = smem + 256;
     uint8_t* stage0 = xs + ((p.xhat_bytes + 127) & ~127u);
     const int tr = kConsumerWarps * p.rpw;
-    const uint32_t stage_bytes = p.seg_cap * (uint32_t)tr;
+    const uint32_t stage_bytes = p.stage_bytes;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t n_tiles = (p.rows + tr - 1) / tr;
@@ -271,7 +299,10 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_gemv(const GemvParams p)
 #pragma unroll
                     for (int v = 0; v < NV; ++v) acc[j][v] = 0.f;
             }
-            gemv_rows<T, A8, NV, RIF>(p, X, buf + (size_t)(warp * p.rpw + g) * p.seg_cap, r0, nrows, c0, c1, acc);
+            const uint8_t* slot0 = p.contig ? buf + (((uint32_t)(tile * tr) * (uint32_t)p.rb) & 15u) +
+                                                  (size_t)(warp * p.rpw + g) * p.rb
+                                            : buf + (size_t)(warp * p.rpw + g) * p.seg_cap;
+            gemv_rows<T, A8, NV, RIF>(p, X, slot0, r0, nrows, c0, c1, acc);
             if (chunk == p.n_chunks - 1) {
                 const int row = RIF == 4 ? (lane >> 3) : (RIF == 2 ? (lane >> 4) : 0);
                 const bool writer = (lane & (32 / RIF - 1)) == 0;
@@ -296,7 +327,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_gemv(const GemvParams p)
 
 // ---- host side -------------------------------------------------------------------
 struct GemvPlan {
-    int kb, n_chunks, stages, group, grid, rpw;
+    int kb, n_chunks, stages, group, grid, rpw, wk, contig;
+    uint32_t stage_bytes;
     uint32_t seg_cap, xhat_bytes, smem;
 };
 

@@ -177,9 +177,10 @@ int qmv_matvec(int fmt, const void* W, int64_t rows, int64_t cols,
  *         dequantised to bf16 tiles (w rounded once from its fp32 value) and
  *         multiplied on the tensor cores with fp32 accumulation.
  *         QMV_FMT(QMV_Q4_K, QMV_Q8_K): X Q8_K blocks [m][cols/256] (W4A8):
- *         exact per-super-block integer dots scaled in fp32, the arithmetic of
- *         qmv_matvec, so every token's row equals its decode result bit for bit.
- *         (The int8 tensor-core instruction kind::i8 does not exist on sm_103a.)
+ *         exact int32 sub-block dots on the int8 tensor path (mma.sync
+ *         m16n8k32; tcgen05 has no int8 kind on sm_103a), sub-block scales
+ *         applied in integers, fp32 accumulation per super-block.  Agrees with
+ *         the W4A8 decode of each token within the accuracy bar above.
  *   X   : 16-byte aligned.   Y : fp32 [m][rows], overwritten.
  *   m   : >= 0.
  * ------------------------------------------------------------------------- */
