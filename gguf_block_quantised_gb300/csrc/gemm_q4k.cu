@@ -13,35 +13,39 @@
 //               128-byte swizzle, the UMMA K-major canonical layout)
 //   warp 1      TMEM owner (alloc/free) and the single-thread MMA issuer
 //   warp 2      TMA producer of raw Q4_K super-block tiles W[128 rows][144 B]
-//   warps 4-7   dequantisers: raw super-block -> four bf16 A tiles
+//   warps 4-11  dequantisers: raw super-block -> four bf16 A tiles
 //               [128 rows][64 k] written in the 128-byte swizzled layout
-//   warps 8-11  epilogue: TMEM -> registers -> Y, one 128-byte row segment
+//               (packed fp32x2 arithmetic, two weights per instruction)
+//   warps 12-15 epilogue: TMEM -> registers -> Y, one 128-byte row segment
 //               per column, so every store is coalesced
-// MMA: M = 128 weight rows, N = 256 tokens, K = 16 per instruction, fp32
-// accumulator in TMEM, double-buffered (2 x 256 columns) so the epilogue of
-// one tile overlaps the MMAs of the next.  Every mbarrier wait is bounded;
+// MMA: M = 128 weight rows, N = BN tokens (256, or 128 when 256-token tiles
+// would leave SMs idle), K = 16 per instruction, fp32 accumulator in TMEM,
+// double-buffered (2 x BN columns) so the epilogue of one tile overlaps the
+// MMAs of the next.  Every mbarrier wait is bounded;
 // on a timeout the kernel flags the status word, unwinds and frees its TMEM.
 #include <cuda.h>
 
 #include "formats.cuh"
+#include "mma_units.cuh"
 #include "runtime.cuh"
 #include "tc.cuh"
 
 namespace qmv {
 
 namespace gq {
-constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int BM = 128, BK = 64;
 constexpr int SX = 4, SA = 3, SR = 2;
-constexpr int X_BYTES = BN * BK * 2;    // 32768
-constexpr int A_BYTES = BM * BK * 2;    // 16384
-constexpr int R_BYTES = BM * 144;       // 18432
+constexpr int X_BYTES_MAX = 256 * BK * 2;   // 32768 (BN = 256)
+constexpr int A_BYTES = BM * BK * 2;        // 16384
+constexpr int R_BYTES = BM * 144;           // 18432
 constexpr int OFF_X = 0;
-constexpr int OFF_A = OFF_X + SX * X_BYTES;
+constexpr int OFF_A = OFF_X + SX * X_BYTES_MAX;
 constexpr int OFF_R = OFF_A + SA * A_BYTES;
 constexpr int OFF_BAR = OFF_R + SR * R_BYTES;
 constexpr int N_BARS = 2 * SX + 2 * SR + 2 * SA + 4;
 constexpr int SMEM = OFF_BAR + N_BARS * 8 + 16 + 1024;   // + alignment slack
-constexpr int THREADS = 384;
+constexpr int DEQ_WARPS = 8;                // warps 4..11
+constexpr int THREADS = 512;                // 16 warps
 constexpr uint32_t TMEM_COLS = 512;
 }  // namespace gq
 
@@ -53,40 +57,57 @@ struct GemmArgs {
     unsigned* status;
 };
 
+// Two fp32 values in one 64-bit register for the packed f32x2 instructions.
+__device__ __forceinline__ uint64_t pk2(float lo, float hi)
+{
+    return ((uint64_t)__float_as_uint(hi) << 32) | __float_as_uint(lo);
+}
+
+// (D*q - M) for the two codes packed in bytes j0, j1 of `codes` (each 0..15),
+// exactly as two fp32 fused multiply-adds: 0x4B0000qq is the float 2^23 + q,
+// so subtracting 2^23 gives q exactly.
+__device__ __forceinline__ uint32_t dq2_bf16(uint32_t codes, uint32_t sel, uint64_t D2, uint64_t negM2)
+{
+    const uint32_t f0 = __byte_perm(codes, 0x4B000000u, sel & 0xffffu);          // bytes: code, 0, 0, 0x4B
+    const uint32_t f1 = __byte_perm(codes, 0x4B000000u, sel >> 16);
+    uint64_t v = ((uint64_t)f1 << 32) | f0, q, w;
+    const uint64_t two23 = pk2(-8388608.f, -8388608.f);
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(q) : "l"(v), "l"(two23));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(w) : "l"(D2), "l"(q), "l"(negM2));
+    const __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float((uint32_t)w), __uint_as_float((uint32_t)(w >> 32)));
+    return *reinterpret_cast<const uint32_t*>(&b);
+}
+
 // Dequantise sub-blocks 2c, 2c+1 of the raw super-block tile into a bf16 A
-// tile (128 rows x 64 k, K-major, 128-byte swizzle).  128 threads; thread t
-// handles rows r = t and 8-k groups jj = 0..3 of both sub-blocks.
+// tile (128 rows x 64 k, K-major, 128-byte swizzle): w = RN_fp32(d*sc*q - dmin*m)
+// (d*sc and dmin*m are exact products), then rounded to bf16.  256 threads:
+// thread t handles row t % 128 and the 8-k groups jj = 2*(t / 128) + {0, 1}
+// of both sub-blocks.
 __device__ __forceinline__ void dequant_q4k_tile(const uint8_t* raw, uint8_t* A, int c, int t)
 {
-    const int r = t;
+    const int r = t & 127;
     const uint8_t* rp = raw + r * 144;
     const uint4 h = *reinterpret_cast<const uint4*>(rp);
-    int sc0, m0, sc1, m1;
-    Fmt<QMV_Q4_K>::scale_min(h.y, h.z, h.w, 2 * c, sc0, m0);
-    Fmt<QMV_Q4_K>::scale_min(h.y, h.z, h.w, 2 * c + 1, sc1, m1);
+    const Q4kScales ks = q4k_scales(h.y, h.z, h.w);
     const float d = half_bits_to_float(h.x & 0xffffu), dmin = half_bits_to_float(h.x >> 16);
-    const float D0 = d * (float)sc0, M0 = dmin * (float)m0;   // exact
-    const float D1 = d * (float)sc1, M1 = dmin * (float)m1;
+    const float D0 = d * (float)ks.sc(2 * c), M0 = dmin * (float)ks.m(2 * c);       // exact
+    const float D1 = d * (float)ks.sc(2 * c + 1), M1 = dmin * (float)ks.m(2 * c + 1);
+    const uint64_t D0x2 = pk2(D0, D0), nM0x2 = pk2(-M0, -M0), D1x2 = pk2(D1, D1), nM1x2 = pk2(-M1, -M1);
     uint8_t* rowA = A + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-        const uint2 q = *reinterpret_cast<const uint2*>(rp + 16 + 32 * c + 8 * jj);
-        const uint32_t qw[2] = {q.x, q.y};
+    for (int i = 0; i < 2; ++i) {
+        const int jj = 2 * (t >> 7) + i;
+        const uint2 qv = *reinterpret_cast<const uint2*>(rp + 16 + 32 * c + 8 * jj);
         uint32_t lo[4], hi[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const uint32_t w = qw[k >> 1];
-            const int sh = (k & 1) * 16;
-            // bytes 2k', 2k'+1 of the 8: low nibbles -> sub-block 2c, high -> 2c+1
-            const uint32_t b0 = (w >> sh) & 0xffu, b1 = (w >> (sh + 8)) & 0xffu;
-            const float l0 = __int_as_float(0x4B000000 | (b0 & 15u)) - 8388608.f;
-            const float l1 = __int_as_float(0x4B000000 | (b1 & 15u)) - 8388608.f;
-            const float g0 = __int_as_float(0x4B000000 | (b0 >> 4)) - 8388608.f;
-            const float g1 = __int_as_float(0x4B000000 | (b1 >> 4)) - 8388608.f;
-            const __nv_bfloat162 pl = __floats2bfloat162_rn(__fmaf_rn(D0, l0, -M0), __fmaf_rn(D0, l1, -M0));
-            const __nv_bfloat162 ph = __floats2bfloat162_rn(__fmaf_rn(D1, g0, -M1), __fmaf_rn(D1, g1, -M1));
-            lo[k] = *reinterpret_cast<const uint32_t*>(&pl);
-            hi[k] = *reinterpret_cast<const uint32_t*>(&ph);
+        for (int k = 0; k < 2; ++k) {
+            const uint32_t w = k ? qv.y : qv.x;                 // codes of 4 consecutive k
+            const uint32_t l4 = w & 0x0f0f0f0fu, h4 = (w >> 4) & 0x0f0f0f0fu;
+            // selectors: byte j of the codes word, then bytes 5, 6, 7 of 0x4B000000
+            lo[2 * k] = dq2_bf16(l4, 0x76517650u, D0x2, nM0x2);
+            lo[2 * k + 1] = dq2_bf16(l4, 0x76537652u, D0x2, nM0x2);
+            hi[2 * k] = dq2_bf16(h4, 0x76517650u, D1x2, nM1x2);
+            hi[2 * k + 1] = dq2_bf16(h4, 0x76537652u, D1x2, nM1x2);
         }
         const int jl = jj, jh = 4 + jj;   // 16-byte chunks of the 128-byte row
         *reinterpret_cast<uint4*>(rowA + ((jl ^ (r & 7)) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
@@ -94,10 +115,12 @@ __device__ __forceinline__ void dequant_q4k_tile(const uint8_t* raw, uint8_t* A,
     }
 }
 
+template <int BN>
 __global__ void __launch_bounds__(gq::THREADS, 1)
     k_gemm_q4k_bf16(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, const GemmArgs a)
 {
     using namespace gq;
+    constexpr int X_BYTES = BN * BK * 2;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
@@ -121,8 +144,8 @@ __global__ void __launch_bounds__(gq::THREADS, 1)
 
     if (tid == 0) {
         for (int i = 0; i < SX; ++i) { mbar_init(&xf[i], 1); mbar_init(&xe[i], 1); }
-        for (int i = 0; i < SR; ++i) { mbar_init(&rf[i], 1); mbar_init(&re[i], 4); }
-        for (int i = 0; i < SA; ++i) { mbar_init(&af[i], 4); mbar_init(&ae[i], 1); }
+        for (int i = 0; i < SR; ++i) { mbar_init(&rf[i], 1); mbar_init(&re[i], DEQ_WARPS); }
+        for (int i = 0; i < SA; ++i) { mbar_init(&af[i], DEQ_WARPS); mbar_init(&ae[i], 1); }
         for (int i = 0; i < 2; ++i) { mbar_init(&accf[i], 1); mbar_init(&acce[i], 4); }
         *abort_flag = 0;
         fence_barrier_init();
@@ -206,7 +229,7 @@ __global__ void __launch_bounds__(gq::THREADS, 1)
                 mma_commit(&accf[buf]);
             }
         }
-    } else if (warp >= 4 && warp < 8) {
+    } else if (warp >= 4 && warp < 4 + DEQ_WARPS) {
         // ---- dequantisers
         const int t0 = tid - 128;
         int sr = 0, sa = 0;
@@ -231,7 +254,7 @@ __global__ void __launch_bounds__(gq::THREADS, 1)
             }
             if (bad) { fail(); break; }
         }
-    } else if (warp >= 8) {
+    } else if (warp >= 4 + DEQ_WARPS) {
         // ---- epilogue: lane quarter (warp % 4) of the 128 TMEM lanes
         const int q = warp & 3;
         int local = 0;
@@ -310,10 +333,7 @@ int qmv_launch_gemm_q4k_bf16(const void* W, int64_t rows, int64_t cols, const vo
     using namespace qmv;
     if (rows == 0 || m == 0) return 0;
     const uint64_t rb = (uint64_t)(cols / 256) * 144;
-    CUtensorMap tmX, tmW;
-    if (!make_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, (uint64_t)cols, (uint64_t)m, (uint64_t)cols * 2,
-                      gq::BK, gq::BN, CU_TENSOR_MAP_SWIZZLE_128B))
-        return -8;
+    CUtensorMap tmW;
     if (!make_tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, rb, (uint64_t)rows, rb, 144, gq::BM,
                       CU_TENSOR_MAP_SWIZZLE_NONE))
         return -8;
@@ -323,9 +343,17 @@ int qmv_launch_gemm_q4k_bf16(const void* W, int64_t rows, int64_t cols, const vo
     a.m = (int)m;
     a.Y = Y;
     a.status = status_word();
-    auto* k = &k_gemm_q4k_bf16;
+    // 256-token tiles unless they cannot even give every SM one tile.
+    const int64_t n_rt = (rows + gq::BM - 1) / gq::BM;
+    const bool narrow = n_rt * ((m + 255) / 256) < (int64_t)num_sms();
+    const int BN = narrow ? 128 : 256;
+    CUtensorMap tmX;
+    if (!make_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, (uint64_t)cols, (uint64_t)m, (uint64_t)cols * 2,
+                      gq::BK, BN, CU_TENSOR_MAP_SWIZZLE_128B))
+        return -8;
+    auto* k = narrow ? &k_gemm_q4k_bf16<128> : &k_gemm_q4k_bf16<256>;
     prepare_kernel(k, gq::THREADS, gq::SMEM);
-    const int64_t n_tiles = ((rows + gq::BM - 1) / gq::BM) * ((m + gq::BN - 1) / gq::BN);
+    const int64_t n_tiles = n_rt * ((m + BN - 1) / BN);
     const int grid = (int)std::min<int64_t>(n_tiles, num_sms());
     return launch_ex(k, dim3(grid), dim3(gq::THREADS), gq::SMEM, st, pdl, tmX, tmW, a) == cudaSuccess ? 0 : -6;
 }
