@@ -350,55 +350,64 @@ def prefill_leg(q, torch, stream, tflops_peak):
 def moe_leg(q, torch, stream, hbm):
     """gpt-oss-20B-shaped MoE layer: 32 MXFP4 experts, gate_up 5760x2880 (up
     form, x shared by the 4 slots) then down 2880x2880 (per-slot inputs,
-    gate-weighted), fp32 biases, top-4 of N(0,1) router logits, activations
-    quantised to Q8_0 in the kernels.  Metric: distinct expert weight bytes
-    read per layer / time."""
+    gate-weighted), fp32 biases, top-4 of N(0,1) router logits.  Two paths:
+    W4A8 (fp32 activations quantised to Q8_0 inside the grouped matvec) and
+    bf16 activations through the grouped tensor-core GEMM.  Metric: distinct
+    expert weight bytes read per layer / time, and useful TFLOP/s."""
     E, k = 32, 4
     Wgu = torch.from_numpy(synth.weights(MXFP4, E * 5760, 2880, seed=5, tensor_id=1)).cuda()
     Wd = torch.from_numpy(synth.weights(MXFP4, E * 2880, 2880, seed=5, tensor_id=2)).cuda()
     bgu = torch.from_numpy(synth.bias(E, 5760, seed=5)).cuda()
     bd = torch.from_numpy(synth.bias(E, 2880, seed=5, tensor_id=2001)).cuda()
-    fmt = q.FMT(MXFP4, Q8_0) | q.FLAG_QUANTIZE_X
-    res = {}
+    paths = {"w4a8": (q.FMT(MXFP4, Q8_0) | q.FLAG_QUANTIZE_X, torch.float32),
+             "bf16_gemm": (q.FMT(MXFP4, BF16), torch.bfloat16)}
+    out = {}
     ws = None
-    for n_tok in (1, 64, 1024):
-        # four routings rotate, so the experts one launch reads were not just read
-        routes = [synth.router(n_tok, E, k, seed=6 + r) for r in range(4)]
-        x = torch.randn(n_tok, 2880, device="cuda")
-        h = torch.randn(n_tok, k, 2880, device="cuda")
-        y1 = torch.empty(n_tok, k, 5760, device="cuda")
-        y2 = torch.empty(n_tok, 2880, device="cuda")
-        need = q.qmv_workspace_size(q.OP_MOE, fmt, 5760, 2880, n_tok * k)
-        if ws is None or ws.numel() < need:
-            ws = torch.empty(need, dtype=torch.uint8, device="cuda")
-        q.qmv_set_workspace(ws, ws.numel())
-        calls = []
-        for ids_np, gates_np in routes:
-            ids, gates = torch.from_numpy(ids_np).cuda(), torch.from_numpy(gates_np).cuda()
+    for name, (fmt, xdt) in paths.items():
+        res = {}
+        for n_tok in (1, 64, 1024):
+            # four routings rotate, so the experts one launch reads were not just read
+            routes = [synth.router(n_tok, E, k, seed=6 + r) for r in range(4)]
+            x = torch.randn(n_tok, 2880, device="cuda").to(xdt)
+            h = torch.randn(n_tok, k, 2880, device="cuda").to(xdt)
+            y1 = torch.empty(n_tok, k, 5760, device="cuda")
+            y2 = torch.empty(n_tok, 2880, device="cuda")
+            need = q.qmv_workspace_size(q.OP_MOE, fmt, 5760, 2880, n_tok * k)
+            if ws is None or ws.numel() < need:
+                ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+            q.qmv_set_workspace(ws, ws.numel())
+            calls = []
+            for ids_np, gates_np in routes:
+                ids, gates = torch.from_numpy(ids_np).cuda(), torch.from_numpy(gates_np).cuda()
 
-            def layer(s, ids=ids, gates=gates):
-                q.qmv_moe_matvec(fmt, Wgu, E, 5760, 2880, ids, None, k, x, y1, n_tok, bgu, s.cuda_stream)
-                q.qmv_moe_matvec(fmt, Wd, E, 2880, 2880, ids, gates, k, h, y2, n_tok, bd, s.cuda_stream)
-            calls.append(layer)
-        reps = 20 if n_tok >= 1024 else 100
-        ms = time_rotating(torch, stream, calls, reps)
-        used = float(np.mean([len(np.unique(r[0])) for r in routes]))
-        wbytes = used * (5760 + 2880) * synth.row_bytes(MXFP4, 2880)
-        flop = 2.0 * n_tok * k * (5760 + 2880) * 2880
-        res[f"tok{n_tok}"] = {"ms": ms, "experts_used": used, "weight_bytes": int(wbytes),
-                              "weight_gbs": wbytes / (ms / 1e3) / 1e9, "frac_of_hbm": wbytes / (ms / 1e3) / 1e9 / hbm,
-                              "tflops": flop / (ms / 1e3) / 1e12}
+                def layer(s, ids=ids, gates=gates, fmt=fmt, x=x, h=h, y1=y1, y2=y2, n_tok=n_tok):
+                    q.qmv_moe_matvec(fmt, Wgu, E, 5760, 2880, ids, None, k, x, y1, n_tok, bgu, s.cuda_stream)
+                    q.qmv_moe_matvec(fmt, Wd, E, 2880, 2880, ids, gates, k, h, y2, n_tok, bd, s.cuda_stream)
+                calls.append(layer)
+            reps = 20 if n_tok >= 1024 else 100
+            ms = time_rotating(torch, stream, calls, reps)
+            used = float(np.mean([len(np.unique(r[0])) for r in routes]))
+            wbytes = used * (5760 + 2880) * synth.row_bytes(MXFP4, 2880)
+            flop = 2.0 * n_tok * k * (5760 + 2880) * 2880
+            res[f"tok{n_tok}"] = {"ms": ms, "experts_used": used, "weight_bytes": int(wbytes),
+                                  "weight_gbs": wbytes / (ms / 1e3) / 1e9,
+                                  "frac_of_hbm": wbytes / (ms / 1e3) / 1e9 / hbm,
+                                  "tflops": flop / (ms / 1e3) / 1e12}
+        out[name] = res
     q.qmv_set_workspace(None, 0)
     q.qmv_get_status(stream)
-    return {"metric": "MoE layer (gate_up + down) expert weight GB/s", "unit": "GB/s", "by_tokens": res,
-            "path": "grouped per-expert matvec (k_moe_group + k_moe_gemv + k_moe_combine) for every token count"}
+    return {"metric": "MoE layer (gate_up + down) expert weight GB/s", "unit": "GB/s", "by_path": out,
+            "paths": {"w4a8": "k_moe_group + k_moe_gemv (dp4a, grouped per expert) + k_moe_combine",
+                      "bf16_gemm": "k_moe_group + k_moe_tiles + k_moe_gather + k_moe_gemm_mxfp4_bf16 (tcgen05) "
+                                   "+ k_moe_combine"}}
 
 
 def run_probe(spec):
     """Single-kernel runs for profiling (ncu captures).  Specs:
       gemv:T:rows:cols:atype:n_vec   qmv_matvec on synthetic weights (atype 8 = fp32)
       gemm:rows:cols:m               qmv_matmul, Q4_K x bf16
-      moe:n_tok                      one gpt-oss-shaped MoE layer (gate_up + down)
+      moe:n_tok[:atype]              one gpt-oss-shaped MoE layer (gate_up + down); atype 3 = Q8_0
+                                     quantised in-kernel (default), 9 = bf16 (grouped tensor-core GEMM)
     Each runs its call five times and prints the event-timed mean of the last three."""
     import torch
     import gguf_block_quantised_gb300 as q
@@ -426,7 +435,7 @@ def run_probe(spec):
         call = lambda: q.qmv_matmul(q.FMT(Q4_K, BF16), W, rows, cols, X, Y, m)
         nbytes, what = 2 * m * rows * cols / 1e3, "TFLOP/s"
     elif kind == "moe":
-        (n_tok,) = a
+        n_tok, at = (a + [Q8_0])[:2]
         E, k = 32, 4
         Wgu = torch.from_numpy(synth.weights(MXFP4, E * 5760, 2880, seed=5, tensor_id=1)).cuda()
         Wd = torch.from_numpy(synth.weights(MXFP4, E * 2880, 2880, seed=5, tensor_id=2)).cuda()
@@ -434,11 +443,12 @@ def run_probe(spec):
         bd = torch.from_numpy(synth.bias(E, 2880, seed=5, tensor_id=2001)).cuda()
         ids_np, gates_np = synth.router(n_tok, E, k, seed=6)
         ids, gates = torch.from_numpy(ids_np).cuda(), torch.from_numpy(gates_np).cuda()
-        x = torch.randn(n_tok, 2880, device="cuda")
-        h = torch.randn(n_tok, k, 2880, device="cuda")
+        xdt = torch.bfloat16 if at == BF16 else torch.float32
+        x = torch.randn(n_tok, 2880, device="cuda").to(xdt)
+        h = torch.randn(n_tok, k, 2880, device="cuda").to(xdt)
         y1 = torch.empty(n_tok, k, 5760, device="cuda")
         y2 = torch.empty(n_tok, 2880, device="cuda")
-        fmt = q.FMT(MXFP4, Q8_0) | q.FLAG_QUANTIZE_X
+        fmt = q.FMT(MXFP4, BF16) if at == BF16 else q.FMT(MXFP4, Q8_0) | q.FLAG_QUANTIZE_X
         ws = torch.empty(q.qmv_workspace_size(q.OP_MOE, fmt, 5760, 2880, n_tok * k), dtype=torch.uint8, device="cuda")
         q.qmv_set_workspace(ws, ws.numel())
 

@@ -33,10 +33,10 @@ QMV_GEMV_DECL(qmv_gemv_mxfp4)
 QMV_GEMV_DECL(qmv_gemv_q4_k)
 QMV_GEMV_DECL(qmv_gemv_q6_k)
 int qmv_gemm_mma_q4_k(bool pdl, const void* W, int64_t rows, int64_t cols, const void* X, float* Y, int m, cudaStream_t st);
-size_t qmv_moe_workspace_bytes(int64_t rows, int64_t n_pairs);
-int qmv_launch_moe(int wtype, bool a8, bool quant_x, size_t act_block_bytes, const void* W3d, int n_expert,
-                   int64_t rows, int64_t cols, const int32_t* ids, const float* gates, int k, const void* x, float* y,
-                   int64_t n_tok, const float* bias, void* ws, cudaStream_t st);
+size_t qmv_moe_workspace_bytes(bool bf16, int64_t rows, int64_t cols, int64_t n_pairs);
+int qmv_launch_moe(int wtype, bool a8, bool quant_x, bool bf16, size_t act_block_bytes, const void* W3d,
+                   int n_expert, int64_t rows, int64_t cols, const int32_t* ids, const float* gates, int k,
+                   const void* x, float* y, int64_t n_tok, const float* bias, void* ws, cudaStream_t st);
 int qmv_launch_gemm_q4k_bf16(const void* W, int64_t rows, int64_t cols, const void* X, float* Y, int64_t m, bool pdl,
                              cudaStream_t st);
 
@@ -149,6 +149,65 @@ struct Workspace {
 };
 std::mutex g_ws_mu;
 Workspace g_ws[qmv::kMaxDevices];
+
+// What the argument checks of the MoE calls settle.
+struct MoeCall {
+    int wtype = 0;
+    bool a8 = false, quant_x = false, bf16 = false;
+    bool empty = false;   // nothing to compute: return QMV_OK
+    size_t need = 0;      // bytes of scratch
+};
+
+// The checks both MoE entry points share.  Activations: F32, the paired 8-bit
+// blocks (optionally quantised in-kernel), or -- MXFP4 experts only -- BF16
+// rows for the grouped tensor-core GEMM.
+int moe_check(const char* name, int fmt, const void* W3d, int n_expert, int64_t rows, int64_t cols,
+              const int32_t* ids, const float* gates, int k, const void* x, float* y, int64_t n_tok,
+              const float* bias, MoeCall& c)
+{
+    if (fmt & ~(0xffff | QMV_FLAG_QUANTIZE_X)) return fail(QMV_ERR_INVALID_ARG, "unknown flags 0x%x", fmt & ~0xffff);
+    c.quant_x = (fmt & QMV_FLAG_QUANTIZE_X) != 0;
+    c.wtype = fmt & 0xff;
+    const int atype = (fmt >> 8) & 0xff;
+    c.bf16 = atype == QMV_BF16 && c.wtype == QMV_MXFP4;
+    if (is_weight_type(c.wtype) && atype != QMV_F32 && atype != paired_act(c.wtype) && !c.bf16)
+        return fail(QMV_ERR_UNSUPPORTED, "%s: %s experts take F32 or %s activations%s (got %s)", name,
+                    type_name(c.wtype), type_name(paired_act(c.wtype)), c.wtype == QMV_MXFP4 ? " or BF16" : "",
+                    type_name(atype));
+    int rc = check_weights(c.wtype, W3d, rows, cols);
+    if (rc) return rc;
+    if (c.quant_x && (atype == QMV_F32 || c.bf16))
+        return fail(QMV_ERR_INVALID_ARG, "QMV_FLAG_QUANTIZE_X needs an 8-bit activation type (Q8_0 or Q8_K)");
+    if (n_expert < 1 || n_expert > 1024) return fail(QMV_ERR_INVALID_ARG, "n_expert must be in 1..1024 (got %d)", n_expert);
+    if (k < 1 || k > 64) return fail(QMV_ERR_INVALID_ARG, "k must be in 1..64 (got %d)", k);
+    if (n_tok < 0 || n_tok * k > (int64_t)1 << 24)
+        return fail(QMV_ERR_INVALID_ARG, "n_tok must be >= 0 with n_tok*k <= 16777216");
+    if (c.bf16 && rows > (int64_t)1 << 30) return fail(QMV_ERR_SHAPE, "rows must be below 2^30");
+    c.empty = n_tok == 0 || rows == 0;
+    if (c.empty) return QMV_OK;
+    if (!ids || !x || !y) return fail(QMV_ERR_INVALID_ARG, "ids, x and y must not be NULL");
+    c.a8 = atype != QMV_F32 && !c.bf16;
+    const int xal = (c.a8 && !c.quant_x) ? 4 : 16;
+    if (!aligned(x, xal)) return fail(QMV_ERR_ALIGN, "x must be %d-byte aligned", xal);
+    if (!aligned(ids, 4) || !aligned(y, 4) || (gates && !aligned(gates, 4)) || (bias && !aligned(bias, 4)))
+        return fail(QMV_ERR_ALIGN, "ids, gates, bias and y must be 4-byte aligned");
+    c.need = qmv_moe_workspace_bytes(c.bf16, rows, cols, n_tok * k);
+    return QMV_OK;
+}
+
+int moe_run(const char* name, const MoeCall& c, const void* W3d, int n_expert, int64_t rows, int64_t cols,
+            const int32_t* ids, const float* gates, int k, const void* x, float* y, int64_t n_tok, const float* bias,
+            void* ws, void* stream)
+{
+    if (!qmv::status_word()) return cuda_fail(name);
+    const int rc = qmv_launch_moe(c.wtype, c.a8, c.quant_x, c.bf16, qmv_block_bytes(paired_act(c.wtype)), W3d,
+                                  n_expert, rows, cols, ids, gates, k, x, y, n_tok, bias, ws,
+                                  static_cast<cudaStream_t>(stream));
+    if (rc == -2) return fail(QMV_ERR_SHAPE, "cols = %lld needs more shared memory than one SM has", (long long)cols);
+    if (rc == -8) return fail(QMV_ERR_CUDA, "%s: could not build a TMA tensor map", name);
+    if (rc) return cuda_fail(name);
+    return ok();
+}
 
 }  // namespace
 
@@ -322,29 +381,9 @@ int qmv_matmul(int fmt, const void* W, int64_t rows, int64_t cols, const void* X
 int qmv_moe_matvec(int fmt, const void* W3d, int n_expert, int64_t rows, int64_t cols, const int32_t* ids,
                    const float* gates, int k, const void* x, float* y, int64_t n_tok, const float* bias, void* stream)
 {
-    if (fmt & ~(0xffff | QMV_FLAG_QUANTIZE_X)) return fail(QMV_ERR_INVALID_ARG, "unknown flags 0x%x", fmt & ~0xffff);
-    const bool quant_x = (fmt & QMV_FLAG_QUANTIZE_X) != 0;
-    const int wtype = fmt & 0xff, atype = (fmt >> 8) & 0xff;
-    if (is_weight_type(wtype) && atype != QMV_F32 && atype != paired_act(wtype))
-        return fail(QMV_ERR_UNSUPPORTED,
-                    "qmv_moe_matvec: %s experts take F32 or %s activations (got %s)", type_name(wtype),
-                    type_name(paired_act(wtype)), type_name(atype));
-    int rc = check_weights(wtype, W3d, rows, cols);
-    if (rc) return rc;
-    if (quant_x && atype == QMV_F32)
-        return fail(QMV_ERR_INVALID_ARG, "QMV_FLAG_QUANTIZE_X needs an 8-bit activation type (Q8_0 or Q8_K)");
-    if (n_expert < 1 || n_expert > 1024) return fail(QMV_ERR_INVALID_ARG, "n_expert must be in 1..1024 (got %d)", n_expert);
-    if (k < 1 || k > 64) return fail(QMV_ERR_INVALID_ARG, "k must be in 1..64 (got %d)", k);
-    if (n_tok < 0 || n_tok * k > (int64_t)1 << 24)
-        return fail(QMV_ERR_INVALID_ARG, "n_tok must be >= 0 with n_tok*k <= 16777216");
-    if (n_tok == 0 || rows == 0) return ok();
-    if (!ids || !x || !y) return fail(QMV_ERR_INVALID_ARG, "ids, x and y must not be NULL");
-    const bool a8 = atype != QMV_F32;
-    const int xal = (a8 && !quant_x) ? 4 : 16;
-    if (!aligned(x, xal)) return fail(QMV_ERR_ALIGN, "x must be %d-byte aligned", xal);
-    if (!aligned(ids, 4) || !aligned(y, 4) || (gates && !aligned(gates, 4)) || (bias && !aligned(bias, 4)))
-        return fail(QMV_ERR_ALIGN, "ids, gates, bias and y must be 4-byte aligned");
-    const size_t need = qmv_moe_workspace_bytes(rows, n_tok * k);
+    MoeCall c;
+    int rc = moe_check("qmv_moe_matvec", fmt, W3d, n_expert, rows, cols, ids, gates, k, x, y, n_tok, bias, c);
+    if (rc || c.empty) return rc;
     const int d = qmv::current_device();
     void* ws = nullptr;
     size_t have = 0;
@@ -353,23 +392,17 @@ int qmv_moe_matvec(int fmt, const void* W3d, int n_expert, int64_t rows, int64_t
         ws = g_ws[d].ptr;
         have = g_ws[d].bytes;
     }
-    if (!ws || have < need)
+    if (!ws || have < c.need)
         return fail(QMV_ERR_WORKSPACE,
                     "qmv_moe_matvec needs %zu bytes of workspace (qmv_workspace_size(QMV_OP_MOE, ...)); %zu set",
-                    need, have);
-    if (!qmv::status_word()) return cuda_fail("qmv_moe_matvec (status word)");
-    rc = qmv_launch_moe(wtype, a8, quant_x, qmv_block_bytes(paired_act(wtype)), W3d, n_expert, rows, cols, ids, gates,
-                        k, x, y, n_tok, bias, ws, static_cast<cudaStream_t>(stream));
-    if (rc == -2) return fail(QMV_ERR_SHAPE, "cols = %lld needs more shared memory than one SM has", (long long)cols);
-    if (rc) return cuda_fail("qmv_moe_matvec");
-    return ok();
+                    c.need, have);
+    return moe_run("qmv_moe_matvec", c, W3d, n_expert, rows, cols, ids, gates, k, x, y, n_tok, bias, ws, stream);
 }
 
 size_t qmv_workspace_size(int op, int fmt, int64_t rows, int64_t cols, int64_t n)
 {
-    (void)fmt;
-    (void)cols;
-    if (op == QMV_OP_MOE && rows > 0 && n > 0) return qmv_moe_workspace_bytes(rows, n);
+    if (op == QMV_OP_MOE && rows > 0 && n > 0 && cols >= 0)
+        return qmv_moe_workspace_bytes(((fmt >> 8) & 0xff) == QMV_BF16, rows, cols, n);
     return 0;
 }
 
@@ -431,42 +464,19 @@ int qmv_moe_matvec_noalloc(int fmt, const void* W3d, int n_expert, int64_t rows,
                            const float* gates, int k, const void* x, float* y, int64_t n_tok, const float* bias,
                            void* stream)
 {
-    if (fmt & ~(0xffff | QMV_FLAG_QUANTIZE_X)) return fail(QMV_ERR_INVALID_ARG, "unknown flags 0x%x", fmt & ~0xffff);
-    const bool quant_x = (fmt & QMV_FLAG_QUANTIZE_X) != 0;
-    const int wtype = fmt & 0xff, atype = (fmt >> 8) & 0xff;
-    if (is_weight_type(wtype) && atype != QMV_F32 && atype != paired_act(wtype))
-        return fail(QMV_ERR_UNSUPPORTED, "qmv_moe_matvec_noalloc: %s experts take F32 or %s activations (got %s)",
-                    type_name(wtype), type_name(paired_act(wtype)), type_name(atype));
-    int rc = check_weights(wtype, W3d, rows, cols);
-    if (rc) return rc;
-    if (quant_x && atype == QMV_F32)
-        return fail(QMV_ERR_INVALID_ARG, "QMV_FLAG_QUANTIZE_X needs an 8-bit activation type (Q8_0 or Q8_K)");
-    if (n_expert < 1 || n_expert > 1024) return fail(QMV_ERR_INVALID_ARG, "n_expert must be in 1..1024 (got %d)", n_expert);
-    if (k < 1 || k > 64) return fail(QMV_ERR_INVALID_ARG, "k must be in 1..64 (got %d)", k);
-    if (n_tok < 0 || n_tok * k > (int64_t)1 << 24)
-        return fail(QMV_ERR_INVALID_ARG, "n_tok must be >= 0 with n_tok*k <= 16777216");
-    if (n_tok == 0 || rows == 0) return ok();
-    const size_t need = qmv_moe_workspace_bytes(rows, n_tok * k);
-    if (need > QMV_MOE_NOALLOC_MAX_BYTES)
+    MoeCall c;
+    int rc = moe_check("qmv_moe_matvec_noalloc", fmt, W3d, n_expert, rows, cols, ids, gates, k, x, y, n_tok, bias, c);
+    if (rc || c.empty) return rc;
+    if (c.need > QMV_MOE_NOALLOC_MAX_BYTES)
         return fail(QMV_ERR_SHAPE,
                     "qmv_moe_matvec_noalloc: %lld (token, slot) pairs x %lld rows need %zu bytes of scratch; the "
                     "built-in scratch holds %zu (about n_tok*k*rows*4 bytes are needed); use qmv_moe_matvec with a "
                     "workspace for larger calls",
-                    (long long)(n_tok * k), (long long)rows, need, (size_t)QMV_MOE_NOALLOC_MAX_BYTES);
-    if (!ids || !x || !y) return fail(QMV_ERR_INVALID_ARG, "ids, x and y must not be NULL");
-    const bool a8 = atype != QMV_F32;
-    const int xal = (a8 && !quant_x) ? 4 : 16;
-    if (!aligned(x, xal)) return fail(QMV_ERR_ALIGN, "x must be %d-byte aligned", xal);
-    if (!aligned(ids, 4) || !aligned(y, 4) || (gates && !aligned(gates, 4)) || (bias && !aligned(bias, 4)))
-        return fail(QMV_ERR_ALIGN, "ids, gates, bias and y must be 4-byte aligned");
+                    (long long)(n_tok * k), (long long)rows, c.need, (size_t)QMV_MOE_NOALLOC_MAX_BYTES);
     void* ws = moe_noalloc_scratch();
     if (!ws) return cuda_fail("qmv_moe_matvec_noalloc (scratch address)");
-    if (!qmv::status_word()) return cuda_fail("qmv_moe_matvec_noalloc (status word)");
-    rc = qmv_launch_moe(wtype, a8, quant_x, qmv_block_bytes(paired_act(wtype)), W3d, n_expert, rows, cols, ids, gates,
-                        k, x, y, n_tok, bias, ws, static_cast<cudaStream_t>(stream));
-    if (rc == -2) return fail(QMV_ERR_SHAPE, "cols = %lld needs more shared memory than one SM has", (long long)cols);
-    if (rc) return cuda_fail("qmv_moe_matvec_noalloc");
-    return ok();
+    return moe_run("qmv_moe_matvec_noalloc", c, W3d, n_expert, rows, cols, ids, gates, k, x, y, n_tok, bias, ws,
+                   stream);
 }
 
 }  // extern "C"

@@ -89,6 +89,25 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     }
 }
 
+// mbar_wait_bounded for warps off the critical path (producers that run ahead,
+// an epilogue waiting a whole tile): between polls the warp sleeps for about
+// sleep_ns, so that its polling does not take issue slots from the warps that
+// do the work.
+__device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity, unsigned* status,
+                                                  unsigned sleep_ns, uint64_t limit_ns = QMV_WAIT_LIMIT_NS)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        __nanosleep(sleep_ns);
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            atomicOr(status, QMV_DEV_WAIT_TIMEOUT);
+            return false;
+        }
+    }
+}
+
 // ---- bulk copy global -> shared (TMA, 1-D) ------------------------------------
 // dst and src 16-byte aligned, bytes a multiple of 16.  Completion is signalled
 // as transaction bytes on `bar`.

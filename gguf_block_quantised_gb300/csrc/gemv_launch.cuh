@@ -274,9 +274,10 @@ inline int launch_moe_t(bool a8, bool quant_x, const void* W3d, int n_expert, in
     using F = Fmt<T>;
     if (rows == 0 || n_pairs == 0) return 0;
     GemvPlan pl;
-    // Many small tiles (one row per warp) so an expert's rows spread over many
-    // SMs; the stage ring is sized for that tile.
-    if (!plan_gemv<T>(a8, rows, cols, n_pairs < 16 ? n_pairs : 16, pl, 1)) return -2;
+    // Small tiles (as many rows per warp as the kernel decodes at once) so an
+    // expert's rows spread over many SMs; the stage ring is sized for that tile.
+    const int gmax = n_pairs < 16 ? n_pairs : 16;
+    if (!plan_gemv<T>(a8, rows, cols, gmax, pl, rows_in_flight_rt(T, gmax))) return -2;
     MoeParams mp{};
     GemvParams& p = mp.g;
     p.W = static_cast<const uint8_t*>(W3d);

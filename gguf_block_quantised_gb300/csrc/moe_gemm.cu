@@ -1,0 +1,542 @@
+// moe_gemm.cu -- grouped tensor-core GEMM for the mixture of experts with
+// bf16 activations.
+//
+// "Models and formats" page, "Architectures": experts are stacked 3-D tensors,
+// a router sends each token to k of n experts, and gpt-oss adds a bias to
+// every expert projection; "Tensor formats": the experts are MXFP4.  Every
+// MXFP4 weight 2^(e-127) * E2M1 is exact in bf16 (E2M1 values have at most two
+// significant bits), so the bf16 tensor-core product is the plain definition
+// up to the fp32 accumulation order.
+//
+//   k_moe_tiles   one warp: the list of (expert, token tile) slots of the
+//                 experts that received pairs, from the grouping offsets.
+//   k_moe_gather  the routed activation rows, packed per expert in grouped
+//                 order (bf16 [n_valid][cols]) so one TMA tensor map covers
+//                 every expert's token tiles.
+//   k_moe_gemm_mxfp4_bf16   persistent, one CTA per SM, warp-specialised:
+//     warp 0      TMA producer of packed token tiles X[128 tokens][64 k]
+//                 (bf16, 128-byte swizzle)
+//     warp 1      TMEM owner and the single-thread MMA issuer
+//     warps 2-3, 16-19  raw weight producers: per weight row, the 16-byte pieces of
+//                 its next 8 MXFP4 blocks (256 k) as cp.async copies (the
+//                 1530-byte row pitch of the gpt-oss experts is not a legal
+//                 TMA tensor stride, and one bulk copy per 136-byte row
+//                 segment is bound by the copy engine's per-request cost)
+//     warps 4-11  dequantisers (two 64-k chunks per pass): MXFP4 -> bf16 A
+//                 tiles [128 rows][64 k] stored
+//                 straight into TMEM (tcgen05.st; row = TMEM lane), through a
+//                 per-block table of the eight E2M1 magnitudes already scaled
+//                 by 2^(e-127).  Keeping A out of shared memory leaves the
+//                 shared-memory bandwidth to the token tiles and raw blocks.
+//     warps 12-15 epilogue: TMEM -> registers -> the (token, slot) output rows,
+//                 plus the expert bias
+//   MMA M = 128 weight rows, N = 128 tokens, K = 16, A from TMEM, B (tokens)
+//   from shared memory, fp32 accumulator in TMEM, double-buffered so one
+//   tile's epilogue overlaps the next tile's MMAs.
+//   Every mbarrier wait is bounded; on a timeout the kernel flags the status
+//   word, unwinds and frees its TMEM.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "formats.cuh"
+#include "runtime.cuh"
+#include "tc.cuh"
+
+namespace qmv {
+
+bool make_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                  uint64_t pitch, uint32_t box_in, uint32_t box_out, CUtensorMapSwizzle sw);
+
+namespace mg {
+constexpr int BM = 128, BN = 128, BK = 64;
+constexpr int SX = 4, SA = 4, SR = 4;
+constexpr int X_BYTES = BN * BK * 2;     // 16384
+constexpr int SC_BLOCKS = 8;             // MXFP4 blocks per row per raw stage (256 k)
+constexpr int PIECES = 10;               // 16-byte pieces per row per raw stage: 136 bytes + up to 15 of alignment
+constexpr int SLOT = 176;                // bytes per row per raw stage (>= 16 * PIECES; 11 x 16 bytes, odd)
+constexpr int R_BYTES = BM * SLOT;       // 22528
+constexpr int OFF_X = 0;
+constexpr int OFF_R = OFF_X + SX * X_BYTES;
+constexpr int OFF_BAR = OFF_R + SR * R_BYTES;
+constexpr int N_BARS = 2 * SX + 2 * SR + 2 * SA + 4;
+constexpr int SMEM = OFF_BAR + N_BARS * 8 + 16 + 1024;   // + alignment slack
+constexpr int DEQ_WARPS = 8;             // warps 4..11
+constexpr int EPI_WARP0 = 12;            // warps 12..15
+constexpr int RAW_THREADS = 192;         // warps 2, 3 and 16..19
+constexpr int THREADS = 640;
+// TMEM columns: two 128-column fp32 accumulators, then SA bf16 A tiles of
+// 32 columns each (128 rows x 64 k, two elements per column).
+constexpr uint32_t A_COL = 2 * BN;
+constexpr uint32_t TMEM_COLS = 512;
+static_assert(A_COL + SA * (BK / 2) <= TMEM_COLS, "TMEM budget");
+}  // namespace mg
+
+// 16-byte asynchronous copy global -> shared (dst, src 16-byte aligned);
+// bytes beyond src_bytes (< 16 only at the end of the tensor) are zero-filled.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+
+// Arrive on `bar` once every cp.async this thread issued so far has landed
+// (the barrier's expected count includes this arrival).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// bf16 bit patterns of the eight E2M1 magnitudes {0, 0.5, 1, 1.5, 2, 3, 4, 6}
+// times 2^(e-127), as two byte tables (high bytes, low bytes) that prmt.b32
+// indexes with a 3-bit magnitude.  For magnitude 2^j * (1 + m/2) the bf16
+// pattern is ((e + j) << 7) | (m << 6); this holds while every exponent field
+// e + j (j = -1..2) stays in the normal range 1..254, i.e. 2 <= e <= 252.
+struct E2m1Tab {
+    uint32_t hi0, hi1, lo0, lo1;
+};
+
+__device__ __forceinline__ bool e2m1_table(uint32_t e, E2m1Tab& t)
+{
+    const uint32_t b = e << 7, bb = b | (b << 16);
+    const uint32_t p01 = (b - 128u) << 16;    // [0, 0.5 s]
+    const uint32_t p23 = bb + 0x00400000u;    // [1 s, 1.5 s]
+    const uint32_t p45 = bb + 0x00C00080u;    // [2 s, 3 s]
+    const uint32_t p67 = bb + 0x01400100u;    // [4 s, 6 s]
+    t.hi0 = prmt(p01, p23, 0x7531u);
+    t.hi1 = prmt(p45, p67, 0x7531u);
+    t.lo0 = prmt(p01, p23, 0x6420u);
+    t.lo1 = prmt(p45, p67, 0x6420u);
+    return e - 2u <= 250u;
+}
+
+// Four E2M1 codes, the nibbles of the selector's low 16 bits (elements i,
+// i+16, i+1, i+17 of a block: the low and high nibbles of code bytes i and
+// i+1), -> bf16 pairs (i, i+1) and (i+16, i+17).
+__device__ __forceinline__ void e2m1_quad(uint32_t s, const E2m1Tab& t, uint32_t& p_lo, uint32_t& p_hi)
+{
+    const uint32_t mag = s & 0x7777u;
+    uint32_t H = prmt(t.hi0, t.hi1, mag);
+    const uint32_t L = prmt(t.lo0, t.lo1, mag);
+    // 0xff in the bytes whose code has its sign bit (nibble bit 3) set: a
+    // selector nibble with bit 3 set makes prmt.b32 replicate bit 7 of the
+    // selected byte.
+    const uint32_t neg = prmt(s << 4, s, 0xd9c8u);
+    H |= neg & 0x80808080u;
+    p_lo = prmt(L, H, 0x6240u);
+    p_hi = prmt(L, H, 0x7351u);
+}
+
+// Exact bf16 of one block whose exponent leaves the table's range (zero or
+// subnormal scales, overflow, NaN): code * 2^(e-127) in fp32, then rounded to
+// bf16 (exact unless it overflows).
+__device__ __forceinline__ void mxfp4_block_bf16_slow(uint32_t e, const uint32_t (&w)[4], uint32_t (&o)[16])
+{
+    using M = Fmt<QMV_MXFP4>;
+    const float sc = M::e8m0_half(e);   // 2^(e-128); the codes below are doubled
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t nib = h ? (w[k] >> 4) & 0x0f0f0f0fu : w[k] & 0x0f0f0f0fu;
+            const uint32_t v = M::lut4(__byte_perm(nib | (nib >> 4), 0u, 0x0020u) & 0xffffu);
+            float f[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) f[j] = (float)(int)(int8_t)((v >> (8 * j)) & 0xffu) * sc;
+            const __nv_bfloat162 p = __floats2bfloat162_rn(f[0], f[1]), q = __floats2bfloat162_rn(f[2], f[3]);
+            o[8 * h + 2 * k] = *reinterpret_cast<const uint32_t*>(&p);
+            o[8 * h + 2 * k + 1] = *reinterpret_cast<const uint32_t*>(&q);
+        }
+    }
+}
+
+// One 32-element MXFP4 block (17 bytes at byte offset o of a 16-byte-aligned
+// shared-memory row slot; o % 16 + 17 <= 32) -> 16 bf16x2 words in element
+// order (word i = elements 2i, 2i+1).  The block is read with two aligned
+// 16-byte loads and shifted into place in registers.
+__device__ __forceinline__ void mxfp4_block_bf16(const uint8_t* slot, int o, uint32_t (&out)[16])
+{
+    const uint4* p = reinterpret_cast<const uint4*>(slot + (o & ~15));
+    const uint4 u0 = p[0], u1 = p[1];
+    const uint32_t W[9] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w, 0u};
+    const int q = (o >> 2) & 3;
+    uint32_t Y[7], X[6];
+#pragma unroll
+    for (int i = 0; i < 7; ++i) Y[i] = (q & 2) ? W[i + 2] : W[i];
+#pragma unroll
+    for (int i = 0; i < 6; ++i) X[i] = (q & 1) ? Y[i + 1] : Y[i];
+    const uint32_t sh = (uint32_t)(o & 3) * 8u;
+    uint32_t w5[5];
+#pragma unroll
+    for (int k = 0; k < 5; ++k) w5[k] = __funnelshift_r(X[k], X[k + 1], sh);   // byte 0: exponent, 1..16: codes
+    const uint32_t e = w5[0] & 0xffu;
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) w[k] = __funnelshift_r(w5[k], w5[k + 1], 8);
+    E2m1Tab t;
+    if (e2m1_table(e, t)) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            e2m1_quad(w[k], t, out[2 * k], out[8 + 2 * k]);
+            e2m1_quad(w[k] >> 16, t, out[2 * k + 1], out[8 + 2 * k + 1]);
+        }
+    } else {
+        mxfp4_block_bf16_slow(e, w, out);
+    }
+}
+
+// tiles[0] = number of (expert, token tile) slots; slot i = (tiles[1+2i] =
+// expert, tiles[2+2i] = token tile within the expert's group).
+__global__ void k_moe_tiles(const int* __restrict__ offsets, const int* __restrict__ active, int* __restrict__ tiles)
+{
+    const int lane = threadIdx.x;
+    pdl_wait();
+    const int na = active[0];
+    int base = 0;
+    for (int i0 = 0; i0 < na; i0 += 32) {
+        const int i = i0 + lane;
+        const int e = i < na ? active[1 + i] : 0;
+        const int nt = i < na ? (offsets[e + 1] - offsets[e] + mg::BN - 1) / mg::BN : 0;
+        int pre = nt;   // inclusive prefix sum over the warp
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, pre, o);
+            if (lane >= o) pre += v;
+        }
+        const int start = base + pre - nt;
+        for (int j = 0; j < nt; ++j) {
+            tiles[1 + 2 * (start + j)] = e;
+            tiles[2 + 2 * (start + j)] = j;
+        }
+        base += __shfl_sync(0xffffffffu, pre, 31);
+    }
+    if (lane == 0) tiles[0] = base;
+}
+
+// Xs[j] = x row perm[j] / kdiv for the n_valid grouped pairs (bf16, 16 bytes
+// per thread).
+__global__ void k_moe_gather(const uint16_t* __restrict__ x, const int* __restrict__ perm,
+                             const int* __restrict__ offsets, int n_expert, int kdiv, int cols,
+                             uint16_t* __restrict__ Xs)
+{
+    const int n_valid = offsets[n_expert];
+    const int per_row = cols / 8;
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (int64_t)n_valid * per_row) return;
+    const int j = (int)(i / per_row), c = (int)(i % per_row);
+    const int src = perm[j] / kdiv;
+    reinterpret_cast<uint4*>(Xs + (size_t)j * cols)[c] = reinterpret_cast<const uint4*>(x + (size_t)src * cols)[c];
+}
+
+struct MoeGemmArgs {
+    const uint8_t* W3d;   // 16-byte aligned
+    int64_t rows;         // rows per expert
+    int64_t rb;           // bytes per row
+    int64_t total;        // bytes of all experts
+    int nblk;             // MXFP4 blocks per row
+    const int* offsets;
+    const int* perm;
+    const int* tiles;
+    const float* bias;    // [n_expert][rows] or NULL
+    float* out;           // row of pair p at out + p*rows
+    unsigned* status;
+};
+
+__global__ void __launch_bounds__(mg::THREADS, 1)
+    k_moe_gemm_mxfp4_bf16(const __grid_constant__ CUtensorMap tmX, const MoeGemmArgs a)
+{
+    using namespace mg;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+    uint64_t* xf = bars;
+    uint64_t* xe = xf + SX;
+    uint64_t* rf = xe + SX;
+    uint64_t* re = rf + SR;
+    uint64_t* af = re + SR;
+    uint64_t* ae = af + SA;
+    uint64_t* accf = ae + SA;
+    uint64_t* acce = accf + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 2);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_wait();
+    const int n_rt = (int)((a.rows + BM - 1) / BM);
+    const int n_tiles = n_rt * a.tiles[0];
+    const int nk = (a.nblk + 1) / 2;                       // 64-k chunks (the last may hold one block)
+    const int nsc = (a.nblk + SC_BLOCKS - 1) / SC_BLOCKS;  // raw stages per row
+
+    if (tid == 0) {
+        for (int i = 0; i < SX; ++i) { mbar_init(&xf[i], 1); mbar_init(&xe[i], 1); }
+        for (int i = 0; i < SR; ++i) { mbar_init(&rf[i], RAW_THREADS); mbar_init(&re[i], DEQ_WARPS); }
+        for (int i = 0; i < SA; ++i) { mbar_init(&af[i], DEQ_WARPS); mbar_init(&ae[i], 1); }
+        for (int i = 0; i < 2; ++i) { mbar_init(&accf[i], 1); mbar_init(&acce[i], 4); }
+        *abort_flag = 0;
+        fence_barrier_init();
+        prefetch_tmap(&tmX);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    auto fail = [&]() { *abort_flag = 1; };
+    auto tile_of = [&](int t, int& e, int& nt, int& rt) {
+        const int slot = t / n_rt;
+        rt = t - slot * n_rt;
+        e = a.tiles[1 + 2 * slot];
+        nt = a.tiles[2 + 2 * slot];
+    };
+
+    if (warp == 0) {
+        // ---- packed token tiles
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 1;
+            for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x) {
+                int e, nt, rt;
+                tile_of(t, e, nt, rt);
+                const int row0 = a.offsets[e] + nt * BN;
+                for (int kk = 0; kk < nk; ++kk) {
+                    if (!mbar_wait_backoff(&xe[s], ph, a.status, 128)) { fail(); break; }
+                    mbar_arrive_expect_tx(&xf[s], X_BYTES);
+                    tma_load_2d(smem + OFF_X + s * X_BYTES, &tmX, kk * BK, row0, &xf[s]);
+                    if (++s == SX) { s = 0; ph ^= 1; }
+                }
+            }
+        }
+    } else if (warp == 2 || warp == 3 || warp >= EPI_WARP0 + 4) {
+        // ---- raw weights: for each row of the tile, the 16-byte-aligned span
+        // holding its next (up to) 8 blocks, as 16-byte cp.async pieces spread
+        // over the 192 threads of warps 2, 3 and 16..19 (consecutive threads take
+        // consecutive pieces of a row).  The last piece of the tensor reads
+        // only the bytes that exist and zero-fills the rest.  Each thread then
+        // arrives on the stage's barrier once its own copies have landed.
+        const int pt = warp < 4 ? tid - 64 : tid - 32 * (EPI_WARP0 + 4) + 64;
+        int s = 0;
+        uint32_t ph = 1;
+        for (int t = blockIdx.x; t < n_tiles && !__any_sync(0xffffffffu, *abort_flag); t += gridDim.x) {
+            int e, nt, rt;
+            tile_of(t, e, nt, rt);
+            const int64_t tile0 = ((int64_t)e * a.rows + (int64_t)rt * BM) * a.rb;   // byte offset of row 0
+            const int nrows = (int)min((int64_t)BM, a.rows - (int64_t)rt * BM);
+            bool bad = false;
+            for (int sc = 0; sc < nsc; ++sc) {
+                if (!__all_sync(0xffffffffu, mbar_wait_backoff(&re[s], ph, a.status, 128))) { bad = true; break; }
+                uint8_t* buf = smem + OFF_R + s * R_BYTES;
+                const int nb = min(SC_BLOCKS, a.nblk - sc * SC_BLOCKS);
+                for (int p = pt; p < nrows * PIECES; p += RAW_THREADS) {
+                    const int i = p / PIECES, j = p - i * PIECES;
+                    const int64_t b0 = tile0 + (int64_t)i * a.rb + (int64_t)sc * SC_BLOCKS * 17;
+                    const int64_t src = (b0 & ~int64_t(15)) + 16 * j;
+                    if (src < b0 + nb * 17)
+                        cp_async16(buf + i * SLOT + 16 * j, a.W3d + src, (uint32_t)min((int64_t)16, a.total - src));
+                }
+                cp_async_arrive_noinc(&rf[s]);
+                if (++s == SR) { s = 0; ph ^= 1; }
+            }
+            if (bad) { fail(); break; }
+        }
+    } else if (warp == 1) {
+        // ---- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16(BM, BN);
+            int sx = 0, sa = 0;
+            uint32_t pxf = 0, paf = 0;
+            int local = 0;
+            for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x, ++local) {
+                const int buf = local & 1;
+                const uint32_t use = (uint32_t)(local >> 1);
+                if (!mbar_wait_bounded(&acce[buf], (use & 1) ^ 1, a.status)) { fail(); break; }
+                tc_fence_after();
+                const uint32_t d = tmem + buf * BN;
+                bool bad = false;
+                for (int kk = 0; kk < nk; ++kk) {
+                    if (!mbar_wait_bounded(&af[sa], paf, a.status) || !mbar_wait_bounded(&xf[sx], pxf, a.status)) {
+                        bad = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t at = tmem + A_COL + sa * (BK / 2);
+                    const uint64_t bdesc = smem_desc_sw128(smem + OFF_X + sx * X_BYTES);
+#pragma unroll
+                    for (int k4 = 0; k4 < BK / 16; ++k4)   // A: 8 TMEM columns, B: 32 bytes per K = 16 step
+                        mma_f16_ts(d, at + 8 * k4, bdesc + 2 * k4, idesc, (kk | k4) != 0);
+                    mma_commit(&ae[sa]);
+                    mma_commit(&xe[sx]);
+                    if (++sa == SA) { sa = 0; paf ^= 1; }
+                    if (++sx == SX) { sx = 0; pxf ^= 1; }
+                }
+                if (bad) { fail(); break; }
+                mma_commit(&accf[buf]);
+            }
+        }
+    } else if (warp >= 4 && warp < 4 + DEQ_WARPS) {
+        // ---- dequantisers: thread t -> weight row t % 128 (its TMEM lane:
+        // warp % 4 is the warp's lane quarter) and block 2c + t / 128 of each
+        // 64-k chunk c, i.e. A tile columns 16 * (t / 128) .. +15
+        const int t0 = tid - 128, r = t0 & 127, half = t0 >> 7;
+        const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + A_COL + 16 * half;
+        int sr = 0, sa = 0;
+        uint32_t prf = 0, pae = 1;
+        for (int t = blockIdx.x; t < n_tiles && !__any_sync(0xffffffffu, *abort_flag); t += gridDim.x) {
+            int e, nt, rt;
+            tile_of(t, e, nt, rt);
+            const int64_t row = (int64_t)rt * BM + r;
+            const int64_t row_start = ((int64_t)e * a.rows + row) * a.rb;   // byte offset of the row
+            bool bad = false;
+            for (int sc = 0; sc < nsc && !bad; ++sc) {
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&rf[sr], prf, a.status))) { bad = true; break; }
+                const uint8_t* slot = smem + OFF_R + sr * R_BYTES + r * SLOT;
+                const int off = (int)((row_start + (int64_t)sc * SC_BLOCKS * 17) & 15);
+                const int nb = min(SC_BLOCKS, a.nblk - sc * SC_BLOCKS);
+                const int nc = (nb + 1) / 2;
+                // two chunks per pass: two independent blocks per thread in
+                // flight, one wait for both TMEM stores
+                for (int c = 0; c < nc; c += 2) {
+                    const bool two = c + 1 < nc;
+                    const int sb = sa + 1 == SA ? 0 : sa + 1;
+                    const uint32_t pb = sb == 0 ? pae ^ 1 : pae;
+                    if (!__all_sync(0xffffffffu, mbar_wait_bounded(&ae[sa], pae, a.status) &&
+                                                     (!two || mbar_wait_bounded(&ae[sb], pb, a.status)))) {
+                        bad = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    uint32_t o0[16], o1[16];
+                    const int b0i = 2 * c + half, b1i = b0i + 2;
+                    if (row < a.rows && b0i < nb) {
+                        mxfp4_block_bf16(slot, off + 17 * b0i, o0);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) o0[i] = 0u;
+                    }
+                    tmem_st16_async(ta + sa * (BK / 2), o0);
+                    if (two) {
+                        if (row < a.rows && b1i < nb) {
+                            mxfp4_block_bf16(slot, off + 17 * b1i, o1);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) o1[i] = 0u;
+                        }
+                        tmem_st16_async(ta + sb * (BK / 2), o1);
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&af[sa]);
+                        if (two) mbar_arrive(&af[sb]);
+                    }
+                    const int adv = two ? 2 : 1;
+                    for (int i = 0; i < adv; ++i)
+                        if (++sa == SA) { sa = 0; pae ^= 1; }
+                }
+                if (bad) break;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&re[sr]);
+                if (++sr == SR) { sr = 0; prf ^= 1; }
+            }
+            if (bad) { fail(); break; }
+        }
+    } else if (warp >= EPI_WARP0) {
+        // ---- epilogue: lane quarter (warp % 4) of the 128 TMEM lanes; column
+        // j of the accumulator is the expert's grouped pair offsets[e] + nt*128 + j
+        const int q = warp & 3;
+        int local = 0;
+        for (int t = blockIdx.x; t < n_tiles && !__any_sync(0xffffffffu, *abort_flag); t += gridDim.x, ++local) {
+            int e, nt, rt;
+            tile_of(t, e, nt, rt);
+            const int buf = local & 1;
+            const uint32_t use = (uint32_t)(local >> 1);
+            // warp-uniform: every lane must take part in the tcgen05.ld below
+            if (!__all_sync(0xffffffffu, mbar_wait_backoff(&accf[buf], use & 1, a.status, 512))) { fail(); break; }
+            tc_fence_after();
+            const int64_t row = (int64_t)rt * BM + 32 * q + lane;
+            const bool row_ok = row < a.rows;
+            const float bv = (a.bias && row_ok) ? a.bias[(int64_t)e * a.rows + row] : 0.f;
+            const int g0 = a.offsets[e] + nt * BN, cnt = a.offsets[e + 1] - g0;
+            for (int c16 = 0; c16 < BN / 16; ++c16) {
+                float v[16];
+                tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + buf * BN + c16 * 16, v);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int j = c16 * 16 + i;
+                    if (j < cnt && row_ok) a.out[(int64_t)a.perm[g0 + j] * a.rows + row] = v[i] + bv;
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acce[buf]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+inline size_t tiles_bytes(int64_t n_pairs)
+{
+    const size_t slots = (size_t)n_pairs + (size_t)n_pairs / mg::BN + 1;   // >= sum over experts of ceil(count/128)
+    return ((1 + 2 * slots) * 4 + 255) & ~size_t(255);
+}
+
+}  // namespace qmv
+
+// Bytes of workspace beyond the grouping that the grouped GEMM needs: the slot
+// list and the packed bf16 activations.
+size_t qmv_moe_gemm_extra_bytes(int64_t cols, int64_t n_pairs)
+{
+    return qmv::tiles_bytes(n_pairs) + (size_t)n_pairs * (size_t)cols * 2;
+}
+
+// Enqueues the slot list, the gather and the grouped GEMM.  ws points at the
+// GEMM's part of the workspace (qmv_moe_gemm_extra_bytes bytes, 256-aligned).
+// Returns 0, -6 (launch failure) or -8 (tensor map).
+int qmv_launch_moe_gemm_mxfp4(const void* W3d, int n_expert, int64_t rows, int64_t cols, const void* x, int kdiv,
+                              int64_t n_pairs, const int* offsets, const int* active, const int* perm, void* ws,
+                              float* out, const float* bias, cudaStream_t st)
+{
+    using namespace qmv;
+    int* tiles = static_cast<int*>(ws);
+    uint16_t* Xs = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + tiles_bytes(n_pairs));
+    k_moe_tiles<<<1, 32, 0, st>>>(offsets, active, tiles);
+    const int64_t per = n_pairs * (cols / 8);
+    k_moe_gather<<<(unsigned)((per + 255) / 256), 256, 0, st>>>(static_cast<const uint16_t*>(x), perm, offsets,
+                                                                  n_expert, kdiv, (int)cols, Xs);
+    if (cudaGetLastError() != cudaSuccess) return -6;
+    CUtensorMap tmX;
+    if (!make_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Xs, (uint64_t)cols, (uint64_t)n_pairs,
+                      (uint64_t)cols * 2, mg::BK, mg::BN, CU_TENSOR_MAP_SWIZZLE_128B))
+        return -8;
+    MoeGemmArgs a;
+    a.W3d = static_cast<const uint8_t*>(W3d);
+    a.rows = rows;
+    a.nblk = (int)(cols / 32);
+    a.rb = (int64_t)a.nblk * 17;
+    a.total = (int64_t)n_expert * rows * a.rb;
+    a.offsets = offsets;
+    a.perm = perm;
+    a.tiles = tiles;
+    a.bias = bias;
+    a.out = out;
+    a.status = status_word();
+    auto* k = &k_moe_gemm_mxfp4_bf16;
+    prepare_kernel(k, mg::THREADS, mg::SMEM);
+    return launch_ex(k, dim3(num_sms()), dim3(mg::THREADS), mg::SMEM, st, false, tmX, a) == cudaSuccess ? 0 : -6;
+}

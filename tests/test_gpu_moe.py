@@ -151,3 +151,101 @@ def test_moe_bad_expert_and_workspace(qmv, orc, workspace):
         assert e.value.code == qmv.ERR_WORKSPACE
     finally:
         qmv.qmv_set_workspace(workspace, workspace.numel())
+
+
+# ---- MXFP4 experts x bf16 activations: the grouped tensor-core GEMM ---------------
+BF16 = 9
+
+
+def bf16_rows(n, cols, seed):
+    """bf16 activation rows (torch's round-to-nearest of N(0,1)) and their bit
+    patterns for the oracle."""
+    xb = torch.from_numpy(synth.activations(n, cols, seed=seed)).to(torch.bfloat16)
+    return xb, xb.view(torch.int16).numpy()
+
+
+@pytest.mark.parametrize("rows,cols,n_tok", [(296, 544, 1), (128, 256, 37), (200, 2880, 9), (136, 320, 300)])
+def test_moe_bf16_gemm_parity(qmv, orc, workspace, rows, cols, n_tok):
+    """Ragged row tiles, an odd number of blocks per row (a half 64-k chunk and
+    a short last raw stage), experts with more than one 128-token tile, both
+    forms, with biases."""
+    E, k, t = 8, 4, MXFP4
+    W3, ids, gates, b = moe_inputs(t, E, rows, cols, n_tok, k, 40 + cols)
+    W3d = dev(W3)
+    fmt = qmv.FMT(t, BF16)
+    xb, xbits = bf16_rows(n_tok, cols, 41)
+    y = run_moe(qmv, fmt, W3d, E, rows, cols, ids, None, k, xb.cuda(), n_tok, b)
+    yref, yabs = orc.moe(t, BF16, W3, E, rows, cols, ids, None, k, xbits, n_tok, bias=b)
+    assert_close(y, yref, yabs, what="up")
+    hb, hbits = bf16_rows(n_tok * k, cols, 42)
+    y = run_moe(qmv, fmt, W3d, E, rows, cols, ids, gates, k, hb.reshape(n_tok, k, cols).cuda(), n_tok, b)
+    yref, yabs = orc.moe(t, BF16, W3, E, rows, cols, ids, gates, k, hbits.reshape(n_tok, k, cols), n_tok, bias=b)
+    assert_close(y, yref, yabs, what="down")
+    qmv.qmv_get_status()
+
+
+def test_moe_bf16_exponent_range(qmv, orc, workspace):
+    """E8M0 exponents across 0..200: the table path (2..252) at both ends of its
+    range and the exact fallback for the zero and subnormal scales (0, 1)."""
+    E, rows, cols, k, n_tok, t = 4, 160, 512, 2, 20, MXFP4
+    W3, ids, gates, b = moe_inputs(t, E, rows, cols, n_tok, k, 50)
+    blocks = W3.reshape(-1, 17)
+    g = np.random.default_rng(50)
+    blocks[:, 0] = g.integers(0, 201, size=blocks.shape[0], dtype=np.uint8)
+    blocks[::7, 0] = 2
+    blocks[3::11, 0] = g.integers(0, 2, size=blocks[3::11].shape[0], dtype=np.uint8)
+    W3 = blocks.reshape(-1)
+    xb, xbits = bf16_rows(n_tok, cols, 51)
+    y = run_moe(qmv, qmv.FMT(t, BF16), dev(W3), E, rows, cols, ids, None, k, xb.cuda(), n_tok, None)
+    yref, yabs = orc.moe(t, BF16, W3, E, rows, cols, ids, None, k, xbits, n_tok)
+    assert_close(y, yref, yabs, what="exponents")
+    qmv.qmv_get_status()
+
+
+@pytest.mark.parametrize("n_tok", [1, 64, 1024])
+def test_moe_bf16_gpt_oss_shapes_sampled(qmv, orc, workspace, n_tok):
+    """gpt-oss-20B-shaped experts with bf16 activations through the grouped
+    GEMM: gate_up 5760x2880 (up form) and down 2880x2880 (gate-weighted),
+    biases, top-4 of 32; sampled tokens and rows against the oracle."""
+    E, k, t = 32, 4, MXFP4
+    g = np.random.default_rng(100 + n_tok)
+    for rows, cols, down in ((5760, 2880, False), (2880, 2880, True)):
+        W3, ids, gates, b = moe_inputs(t, E, rows, cols, n_tok, k, 60 + rows)
+        xb, xbits = bf16_rows(n_tok * (k if down else 1), cols, 61)
+        if down:
+            xb, xbits = xb.reshape(n_tok, k, cols), xbits.reshape(n_tok, k, cols)
+        y = run_moe(qmv, qmv.FMT(t, BF16), dev(W3), E, rows, cols, ids, gates if down else None, k, xb.cuda(),
+                    n_tok, b)
+        toks = np.unique(np.concatenate([[0, n_tok - 1], g.integers(0, n_tok, 4)]))
+        rids = np.unique(np.concatenate([[0, rows - 1], g.integers(0, rows, 30)]))
+        yref, yabs = oracle_sampled(orc, t, BF16, W3, E, rows, cols, ids, gates, k, xbits, toks, rids, b, down)
+        assert_close(y[toks][..., rids], yref, yabs, what=f"n_tok={n_tok} down={down}")
+    qmv.qmv_get_status()
+
+
+def test_moe_bf16_routing_invariance(qmv, orc, workspace):
+    """A token's outputs from the grouped GEMM do not depend on the other
+    tokens routed with it (its column of the expert's tile): a 200-token call
+    equals single-token calls bit for bit."""
+    E, rows, cols, k, n_tok, t = 4, 256, 512, 2, 200, MXFP4
+    W3, ids, gates, b = moe_inputs(t, E, rows, cols, n_tok, k, 70)
+    W3d = dev(W3)
+    xb, _ = bf16_rows(n_tok, cols, 71)
+    y = run_moe(qmv, qmv.FMT(t, BF16), W3d, E, rows, cols, ids, None, k, xb.cuda(), n_tok, b)
+    for tok in (0, 77, 199):
+        y1 = run_moe(qmv, qmv.FMT(t, BF16), W3d, E, rows, cols, ids[tok:tok + 1], None, k, xb[tok:tok + 1].cuda(),
+                     1, b)
+        assert np.array_equal(y1[0].view(np.uint32), y[tok].view(np.uint32))
+
+
+def test_moe_bf16_refusals(qmv, workspace):
+    W = torch.zeros(64 * 17, dtype=torch.uint8, device="cuda")
+    x = torch.zeros((1, 64), dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros((1, 2, 32), dtype=torch.float32, device="cuda")
+    ids = torch.zeros((1, 2), dtype=torch.int32, device="cuda")
+    with pytest.raises(qmv.QmvError) as e:   # BF16 activations are for MXFP4 experts only
+        qmv.qmv_moe_matvec(qmv.FMT(Q4_K, BF16), W, 1, 32, 256, ids, None, 2, x, y, 1, None)
+    assert e.value.code == qmv.ERR_UNSUPPORTED
+    with pytest.raises(qmv.QmvError) as e:   # nothing to quantise
+        qmv.qmv_moe_matvec(qmv.FMT(MXFP4, BF16) | qmv.FLAG_QUANTIZE_X, W, 1, 32, 64, ids, None, 2, x, y, 1, None)
+    assert e.value.code == qmv.ERR_INVALID_ARG
