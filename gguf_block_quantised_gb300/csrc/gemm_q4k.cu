@@ -4,25 +4,29 @@
 // "Architecture" page, "The package map": pkg/tensor MatMul is the prefill
 // multiply; "The two phases": prefill is bound by arithmetic, so it runs on
 // the tensor cores.  Y[m][r] = sum_k X[m][k] * bf16(w[r][k]): the Q4_K weights
-// are dequantised to bf16 tiles in shared memory (w = d*sc*q - dmin*m in fp32,
-// one rounding, then rounded to bf16) and multiplied with bf16 activations,
-// accumulating in fp32.
+// are dequantised to bf16 (w = d*sc*q - dmin*m in fp32, one rounding, then
+// rounded to bf16) and multiplied with bf16 activations, accumulating in fp32.
 //
-// One persistent CTA per SM, 12 warps, warp-specialised:
-//   warp 0      TMA producer of activation tiles X[256 tokens][64 k] (bf16,
+// One persistent CTA per SM, 16 warps, warp-specialised:
+//   warp 0      TMA producer of activation tiles X[BN tokens][64 k] (bf16,
 //               128-byte swizzle, the UMMA K-major canonical layout)
 //   warp 1      TMEM owner (alloc/free) and the single-thread MMA issuer
 //   warp 2      TMA producer of raw Q4_K super-block tiles W[128 rows][144 B]
-//   warps 4-11  dequantisers: raw super-block -> four bf16 A tiles
-//               [128 rows][64 k] written in the 128-byte swizzled layout
-//               (packed fp32x2 arithmetic, two weights per instruction)
+//   warps 4-11  dequantisers: raw super-block -> bf16 A tiles [128 rows][64 k]
+//               written straight into TMEM with tcgen05.st (row = TMEM lane,
+//               two k per column), packed fp32x2 arithmetic.  A never touches
+//               shared memory, which leaves the shared-memory bandwidth to the
+//               MMA's reads of X and to the TMA writes.
 //   warps 12-15 epilogue: TMEM -> registers -> Y, one 128-byte row segment
 //               per column, so every store is coalesced
 // MMA: M = 128 weight rows, N = BN tokens (256, or 128 when 256-token tiles
-// would leave SMs idle), K = 16 per instruction, fp32 accumulator in TMEM,
-// double-buffered (2 x BN columns) so the epilogue of one tile overlaps the
-// MMAs of the next.  Every mbarrier wait is bounded;
-// on a timeout the kernel flags the status word, unwinds and frees its TMEM.
+// would leave SMs idle or pad the tokens more), K = 16 per instruction, A from
+// TMEM, B from shared memory, fp32 accumulator in TMEM.  TMEM holds 256
+// accumulator columns (two 128-column buffers, so that one tile's epilogue
+// overlaps the next tile's MMAs, or one 256-column buffer) and four 32-column
+// A stages.  X and A of a 64-k stage share one full and one empty barrier.  Every
+// mbarrier wait is bounded; on a timeout the kernel flags the status word,
+// unwinds and frees its TMEM.
 #include <cuda.h>
 
 #include "formats.cuh"
@@ -34,19 +38,21 @@ namespace qmv {
 
 namespace gq {
 constexpr int BM = 128, BK = 64;
-constexpr int SX = 4, SA = 3, SR = 2;
+constexpr int SK = 4, SR = 3;               // k stages (X tile + A tile), raw stages
 constexpr int X_BYTES_MAX = 256 * BK * 2;   // 32768 (BN = 256)
-constexpr int A_BYTES = BM * BK * 2;        // 16384
 constexpr int R_BYTES = BM * 144;           // 18432
 constexpr int OFF_X = 0;
-constexpr int OFF_A = OFF_X + SX * X_BYTES_MAX;
-constexpr int OFF_R = OFF_A + SA * A_BYTES;
+constexpr int OFF_R = OFF_X + SK * X_BYTES_MAX;
 constexpr int OFF_BAR = OFF_R + SR * R_BYTES;
-constexpr int N_BARS = 2 * SX + 2 * SR + 2 * SA + 4;
+constexpr int N_BARS = 2 * SK + 2 * SR + 4;
 constexpr int SMEM = OFF_BAR + N_BARS * 8 + 16 + 1024;   // + alignment slack
 constexpr int DEQ_WARPS = 8;                // warps 4..11
+constexpr int EPI_WARP0 = 12;               // warps 12..15
 constexpr int THREADS = 512;                // 16 warps
 constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t A_STAGE_COLS = BK / 2;   // 64 bf16 k per row = 32 columns
+// accumulators: two of 128 columns (BN = 128) or one of 256 (BN = 256)
+static_assert(256 + SK * A_STAGE_COLS <= TMEM_COLS, "TMEM budget");
 }  // namespace gq
 
 struct GemmArgs {
@@ -78,40 +84,33 @@ __device__ __forceinline__ uint32_t dq2_bf16(uint32_t codes, uint32_t sel, uint6
     return *reinterpret_cast<const uint32_t*>(&b);
 }
 
-// Dequantise sub-blocks 2c, 2c+1 of the raw super-block tile into a bf16 A
-// tile (128 rows x 64 k, K-major, 128-byte swizzle): w = RN_fp32(d*sc*q - dmin*m)
-// (d*sc and dmin*m are exact products), then rounded to bf16.  256 threads:
-// thread t handles row t % 128 and the 8-k groups jj = 2*(t / 128) + {0, 1}
-// of both sub-blocks.
-__device__ __forceinline__ void dequant_q4k_tile(const uint8_t* raw, uint8_t* A, int c, int t)
+// Dequantise this thread's part of sub-blocks 2c, 2c+1 of the raw super-block
+// tile: w = RN_fp32(d*sc*q - dmin*m) (d*sc and dmin*m are exact products),
+// then rounded to bf16.  256 threads: thread t handles row t % 128 and the
+// 8-k groups jj = 2*(t / 128) + {0, 1} of both sub-blocks, i.e. k = 16h..16h+15
+// (lo, sub-block 2c) and 32+16h..32+16h+15 (hi, sub-block 2c+1) of the 64-k
+// chunk, h = t / 128: eight bf16x2 words each, in k order.
+__device__ __forceinline__ void dequant_q4k_regs(const uint8_t* raw, int c, int t, uint32_t (&lo)[8],
+                                                 uint32_t (&hi)[8])
 {
     const int r = t & 127;
     const uint8_t* rp = raw + r * 144;
     const uint4 h = *reinterpret_cast<const uint4*>(rp);
+    const uint4 qv = *reinterpret_cast<const uint4*>(rp + 16 + 32 * c + 16 * (t >> 7));
     const Q4kScales ks = q4k_scales(h.y, h.z, h.w);
     const float d = half_bits_to_float(h.x & 0xffffu), dmin = half_bits_to_float(h.x >> 16);
     const float D0 = d * (float)ks.sc(2 * c), M0 = dmin * (float)ks.m(2 * c);       // exact
     const float D1 = d * (float)ks.sc(2 * c + 1), M1 = dmin * (float)ks.m(2 * c + 1);
     const uint64_t D0x2 = pk2(D0, D0), nM0x2 = pk2(-M0, -M0), D1x2 = pk2(D1, D1), nM1x2 = pk2(-M1, -M1);
-    uint8_t* rowA = A + (r >> 3) * 1024 + (r & 7) * 128;
+    const uint32_t q[4] = {qv.x, qv.y, qv.z, qv.w};   // codes of 16 consecutive k
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int jj = 2 * (t >> 7) + i;
-        const uint2 qv = *reinterpret_cast<const uint2*>(rp + 16 + 32 * c + 8 * jj);
-        uint32_t lo[4], hi[4];
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const uint32_t w = k ? qv.y : qv.x;                 // codes of 4 consecutive k
-            const uint32_t l4 = w & 0x0f0f0f0fu, h4 = (w >> 4) & 0x0f0f0f0fu;
-            // selectors: byte j of the codes word, then bytes 5, 6, 7 of 0x4B000000
-            lo[2 * k] = dq2_bf16(l4, 0x76517650u, D0x2, nM0x2);
-            lo[2 * k + 1] = dq2_bf16(l4, 0x76537652u, D0x2, nM0x2);
-            hi[2 * k] = dq2_bf16(h4, 0x76517650u, D1x2, nM1x2);
-            hi[2 * k + 1] = dq2_bf16(h4, 0x76537652u, D1x2, nM1x2);
-        }
-        const int jl = jj, jh = 4 + jj;   // 16-byte chunks of the 128-byte row
-        *reinterpret_cast<uint4*>(rowA + ((jl ^ (r & 7)) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        *reinterpret_cast<uint4*>(rowA + ((jh ^ (r & 7)) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t l4 = q[k] & 0x0f0f0f0fu, h4 = (q[k] >> 4) & 0x0f0f0f0fu;
+        // selectors: byte j of the codes word, then bytes 5, 6, 7 of 0x4B000000
+        lo[2 * k] = dq2_bf16(l4, 0x76517650u, D0x2, nM0x2);
+        lo[2 * k + 1] = dq2_bf16(l4, 0x76537652u, D0x2, nM0x2);
+        hi[2 * k] = dq2_bf16(h4, 0x76517650u, D1x2, nM1x2);
+        hi[2 * k + 1] = dq2_bf16(h4, 0x76537652u, D1x2, nM1x2);
     }
 }
 
@@ -121,16 +120,24 @@ __global__ void __launch_bounds__(gq::THREADS, 1)
 {
     using namespace gq;
     constexpr int X_BYTES = BN * BK * 2;
+    // TMEM: NBUF accumulators of BN columns from column 0, then the A stages.
+    // 128-token tiles double-buffer the accumulator so one tile's epilogue
+    // overlaps the next tile's MMAs; 256-token tiles have room for one only.
+    constexpr int NBUF = BN == 256 ? 1 : 2;
+    constexpr uint32_t A_COL = 256;
+    static_assert(NBUF * BN <= (int)A_COL, "tile width");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-    uint64_t* xf = bars;
-    uint64_t* xe = xf + SX;
-    uint64_t* rf = xe + SX;
+    // k stage s holds the X tile (shared memory) and the A tile (TMEM) of one
+    // 64-k chunk: full[s] completes when the X bytes have landed and the eight
+    // dequantising warps have stored A; empty[s] when the MMAs reading both
+    // are done (one commit).
+    uint64_t* full = bars;
+    uint64_t* empty = full + SK;
+    uint64_t* rf = empty + SK;
     uint64_t* re = rf + SR;
-    uint64_t* af = re + SR;
-    uint64_t* ae = af + SA;
-    uint64_t* accf = ae + SA;
+    uint64_t* accf = re + SR;
     uint64_t* acce = accf + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -143,9 +150,8 @@ __global__ void __launch_bounds__(gq::THREADS, 1)
     const int nsb = a.cols / 256;
 
     if (tid == 0) {
-        for (int i = 0; i < SX; ++i) { mbar_init(&xf[i], 1); mbar_init(&xe[i], 1); }
+        for (int i = 0; i < SK; ++i) { mbar_init(&full[i], DEQ_WARPS + 1); mbar_init(&empty[i], 1); }
         for (int i = 0; i < SR; ++i) { mbar_init(&rf[i], 1); mbar_init(&re[i], DEQ_WARPS); }
-        for (int i = 0; i < SA; ++i) { mbar_init(&af[i], DEQ_WARPS); mbar_init(&ae[i], 1); }
         for (int i = 0; i < 2; ++i) { mbar_init(&accf[i], 1); mbar_init(&acce[i], 4); }
         *abort_flag = 0;
         fence_barrier_init();
@@ -173,10 +179,10 @@ __global__ void __launch_bounds__(gq::THREADS, 1)
             for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x) {
                 const int nt = t / n_rt;
                 for (int kk = 0; kk < nk; ++kk) {
-                    if (!mbar_wait_bounded(&xe[s], ph, a.status)) { fail(); break; }
-                    mbar_arrive_expect_tx(&xf[s], X_BYTES);
-                    tma_load_2d(smem + OFF_X + s * X_BYTES, &tmX, kk * BK, nt * BN, &xf[s]);
-                    if (++s == SX) { s = 0; ph ^= 1; }
+                    if (!mbar_wait_backoff(&empty[s], ph, a.status, 64)) { fail(); break; }
+                    mbar_arrive_expect_tx(&full[s], X_BYTES);
+                    tma_load_2d(smem + OFF_X + s * X_BYTES, &tmX, kk * BK, nt * BN, &full[s]);
+                    if (++s == SK) { s = 0; ph ^= 1; }
                 }
             }
         }
@@ -199,53 +205,58 @@ __global__ void __launch_bounds__(gq::THREADS, 1)
         // ---- MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16(BM, BN);
-            int sx = 0, sa = 0;
-            uint32_t pxf = 0, paf = 0;
+            int s = 0;
+            uint32_t pf = 0;
             int local = 0;
             for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x, ++local) {
-                const int buf = local & 1;
-                const uint32_t use = (uint32_t)(local >> 1);
+                const int buf = local % NBUF;
+                const uint32_t use = (uint32_t)(local / NBUF);
                 if (!mbar_wait_bounded(&acce[buf], (use & 1) ^ 1, a.status)) { fail(); break; }
                 tc_fence_after();
                 const uint32_t d = tmem + buf * BN;
                 bool bad = false;
                 for (int kk = 0; kk < nk; ++kk) {
-                    if (!mbar_wait_bounded(&af[sa], paf, a.status) || !mbar_wait_bounded(&xf[sx], pxf, a.status)) {
+                    if (!mbar_wait_bounded(&full[s], pf, a.status)) {
                         bad = true;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t adesc = smem_desc_sw128(smem + OFF_A + sa * A_BYTES);
-                    const uint64_t bdesc = smem_desc_sw128(smem + OFF_X + sx * X_BYTES);
+                    const uint32_t at = tmem + A_COL + s * A_STAGE_COLS;
+                    const uint64_t bdesc = smem_desc_sw128(smem + OFF_X + s * X_BYTES);
 #pragma unroll
-                    for (int k4 = 0; k4 < BK / 16; ++k4)   // 32 bytes per K = 16 step, inside the swizzle atom
-                        mma_f16(d, adesc + 2 * k4, bdesc + 2 * k4, idesc, (kk | k4) != 0);
-                    mma_commit(&ae[sa]);
-                    mma_commit(&xe[sx]);
-                    if (++sa == SA) { sa = 0; paf ^= 1; }
-                    if (++sx == SX) { sx = 0; pxf ^= 1; }
+                    for (int k4 = 0; k4 < BK / 16; ++k4)   // A: 8 TMEM columns, B: 32 bytes per K = 16 step
+                        mma_f16_ts(d, at + 8 * k4, bdesc + 2 * k4, idesc, (kk | k4) != 0);
+                    mma_commit(&empty[s]);
+                    if (++s == SK) { s = 0; pf ^= 1; }
                 }
                 if (bad) { fail(); break; }
                 mma_commit(&accf[buf]);
             }
         }
-    } else if (warp >= 4 && warp < 4 + DEQ_WARPS) {
-        // ---- dequantisers
+    } else if (warp >= 4 && warp < EPI_WARP0) {
+        // ---- dequantisers: thread t -> TMEM lane (row) t % 128 (warp % 4 is the
+        // warp's lane quarter), columns 8h.. and 16+8h.. of the A stage
         const int t0 = tid - 128;
-        int sr = 0, sa = 0;
-        uint32_t prf = 0, pae = 1;
+        const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + A_COL + 8 * (t0 >> 7);
+        int sr = 0, s = 0;
+        uint32_t prf = 0, pe = 1;
         for (int t = blockIdx.x; t < n_tiles && !__any_sync(0xffffffffu, *abort_flag); t += gridDim.x) {
             bool bad = false;
             for (int sb = 0; sb < nsb && !bad; ++sb) {
                 if (!__all_sync(0xffffffffu, mbar_wait_bounded(&rf[sr], prf, a.status))) { bad = true; break; }
                 const uint8_t* raw = smem + OFF_R + sr * R_BYTES;
                 for (int c = 0; c < 4; ++c) {
-                    if (!__all_sync(0xffffffffu, mbar_wait_bounded(&ae[sa], pae, a.status))) { bad = true; break; }
-                    dequant_q4k_tile(raw, smem + OFF_A + sa * A_BYTES, c, t0);
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // make the tile visible to the MMA
+                    if (!__all_sync(0xffffffffu, mbar_wait_bounded(&empty[s], pe, a.status))) { bad = true; break; }
+                    tc_fence_after();
+                    uint32_t lo[8], hi[8];
+                    dequant_q4k_regs(raw, c, t0, lo, hi);
+                    tmem_st8_async(ta + s * A_STAGE_COLS, lo);
+                    tmem_st8_async(ta + s * A_STAGE_COLS + 16, hi);
+                    tmem_wait_st();
+                    tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&af[sa]);
-                    if (++sa == SA) { sa = 0; pae ^= 1; }
+                    if (lane == 0) mbar_arrive(&full[s]);
+                    if (++s == SK) { s = 0; pe ^= 1; }
                 }
                 if (bad) break;
                 __syncwarp();
@@ -254,14 +265,14 @@ __global__ void __launch_bounds__(gq::THREADS, 1)
             }
             if (bad) { fail(); break; }
         }
-    } else if (warp >= 4 + DEQ_WARPS) {
+    } else if (warp >= EPI_WARP0) {
         // ---- epilogue: lane quarter (warp % 4) of the 128 TMEM lanes
         const int q = warp & 3;
         int local = 0;
         for (int t = blockIdx.x; t < n_tiles && !__any_sync(0xffffffffu, *abort_flag); t += gridDim.x, ++local) {
             const int rt = t % n_rt, nt = t / n_rt;
-            const int buf = local & 1;
-            const uint32_t use = (uint32_t)(local >> 1);
+            const int buf = local % NBUF;
+            const uint32_t use = (uint32_t)(local / NBUF);
             // warp-uniform: every lane must take part in the tcgen05.ld below
             if (!__all_sync(0xffffffffu, mbar_wait_bounded(&accf[buf], use & 1, a.status))) { fail(); break; }
             tc_fence_after();
@@ -343,9 +354,11 @@ int qmv_launch_gemm_q4k_bf16(const void* W, int64_t rows, int64_t cols, const vo
     a.m = (int)m;
     a.Y = Y;
     a.status = status_word();
-    // 256-token tiles unless they cannot even give every SM one tile.
+    // 256-token tiles unless they cannot give every SM a tile or pad the
+    // tokens by more than 128-token tiles would (by over 8%).
     const int64_t n_rt = (rows + gq::BM - 1) / gq::BM;
-    const bool narrow = n_rt * ((m + 255) / 256) < (int64_t)num_sms();
+    const int64_t pad256 = (m + 255) / 256 * 256, pad128 = (m + 127) / 128 * 128;
+    const bool narrow = n_rt * ((m + 255) / 256) < (int64_t)num_sms() || pad256 * 100 > pad128 * 108;
     const int BN = narrow ? 128 : 256;
     CUtensorMap tmX;
     if (!make_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, (uint64_t)cols, (uint64_t)m, (uint64_t)cols * 2,

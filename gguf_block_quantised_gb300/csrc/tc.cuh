@@ -128,6 +128,23 @@ __device__ __forceinline__ void tmem_st16_async(uint32_t taddr, const uint32_t (
           "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
         : "memory");
 }
+// 4 consecutive 32-bit TMEM columns of this thread's lane <- v (complete after
+// tmem_wait_st()).
+__device__ __forceinline__ void tmem_st4_async(uint32_t taddr, const uint32_t (&v)[4])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(v[0]), "r"(v[1]),
+                 "r"(v[2]), "r"(v[3])
+                 : "memory");
+}
+
+// 8 consecutive 32-bit TMEM columns of this thread's lane <- v (complete after
+// tmem_wait_st()).
+__device__ __forceinline__ void tmem_st8_async(uint32_t taddr, const uint32_t (&v)[8])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
+                 "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // 16 consecutive 32-bit TMEM columns of this thread's lane <- v; then wait

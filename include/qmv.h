@@ -205,11 +205,16 @@ int qmv_matmul(int fmt, const void* W, int64_t rows, int64_t cols,
  *   fmt   : QMV_FMT(wtype, atype) with the pairs of qmv_matvec: activations
  *           F32 (fp32 rows, 16-byte aligned) or the paired 8-bit blocks (one
  *           block row per input vector, 4-byte aligned), optionally
- *           | QMV_FLAG_QUANTIZE_X (fp32 rows quantised inside the kernel).
+ *           | QMV_FLAG_QUANTIZE_X (fp32 rows quantised inside the kernel);
+ *           or, for MXFP4 experts only, BF16 (bf16 rows, 16-byte aligned):
+ *           the grouped tensor-core GEMM, whose weights 2^(e-127)*E2M1 are
+ *           exact in bf16 (fp32 accumulation; rows < 2^30).
  *   n_expert in 1..1024, k in 1..64, n_tok*k <= 2^24.
- *   Results per (token, slot) are those of qmv_matvec on that expert's
- *   matrix (same arithmetic and reduction order), plus the bias; the down
- *   form's gate-weighted sum runs in fp32 in slot order.
+ *   Results per (token, slot) are, for F32 and 8-bit activations, those of
+ *   qmv_matvec on that expert's matrix (same arithmetic and reduction
+ *   order), plus the bias; with BF16 activations a token's result does not
+ *   depend on the other tokens routed with it.  The down form's
+ *   gate-weighted sum runs in fp32 in slot order.
  *   Workspace: qmv_workspace_size(QMV_OP_MOE, ...) bytes set by
  *           qmv_set_workspace(); calls that share the workspace must be
  *           ordered on one stream.
@@ -254,7 +259,9 @@ int qmv_moe_matvec_noalloc(int fmt, const void* W3d, int n_expert, int64_t rows,
 /* Workspace for the calls that need scratch. */
 enum { QMV_OP_MATVEC = 1, QMV_OP_MATMUL = 2, QMV_OP_MOE = 3 };
 /* Bytes of workspace `op` needs for these sizes (n = n_tok*k for MoE: the
- * grouping, 2050 + n ints, and n*rows fp32 slot outputs).  0 if none. */
+ * grouping, 2050 + n ints, and n*rows fp32 slot outputs; with BF16
+ * activations also the GEMM's slot list, about 2n ints, and the n packed
+ * bf16 activation rows, n*cols*2 bytes).  0 if none. */
 size_t qmv_workspace_size(int op, int fmt, int64_t rows, int64_t cols, int64_t n);
 /* Register a caller-owned device buffer (256-byte aligned) as the workspace of
  * the current device; NULL/0 clears it.  The library keeps the pointer only. */

@@ -40,6 +40,21 @@ def test_matmul_bf16_parity(qmv, orc, rows, cols, m):
     qmv.qmv_get_status()
 
 
+@pytest.mark.parametrize("rows,m", [(9700, 500), (19500, 200)])
+def test_matmul_many_tiles_parity(qmv, orc, rows, m):
+    """Enough row tiles that every SM gets at least one: 256-token tiles (the
+    wide tile of the large prefill shapes; 9700 x 500) and several 128-token
+    tiles per SM (19500 x 200), each with a ragged last row tile and a ragged
+    last token tile; every output checked."""
+    cols = 256
+    W = synth.weights(Q4_K, rows, cols, seed=8, tensor_id=rows)
+    xb, xbits = bf16_x(m, cols, 8)
+    Y = run_matmul(qmv, dev(W), rows, cols, xb, m)
+    yref, yabs = orc.matvec(Q4_K, BF16, W, rows, cols, xbits, m)
+    assert_close(Y, yref, yabs, what=f"{rows}x{cols} m={m}")
+    qmv.qmv_get_status()
+
+
 @pytest.mark.parametrize("rows,cols,m", [(14336, 4096, 512), (4096, 14336, 512), (14336, 4096, 2048),
                                          (4096, 14336, 2048)])
 def test_matmul_config_shapes_sampled(qmv, orc, rows, cols, m):
