@@ -23,8 +23,9 @@
 // would leave SMs idle or pad the tokens more), K = 16 per instruction, A from
 // TMEM, B from shared memory, fp32 accumulator in TMEM.  TMEM holds 256
 // accumulator columns (two 128-column buffers, so that one tile's epilogue
-// overlaps the next tile's MMAs, or one 256-column buffer) and four 32-column
-// A stages.  X and A of a 64-k stage share one full and one empty barrier.  Every
+// overlaps the next tile's MMAs, or one 256-column buffer) and two 64-column
+// A stages.  X and A of a 128-k stage share one full and one empty barrier, so
+// the MMA thread waits once and commits once per eight MMAs.  Every
 // mbarrier wait is bounded; on a timeout the kernel flags the status word,
 // unwinds and frees its TMEM.
 #include <cuda.h>
@@ -37,12 +38,13 @@
 namespace qmv {
 
 namespace gq {
-constexpr int BM = 128, BK = 64;
-constexpr int SK = 4, SR = 3;               // k stages (X tile + A tile), raw stages
-constexpr int X_BYTES_MAX = 256 * BK * 2;   // 32768 (BN = 256)
+constexpr int BM = 128, BK = 64;           // BK: k of one 128-byte swizzled X row = one TMA box
+constexpr int KSUB = 2;                     // 64-k sub-chunks per k stage (8 MMAs per barrier round)
+constexpr int SK = 2, SR = 3;               // k stages (X tiles + A tile), raw stages
+constexpr int X_BYTES_MAX = 256 * BK * 2;   // 32768 per sub-chunk (BN = 256)
 constexpr int R_BYTES = BM * 144;           // 18432
 constexpr int OFF_X = 0;
-constexpr int OFF_R = OFF_X + SK * X_BYTES_MAX;
+constexpr int OFF_R = OFF_X + SK * KSUB * X_BYTES_MAX;
 constexpr int OFF_BAR = OFF_R + SR * R_BYTES;
 constexpr int N_BARS = 2 * SK + 2 * SR + 4;
 constexpr int SMEM = OFF_BAR + N_BARS * 8 + 16 + 1024;   // + alignment slack
@@ -50,7 +52,7 @@ constexpr int DEQ_WARPS = 8;                // warps 4..11
 constexpr int EPI_WARP0 = 12;               // warps 12..15
 constexpr int THREADS = 512;                // 16 warps
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t A_STAGE_COLS = BK / 2;   // 64 bf16 k per row = 32 columns
+constexpr uint32_t A_STAGE_COLS = KSUB * BK / 2;   // 128 bf16 k per row = 64 columns
 // accumulators: two of 128 columns (BN = 128) or one of 256 (BN = 256)
 static_assert(256 + SK * A_STAGE_COLS <= TMEM_COLS, "TMEM budget");
 }  // namespace gq
@@ -129,8 +131,8 @@ __global__ void __launch_bounds__(gq::THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-    // k stage s holds the X tile (shared memory) and the A tile (TMEM) of one
-    // 64-k chunk: full[s] completes when the X bytes have landed and the eight
+    // k stage s holds the X tiles (shared memory) and the A tile (TMEM) of 128
+    // k: full[s] completes when the X bytes have landed and the eight
     // dequantising warps have stored A; empty[s] when the MMAs reading both
     // are done (one commit).
     uint64_t* full = bars;
@@ -146,7 +148,7 @@ __global__ void __launch_bounds__(gq::THREADS, 1)
     const int n_rt = (int)((a.rows + BM - 1) / BM);
     const int n_nt = (a.m + BN - 1) / BN;
     const int n_tiles = n_rt * n_nt;
-    const int nk = a.cols / BK;
+    const int nks = a.cols / (KSUB * BK);   // k stages per tile
     const int nsb = a.cols / 256;
 
     if (tid == 0) {
@@ -178,10 +180,13 @@ __global__ void __launch_bounds__(gq::THREADS, 1)
             uint32_t ph = 1;
             for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x) {
                 const int nt = t / n_rt;
-                for (int kk = 0; kk < nk; ++kk) {
+                for (int ks = 0; ks < nks; ++ks) {
                     if (!mbar_wait_backoff(&empty[s], ph, a.status, 64)) { fail(); break; }
-                    mbar_arrive_expect_tx(&full[s], X_BYTES);
-                    tma_load_2d(smem + OFF_X + s * X_BYTES, &tmX, kk * BK, nt * BN, &full[s]);
+                    mbar_arrive_expect_tx(&full[s], KSUB * X_BYTES);
+#pragma unroll
+                    for (int j = 0; j < KSUB; ++j)
+                        tma_load_2d(smem + OFF_X + (s * KSUB + j) * X_BYTES, &tmX, (ks * KSUB + j) * BK, nt * BN,
+                                    &full[s]);
                     if (++s == SK) { s = 0; ph ^= 1; }
                 }
             }
@@ -215,17 +220,20 @@ __global__ void __launch_bounds__(gq::THREADS, 1)
                 tc_fence_after();
                 const uint32_t d = tmem + buf * BN;
                 bool bad = false;
-                for (int kk = 0; kk < nk; ++kk) {
+                for (int ks = 0; ks < nks; ++ks) {
                     if (!mbar_wait_bounded(&full[s], pf, a.status)) {
                         bad = true;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t at = tmem + A_COL + s * A_STAGE_COLS;
-                    const uint64_t bdesc = smem_desc_sw128(smem + OFF_X + s * X_BYTES);
 #pragma unroll
-                    for (int k4 = 0; k4 < BK / 16; ++k4)   // A: 8 TMEM columns, B: 32 bytes per K = 16 step
-                        mma_f16_ts(d, at + 8 * k4, bdesc + 2 * k4, idesc, (kk | k4) != 0);
+                    for (int j = 0; j < KSUB; ++j) {
+                        const uint64_t bdesc = smem_desc_sw128(smem + OFF_X + (s * KSUB + j) * X_BYTES);
+#pragma unroll
+                        for (int k4 = 0; k4 < BK / 16; ++k4)   // A: 8 TMEM columns, B: 32 bytes per K = 16 step
+                            mma_f16_ts(d, at + 32 * j + 8 * k4, bdesc + 2 * k4, idesc, (ks | j | k4) != 0);
+                    }
                     mma_commit(&empty[s]);
                     if (++s == SK) { s = 0; pf ^= 1; }
                 }
@@ -245,13 +253,16 @@ __global__ void __launch_bounds__(gq::THREADS, 1)
             for (int sb = 0; sb < nsb && !bad; ++sb) {
                 if (!__all_sync(0xffffffffu, mbar_wait_bounded(&rf[sr], prf, a.status))) { bad = true; break; }
                 const uint8_t* raw = smem + OFF_R + sr * R_BYTES;
-                for (int c = 0; c < 4; ++c) {
+                for (int cs = 0; cs < 4 / KSUB; ++cs) {
                     if (!__all_sync(0xffffffffu, mbar_wait_bounded(&empty[s], pe, a.status))) { bad = true; break; }
                     tc_fence_after();
-                    uint32_t lo[8], hi[8];
-                    dequant_q4k_regs(raw, c, t0, lo, hi);
-                    tmem_st8_async(ta + s * A_STAGE_COLS, lo);
-                    tmem_st8_async(ta + s * A_STAGE_COLS + 16, hi);
+#pragma unroll
+                    for (int j = 0; j < KSUB; ++j) {
+                        uint32_t lo[8], hi[8];
+                        dequant_q4k_regs(raw, cs * KSUB + j, t0, lo, hi);
+                        tmem_st8_async(ta + s * A_STAGE_COLS + 32 * j, lo);
+                        tmem_st8_async(ta + s * A_STAGE_COLS + 32 * j + 16, hi);
+                    }
                     tmem_wait_st();
                     tc_fence_before();
                     __syncwarp();
