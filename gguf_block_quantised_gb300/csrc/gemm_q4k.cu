@@ -7,7 +7,7 @@
 // are dequantised to bf16 (w = d*sc*q - dmin*m in fp32, one rounding, then
 // rounded to bf16) and multiplied with bf16 activations, accumulating in fp32.
 //
-// One persistent CTA per SM, 16 warps, warp-specialised:
+// One persistent CTA per SM, 20 warps, warp-specialised:
 //   warp 0      TMA producer of activation tiles X[BN tokens][64 k] (bf16,
 //               128-byte swizzle, the UMMA K-major canonical layout)
 //   warp 1      TMEM owner (alloc/free) and the single-thread MMA issuer
@@ -17,7 +17,7 @@
 //               two k per column), packed fp32x2 arithmetic.  A never touches
 //               shared memory, which leaves the shared-memory bandwidth to the
 //               MMA's reads of X and to the TMA writes.
-//   warps 12-15 epilogue: TMEM -> registers -> Y, one 128-byte row segment
+//   warps 12-19 epilogue: TMEM -> registers -> Y, one 128-byte row segment
 //               per column, so every store is coalesced
 // MMA: M = 128 weight rows, N = BN tokens (256, or 128 when 256-token tiles
 // would leave SMs idle or pad the tokens more), K = 16 per instruction, A from
@@ -49,8 +49,9 @@ constexpr int OFF_BAR = OFF_R + SR * R_BYTES;
 constexpr int N_BARS = 2 * SK + 2 * SR + 4;
 constexpr int SMEM = OFF_BAR + N_BARS * 8 + 16 + 1024;   // + alignment slack
 constexpr int DEQ_WARPS = 8;                // warps 4..11
-constexpr int EPI_WARP0 = 12;               // warps 12..15
-constexpr int THREADS = 512;                // 16 warps
+constexpr int EPI_WARP0 = 12;               // warps 12..19
+constexpr int EPI_WARPS = 8;                // two per TMEM lane quarter, each half of the columns
+constexpr int THREADS = 640;                // 20 warps
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t A_STAGE_COLS = KSUB * BK / 2;   // 128 bf16 k per row = 64 columns
 // accumulators: two of 128 columns (BN = 128) or one of 256 (BN = 256)
@@ -154,7 +155,7 @@ __global__ void __launch_bounds__(gq::THREADS, 1)
     if (tid == 0) {
         for (int i = 0; i < SK; ++i) { mbar_init(&full[i], DEQ_WARPS + 1); mbar_init(&empty[i], 1); }
         for (int i = 0; i < SR; ++i) { mbar_init(&rf[i], 1); mbar_init(&re[i], DEQ_WARPS); }
-        for (int i = 0; i < 2; ++i) { mbar_init(&accf[i], 1); mbar_init(&acce[i], 4); }
+        for (int i = 0; i < 2; ++i) { mbar_init(&accf[i], 1); mbar_init(&acce[i], EPI_WARPS); }
         *abort_flag = 0;
         fence_barrier_init();
         prefetch_tmap(&tmX);
@@ -277,8 +278,9 @@ __global__ void __launch_bounds__(gq::THREADS, 1)
             if (bad) { fail(); break; }
         }
     } else if (warp >= EPI_WARP0) {
-        // ---- epilogue: lane quarter (warp % 4) of the 128 TMEM lanes
-        const int q = warp & 3;
+        // ---- epilogue: lane quarter (warp % 4) of the 128 TMEM lanes, column
+        // half (warp - 12) / 4 of the tile
+        const int q = warp & 3, ch = (warp - EPI_WARP0) >> 2;
         int local = 0;
         for (int t = blockIdx.x; t < n_tiles && !__any_sync(0xffffffffu, *abort_flag); t += gridDim.x, ++local) {
             const int rt = t % n_rt, nt = t / n_rt;
@@ -289,7 +291,7 @@ __global__ void __launch_bounds__(gq::THREADS, 1)
             tc_fence_after();
             const int64_t row = (int64_t)rt * BM + 32 * q + lane;
             const bool row_ok = row < a.rows;
-            for (int c16 = 0; c16 < BN / 16; ++c16) {
+            for (int c16 = ch * BN / 32; c16 < (ch + 1) * BN / 32; ++c16) {
                 float v[16];
                 tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + buf * BN + c16 * 16, v);
                 const int tok0 = nt * BN + c16 * 16;
