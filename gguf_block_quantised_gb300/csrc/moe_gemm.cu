@@ -14,16 +14,16 @@
 //                 order (bf16 [n_valid][cols]) so one TMA tensor map covers
 //                 every expert's token tiles.
 //   k_moe_gemm_mxfp4_bf16   persistent, one CTA per SM, warp-specialised:
-//     warp 0      TMA producer of packed token tiles X[128 tokens][64 k]
-//                 (bf16, 128-byte swizzle)
+//     warp 0      TMA producer of packed token tiles X[128 tokens][128 k]
+//                 (bf16, two 64-k boxes with 128-byte swizzle)
 //     warp 1      TMEM owner and the single-thread MMA issuer
 //     warps 2-3, 16-19  raw weight producers: per weight row, the 16-byte pieces of
 //                 its next 8 MXFP4 blocks (256 k) as cp.async copies (the
 //                 1530-byte row pitch of the gpt-oss experts is not a legal
 //                 TMA tensor stride, and one bulk copy per 136-byte row
 //                 segment is bound by the copy engine's per-request cost)
-//     warps 4-11  dequantisers (two 64-k chunks per pass): MXFP4 -> bf16 A
-//                 tiles [128 rows][64 k] stored
+//     warps 4-11  dequantisers (one 128-k stage per pass): MXFP4 -> bf16 A
+//                 tiles [128 rows][128 k] stored
 //                 straight into TMEM (tcgen05.st; row = TMEM lane), through a
 //                 per-block table of the eight E2M1 magnitudes already scaled
 //                 by 2^(e-127).  Keeping A out of shared memory leaves the
@@ -32,7 +32,9 @@
 //                 plus the expert bias
 //   MMA M = 128 weight rows, N = 128 tokens, K = 16, A from TMEM, B (tokens)
 //   from shared memory, fp32 accumulator in TMEM, double-buffered so one
-//   tile's epilogue overlaps the next tile's MMAs.
+//   tile's epilogue overlaps the next tile's MMAs.  The X and A tiles of a
+//   128-k stage share one full and one empty barrier: one wait and one commit
+//   per eight MMAs.
 //   Every mbarrier wait is bounded; on a timeout the kernel flags the status
 //   word, unwinds and frees its TMEM.
 #include <cuda.h>
@@ -48,27 +50,29 @@ bool make_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint
                   uint64_t pitch, uint32_t box_in, uint32_t box_out, CUtensorMapSwizzle sw);
 
 namespace mg {
-constexpr int BM = 128, BN = 128, BK = 64;
-constexpr int SX = 4, SA = 4, SR = 4;
-constexpr int X_BYTES = BN * BK * 2;     // 16384
+constexpr int BM = 128, BN = 128, BK = 64;   // BK: k of one 128-byte swizzled X row = one TMA box
+constexpr int KSUB = 2;                  // 64-k sub-chunks per k stage (8 MMAs per barrier round)
+constexpr int SK = 3, SR = 4;            // k stages (X tiles + A tile), raw stages
+constexpr int X_BYTES = BN * BK * 2;     // 16384 per sub-chunk
 constexpr int SC_BLOCKS = 8;             // MXFP4 blocks per row per raw stage (256 k)
 constexpr int PIECES = 10;               // 16-byte pieces per row per raw stage: 136 bytes + up to 15 of alignment
 constexpr int SLOT = 176;                // bytes per row per raw stage (>= 16 * PIECES; 11 x 16 bytes, odd)
 constexpr int R_BYTES = BM * SLOT;       // 22528
 constexpr int OFF_X = 0;
-constexpr int OFF_R = OFF_X + SX * X_BYTES;
+constexpr int OFF_R = OFF_X + SK * KSUB * X_BYTES;
 constexpr int OFF_BAR = OFF_R + SR * R_BYTES;
-constexpr int N_BARS = 2 * SX + 2 * SR + 2 * SA + 4;
+constexpr int N_BARS = 2 * SK + 2 * SR + 4;
 constexpr int SMEM = OFF_BAR + N_BARS * 8 + 16 + 1024;   // + alignment slack
 constexpr int DEQ_WARPS = 8;             // warps 4..11
 constexpr int EPI_WARP0 = 12;            // warps 12..15
 constexpr int RAW_THREADS = 192;         // warps 2, 3 and 16..19
 constexpr int THREADS = 640;
-// TMEM columns: two 128-column fp32 accumulators, then SA bf16 A tiles of
-// 32 columns each (128 rows x 64 k, two elements per column).
+// TMEM columns: two 128-column fp32 accumulators, then SK bf16 A tiles of
+// 64 columns each (128 rows x 128 k, two elements per column).
 constexpr uint32_t A_COL = 2 * BN;
+constexpr uint32_t A_STAGE_COLS = KSUB * BK / 2;
 constexpr uint32_t TMEM_COLS = 512;
-static_assert(A_COL + SA * (BK / 2) <= TMEM_COLS, "TMEM budget");
+static_assert(A_COL + SK * A_STAGE_COLS <= TMEM_COLS, "TMEM budget");
 }  // namespace mg
 
 // 16-byte asynchronous copy global -> shared (dst, src 16-byte aligned);
@@ -255,13 +259,15 @@ __global__ void __launch_bounds__(mg::THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-    uint64_t* xf = bars;
-    uint64_t* xe = xf + SX;
-    uint64_t* rf = xe + SX;
+    // k stage s holds the X tiles (shared memory) and the A tile (TMEM) of 128
+    // k: full[s] completes when the X bytes have landed and the eight
+    // dequantising warps have stored A; empty[s] when the MMAs reading both
+    // are done (one commit).
+    uint64_t* full = bars;
+    uint64_t* empty = full + SK;
+    uint64_t* rf = empty + SK;
     uint64_t* re = rf + SR;
-    uint64_t* af = re + SR;
-    uint64_t* ae = af + SA;
-    uint64_t* accf = ae + SA;
+    uint64_t* accf = re + SR;
     uint64_t* acce = accf + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -270,13 +276,12 @@ __global__ void __launch_bounds__(mg::THREADS, 1)
     pdl_wait();
     const int n_rt = (int)((a.rows + BM - 1) / BM);
     const int n_tiles = n_rt * a.tiles[0];
-    const int nk = (a.nblk + 1) / 2;                       // 64-k chunks (the last may hold one block)
+    const int nks = (a.nblk + 3) / 4;                      // 128-k stages (the last may be partly empty)
     const int nsc = (a.nblk + SC_BLOCKS - 1) / SC_BLOCKS;  // raw stages per row
 
     if (tid == 0) {
-        for (int i = 0; i < SX; ++i) { mbar_init(&xf[i], 1); mbar_init(&xe[i], 1); }
+        for (int i = 0; i < SK; ++i) { mbar_init(&full[i], DEQ_WARPS + 1); mbar_init(&empty[i], 1); }
         for (int i = 0; i < SR; ++i) { mbar_init(&rf[i], RAW_THREADS); mbar_init(&re[i], DEQ_WARPS); }
-        for (int i = 0; i < SA; ++i) { mbar_init(&af[i], DEQ_WARPS); mbar_init(&ae[i], 1); }
         for (int i = 0; i < 2; ++i) { mbar_init(&accf[i], 1); mbar_init(&acce[i], 4); }
         *abort_flag = 0;
         fence_barrier_init();
@@ -307,11 +312,14 @@ __global__ void __launch_bounds__(mg::THREADS, 1)
                 int e, nt, rt;
                 tile_of(t, e, nt, rt);
                 const int row0 = a.offsets[e] + nt * BN;
-                for (int kk = 0; kk < nk; ++kk) {
-                    if (!mbar_wait_backoff(&xe[s], ph, a.status, 128)) { fail(); break; }
-                    mbar_arrive_expect_tx(&xf[s], X_BYTES);
-                    tma_load_2d(smem + OFF_X + s * X_BYTES, &tmX, kk * BK, row0, &xf[s]);
-                    if (++s == SX) { s = 0; ph ^= 1; }
+                for (int ks = 0; ks < nks; ++ks) {
+                    if (!mbar_wait_backoff(&empty[s], ph, a.status, 128)) { fail(); break; }
+                    mbar_arrive_expect_tx(&full[s], KSUB * X_BYTES);
+#pragma unroll
+                    for (int j = 0; j < KSUB; ++j)
+                        tma_load_2d(smem + OFF_X + (s * KSUB + j) * X_BYTES, &tmX, (ks * KSUB + j) * BK, row0,
+                                    &full[s]);
+                    if (++s == SK) { s = 0; ph ^= 1; }
                 }
             }
         }
@@ -351,8 +359,8 @@ __global__ void __launch_bounds__(mg::THREADS, 1)
         // ---- MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16(BM, BN);
-            int sx = 0, sa = 0;
-            uint32_t pxf = 0, paf = 0;
+            int s = 0;
+            uint32_t pf = 0;
             int local = 0;
             for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x, ++local) {
                 const int buf = local & 1;
@@ -361,21 +369,22 @@ __global__ void __launch_bounds__(mg::THREADS, 1)
                 tc_fence_after();
                 const uint32_t d = tmem + buf * BN;
                 bool bad = false;
-                for (int kk = 0; kk < nk; ++kk) {
-                    if (!mbar_wait_bounded(&af[sa], paf, a.status) || !mbar_wait_bounded(&xf[sx], pxf, a.status)) {
+                for (int ks = 0; ks < nks; ++ks) {
+                    if (!mbar_wait_bounded(&full[s], pf, a.status)) {
                         bad = true;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t at = tmem + A_COL + sa * (BK / 2);
-                    const uint64_t bdesc = smem_desc_sw128(smem + OFF_X + sx * X_BYTES);
+                    const uint32_t at = tmem + A_COL + s * A_STAGE_COLS;
 #pragma unroll
-                    for (int k4 = 0; k4 < BK / 16; ++k4)   // A: 8 TMEM columns, B: 32 bytes per K = 16 step
-                        mma_f16_ts(d, at + 8 * k4, bdesc + 2 * k4, idesc, (kk | k4) != 0);
-                    mma_commit(&ae[sa]);
-                    mma_commit(&xe[sx]);
-                    if (++sa == SA) { sa = 0; paf ^= 1; }
-                    if (++sx == SX) { sx = 0; pxf ^= 1; }
+                    for (int j = 0; j < KSUB; ++j) {
+                        const uint64_t bdesc = smem_desc_sw128(smem + OFF_X + (s * KSUB + j) * X_BYTES);
+#pragma unroll
+                        for (int k4 = 0; k4 < BK / 16; ++k4)   // A: 8 TMEM columns, B: 32 bytes per K = 16 step
+                            mma_f16_ts(d, at + 32 * j + 8 * k4, bdesc + 2 * k4, idesc, (ks | j | k4) != 0);
+                    }
+                    mma_commit(&empty[s]);
+                    if (++s == SK) { s = 0; pf ^= 1; }
                 }
                 if (bad) { fail(); break; }
                 mma_commit(&accf[buf]);
@@ -387,8 +396,8 @@ __global__ void __launch_bounds__(mg::THREADS, 1)
         // 64-k chunk c, i.e. A tile columns 16 * (t / 128) .. +15
         const int t0 = tid - 128, r = t0 & 127, half = t0 >> 7;
         const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + A_COL + 16 * half;
-        int sr = 0, sa = 0;
-        uint32_t prf = 0, pae = 1;
+        int sr = 0, s = 0;
+        uint32_t prf = 0, pe = 1;
         for (int t = blockIdx.x; t < n_tiles && !__any_sync(0xffffffffu, *abort_flag); t += gridDim.x) {
             int e, nt, rt;
             tile_of(t, e, nt, rt);
@@ -401,46 +410,28 @@ __global__ void __launch_bounds__(mg::THREADS, 1)
                 const int off = (int)((row_start + (int64_t)sc * SC_BLOCKS * 17) & 15);
                 const int nb = min(SC_BLOCKS, a.nblk - sc * SC_BLOCKS);
                 const int nc = (nb + 1) / 2;
-                // two chunks per pass: two independent blocks per thread in
-                // flight, one wait for both TMEM stores
-                for (int c = 0; c < nc; c += 2) {
-                    const bool two = c + 1 < nc;
-                    const int sb = sa + 1 == SA ? 0 : sa + 1;
-                    const uint32_t pb = sb == 0 ? pae ^ 1 : pae;
-                    if (!__all_sync(0xffffffffu, mbar_wait_bounded(&ae[sa], pae, a.status) &&
-                                                     (!two || mbar_wait_bounded(&ae[sb], pb, a.status)))) {
-                        bad = true;
-                        break;
-                    }
+                // one 128-k stage (chunks 2cs, 2cs+1) per pass: two independent
+                // blocks per thread in flight, one wait for both TMEM stores
+                for (int cs = 0; 2 * cs < nc; ++cs) {
+                    if (!__all_sync(0xffffffffu, mbar_wait_bounded(&empty[s], pe, a.status))) { bad = true; break; }
                     tc_fence_after();
-                    uint32_t o0[16], o1[16];
-                    const int b0i = 2 * c + half, b1i = b0i + 2;
-                    if (row < a.rows && b0i < nb) {
-                        mxfp4_block_bf16(slot, off + 17 * b0i, o0);
-                    } else {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) o0[i] = 0u;
-                    }
-                    tmem_st16_async(ta + sa * (BK / 2), o0);
-                    if (two) {
-                        if (row < a.rows && b1i < nb) {
-                            mxfp4_block_bf16(slot, off + 17 * b1i, o1);
+                    for (int j = 0; j < KSUB; ++j) {
+                        const int blk = 2 * (KSUB * cs + j) + half;
+                        uint32_t o[16];
+                        if (row < a.rows && blk < nb) {
+                            mxfp4_block_bf16(slot, off + 17 * blk, o);
                         } else {
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) o1[i] = 0u;
+                            for (int i = 0; i < 16; ++i) o[i] = 0u;
                         }
-                        tmem_st16_async(ta + sb * (BK / 2), o1);
+                        tmem_st16_async(ta + s * A_STAGE_COLS + 32 * j, o);
                     }
                     tmem_wait_st();
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) {
-                        mbar_arrive(&af[sa]);
-                        if (two) mbar_arrive(&af[sb]);
-                    }
-                    const int adv = two ? 2 : 1;
-                    for (int i = 0; i < adv; ++i)
-                        if (++sa == SA) { sa = 0; pae ^= 1; }
+                    if (lane == 0) mbar_arrive(&full[s]);
+                    if (++s == SK) { s = 0; pe ^= 1; }
                 }
                 if (bad) break;
                 __syncwarp();
