@@ -108,11 +108,13 @@ struct E2m1Tab {
 
 __device__ __forceinline__ bool e2m1_table(uint32_t e, E2m1Tab& t)
 {
-    const uint32_t b = e << 7, bb = b | (b << 16);
-    const uint32_t p01 = (b - 128u) << 16;    // [0, 0.5 s]
-    const uint32_t p23 = bb + 0x00400000u;    // [1 s, 1.5 s]
-    const uint32_t p45 = bb + 0x00C00080u;    // [2 s, 3 s]
-    const uint32_t p67 = bb + 0x01400100u;    // [4 s, 6 s]
+    // pairs of 16-bit patterns (low half = even magnitude): with b = e << 7,
+    // [0, b - 128], [b, b + 64], [b + 128, b + 192], [b + 256, b + 320];
+    // written as multiply-adds of e
+    const uint32_t p01 = e * 0x00800000u - 0x00800000u;
+    const uint32_t p23 = e * 0x00800080u + 0x00400000u;
+    const uint32_t p45 = e * 0x00800080u + 0x00C00080u;
+    const uint32_t p67 = e * 0x00800080u + 0x01400100u;
     t.hi0 = prmt(p01, p23, 0x7531u);
     t.hi1 = prmt(p45, p67, 0x7531u);
     t.lo0 = prmt(p01, p23, 0x6420u);
@@ -120,21 +122,28 @@ __device__ __forceinline__ bool e2m1_table(uint32_t e, E2m1Tab& t)
     return e - 2u <= 250u;
 }
 
-// Four E2M1 codes, the nibbles of the selector's low 16 bits (elements i,
-// i+16, i+1, i+17 of a block: the low and high nibbles of code bytes i and
-// i+1), -> bf16 pairs (i, i+1) and (i+16, i+17).
-__device__ __forceinline__ void e2m1_quad(uint32_t s, const E2m1Tab& t, uint32_t& p_lo, uint32_t& p_hi)
+// Eight E2M1 codes, the nibbles of code word w (bytes i..i+3 of a block:
+// element i+j in the low nibble of byte j, element i+16+j in the high one),
+// -> bf16 pairs o_lo[0] = (i, i+1), o_lo[1] = (i+2, i+3), o_hi[0] =
+// (i+16, i+17), o_hi[1] = (i+18, i+19).
+__device__ __forceinline__ void e2m1_word(uint32_t w, const E2m1Tab& t, uint32_t (&o_lo)[2], uint32_t (&o_hi)[2])
 {
-    const uint32_t mag = s & 0x7777u;
-    uint32_t H = prmt(t.hi0, t.hi1, mag);
-    const uint32_t L = prmt(t.lo0, t.lo1, mag);
-    // 0xff in the bytes whose code has its sign bit (nibble bit 3) set: a
-    // selector nibble with bit 3 set makes prmt.b32 replicate bit 7 of the
-    // selected byte.
-    const uint32_t neg = prmt(s << 4, s, 0xd9c8u);
-    H |= neg & 0x80808080u;
-    p_lo = prmt(L, H, 0x6240u);
-    p_hi = prmt(L, H, 0x7351u);
+    // prmt.b32 reads a selector's low 16 bits; bit 3 of a selector nibble
+    // switches to replicating bit 7 of the selected byte, so magnitudes are
+    // masked to 3 bits, and the sign masks come from that replication:
+    // byte k of (w << 4) has the sign of the even nibbles in bit 7, byte k of
+    // w that of the odd ones.
+    const uint32_t mag = w & 0x77777777u, mag_h = mag >> 16, w4 = w << 4;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const uint32_t m = q ? mag_h : mag;
+        uint32_t H = prmt(t.hi0, t.hi1, m);
+        const uint32_t L = prmt(t.lo0, t.lo1, m);
+        const uint32_t neg = prmt(w4, w, q ? 0xfbeau : 0xd9c8u);   // 0xff where the code is negative
+        H |= neg & 0x80808080u;
+        o_lo[q] = prmt(L, H, 0x6240u);
+        o_hi[q] = prmt(L, H, 0x7351u);
+    }
 }
 
 // Exact bf16 of one block whose exponent leaves the table's range (zero or
@@ -160,35 +169,25 @@ __device__ __forceinline__ void mxfp4_block_bf16_slow(uint32_t e, const uint32_t
     }
 }
 
-// One 32-element MXFP4 block (17 bytes at byte offset o of a 16-byte-aligned
-// shared-memory row slot; o % 16 + 17 <= 32) -> 16 bf16x2 words in element
-// order (word i = elements 2i, 2i+1).  The block is read with two aligned
-// 16-byte loads and shifted into place in registers.
+// One 32-element MXFP4 block (17 bytes at byte offset o of a shared-memory
+// row slot, any alignment) -> 16 bf16x2 words in element order (word i =
+// elements 2i, 2i+1).
 __device__ __forceinline__ void mxfp4_block_bf16(const uint8_t* slot, int o, uint32_t (&out)[16])
 {
-    const uint4* p = reinterpret_cast<const uint4*>(slot + (o & ~15));
-    const uint4 u0 = p[0], u1 = p[1];
-    const uint32_t W[9] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w, 0u};
-    const int q = (o >> 2) & 3;
-    uint32_t Y[7], X[6];
-#pragma unroll
-    for (int i = 0; i < 7; ++i) Y[i] = (q & 2) ? W[i + 2] : W[i];
-#pragma unroll
-    for (int i = 0; i < 6; ++i) X[i] = (q & 1) ? Y[i + 1] : Y[i];
-    const uint32_t sh = (uint32_t)(o & 3) * 8u;
-    uint32_t w5[5];
-#pragma unroll
-    for (int k = 0; k < 5; ++k) w5[k] = __funnelshift_r(X[k], X[k + 1], sh);   // byte 0: exponent, 1..16: codes
-    const uint32_t e = w5[0] & 0xffu;
+    const uint8_t* p = slot + o;
+    const uint32_t e = p[0];
     uint32_t w[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) w[k] = __funnelshift_r(w5[k], w5[k + 1], 8);
+    load_words<4>(p + 1, w);   // the 16 code bytes
     E2m1Tab t;
     if (e2m1_table(e, t)) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            e2m1_quad(w[k], t, out[2 * k], out[8 + 2 * k]);
-            e2m1_quad(w[k] >> 16, t, out[2 * k + 1], out[8 + 2 * k + 1]);
+            uint32_t lo[2], hi[2];
+            e2m1_word(w[k], t, lo, hi);
+            out[2 * k] = lo[0];
+            out[2 * k + 1] = lo[1];
+            out[8 + 2 * k] = hi[0];
+            out[8 + 2 * k + 1] = hi[1];
         }
     } else {
         mxfp4_block_bf16_slow(e, w, out);
