@@ -5,8 +5,10 @@ Workload (one step): a Qwen2.5-0.5B-shaped decode step through the W4A8 path
 -- for each of 24 layers, the fp32 activations are quantised to Q8_0 blocks
 and multiplied by q 896x896, k 128x896, v 128x896, o 896x896, gate 4864x896,
 up 4864x896 and down 896x4864 weights in Q5_0; then the lm_head 151936x896 in
-Q8_0.  169 matvec launches, each quantising its own input, chained with
-programmatic dependent launch; 390,648,832 weight bytes per step
+Q8_0.  Matrices that read the same activations are stored stacked (q|k|v,
+gate|up), so a step is 97 matvec launches (4 per layer + lm_head), each
+quantising its own input, chained with programmatic dependent launch;
+390,648,832 weight bytes per step
 (372.55 MiB), synthetic weights and N(0,1) activations, batch 1.
 The weights (> 3x the 129 MB L2) are streamed cold every step.
 
@@ -45,6 +47,10 @@ HID, FFN, KV, VOCAB = 896, 4864, 128, 151936
 LAYER_MATS = [("q", HID, HID, 0), ("k", KV, HID, 0), ("v", KV, HID, 0), ("o", HID, HID, 1),
               ("gate", FFN, HID, 2), ("up", FFN, HID, 2), ("down", HID, FFN, 3)]
 IN_COLS = [HID, HID, HID, FFN]
+# Matrices that read the same input are stored stacked (rows concatenated) and
+# multiplied by one launch: q|k|v, o, gate|up, down.  Same weights and bytes as
+# the seven matrices; four dependent launches per layer.
+LAYER_GROUPS = [[0, 1, 2], [3], [4, 5], [6]]
 
 
 def row_bytes(t, cols):
@@ -136,10 +142,13 @@ class ClockSampler:
 class DecodeStep:
     """Weights and buffers of the Qwen2.5-0.5B-shaped decode step on one device.
 
-    fused=True: each matvec quantises its fp32 activations itself
-    (QMV_FLAG_QUANTIZE_X) and is launched as a programmatic dependent of the
-    one before (QMV_FLAG_PDL): 169 launches per step.  fused=False: separate
-    qmv_quantize_act launches, plain stream order: 266 launches per step."""
+    The seven matrices of a layer are held as four stacked groups (q|k|v,
+    o, gate|up, down: the matrices of a group read the same activations), so
+    a step is 24 x 4 + 1 = 97 matvecs.  fused=True: each matvec quantises
+    its fp32 activations itself (QMV_FLAG_QUANTIZE_X) and is launched as a
+    programmatic dependent of the one before (QMV_FLAG_PDL): 97 launches per
+    step.  fused=False: separate qmv_quantize_act launches, plain stream
+    order: 194 launches per step."""
 
     def __init__(self, q, torch, n_vec, seed=1, fused=True):
         self.q, self.torch, self.n_vec, self.fused = q, torch, n_vec, fused
@@ -147,12 +156,16 @@ class DecodeStep:
         self.W = []
         tid = 0
         for layer in range(LAYERS):
-            mats = []
-            for name, rows, cols, inp in LAYER_MATS:
-                mats.append((torch.from_numpy(synth.weights(Q5_0, rows, cols, seed=seed, tensor_id=tid)).to(dev),
-                             rows, cols, inp))
-                tid += 1
-            self.W.append(mats)
+            mats = [synth.weights(Q5_0, rows, cols, seed=seed, tensor_id=tid + m)
+                    for m, (name, rows, cols, inp) in enumerate(LAYER_MATS)]
+            tid += len(LAYER_MATS)
+            groups = []
+            for g in LAYER_GROUPS:
+                rows = sum(LAYER_MATS[m][1] for m in g)
+                cols, inp = LAYER_MATS[g[0]][2], LAYER_MATS[g[0]][3]
+                W = np.concatenate([mats[m] for m in g])   # rows are contiguous: stacking = concatenation
+                groups.append((torch.from_numpy(W).to(dev), rows, cols, inp))
+            self.W.append(groups)
         self.lm = torch.from_numpy(synth.weights(Q8_0, VOCAB, HID, seed=seed, tensor_id=tid)).to(dev)
         # activations: 4 inputs per layer + the final hidden state
         self.x_host = [synth.activations(n_vec, IN_COLS[i], seed=seed, tensor_id=10000 + 4 * l + i)
@@ -161,10 +174,11 @@ class DecodeStep:
         self.x = [torch.from_numpy(a).to(dev) for a in self.x_host]
         self.xq = [torch.empty(n_vec * q.qmv_row_bytes(Q8_0, a.shape[1]), dtype=torch.uint8, device=dev)
                    for a in self.x_host]
-        self.y = [[torch.empty((n_vec, r), dtype=torch.float32, device=dev) for _, r, _, _ in LAYER_MATS]
+        self.y = [[torch.empty((n_vec, r), dtype=torch.float32, device=dev) for _, r, _, _ in self.W[0]]
                   for _ in range(LAYERS)]
         self.logits = torch.empty((n_vec, VOCAB), dtype=torch.float32, device=dev)
-        self.launches = LAYERS * 7 + 1 if fused else LAYERS * (4 + 7) + 2
+        per_layer = len(LAYER_GROUPS)
+        self.launches = LAYERS * per_layer + 1 if fused else LAYERS * (4 + per_layer) + 2
 
     def run(self, stream):
         q, n = self.q, self.n_vec
@@ -614,8 +628,9 @@ def main():
         "vs_baseline": None,
         "dtype": "int8xint4->fp32",
         "data": "synthetic",
-        "config": {"workload": "qwen2.5-0.5b-shaped decode step (24 layers q/k/v/o/gate/up/down Q5_0 + lm_head "
-                               "151936x896 Q8_0; fp32 activations quantised to Q8_0 inside each matvec), batch 1",
+        "config": {"workload": "qwen2.5-0.5b-shaped decode step (24 layers q/k/v/o/gate/up/down Q5_0, stored as "
+                               "q|k|v, o, gate|up, down stacks, + lm_head 151936x896 Q8_0; fp32 activations "
+                               "quantised to Q8_0 inside each matvec), batch 1",
                    "launches_per_step": step1.launches,
                    "weight_bytes_per_step": STEP_WEIGHT_BYTES, "parallelism": f"replicas x{ws}",
                    "l2": "weights 390.6 MB > 129 MB L2, streamed cold every step (no flush needed)",

@@ -69,17 +69,20 @@ __device__ __forceinline__ int64_t ceil16(int64_t v) { return (v + 15) & ~int64_
 
 // Producer warp: arm `bar` and issue the bulk copies of one work item (tile,
 // chunk): lane i copies row i's chunk (its 16-byte aligned superset) into its
-// slot.  The ragged end of the matrix past its last 16-byte boundary is
-// stored with plain loads before the arrive, whose release orders them for
-// the consumers.
-template <int BB>
+// slot (WIDE: tiles of up to 128 rows, lane i copies rows i, i+32, ...; or,
+// with p.contig, lane 0 copies the tile's consecutive whole rows at once).
+// The ragged end of the matrix past its last 16-byte boundary is stored with
+// plain loads before the arrive, whose release orders them for the consumers.
+// The decode kernels use the narrow form, whose code stays lean.
+template <int BB, bool WIDE = false>
 __device__ __forceinline__ void gemv_produce(const GemvParams& p, int64_t tile, int chunk, uint8_t* buf,
                                              uint64_t* bar, int tr = 0)
 {
+    constexpr int RPL = WIDE ? 4 : 1;   // rows per lane
     const int lane = threadIdx.x & 31;
     if (tr == 0) tr = kConsumerWarps * p.rpw;
     const int64_t lim = floor16(p.total);
-    if (p.contig) {
+    if (WIDE && p.contig) {
         // Rows r0 .. r1-1 are one byte range: copy its 16-byte aligned superset
         // at once (the ragged end of the matrix with plain loads).
         if (lane == 0) {
@@ -99,10 +102,12 @@ __device__ __forceinline__ void gemv_produce(const GemvParams& p, int64_t tile, 
     }
     const int c0 = chunk * p.kb;
     const int c1 = min(p.nb, c0 + p.kb);
-    uint32_t bytes[4] = {0, 0, 0, 0};   // up to 128 rows: 4 per lane
-    int64_t a[4] = {0, 0, 0, 0};
+    uint32_t bytes[RPL];
+    int64_t a[RPL];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < RPL; ++j) {
+        bytes[j] = 0;
+        a[j] = 0;
         const int i = lane + 32 * j;
         const int64_t r = tile * tr + i;
         if (i < tr && r < p.rows) {
@@ -115,7 +120,9 @@ __device__ __forceinline__ void gemv_produce(const GemvParams& p, int64_t tile, 
             for (int64_t k = max(lim, a[j]); k < e; ++k) slot[k - a[j]] = p.W[k];   // only the matrix's last row
         }
     }
-    uint32_t total = bytes[0] + bytes[1] + bytes[2] + bytes[3];
+    uint32_t total = 0;
+#pragma unroll
+    for (int j = 0; j < RPL; ++j) total += bytes[j];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
     // Order this buffer's earlier generic-proxy accesses (consumer reads,
@@ -125,7 +132,7 @@ __device__ __forceinline__ void gemv_produce(const GemvParams& p, int64_t tile, 
     if (lane == 0) mbar_arrive_expect_tx(bar, total);
     __syncwarp();
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
+    for (int j = 0; j < RPL; ++j)
         if (bytes[j]) bulk_g2s(buf + (size_t)(lane + 32 * j) * p.seg_cap, p.W + a[j], bytes[j], bar);
 }
 
@@ -140,9 +147,8 @@ __device__ __forceinline__ void gemv_rows(const GemvParams& p, const XView& X, c
     const uint8_t* rowp[RIF];
 #pragma unroll
     for (int j = 0; j < RIF; ++j)
-        rowp[j] = p.contig ? slot0 + (size_t)j * p.rb
-                           : slot0 + (size_t)j * p.seg_cap +
-                                 (((uint32_t)(r0 + j) * (uint32_t)p.rb + (uint32_t)c0 * (uint32_t)F::BB) & 15u);
+        rowp[j] = slot0 + (size_t)j * p.seg_cap +
+                  (((uint32_t)(r0 + j) * (uint32_t)p.rb + (uint32_t)c0 * (uint32_t)F::BB) & 15u);
     const int u0 = c0 * F::UPB, u1 = c1 * F::UPB;
 #pragma unroll 1
     for (int u = u0 + lane; u < u1; u += 32) {
@@ -215,7 +221,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_gemv(const GemvParams p)
     uint8_t* xs = smem + 256;
     uint8_t* stage0 = xs + ((p.xhat_bytes + 127) & ~127u);
     const int tr = kConsumerWarps * p.rpw;
-    const uint32_t stage_bytes = p.stage_bytes;
+    const uint32_t stage_bytes = p.seg_cap * (uint32_t)tr;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t n_tiles = (p.rows + tr - 1) / tr;
@@ -299,10 +305,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_gemv(const GemvParams p)
 #pragma unroll
                     for (int v = 0; v < NV; ++v) acc[j][v] = 0.f;
             }
-            const uint8_t* slot0 = p.contig ? buf + (((uint32_t)(tile * tr) * (uint32_t)p.rb) & 15u) +
-                                                  (size_t)(warp * p.rpw + g) * p.rb
-                                            : buf + (size_t)(warp * p.rpw + g) * p.seg_cap;
-            gemv_rows<T, A8, NV, RIF>(p, X, slot0, r0, nrows, c0, c1, acc);
+            gemv_rows<T, A8, NV, RIF>(p, X, buf + (size_t)(warp * p.rpw + g) * p.seg_cap, r0, nrows, c0, c1, acc);
             if (chunk == p.n_chunks - 1) {
                 const int row = RIF == 4 ? (lane >> 3) : (RIF == 2 ? (lane >> 4) : 0);
                 const bool writer = (lane & (32 / RIF - 1)) == 0;

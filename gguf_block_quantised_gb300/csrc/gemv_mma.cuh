@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_gemv_mma(const GemvParams p
         int64_t tile = blockIdx.x;
         int chunk = 0;
         for (int it = 0; it < S && it < n_items; ++it) {
-            gemv_produce<F::BB>(p, tile, chunk, stage0 + (size_t)it * stage_bytes, &full[it], tr);
+            gemv_produce<F::BB, true>(p, tile, chunk, stage0 + (size_t)it * stage_bytes, &full[it], tr);
             if (++chunk == p.n_chunks) { chunk = 0; tile += gridDim.x; }
         }
     }
@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_gemv_mma(const GemvParams p
         for (; it < n_items; ++it) {
             ok = mbar_wait_bounded(&empty[s], ph, p.status);
             if (!ok) break;
-            gemv_produce<F::BB>(p, tile, chunk, stage0 + (size_t)s * stage_bytes, &full[s], tr);
+            gemv_produce<F::BB, true>(p, tile, chunk, stage0 + (size_t)s * stage_bytes, &full[s], tr);
             if (++chunk == p.n_chunks) { chunk = 0; tile += gridDim.x; }
             if (++s == S) { s = 0; ph ^= 1u; }
         }
