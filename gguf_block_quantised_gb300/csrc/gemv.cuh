@@ -212,7 +212,10 @@ __device__ __forceinline__ float warp_sum_rows(const float (&v)[RIF])
 }
 
 template <int T, bool A8, int NV, int RIF>
-__global__ void __launch_bounds__(kGemvThreads, 1) k_gemv(const GemvParams p)
+// Decode with 8-bit activations and one or two vectors: registers for two CTAs
+// per SM (the K-quant decoders otherwise take ~165 and leave one 9-warp CTA
+// per SM, too few warps to keep the weight stream in flight).
+__global__ void __launch_bounds__(kGemvThreads, A8 && NV <= 2 ? 2 : 1) k_gemv(const GemvParams p)
 {
     using F = Fmt<T>;
     extern __shared__ __align__(128) uint8_t smem[];

@@ -55,25 +55,37 @@ inline bool plan_gemv(bool a8, int64_t rows, int64_t cols, int n_vec, GemvPlan& 
         // Accumulators stay in registers across K-chunks only for one row
         // group, so a multi-chunk row gives each warp as many rows as this
         // group's kernel decodes at once (smaller groups decode at least as many).
+        // With 8-bit activations and one or two vectors the kernel's registers
+        // allow two CTAs per SM, and tiles that let two CTAs share an SM (three
+        // stages each) are preferred over larger tiles with one CTA per SM;
+        // otherwise the largest tile wins, with two CTAs per SM if it fits.
         const int rif = rows_in_flight_rt(T, g);
-        for (int rpw = pl.n_chunks > 1 ? rif : max_rpw; rpw >= 1; rpw /= 2) {
-            if (pl.n_chunks > 1 && rpw != rif) break;
-            const size_t xb = xhat_bytes(T, a8, g, (int)cols);
-            if (xb > kXhatMaxBytes && g > 1) break;
-            const size_t stage = (size_t)pl.seg_cap * kConsumerWarps * rpw;
-            const size_t base = 256 + ((xb + 127) & ~size_t(127));
-            int S = base < kSmemTwoPerSm ? (int)((kSmemTwoPerSm - base) / stage) : 0;
-            if (S < 3) S = base < kSmemOnePerSm ? (int)((kSmemOnePerSm - base) / stage) : 0;
-            if (S >= 2) {
-                if (S > kMaxStages) S = kMaxStages;
-                pl.group = g;
-                pl.rpw = rpw;
-                pl.xhat_bytes = (uint32_t)xb;
-                pl.stages = S;
-                pl.smem = (uint32_t)(base + S * stage);
-                return true;
+        const bool prefer_two = a8 && g <= 2;
+        bool found = false;
+        for (int pass = prefer_two ? 0 : 2; pass < 3 && !found; ++pass) {
+            for (int rpw = pl.n_chunks > 1 ? rif : max_rpw; rpw >= 1; rpw /= 2) {
+                if (pl.n_chunks > 1 && rpw != rif) break;
+                const size_t xb = xhat_bytes(T, a8, g, (int)cols);
+                if (xb > kXhatMaxBytes && g > 1) break;
+                const size_t stage = (size_t)pl.seg_cap * kConsumerWarps * rpw;
+                const size_t base = 256 + ((xb + 127) & ~size_t(127));
+                // pass 0: two per SM only; 1: one per SM; 2: two if it fits, else one
+                int S2 = base < kSmemTwoPerSm ? (int)((kSmemTwoPerSm - base) / stage) : 0;
+                int S1 = base < kSmemOnePerSm ? (int)((kSmemOnePerSm - base) / stage) : 0;
+                int S = pass == 0 ? (S2 >= 3 ? S2 : 0) : pass == 1 ? S1 : (S2 >= 3 ? S2 : S1);
+                if (S >= 2) {
+                    if (S > kMaxStages) S = kMaxStages;
+                    pl.group = g;
+                    pl.rpw = rpw;
+                    pl.xhat_bytes = (uint32_t)xb;
+                    pl.stages = S;
+                    pl.smem = (uint32_t)(base + S * stage);
+                    found = true;
+                    break;
+                }
             }
         }
+        if (found) return true;
         if (g == 1) return false;
         --g;
     }
