@@ -254,15 +254,18 @@ def cpu_baseline(n_steps=4):
             "sample": f"{n_steps} full decode steps (batch 1, W4A8), single-threaded C oracle, {dt:.1f} s"}
 
 
-def lm_roofline(q, torch, stream, step, dev_index):
-    """The dominant kernel alone: the lm_head matvec (144.6 MB per launch).
-    Four copies of the weights rotate (578 MB > 4x L2), so every launch reads
-    its weights from HBM; 200 launches replay from one CUDA graph."""
+def lm_roofline(q, torch, stream, step, dev_index, pdl=True):
+    """The dominant kernel alone: the lm_head matvec (144.6 MB per launch),
+    launched as in the decode step (quantising its fp32 input; with pdl, as a
+    programmatic dependent of the launch before it).  Four copies of the
+    weights rotate (578 MB > 4x L2), so every launch reads its weights from
+    HBM; 200 launches replay from one CUDA graph.  Returns (ms per launch,
+    clocks)."""
     lm_copies = [step.lm] + [step.lm.clone() for _ in range(3)]
+    fl = q.FLAG_QUANTIZE_X | (q.FLAG_PDL if pdl else 0)
 
     def lm_only(s, Wl):
-        q.qmv_matvec(q.FMT(Q8_0, Q8_0) | q.FLAG_QUANTIZE_X, Wl, VOCAB, HID, step.x[-1], step.logits, 1,
-                     s.cuda_stream)
+        q.qmv_matvec(q.FMT(Q8_0, Q8_0) | fl, Wl, VOCAB, HID, step.x[-1], step.logits, 1, s.cuda_stream)
     lm_reps = 200
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
@@ -271,7 +274,8 @@ def lm_roofline(q, torch, stream, step, dev_index):
         with torch.cuda.graph(g, stream=stream):
             for i in range(lm_reps):
                 lm_only(stream, lm_copies[i % 4])
-    g.replay()
+    for _ in range(3):
+        g.replay()
     stream.synchronize()
     sampler = ClockSampler(dev_index)
     sampler.__enter__()
@@ -420,6 +424,7 @@ def run_probe(spec):
     """Single-kernel runs for profiling (ncu captures).  Specs:
       gemv:T:rows:cols:atype:n_vec   qmv_matvec on synthetic weights (atype 8 = fp32)
       gemm:rows:cols:m               qmv_matmul, Q4_K x bf16
+      step[:n_vec]                   one fused decode step of the Qwen2.5-0.5B shape (97 matvecs)
       moe:n_tok[:atype]              one gpt-oss-shaped MoE layer (gate_up + down); atype 3 = Q8_0
                                      quantised in-kernel (default), 9 = bf16 (grouped tensor-core GEMM)
     Each runs its call five times and prints the event-timed mean of the last three."""
@@ -448,6 +453,12 @@ def run_probe(spec):
         Y = torch.empty(m, rows, device="cuda")
         call = lambda: q.qmv_matmul(q.FMT(Q4_K, BF16), W, rows, cols, X, Y, m)
         nbytes, what = 2 * m * rows * cols / 1e3, "TFLOP/s"
+    elif kind == "step":
+        (n_vec,) = (a + [1])[:1]
+        step = DecodeStep(q, torch, n_vec)
+        stream = torch.cuda.current_stream()
+        call = lambda: step.run(stream)
+        nbytes, what = STEP_WEIGHT_BYTES, "weight GB/s"
     elif kind == "moe":
         n_tok, at = (a + [Q8_0])[:2]
         E, k = 32, 4
@@ -586,6 +597,7 @@ def main():
         ms1, ms8 = t.tolist()
 
     lm_ms, lm_clocks = lm_roofline(q, torch, stream, step1, local)
+    lm_ms_nopdl, _ = lm_roofline(q, torch, stream, step1, local, pdl=False)
     lm_bytes = VOCAB * row_bytes(Q8_0, HID)
     lm_gbs = lm_bytes / (lm_ms / 1e3) / 1e9
 
@@ -641,10 +653,13 @@ def main():
         "unfused_batch1": {"ms_per_step": ms1u, "value": ws * STEP_WEIGHT_BYTES / (ms1u / 1e3) / 1e9,
                            "unit": "GB/s", "launches_per_step": step1u.launches,
                            "how": "qmv_quantize_act + qmv_matvec as separate launches, no PDL"},
-        "roofline": {"bound": "hbm", "kernel": "k_gemv<Q8_0,A8,NV=1> lm_head 151936x896 (quantising its fp32 input)",
+        "roofline": {"bound": "hbm", "kernel": "k_gemv<Q8_0,A8,NV=1> lm_head 151936x896 (quantising its fp32 input; "
+                               "launched as in the step, a programmatic dependent of the launch before)",
                      "achieved": lm_gbs, "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": lm_gbs / hbm, "traffic": traffic_for("k_gemv<Q8_0,A8,NV=1> lm_head 151936x896"),
                      "algorithmic_bytes_per_launch": lm_bytes, "launch_ms": lm_ms,
+                     "launch_ms_plain_launches": lm_ms_nopdl,
+                     "achieved_plain_launches": lm_bytes / (lm_ms_nopdl / 1e3) / 1e9,
                      "launch_ms_before_step_graphs": lm_ms_first, "clocks": lm_clocks,
                      "l2": "4 weight copies rotated, each launch reads cold"},
         "clocks": clocks,
