@@ -356,7 +356,7 @@ def prefill_leg(q, torch, stream, tflops_peak):
     calls = [(lambda s, W=W: q.qmv_matmul(q.FMT(Q4_K, Q8_K), W, rows, cols, Xq, Y, m, s.cuda_stream)) for W in Ws]
     ms = time_rotating(torch, stream, calls, 8)
     w4a8 = {"shape": f"{rows}x{cols}_m{m}", "ms": ms, "tflops": 2.0 * m * rows * cols / (ms / 1e3) / 1e12,
-            "path": "exact int8 dp4a block dots (the decode engine over token groups of 16)"}
+            "path": "exact int8 block dots on mma.sync.m16n8k32 (the decode pipeline over 16-token groups)"}
     del Ws, Xq, Y
     q.qmv_get_status(stream)
     return {"metric": "prefill GEMM TFLOP/s (Q4_K x bf16, fp32 accumulate)", "unit": "TFLOP/s", "w4a8": w4a8,

@@ -34,7 +34,8 @@ inline int rows_in_flight_rt(int T, int nv)
 }
 
 template <int T>
-inline bool plan_gemv(bool a8, int64_t rows, int64_t cols, int n_vec, GemvPlan& pl, int max_rpw = 4)
+inline bool plan_gemv(bool a8, int64_t rows, int64_t cols, int n_vec, GemvPlan& pl, int max_rpw = 4,
+                      int64_t min_tiles = 0)
 {
     using F = Fmt<T>;
     const int nb = (int)(cols / F::BS);
@@ -63,16 +64,23 @@ inline bool plan_gemv(bool a8, int64_t rows, int64_t cols, int n_vec, GemvPlan& 
         const bool prefer_two = a8 && g <= 2;
         bool found = false;
         for (int pass = prefer_two ? 0 : 2; pass < 3 && !found; ++pass) {
-            for (int rpw = pl.n_chunks > 1 ? rif : max_rpw; rpw >= 1; rpw /= 2) {
-                if (pl.n_chunks > 1 && rpw != rif) break;
+            // Rows per warp: at most the rows the kernel decodes at once when a
+            // row spans several chunks (the accumulators then stay in registers
+            // across chunks); fewer while the matrix would give fewer than
+            // min_tiles tiles (small matrices spread over more SMs).
+            int rpw0 = pl.n_chunks > 1 ? rif : max_rpw;
+            while (rpw0 > 1 && (rows + kConsumerWarps * rpw0 - 1) / (kConsumerWarps * rpw0) < min_tiles) rpw0 /= 2;
+            for (int rpw = rpw0; rpw >= 1; rpw /= 2) {
                 const size_t xb = xhat_bytes(T, a8, g, (int)cols);
                 if (xb > kXhatMaxBytes && g > 1) break;
                 const size_t stage = (size_t)pl.seg_cap * kConsumerWarps * rpw;
                 const size_t base = 256 + ((xb + 127) & ~size_t(127));
-                // pass 0: two per SM only; 1: one per SM; 2: two if it fits, else one
+                // pass 0: two per SM only (tiles of two or more rows per warp may
+                // run two stages each: four per SM); 1: one per SM; 2: two if it
+                // fits, else one
                 int S2 = base < kSmemTwoPerSm ? (int)((kSmemTwoPerSm - base) / stage) : 0;
                 int S1 = base < kSmemOnePerSm ? (int)((kSmemOnePerSm - base) / stage) : 0;
-                int S = pass == 0 ? (S2 >= 3 ? S2 : 0) : pass == 1 ? S1 : (S2 >= 3 ? S2 : S1);
+                int S = pass == 0 ? (S2 >= (rpw >= 2 ? 2 : 3) ? S2 : 0) : pass == 1 ? S1 : (S2 >= 3 ? S2 : S1);
                 if (S >= 2) {
                     if (S > kMaxStages) S = kMaxStages;
                     pl.group = g;
@@ -222,12 +230,9 @@ inline int launch_gemv_t(bool a8, bool quant_x, bool pdl, const void* W, int64_t
     using F = Fmt<T>;
     if (rows == 0 || n_vec == 0) return 0;
     GemvPlan pl;
-    if (!plan_gemv<T>(a8, rows, cols, n_vec, pl)) return -2;
-    // Small matrices: shorter tiles so that more SMs take part (the tile shape
-    // does not enter the arithmetic of any output).
-    if (pl.n_chunks == 1)
-        while (pl.rpw > 1 && (rows + kConsumerWarps * pl.rpw - 1) / (kConsumerWarps * pl.rpw) < 2 * num_sms())
-            pl.rpw /= 2;
+    // Small matrices get shorter tiles so that more SMs take part (the tile
+    // shape does not enter the arithmetic of any output).
+    if (!plan_gemv<T>(a8, rows, cols, n_vec, pl, 4, (int64_t)num_sms())) return -2;
     GemvParams p{};
     p.W = static_cast<const uint8_t*>(W);
     p.rows = rows;
