@@ -40,7 +40,7 @@ sys.path.insert(0, ROOT)
 
 from gguf_block_quantised_gb300 import synth  # noqa: E402
 
-Q4_0, Q5_0, Q8_0, Q4_K, Q6_K, MXFP4, Q8_K, F32, BF16 = 1, 2, 3, 4, 5, 6, 7, 8, 9
+Q4_0, Q5_0, Q8_0, Q4_K, Q6_K, MXFP4, Q8_K, F32, BF16, MXFP4_R = 1, 2, 3, 4, 5, 6, 7, 8, 9, 10
 LAYERS = 24
 HID, FFN, KV, VOCAB = 896, 4864, 128, 151936
 # (name, rows, cols, input index) per layer; inputs: 0 attn-in, 1 o-in, 2 ffn-in, 3 down-in
@@ -377,11 +377,17 @@ def moe_leg(q, torch, stream, hbm):
     Wd = torch.from_numpy(synth.weights(MXFP4, E * 2880, 2880, seed=5, tensor_id=2)).cuda()
     bgu = torch.from_numpy(synth.bias(E, 5760, seed=5)).cuda()
     bd = torch.from_numpy(synth.bias(E, 2880, seed=5, tensor_id=2001)).cuda()
-    paths = {"w4a8": (q.FMT(MXFP4, Q8_0) | q.FLAG_QUANTIZE_X, torch.float32),
-             "bf16_gemm": (q.FMT(MXFP4, BF16), torch.bfloat16)}
+    # the same experts repacked once (qmv_repack, MXFP4 -> MXFP4_R rows)
+    Wgu_r = torch.empty(E * 5760 * q.qmv_row_bytes(MXFP4_R, 2880), dtype=torch.uint8, device="cuda")
+    Wd_r = torch.empty(E * 2880 * q.qmv_row_bytes(MXFP4_R, 2880), dtype=torch.uint8, device="cuda")
+    q.qmv_repack(MXFP4, Wgu, E * 5760, 2880, Wgu_r)
+    q.qmv_repack(MXFP4, Wd, E * 2880, 2880, Wd_r)
+    paths = {"w4a8": (q.FMT(MXFP4, Q8_0) | q.FLAG_QUANTIZE_X, torch.float32, Wgu, Wd),
+             "bf16_gemm": (q.FMT(MXFP4, BF16), torch.bfloat16, Wgu, Wd),
+             "bf16_gemm_repacked": (q.FMT(MXFP4_R, BF16), torch.bfloat16, Wgu_r, Wd_r)}
     out = {}
     ws = None
-    for name, (fmt, xdt) in paths.items():
+    for name, (fmt, xdt, Wgu_p, Wd_p) in paths.items():
         res = {}
         for n_tok in (1, 64, 1024):
             # four routings rotate, so the experts one launch reads were not just read
@@ -398,9 +404,9 @@ def moe_leg(q, torch, stream, hbm):
             for ids_np, gates_np in routes:
                 ids, gates = torch.from_numpy(ids_np).cuda(), torch.from_numpy(gates_np).cuda()
 
-                def layer(s, ids=ids, gates=gates, fmt=fmt, x=x, h=h, y1=y1, y2=y2, n_tok=n_tok):
-                    q.qmv_moe_matvec(fmt, Wgu, E, 5760, 2880, ids, None, k, x, y1, n_tok, bgu, s.cuda_stream)
-                    q.qmv_moe_matvec(fmt, Wd, E, 2880, 2880, ids, gates, k, h, y2, n_tok, bd, s.cuda_stream)
+                def layer(s, ids=ids, gates=gates, fmt=fmt, x=x, h=h, y1=y1, y2=y2, n_tok=n_tok, A=Wgu_p, B=Wd_p):
+                    q.qmv_moe_matvec(fmt, A, E, 5760, 2880, ids, None, k, x, y1, n_tok, bgu, s.cuda_stream)
+                    q.qmv_moe_matvec(fmt, B, E, 2880, 2880, ids, gates, k, h, y2, n_tok, bd, s.cuda_stream)
                 calls.append(layer)
             reps = 20 if n_tok >= 1024 else 100
             ms = time_rotating(torch, stream, calls, reps)
@@ -417,7 +423,9 @@ def moe_leg(q, torch, stream, hbm):
     return {"metric": "MoE layer (gate_up + down) expert weight GB/s", "unit": "GB/s", "by_path": out,
             "paths": {"w4a8": "k_moe_group + k_moe_gemv (dp4a, grouped per expert) + k_moe_combine",
                       "bf16_gemm": "k_moe_group + k_moe_tiles + k_moe_gather + k_moe_gemm_mxfp4_bf16 (tcgen05) "
-                                   "+ k_moe_combine"}}
+                                   "+ k_moe_combine",
+                      "bf16_gemm_repacked": "the same on MXFP4_R experts (qmv_repack once; TMA tensor copies of "
+                                            "the codes and exponents)"}}
 
 
 def run_probe(spec):
@@ -425,8 +433,9 @@ def run_probe(spec):
       gemv:T:rows:cols:atype:n_vec   qmv_matvec on synthetic weights (atype 8 = fp32)
       gemm:rows:cols:m               qmv_matmul, Q4_K x bf16
       step[:n_vec]                   one fused decode step of the Qwen2.5-0.5B shape (97 matvecs)
-      moe:n_tok[:atype]              one gpt-oss-shaped MoE layer (gate_up + down); atype 3 = Q8_0
-                                     quantised in-kernel (default), 9 = bf16 (grouped tensor-core GEMM)
+      moe:n_tok[:atype[:repacked]]   one gpt-oss-shaped MoE layer (gate_up + down); atype 3 = Q8_0
+                                     quantised in-kernel (default), 9 = bf16 (grouped tensor-core GEMM);
+                                     repacked 1: experts repacked to MXFP4_R first (bf16 only)
     Each runs its call five times and prints the event-timed mean of the last three."""
     import torch
     import gguf_block_quantised_gb300 as q
@@ -460,7 +469,7 @@ def run_probe(spec):
         call = lambda: step.run(stream)
         nbytes, what = STEP_WEIGHT_BYTES, "weight GB/s"
     elif kind == "moe":
-        n_tok, at = (a + [Q8_0])[:2]
+        n_tok, at, repacked = (a + [Q8_0, 0][len(a) - 1:])[:3]
         E, k = 32, 4
         Wgu = torch.from_numpy(synth.weights(MXFP4, E * 5760, 2880, seed=5, tensor_id=1)).cuda()
         Wd = torch.from_numpy(synth.weights(MXFP4, E * 2880, 2880, seed=5, tensor_id=2)).cuda()
@@ -474,6 +483,12 @@ def run_probe(spec):
         y1 = torch.empty(n_tok, k, 5760, device="cuda")
         y2 = torch.empty(n_tok, 2880, device="cuda")
         fmt = q.FMT(MXFP4, BF16) if at == BF16 else q.FMT(MXFP4, Q8_0) | q.FLAG_QUANTIZE_X
+        if repacked and at == BF16:
+            Wgu_r = torch.empty(E * 5760 * q.qmv_row_bytes(MXFP4_R, 2880), dtype=torch.uint8, device="cuda")
+            Wd_r = torch.empty(E * 2880 * q.qmv_row_bytes(MXFP4_R, 2880), dtype=torch.uint8, device="cuda")
+            q.qmv_repack(MXFP4, Wgu, E * 5760, 2880, Wgu_r)
+            q.qmv_repack(MXFP4, Wd, E * 2880, 2880, Wd_r)
+            Wgu, Wd, fmt = Wgu_r, Wd_r, q.FMT(MXFP4_R, BF16)
         ws = torch.empty(q.qmv_workspace_size(q.OP_MOE, fmt, 5760, 2880, n_tok * k), dtype=torch.uint8, device="cuda")
         q.qmv_set_workspace(ws, ws.numel())
 

@@ -16,9 +16,9 @@ import threading
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "_build", "libqmv.so")
 
-Q4_0, Q5_0, Q8_0, Q4_K, Q6_K, MXFP4, Q8_K, F32, BF16 = 1, 2, 3, 4, 5, 6, 7, 8, 9
+Q4_0, Q5_0, Q8_0, Q4_K, Q6_K, MXFP4, Q8_K, F32, BF16, MXFP4_R = 1, 2, 3, 4, 5, 6, 7, 8, 9, 10
 NAMES = {Q4_0: "Q4_0", Q5_0: "Q5_0", Q8_0: "Q8_0", Q4_K: "Q4_K", Q6_K: "Q6_K", MXFP4: "MXFP4",
-         Q8_K: "Q8_K", F32: "F32", BF16: "BF16"}
+         Q8_K: "Q8_K", F32: "F32", BF16: "BF16", MXFP4_R: "MXFP4_R"}
 OP_MATVEC, OP_MATMUL, OP_MOE = 1, 2, 3
 OK, ERR_INVALID_ARG, ERR_SHAPE, ERR_UNSUPPORTED, ERR_ALIGN, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_STATUS = \
     0, -1, -2, -3, -4, -5, -6, -7
@@ -51,6 +51,7 @@ _SIGS = {
     "qmv_block_bytes": (_SZ, [_I]),
     "qmv_row_bytes": (_SZ, [_I, _I64]),
     "qmv_quantize_act": (_I, [_I, _P, _P, _I64, _P]),
+    "qmv_repack": (_I, [_I, _P, _I64, _I64, _P, _P]),
     "qmv_dequantize": (_I, [_I, _P, _I64, _I64, _P, _P]),
     "qmv_block_dots": (_I, [_I, _P, _I64, _I64, _P, _I, _P, _P]),
     "qmv_matvec": (_I, [_I, _P, _I64, _I64, _P, _P, _I, _P]),
@@ -133,6 +134,10 @@ def qmv_row_bytes(t: int, cols: int) -> int:
 
 def qmv_quantize_act(fmt, x, xq, n, stream=None):
     return _call("qmv_quantize_act", fmt, _ptr(x), _ptr(xq), n, _stream(stream))
+
+
+def qmv_repack(t, W, rows, cols, Wout, stream=None):
+    return _call("qmv_repack", t, _ptr(W), rows, cols, _ptr(Wout), _stream(stream))
 
 
 def qmv_dequantize(t, W, rows, cols, out, stream=None):

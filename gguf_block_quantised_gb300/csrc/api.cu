@@ -34,6 +34,7 @@ QMV_GEMV_DECL(qmv_gemv_q4_k)
 QMV_GEMV_DECL(qmv_gemv_q6_k)
 int qmv_gemm_mma_q4_k(bool pdl, const void* W, int64_t rows, int64_t cols, const void* X, float* Y, int m, cudaStream_t st);
 size_t qmv_moe_workspace_bytes(bool bf16, int64_t rows, int64_t cols, int64_t n_pairs);
+int qmv_launch_repack_mxfp4(const void* W, int64_t rows, int64_t cols, void* Wout, cudaStream_t st);
 int qmv_launch_moe(int wtype, bool a8, bool quant_x, bool bf16, size_t act_block_bytes, const void* W3d,
                    int n_expert, int64_t rows, int64_t cols, const int32_t* ids, const float* gates, int k,
                    const void* x, float* y, int64_t n_tok, const float* bias, void* ws, cudaStream_t st);
@@ -100,6 +101,7 @@ const char* type_name(int t)
     case QMV_Q8_K: return "Q8_K";
     case QMV_F32: return "F32";
     case QMV_BF16: return "BF16";
+    case QMV_MXFP4_R: return "MXFP4_R";
     default: return "unknown";
     }
 }
@@ -169,12 +171,16 @@ int moe_check(const char* name, int fmt, const void* W3d, int n_expert, int64_t 
     c.quant_x = (fmt & QMV_FLAG_QUANTIZE_X) != 0;
     c.wtype = fmt & 0xff;
     const int atype = (fmt >> 8) & 0xff;
-    c.bf16 = atype == QMV_BF16 && c.wtype == QMV_MXFP4;
+    c.bf16 = atype == QMV_BF16 && (c.wtype == QMV_MXFP4 || c.wtype == QMV_MXFP4_R);
+    if (c.wtype == QMV_MXFP4_R && !c.bf16)
+        return fail(QMV_ERR_UNSUPPORTED, "%s: repacked MXFP4_R experts take BF16 activations (got %s)", name,
+                    type_name(atype));
     if (is_weight_type(c.wtype) && atype != QMV_F32 && atype != paired_act(c.wtype) && !c.bf16)
         return fail(QMV_ERR_UNSUPPORTED, "%s: %s experts take F32 or %s activations%s (got %s)", name,
                     type_name(c.wtype), type_name(paired_act(c.wtype)), c.wtype == QMV_MXFP4 ? " or BF16" : "",
                     type_name(atype));
-    int rc = check_weights(c.wtype, W3d, rows, cols);
+    // MXFP4_R has the MXFP4 block geometry (padded rows)
+    int rc = check_weights(c.wtype == QMV_MXFP4_R ? QMV_MXFP4 : c.wtype, W3d, rows, cols);
     if (rc) return rc;
     if (c.quant_x && (atype == QMV_F32 || c.bf16))
         return fail(QMV_ERR_INVALID_ARG, "QMV_FLAG_QUANTIZE_X needs an 8-bit activation type (Q8_0 or Q8_K)");
@@ -235,7 +241,7 @@ const char* qmv_last_error(void) { return t_err.c_str(); }
 int qmv_block_elems(int type)
 {
     switch (type) {
-    case QMV_Q4_0: case QMV_Q5_0: case QMV_Q8_0: case QMV_MXFP4: return 32;
+    case QMV_Q4_0: case QMV_Q5_0: case QMV_Q8_0: case QMV_MXFP4: case QMV_MXFP4_R: return 32;
     case QMV_Q4_K: case QMV_Q6_K: case QMV_Q8_K: return 256;
     case QMV_F32: case QMV_BF16: return 1;
     default: return 0;
@@ -248,7 +254,7 @@ size_t qmv_block_bytes(int type)
     case QMV_Q4_0: return 18;
     case QMV_Q5_0: return 22;
     case QMV_Q8_0: return 34;
-    case QMV_MXFP4: return 17;
+    case QMV_MXFP4: case QMV_MXFP4_R: return 17;
     case QMV_Q4_K: return 144;
     case QMV_Q6_K: return 210;
     case QMV_Q8_K: return 292;
@@ -262,6 +268,7 @@ size_t qmv_row_bytes(int type, int64_t cols)
 {
     const int bs = qmv_block_elems(type);
     if (bs == 0 || cols < 0 || cols % bs) return 0;
+    if (type == QMV_MXFP4_R) return ((size_t)(cols / 32) * 17 + 15) & ~size_t(15);   // padded rows
     return (size_t)(cols / bs) * qmv_block_bytes(type);
 }
 
@@ -282,6 +289,23 @@ int qmv_quantize_act(int fmt, const float* x, void* xq, int64_t n, void* stream)
     if (!aligned(x, fmt == QMV_Q8_K ? 16 : 4)) return fail(QMV_ERR_ALIGN, "x must be %d-byte aligned", fmt == QMV_Q8_K ? 16 : 4);
     if (!aligned(xq, fmt == QMV_Q8_K ? 4 : 2)) return fail(QMV_ERR_ALIGN, "xq must be %d-byte aligned", fmt == QMV_Q8_K ? 4 : 2);
     if (qmv_launch_quantize(fmt, x, xq, n, pdl, static_cast<cudaStream_t>(stream))) return cuda_fail("qmv_quantize_act");
+    return ok();
+}
+
+int qmv_repack(int type, const void* W, int64_t rows, int64_t cols, void* Wout, void* stream)
+{
+    if (type != QMV_MXFP4)
+        return fail(QMV_ERR_UNSUPPORTED, "qmv_repack: %s weights have no repacked layout; supported: MXFP4 (-> MXFP4_R)",
+                    type_name(type));
+    int rc = check_weights(type, W, rows, cols);
+    if (rc) return rc;
+    if (rows == 0) return ok();
+    if (!Wout) return fail(QMV_ERR_INVALID_ARG, "Wout must not be NULL");
+    if (!aligned(Wout, 16)) return fail(QMV_ERR_ALIGN, "Wout must start on a 16-byte boundary");
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(W), a1 = a0 + (uintptr_t)rows * qmv_row_bytes(type, cols);
+    const uintptr_t b0 = reinterpret_cast<uintptr_t>(Wout), b1 = b0 + (uintptr_t)rows * qmv_row_bytes(QMV_MXFP4_R, cols);
+    if (a0 < b1 && b0 < a1) return fail(QMV_ERR_INVALID_ARG, "qmv_repack: Wout overlaps W");
+    if (qmv_launch_repack_mxfp4(W, rows, cols, Wout, static_cast<cudaStream_t>(stream))) return cuda_fail("qmv_repack");
     return ok();
 }
 

@@ -100,9 +100,9 @@ QMV_MOE_DECL(qmv_moe_q4_k)
 QMV_MOE_DECL(qmv_moe_q6_k)
 
 size_t qmv_moe_gemm_extra_bytes(int64_t cols, int64_t n_pairs);
-int qmv_launch_moe_gemm_mxfp4(const void* W3d, int n_expert, int64_t rows, int64_t cols, const void* x, int kdiv,
-                              int64_t n_pairs, const int* offsets, const int* active, const int* perm, void* ws,
-                              float* out, const float* bias, cudaStream_t st);
+int qmv_launch_moe_gemm_mxfp4(const void* W3d, bool planar, int n_expert, int64_t rows, int64_t cols, const void* x,
+                              int kdiv, int64_t n_pairs, const int* offsets, const int* active, const int* perm,
+                              void* ws, float* out, const float* bias, cudaStream_t st);
 
 // Workspace layout: offsets[1025] + active[1025] | perm[n_pairs] | per-slot
 // outputs [n_pairs][rows] fp32 | (bf16 activations only) the grouped GEMM's
@@ -140,9 +140,10 @@ int qmv_launch_moe(int wtype, bool a8, bool quant_x, bool bf16, size_t act_block
     int rc = -3;
     if (bf16) {
         void* gws = w + r256(2050 * 4) + r256((size_t)n_pairs * 4) + r256((size_t)n_pairs * (size_t)rows * 4);
-        rc = wtype == QMV_MXFP4 ? qmv_launch_moe_gemm_mxfp4(W3d, n_expert, rows, cols, x, kdiv, n_pairs, offsets,
-                                                            active, perm, gws, out, b, st)
-                                : -3;
+        rc = wtype == QMV_MXFP4 || wtype == QMV_MXFP4_R
+                 ? qmv_launch_moe_gemm_mxfp4(W3d, wtype == QMV_MXFP4_R, n_expert, rows, cols, x, kdiv, n_pairs,
+                                             offsets, active, perm, gws, out, b, st)
+                 : -3;
     }
 #define QMV_MOE_CALL(NAME) \
     NAME(a8, quant_x, W3d, n_expert, rows, cols, offsets, active, perm, (int)n_pairs, x, xrow, kdiv, out, b, st)

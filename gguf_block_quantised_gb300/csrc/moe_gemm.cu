@@ -52,21 +52,34 @@ bool make_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint
 namespace mg {
 constexpr int BM = 128, BN = 128, BK = 64;   // BK: k of one 128-byte swizzled X row = one TMA box
 constexpr int KSUB = 2;                  // 64-k sub-chunks per k stage (8 MMAs per barrier round)
-constexpr int SK = 3, SR = 4;            // k stages (X tiles + A tile), raw stages
+constexpr int SK = 4;                    // k stages (X tiles + A tile)
 constexpr int X_BYTES = BN * BK * 2;     // 16384 per sub-chunk
-constexpr int SC_BLOCKS = 8;             // MXFP4 blocks per row per raw stage (256 k)
-constexpr int PIECES = 10;               // 16-byte pieces per row per raw stage: 136 bytes + up to 15 of alignment
-constexpr int SLOT = 176;                // bytes per row per raw stage (>= 16 * PIECES; 11 x 16 bytes, odd)
-constexpr int R_BYTES = BM * SLOT;       // 22528
 constexpr int OFF_X = 0;
 constexpr int OFF_R = OFF_X + SK * KSUB * X_BYTES;
-constexpr int OFF_BAR = OFF_R + SR * R_BYTES;
-constexpr int N_BARS = 2 * SK + 2 * SR + 4;
-constexpr int SMEM = OFF_BAR + N_BARS * 8 + 16 + 1024;   // + alignment slack
 constexpr int DEQ_WARPS = 8;             // warps 4..11
 constexpr int EPI_WARP0 = 12;            // warps 12..15
-constexpr int RAW_THREADS = 192;         // warps 2, 3 and 16..19
-constexpr int THREADS = 640;
+
+// Raw weight staging per layout.
+// GGUF MXFP4 rows: per raw stage, each row's next 8 blocks (256 k) as the
+// 16-byte-aligned span holding them, cp.async pieces from warps 2, 3 and 16..19.
+constexpr int PIECES = 10;               // 16-byte pieces per row per raw stage: 136 bytes + up to 15 of alignment
+constexpr int SLOT = 176;                // bytes per row per raw stage (>= 16 * PIECES; 11 x 16 bytes, odd)
+// Repacked MXFP4_R rows: per raw stage, 16 blocks (512 k) of 128 rows as TMA
+// tensor copies: two 128-byte-swizzled code boxes [128 rows][128 B] and one
+// exponent box [128 rows][16 B].
+constexpr int RC_BYTES = BM * 128;       // one code box
+template <bool PLANAR>
+struct RawCfg {
+    static constexpr int BLOCKS = PLANAR ? 16 : 8;                        // blocks per row per raw stage
+    static constexpr int SR = PLANAR ? 2 : 4;                             // raw stages
+    static constexpr int R_BYTES = PLANAR ? 2 * RC_BYTES + BM * 16 : BM * SLOT;   // 34816 / 22528
+    static constexpr int ARRIVALS = PLANAR ? 1 : 192;                     // arrivals that fill a raw stage
+    static constexpr int THREADS = PLANAR ? 512 : 640;
+    static constexpr int OFF_BAR = OFF_R + SR * R_BYTES;
+    static constexpr int N_BARS = 2 * SK + 2 * SR + 4;
+    static constexpr int SMEM = OFF_BAR + N_BARS * 8 + 16 + 1024;   // + alignment slack
+    static_assert(SMEM <= 227 * 1024, "shared memory");
+};
 // TMEM columns: two 128-column fp32 accumulators, then SK bf16 A tiles of
 // 64 columns each (128 rows x 128 k, two elements per column).
 constexpr uint32_t A_COL = 2 * BN;
@@ -172,12 +185,19 @@ __device__ __forceinline__ void mxfp4_block_bf16_slow(uint32_t e, const uint32_t
 // One 32-element MXFP4 block (17 bytes at byte offset o of a shared-memory
 // row slot, any alignment) -> 16 bf16x2 words in element order (word i =
 // elements 2i, 2i+1).
+__device__ __forceinline__ void mxfp4_codes_bf16(uint32_t e, const uint32_t (&w)[4], uint32_t (&out)[16]);
+
 __device__ __forceinline__ void mxfp4_block_bf16(const uint8_t* slot, int o, uint32_t (&out)[16])
 {
     const uint8_t* p = slot + o;
-    const uint32_t e = p[0];
     uint32_t w[4];
     load_words<4>(p + 1, w);   // the 16 code bytes
+    mxfp4_codes_bf16(p[0], w, out);
+}
+
+// One block given as its exponent and its four code words.
+__device__ __forceinline__ void mxfp4_codes_bf16(uint32_t e, const uint32_t (&w)[4], uint32_t (&out)[16])
+{
     E2m1Tab t;
     if (e2m1_table(e, t)) {
 #pragma unroll
@@ -251,10 +271,16 @@ struct MoeGemmArgs {
     unsigned* status;
 };
 
-__global__ void __launch_bounds__(mg::THREADS, 1)
-    k_moe_gemm_mxfp4_bf16(const __grid_constant__ CUtensorMap tmX, const MoeGemmArgs a)
+// PLANAR: the experts are MXFP4_R rows (tmC, tmE: code and exponent tensor
+// maps over all experts' rows); otherwise GGUF MXFP4 rows (tmC, tmE unused).
+template <bool PLANAR>
+__global__ void __launch_bounds__(mg::RawCfg<PLANAR>::THREADS, 1)
+    k_moe_gemm_mxfp4_bf16(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmC,
+                          const __grid_constant__ CUtensorMap tmE, const MoeGemmArgs a)
 {
     using namespace mg;
+    using RC = RawCfg<PLANAR>;
+    constexpr int SR = RC::SR, R_BYTES = RC::R_BYTES, OFF_BAR = RC::OFF_BAR, SC_BLOCKS = RC::BLOCKS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
@@ -280,11 +306,15 @@ __global__ void __launch_bounds__(mg::THREADS, 1)
 
     if (tid == 0) {
         for (int i = 0; i < SK; ++i) { mbar_init(&full[i], DEQ_WARPS + 1); mbar_init(&empty[i], 1); }
-        for (int i = 0; i < SR; ++i) { mbar_init(&rf[i], RAW_THREADS); mbar_init(&re[i], DEQ_WARPS); }
+        for (int i = 0; i < SR; ++i) { mbar_init(&rf[i], RC::ARRIVALS); mbar_init(&re[i], DEQ_WARPS); }
         for (int i = 0; i < 2; ++i) { mbar_init(&accf[i], 1); mbar_init(&acce[i], 4); }
         *abort_flag = 0;
         fence_barrier_init();
         prefetch_tmap(&tmX);
+        if (PLANAR) {
+            prefetch_tmap(&tmC);
+            prefetch_tmap(&tmE);
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, TMEM_COLS);
@@ -322,7 +352,27 @@ __global__ void __launch_bounds__(mg::THREADS, 1)
                 }
             }
         }
-    } else if (warp == 2 || warp == 3 || warp >= EPI_WARP0 + 4) {
+    } else if (PLANAR && warp == 2) {
+        // ---- raw weights, repacked rows: three TMA tensor copies per stage
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 1;
+            for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x) {
+                int e, nt, rt;
+                tile_of(t, e, nt, rt);
+                const int y = (int)((int64_t)e * a.rows + (int64_t)rt * BM);   // first row of the tile
+                for (int sc = 0; sc < nsc; ++sc) {
+                    if (!mbar_wait_backoff(&re[s], ph, a.status, 128)) { fail(); break; }
+                    uint8_t* buf = smem + OFF_R + s * R_BYTES;
+                    mbar_arrive_expect_tx(&rf[s], R_BYTES);
+                    tma_load_2d(buf, &tmC, sc * 256, y, &rf[s]);
+                    tma_load_2d(buf + RC_BYTES, &tmC, sc * 256 + 128, y, &rf[s]);
+                    tma_load_2d(buf + 2 * RC_BYTES, &tmE, sc * 16, y, &rf[s]);
+                    if (++s == SR) { s = 0; ph ^= 1; }
+                }
+            }
+        }
+    } else if (!PLANAR && (warp == 2 || warp == 3 || warp >= EPI_WARP0 + 4)) {
         // ---- raw weights: for each row of the tile, the 16-byte-aligned span
         // holding its next (up to) 8 blocks, as 16-byte cp.async pieces spread
         // over the 192 threads of warps 2, 3 and 16..19 (consecutive threads take
@@ -342,7 +392,7 @@ __global__ void __launch_bounds__(mg::THREADS, 1)
                 if (!__all_sync(0xffffffffu, mbar_wait_backoff(&re[s], ph, a.status, 128))) { bad = true; break; }
                 uint8_t* buf = smem + OFF_R + s * R_BYTES;
                 const int nb = min(SC_BLOCKS, a.nblk - sc * SC_BLOCKS);
-                for (int p = pt; p < nrows * PIECES; p += RAW_THREADS) {
+                for (int p = pt; p < nrows * PIECES; p += RC::ARRIVALS) {
                     const int i = p / PIECES, j = p - i * PIECES;
                     const int64_t b0 = tile0 + (int64_t)i * a.rb + (int64_t)sc * SC_BLOCKS * 17;
                     const int64_t src = (b0 & ~int64_t(15)) + 16 * j;
@@ -405,7 +455,8 @@ __global__ void __launch_bounds__(mg::THREADS, 1)
             bool bad = false;
             for (int sc = 0; sc < nsc && !bad; ++sc) {
                 if (!__all_sync(0xffffffffu, mbar_wait_bounded(&rf[sr], prf, a.status))) { bad = true; break; }
-                const uint8_t* slot = smem + OFF_R + sr * R_BYTES + r * SLOT;
+                const uint8_t* rbuf = smem + OFF_R + sr * R_BYTES;
+                const uint8_t* slot = rbuf + r * SLOT;
                 const int off = (int)((row_start + (int64_t)sc * SC_BLOCKS * 17) & 15);
                 const int nb = min(SC_BLOCKS, a.nblk - sc * SC_BLOCKS);
                 const int nc = (nb + 1) / 2;
@@ -419,7 +470,15 @@ __global__ void __launch_bounds__(mg::THREADS, 1)
                         const int blk = 2 * (KSUB * cs + j) + half;
                         uint32_t o[16];
                         if (row < a.rows && blk < nb) {
-                            mxfp4_block_bf16(slot, off + 17 * blk, o);
+                            if constexpr (PLANAR) {
+                                // code box blk / 8, 16-byte chunk (blk % 8) swizzled by the row
+                                const uint4 u = *reinterpret_cast<const uint4*>(
+                                    rbuf + (blk >> 3) * RC_BYTES + r * 128 + (((blk & 7) ^ (r & 7)) << 4));
+                                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+                                mxfp4_codes_bf16(rbuf[2 * RC_BYTES + r * 16 + blk], w, o);
+                            } else {
+                                mxfp4_block_bf16(slot, off + 17 * blk, o);
+                            }
                         } else {
 #pragma unroll
                             for (int i = 0; i < 16; ++i) o[i] = 0u;
@@ -497,10 +556,11 @@ size_t qmv_moe_gemm_extra_bytes(int64_t cols, int64_t n_pairs)
 
 // Enqueues the slot list, the gather and the grouped GEMM.  ws points at the
 // GEMM's part of the workspace (qmv_moe_gemm_extra_bytes bytes, 256-aligned).
-// Returns 0, -6 (launch failure) or -8 (tensor map).
-int qmv_launch_moe_gemm_mxfp4(const void* W3d, int n_expert, int64_t rows, int64_t cols, const void* x, int kdiv,
-                              int64_t n_pairs, const int* offsets, const int* active, const int* perm, void* ws,
-                              float* out, const float* bias, cudaStream_t st)
+// planar: W3d holds MXFP4_R rows.  Returns 0, -6 (launch failure) or -8 (tensor
+// map).
+int qmv_launch_moe_gemm_mxfp4(const void* W3d, bool planar, int n_expert, int64_t rows, int64_t cols, const void* x,
+                              int kdiv, int64_t n_pairs, const int* offsets, const int* active, const int* perm,
+                              void* ws, float* out, const float* bias, cudaStream_t st)
 {
     using namespace qmv;
     int* tiles = static_cast<int*>(ws);
@@ -510,7 +570,7 @@ int qmv_launch_moe_gemm_mxfp4(const void* W3d, int n_expert, int64_t rows, int64
     k_moe_gather<<<(unsigned)((per + 255) / 256), 256, 0, st>>>(static_cast<const uint16_t*>(x), perm, offsets,
                                                                   n_expert, kdiv, (int)cols, Xs);
     if (cudaGetLastError() != cudaSuccess) return -6;
-    CUtensorMap tmX;
+    CUtensorMap tmX, tmC, tmE;
     if (!make_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Xs, (uint64_t)cols, (uint64_t)n_pairs,
                       (uint64_t)cols * 2, mg::BK, mg::BN, CU_TENSOR_MAP_SWIZZLE_128B))
         return -8;
@@ -518,7 +578,7 @@ int qmv_launch_moe_gemm_mxfp4(const void* W3d, int n_expert, int64_t rows, int64
     a.W3d = static_cast<const uint8_t*>(W3d);
     a.rows = rows;
     a.nblk = (int)(cols / 32);
-    a.rb = (int64_t)a.nblk * 17;
+    a.rb = planar ? (((int64_t)a.nblk * 17 + 15) & ~int64_t(15)) : (int64_t)a.nblk * 17;
     a.total = (int64_t)n_expert * rows * a.rb;
     a.offsets = offsets;
     a.perm = perm;
@@ -526,7 +586,61 @@ int qmv_launch_moe_gemm_mxfp4(const void* W3d, int n_expert, int64_t rows, int64
     a.bias = bias;
     a.out = out;
     a.status = status_word();
-    auto* k = &k_moe_gemm_mxfp4_bf16;
-    prepare_kernel(k, mg::THREADS, mg::SMEM);
-    return launch_ex(k, dim3(num_sms()), dim3(mg::THREADS), mg::SMEM, st, false, tmX, a) == cudaSuccess ? 0 : -6;
+    if (planar) {
+        // codes: [all rows][16 * nblk bytes], exponents: [all rows][nblk bytes] at +16*nblk; row pitch rb
+        const uint64_t all_rows = (uint64_t)n_expert * (uint64_t)rows;
+        if (!make_tmap_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT8, W3d, (uint64_t)a.nblk * 16, all_rows, (uint64_t)a.rb,
+                          128, mg::BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !make_tmap_2d(&tmE, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<const uint8_t*>(W3d) + (size_t)a.nblk * 16,
+                          (uint64_t)a.nblk, all_rows, (uint64_t)a.rb, 16, mg::BM, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return -8;
+        auto* k = &k_moe_gemm_mxfp4_bf16<true>;
+        prepare_kernel(k, mg::RawCfg<true>::THREADS, mg::RawCfg<true>::SMEM);
+        return launch_ex(k, dim3(num_sms()), dim3(mg::RawCfg<true>::THREADS), mg::RawCfg<true>::SMEM, st, false, tmX,
+                         tmC, tmE, a) == cudaSuccess
+                   ? 0
+                   : -6;
+    }
+    tmC = tmX;   // unused by the GGUF-layout kernel
+    tmE = tmX;
+    auto* k = &k_moe_gemm_mxfp4_bf16<false>;
+    prepare_kernel(k, mg::RawCfg<false>::THREADS, mg::RawCfg<false>::SMEM);
+    return launch_ex(k, dim3(num_sms()), dim3(mg::RawCfg<false>::THREADS), mg::RawCfg<false>::SMEM, st, false, tmX,
+                     tmC, tmE, a) == cudaSuccess
+               ? 0
+               : -6;
+}
+
+// ---- repack: GGUF MXFP4 rows -> MXFP4_R rows --------------------------------------
+// One thread per block: its 16 code bytes to 16-byte-aligned position 16*b of
+// the row, its exponent to 16*nblk + b; the first thread of a row zeroes the
+// row's padding.
+__global__ void k_repack_mxfp4(const uint8_t* __restrict__ W, int64_t rows, int nblk, int64_t rb_out,
+                               uint8_t* __restrict__ out)
+{
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= rows * nblk) return;
+    const int64_t r = i / nblk;
+    const int b = (int)(i - r * nblk);
+    const uint8_t* src = W + i * 17;
+    uint8_t* row = out + r * rb_out;
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        w[k] = (uint32_t)src[1 + 4 * k] | ((uint32_t)src[2 + 4 * k] << 8) | ((uint32_t)src[3 + 4 * k] << 16) |
+               ((uint32_t)src[4 + 4 * k] << 24);
+    *reinterpret_cast<uint4*>(row + 16 * b) = make_uint4(w[0], w[1], w[2], w[3]);
+    row[16 * nblk + b] = src[0];
+    if (b == 0)
+        for (int64_t k = (int64_t)17 * nblk; k < rb_out; ++k) row[k] = 0;
+}
+
+int qmv_launch_repack_mxfp4(const void* W, int64_t rows, int64_t cols, void* Wout, cudaStream_t st)
+{
+    const int nblk = (int)(cols / 32);
+    const int64_t rb_out = ((int64_t)nblk * 17 + 15) & ~int64_t(15);
+    const int64_t n = rows * nblk;
+    k_repack_mxfp4<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(static_cast<const uint8_t*>(W), rows, nblk, rb_out,
+                                                                static_cast<uint8_t*>(Wout));
+    return cudaGetLastError() == cudaSuccess ? 0 : -6;
 }

@@ -64,7 +64,11 @@ typedef enum {
     QMV_MXFP4 = 6,  /* 32 w, 17 B: E8M0 e | 16 B E2M1 codes;             w = 2^(e-127)*E2M1(q)  */
     QMV_Q8_K = 7,   /* activations only, 256 w, 292 B: fp32 d | int8[256] | int16 bsums[16]      */
     QMV_F32 = 8,    /* plain fp32 */
-    QMV_BF16 = 9    /* plain bfloat16 */
+    QMV_BF16 = 9,   /* plain bfloat16 */
+    QMV_MXFP4_R = 10 /* MXFP4 rows repacked by qmv_repack: the 16 code bytes of each 32-element
+                        block in block order, then the row's E8M0 bytes, zero-padded to a
+                        multiple of 16 bytes (row bytes = 16*ceil(17*cols/32/16)).  Weights of
+                        qmv_moe_matvec with BF16 activations only. */
 } qmv_type;
 
 /* A multiply's format is the weight type plus the activation type. */
@@ -102,8 +106,8 @@ const char* qmv_strerror(int err);
 const char* qmv_last_error(void);
 
 /* Block geometry: elements per block (32 or 256; 1 for F32/BF16; 0 if unknown),
- * bytes per block, bytes of one row of `cols` elements (0 if cols is not a
- * multiple of the block length). */
+ * bytes per block (17 for QMV_MXFP4_R, whose rows are padded), bytes of one row
+ * of `cols` elements (0 if cols is not a multiple of the block length). */
 int    qmv_block_elems(int type);
 size_t qmv_block_bytes(int type);
 size_t qmv_row_bytes(int type, int64_t cols);
@@ -123,6 +127,24 @@ size_t qmv_row_bytes(int type, int64_t cols);
  * operation.  Q8_0 stores d rounded to fp16, Q8_K the fp32 d.
  * ------------------------------------------------------------------------- */
 int qmv_quantize_act(int fmt, const float* x, void* xq, int64_t n, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * qmv_repack -- weights to a layout for the tensor-core kernels, once at load
+ * time (the "Architecture" page's bench transcript runs its engine with
+ * "repack on").  The GGUF layout stays the canonical input; the repacked copy
+ * holds the same bits.
+ *   type : QMV_MXFP4 -> Wout in QMV_MXFP4_R rows: every 17-byte block's 16
+ *          code bytes land 16-byte aligned and the row pitch becomes a
+ *          multiple of 16, so TMA tensor copies can move the codes and the
+ *          exponents of many rows at once.
+ *   W    : rows x cols GGUF blocks (16-byte aligned; for stacked experts rows
+ *          counts all of them, n_expert*rows).  Wout: rows x
+ *          qmv_row_bytes(QMV_MXFP4_R, cols) bytes, 16-byte aligned, not
+ *          overlapping W.  Asynchronous on `stream`; allocates nothing.
+ * Returns QMV_OK, or QMV_ERR_UNSUPPORTED for other types, QMV_ERR_SHAPE,
+ * QMV_ERR_ALIGN, QMV_ERR_INVALID_ARG, QMV_ERR_CUDA.
+ * ------------------------------------------------------------------------- */
+int qmv_repack(int type, const void* W, int64_t rows, int64_t cols, void* Wout, void* stream);
 
 /* ---------------------------------------------------------------------------
  * qmv_dequantize -- weights to fp32 ("The package map", pkg/quant:
@@ -208,7 +230,9 @@ int qmv_matmul(int fmt, const void* W, int64_t rows, int64_t cols,
  *           | QMV_FLAG_QUANTIZE_X (fp32 rows quantised inside the kernel);
  *           or, for MXFP4 experts only, BF16 (bf16 rows, 16-byte aligned):
  *           the grouped tensor-core GEMM, whose weights 2^(e-127)*E2M1 are
- *           exact in bf16 (fp32 accumulation; rows < 2^30).
+ *           exact in bf16 (fp32 accumulation; rows < 2^30).  The experts may
+ *           also be given as QMV_MXFP4_R (qmv_repack output, same results),
+ *           which the GEMM moves with TMA tensor copies.
  *   n_expert in 1..1024, k in 1..64, n_tok*k <= 2^24.
  *   Results per (token, slot) are, for F32 and 8-bit activations, those of
  *   qmv_matvec on that expert's matrix (same arithmetic and reduction

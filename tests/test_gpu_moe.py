@@ -164,15 +164,71 @@ def bf16_rows(n, cols, seed):
     return xb, xb.view(torch.int16).numpy()
 
 
+MXFP4_R = 10
+
+
+def repack_reference(W, rows, cols):
+    """MXFP4 GGUF rows -> MXFP4_R rows, by a plain reshuffle: per row the 16
+    code bytes of each block in block order, then the exponent bytes, then
+    zeros up to a multiple of 16 bytes."""
+    nblk = cols // 32
+    blocks = W.reshape(rows, nblk, 17)
+    rb = (17 * nblk + 15) // 16 * 16
+    out = np.zeros((rows, rb), dtype=np.uint8)
+    out[:, :16 * nblk] = blocks[:, :, 1:].reshape(rows, 16 * nblk)
+    out[:, 16 * nblk:17 * nblk] = blocks[:, :, 0]
+    return out.reshape(-1)
+
+
+def experts_on_device(qmv, W3, n_rows, cols, repacked):
+    """(device weights, weight type): the GGUF rows, or their qmv_repack output."""
+    Wd = dev(W3)
+    if not repacked:
+        return Wd, MXFP4
+    Wr = torch.empty(n_rows * qmv.qmv_row_bytes(MXFP4_R, cols), dtype=torch.uint8, device="cuda")
+    qmv.qmv_repack(MXFP4, Wd, n_rows, cols, Wr)
+    return Wr, MXFP4_R
+
+
+@pytest.mark.parametrize("rows,cols", [(37, 544), (5, 32), (64, 2880)])
+def test_repack_bytes(qmv, rows, cols):
+    """qmv_repack writes exactly the reshuffled bytes (padding zeroed)."""
+    W = synth.weights(MXFP4, rows, cols, seed=81, tensor_id=cols)
+    assert qmv.qmv_row_bytes(MXFP4_R, cols) == (17 * (cols // 32) + 15) // 16 * 16
+    Wr = torch.full((rows * qmv.qmv_row_bytes(MXFP4_R, cols),), 0xAB, dtype=torch.uint8, device="cuda")
+    qmv.qmv_repack(MXFP4, dev(W), rows, cols, Wr)
+    assert np.array_equal(host(Wr), repack_reference(W, rows, cols))
+
+
+def test_repack_refusals(qmv):
+    W = torch.zeros(4 * 144, dtype=torch.uint8, device="cuda")
+    out = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    with pytest.raises(qmv.QmvError) as e:   # no repacked layout for Q4_K
+        qmv.qmv_repack(Q4_K, W, 4, 256, out)
+    assert e.value.code == qmv.ERR_UNSUPPORTED
+    with pytest.raises(qmv.QmvError) as e:   # output overlapping the input
+        qmv.qmv_repack(MXFP4, out, 4, 64, out[16:])
+    assert e.value.code == qmv.ERR_INVALID_ARG
+    y = torch.zeros((1, 32), dtype=torch.float32, device="cuda")
+    with pytest.raises(qmv.QmvError) as e:   # MXFP4_R is a MoE bf16 operand only
+        qmv.qmv_matvec(qmv.FMT(MXFP4_R, Q8_0), out, 32, 64, y, y, 1)
+    assert e.value.code == qmv.ERR_UNSUPPORTED
+    ids = torch.zeros((1, 1), dtype=torch.int32, device="cuda")
+    with pytest.raises(qmv.QmvError) as e:
+        qmv.qmv_moe_matvec(qmv.FMT(MXFP4_R, Q8_0), out, 1, 32, 64, ids, None, 1, y, y, 1, None)
+    assert e.value.code == qmv.ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("repacked", [False, True])
 @pytest.mark.parametrize("rows,cols,n_tok", [(296, 544, 1), (128, 256, 37), (200, 2880, 9), (136, 320, 300)])
-def test_moe_bf16_gemm_parity(qmv, orc, workspace, rows, cols, n_tok):
+def test_moe_bf16_gemm_parity(qmv, orc, workspace, rows, cols, n_tok, repacked):
     """Ragged row tiles, an odd number of blocks per row (a half 64-k chunk and
     a short last raw stage), experts with more than one 128-token tile, both
-    forms, with biases."""
+    forms, with biases; GGUF rows and repacked MXFP4_R rows."""
     E, k, t = 8, 4, MXFP4
     W3, ids, gates, b = moe_inputs(t, E, rows, cols, n_tok, k, 40 + cols)
-    W3d = dev(W3)
-    fmt = qmv.FMT(t, BF16)
+    W3d, wt = experts_on_device(qmv, W3, E * rows, cols, repacked)
+    fmt = qmv.FMT(wt, BF16)
     xb, xbits = bf16_rows(n_tok, cols, 41)
     y = run_moe(qmv, fmt, W3d, E, rows, cols, ids, None, k, xb.cuda(), n_tok, b)
     yref, yabs = orc.moe(t, BF16, W3, E, rows, cols, ids, None, k, xbits, n_tok, bias=b)
@@ -184,7 +240,8 @@ def test_moe_bf16_gemm_parity(qmv, orc, workspace, rows, cols, n_tok):
     qmv.qmv_get_status()
 
 
-def test_moe_bf16_exponent_range(qmv, orc, workspace):
+@pytest.mark.parametrize("repacked", [False, True])
+def test_moe_bf16_exponent_range(qmv, orc, workspace, repacked):
     """E8M0 exponents across 0..200: the table path (2..252) at both ends of its
     range and the exact fallback for the zero and subnormal scales (0, 1)."""
     E, rows, cols, k, n_tok, t = 4, 160, 512, 2, 20, MXFP4
@@ -196,14 +253,16 @@ def test_moe_bf16_exponent_range(qmv, orc, workspace):
     blocks[3::11, 0] = g.integers(0, 2, size=blocks[3::11].shape[0], dtype=np.uint8)
     W3 = blocks.reshape(-1)
     xb, xbits = bf16_rows(n_tok, cols, 51)
-    y = run_moe(qmv, qmv.FMT(t, BF16), dev(W3), E, rows, cols, ids, None, k, xb.cuda(), n_tok, None)
+    W3d, wt = experts_on_device(qmv, W3, E * rows, cols, repacked)
+    y = run_moe(qmv, qmv.FMT(wt, BF16), W3d, E, rows, cols, ids, None, k, xb.cuda(), n_tok, None)
     yref, yabs = orc.moe(t, BF16, W3, E, rows, cols, ids, None, k, xbits, n_tok)
     assert_close(y, yref, yabs, what="exponents")
     qmv.qmv_get_status()
 
 
+@pytest.mark.parametrize("repacked", [False, True])
 @pytest.mark.parametrize("n_tok", [1, 64, 1024])
-def test_moe_bf16_gpt_oss_shapes_sampled(qmv, orc, workspace, n_tok):
+def test_moe_bf16_gpt_oss_shapes_sampled(qmv, orc, workspace, n_tok, repacked):
     """gpt-oss-20B-shaped experts with bf16 activations through the grouped
     GEMM: gate_up 5760x2880 (up form) and down 2880x2880 (gate-weighted),
     biases, top-4 of 32; sampled tokens and rows against the oracle."""
@@ -214,7 +273,8 @@ def test_moe_bf16_gpt_oss_shapes_sampled(qmv, orc, workspace, n_tok):
         xb, xbits = bf16_rows(n_tok * (k if down else 1), cols, 61)
         if down:
             xb, xbits = xb.reshape(n_tok, k, cols), xbits.reshape(n_tok, k, cols)
-        y = run_moe(qmv, qmv.FMT(t, BF16), dev(W3), E, rows, cols, ids, gates if down else None, k, xb.cuda(),
+        W3d, wt = experts_on_device(qmv, W3, E * rows, cols, repacked)
+        y = run_moe(qmv, qmv.FMT(wt, BF16), W3d, E, rows, cols, ids, gates if down else None, k, xb.cuda(),
                     n_tok, b)
         toks = np.unique(np.concatenate([[0, n_tok - 1], g.integers(0, n_tok, 4)]))
         rids = np.unique(np.concatenate([[0, rows - 1], g.integers(0, rows, 30)]))
