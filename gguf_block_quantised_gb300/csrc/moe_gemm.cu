@@ -17,18 +17,22 @@
 //     warp 0      TMA producer of packed token tiles X[128 tokens][128 k]
 //                 (bf16, two 64-k boxes with 128-byte swizzle)
 //     warp 1      TMEM owner and the single-thread MMA issuer
-//     warps 2-3, 16-19  raw weight producers: per weight row, the 16-byte pieces of
+//     raw weight producers:
+//       GGUF rows (warps 2, 3, 24-27): per weight row, the 16-byte pieces of
 //                 its next 8 MXFP4 blocks (256 k) as cp.async copies (the
 //                 1530-byte row pitch of the gpt-oss experts is not a legal
 //                 TMA tensor stride, and one bulk copy per 136-byte row
 //                 segment is bound by the copy engine's per-request cost)
-//     warps 4-11  dequantisers (one 128-k stage per pass): MXFP4 -> bf16 A
-//                 tiles [128 rows][128 k] stored
+//       MXFP4_R rows (warp 2, one thread): per 512-k stage of 128 rows, two
+//                 128-byte-swizzled code boxes and one exponent box, as TMA
+//                 tensor copies
+//     warps 4-19  dequantisers, two groups of eight taking alternate 128-k
+//                 stages: MXFP4 -> bf16 A tiles [128 rows][128 k] stored
 //                 straight into TMEM (tcgen05.st; row = TMEM lane), through a
 //                 per-block table of the eight E2M1 magnitudes already scaled
 //                 by 2^(e-127).  Keeping A out of shared memory leaves the
 //                 shared-memory bandwidth to the token tiles and raw blocks.
-//     warps 12-15 epilogue: TMEM -> registers -> the (token, slot) output rows,
+//     warps 20-23 epilogue: TMEM -> registers -> the (token, slot) output rows,
 //                 plus the expert bias
 //   MMA M = 128 weight rows, N = 128 tokens, K = 16, A from TMEM, B (tokens)
 //   from shared memory, fp32 accumulator in TMEM, double-buffered so one
@@ -56,8 +60,8 @@ constexpr int SK = 4;                    // k stages (X tiles + A tile)
 constexpr int X_BYTES = BN * BK * 2;     // 16384 per sub-chunk
 constexpr int OFF_X = 0;
 constexpr int OFF_R = OFF_X + SK * KSUB * X_BYTES;
-constexpr int DEQ_WARPS = 8;             // warps 4..11
-constexpr int EPI_WARP0 = 12;            // warps 12..15
+constexpr int DEQ_WARPS = 16;            // warps 4..19: two groups of eight, alternate 128-k stages
+constexpr int EPI_WARP0 = 20;            // warps 20..23
 
 // Raw weight staging per layout.
 // GGUF MXFP4 rows: per raw stage, each row's next 8 blocks (256 k) as the
@@ -74,7 +78,7 @@ struct RawCfg {
     static constexpr int SR = PLANAR ? 2 : 4;                             // raw stages
     static constexpr int R_BYTES = PLANAR ? 2 * RC_BYTES + BM * 16 : BM * SLOT;   // 34816 / 22528
     static constexpr int ARRIVALS = PLANAR ? 1 : 192;                     // arrivals that fill a raw stage
-    static constexpr int THREADS = PLANAR ? 512 : 640;
+    static constexpr int THREADS = PLANAR ? 768 : 896;                    // + warps 24..27 (GGUF producers)
     static constexpr int OFF_BAR = OFF_R + SR * R_BYTES;
     static constexpr int N_BARS = 2 * SK + 2 * SR + 4;
     static constexpr int SMEM = OFF_BAR + N_BARS * 8 + 16 + 1024;   // + alignment slack
@@ -305,7 +309,7 @@ __global__ void __launch_bounds__(mg::RawCfg<PLANAR>::THREADS, 1)
     const int nsc = (a.nblk + SC_BLOCKS - 1) / SC_BLOCKS;  // raw stages per row
 
     if (tid == 0) {
-        for (int i = 0; i < SK; ++i) { mbar_init(&full[i], DEQ_WARPS + 1); mbar_init(&empty[i], 1); }
+        for (int i = 0; i < SK; ++i) { mbar_init(&full[i], DEQ_WARPS / 2 + 1); mbar_init(&empty[i], 1); }
         for (int i = 0; i < SR; ++i) { mbar_init(&rf[i], RC::ARRIVALS); mbar_init(&re[i], DEQ_WARPS); }
         for (int i = 0; i < 2; ++i) { mbar_init(&accf[i], 1); mbar_init(&acce[i], 4); }
         *abort_flag = 0;
@@ -372,7 +376,7 @@ __global__ void __launch_bounds__(mg::RawCfg<PLANAR>::THREADS, 1)
                 }
             }
         }
-    } else if (!PLANAR && (warp == 2 || warp == 3 || warp >= EPI_WARP0 + 4)) {
+    } else if (!PLANAR && (warp == 2 || warp == 3 || warp >= EPI_WARP0 + 4)) {   // warps 2, 3, 24..27
         // ---- raw weights: for each row of the tile, the 16-byte-aligned span
         // holding its next (up to) 8 blocks, as 16-byte cp.async pieces spread
         // over the 192 threads of warps 2, 3 and 16..19 (consecutive threads take
@@ -440,13 +444,17 @@ __global__ void __launch_bounds__(mg::RawCfg<PLANAR>::THREADS, 1)
             }
         }
     } else if (warp >= 4 && warp < 4 + DEQ_WARPS) {
-        // ---- dequantisers: thread t -> weight row t % 128 (its TMEM lane:
-        // warp % 4 is the warp's lane quarter) and block 2c + t / 128 of each
-        // 64-k chunk c, i.e. A tile columns 16 * (t / 128) .. +15
-        const int t0 = tid - 128, r = t0 & 127, half = t0 >> 7;
+        // ---- dequantisers, two groups of eight warps taking alternate 128-k
+        // stages (group g the stages of even / odd global index; with four
+        // stages each group cycles through two of them).  Within a group,
+        // thread t -> weight row t % 128 (its TMEM lane: warp % 4 is the warp's
+        // lane quarter) and block 2c + t / 128 of each 64-k chunk c, i.e. A
+        // tile columns 16 * (t / 128) .. +15
+        const int t0 = (tid - 128) & 255, grp = (tid - 128) >> 8, r = t0 & 127, half = t0 >> 7;
         const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + A_COL + 16 * half;
-        int sr = 0, s = 0;
-        uint32_t prf = 0, pe = 1;
+        int sr = 0;
+        uint32_t prf = 0;
+        uint32_t gk = 0;   // global index of the next 128-k stage
         for (int t = blockIdx.x; t < n_tiles && !__any_sync(0xffffffffu, *abort_flag); t += gridDim.x) {
             int e, nt, rt;
             tile_of(t, e, nt, rt);
@@ -462,7 +470,10 @@ __global__ void __launch_bounds__(mg::RawCfg<PLANAR>::THREADS, 1)
                 const int nc = (nb + 1) / 2;
                 // one 128-k stage (chunks 2cs, 2cs+1) per pass: two independent
                 // blocks per thread in flight, one wait for both TMEM stores
-                for (int cs = 0; 2 * cs < nc; ++cs) {
+                for (int cs = 0; 2 * cs < nc; ++cs, ++gk) {
+                    if ((int)(gk & 1) != grp) continue;
+                    const int s = (int)(gk % SK);
+                    const uint32_t pe = ((gk / SK) & 1) ^ 1;
                     if (!__all_sync(0xffffffffu, mbar_wait_bounded(&empty[s], pe, a.status))) { bad = true; break; }
                     tc_fence_after();
 #pragma unroll
@@ -489,7 +500,6 @@ __global__ void __launch_bounds__(mg::RawCfg<PLANAR>::THREADS, 1)
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&full[s]);
-                    if (++s == SK) { s = 0; pe ^= 1; }
                 }
                 if (bad) break;
                 __syncwarp();
