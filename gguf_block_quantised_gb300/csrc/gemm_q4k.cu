@@ -54,8 +54,7 @@ constexpr int EPI_WARPS = 8;                // two per TMEM lane quarter, each h
 constexpr int THREADS = 640;                // 20 warps
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t A_STAGE_COLS = KSUB * BK / 2;   // 128 bf16 k per row = 64 columns
-// accumulators: two of 128 columns (BN = 128) or one of 256 (BN = 256)
-static_assert(256 + SK * A_STAGE_COLS <= TMEM_COLS, "TMEM budget");
+// accumulators: two of 128 or 192 columns, or one of 256, then the A stages
 }  // namespace gq
 
 struct GemmArgs {
@@ -127,8 +126,8 @@ __global__ void __launch_bounds__(gq::THREADS, 1)
     // 128-token tiles double-buffer the accumulator so one tile's epilogue
     // overlaps the next tile's MMAs; 256-token tiles have room for one only.
     constexpr int NBUF = BN == 256 ? 1 : 2;
-    constexpr uint32_t A_COL = 256;
-    static_assert(NBUF * BN <= (int)A_COL, "tile width");
+    constexpr uint32_t A_COL = NBUF * BN;
+    static_assert(A_COL + SK * A_STAGE_COLS <= TMEM_COLS, "TMEM budget");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
@@ -291,17 +290,28 @@ __global__ void __launch_bounds__(gq::THREADS, 1)
             tc_fence_after();
             const int64_t row = (int64_t)rt * BM + 32 * q + lane;
             const bool row_ok = row < a.rows;
-            for (int c16 = ch * BN / 32; c16 < (ch + 1) * BN / 32; ++c16) {
-                float v[16];
-                tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + buf * BN + c16 * 16, v);
-                const int tok0 = nt * BN + c16 * 16;
+            // 32 columns per TMEM round trip; the accumulator is released as
+            // soon as the last columns are in registers, before their stores
+            const int c0 = ch * BN / 2, nr = BN / 64;
+            for (int rd = 0; rd < nr; ++rd) {
+                uint32_t v0[16], v1[16];
+                const uint32_t tc = tmem + ((uint32_t)(32 * q) << 16) + buf * BN + c0 + rd * 32;
+                tmem_ld16_async(tc, v0);
+                tmem_ld16_async(tc + 16, v1);
+                tmem_wait_ld();
+                if (rd == nr - 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&acce[buf]);
+                }
+                const int tok0 = nt * BN + c0 + rd * 32;
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    if (row_ok && tok0 + i < a.m) a.Y[(int64_t)(tok0 + i) * a.rows + row] = v[i];
+                for (int i = 0; i < 16; ++i) {
+                    if (row_ok && tok0 + i < a.m) a.Y[(int64_t)(tok0 + i) * a.rows + row] = __uint_as_float(v0[i]);
+                    if (row_ok && tok0 + 16 + i < a.m)
+                        a.Y[(int64_t)(tok0 + 16 + i) * a.rows + row] = __uint_as_float(v1[i]);
+                }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acce[buf]);
         }
     }
 
