@@ -8,7 +8,15 @@
 
 namespace qmv {
 
-constexpr int kChunkTargetBytes = 2560;          // per row segment of a stage
+// Bytes of one row segment of a stage.  Longer segments give each consumer
+// lane more units per pipeline item (fewer barrier round trips per byte);
+// Q4_K keeps shorter ones, whose stages are small enough for two CTAs per SM
+// with two rows per warp on its long rows.
+template <int T>
+constexpr int chunk_target_bytes()
+{
+    return T == QMV_Q4_K ? 2560 : 4096;
+}
 constexpr size_t kXhatMaxBytes = 96 * 1024;      // staged activations per CTA
 constexpr size_t kSmemTwoPerSm = 112 * 1024;     // two CTAs per SM
 constexpr size_t kSmemOnePerSm = 227 * 1024;
@@ -39,6 +47,7 @@ inline bool plan_gemv(bool a8, int64_t rows, int64_t cols, int n_vec, GemvPlan& 
 {
     using F = Fmt<T>;
     const int nb = (int)(cols / F::BS);
+    constexpr int kChunkTargetBytes = chunk_target_bytes<T>();
     if ((int64_t)nb * F::BB <= kChunkTargetBytes) {
         pl.kb = nb;
     } else {
