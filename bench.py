@@ -41,6 +41,7 @@ sys.path.insert(0, ROOT)
 from gguf_block_quantised_gb300 import synth  # noqa: E402
 
 Q4_0, Q5_0, Q8_0, Q4_K, Q6_K, MXFP4, Q8_K, F32, BF16, MXFP4_R = 1, 2, 3, 4, 5, 6, 7, 8, 9, 10
+NAMES = {Q4_0: "Q4_0", Q5_0: "Q5_0", Q8_0: "Q8_0", Q4_K: "Q4_K", Q6_K: "Q6_K", MXFP4: "MXFP4"}
 LAYERS = 24
 HID, FFN, KV, VOCAB = 896, 4864, 128, 151936
 # (name, rows, cols, input index) per layer; inputs: 0 attn-in, 1 o-in, 2 ffn-in, 3 down-in
@@ -330,6 +331,34 @@ def time_rotating(torch, stream, calls, reps, warmup=3, timed=3):
         e1.record(stream)
     e1.synchronize()
     return e0.elapsed_time(e1) / (timed * reps)
+
+
+def kquant_decode_leg(q, torch, stream, hbm):
+    """Llama-3-8B-shaped decode matvecs in K-quants (Q4_K 4096x4096,
+    1024x4096, 14336x4096, 4096x14336; Q6_K lm_head 128256x4096) with Q8_K
+    activations quantised in the kernel, at 1, 4 and 16 vectors.  Each shape
+    is launched as in a decode step (a programmatic dependent of the launch
+    before it), round robin over enough weight copies to exceed L2 twice, so
+    every launch reads its weights from HBM.  Metric: weight GB/s."""
+    shapes = [(Q4_K, 4096, 4096), (Q4_K, 1024, 4096), (Q4_K, 14336, 4096), (Q4_K, 4096, 14336),
+              (Q6_K, 128256, 4096)]
+    res = {}
+    for t, rows, cols in shapes:
+        W0 = torch.from_numpy(synth.weights(t, rows, cols, seed=7)).cuda()
+        copies = [W0] + [W0.clone() for _ in range(max(1, -(-300_000_000 // W0.numel())) - 1)]
+        for nv in (1, 4, 16):
+            x = torch.from_numpy(synth.activations(nv, cols, seed=8)).cuda()
+            y = torch.empty((nv, rows), dtype=torch.float32, device="cuda")
+            fmt = q.FMT(t, Q8_K) | q.FLAG_QUANTIZE_X | q.FLAG_PDL
+            calls = [lambda s, W=W: q.qmv_matvec(fmt, W, rows, cols, x, y, nv, s.cuda_stream) for W in copies]
+            reps = max(len(copies), 40)
+            ms = time_rotating(torch, stream, calls, reps)
+            gbs = W0.numel() / (ms / 1e3) / 1e9
+            res[f"{NAMES[t]}_{rows}x{cols}_nv{nv}"] = {"us": ms * 1e3, "weight_gbs": gbs, "frac_of_hbm": gbs / hbm}
+        del copies, W0
+    q.qmv_get_status(stream)
+    return {"metric": "decode matvec weight GB/s (K-quants, Q8_K activations quantised in-kernel, PDL chain)",
+            "unit": "GB/s", "by_shape": res}
 
 
 def prefill_leg(q, torch, stream, tflops_peak):
@@ -639,6 +668,7 @@ def main():
 
     hbm, peak_kind = load_peaks()
     tflops_peak = 1900.0 if peak_kind == "fallback" else load_tflops_peak()
+    kquant = None if args.no_extra else kquant_decode_leg(q, torch, stream, hbm)
     prefill = None if args.no_extra else prefill_leg(q, torch, stream, tflops_peak)
     moe = None if args.no_extra else moe_leg(q, torch, stream, hbm)
     value = ws * STEP_WEIGHT_BYTES / (ms1 / 1e3) / 1e9
@@ -690,6 +720,7 @@ def main():
                        "step, all in one replayed CUDA graph on the caller's stream"},
         "gpu_launches": launches_per_step * args.steps,
         "cpu_baseline": cpu,
+        "kquant_decode": kquant,
         "prefill": prefill,
         "moe": moe,
     }
