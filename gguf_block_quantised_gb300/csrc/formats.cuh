@@ -50,6 +50,21 @@ struct XView {
     int nb;   // activation blocks per vector (= weight blocks per row)
 };
 
+// Staged 8-bit activations of the K-quants: each 256-element block takes
+// kKPitch bytes, one 80-byte slot (64 codes + 16 of padding) per 64-element
+// unit, so that consecutive lanes, which decode consecutive units, read 16-byte
+// chunks 80 bytes apart (no shared-memory bank conflicts).  The unit slot holds
+// the unit's elements in this order: Q4_K unit c = elements 64c..64c+63;
+// Q6_K unit (h, lh) = elements 128h + 32g + 16lh + j for g = 0..3, j = 0..15.
+// Position of 16-element run r (elements 16r..16r+15) of a block:
+constexpr int kKPitch = 320;
+template <int T>
+__host__ __device__ constexpr int kquant_run_pos(int r)
+{
+    if constexpr (T == QMV_Q4_K) return 80 * (r >> 2) + 16 * (r & 3);
+    else return 80 * (2 * (r >> 3) + (r & 1)) + 16 * ((r & 7) >> 1);   // h = r/8, g = (r%8)/2, lh = r%2
+}
+
 template <int T>
 struct Fmt;
 
@@ -230,7 +245,7 @@ struct Fmt<QMV_Q4_K> {
     };
     static __device__ __forceinline__ void load_x_a8(const XView& X, int v, int b, int c, XA8& x)
     {
-        const uint4* p = reinterpret_cast<const uint4*>(X.codes + (size_t)v * X.cols + (size_t)b * 256 + 64 * c);
+        const uint4* p = reinterpret_cast<const uint4*>(X.codes + ((size_t)v * X.nb + b) * kKPitch + 80 * c);
         const uint4 a0 = p[0], a1 = p[1], a2 = p[2], a3 = p[3];
         x.lo[0] = a0.x; x.lo[1] = a0.y; x.lo[2] = a0.z; x.lo[3] = a0.w;
         x.lo[4] = a1.x; x.lo[5] = a1.y; x.lo[6] = a1.z; x.lo[7] = a1.w;
@@ -325,11 +340,11 @@ struct Fmt<QMV_Q6_K> {
     static __device__ __forceinline__ void load_x_a8(const XView& X, int v, int b, int sub, XA8& x)
     {
         const int h = sub >> 1, lh = sub & 1;
-        const uint8_t* base = X.codes + (size_t)v * X.cols + (size_t)b * 256 + 128 * h + 16 * lh;
+        const uint8_t* base = X.codes + ((size_t)v * X.nb + b) * kKPitch + 80 * sub;
         const int16_t* bs = X.bsum + ((size_t)v * X.nb + b) * 16 + 8 * h + lh;
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
-            const uint4 a = *reinterpret_cast<const uint4*>(base + 32 * g);
+            const uint4 a = *reinterpret_cast<const uint4*>(base + 16 * g);
             x.g[g][0] = a.x; x.g[g][1] = a.y; x.g[g][2] = a.z; x.g[g][3] = a.w;
             x.s[g] = bs[2 * g];
         }
@@ -445,6 +460,12 @@ __device__ __forceinline__ int staged_pos(int i)
     else return i;
 }
 
+// Bytes of staged activation codes for g vectors (8-bit staging).
+__host__ __device__ inline size_t xcode_bytes(int T, int g, int cols)
+{
+    return (T == QMV_Q4_K || T == QMV_Q6_K) ? (size_t)g * (cols / 256) * kKPitch : (size_t)g * cols;
+}
+
 // Bytes of staged activations for g vectors of `cols` elements.
 __host__ __device__ inline size_t xhat_bytes(int T, bool a8, int g, int cols)
 {
@@ -452,7 +473,7 @@ __host__ __device__ inline size_t xhat_bytes(int T, bool a8, int g, int cols)
     const size_t nb = (size_t)cols / bs;
     auto r16 = [](size_t v) { return (v + 15) & ~size_t(15); };
     if (a8) {
-        size_t s = r16((size_t)g * cols) + r16((size_t)g * nb * 4);
+        size_t s = r16(xcode_bytes(T, g, cols)) + r16((size_t)g * nb * 4);
         s += (bs == 32) ? r16((size_t)g * nb * 4) : r16((size_t)g * nb * 32);
         return s;
     }
@@ -472,7 +493,7 @@ __device__ __forceinline__ XView carve_xview(uint8_t* base, bool a8, int g, int 
     X.nb = nb;
     if (a8) {
         X.codes = base;
-        uint8_t* p = base + r16((size_t)g * cols);
+        uint8_t* p = base + r16(xcode_bytes(T, g, cols));
         X.d = reinterpret_cast<const float*>(p);
         p += r16((size_t)g * nb * 4);
         if (bs == 32) X.sum32 = reinterpret_cast<const int*>(p);
@@ -502,8 +523,8 @@ __device__ void stage_xhat(uint8_t* base, bool a8, bool quant_x, const void* x, 
     auto row = [&](int v) { return xb + (size_t)(idx ? idx[v] : v) * xrow; };
     if (a8 && quant_x) {
         uint8_t* codes = base;
-        float* d = reinterpret_cast<float*>(base + r16((size_t)g * cols));
-        uint8_t* tail = base + r16((size_t)g * cols) + r16((size_t)g * nb * 4);
+        float* d = reinterpret_cast<float*>(base + r16(xcode_bytes(T, g, cols)));
+        uint8_t* tail = base + r16(xcode_bytes(T, g, cols)) + r16((size_t)g * nb * 4);
         for (int i = tid; i < g * nb; i += nth) {       // one activation block per thread
             const int v = i / nb, b = i % nb;
             const float4* xp = reinterpret_cast<const float4*>(row(v)) + (size_t)b * (bs / 4);
@@ -514,7 +535,7 @@ __device__ void stage_xhat(uint8_t* base, bool a8, bool quant_x, const void* x, 
             }
             float dd, id;
             act_scale(amax, dd, id);
-            uint8_t* dst = codes + (size_t)i * bs;
+            uint8_t* dst = codes + (size_t)i * (bs == 32 || NATURAL ? bs : kKPitch);
             if constexpr (bs == 32) {
                 int s = 0;
                 for (int k = 0; k < 8; ++k) {
@@ -536,7 +557,7 @@ __device__ void stage_xhat(uint8_t* base, bool a8, bool quant_x, const void* x, 
                         const float4 w = xp[4 * r + k];
                         const int8_t q0 = quant1(w.x, id), q1 = quant1(w.y, id), q2 = quant1(w.z, id),
                                      q3 = quant1(w.w, id);
-                        reinterpret_cast<uint32_t*>(dst)[4 * r + k] =
+                        reinterpret_cast<uint32_t*>(dst + (NATURAL ? 16 * r : kquant_run_pos<T>(r)))[k] =
                             (uint32_t)(uint8_t)q0 | ((uint32_t)(uint8_t)q1 << 8) | ((uint32_t)(uint8_t)q2 << 16) |
                             ((uint32_t)(uint8_t)q3 << 24);
                         s += q0 + q1 + q2 + q3;
@@ -548,8 +569,8 @@ __device__ void stage_xhat(uint8_t* base, bool a8, bool quant_x, const void* x, 
         }
     } else if (a8) {
         uint8_t* codes = base;
-        float* d = reinterpret_cast<float*>(base + r16((size_t)g * cols));
-        uint8_t* tail = base + r16((size_t)g * cols) + r16((size_t)g * nb * 4);
+        float* d = reinterpret_cast<float*>(base + r16(xcode_bytes(T, g, cols)));
+        uint8_t* tail = base + r16(xcode_bytes(T, g, cols)) + r16((size_t)g * nb * 4);
         if constexpr (bs == 32) {
             // Q8_0 blocks: fp16 d | int8[32], 34 bytes, 2-byte aligned.
             int* sum = reinterpret_cast<int*>(tail);
@@ -579,7 +600,11 @@ __device__ void stage_xhat(uint8_t* base, bool a8, bool quant_x, const void* x, 
                 const int v = blkno / nb, b = blkno % nb;
                 const uint32_t val = reinterpret_cast<const uint32_t*>(row(v) + (size_t)b * 292)[wd];
                 if (wd == 0) d[blkno] = __uint_as_float(val);
-                else if (wd <= 64) reinterpret_cast<uint32_t*>(codes + (size_t)blkno * 256)[wd - 1] = val;
+                else if (wd <= 64) {
+                    const int w = wd - 1;   // code word w: elements 4w..4w+3, run w / 4
+                    if (NATURAL) reinterpret_cast<uint32_t*>(codes + (size_t)blkno * 256)[w] = val;
+                    else reinterpret_cast<uint32_t*>(codes + (size_t)blkno * kKPitch + kquant_run_pos<T>(w >> 2))[w & 3] = val;
+                }
                 else reinterpret_cast<uint32_t*>(bsum + (size_t)blkno * 16)[wd - 65] = val;
             }
         }

@@ -99,7 +99,7 @@ __global__ void k_block_dots(const uint8_t* __restrict__ W, int64_t rows, int co
     copy_block<T>(W + (r * nb + b) * F::BB, buf);
 
     // Stage this activation block in the matvec kernels' shared-memory layout.
-    __align__(16) uint8_t codes[F::BS];
+    __align__(16) uint8_t codes[F::BS == 32 ? 32 : kKPitch];
     float d;
     int sum32 = 0;
     __align__(16) int16_t bsum[16];
@@ -120,7 +120,7 @@ __global__ void k_block_dots(const uint8_t* __restrict__ W, int64_t rows, int co
         const uint8_t* a = xq + ((int64_t)v * nb + b) * 292;
         uint32_t u = (uint32_t)a[0] | ((uint32_t)a[1] << 8) | ((uint32_t)a[2] << 16) | ((uint32_t)a[3] << 24);
         d = __uint_as_float(u);
-        for (int k = 0; k < 256; ++k) codes[k] = a[4 + k];
+        for (int k = 0; k < 256; ++k) codes[kquant_run_pos<T>(k >> 4) + (k & 15)] = a[4 + k];
         for (int g = 0; g < 16; ++g) bsum[g] = (int16_t)((uint32_t)a[260 + 2 * g] | ((uint32_t)a[261 + 2 * g] << 8));
         X.bsum = bsum;
     }
