@@ -58,6 +58,10 @@ struct XView {
 // Q6_K unit (h, lh) = elements 128h + 32g + 16lh + j for g = 0..3, j = 0..15.
 // Position of 16-element run r (elements 16r..16r+15) of a block:
 constexpr int kKPitch = 320;
+// Staged 8-bit activations of the 32-element formats: kBPitch bytes per block
+// (32 codes + 16 of padding), so that consecutive lanes' 16-byte loads land in
+// distinct banks.
+constexpr int kBPitch = 48;
 template <int T>
 __host__ __device__ constexpr int kquant_run_pos(int r)
 {
@@ -88,7 +92,7 @@ struct Fmt32Base {
 
     static __device__ __forceinline__ void load_x_a8(const XView& X, int v, int b, int /*sub*/, XA8& x)
     {
-        const uint4* p = reinterpret_cast<const uint4*>(X.codes + (size_t)v * X.cols + (size_t)b * 32);
+        const uint4* p = reinterpret_cast<const uint4*>(X.codes + ((size_t)v * X.nb + b) * kBPitch);
         const uint4 a = p[0], c = p[1];
         x.w[0] = a.x; x.w[1] = a.y; x.w[2] = a.z; x.w[3] = a.w;
         x.w[4] = c.x; x.w[5] = c.y; x.w[6] = c.z; x.w[7] = c.w;
@@ -463,7 +467,7 @@ __device__ __forceinline__ int staged_pos(int i)
 // Bytes of staged activation codes for g vectors (8-bit staging).
 __host__ __device__ inline size_t xcode_bytes(int T, int g, int cols)
 {
-    return (T == QMV_Q4_K || T == QMV_Q6_K) ? (size_t)g * (cols / 256) * kKPitch : (size_t)g * cols;
+    return (T == QMV_Q4_K || T == QMV_Q6_K) ? (size_t)g * (cols / 256) * kKPitch : (size_t)g * (cols / 32) * kBPitch;
 }
 
 // Bytes of staged activations for g vectors of `cols` elements.
@@ -535,7 +539,7 @@ __device__ void stage_xhat(uint8_t* base, bool a8, bool quant_x, const void* x, 
             }
             float dd, id;
             act_scale(amax, dd, id);
-            uint8_t* dst = codes + (size_t)i * (bs == 32 || NATURAL ? bs : kKPitch);
+            uint8_t* dst = codes + (size_t)i * (NATURAL ? bs : bs == 32 ? kBPitch : kKPitch);
             if constexpr (bs == 32) {
                 int s = 0;
                 for (int k = 0; k < 8; ++k) {
@@ -586,7 +590,7 @@ __device__ void stage_xhat(uint8_t* base, bool a8, bool quant_x, const void* x, 
                     q[2 * k + 1] = two >> 8;
                     s += (int)(int8_t)(two & 0xffu) + (int)(int8_t)(two >> 8);
                 }
-                uint8_t* dst = codes + (size_t)i * 32;   // vector v, block b: i = v*nb + b
+                uint8_t* dst = codes + (size_t)i * (NATURAL ? 32 : kBPitch);   // vector v, block b: i = v*nb + b
 #pragma unroll
                 for (int k = 0; k < 32; ++k) dst[NATURAL ? k : staged_pos<T>(k)] = q[k];
                 d[i] = half_bits_to_float(h[0]);

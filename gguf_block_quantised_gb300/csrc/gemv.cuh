@@ -211,11 +211,20 @@ __device__ __forceinline__ float warp_sum_rows(const float (&v)[RIF])
     }
 }
 
+// Decode with 8-bit activations and one or two vectors (up to eight for the
+// 32-element formats): registers for two CTAs per SM, at most 96 per thread
+// since the register file is split per scheduler and two 9-warp CTAs put five
+// warps on some schedulers.  (The K-quant decoders otherwise take ~165 and
+// leave one 9-warp CTA per SM, too few warps to keep the weight stream in
+// flight; beyond these vector counts the two-CTA bound would spill.)
+template <int T, bool A8, int NV>
+constexpr bool two_ctas_per_sm()
+{
+    return A8 && (NV <= 2 || (Fmt<T>::BS == 32 && NV <= 8));
+}
+
 template <int T, bool A8, int NV, int RIF>
-// Decode with 8-bit activations and one or two vectors: registers for two CTAs
-// per SM (the K-quant decoders otherwise take ~165 and leave one 9-warp CTA
-// per SM, too few warps to keep the weight stream in flight).
-__global__ void __launch_bounds__(kGemvThreads, A8 && NV <= 2 ? 2 : 1) k_gemv(const GemvParams p)
+__global__ void __launch_bounds__(kGemvThreads, two_ctas_per_sm<T, A8, NV>() ? 2 : 1) k_gemv(const GemvParams p)
 {
     using F = Fmt<T>;
     extern __shared__ __align__(128) uint8_t smem[];

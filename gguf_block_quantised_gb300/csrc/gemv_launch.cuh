@@ -65,12 +65,12 @@ inline bool plan_gemv(bool a8, int64_t rows, int64_t cols, int n_vec, GemvPlan& 
         // Accumulators stay in registers across K-chunks only for one row
         // group, so a multi-chunk row gives each warp as many rows as this
         // group's kernel decodes at once (smaller groups decode at least as many).
-        // With 8-bit activations and one or two vectors the kernel's registers
-        // allow two CTAs per SM, and tiles that let two CTAs share an SM (three
+        // With 8-bit activations and one or two vectors (up to eight for the
+        // 32-element formats) the kernel's registers allow two CTAs per SM, and tiles that let two CTAs share an SM (three
         // stages each) are preferred over larger tiles with one CTA per SM;
         // otherwise the largest tile wins, with two CTAs per SM if it fits.
         const int rif = rows_in_flight_rt(T, g);
-        const bool prefer_two = a8 && g <= 2;
+        const bool prefer_two = a8 && (g <= 2 || (F::BS == 32 && g <= 8));   // as two_ctas_per_sm()
         bool found = false;
         for (int pass = prefer_two ? 0 : 2; pass < 3 && !found; ++pass) {
             // Rows per warp: at most the rows the kernel decodes at once when a

@@ -99,7 +99,7 @@ __global__ void k_block_dots(const uint8_t* __restrict__ W, int64_t rows, int co
     copy_block<T>(W + (r * nb + b) * F::BB, buf);
 
     // Stage this activation block in the matvec kernels' shared-memory layout.
-    __align__(16) uint8_t codes[F::BS == 32 ? 32 : kKPitch];
+    __align__(16) uint8_t codes[F::BS == 32 ? kBPitch : kKPitch];
     float d;
     int sum32 = 0;
     __align__(16) int16_t bsum[16];
