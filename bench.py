@@ -564,6 +564,18 @@ def traffic_for(kernel):
         return None
 
 
+def max_over_ranks(torch, values, device):
+    """The element-wise maximum of `values` over the ranks of the process group
+    (a copy of `values` for a single process): replicas report the slowest
+    rank's time, so value = all ranks' units / that time."""
+    dist = torch.distributed
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return list(values)
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -642,10 +654,7 @@ def main():
     ms8, _ = time_graph(torch, step8.run, stream, max(args.steps // 4, 10), args.warmup)
     ms1u, _ = time_graph(torch, step1u.run, stream, max(args.steps // 4, 10), args.warmup)
     q.qmv_get_status(stream)
-    if ws > 1:
-        t = torch.tensor([ms1, ms8], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms1, ms8 = t.tolist()
+    ms1, ms8 = max_over_ranks(torch, [ms1, ms8], "cuda")
 
     lm_ms, lm_clocks = lm_roofline(q, torch, stream, step1, local)
     lm_ms_nopdl, _ = lm_roofline(q, torch, stream, step1, local, pdl=False)

@@ -228,3 +228,86 @@ def test_pdl_flag_same_results(qmv, orc):
     b = chain(qmv.FLAG_PDL)
     assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
     qmv.qmv_get_status()
+
+
+# ---- degenerate blocks, many vectors, the longest rows ------------------------------
+
+@pytest.mark.parametrize("t", [1, 2, 3, 4, 5, 6])
+def test_matvec_degenerate_blocks(qmv, orc, t):
+    """Rows whose blocks all have a zero scale (Q4_K: zero d and dmin; MXFP4:
+    zero codes) give exactly zero, with 8-bit and fp32 activations; the other
+    rows are unaffected."""
+    rows, cols = 12, 512
+    blocks = synth.weights(t, rows, cols, seed=60 + t).view(synth.block_dtype(t)).reshape(rows, -1)
+    zero_rows = [0, 5, 11]
+    for r in zero_rows:
+        if t == 6:
+            blocks[r]["qs"] = 0
+        else:
+            blocks[r]["d"] = 0
+            if t == 4:
+                blocks[r]["dmin"] = 0
+    W = blocks.view(np.uint8).reshape(-1)
+    at8 = 7 if t in (4, 5) else 3
+    x = synth.activations(3, cols, seed=61)
+    for at in (at8, 8):
+        xin = orc.quantize_act(at, x) if at != 8 else x
+        yref, yabs = orc.matvec(t, at, W, rows, cols, xin, 3)
+        y = torch.full((3, rows), float("nan"), dtype=torch.float32, device="cuda")
+        qmv.qmv_matvec(qmv.FMT(t, at) | (qmv.FLAG_QUANTIZE_X if at != 8 else 0), dev(W), rows, cols, dev(x), y, 3)
+        yh = host(y)
+        assert (yh[:, zero_rows] == 0).all() and (yref[:, zero_rows] == 0).all()
+        assert_close(yh, yref, yabs, what=f"t={t} at={at}")
+
+
+def test_matvec_mxfp4_nan_exponent(qmv, orc):
+    """An E8M0 exponent of 255 is NaN (OCP): the row holding that block is NaN
+    on both sides, the other rows are finite and match."""
+    rows, cols = 6, 256
+    blocks = synth.weights(6, rows, cols, seed=70).view(synth.block_dtype(6)).reshape(rows, -1)
+    blocks[2, 3]["e"] = 255
+    W = blocks.view(np.uint8).reshape(-1)
+    x = synth.activations(2, cols, seed=71)
+    for at in (3, 8):
+        xin = orc.quantize_act(at, x) if at != 8 else x
+        yref, yabs = orc.matvec(6, at, W, rows, cols, xin, 2)
+        y = torch.empty((2, rows), dtype=torch.float32, device="cuda")
+        qmv.qmv_matvec(qmv.FMT(6, at) | (qmv.FLAG_QUANTIZE_X if at != 8 else 0), dev(W), rows, cols, dev(x), y, 2)
+        yh = host(y)
+        assert np.isnan(yref[:, 2]).all() and np.isnan(yh[:, 2]).all()
+        keep = [r for r in range(rows) if r != 2]
+        assert_close(yh[:, keep], yref[:, keep], yabs[:, keep], what=f"at={at}")
+
+
+@pytest.mark.parametrize("t,at", [(2, 3), (4, 7), (6, 8)])
+def test_matvec_many_vectors(qmv, orc, t, at):
+    """37 vectors: several launches of up to 16 vectors each, a ragged last group."""
+    rows, cols, n_vec = 70, 512, 37
+    W = synth.weights(t, rows, cols, seed=80 + t)
+    x = synth.activations(n_vec, cols, seed=81)
+    xin = orc.quantize_act(at, x) if at != 8 else x
+    yref, yabs = orc.matvec(t, at, W, rows, cols, xin, n_vec)
+    y = torch.full((n_vec, rows), float("nan"), dtype=torch.float32, device="cuda")
+    qmv.qmv_matvec(qmv.FMT(t, at) | (qmv.FLAG_QUANTIZE_X if at != 8 else 0), dev(W), rows, cols, dev(x), y, n_vec)
+    assert_close(host(y), yref, yabs, what=f"t={t} at={at}")
+
+
+def test_matvec_longest_rows(qmv, orc):
+    """A row of 65536 elements stages its 8-bit activations in one SM's shared
+    memory and is computed; rows whose staged activations cannot fit are
+    refused with QMV_ERR_SHAPE before anything is launched."""
+    rows, cols = 3, 65536
+    W = synth.weights(1, rows, cols, seed=90)
+    x = synth.activations(1, cols, seed=91)
+    yref, yabs = orc.matvec(1, 3, W, rows, cols, orc.quantize_act(3, x), 1)
+    y = torch.full((1, rows), float("nan"), dtype=torch.float32, device="cuda")
+    qmv.qmv_matvec(qmv.FMT(1, 3) | qmv.FLAG_QUANTIZE_X, dev(W), rows, cols, dev(x), y, 1)
+    assert_close(host(y), yref, yabs, what="65536 cols")
+    big = torch.zeros(rows * qmv.qmv_row_bytes(1, 1 << 17), dtype=torch.uint8, device="cuda")
+    xb = torch.zeros((1, 1 << 17), dtype=torch.float32, device="cuda")
+    yb = torch.zeros((1, rows), dtype=torch.float32, device="cuda")
+    for fmt, c in ((qmv.FMT(1, 3) | qmv.FLAG_QUANTIZE_X, 1 << 17), (qmv.FMT(1, 8), 1 << 16)):
+        with pytest.raises(qmv.QmvError) as e:
+            qmv.qmv_matvec(fmt, big, rows, c, xb, yb, 1)
+        assert e.value.code == qmv.ERR_SHAPE and "shared memory" in str(e.value)
+    qmv.qmv_get_status()
