@@ -509,8 +509,153 @@ __device__ __forceinline__ XView carve_xview(uint8_t* base, bool a8, int g, int 
     return X;
 }
 
-// Stage g activation vectors with threads tid = 0..nth-1 of the block (the
-// caller synchronises afterwards).  Vector v is row idx[v] (v when idx is
+// Quantise-while-staging: TPB threads per activation block, each loading its
+// 32/TPB (or 256/TPB) consecutive values at once; the block's amax and code
+// sums are xor-shuffles over the TPB lanes, which are consecutive lanes of one
+// warp (the loop runs over whole warps: nth is a multiple of 32).  Scale,
+// codes and sums are those of the activation quantiser.  Small activations
+// (one decode vector of a few thousand elements) would otherwise be quantised
+// by a few dozen threads, each over a whole block, on the critical path of
+// every launch.
+template <int T, bool NATURAL, int TPB, typename Row>
+__device__ __forceinline__ void stage_quant32(uint8_t* codes, float* d, uint8_t* tail, const Row& row, int nbk,
+                                              int nb, int tid, int nth)
+{
+    if constexpr (TPB == 1) {
+        // One block per thread: an amax pass, then a quantising pass over the
+        // same (cached) values; measured faster here than holding the block
+        // in registers.
+        for (int i = tid; i < nbk; i += nth) {
+            const float4* xp = reinterpret_cast<const float4*>(row(i / nb)) + (size_t)(i % nb) * 8;
+            float amax = 0.f;
+            for (int k = 0; k < 8; ++k) {
+                const float4 w = xp[k];
+                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(w.x), fabsf(w.y)), fmaxf(fabsf(w.z), fabsf(w.w))));
+            }
+            float dd, id;
+            act_scale(amax, dd, id);
+            uint8_t* dst = codes + (size_t)i * (NATURAL ? 32 : kBPitch);
+            int sum = 0;
+            for (int k = 0; k < 8; ++k) {
+                const float4 w = xp[k];
+                const int8_t q0 = quant1(w.x, id), q1 = quant1(w.y, id), q2 = quant1(w.z, id), q3 = quant1(w.w, id);
+                dst[NATURAL ? 4 * k + 0 : staged_pos<T>(4 * k + 0)] = (uint8_t)q0;
+                dst[NATURAL ? 4 * k + 1 : staged_pos<T>(4 * k + 1)] = (uint8_t)q1;
+                dst[NATURAL ? 4 * k + 2 : staged_pos<T>(4 * k + 2)] = (uint8_t)q2;
+                dst[NATURAL ? 4 * k + 3 : staged_pos<T>(4 * k + 3)] = (uint8_t)q3;
+                sum += q0 + q1 + q2 + q3;
+            }
+            d[i] = __half2float(__float2half_rn(dd));   // Q8_0 keeps its scale in fp16
+            reinterpret_cast<int*>(tail)[i] = sum;
+        }
+        return;
+    }
+    constexpr int E = 32 / TPB, NF4 = E / 4;
+    const int lane = tid & 31, total = nbk * TPB;
+    for (int i0 = tid - lane; i0 < total; i0 += nth) {
+        const int i = i0 + lane, blk = i / TPB, part = i % TPB;
+        const bool valid = i < total;    // the same for the TPB lanes of a block
+        float4 w[NF4];
+        float amax = 0.f;
+#pragma unroll
+        for (int f = 0; f < NF4; ++f) w[f] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (valid) {
+            const float4* xp = reinterpret_cast<const float4*>(row(blk / nb)) + (size_t)(blk % nb) * 8 + part * NF4;
+#pragma unroll
+            for (int f = 0; f < NF4; ++f) w[f] = xp[f];
+        }
+#pragma unroll
+        for (int f = 0; f < NF4; ++f)
+            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(w[f].x), fabsf(w[f].y)), fmaxf(fabsf(w[f].z), fabsf(w[f].w))));
+#pragma unroll
+        for (int o = 1; o < TPB; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        float dd, id;
+        act_scale(amax, dd, id);
+        uint8_t* dst = codes + (size_t)blk * (NATURAL ? 32 : kBPitch);
+        int sum = 0;
+#pragma unroll
+        for (int f = 0; f < NF4; ++f) {
+            const int8_t q0 = quant1(w[f].x, id), q1 = quant1(w[f].y, id), q2 = quant1(w[f].z, id),
+                         q3 = quant1(w[f].w, id);
+            sum += q0 + q1 + q2 + q3;
+            const int e = part * E + 4 * f;
+            if (!valid) continue;
+            if (NATURAL || T != QMV_MXFP4) {
+                reinterpret_cast<uint32_t*>(dst)[e >> 2] = (uint32_t)(uint8_t)q0 | ((uint32_t)(uint8_t)q1 << 8) |
+                                                           ((uint32_t)(uint8_t)q2 << 16) |
+                                                           ((uint32_t)(uint8_t)q3 << 24);
+            } else {
+                dst[staged_pos<T>(e + 0)] = (uint8_t)q0;
+                dst[staged_pos<T>(e + 1)] = (uint8_t)q1;
+                dst[staged_pos<T>(e + 2)] = (uint8_t)q2;
+                dst[staged_pos<T>(e + 3)] = (uint8_t)q3;
+            }
+        }
+#pragma unroll
+        for (int o = 1; o < TPB; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        if (valid && part == 0) {
+            d[blk] = __half2float(__float2half_rn(dd));   // Q8_0 keeps its scale in fp16
+            reinterpret_cast<int*>(tail)[blk] = sum;
+        }
+    }
+}
+
+template <int T, bool NATURAL, int TPB, typename Row>
+__device__ __forceinline__ void stage_quant256(uint8_t* codes, float* d, uint8_t* tail, const Row& row, int nbk,
+                                               int nb, int tid, int nth)
+{
+    static_assert(TPB == 8 || TPB == 16 || TPB == 32, "256-element blocks: 8, 16 or 32 threads each");
+    constexpr int E = 256 / TPB, NF4 = E / 4;
+    const int lane = tid & 31, total = nbk * TPB;
+    for (int i0 = tid - lane; i0 < total; i0 += nth) {
+        const int i = i0 + lane, blk = i / TPB, part = i % TPB;
+        const bool valid = i < total;
+        float4 w[NF4];
+        float amax = 0.f;
+#pragma unroll
+        for (int f = 0; f < NF4; ++f) w[f] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (valid) {
+            const float4* xp = reinterpret_cast<const float4*>(row(blk / nb)) + (size_t)(blk % nb) * 64 + part * NF4;
+#pragma unroll
+            for (int f = 0; f < NF4; ++f) w[f] = xp[f];
+        }
+#pragma unroll
+        for (int f = 0; f < NF4; ++f)
+            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(w[f].x), fabsf(w[f].y)), fmaxf(fabsf(w[f].z), fabsf(w[f].w))));
+#pragma unroll
+        for (int o = 1; o < TPB; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        float dd, id;
+        act_scale(amax, dd, id);
+        uint8_t* dst = codes + (size_t)blk * (NATURAL ? 256 : kKPitch);
+        int16_t* bsum = reinterpret_cast<int16_t*>(tail) + (size_t)blk * 16;
+        int s16 = 0;   // running sum of the current 16-group
+#pragma unroll
+        for (int f = 0; f < NF4; ++f) {
+            const int8_t q0 = quant1(w[f].x, id), q1 = quant1(w[f].y, id), q2 = quant1(w[f].z, id),
+                         q3 = quant1(w[f].w, id);
+            s16 += q0 + q1 + q2 + q3;
+            const int e = part * E + 4 * f, r = e >> 4;
+            if (valid)
+                reinterpret_cast<uint32_t*>(dst + (NATURAL ? 16 * r : kquant_run_pos<T>(r)))[(e & 15) >> 2] =
+                    (uint32_t)(uint8_t)q0 | ((uint32_t)(uint8_t)q1 << 8) | ((uint32_t)(uint8_t)q2 << 16) |
+                    ((uint32_t)(uint8_t)q3 << 24);
+            if constexpr (E >= 16) {
+                if ((f & 3) == 3) {   // a whole 16-group in this thread
+                    if (valid) bsum[r] = (int16_t)s16;
+                    s16 = 0;
+                }
+            }
+        }
+        if constexpr (E == 8) {   // a 16-group spans two lanes
+            s16 += __shfl_xor_sync(0xffffffffu, s16, 1);
+            if (valid && (part & 1) == 0) bsum[(part * E) >> 4] = (int16_t)s16;
+        }
+        if (valid && part == 0) d[blk] = dd;
+    }
+}
+
+// Stage g activation vectors with threads tid = 0..nth-1 of the block, whole
+// warps (nth a multiple of 32; the caller synchronises afterwards).  Vector v is row idx[v] (v when idx is
 // NULL) of the caller's activations, whose rows are xrow bytes apart: fp32
 // [cols] (A32, or A8 with quant_x) or Q8_0/Q8_K blocks [nb] (A8).  With
 // quant_x the fp32 activations are quantised here with the exact steps of the
@@ -529,47 +674,18 @@ __device__ void stage_xhat(uint8_t* base, bool a8, bool quant_x, const void* x, 
         uint8_t* codes = base;
         float* d = reinterpret_cast<float*>(base + r16(xcode_bytes(T, g, cols)));
         uint8_t* tail = base + r16(xcode_bytes(T, g, cols)) + r16((size_t)g * nb * 4);
-        for (int i = tid; i < g * nb; i += nth) {       // one activation block per thread
-            const int v = i / nb, b = i % nb;
-            const float4* xp = reinterpret_cast<const float4*>(row(v)) + (size_t)b * (bs / 4);
-            float amax = 0.f;
-            for (int k = 0; k < bs / 4; ++k) {
-                const float4 w = xp[k];
-                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(w.x), fabsf(w.y)), fmaxf(fabsf(w.z), fabsf(w.w))));
-            }
-            float dd, id;
-            act_scale(amax, dd, id);
-            uint8_t* dst = codes + (size_t)i * (NATURAL ? bs : bs == 32 ? kBPitch : kKPitch);
-            if constexpr (bs == 32) {
-                int s = 0;
-                for (int k = 0; k < 8; ++k) {
-                    const float4 w = xp[k];
-                    const int8_t q0 = quant1(w.x, id), q1 = quant1(w.y, id), q2 = quant1(w.z, id), q3 = quant1(w.w, id);
-                    dst[NATURAL ? 4 * k + 0 : staged_pos<T>(4 * k + 0)] = (uint8_t)q0;
-                    dst[NATURAL ? 4 * k + 1 : staged_pos<T>(4 * k + 1)] = (uint8_t)q1;
-                    dst[NATURAL ? 4 * k + 2 : staged_pos<T>(4 * k + 2)] = (uint8_t)q2;
-                    dst[NATURAL ? 4 * k + 3 : staged_pos<T>(4 * k + 3)] = (uint8_t)q3;
-                    s += q0 + q1 + q2 + q3;
-                }
-                d[i] = __half2float(__float2half_rn(dd));   // Q8_0 keeps its scale in fp16
-                reinterpret_cast<int*>(tail)[i] = s;
-            } else {
-                int16_t* bsum = reinterpret_cast<int16_t*>(tail) + (size_t)i * 16;
-                for (int r = 0; r < 16; ++r) {
-                    int s = 0;
-                    for (int k = 0; k < 4; ++k) {
-                        const float4 w = xp[4 * r + k];
-                        const int8_t q0 = quant1(w.x, id), q1 = quant1(w.y, id), q2 = quant1(w.z, id),
-                                     q3 = quant1(w.w, id);
-                        reinterpret_cast<uint32_t*>(dst + (NATURAL ? 16 * r : kquant_run_pos<T>(r)))[k] =
-                            (uint32_t)(uint8_t)q0 | ((uint32_t)(uint8_t)q1 << 8) | ((uint32_t)(uint8_t)q2 << 16) |
-                            ((uint32_t)(uint8_t)q3 << 24);
-                        s += q0 + q1 + q2 + q3;
-                    }
-                    bsum[r] = (int16_t)s;
-                }
-                d[i] = dd;
-            }
+        // As many threads per block as one pass of the block's threads allows
+        // (a block's activations then arrive with one round of loads).
+        const int nbk = g * nb;
+        if constexpr (bs == 32) {
+            if (nbk * 8 <= nth) stage_quant32<T, NATURAL, 8>(codes, d, tail, row, nbk, nb, tid, nth);
+            else if (nbk * 4 <= nth) stage_quant32<T, NATURAL, 4>(codes, d, tail, row, nbk, nb, tid, nth);
+            else if (nbk * 2 <= nth) stage_quant32<T, NATURAL, 2>(codes, d, tail, row, nbk, nb, tid, nth);
+            else stage_quant32<T, NATURAL, 1>(codes, d, tail, row, nbk, nb, tid, nth);
+        } else {
+            if (nbk * 32 <= nth) stage_quant256<T, NATURAL, 32>(codes, d, tail, row, nbk, nb, tid, nth);
+            else if (nbk * 16 <= nth) stage_quant256<T, NATURAL, 16>(codes, d, tail, row, nbk, nb, tid, nth);
+            else stage_quant256<T, NATURAL, 8>(codes, d, tail, row, nbk, nb, tid, nth);
         }
     } else if (a8) {
         uint8_t* codes = base;

@@ -189,13 +189,14 @@ def test_config_shapes_sampled(qmv, orc, cfg):
 @pytest.mark.parametrize("t", ALLW)
 def test_quantize_x_flag_bit_identical(qmv, orc, t):
     """QMV_FLAG_QUANTIZE_X (quantise fp32 activations inside the matvec) gives
-    the same bits as qmv_quantize_act followed by qmv_matvec."""
+    the same bits as qmv_quantize_act followed by qmv_matvec.  The vector
+    counts and widths reach every thread-per-block split of the in-kernel
+    quantiser (8, 4, 2, 1 threads per 32-element block; 32, 16, 8 per 256)."""
     at = act_for(t)
-    for rows, cols in shapes_for(t)[1:]:
-        n_vec = 5
+    for (rows, cols), n_vec in [(rc, n) for rc in shapes_for(t)[1:] for n in (1, 2, 5)]:
         W = dev(synth.weights(t, rows, cols, seed=6))
         x = synth.activations(n_vec, cols, seed=6)
-        x[1, :64] = 0.0
+        x[n_vec - 1, :64] = 0.0       # an all-zero block
         xd = dev(x)
         xq = torch.empty(n_vec * qmv.qmv_row_bytes(at, cols), dtype=torch.uint8, device="cuda")
         qmv.qmv_quantize_act(at, xd, xq, n_vec * cols)
