@@ -120,6 +120,21 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 }
 
 // Hint the L2 to start fetching [src, src+bytes) (16-byte aligned, multiple of 16).
+// Pull the 128-byte lines of [p, p + bytes) into L2, the lanes of one warp
+// taking lines in turn.  A hint only: nothing returns to the thread, and a
+// store by another grid to those lines still lands in L2, so it may precede
+// the wait for the grid that writes them.
+__device__ __forceinline__ void prefetch_l2_lines(const void* p, size_t bytes, int lane)
+{
+    if (bytes == 0) return;
+    const char* c = static_cast<const char*>(p);
+    const size_t n = bytes / 128 + 2;   // lines touched by an unaligned range
+    for (size_t k = lane; k < n; k += 32) {
+        const char* a = c + (k * 128 < bytes ? k * 128 : bytes - 1);
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+    }
+}
+
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes)
 {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");

@@ -674,13 +674,16 @@ __device__ void stage_xhat(uint8_t* base, bool a8, bool quant_x, const void* x, 
         uint8_t* codes = base;
         float* d = reinterpret_cast<float*>(base + r16(xcode_bytes(T, g, cols)));
         uint8_t* tail = base + r16(xcode_bytes(T, g, cols)) + r16((size_t)g * nb * 4);
-        // As many threads per block as one pass of the block's threads allows
-        // (a block's activations then arrive with one round of loads).
+        // As many threads per block as one pass of the CTA's threads allows (a
+        // block's activations then arrive with one round of loads), or two
+        // passes if the second is at least half full (else the CTA would wait
+        // a whole pass for a few threads).
         const int nbk = g * nb;
+        auto fits = [&](int t) { return nbk * t <= nth || (nbk * t <= 2 * nth && 2 * nbk * t >= 3 * nth); };
         if constexpr (bs == 32) {
-            if (nbk * 8 <= nth) stage_quant32<T, NATURAL, 8>(codes, d, tail, row, nbk, nb, tid, nth);
-            else if (nbk * 4 <= nth) stage_quant32<T, NATURAL, 4>(codes, d, tail, row, nbk, nb, tid, nth);
-            else if (nbk * 2 <= nth) stage_quant32<T, NATURAL, 2>(codes, d, tail, row, nbk, nb, tid, nth);
+            if (fits(8)) stage_quant32<T, NATURAL, 8>(codes, d, tail, row, nbk, nb, tid, nth);
+            else if (fits(4)) stage_quant32<T, NATURAL, 4>(codes, d, tail, row, nbk, nb, tid, nth);
+            else if (fits(2)) stage_quant32<T, NATURAL, 2>(codes, d, tail, row, nbk, nb, tid, nth);
             else stage_quant32<T, NATURAL, 1>(codes, d, tail, row, nbk, nb, tid, nth);
         } else {
             if (nbk * 32 <= nth) stage_quant256<T, NATURAL, 32>(codes, d, tail, row, nbk, nb, tid, nth);

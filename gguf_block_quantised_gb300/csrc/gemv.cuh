@@ -251,8 +251,12 @@ __global__ void __launch_bounds__(kGemvThreads, two_ctas_per_sm<T, A8, NV>() ? 2
     __syncthreads();
     pdl_trigger();
     const bool producer = warp == kConsumerWarps;
-    // Weights first: they do not depend on the grids before this one.
+    const size_t xrow = (A8 && !p.quant_x) ? (size_t)p.nb * (F::BS == 32 ? 34 : 292) : (size_t)p.cols * 4;
+    // The activation rows into L2 first, then the weights: neither waits for
+    // the grids before this one (the activations are read after the wait).
+    // Otherwise the activation loads queue behind the stage ring's copies.
     if (producer) {
+        prefetch_l2_lines(p.x, (size_t)p.nv * xrow, lane);
         int64_t tile = blockIdx.x;
         int chunk = 0;
         for (int it = 0; it < S && it < n_items; ++it) {
@@ -262,7 +266,6 @@ __global__ void __launch_bounds__(kGemvThreads, two_ctas_per_sm<T, A8, NV>() ? 2
     }
     pdl_wait();
     {
-        const size_t xrow = (A8 && !p.quant_x) ? (size_t)p.nb * (F::BS == 32 ? 34 : 292) : (size_t)p.cols * 4;
         stage_xhat<T>(xs, A8, p.quant_x != 0, p.x, xrow, nullptr, p.nv, p.cols, tid, kGemvThreads);
         __syncthreads();
         if (!A8) {
