@@ -1,6 +1,6 @@
 """Python face of the CPU oracle (test infrastructure only).
 
-The oracle is plain C in this directory (fp.c, blocks.c, quant.c, mm.c),
+The oracle is plain C in this directory (fp.c, blocks.c, quant.c, wquant.c, mm.c),
 compiled with gcc into ``oracle/_build/liboracle.so`` and loaded through
 ctypes.  Only the test-suite, ``__graft_entry__.smoke()`` and the CPU-baseline
 leg of ``bench.py`` may import this module; the CUDA library never does, and
@@ -21,7 +21,7 @@ import numpy as np
 HERE = os.path.dirname(os.path.abspath(__file__))
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "liboracle.so")
-SOURCES = ["fp.c", "blocks.c", "quant.c", "mm.c"]
+SOURCES = ["fp.c", "blocks.c", "quant.c", "wquant.c", "mm.c"]
 
 # The oracle's own type numbers (oracle.h).
 Q4_0, Q5_0, Q8_0, Q4_K, Q6_K, MXFP4, Q8_K, F32, BF16 = 1, 2, 3, 4, 5, 6, 7, 8, 9
@@ -70,11 +70,12 @@ def lib():
             L.orc_f32_to_bf16_rn.restype = C.c_uint16
             L.orc_dequant.argtypes = [I, P, I64, I64, P]
             L.orc_quantize_act.argtypes = [I, P, I64, P]
+            L.orc_quantize_weights.argtypes = [I, P, I64, P]
             L.orc_block_dots.argtypes = [I, P, I64, I64, P, I64, P]
             L.orc_matvec.argtypes = [I, I, P, I64, I64, P, I64, P, I64, P, P]
             L.orc_moe.argtypes = [I, I, P, I64, I64, I64, P, P, I64, P, I64, P, P, P]
             L.orc_decode_block.argtypes = [I, P, P]
-            for f in ("orc_dequant", "orc_quantize_act", "orc_block_dots", "orc_matvec",
+            for f in ("orc_dequant", "orc_quantize_act", "orc_quantize_weights", "orc_block_dots", "orc_matvec",
                       "orc_moe", "orc_decode_block"):
                 getattr(L, f).restype = I
             _lib = L
@@ -144,6 +145,14 @@ def quantize_act(atype: int, x: np.ndarray) -> np.ndarray:
     cols = x.shape[-1]
     out = np.empty(x.shape[:-1] + (cols // bs * bb,), dtype=np.uint8)
     _check(lib().orc_quantize_act(atype, _ptr(x), x.size, _ptr(out)), "quantize_act")
+    return out
+
+
+def quantize_weights(wt: int, w: np.ndarray) -> np.ndarray:
+    """w float32 [rows, cols] (cols % 32 == 0) -> Q4_0 / Q5_0 / Q8_0 blocks, uint8 [rows * row_bytes]."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    out = np.empty(w.size // 32 * BLOCK_BYTES[wt], dtype=np.uint8)
+    _check(lib().orc_quantize_weights(wt, _ptr(w), w.size, _ptr(out)), "quantize_weights")
     return out
 
 
