@@ -12,10 +12,10 @@
  *   Q4_0: m = the value of largest magnitude in the block, with its sign
  *         (the first such element when several tie);
  *         d = m / -8, id = (d == 0 ? 0 : 1 / d),
- *         q_i = min(15, trunc(x_i * id + 8.5));  w = d * (q - 8).
+ *         q_i = trunc(clamp(x_i * id + 8.5, 0, 15));  w = d * (q - 8).
  *         The largest-magnitude element lands on code 0 (w = -8 d = m); the
  *         grid reaches +7 d on the other side, where values clamp.
- *   Q5_0: the same with d = m / -16 and q_i = min(31, trunc(x_i * id + 16.5)).
+ *   Q5_0: the same with d = m / -16 and q_i = trunc(clamp(x_i * id + 16.5, 0, 31)).
  *
  * Every step is one fp32 IEEE operation (this file is built without FMA
  * contraction), so the integer codes are decided in fp32 as a kernel doing
@@ -54,10 +54,11 @@ static float block_codes(const float* x, int bits, uint8_t* q)
     for (int i = 0; i < 32; i++) {
         float v = x[i] * id;
         v = v + (half + 0.5f);
-        int c = (int)v;                             /* truncation; v >= 0 here */
-        if (c > top) c = top;
-        if (c < 0) c = 0;
-        q[i] = (uint8_t)c;
+        /* Clamp in fp32 before truncating, so that every value has a defined
+         * code: fminf/fmaxf return the non-NaN operand, and a subnormal block
+         * extreme can make 1 / d overflow. */
+        v = fmaxf(fminf(v, (float)top), 0.0f);
+        q[i] = (uint8_t)(int)v;                     /* truncation */
     }
     return d;
 }
