@@ -12,6 +12,7 @@
  *     d    = amax / 127                     (fp32, one rounding)
  *     id   = d == 0 ? 0 : 1 / d             (fp32, one rounding)
  *     q_i  = round half away from zero (x_i * id), clamped to [-127, 127]
+ *            (a NaN product clamps to -127)
  *   Q8_0 stores fp16(d) (round to nearest even) and q[32]    -> 34 bytes;
  *   Q8_K stores the fp32 d, q[256] and int16 bsums[16], the sums of q over
  *   each run of 16                                           -> 292 bytes.
@@ -34,8 +35,10 @@ static void quantize_block(const float* x, int bs, float* d_out, int8_t* q)
     for (int i = 0; i < bs; i++) {
         float v = x[i] * id;
         float r = roundf(v);                    /* halves away from zero */
-        if (r > 127.0f) r = 127.0f;
-        if (r < -127.0f) r = -127.0f;
+        /* Clamp with IEEE maxNum/minNum (the non-NaN operand), so that every
+         * value has a defined code: when amax / 127 is subnormal, 1 / d
+         * overflows and 0 * id is NaN (the block's fp16 scale is 0 then). */
+        r = fminf(fmaxf(r, -127.0f), 127.0f);
         q[i] = (int8_t)r;
     }
     *d_out = d;
