@@ -583,6 +583,39 @@ def dist_env():
     return ws, rank, local
 
 
+def wquant_leg(q, torch, stream, hbm):
+    """The weight quantiser (qmv_quantize_weights): a 14336x4096 fp32 matrix
+    (235 MB, two copies alternating so each launch reads from HBM) to Q4_0,
+    Q5_0 and Q8_0.  Bytes = the fp32 read plus the blocks written."""
+    rows, cols = 14336, 4096
+    n = rows * cols
+    g = torch.Generator(device="cuda").manual_seed(7)
+    src = [torch.randn(rows, cols, device="cuda", generator=g) * 0.02 for _ in range(2)]
+    res = {}
+    for t, name in ((Q4_0, "Q4_0"), (Q5_0, "Q5_0"), (Q8_0, "Q8_0")):
+        out = torch.empty(rows * q.qmv_row_bytes(t, cols), dtype=torch.uint8, device="cuda")
+        nbytes = 4 * n + out.numel()
+        with torch.cuda.stream(stream):
+            for i in range(4):
+                q.qmv_quantize_weights(t, src[i % 2], rows, cols, out, stream.cuda_stream)
+            reps = 20
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(reps):
+                q.qmv_quantize_weights(t, src[i % 2], rows, cols, out, stream.cuda_stream)
+            e1.record(stream)
+        e1.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        gbs = nbytes / (ms / 1e3) / 1e9
+        res[name] = {"us": 1e3 * ms, "gbs": gbs, "frac_of_hbm": gbs / hbm, "bytes": nbytes}
+    q.qmv_get_status(stream)
+    del src
+    torch.cuda.empty_cache()
+    return {"metric": "weight quantiser GB/s (fp32 read + blocks written)", "unit": "GB/s",
+            "shape": f"{rows}x{cols} fp32", "by_type": res,
+            "kernel": "k_quant_w (Q4_0, Q5_0: eight threads per block); Q8_0 runs the activation quantiser"}
+
+
 def _oracle_step_workload():
     """The decode step's matrices and activations for the oracle (single thread)."""
     mats, tid = [], 0
@@ -718,6 +751,7 @@ def main():
     kquant = None if args.no_extra else kquant_decode_leg(q, torch, stream, hbm)
     prefill = None if args.no_extra else prefill_leg(q, torch, stream, tflops_peak)
     moe = None if args.no_extra else moe_leg(q, torch, stream, hbm)
+    wquant = None if args.no_extra else wquant_leg(q, torch, stream, hbm)
     value = ws * STEP_WEIGHT_BYTES / (ms1 / 1e3) / 1e9
     if rank != 0:
         if ws > 1:
@@ -770,6 +804,7 @@ def main():
         "kquant_decode": kquant,
         "prefill": prefill,
         "moe": moe,
+        "weight_quantiser": wquant,
     }
     print(json.dumps(line))
     if ws > 1:

@@ -51,6 +51,7 @@ _SIGS = {
     "qmv_block_bytes": (_SZ, [_I]),
     "qmv_row_bytes": (_SZ, [_I, _I64]),
     "qmv_quantize_act": (_I, [_I, _P, _P, _I64, _P]),
+    "qmv_quantize_weights": (_I, [_I, _P, _I64, _I64, _P, _P]),
     "qmv_repack": (_I, [_I, _P, _I64, _I64, _P, _P]),
     "qmv_dequantize": (_I, [_I, _P, _I64, _I64, _P, _P]),
     "qmv_block_dots": (_I, [_I, _P, _I64, _I64, _P, _I, _P, _P]),
@@ -134,6 +135,10 @@ def qmv_row_bytes(t: int, cols: int) -> int:
 
 def qmv_quantize_act(fmt, x, xq, n, stream=None):
     return _call("qmv_quantize_act", fmt, _ptr(x), _ptr(xq), n, _stream(stream))
+
+
+def qmv_quantize_weights(t, W, rows, cols, out, stream=None):
+    return _call("qmv_quantize_weights", t, _ptr(W), rows, cols, _ptr(out), _stream(stream))
 
 
 def qmv_repack(t, W, rows, cols, Wout, stream=None):

@@ -22,6 +22,7 @@
 // Launchers defined in the kernel translation units.
 int qmv_launch_quantize(int atype, const float* x, void* xq, int64_t n, bool pdl, cudaStream_t st);
 int qmv_launch_dequant(int t, const void* W, int64_t rows, int64_t cols, float* out, cudaStream_t st);
+int qmv_launch_quantize_weights(int wtype, const float* W, int64_t n, void* out, cudaStream_t st);
 int qmv_launch_block_dots(int t, const void* W, int64_t rows, int64_t cols, const void* xq, int n_vec,
                           int32_t* out, cudaStream_t st);
 #define QMV_GEMV_DECL(NAME) \
@@ -289,6 +290,29 @@ int qmv_quantize_act(int fmt, const float* x, void* xq, int64_t n, void* stream)
     if (!aligned(x, fmt == QMV_Q8_K ? 16 : 4)) return fail(QMV_ERR_ALIGN, "x must be %d-byte aligned", fmt == QMV_Q8_K ? 16 : 4);
     if (!aligned(xq, fmt == QMV_Q8_K ? 4 : 2)) return fail(QMV_ERR_ALIGN, "xq must be %d-byte aligned", fmt == QMV_Q8_K ? 4 : 2);
     if (qmv_launch_quantize(fmt, x, xq, n, pdl, static_cast<cudaStream_t>(stream))) return cuda_fail("qmv_quantize_act");
+    return ok();
+}
+
+int qmv_quantize_weights(int type, const float* W, int64_t rows, int64_t cols, void* out, void* stream)
+{
+    if (type != QMV_Q4_0 && type != QMV_Q5_0 && type != QMV_Q8_0)
+        return fail(QMV_ERR_UNSUPPORTED,
+                    "qmv_quantize_weights writes Q4_0, Q5_0 and Q8_0 (got %s); the K-quants' scale search is not "
+                    "part of this library", type_name(type));
+    if (rows < 0 || cols <= 0) return fail(QMV_ERR_INVALID_ARG, "rows must be >= 0 and cols > 0 (got %lld x %lld)",
+                                           (long long)rows, (long long)cols);
+    if (cols % 32) return fail(QMV_ERR_SHAPE, "%s rows hold 32-element blocks; cols = %lld is not a multiple of 32",
+                               type_name(type), (long long)cols);
+    if (rows == 0) return ok();
+    if (rows > ((int64_t)1 << 40) / cols) return fail(QMV_ERR_SHAPE, "rows * cols must be below 2^40");
+    if (!W || !out) return fail(QMV_ERR_INVALID_ARG, "W and out must not be NULL");
+    if (!aligned(W, 16)) return fail(QMV_ERR_ALIGN, "W must be 16-byte aligned");
+    if (!aligned(out, 2)) return fail(QMV_ERR_ALIGN, "out must be 2-byte aligned");
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(W), a1 = a0 + (uintptr_t)(rows * cols) * 4;
+    const uintptr_t b0 = reinterpret_cast<uintptr_t>(out), b1 = b0 + (uintptr_t)rows * qmv_row_bytes(type, cols);
+    if (a0 < b1 && b0 < a1) return fail(QMV_ERR_INVALID_ARG, "qmv_quantize_weights: out overlaps W");
+    if (qmv_launch_quantize_weights(type, W, rows * cols, out, static_cast<cudaStream_t>(stream)))
+        return cuda_fail("qmv_quantize_weights");
     return ok();
 }
 

@@ -129,6 +129,25 @@ size_t qmv_row_bytes(int type, int64_t cols);
 int qmv_quantize_act(int fmt, const float* x, void* xq, int64_t n, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * qmv_quantize_weights -- fp32 weights to Q4_0, Q5_0 or Q8_0 blocks, the
+ * formats the pages' quantiser writes ("Models and formats", "Tensor
+ * formats").  The pages do not print the procedure; this is the reading that
+ * keeps the files those of the GGUF ecosystem:
+ *   Q4_0 / Q5_0: per 32 weights, m = the signed value of largest magnitude
+ *     (the first on ties), d = m / -8 (Q4_0) or m / -16 (Q5_0), and each code
+ *     is trunc(clamp(w / d + 8.5, 0, 15)) (Q5_0: + 16.5, 0, 31), every step one
+ *     fp32 IEEE rounding; fp16(d) is stored.  The largest-magnitude weight
+ *     decodes exactly to -8 fp16(d) (-16 for Q5_0).
+ *   Q8_0: the symmetric 8-bit form, byte for byte qmv_quantize_act(QMV_Q8_0).
+ *   W   : fp32 [rows][cols], 16-byte aligned; cols a multiple of 32.
+ *   out : rows * qmv_row_bytes(type, cols) bytes, 2-byte aligned, not
+ *         overlapping W.
+ * Returns QMV_ERR_UNSUPPORTED for other types (the K-quants' scale search is
+ * not part of this library), QMV_ERR_SHAPE, QMV_ERR_ALIGN, QMV_ERR_INVALID_ARG.
+ * ------------------------------------------------------------------------- */
+int qmv_quantize_weights(int type, const float* W, int64_t rows, int64_t cols, void* out, void* stream);
+
+/* ---------------------------------------------------------------------------
  * qmv_repack -- weights to a layout for the tensor-core kernels, once at load
  * time (the "Architecture" page's bench transcript runs its engine with
  * "repack on").  The GGUF layout stays the canonical input; the repacked copy

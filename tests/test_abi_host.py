@@ -73,6 +73,14 @@ def test_refusals(lib):
     assert rc(lib, "qmv_quantize_act", q.Q8_K, 4096, 4096, 32, None) == q.ERR_SHAPE
     assert rc(lib, "qmv_quantize_act", q.Q8_0, 4096, 4096, 0, None) == q.OK
     assert rc(lib, "qmv_quantize_act", q.Q8_0, None, 4096, 32, None) == q.ERR_INVALID_ARG
+    # weight quantiser
+    assert rc(lib, "qmv_quantize_weights", q.Q4_K, 4096, 2, 256, 8192, None) == q.ERR_UNSUPPORTED
+    assert "Q4_0" in q.qmv_last_error()
+    assert rc(lib, "qmv_quantize_weights", q.Q4_0, 4096, 2, 48, 8192, None) == q.ERR_SHAPE
+    assert rc(lib, "qmv_quantize_weights", q.Q5_0, 4100, 2, 64, 8192, None) == q.ERR_ALIGN
+    assert rc(lib, "qmv_quantize_weights", q.Q8_0, 4096, 2, 64, 8193, None) == q.ERR_ALIGN
+    assert rc(lib, "qmv_quantize_weights", q.Q4_0, 4096, 2, 64, 4160, None) == q.ERR_INVALID_ARG   # overlaps W
+    assert rc(lib, "qmv_quantize_weights", q.Q4_0, None, 0, 64, None, None) == q.OK
     # verification calls
     assert rc(lib, "qmv_dequantize", q.Q6_K, 4096, 2, 200, 4096, None) == q.ERR_SHAPE
     assert rc(lib, "qmv_block_dots", q.Q8_0, 4096, 2, 64, 4096, -1, 4096, None) == q.ERR_INVALID_ARG
