@@ -644,6 +644,46 @@ def _oracle_step_sample(O, mats, xs, frac):
     return time.perf_counter() - t0, nbytes
 
 
+_MC = None
+
+
+def _mc_init():
+    """Process-pool worker set-up: the oracle and the step's workload, once."""
+    global _MC
+    from oracle import oracle as O
+    _MC = (O,) + _oracle_step_workload()
+
+
+def _mc_task(args):
+    """One worker's share of a decode step: rows [w/W, (w+1)/W) of every matrix."""
+    w, nw = args
+    O, mats, xs = _MC
+    xq = [O.quantize_act(O.Q8_0, a) for a in xs]
+    for W, rows, cols, xi, t in mats:
+        r0, r1 = rows * w // nw, rows * (w + 1) // nw
+        if r1 > r0:
+            rb = row_bytes(t, cols)
+            O.matvec(t, O.Q8_0, W[r0 * rb:r1 * rb], r1 - r0, cols, xq[xi], 1, want_abs=False)
+    return w
+
+
+def cpu_baseline_all_cores(n_steps=8):
+    """The oracle on every host core: a pool of processes (spawned, never forked
+    from a process that has used the GPU), each owning a static share of the
+    rows of every matrix of the step; a step ends when every share is done."""
+    import multiprocessing as mp
+    nw = os.cpu_count() or 1
+    with mp.get_context("spawn").Pool(nw, initializer=_mc_init) as pool:
+        pool.map(_mc_task, [(w, nw) for w in range(nw)], chunksize=1)   # set-up and a warm step
+        t0 = time.perf_counter()
+        for _ in range(n_steps):
+            pool.map(_mc_task, [(w, nw) for w in range(nw)], chunksize=1)
+        dt = time.perf_counter() - t0
+    return {"value": STEP_WEIGHT_BYTES * n_steps / dt / 1e9, "unit": "GB/s", "cores": nw, "kind": "oracle",
+            "sample": f"{n_steps} full decode steps (batch 1, W4A8), the rows of every matrix split statically "
+                      f"over {nw} processes, {dt:.1f} s"}
+
+
 def run_reference(args):
     """The oracle on the bench's workload, on the host cores: each step a sampled
     decode step (the same row fraction of every matrix), the fraction sized so
@@ -758,6 +798,7 @@ def main():
             torch.distributed.barrier()
         return 0
     cpu = None if args.no_cpu_baseline else cpu_baseline(4)
+    cpu_all = None if args.no_cpu_baseline else cpu_baseline_all_cores()
     launches_per_step = step1.launches
     line = {
         "metric": "quant GEMV weight GB/s (decode step, W4A8)",
@@ -801,6 +842,7 @@ def main():
                        "step, all in one replayed CUDA graph on the caller's stream"},
         "gpu_launches": launches_per_step * args.steps,
         "cpu_baseline": cpu,
+        "cpu_baseline_all_cores": cpu_all,
         "kquant_decode": kquant,
         "prefill": prefill,
         "moe": moe,
