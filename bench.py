@@ -673,11 +673,13 @@ def cpu_baseline_all_cores(n_steps=8):
     rows of every matrix of the step; a step ends when every share is done."""
     import multiprocessing as mp
     nw = os.cpu_count() or 1
+    tasks = [(w, nw) for w in range(nw)]
+    # map_async with a time limit: a worker that dies would leave a plain map waiting forever
     with mp.get_context("spawn").Pool(nw, initializer=_mc_init) as pool:
-        pool.map(_mc_task, [(w, nw) for w in range(nw)], chunksize=1)   # set-up and a warm step
+        pool.map_async(_mc_task, tasks, chunksize=1).get(timeout=300)   # set-up and a warm step
         t0 = time.perf_counter()
         for _ in range(n_steps):
-            pool.map(_mc_task, [(w, nw) for w in range(nw)], chunksize=1)
+            pool.map_async(_mc_task, tasks, chunksize=1).get(timeout=120)
         dt = time.perf_counter() - t0
     return {"value": STEP_WEIGHT_BYTES * n_steps / dt / 1e9, "unit": "GB/s", "cores": nw, "kind": "oracle",
             "sample": f"{n_steps} full decode steps (batch 1, W4A8), the rows of every matrix split statically "
