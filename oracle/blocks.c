@@ -13,6 +13,10 @@
  *   Q5_0  (22 B / 32 w): fp16 d | u32 high-bit mask | 16 bytes of nibbles.
  *         Nibbles as Q4_0; bit i of the mask is bit 4 of element i.  w = d*(q-16).
  *   Q8_0  (34 B / 32 w): fp16 d | 32 int8.  w = d*q.
+ *   Q4_1  (20 B / 32 w): fp16 d | fp16 m | 16 bytes of nibbles, order as Q4_0.
+ *         w = d*q + m (carried below as dmin = -m with sub_min = 1).
+ *   Q5_1  (24 B / 32 w): fp16 d | fp16 m | u32 high-bit mask | 16 bytes of
+ *         nibbles, bits and order as Q5_0.  w = d*q + m.
  *   MXFP4 (17 B / 32 w): u8 E8M0 exponent e | 16 bytes of E2M1 codes, nibble
  *         order as Q4_0.  w = 2^(e-127) * E2M1(code); e = 255 is NaN (OCP MX).
  *   Q4_K  (144 B / 256 w): fp16 d | fp16 dmin | 12 bytes of packed 6-bit
@@ -37,7 +41,7 @@ static uint32_t rd_u32(const uint8_t* p)
 int64_t orc_block_elems(int type)
 {
     switch (type) {
-    case ORC_Q4_0: case ORC_Q5_0: case ORC_Q8_0: case ORC_MXFP4: return 32;
+    case ORC_Q4_0: case ORC_Q5_0: case ORC_Q8_0: case ORC_MXFP4: case ORC_Q4_1: case ORC_Q5_1: return 32;
     case ORC_Q4_K: case ORC_Q6_K: case ORC_Q8_K: return 256;
     default: return 0;
     }
@@ -49,6 +53,8 @@ int64_t orc_block_bytes(int type)
     case ORC_Q4_0: return 18;
     case ORC_Q5_0: return 22;
     case ORC_Q8_0: return 34;
+    case ORC_Q4_1: return 20;
+    case ORC_Q5_1: return 24;
     case ORC_MXFP4: return 17;
     case ORC_Q4_K: return 144;
     case ORC_Q6_K: return 210;
@@ -123,6 +129,21 @@ int orc_decode_block(int type, const uint8_t* b, orc_block* out)
         for (int i = 0; i < 32; i++) {
             out->code[i] = (int8_t)b[2 + i];
             out->sub_scale[i] = 1;
+        }
+        return ORC_OK;
+    }
+    case ORC_Q4_1:
+    case ORC_Q5_1: {
+        /* w = d*q + m with the unsigned 4- or 5-bit code q */
+        out->n = 32;
+        out->d = orc_f16_to_f64((uint16_t)rd_u16(b));
+        out->dmin = -orc_f16_to_f64((uint16_t)rd_u16(b + 2));
+        const uint32_t qh = type == ORC_Q5_1 ? rd_u32(b + 4) : 0u;
+        const uint8_t* qs = b + (type == ORC_Q5_1 ? 8 : 4);
+        for (int i = 0; i < 32; i++) {
+            out->code[i] = nibble32(qs, i) | (int)(((qh >> i) & 1u) << 4);
+            out->sub_scale[i] = 1;
+            out->sub_min[i] = 1;
         }
         return ORC_OK;
     }

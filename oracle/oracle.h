@@ -33,7 +33,8 @@
 /* Type numbers (the oracle's own table). */
 enum {
     ORC_Q4_0 = 1, ORC_Q5_0 = 2, ORC_Q8_0 = 3, ORC_Q4_K = 4, ORC_Q6_K = 5,
-    ORC_MXFP4 = 6, ORC_Q8_K = 7, ORC_F32 = 8, ORC_BF16 = 9
+    ORC_MXFP4 = 6, ORC_Q8_K = 7, ORC_F32 = 8, ORC_BF16 = 9,
+    ORC_Q4_1 = 10, ORC_Q5_1 = 11
 };
 
 /* Return codes. */
@@ -49,8 +50,8 @@ uint16_t orc_f32_to_bf16_rn(float f);
 /* A decoded block.  Every element i satisfies
  *     w_i = d * sub_scale[i] * code[i] - dmin * sub_min[i]
  * exactly (in real arithmetic).  For the 32-element formats sub_scale = 1 and
- * sub_min = 0; Q4_K carries its 6-bit sub-block scale/min, Q6_K its int8
- * sub-block scale.  MXFP4 stores twice the E2M1 value (an integer) in code[]
+ * sub_min = 0 (Q4_1 and Q5_1: sub_min = 1 and dmin = -m, their offset);
+ * Q4_K carries its 6-bit sub-block scale/min, Q6_K its int8 sub-block scale.  MXFP4 stores twice the E2M1 value (an integer) in code[]
  * and 2^(e-128) in d. */
 typedef struct {
     int     n;              /* elements in the block: 32 or 256 */
@@ -67,7 +68,8 @@ int     orc_decode_block(int type, const uint8_t* blk, orc_block* out);
 /* Decoded weight of element i as an exact fp64 value. */
 double  orc_block_weight(const orc_block* b, int i);
 /* rows x cols weights -> fp32.  Every format's weight is exactly representable
- * in fp32 except Q4_K's, which is the single rounding RN_fp32(d*sc*q - dmin*m). */
+ * in fp32 except Q4_K's, which is the single rounding RN_fp32(d*sc*q - dmin*m),
+ * and Q4_1's and Q5_1's, the single rounding RN_fp32(d*q + m). */
 int     orc_dequant(int type, const uint8_t* W, int64_t rows, int64_t cols, float* out);
 
 /* ---- quant.c : the 8-bit activation quantisers ---- */

@@ -195,3 +195,22 @@ def read_golden(path):
         elif key == "expect":
             cur["expect"] = expand(rest.split(), float)
     return [(r["name"], r["type"], r["bytes"], r["expect"]) for r in recs]
+
+
+# ---- Q4_1 / Q5_1: w = d*q + m (unsigned codes, a per-block offset) ----------------
+
+def pack_q4_1(d, m, q):
+    return f16_bytes(d) + f16_bytes(m) + _nib_pack(q)
+
+
+def pack_q5_1(d, m, q):
+    q = np.asarray(q)
+    mask = 0
+    for i in range(32):
+        mask |= ((int(q[i]) >> 4) & 1) << i
+    return f16_bytes(d) + f16_bytes(m) + int(mask).to_bytes(4, "little") + _nib_pack(q & 15)
+
+
+def closed_q_1(d, m, q):
+    return [f16_val(d) * int(x) + f16_val(m) for x in q]
+
