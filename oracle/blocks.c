@@ -24,6 +24,10 @@
  *         Sub-block j holds elements 32j..32j+31; 32-byte chunk c of the
  *         nibbles holds sub-block 2c in its low nibbles and 2c+1 in its high
  *         nibbles.  w = d*sc_j*q - dmin*m_j.
+ *   Q5_K  (176 B / 256 w): fp16 d | fp16 dmin | the 12 scale/min bytes of Q4_K |
+ *         32 B of fifth bits | 128 bytes of nibbles laid out as in Q4_K.  The
+ *         fifth bit of element 32j+l (sub-block j) is bit j of byte l of the
+ *         fifth-bit field.  w = d*sc_j*q - dmin*m_j with 5-bit q.
  *   Q6_K  (210 B / 256 w): 128 B low nibbles | 64 B high 2-bit pairs |
  *         int8 scales[16] | fp16 d.  Element i uses scales[i/16].
  *         w = d*sc*(q-32).
@@ -42,7 +46,7 @@ int64_t orc_block_elems(int type)
 {
     switch (type) {
     case ORC_Q4_0: case ORC_Q5_0: case ORC_Q8_0: case ORC_MXFP4: case ORC_Q4_1: case ORC_Q5_1: return 32;
-    case ORC_Q4_K: case ORC_Q6_K: case ORC_Q8_K: return 256;
+    case ORC_Q4_K: case ORC_Q5_K: case ORC_Q6_K: case ORC_Q8_K: return 256;
     default: return 0;
     }
 }
@@ -57,6 +61,7 @@ int64_t orc_block_bytes(int type)
     case ORC_Q5_1: return 24;
     case ORC_MXFP4: return 17;
     case ORC_Q4_K: return 144;
+    case ORC_Q5_K: return 176;
     case ORC_Q6_K: return 210;
     case ORC_Q8_K: return 292;
     default: return 0;
@@ -170,6 +175,27 @@ int orc_decode_block(int type, const uint8_t* b, orc_block* out)
             const uint8_t* chunk = qs + 32 * (j / 2);
             for (int l = 0; l < 32; l++) {
                 int q = (j % 2 == 0) ? (chunk[l] & 0x0f) : (chunk[l] >> 4);
+                out->code[32 * j + l] = q;
+                out->sub_scale[32 * j + l] = sc;
+                out->sub_min[32 * j + l] = m;
+            }
+        }
+        return ORC_OK;
+    }
+    case ORC_Q5_K: {
+        out->n = 256;
+        out->d = orc_f16_to_f64((uint16_t)rd_u16(b));
+        out->dmin = orc_f16_to_f64((uint16_t)rd_u16(b + 2));
+        const uint8_t* scf = b + 4;
+        const uint8_t* qh = b + 16;
+        const uint8_t* qs = b + 48;
+        for (int j = 0; j < 8; j++) {
+            int sc, m;
+            q4k_scale_min(scf, j, &sc, &m);
+            const uint8_t* chunk = qs + 32 * (j / 2);
+            for (int l = 0; l < 32; l++) {
+                int q = (j % 2 == 0) ? (chunk[l] & 0x0f) : (chunk[l] >> 4);
+                q |= ((qh[l] >> j) & 1) << 4;
                 out->code[32 * j + l] = q;
                 out->sub_scale[32 * j + l] = sc;
                 out->sub_min[32 * j + l] = m;

@@ -214,3 +214,19 @@ def pack_q5_1(d, m, q):
 def closed_q_1(d, m, q):
     return [f16_val(d) * int(x) + f16_val(m) for x in q]
 
+
+# ---- Q5_K: Q4_K's fields plus a 32-byte field of fifth bits ---------------------
+
+def pack_q5_k(d, dmin, sc, m, q):
+    """Element 32j+l (sub-block j): low 4 bits as in Q4_K, bit 4 in bit j of byte l."""
+    q = np.asarray(q)
+    qh = bytearray(32)
+    qs = bytearray(128)
+    for j in range(8):
+        for l in range(32):
+            qh[l] |= ((int(q[32 * j + l]) >> 4) & 1) << j
+    for c in range(4):
+        for l in range(32):
+            qs[32 * c + l] = (int(q[64 * c + l]) & 15) | ((int(q[64 * c + 32 + l]) & 15) << 4)
+    return f16_bytes(d) + f16_bytes(dmin) + pack_q4_k_scales(sc, m) + bytes(qh) + bytes(qs)
+
