@@ -28,6 +28,16 @@
  *         32 B of fifth bits | 128 bytes of nibbles laid out as in Q4_K.  The
  *         fifth bit of element 32j+l (sub-block j) is bit j of byte l of the
  *         fifth-bit field.  w = d*sc_j*q - dmin*m_j with 5-bit q.
+ *   Q2_K  (84 B / 256 w): 16 scale bytes (low nibble sc, high nibble m) |
+ *         64 B of 2-bit codes | fp16 d | fp16 dmin.  Element 128n+32j+l
+ *         (n < 2, j < 4, l < 32) is bits 2j..2j+1 of code byte 32n+l and uses
+ *         scale byte 8n+2j+(l >= 16).  w = d*sc*q - dmin*m.
+ *   Q3_K  (110 B / 256 w): 32 B high-bit mask | 64 B of 2-bit codes | 12 bytes
+ *         of sixteen 6-bit scales | fp16 d.  Element 128n+32j+l takes its low
+ *         bits as in Q2_K and bit 4n+j of mask byte l; its code is the low
+ *         bits minus 4 when that bit is clear.  Scale s (0..15): low 4 bits
+ *         from byte s (s < 8, low nibble) or byte s-8 (high nibble), high 2
+ *         bits from bits 2*(s/4) of byte 8 + s%4.  w = d*(s6 - 32)*code.
  *   Q6_K  (210 B / 256 w): 128 B low nibbles | 64 B high 2-bit pairs |
  *         int8 scales[16] | fp16 d.  Element i uses scales[i/16].
  *         w = d*sc*(q-32).
@@ -46,7 +56,7 @@ int64_t orc_block_elems(int type)
 {
     switch (type) {
     case ORC_Q4_0: case ORC_Q5_0: case ORC_Q8_0: case ORC_MXFP4: case ORC_Q4_1: case ORC_Q5_1: return 32;
-    case ORC_Q4_K: case ORC_Q5_K: case ORC_Q6_K: case ORC_Q8_K: return 256;
+    case ORC_Q4_K: case ORC_Q5_K: case ORC_Q6_K: case ORC_Q8_K: case ORC_Q2_K: case ORC_Q3_K: return 256;
     default: return 0;
     }
 }
@@ -62,6 +72,8 @@ int64_t orc_block_bytes(int type)
     case ORC_MXFP4: return 17;
     case ORC_Q4_K: return 144;
     case ORC_Q5_K: return 176;
+    case ORC_Q2_K: return 84;
+    case ORC_Q3_K: return 110;
     case ORC_Q6_K: return 210;
     case ORC_Q8_K: return 292;
     default: return 0;
@@ -180,6 +192,46 @@ int orc_decode_block(int type, const uint8_t* b, orc_block* out)
                 out->sub_min[32 * j + l] = m;
             }
         }
+        return ORC_OK;
+    }
+    case ORC_Q2_K: {
+        out->n = 256;
+        const uint8_t* sc = b;
+        const uint8_t* qs = b + 16;
+        out->d = orc_f16_to_f64((uint16_t)rd_u16(b + 80));
+        out->dmin = orc_f16_to_f64((uint16_t)rd_u16(b + 82));
+        for (int n = 0; n < 2; n++)
+            for (int j = 0; j < 4; j++)
+                for (int l = 0; l < 32; l++) {
+                    const int e = 128 * n + 32 * j + l;
+                    const int s = sc[8 * n + 2 * j + (l >= 16)];
+                    out->code[e] = (qs[32 * n + l] >> (2 * j)) & 3;
+                    out->sub_scale[e] = s & 15;
+                    out->sub_min[e] = s >> 4;
+                }
+        return ORC_OK;
+    }
+    case ORC_Q3_K: {
+        out->n = 256;
+        const uint8_t* hm = b;
+        const uint8_t* qs = b + 32;
+        const uint8_t* sf = b + 96;
+        out->d = orc_f16_to_f64((uint16_t)rd_u16(b + 108));
+        int s6[16];
+        for (int s = 0; s < 16; s++) {
+            const int lo = s < 8 ? (sf[s] & 15) : (sf[s - 8] >> 4);
+            const int hi = (sf[8 + s % 4] >> (2 * (s / 4))) & 3;
+            s6[s] = lo | (hi << 4);
+        }
+        for (int n = 0; n < 2; n++)
+            for (int j = 0; j < 4; j++)
+                for (int l = 0; l < 32; l++) {
+                    const int e = 128 * n + 32 * j + l;
+                    const int q = (qs[32 * n + l] >> (2 * j)) & 3;
+                    const int h = (hm[l] >> (4 * n + j)) & 1;
+                    out->code[e] = q - (h ? 0 : 4);
+                    out->sub_scale[e] = s6[8 * n + 2 * j + (l >= 16)] - 32;
+                }
         return ORC_OK;
     }
     case ORC_Q5_K: {

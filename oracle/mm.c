@@ -35,7 +35,7 @@
 static int weight_type_ok(int t)
 {
     return t == ORC_Q4_0 || t == ORC_Q5_0 || t == ORC_Q8_0 || t == ORC_MXFP4 || t == ORC_Q4_K || t == ORC_Q6_K ||
-           t == ORC_Q4_1 || t == ORC_Q5_1 || t == ORC_Q5_K;
+           t == ORC_Q4_1 || t == ORC_Q5_1 || t == ORC_Q5_K || t == ORC_Q2_K || t == ORC_Q3_K;
 }
 
 /* The 8-bit activation format that pairs with a weight format: the same block

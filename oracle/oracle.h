@@ -34,7 +34,7 @@
 enum {
     ORC_Q4_0 = 1, ORC_Q5_0 = 2, ORC_Q8_0 = 3, ORC_Q4_K = 4, ORC_Q6_K = 5,
     ORC_MXFP4 = 6, ORC_Q8_K = 7, ORC_F32 = 8, ORC_BF16 = 9,
-    ORC_Q4_1 = 10, ORC_Q5_1 = 11, ORC_Q5_K = 12
+    ORC_Q4_1 = 10, ORC_Q5_1 = 11, ORC_Q5_K = 12, ORC_Q2_K = 13, ORC_Q3_K = 14
 };
 
 /* Return codes. */
@@ -51,8 +51,8 @@ uint16_t orc_f32_to_bf16_rn(float f);
  *     w_i = d * sub_scale[i] * code[i] - dmin * sub_min[i]
  * exactly (in real arithmetic).  For the 32-element formats sub_scale = 1 and
  * sub_min = 0 (Q4_1 and Q5_1: sub_min = 1 and dmin = -m, their offset);
- * Q4_K and Q5_K carry their 6-bit sub-block scale/min, Q6_K its int8
- * sub-block scale.  MXFP4 stores twice the E2M1 value (an integer) in code[]
+ * Q4_K and Q5_K carry their 6-bit sub-block scale/min, Q2_K its 4-bit
+ * scale/min, Q3_K its 6-bit scale minus 32, Q6_K its int8 sub-block scale.  MXFP4 stores twice the E2M1 value (an integer) in code[]
  * and 2^(e-128) in d. */
 typedef struct {
     int     n;              /* elements in the block: 32 or 256 */

@@ -230,3 +230,55 @@ def pack_q5_k(d, dmin, sc, m, q):
             qs[32 * c + l] = (int(q[64 * c + l]) & 15) | ((int(q[64 * c + 32 + l]) & 15) << 4)
     return f16_bytes(d) + f16_bytes(dmin) + pack_q4_k_scales(sc, m) + bytes(qh) + bytes(qs)
 
+
+# ---- Q2_K and Q3_K: 2-bit codes in 128-element halves --------------------------
+
+def _k23_pos(e):
+    """Element e -> (code byte 32n+l, bit shift 2j, sub-block 8n+2j+(l>=16), l, n, j)."""
+    n, rem = divmod(e, 128)
+    j, l = divmod(rem, 32)
+    return 32 * n + l, 2 * j, 8 * n + 2 * j + (1 if l >= 16 else 0), l, n, j
+
+
+def pack_q2_k(d, dmin, sc, m, q):
+    """sc, m: sixteen 4-bit scales and mins; q: 256 codes 0..3."""
+    scales = bytes((int(sc[i]) & 15) | ((int(m[i]) & 15) << 4) for i in range(16))
+    qs = bytearray(64)
+    for e in range(256):
+        byte, shift, _, _, _, _ = _k23_pos(e)
+        qs[byte] |= (int(q[e]) & 3) << shift
+    return scales + bytes(qs) + f16_bytes(d) + f16_bytes(dmin)
+
+
+def closed_q2_k(d, dmin, sc, m, q):
+    out = []
+    for e in range(256):
+        s = _k23_pos(e)[2]
+        out.append(f16_val(d) * int(sc[s]) * int(q[e]) - f16_val(dmin) * int(m[s]))
+    return out
+
+
+def pack_q3_k(d, s6, code):
+    """s6: sixteen 6-bit scales (factor s6 - 32); code: 256 values in -4..3, kept
+    as low 2 bits plus a mask bit that is set for codes 0..3."""
+    hm = bytearray(32)
+    qs = bytearray(64)
+    for e in range(256):
+        byte, shift, _, l, n, j = _k23_pos(e)
+        c = int(code[e])
+        qs[byte] |= ((c + 4) & 3 if c < 0 else c) << shift
+        hm[l] |= (1 if c >= 0 else 0) << (4 * n + j)
+    sf = bytearray(12)
+    for s in range(16):
+        v = int(s6[s])
+        if s < 8:
+            sf[s] |= v & 15
+        else:
+            sf[s - 8] |= (v & 15) << 4
+        sf[8 + s % 4] |= ((v >> 4) & 3) << (2 * (s // 4))
+    return bytes(hm) + bytes(qs) + bytes(sf) + f16_bytes(d)
+
+
+def closed_q3_k(d, s6, code):
+    return [f16_val(d) * (int(s6[_k23_pos(e)[2]]) - 32) * int(code[e]) for e in range(256)]
+
