@@ -199,10 +199,16 @@ __device__ __forceinline__ void act_scale(float amax, float& d, float& id)
     d = __fdiv_rn(amax, 127.f);
     id = d == 0.f ? 0.f : __fdiv_rn(1.f, d);
 }
-// q = round-half-away-from-zero(v * id), clamped to +-127.
-__device__ __forceinline__ int8_t quant1(float v, float id)
+// q = round-half-away-from-zero(v / d), clamped to +-127, computed as v * id
+// while id = 1/d is finite.  A scale below 2^-128 (a block whose largest
+// magnitude is under 127 * 2^-128) makes 1/d overflow; the code is then the
+// quotient v / d itself, one IEEE division, so that v = 0 still gives 0 and
+// every code is the plain definition's.  The branch is the same for a whole
+// block.
+__device__ __forceinline__ int8_t quant1(float v, float d, float id)
 {
-    float r = roundf(__fmul_rn(v, id));
+    const float t = isinf(id) ? __fdiv_rn(v, d) : __fmul_rn(v, id);
+    float r = roundf(t);
     r = fminf(fmaxf(r, -127.f), 127.f);
     return (int8_t)(int)r;
 }

@@ -538,7 +538,7 @@ __device__ __forceinline__ void stage_quant32(uint8_t* codes, float* d, uint8_t*
             int sum = 0;
             for (int k = 0; k < 8; ++k) {
                 const float4 w = xp[k];
-                const int8_t q0 = quant1(w.x, id), q1 = quant1(w.y, id), q2 = quant1(w.z, id), q3 = quant1(w.w, id);
+                const int8_t q0 = quant1(w.x, dd, id), q1 = quant1(w.y, dd, id), q2 = quant1(w.z, dd, id), q3 = quant1(w.w, dd, id);
                 dst[NATURAL ? 4 * k + 0 : staged_pos<T>(4 * k + 0)] = (uint8_t)q0;
                 dst[NATURAL ? 4 * k + 1 : staged_pos<T>(4 * k + 1)] = (uint8_t)q1;
                 dst[NATURAL ? 4 * k + 2 : staged_pos<T>(4 * k + 2)] = (uint8_t)q2;
@@ -575,8 +575,8 @@ __device__ __forceinline__ void stage_quant32(uint8_t* codes, float* d, uint8_t*
         int sum = 0;
 #pragma unroll
         for (int f = 0; f < NF4; ++f) {
-            const int8_t q0 = quant1(w[f].x, id), q1 = quant1(w[f].y, id), q2 = quant1(w[f].z, id),
-                         q3 = quant1(w[f].w, id);
+            const int8_t q0 = quant1(w[f].x, dd, id), q1 = quant1(w[f].y, dd, id), q2 = quant1(w[f].z, dd, id),
+                         q3 = quant1(w[f].w, dd, id);
             sum += q0 + q1 + q2 + q3;
             const int e = part * E + 4 * f;
             if (!valid) continue;
@@ -631,8 +631,8 @@ __device__ __forceinline__ void stage_quant256(uint8_t* codes, float* d, uint8_t
         int s16 = 0;   // running sum of the current 16-group
 #pragma unroll
         for (int f = 0; f < NF4; ++f) {
-            const int8_t q0 = quant1(w[f].x, id), q1 = quant1(w[f].y, id), q2 = quant1(w[f].z, id),
-                         q3 = quant1(w[f].w, id);
+            const int8_t q0 = quant1(w[f].x, dd, id), q1 = quant1(w[f].y, dd, id), q2 = quant1(w[f].z, dd, id),
+                         q3 = quant1(w[f].w, dd, id);
             s16 += q0 + q1 + q2 + q3;
             const int e = part * E + 4 * f, r = e >> 4;
             if (valid)

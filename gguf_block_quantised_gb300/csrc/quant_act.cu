@@ -2,9 +2,10 @@
 // fused W4A8 kernels, "Architecture" page, "The package map", pkg/quant).
 //
 // Per block: amax = max|x|; d = amax/127; id = 1/d (0 when d = 0);
-// q = round-half-away-from-zero(x*id) clamped to +-127.  Every step is one
-// IEEE fp32 rounding (__fdiv_rn, __fmul_rn, roundf), so the codes are
-// bit-identical to the plain definition whatever the thread layout.  Q8_0
+// q = round-half-away-from-zero(x*id) clamped to +-127, or of x/d when d is
+// below 2^-128 and 1/d overflows.  Every step is one IEEE fp32 rounding
+// (__fdiv_rn, __fmul_rn, roundf), so the codes do not depend on the thread
+// layout and equal those of the plain definition.  Q8_0
 // stores fp16(d) (round to nearest even); Q8_K stores the fp32 d and the
 // int16 sums of each run of 16 codes.
 //
@@ -26,7 +27,7 @@ __global__ void k_quant_q8_0(const float* __restrict__ x, uint8_t* __restrict__ 
     const float amax = warp_max(fabsf(v));
     float d, id;
     act_scale(amax, d, id);
-    const int8_t q = quant1(v, id);
+    const int8_t q = quant1(v, d, id);
     uint8_t* o = out + b * 34;
     o[2 + lane] = (uint8_t)q;
     if (lane == 0) *reinterpret_cast<__half*>(o) = __float2half_rn(d);
@@ -53,7 +54,7 @@ __global__ void k_quant_q8_k(const float* __restrict__ x, uint8_t* __restrict__ 
     int s = 0;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-        const int8_t q = quant1(v[k], id);
+        const int8_t q = quant1(v[k], d, id);
         s += q;
         if (k < 4) w0 |= (uint32_t)(uint8_t)q << (8 * k);
         else w1 |= (uint32_t)(uint8_t)q << (8 * (k - 4));

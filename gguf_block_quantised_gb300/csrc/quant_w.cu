@@ -5,7 +5,8 @@
 //
 // Per 32-element block: m = the signed value of largest magnitude (the first
 // on ties); d = m / -half (half = 8 or 16); id = 1/d (0 when d = 0); code =
-// trunc(clamp(x*id + half + 0.5, 0, 2*half - 1)).  The largest-magnitude
+// trunc(clamp(x*id + half + 0.5, 0, 2*half - 1)), with x/d in place of x*id
+// when |d| is below 2^-128 and 1/d overflows.  The largest-magnitude
 // element lands on code 0.  Every step is one IEEE fp32 rounding (__fdiv_rn,
 // __fmul_rn, __fadd_rn; no contraction), so the codes do not depend on the
 // thread layout.  The block stores fp16(d), for Q5_0 the fifth bits (bit i
@@ -60,7 +61,8 @@ __global__ void __launch_bounds__(256) k_quant_w(const float4* __restrict__ x, u
     uint32_t codes = 0, hi_bits = 0;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        float t = __fadd_rn(__fmul_rn(v[k], id), kHalf + 0.5f);
+        const float u = isinf(id) ? __fdiv_rn(v[k], d) : __fmul_rn(v[k], id);   // block-uniform branch
+        float t = __fadd_rn(u, kHalf + 0.5f);
         t = fmaxf(fminf(t, kTop), 0.f);
         const uint32_t c = (uint32_t)__float2int_rz(t);
         codes |= (c & 15u) << (8 * k);

@@ -12,7 +12,11 @@
  *     d    = amax / 127                     (fp32, one rounding)
  *     id   = d == 0 ? 0 : 1 / d             (fp32, one rounding)
  *     q_i  = round half away from zero (x_i * id), clamped to [-127, 127]
- *            (a NaN product clamps to -127)
+ *   When d is below 2^-128 (amax under 127 * 2^-128), 1 / d overflows to
+ *   infinity and x_i * id is no longer the scaled value (for x_i = 0 it is
+ *   not even a number); the codes of such a block are then taken from the
+ *   quotient x_i / d itself (fp32, one rounding), which is the plain
+ *   definition q = round(x / d): zero stays zero.
  *   Q8_0 stores fp16(d) (round to nearest even) and q[32]    -> 34 bytes;
  *   Q8_K stores the fp32 d, q[256] and int16 bsums[16], the sums of q over
  *   each run of 16                                           -> 292 bytes.
@@ -32,13 +36,12 @@ static void quantize_block(const float* x, int bs, float* d_out, int8_t* q)
     }
     float d = amax / 127.0f;
     float id = (d == 0.0f) ? 0.0f : 1.0f / d;
+    const int overflow = isinf(id);             /* d below 2^-128 */
     for (int i = 0; i < bs; i++) {
-        float v = x[i] * id;
+        float v = overflow ? x[i] / d : x[i] * id;
         float r = roundf(v);                    /* halves away from zero */
-        /* Clamp with IEEE maxNum/minNum (the non-NaN operand), so that every
-         * value has a defined code: when amax / 127 is subnormal, 1 / d
-         * overflows and 0 * id is NaN (the block's fp16 scale is 0 then). */
-        r = fminf(fmaxf(r, -127.0f), 127.0f);
+        if (r > 127.0f) r = 127.0f;
+        if (r < -127.0f) r = -127.0f;
         q[i] = (int8_t)r;
     }
     *d_out = d;

@@ -13,6 +13,9 @@
  *         (the first such element when several tie);
  *         d = m / -8, id = (d == 0 ? 0 : 1 / d),
  *         q_i = trunc(clamp(x_i * id + 8.5, 0, 15));  w = d * (q - 8).
+ *         When |d| is below 2^-128, 1 / d overflows; x_i / d (one fp32
+ *         division) then stands for x_i * id, so that a zero weight still
+ *         lands on code 8 (the quotient is what x_i * id approximates).
  *         The largest-magnitude element lands on code 0 (w = -8 d = m); the
  *         grid reaches +7 d on the other side, where values clamp.
  *   Q5_0: the same with d = m / -16 and q_i = trunc(clamp(x_i * id + 16.5, 0, 31)).
@@ -51,13 +54,14 @@ static float block_codes(const float* x, int bits, uint8_t* q)
     float m = block_extreme(x);
     float d = m / -half;
     float id = (d == 0.0f) ? 0.0f : 1.0f / d;
+    const int overflow = isinf(id);                 /* |d| below 2^-128 */
     for (int i = 0; i < 32; i++) {
-        float v = x[i] * id;
+        float v = overflow ? x[i] / d : x[i] * id;
         v = v + (half + 0.5f);
-        /* Clamp in fp32 before truncating, so that every value has a defined
-         * code: fminf/fmaxf return the non-NaN operand, and a subnormal block
-         * extreme can make 1 / d overflow. */
-        v = fmaxf(fminf(v, (float)top), 0.0f);
+        /* clamp in fp32 before truncating (converting an out-of-range float
+         * to an integer is undefined in C) */
+        if (v > (float)top) v = (float)top;
+        if (v < 0.0f) v = 0.0f;
         q[i] = (uint8_t)(int)v;                     /* truncation */
     }
     return d;

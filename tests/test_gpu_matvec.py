@@ -44,6 +44,36 @@ def test_quantize_act_bit_exact(qmv, orc, atype, n):
     assert np.array_equal(host(xq), ref)
 
 
+@pytest.mark.parametrize("atype", [3, 7])
+def test_quantize_act_scale_below_2_pow_minus_128(qmv, orc, atype):
+    """Blocks whose amax/127 is below 2^-128, so that 1/d overflows: the codes
+    are round(x / d) (zeros stay 0), byte for byte the oracle's, both from
+    qmv_quantize_act and when the matvec quantises its fp32 input itself
+    (QMV_FLAG_QUANTIZE_X gives the same output bits)."""
+    bs = 32 if atype == 3 else 256
+    n_vec, cols = 3, 1024
+    g = np.random.default_rng(31)
+    x = (g.uniform(-1, 1, (n_vec, cols)) * 1e-37).astype(np.float32)
+    x[:, ::5] = 0.0
+    x[0, :bs] = g.standard_normal(bs).astype(np.float32)     # one block with an ordinary scale
+    x[2, bs:2 * bs] = 0.0                                      # and an all-zero block
+    ref = orc.quantize_act(atype, x)
+    xd = dev(x)
+    xq = torch.zeros(ref.size, dtype=torch.uint8, device="cuda")
+    qmv.qmv_quantize_act(atype, xd, xq, x.size)
+    assert np.array_equal(host(xq), ref.reshape(-1))
+    t = 2 if atype == 3 else 4
+    rows = 70
+    W = dev(synth.weights(t, rows, cols, seed=32))
+    y1 = torch.empty((n_vec, rows), dtype=torch.float32, device="cuda")
+    y2 = torch.empty((n_vec, rows), dtype=torch.float32, device="cuda")
+    qmv.qmv_matvec(qmv.FMT(t, atype), W, rows, cols, xq, y1, n_vec)
+    qmv.qmv_matvec(qmv.FMT(t, atype) | qmv.FLAG_QUANTIZE_X, W, rows, cols, xd, y2, n_vec)
+    assert np.array_equal(host(y1).view(np.uint32), host(y2).view(np.uint32))
+    if atype == 7:
+        assert (host(y1)[1:] != 0).any()   # the tiny Q8_K scales still reach the output
+
+
 @pytest.mark.parametrize("t", ALLW)
 def test_dequantize_bit_exact(qmv, orc, t):
     for rows, cols in shapes_for(t)[:3]:

@@ -1,7 +1,8 @@
 """The weight quantiser (qmv_quantize_weights) against the oracle: bit-exact
 blocks for Q4_0, Q5_0 and Q8_0 on adversarial inputs (magnitude ties with
 opposite signs, zero and negative-zero blocks, scales over 2^-30..2^20, ragged
-shapes) and at a full model shape; refusals on the host."""
+shapes, blocks so small that 1/d overflows) and at a full model shape;
+refusals on the host."""
 import numpy as np
 import pytest
 
@@ -19,6 +20,8 @@ def weights(seed, rows, cols):
     b[::13] = 0.0
     b[6::17] = -0.0
     b[::19, :8] = np.float32(2.0 ** -140)   # subnormal neighbours
+    b[4::23] = g.uniform(-1, 1, (len(b[4::23]), 32)).astype(np.float32) * np.float32(2.0 ** -127)
+    b[4::23, 2] = 0.0                       # a zero in a block whose 1/d overflows
     return w
 
 

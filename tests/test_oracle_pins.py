@@ -190,6 +190,42 @@ def test_quantiser_properties(orc, t):
         assert d_st == ref
 
 
+@pytest.mark.parametrize("t", [P.Q8_0, P.Q8_K])
+def test_quantiser_scale_below_2_pow_minus_128(orc, t):
+    """A block whose amax/127 is below 2^-128, so that 1/d overflows: the codes
+    are round(x / d) of the plain definition -- zero stays 0, the extreme
+    is +-127, every code a nearest integer of the exact quotient -- not the
+    saturated or undefined values of x * inf."""
+    bs = 32 if t == P.Q8_0 else 256
+    g = np.random.default_rng(17)
+    amax = np.float32(1e-37)
+    x = (g.uniform(-1, 1, bs) * amax).astype(np.float32)
+    x[3] = amax
+    x[10] = -amax / np.float32(2)
+    x[0] = 0.0
+    x[7] = -0.0
+    x[bs - 1] = 0.0
+    out = orc.quantize_act(t, x)
+    d = np.float32(amax) / np.float32(127)
+    assert float(d) < 2.0 ** -128 and np.isinf(np.float32(1) / d)
+    if t == P.Q8_0:
+        q = out[2:34].view(np.int8).astype(int)
+        assert out[:2].view(np.float16)[0] == 0      # fp16(d) underflows
+    else:
+        q = out[4:260].view(np.int8).astype(int)
+        assert out[:4].view(np.float32)[0] == d
+        assert np.array_equal(out[260:292].view(np.int16).astype(int), q.reshape(16, 16).sum(1))
+    assert q[0] == 0 and q[7] == 0 and q[bs - 1] == 0
+    assert q[3] == 127
+    assert q[10] in (-63, -64)   # -amax/2 over the subnormal d (rounded to ~17 bits) is near -63.5
+    # nearest integer of the exact quotient (fp64), up to the fp32 rounding of x/d
+    exact = x.astype(np.float64) / float(d)
+    assert (np.abs(exact - q) <= 0.5 + 1e-5).all()
+    # halves away from zero, on the quotient the oracle is defined by (fp32 x/d)
+    v = (x / d).astype(np.float64)
+    assert np.array_equal(q, (np.sign(v) * np.floor(np.abs(v) + 0.5)).astype(int))
+
+
 # ---- integer block dots ------------------------------------------------------------
 
 @pytest.mark.parametrize("t", WEIGHT_TYPES)

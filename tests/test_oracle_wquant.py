@@ -46,6 +46,31 @@ def test_extreme_sign_and_ties():
     assert O.quantize_weights(O.Q4_0, y).tobytes()[:2].hex() == "00b6"
 
 
+@pytest.mark.parametrize("t,half", [(O.Q4_0, 8), (O.Q5_0, 16)])
+def test_scale_below_2_pow_minus_128(t, half):
+    """A block extreme so small that 1/d overflows: zero weights still land on
+    the zero point (code 8 / 16), the extreme on code 0, and every code is a
+    nearest grid point of the exact quotient x/d."""
+    g = np.random.default_rng(23)
+    m = np.float32(-2e-38)
+    x = (g.uniform(-1, 1, 32) * np.float32(1.9e-38)).astype(np.float32)
+    x[5] = m
+    x[0] = 0.0
+    x[9] = -0.0
+    d = m / np.float32(-half)
+    assert float(abs(d)) < 2.0 ** -128 and np.isinf(np.float32(1) / d)
+    b = O.quantize_weights(t, x).tobytes()
+    nib = np.frombuffer(b[2 if t == O.Q4_0 else 6:], dtype=np.uint8)
+    q = np.concatenate([nib & 15, nib >> 4]).astype(int)
+    if t == O.Q5_0:
+        qh = int.from_bytes(b[2:6], "little")
+        q += np.array([(qh >> i) & 1 for i in range(32)]) * 16
+    assert q[0] == half and q[9] == half and q[5] == 0
+    exact = x.astype(np.float64) / float(d) + half
+    top = 2 * half - 1
+    assert (np.abs(np.clip(exact, 0, top) - q) <= 0.5 + 1e-5).all()
+
+
 def _blocks(seed, n):
     g = np.random.default_rng(seed)
     x = g.standard_normal((n, 32)).astype(np.float32)
