@@ -187,7 +187,7 @@ int moe_check(const char* name, int fmt, const void* W3d, int n_expert, int64_t 
         return fail(QMV_ERR_INVALID_ARG, "QMV_FLAG_QUANTIZE_X needs an 8-bit activation type (Q8_0 or Q8_K)");
     if (n_expert < 1 || n_expert > 1024) return fail(QMV_ERR_INVALID_ARG, "n_expert must be in 1..1024 (got %d)", n_expert);
     if (k < 1 || k > 64) return fail(QMV_ERR_INVALID_ARG, "k must be in 1..64 (got %d)", k);
-    if (n_tok < 0 || n_tok * k > (int64_t)1 << 24)
+    if (n_tok < 0 || n_tok > ((int64_t)1 << 24) / k)   // range first: n_tok * k must not overflow
         return fail(QMV_ERR_INVALID_ARG, "n_tok must be >= 0 with n_tok*k <= 16777216");
     if (c.bf16 && rows > (int64_t)1 << 30) return fail(QMV_ERR_SHAPE, "rows must be below 2^30");
     c.empty = n_tok == 0 || rows == 0;

@@ -81,9 +81,9 @@ typedef enum {
  *   qmv_matvec (one launch instead of two).
  * QMV_FLAG_PDL: launch as a programmatic dependent of the kernel before it on
  *   the stream.  The kernel may start streaming W before that kernel has
- *   finished; it still waits for it before reading x or writing y.  Only for
- *   weights that the immediately preceding kernels do not write.  Accepted by
- *   qmv_quantize_act and qmv_matvec. */
+ *   finished; it still waits for it before reading x or writing y (X, Y).
+ *   Only for weights that the immediately preceding kernels do not write.
+ *   Accepted by qmv_quantize_act, qmv_matvec and qmv_matmul. */
 #define QMV_FLAG_QUANTIZE_X (1 << 16)
 #define QMV_FLAG_PDL (1 << 17)
 
@@ -123,7 +123,8 @@ size_t qmv_row_bytes(int type, int64_t cols);
  *   xq  : n/bs blocks out.
  *   n   : multiple of 32 (Q8_0) or 256 (Q8_K); 0 is a no-op.
  * Per block: amax = max|x|, d = amax/127, q = round-half-away(x * (1/d))
- * clamped to +-127 (q = 0 when amax = 0); fp32 arithmetic, one rounding per
+ * clamped to +-127 (q = 0 when amax = 0; when d is below 2^-128 and 1/d
+ * overflows, q = round-half-away(x / d)); fp32 arithmetic, one rounding per
  * operation.  Q8_0 stores d rounded to fp16, Q8_K the fp32 d.
  * ------------------------------------------------------------------------- */
 int qmv_quantize_act(int fmt, const float* x, void* xq, int64_t n, void* stream);
@@ -222,6 +223,8 @@ int qmv_matvec(int fmt, const void* W, int64_t rows, int64_t cols,
  *         m16n8k32; tcgen05 has no int8 kind on sm_103a), sub-block scales
  *         applied in integers, fp32 accumulation per super-block.  Agrees with
  *         the W4A8 decode of each token within the accuracy bar above.
+ *         Either may be | QMV_FLAG_PDL (the W these kernels read must not be
+ *         written by the kernels just before them on the stream).
  *   X   : 16-byte aligned.   Y : fp32 [m][rows], overwritten.
  *   m   : >= 0.
  * ------------------------------------------------------------------------- */
