@@ -16,9 +16,13 @@ Metric: weight GB/s = weight bytes of the step / step time (higher is
 better), reported against the HBM roofline.  The step is captured once in a
 CUDA graph and replayed; timing uses CUDA events on the replay stream.
 
-Also reported: batch-8 decode of the same step, the lm_head matvec alone
-(the dominant kernel, for the roofline), end-to-end through host buffers, and
-the CPU oracle on a bounded sample (cpu_baseline).
+Also reported: the dominant kernel for the roofline (the step's 96 Q5_0
+layer matvecs, launched as in the step, ~95% of its launch time) and each of
+their four shapes alone; the lm_head matvec alone; batch-8 and fp32-activation
+(A32) forms of the step; end to end through host buffers; a single Q4_0
+896x896 matvec (cold stream and single-call latency); the K-quant decode
+shapes, the prefill GEMMs, the gpt-oss MoE layer and the weight quantiser;
+and the CPU oracle on bounded samples of each (cpu_baseline).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -151,8 +155,8 @@ class DecodeStep:
     step.  fused=False: separate qmv_quantize_act launches, plain stream
     order: 194 launches per step."""
 
-    def __init__(self, q, torch, n_vec, seed=1, fused=True):
-        self.q, self.torch, self.n_vec, self.fused = q, torch, n_vec, fused
+    def __init__(self, q, torch, n_vec, seed=1, fused=True, a32=False):
+        self.q, self.torch, self.n_vec, self.fused, self.a32 = q, torch, n_vec, fused, a32
         dev = torch.device("cuda")
         self.W = []
         tid = 0
@@ -188,9 +192,25 @@ class DecodeStep:
         per_layer = len(LAYER_GROUPS)
         self.launches = LAYERS * per_layer + 1 if fused else LAYERS * (4 + per_layer) + 2
 
+    def run_layers(self, stream):
+        """The step's 96 layer matvecs alone (no lm_head), launched as in run()."""
+        q, n, s = self.q, self.n_vec, stream.cuda_stream
+        fl = q.FLAG_QUANTIZE_X | q.FLAG_PDL
+        for l in range(LAYERS):
+            for m, (W, rows, cols, inp) in enumerate(self.W[l]):
+                q.qmv_matvec(q.FMT(Q5_0, Q8_0) | fl, W, rows, cols, self.x[4 * l + inp], self.y[l][m], n, s)
+
     def run(self, stream):
         q, n = self.q, self.n_vec
         s = stream.cuda_stream
+        if self.a32:
+            # fp32 activations straight into the matvec (no quantisation), PDL chain
+            for l in range(LAYERS):
+                for m, (W, rows, cols, inp) in enumerate(self.W[l]):
+                    q.qmv_matvec(q.FMT(Q5_0, F32) | q.FLAG_PDL, W, rows, cols, self.x[4 * l + inp], self.y[l][m],
+                                 n, s)
+            q.qmv_matvec(q.FMT(Q8_0, F32) | q.FLAG_PDL, self.lm, VOCAB, HID, self.x[-1], self.logits, n, s)
+            return
         if self.fused:
             fl = q.FLAG_QUANTIZE_X | q.FLAG_PDL
             for l in range(LAYERS):
@@ -298,6 +318,98 @@ def lm_roofline(q, torch, stream, step, dev_index, pdl=True):
     sampler.__exit__(None, None, None)
     del g, lm_copies
     return e0.elapsed_time(e1) / (5 * lm_reps), sampler.summary()
+
+
+LAYER_BYTES_PER_STEP = LAYERS * sum(r * row_bytes(Q5_0, c) for _, r, c, _ in LAYER_MATS)
+LAYER_LAUNCHES_PER_STEP = LAYERS * len(LAYER_GROUPS)
+
+
+def layer_roofline(torch, stream, step, dev_index, reps=200):
+    """The dominant kernel: the Q5_0 layer matvecs, which take ~95% of the
+    step's launch time.  The step's 96 layer launches (q|k|v 1152x896, o
+    896x896, gate|up 9728x896, down 896x4864 per layer; each quantising its
+    fp32 input, a programmatic dependent of the one before) are replayed alone
+    from one CUDA graph and timed with CUDA events on the replay stream.
+    Their 246 MB of weights exceed L2, so every pass streams them from HBM.
+    Returns (ms per launch on average, clocks)."""
+    ms, clocks = time_graph(torch, step.run_layers, stream, reps, 10, sampler_index=dev_index)
+    return ms / LAYER_LAUNCHES_PER_STEP, clocks
+
+
+def layer_shapes_leg(q, torch, stream, step, hbm):
+    """Each of the four stacked Q5_0 layer shapes alone, launched as in the step
+    (fp32 input quantised in the kernel, PDL chain), round robin over enough
+    weight copies (> 300 MB) that every launch reads its weights from HBM."""
+    out = {}
+    for m, (W0, rows, cols, inp) in enumerate(step.W[0]):
+        x, y = step.x[inp], step.y[0][m]
+        copies = [step.W[l][m][0] for l in range(LAYERS)]
+        while sum(c.numel() for c in copies) < 300_000_000:
+            copies.append(W0.clone())
+        fmt = q.FMT(Q5_0, Q8_0) | q.FLAG_QUANTIZE_X | q.FLAG_PDL
+        calls = [lambda s, W=W: q.qmv_matvec(fmt, W, rows, cols, x, y, 1, s.cuda_stream) for W in copies]
+        ms = time_rotating(torch, stream, calls, max(len(copies), 100))
+        nbytes = W0.numel()
+        gbs = nbytes / (ms / 1e3) / 1e9
+        out[f"{rows}x{cols}"] = {"us": ms * 1e3, "bytes": nbytes, "weight_gbs": gbs, "frac_of_hbm": gbs / hbm}
+        del copies
+    return out
+
+
+def config1_leg(q, torch, stream, hbm):
+    """A single Q4_0 896x896 matvec (451,584 weight bytes), fp32 activations
+    (A32) and the W4A8 path (x quantised to Q8_0, in the kernel or by a
+    separate qmv_quantize_act).  The matrix fits in L2 many times over, so
+    (1) the cold-stream rate is taken round robin over 640 weight copies (289 MB,
+    over twice L2), as plain launches and as a PDL chain, and (2) the latency
+    of one call is the event-timed span of a single launch between idle
+    periods, median of 50."""
+    rows = cols = 896
+    W0 = torch.from_numpy(synth.weights(Q4_0, rows, cols, seed=0)).cuda()
+    copies = [W0] + [W0.clone() for _ in range(639)]
+    x = torch.from_numpy(synth.activations(1, cols, seed=0)).cuda()
+    xq = torch.empty(q.qmv_row_bytes(Q8_0, cols), dtype=torch.uint8, device="cuda")
+    q.qmv_quantize_act(Q8_0, x, xq, cols)
+    y = torch.empty((1, rows), dtype=torch.float32, device="cuda")
+    modes = {"A32": (q.FMT(Q4_0, F32), x), "A8_in_kernel": (q.FMT(Q4_0, Q8_0) | q.FLAG_QUANTIZE_X, x),
+             "A8_prequantised": (q.FMT(Q4_0, Q8_0), xq)}
+    res = {}
+    for name, (fmt, xin) in modes.items():
+        r = {}
+        for pdl in (False, True):
+            f = fmt | (q.FLAG_PDL if pdl else 0)
+            calls = [lambda s, W=W, f=f: q.qmv_matvec(f, W, rows, cols, xin, y, 1, s.cuda_stream) for W in copies]
+            ms = time_rotating(torch, stream, calls, len(copies))
+            gbs = W0.numel() / (ms / 1e3) / 1e9
+            r["pdl_chain" if pdl else "plain"] = {"us": ms * 1e3, "weight_gbs": gbs, "frac_of_hbm": gbs / hbm}
+        lat = []
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for i in range(60):
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                q.qmv_matvec(fmt, copies[i % len(copies)], rows, cols, xin, y, 1, stream.cuda_stream)
+                e1.record(stream)
+            e1.synchronize()
+            if i >= 10:
+                lat.append(e0.elapsed_time(e1) * 1e3)
+        r["single_call_latency_us"] = statistics.median(lat)
+        res[name] = r
+    q.qmv_get_status(stream)
+    del copies
+    return {"workload": "Q4_0 896x896, batch 1", "weight_bytes": W0.numel(), "by_mode": res}
+
+
+def oracle_rate(fn, nbytes, min_s=2.0):
+    """Single-threaded oracle rate on a bounded sample: fn() repeated for at
+    least min_s seconds; returns (GB/s of weight bytes, seconds, calls)."""
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        fn()
+        n += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_s:
+            return nbytes * n / dt / 1e9, dt, n
 
 
 def time_rotating(torch, stream, calls, reps, warmup=3, timed=3):
@@ -657,46 +769,173 @@ def _oracle_items(O, mats, xs, items):
     return time.perf_counter() - t0, nbytes
 
 
-_MC = None
+# ---- the oracle on every host core: a pool of spawned processes ----------------------
+# Each worker builds a workload once (from the same seeds as the GPU legs) and
+# then computes its static share of it per step: rows of every matrix (decode
+# step, prefill slice) or tokens (mixture of experts).
+_PW = {}
+
+PREFILL_CPU = (14336, 4096, 64)          # the 14336x4096 prefill on a 64-token slice
+MOE_CPU_TOKENS = 64
 
 
-def _mc_init():
-    """Process-pool worker set-up: the oracle and the step's workload, once."""
-    global _MC
+def _prefill_workload(O):
+    rows, cols, m = PREFILL_CPU
+    import torch
+    W = synth.weights(Q4_K, rows, cols, seed=4, tensor_id=rows)
+    x = synth.activations(m, cols, seed=9)
+    xb = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy()
+    return W, xb, O.quantize_act(O.Q8_K, x)
+
+
+def _moe_workload(O, n_tok):
+    E, k = 32, 4
+    Wgu = synth.weights(MXFP4, E * 5760, 2880, seed=5, tensor_id=1)
+    Wd = synth.weights(MXFP4, E * 2880, 2880, seed=5, tensor_id=2)
+    bgu, bd = synth.bias(E, 5760, seed=5), synth.bias(E, 2880, seed=5, tensor_id=2001)
+    ids, gates = synth.router(n_tok, E, k, seed=6)
+    x = O.quantize_act(O.Q8_0, synth.activations(n_tok, 2880, seed=10))
+    h = O.quantize_act(O.Q8_0, synth.activations(n_tok * k, 2880, seed=11).reshape(n_tok, k, 2880))
+    return Wgu, Wd, bgu, bd, ids, gates, x, h
+
+
+def _moe_tokens(O, wl, t0, t1):
+    """The oracle's W4A8 MoE layer (gate_up up form, then down gate-weighted) on tokens t0..t1."""
+    Wgu, Wd, bgu, bd, ids, gates, x, h = wl
+    E, k = 32, 4
+    O.moe(O.MXFP4, O.Q8_0, Wgu, E, 5760, 2880, ids[t0:t1], None, k, x[t0:t1], t1 - t0, bias=bgu)
+    O.moe(O.MXFP4, O.Q8_0, Wd, E, 2880, 2880, ids[t0:t1], gates[t0:t1], k, h[t0:t1], t1 - t0, bias=bd)
+
+
+def _pw_init(kind):
     from oracle import oracle as O
-    _MC = (O,) + _oracle_step_workload()
+    _PW["O"] = O
+    if kind == "decode":
+        _PW[kind] = _oracle_step_workload()
+    elif kind.startswith("prefill"):
+        _PW[kind] = _prefill_workload(O)
+    elif kind == "moe":
+        _PW[kind] = _moe_workload(O, MOE_CPU_TOKENS)
 
 
-def _mc_task(args):
-    """One worker's share of a decode step: rows [w/W, (w+1)/W) of every matrix."""
-    w, nw = args
-    O, mats, xs = _MC
-    xq = [O.quantize_act(O.Q8_0, a) for a in xs]
-    for W, rows, cols, xi, t in mats:
+def _pw_task(args):
+    """One worker's share of one step of workload `kind`."""
+    kind, w, nw = args
+    O = _PW["O"]
+    if kind == "decode":
+        mats, xs = _PW[kind]
+        xq = [O.quantize_act(O.Q8_0, a) for a in xs]
+        for W, rows, cols, xi, t in mats:
+            r0, r1 = rows * w // nw, rows * (w + 1) // nw
+            if r1 > r0:
+                rb = row_bytes(t, cols)
+                O.matvec(t, O.Q8_0, W[r0 * rb:r1 * rb], r1 - r0, cols, xq[xi], 1, want_abs=False)
+    elif kind.startswith("prefill"):
+        W, xb, xq = _PW[kind]
+        rows, cols, m = PREFILL_CPU
         r0, r1 = rows * w // nw, rows * (w + 1) // nw
+        rb = row_bytes(Q4_K, cols)
+        at, xin = (O.BF16, xb) if kind == "prefill_bf16" else (O.Q8_K, xq)
         if r1 > r0:
-            rb = row_bytes(t, cols)
-            O.matvec(t, O.Q8_0, W[r0 * rb:r1 * rb], r1 - r0, cols, xq[xi], 1, want_abs=False)
+            O.matvec(O.Q4_K, at, W[r0 * rb:r1 * rb], r1 - r0, cols, xin, m, want_abs=False)
+    elif kind == "moe":
+        t0, t1 = MOE_CPU_TOKENS * w // nw, MOE_CPU_TOKENS * (w + 1) // nw
+        if t1 > t0:
+            _moe_tokens(O, _PW[kind], t0, t1)
     return w
+
+
+def pool_time(kind, n_steps):
+    """Seconds per step of workload `kind` on every host core (a warm step first)."""
+    import multiprocessing as mp
+    nw = os.cpu_count() or 1
+    tasks = [(kind, w, nw) for w in range(nw)]
+    # map_async with a time limit: a worker that dies would leave a plain map waiting forever
+    with mp.get_context("spawn").Pool(nw, initializer=_pw_init, initargs=(kind,)) as pool:
+        pool.map_async(_pw_task, tasks, chunksize=1).get(timeout=600)   # set-up and a warm step
+        t0 = time.perf_counter()
+        for _ in range(n_steps):
+            pool.map_async(_pw_task, tasks, chunksize=1).get(timeout=300)
+        dt = time.perf_counter() - t0
+    return dt / n_steps, nw
 
 
 def cpu_baseline_all_cores(n_steps=8):
     """The oracle on every host core: a pool of processes (spawned, never forked
     from a process that has used the GPU), each owning a static share of the
     rows of every matrix of the step; a step ends when every share is done."""
-    import multiprocessing as mp
-    nw = os.cpu_count() or 1
-    tasks = [(w, nw) for w in range(nw)]
-    # map_async with a time limit: a worker that dies would leave a plain map waiting forever
-    with mp.get_context("spawn").Pool(nw, initializer=_mc_init) as pool:
-        pool.map_async(_mc_task, tasks, chunksize=1).get(timeout=300)   # set-up and a warm step
-        t0 = time.perf_counter()
-        for _ in range(n_steps):
-            pool.map_async(_mc_task, tasks, chunksize=1).get(timeout=120)
-        dt = time.perf_counter() - t0
-    return {"value": STEP_WEIGHT_BYTES * n_steps / dt / 1e9, "unit": "GB/s", "cores": nw, "kind": "oracle",
+    sec, nw = pool_time("decode", n_steps)
+    return {"value": STEP_WEIGHT_BYTES / sec / 1e9, "unit": "GB/s", "cores": nw, "kind": "oracle",
             "sample": f"{n_steps} full decode steps (batch 1, W4A8), the rows of every matrix split statically "
-                      f"over {nw} processes, {dt:.1f} s"}
+                      f"over {nw} processes, {sec * n_steps:.1f} s"}
+
+
+def cpu_baseline_kquant():
+    """The oracle, single-threaded, on each K-quant decode shape (a row slice of
+    about 8 MB of each matrix, one vector of Q8_K activations)."""
+    from oracle import oracle as O
+    shapes = [(Q4_K, 4096, 4096), (Q4_K, 1024, 4096), (Q4_K, 14336, 4096), (Q4_K, 4096, 14336),
+              (Q6_K, 128256, 4096)]
+    tot_b = tot_s = 0.0
+    for t, rows, cols in shapes:
+        rb = row_bytes(t, cols)
+        nr = min(rows, max(1, 8_000_000 // rb))
+        W = synth.weights(t, nr, cols, seed=7)
+        xq = O.quantize_act(O.Q8_K, synth.activations(1, cols, seed=8))
+        gbs, dt, n = oracle_rate(lambda: O.matvec(t, O.Q8_K, W, nr, cols, xq, 1, want_abs=False), nr * rb, 0.5)
+        tot_b += nr * rb * n
+        tot_s += dt
+    return {"value": tot_b / tot_s / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"a ~8 MB row slice of each of the five shapes, 1 vector, single-threaded C oracle, "
+                      f"{tot_s:.1f} s"}
+
+
+def cpu_baseline_prefill():
+    """The oracle on the 14336x4096 prefill restricted to a 64-token slice:
+    single-threaded on 256 rows of it, and on every host core over all rows.
+    TFLOP/s counts 2 flops per multiply-add of the definition."""
+    from oracle import oracle as O
+    rows, cols, m = PREFILL_CPU
+    W, xb, xq = _prefill_workload(O)
+    rb = row_bytes(Q4_K, cols)
+    out = {}
+    for name, at, xin in (("bf16", O.BF16, xb), ("w4a8", O.Q8_K, xq)):
+        nr = 256
+        Ws = W[:nr * rb]
+        _, dt, n = oracle_rate(lambda: O.matvec(O.Q4_K, at, Ws, nr, cols, xin, m, want_abs=False), 1, 1.0)
+        one = {"value": 2.0 * m * nr * cols * n / dt / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+               "sample": f"{m} tokens x {nr} rows of 14336x4096 Q4_K ({name}), {n} calls, {dt:.1f} s"}
+        try:
+            sec, nw = pool_time("prefill_" + name, 1)
+            allc = {"value": 2.0 * m * rows * cols / sec / 1e12, "unit": "TFLOP/s", "cores": nw, "kind": "oracle",
+                    "sample": f"{m} tokens x all 14336 rows ({name}), rows split over {nw} processes, "
+                              f"{sec:.2f} s per pass"}
+        except Exception as e:   # an auxiliary measurement: report it, keep the line
+            allc = {"error": f"{type(e).__name__}: {e}"}
+        out[name] = {"single_core": one, "all_cores": allc}
+    return out
+
+
+def cpu_baseline_moe():
+    """The oracle's W4A8 MoE layer (gate_up + down, gpt-oss shapes): one token
+    single-threaded, and 64 tokens on every host core (tokens split)."""
+    from oracle import oracle as O
+    wl = _moe_workload(O, MOE_CPU_TOKENS)
+    ids = wl[4]
+    per_tok_bytes = (5760 + 2880) * synth.row_bytes(MXFP4, 2880) * 4   # four routed experts per token
+    _, dt, n = oracle_rate(lambda: _moe_tokens(O, wl, 0, 1), 1, 1.0)
+    one = {"value": per_tok_bytes * n / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+           "ms_per_layer": 1e3 * dt / n,
+           "sample": f"1 token (4 experts, {per_tok_bytes / 1e6:.1f} MB of expert weights), {n} calls, {dt:.1f} s"}
+    try:
+        sec, nw = pool_time("moe", 1)
+        used = len(np.unique(ids)) * (5760 + 2880) * synth.row_bytes(MXFP4, 2880)
+        allc = {"value": used / sec / 1e9, "unit": "GB/s (distinct expert bytes)", "cores": nw, "kind": "oracle",
+                "ms_per_layer": 1e3 * sec,
+                "sample": f"{MOE_CPU_TOKENS} tokens split over {nw} processes, {sec:.2f} s per layer"}
+    except Exception as e:
+        allc = {"error": f"{type(e).__name__}: {e}"}
+    return {"tok1_single_core": one, "tok64_all_cores": allc}
 
 
 def run_reference(args):
@@ -743,7 +982,8 @@ def run_reference(args):
               f"the lm_head in ~8 MB row slices; single-threaded C oracle")
     line = {"impl": "reference", "metric": "quant GEMV weight GB/s (decode step, W4A8)", "value": value,
             "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8xint4->fp32",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "q5_0/q8_0 weights x int8 activations (dp4a int32, fp32 accumulate)",
             "data": "synthetic",
             "config": {"workload": "qwen2.5-0.5b-shaped decode step (24 layers Q5_0 + lm_head Q8_0), batch 1",
                        "l2": "weights 390.6 MB, streamed from host memory"},
@@ -785,20 +1025,29 @@ def main():
     q.load()
     stream = torch.cuda.Stream()
 
-    # --- the step at batch 1 (the headline) and batch 8; the two-launch form for comparison
+    # --- the step at batch 1 (the headline) and batch 8; the two-launch form and A32 for comparison
     step1 = DecodeStep(q, torch, 1)
     lm_ms_first, _ = lm_roofline(q, torch, stream, step1, local)
     step8 = DecodeStep(q, torch, 8)
     step1u = DecodeStep(q, torch, 1, fused=False)
+    step1f = DecodeStep(q, torch, 1, a32=True)
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     ms1, clocks = time_graph(torch, step1.run, stream, args.steps, args.warmup, sampler_index=local)
     ms8, _ = time_graph(torch, step8.run, stream, max(args.steps // 4, 10), args.warmup)
     ms1u, _ = time_graph(torch, step1u.run, stream, max(args.steps // 4, 10), args.warmup)
+    ms1f, _ = time_graph(torch, step1f.run, stream, max(args.steps // 4, 10), args.warmup)
     q.qmv_get_status(stream)
     ms1, ms8 = max_over_ranks(torch, [ms1, ms8], "cuda")
+    del step1u, step1f
 
+    # --- the dominant kernel (the Q5_0 layer matvecs, as launched in the step) and the lm_head
+    hbm, peak_kind = load_peaks()
+    layer_ms, layer_clocks = layer_roofline(torch, stream, step1, local)
+    layer_bytes = LAYER_BYTES_PER_STEP / LAYER_LAUNCHES_PER_STEP
+    layer_gbs = layer_bytes / (layer_ms / 1e3) / 1e9
+    shapes = layer_shapes_leg(q, torch, stream, step1, hbm)
     lm_ms, lm_clocks = lm_roofline(q, torch, stream, step1, local)
     lm_ms_nopdl, _ = lm_roofline(q, torch, stream, step1, local, pdl=False)
     lm_bytes = VOCAB * row_bytes(Q8_0, HID)
@@ -818,8 +1067,8 @@ def main():
     e2e_steps = max(args.steps // 4, 10)
     e2e_ms, _ = time_graph(torch, e2e_step, stream, e2e_steps, args.warmup)
 
-    hbm, peak_kind = load_peaks()
     tflops_peak = 1900.0 if peak_kind == "fallback" else load_tflops_peak()
+    cfg1 = None if args.no_extra else config1_leg(q, torch, stream, hbm)
     kquant = None if args.no_extra else kquant_decode_leg(q, torch, stream, hbm)
     prefill = None if args.no_extra else prefill_leg(q, torch, stream, tflops_peak)
     moe = None if args.no_extra else moe_leg(q, torch, stream, hbm)
@@ -829,14 +1078,19 @@ def main():
         if ws > 1:
             torch.distributed.barrier()
         return 0
-    cpu = None if args.no_cpu_baseline else cpu_baseline(4)
-    cpu_all = None
+    cpu = cpu_all = None
     if not args.no_cpu_baseline:
+        cpu = cpu_baseline(4)
         try:
             cpu_all = cpu_baseline_all_cores()
         except Exception as e:   # an auxiliary measurement: report it, keep the line
             cpu_all = {"error": f"{type(e).__name__}: {e}"}
-    launches_per_step = step1.launches
+        if kquant is not None:
+            kquant["cpu_baseline"] = cpu_baseline_kquant()
+        if prefill is not None:
+            prefill["cpu_baseline"] = cpu_baseline_prefill()
+        if moe is not None:
+            moe["cpu_baseline"] = cpu_baseline_moe()
     line = {
         "metric": "quant GEMV weight GB/s (decode step, W4A8)",
         "value": value,
@@ -848,7 +1102,7 @@ def main():
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "int8xint4->fp32",
+        "dtype": "q5_0/q8_0 weights x int8 activations (dp4a int32, fp32 accumulate)",
         "data": "synthetic",
         "config": {"workload": "qwen2.5-0.5b-shaped decode step (24 layers q/k/v/o/gate/up/down Q5_0, stored as "
                                "q|k|v, o, gate|up, down stacks, + lm_head 151936x896 Q8_0; fp32 activations "
@@ -860,26 +1114,40 @@ def main():
         "frac_of_hbm": value / ws / hbm,
         "batch8": {"ms_per_step": ms8, "value": ws * STEP_WEIGHT_BYTES / (ms8 / 1e3) / 1e9, "unit": "GB/s",
                    "vector_rate_tok_s": ws * 8 / (ms8 / 1e3)},
+        "a32_batch1": {"ms_per_step": ms1f, "value": ws * STEP_WEIGHT_BYTES / (ms1f / 1e3) / 1e9, "unit": "GB/s",
+                       "how": "fp32 activations straight into every matvec (QMV_FMT(Q5_0|Q8_0, F32)), PDL chain"},
         "unfused_batch1": {"ms_per_step": ms1u, "value": ws * STEP_WEIGHT_BYTES / (ms1u / 1e3) / 1e9,
-                           "unit": "GB/s", "launches_per_step": step1u.launches,
+                           "unit": "GB/s", "launches_per_step": step1.launches * 2,
                            "how": "qmv_quantize_act + qmv_matvec as separate launches, no PDL"},
-        "roofline": {"bound": "hbm", "kernel": "k_gemv<Q8_0,A8,NV=1> lm_head 151936x896 (quantising its fp32 input; "
-                               "launched as in the step, a programmatic dependent of the launch before)",
-                     "achieved": lm_gbs, "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": lm_gbs / hbm, "traffic": traffic_for("k_gemv<Q8_0,A8,NV=1> lm_head 151936x896"),
-                     "algorithmic_bytes_per_launch": lm_bytes, "launch_ms": lm_ms,
-                     "launch_ms_plain_launches": lm_ms_nopdl,
-                     "achieved_plain_launches": lm_bytes / (lm_ms_nopdl / 1e3) / 1e9,
-                     "launch_ms_before_step_graphs": lm_ms_first, "clocks": lm_clocks,
-                     "l2": "4 weight copies rotated, each launch reads cold"},
+        "roofline": {"bound": "hbm",
+                     "kernel": "k_gemv<Q5_0,A8,NV=1> -- the step's 96 layer matvecs (q|k|v 1152x896, o 896x896, "
+                               "gate|up 9728x896, down 896x4864 per layer), launched as in the step (each quantising "
+                               "its fp32 input, a programmatic dependent of the one before); ~95% of the step's "
+                               "launch time",
+                     "achieved": layer_gbs, "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": layer_gbs / hbm, "traffic": traffic_for("k_gemv<Q5_0,A8,NV=1> qwen layer matvecs"),
+                     "algorithmic_bytes_per_launch": layer_bytes, "launch_ms": layer_ms,
+                     "units": "weight bytes of the block format (Q5_0: 0.6875 B per weight) x rows x cols, "
+                              "averaged over the 96 launches (246,005,760 B per step)",
+                     "clocks": layer_clocks, "by_shape": shapes,
+                     "l2": "the 246 MB of layer weights exceed L2; every pass streams them"},
+        "lm_head": {"kernel": "k_gemv<Q8_0,A8,NV=1> lm_head 151936x896 (quantising its fp32 input; PDL)",
+                    "achieved": lm_gbs, "unit": "GB/s", "frac": lm_gbs / hbm, "launch_ms": lm_ms,
+                    "algorithmic_bytes_per_launch": lm_bytes,
+                    "traffic": traffic_for("k_gemv<Q8_0,A8,NV=1> lm_head 151936x896"),
+                    "launch_ms_plain_launches": lm_ms_nopdl,
+                    "achieved_plain_launches": lm_bytes / (lm_ms_nopdl / 1e3) / 1e9,
+                    "launch_ms_before_step_graphs": lm_ms_first, "clocks": lm_clocks,
+                    "l2": "4 weight copies rotated, each launch reads cold"},
         "clocks": clocks,
         "e2e": {"value": ws * STEP_WEIGHT_BYTES / (e2e_ms / 1e3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "how": "the step's pinned host activations copied in (one copy) and the logits copied out every "
                        "step, all in one replayed CUDA graph on the caller's stream"},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": step1.launches * args.steps,
         "cpu_baseline": cpu,
         "cpu_baseline_all_cores": cpu_all,
+        "config1_q4_0_896": cfg1,
         "kquant_decode": kquant,
         "prefill": prefill,
         "moe": moe,
