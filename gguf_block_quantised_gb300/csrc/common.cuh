@@ -199,18 +199,39 @@ __device__ __forceinline__ void act_scale(float amax, float& d, float& id)
     d = __fdiv_rn(amax, 127.f);
     id = d == 0.f ? 0.f : __fdiv_rn(1.f, d);
 }
-// q = round-half-away-from-zero(v / d), clamped to +-127, computed as v * id
-// while id = 1/d is finite.  A scale below 2^-128 (a block whose largest
-// magnitude is under 127 * 2^-128) makes 1/d overflow; the code is then the
-// quotient v / d itself, one IEEE division, so that v = 0 still gives 0 and
-// every code is the plain definition's.  The branch is the same for a whole
-// block.
-__device__ __forceinline__ int8_t quant1(float v, float d, float id)
+// q = round-half-away-from-zero(v * id), clamped to +-127.
+__device__ __forceinline__ int8_t quant1(float v, float id)
 {
-    const float t = isinf(id) ? __fdiv_rn(v, d) : __fmul_rn(v, id);
-    float r = roundf(t);
+    float r = roundf(__fmul_rn(v, id));
     r = fminf(fmaxf(r, -127.f), 127.f);
     return (int8_t)(int)r;
+}
+
+// A scale below 2^-128 (a block whose largest magnitude is under 127 * 2^-128)
+// makes id = 1/d overflow, and v * id is then not the scaled value (0 * inf is
+// not even a number).  Such a block's codes are round(v / d): the rare block
+// divides its values by d first (one IEEE division each) and takes id = 1, so
+// that quant1 multiplies by 1 exactly.  The common path computes no division
+// (the loops are unrolled so that the arrays stay in registers).
+template <int N>
+__device__ __forceinline__ void tiny_scale_divide(float (&v)[N], float d, float& id)
+{
+    if (isinf(id)) {
+#pragma unroll
+        for (int k = 0; k < N; ++k) v[k] = __fdiv_rn(v[k], d);
+        id = 1.f;
+    }
+}
+template <int N>
+__device__ __forceinline__ void tiny_scale_divide(float4 (&v)[N], float d, float& id)
+{
+    if (isinf(id)) {
+#pragma unroll
+        for (int k = 0; k < N; ++k)
+            v[k] = make_float4(__fdiv_rn(v[k].x, d), __fdiv_rn(v[k].y, d), __fdiv_rn(v[k].z, d),
+                               __fdiv_rn(v[k].w, d));
+        id = 1.f;
+    }
 }
 
 // ---- programmatic dependent launch ----------------------------------------------

@@ -27,6 +27,8 @@
 // depends only on the row, never on how many vectors share the pass.
 #pragma once
 
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace qmv {
@@ -535,16 +537,27 @@ __device__ __forceinline__ void stage_quant32(uint8_t* codes, float* d, uint8_t*
             float dd, id;
             act_scale(amax, dd, id);
             uint8_t* dst = codes + (size_t)i * (NATURAL ? 32 : kBPitch);
-            int sum = 0;
-            for (int k = 0; k < 8; ++k) {
-                const float4 w = xp[k];
-                const int8_t q0 = quant1(w.x, dd, id), q1 = quant1(w.y, dd, id), q2 = quant1(w.z, dd, id), q3 = quant1(w.w, dd, id);
-                dst[NATURAL ? 4 * k + 0 : staged_pos<T>(4 * k + 0)] = (uint8_t)q0;
-                dst[NATURAL ? 4 * k + 1 : staged_pos<T>(4 * k + 1)] = (uint8_t)q1;
-                dst[NATURAL ? 4 * k + 2 : staged_pos<T>(4 * k + 2)] = (uint8_t)q2;
-                dst[NATURAL ? 4 * k + 3 : staged_pos<T>(4 * k + 3)] = (uint8_t)q3;
-                sum += q0 + q1 + q2 + q3;
-            }
+            // The quantising pass, in two copies so that the common one holds
+            // no division: TINY for the rare block whose 1/d overflows (its
+            // codes are round(x / d), see tiny_scale_divide).
+            auto pass = [&](auto tiny) {
+                int sum = 0;
+                for (int k = 0; k < 8; ++k) {
+                    float4 wv[1] = {xp[k]};
+                    float idk = id;
+                    if constexpr (decltype(tiny)::value) tiny_scale_divide(wv, dd, idk);
+                    const float4 w = wv[0];
+                    const int8_t q0 = quant1(w.x, idk), q1 = quant1(w.y, idk), q2 = quant1(w.z, idk),
+                                 q3 = quant1(w.w, idk);
+                    dst[NATURAL ? 4 * k + 0 : staged_pos<T>(4 * k + 0)] = (uint8_t)q0;
+                    dst[NATURAL ? 4 * k + 1 : staged_pos<T>(4 * k + 1)] = (uint8_t)q1;
+                    dst[NATURAL ? 4 * k + 2 : staged_pos<T>(4 * k + 2)] = (uint8_t)q2;
+                    dst[NATURAL ? 4 * k + 3 : staged_pos<T>(4 * k + 3)] = (uint8_t)q3;
+                    sum += q0 + q1 + q2 + q3;
+                }
+                return sum;
+            };
+            const int sum = isinf(id) ? pass(std::true_type{}) : pass(std::false_type{});
             d[i] = __half2float(__float2half_rn(dd));   // Q8_0 keeps its scale in fp16
             reinterpret_cast<int*>(tail)[i] = sum;
         }
@@ -571,12 +584,13 @@ __device__ __forceinline__ void stage_quant32(uint8_t* codes, float* d, uint8_t*
         for (int o = 1; o < TPB; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         float dd, id;
         act_scale(amax, dd, id);
+        tiny_scale_divide(w, dd, id);
         uint8_t* dst = codes + (size_t)blk * (NATURAL ? 32 : kBPitch);
         int sum = 0;
 #pragma unroll
         for (int f = 0; f < NF4; ++f) {
-            const int8_t q0 = quant1(w[f].x, dd, id), q1 = quant1(w[f].y, dd, id), q2 = quant1(w[f].z, dd, id),
-                         q3 = quant1(w[f].w, dd, id);
+            const int8_t q0 = quant1(w[f].x, id), q1 = quant1(w[f].y, id), q2 = quant1(w[f].z, id),
+                         q3 = quant1(w[f].w, id);
             sum += q0 + q1 + q2 + q3;
             const int e = part * E + 4 * f;
             if (!valid) continue;
@@ -626,13 +640,14 @@ __device__ __forceinline__ void stage_quant256(uint8_t* codes, float* d, uint8_t
         for (int o = 1; o < TPB; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         float dd, id;
         act_scale(amax, dd, id);
+        tiny_scale_divide(w, dd, id);
         uint8_t* dst = codes + (size_t)blk * (NATURAL ? 256 : kKPitch);
         int16_t* bsum = reinterpret_cast<int16_t*>(tail) + (size_t)blk * 16;
         int s16 = 0;   // running sum of the current 16-group
 #pragma unroll
         for (int f = 0; f < NF4; ++f) {
-            const int8_t q0 = quant1(w[f].x, dd, id), q1 = quant1(w[f].y, dd, id), q2 = quant1(w[f].z, dd, id),
-                         q3 = quant1(w[f].w, dd, id);
+            const int8_t q0 = quant1(w[f].x, id), q1 = quant1(w[f].y, id), q2 = quant1(w[f].z, id),
+                         q3 = quant1(w[f].w, id);
             s16 += q0 + q1 + q2 + q3;
             const int e = part * E + 4 * f, r = e >> 4;
             if (valid)

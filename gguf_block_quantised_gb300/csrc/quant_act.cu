@@ -23,11 +23,12 @@ __global__ void k_quant_q8_0(const float* __restrict__ x, uint8_t* __restrict__ 
     pdl_trigger();
     pdl_wait();
     if (b >= nblk) return;
-    const float v = x[b * 32 + lane];
-    const float amax = warp_max(fabsf(v));
+    float v[1] = {x[b * 32 + lane]};
+    const float amax = warp_max(fabsf(v[0]));
     float d, id;
     act_scale(amax, d, id);
-    const int8_t q = quant1(v, d, id);
+    tiny_scale_divide(v, d, id);
+    const int8_t q = quant1(v[0], id);
     uint8_t* o = out + b * 34;
     o[2 + lane] = (uint8_t)q;
     if (lane == 0) *reinterpret_cast<__half*>(o) = __float2half_rn(d);
@@ -43,18 +44,19 @@ __global__ void k_quant_q8_k(const float* __restrict__ x, uint8_t* __restrict__ 
     if (b >= nblk) return;
     const float4* xp = reinterpret_cast<const float4*>(x + b * 256 + lane * 8);
     const float4 a = xp[0], c = xp[1];
-    const float v[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+    float v[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
     float m = 0.f;
 #pragma unroll
     for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(v[k]));
     const float amax = warp_max(m);
     float d, id;
     act_scale(amax, d, id);
+    tiny_scale_divide(v, d, id);
     uint32_t w0 = 0, w1 = 0;
     int s = 0;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-        const int8_t q = quant1(v[k], d, id);
+        const int8_t q = quant1(v[k], id);
         s += q;
         if (k < 4) w0 |= (uint32_t)(uint8_t)q << (8 * k);
         else w1 |= (uint32_t)(uint8_t)q << (8 * (k - 4));

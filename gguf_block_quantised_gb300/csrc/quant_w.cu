@@ -32,7 +32,7 @@ __global__ void __launch_bounds__(256) k_quant_w(const float4* __restrict__ x, u
     const int part = (int)(i & 7);
     const bool valid = blk < nblk;           // the same for the eight lanes of a block
     const float4 w = valid ? x[i] : make_float4(0.f, 0.f, 0.f, 0.f);
-    const float v[4] = {w.x, w.y, w.z, w.w};
+    float v[4] = {w.x, w.y, w.z, w.w};
 
     // The first element of largest magnitude: strictly larger magnitudes win,
     // and among equal ones the lower index (an all-zero block keeps +0).
@@ -57,12 +57,12 @@ __global__ void __launch_bounds__(256) k_quant_w(const float4* __restrict__ x, u
         }
     }
     const float d = __fdiv_rn(m, -kHalf);
-    const float id = d == 0.f ? 0.f : __fdiv_rn(1.f, d);
+    float id = d == 0.f ? 0.f : __fdiv_rn(1.f, d);
+    tiny_scale_divide(v, d, id);   // |d| below 2^-128: the codes come from x / d
     uint32_t codes = 0, hi_bits = 0;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        const float u = isinf(id) ? __fdiv_rn(v[k], d) : __fmul_rn(v[k], id);   // block-uniform branch
-        float t = __fadd_rn(u, kHalf + 0.5f);
+        float t = __fadd_rn(__fmul_rn(v[k], id), kHalf + 0.5f);
         t = fmaxf(fminf(t, kTop), 0.f);
         const uint32_t c = (uint32_t)__float2int_rz(t);
         codes |= (c & 15u) << (8 * k);
