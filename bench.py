@@ -474,43 +474,58 @@ def kquant_decode_leg(q, torch, stream, hbm):
 
 
 def prefill_leg(q, torch, stream, tflops_peak):
-    """Q4_K prefill GEMMs (bf16 activations, tcgen05): 14336x4096 and 4096x14336
-    at M = 512 and 2048.  Four (W, X) copies rotate so that every launch reads
-    its operands from HBM (> L2 in total)."""
-    out = {}
-    tot_flop, tot_ms = 0.0, 0.0
+    """Q4_K prefill GEMMs on the tensor cores (tcgen05): 14336x4096 and
+    4096x14336 at M = 512 and 2048, with bf16 activations (weights dequantised
+    to bf16) and with Q8_K activations (W4A8: exact integer block dots on fp16
+    operands, plus its activation pre-pass).  Four (W, X) copies rotate so that
+    every launch reads its operands from HBM (> L2 in total).  Both report
+    2*M*rows*cols flops over the kernel time against the measured dense bf16
+    peak (fp16 runs at the bf16 rate)."""
+    out = {"bf16": {}, "w4a8": {}}
+    tot = {"bf16": [0.0, 0.0], "w4a8": [0.0, 0.0]}
+    ws = None
     for rows, cols in ((14336, 4096), (4096, 14336)):
         Ws = [torch.from_numpy(synth.weights(Q4_K, rows, cols, seed=4, tensor_id=rows + i)).cuda() for i in range(4)]
         for m in (512, 2048):
+            flop = 2.0 * m * rows * cols
             Xs = [torch.randn(m, cols, device="cuda").to(torch.bfloat16) for _ in range(4)]
             Y = torch.empty(m, rows, device="cuda")
             calls = [(lambda s, W=W, X=X: q.qmv_matmul(q.FMT(Q4_K, BF16), W, rows, cols, X, Y, m, s.cuda_stream))
                      for W, X in zip(Ws, Xs)]
             ms = time_rotating(torch, stream, calls, 40)
-            flop = 2.0 * m * rows * cols
-            out[f"{rows}x{cols}_m{m}"] = {"ms": ms, "tflops": flop / (ms / 1e3) / 1e12,
-                                         "frac_of_peak": flop / (ms / 1e3) / 1e12 / tflops_peak}
-            tot_flop += flop
-            tot_ms += ms
-            del Xs, Y
+            out["bf16"][f"{rows}x{cols}_m{m}"] = {"ms": ms, "tflops": flop / (ms / 1e3) / 1e12,
+                                                 "frac_of_peak": flop / (ms / 1e3) / 1e12 / tflops_peak}
+            tot["bf16"][0] += flop
+            tot["bf16"][1] += ms
+            del Xs
+            Xq = []
+            for _ in range(4):
+                xq = torch.empty(m * q.qmv_row_bytes(Q8_K, cols), dtype=torch.uint8, device="cuda")
+                q.qmv_quantize_act(Q8_K, torch.randn(m, cols, device="cuda"), xq, m * cols)
+                Xq.append(xq)
+            need = q.qmv_workspace_size(q.OP_MATMUL, q.FMT(Q4_K, Q8_K), rows, cols, m)
+            if ws is None or ws.numel() < need:
+                ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+            q.qmv_set_workspace(ws, ws.numel())
+            calls = [(lambda s, W=W, X=X: q.qmv_matmul(q.FMT(Q4_K, Q8_K), W, rows, cols, X, Y, m, s.cuda_stream))
+                     for W, X in zip(Ws, Xq)]
+            ms = time_rotating(torch, stream, calls, 40)
+            q.qmv_set_workspace(None, 0)
+            out["w4a8"][f"{rows}x{cols}_m{m}"] = {"ms": ms, "tflops": flop / (ms / 1e3) / 1e12,
+                                                 "frac_of_peak": flop / (ms / 1e3) / 1e12 / tflops_peak}
+            tot["w4a8"][0] += flop
+            tot["w4a8"][1] += ms
+            del Xq, Y
         del Ws
-    # W4A8 (Q8_K activations): exact integer path, one shape
-    rows, cols, m = 14336, 4096, 512
-    Ws = [torch.from_numpy(synth.weights(Q4_K, rows, cols, seed=4, tensor_id=rows + i)).cuda() for i in range(4)]
-    x = torch.randn(m, cols, device="cuda")
-    Xq = torch.empty(m * q.qmv_row_bytes(Q8_K, cols), dtype=torch.uint8, device="cuda")
-    q.qmv_quantize_act(Q8_K, x, Xq, m * cols)
-    Y = torch.empty(m, rows, device="cuda")
-    calls = [(lambda s, W=W: q.qmv_matmul(q.FMT(Q4_K, Q8_K), W, rows, cols, Xq, Y, m, s.cuda_stream)) for W in Ws]
-    ms = time_rotating(torch, stream, calls, 8)
-    w4a8 = {"shape": f"{rows}x{cols}_m{m}", "ms": ms, "tflops": 2.0 * m * rows * cols / (ms / 1e3) / 1e12,
-            "path": "exact int8 block dots on mma.sync.m16n8k32 (the decode pipeline over 16-token groups)"}
-    del Ws, Xq, Y
     q.qmv_get_status(stream)
-    return {"metric": "prefill GEMM TFLOP/s (Q4_K x bf16, fp32 accumulate)", "unit": "TFLOP/s", "w4a8": w4a8,
-            "value": tot_flop / (tot_ms / 1e3) / 1e12, "peak": tflops_peak,
-            "frac": tot_flop / (tot_ms / 1e3) / 1e12 / tflops_peak, "shapes": out,
-            "kernel": "k_gemm_q4k_bf16 (tcgen05.mma kind::f16, M=128 rows x N=256 tokens, TMEM accumulator)"}
+    agg = {k: tot[k][0] / (tot[k][1] / 1e3) / 1e12 for k in tot}
+    return {"metric": "prefill GEMM TFLOP/s (Q4_K weights; bf16 and W4A8 activations, fp32 accumulate)",
+            "unit": "TFLOP/s", "value": agg["bf16"], "frac": agg["bf16"] / tflops_peak,
+            "w4a8_value": agg["w4a8"], "w4a8_frac": agg["w4a8"] / tflops_peak, "peak": tflops_peak,
+            "shapes": out["bf16"], "w4a8": out["w4a8"],
+            "kernels": {"bf16": "k_gemm_q4k_bf16 (tcgen05.mma kind::f16 bf16, M=128 rows x N=256 tokens, A in TMEM)",
+                        "w4a8": "k_w4a8_prep + k_gemm_q4k_w4a8 (tcgen05.mma kind::f16 on fp16 integer operands, "
+                                "M=128 x N=128, S and Mn drained per super-block)"}}
 
 
 def moe_leg(q, torch, stream, hbm):
@@ -580,6 +595,7 @@ def run_probe(spec):
     """Single-kernel runs for profiling (ncu captures).  Specs:
       gemv:T:rows:cols:atype:n_vec   qmv_matvec on synthetic weights (atype 8 = fp32)
       gemm:rows:cols:m               qmv_matmul, Q4_K x bf16
+      gemm8:rows:cols:m              qmv_matmul, Q4_K x Q8_K (W4A8, with its activation pre-pass)
       step[:n_vec]                   one fused decode step of the Qwen2.5-0.5B shape (97 matvecs)
       moe:n_tok[:atype[:repacked]]   one gpt-oss-shaped MoE layer (gate_up + down); atype 3 = Q8_0
                                      quantised in-kernel (default), 9 = bf16 (grouped tensor-core GEMM);
@@ -609,6 +625,17 @@ def run_probe(spec):
         X = torch.randn(m, cols, device="cuda").to(torch.bfloat16)
         Y = torch.empty(m, rows, device="cuda")
         call = lambda: q.qmv_matmul(q.FMT(Q4_K, BF16), W, rows, cols, X, Y, m)
+        nbytes, what = 2 * m * rows * cols / 1e3, "TFLOP/s"
+    elif kind == "gemm8":
+        rows, cols, m = a
+        W = torch.from_numpy(synth.weights(Q4_K, rows, cols, seed=1)).cuda()
+        X = torch.empty(m * q.qmv_row_bytes(Q8_K, cols), dtype=torch.uint8, device="cuda")
+        q.qmv_quantize_act(Q8_K, torch.randn(m, cols, device="cuda"), X, m * cols)
+        Y = torch.empty(m, rows, device="cuda")
+        ws = torch.empty(q.qmv_workspace_size(q.OP_MATMUL, q.FMT(Q4_K, Q8_K), rows, cols, m), dtype=torch.uint8,
+                         device="cuda")
+        q.qmv_set_workspace(ws, ws.numel())
+        call = lambda: q.qmv_matmul(q.FMT(Q4_K, Q8_K), W, rows, cols, X, Y, m)
         nbytes, what = 2 * m * rows * cols / 1e3, "TFLOP/s"
     elif kind == "step":
         (n_vec,) = (a + [1])[:1]

@@ -33,7 +33,9 @@ QMV_GEMV_DECL(qmv_gemv_q8_0)
 QMV_GEMV_DECL(qmv_gemv_mxfp4)
 QMV_GEMV_DECL(qmv_gemv_q4_k)
 QMV_GEMV_DECL(qmv_gemv_q6_k)
-int qmv_gemm_mma_q4_k(bool pdl, const void* W, int64_t rows, int64_t cols, const void* X, float* Y, int m, cudaStream_t st);
+size_t qmv_w4a8_workspace_bytes(int64_t cols, int64_t m);
+int qmv_launch_gemm_q4k_w4a8(const void* W, int64_t rows, int64_t cols, const void* X, float* Y, int64_t m,
+                             void* ws, bool pdl, cudaStream_t st);
 size_t qmv_moe_workspace_bytes(bool bf16, int64_t rows, int64_t cols, int64_t n_pairs);
 int qmv_launch_repack_mxfp4(const void* W, int64_t rows, int64_t cols, void* Wout, cudaStream_t st);
 int qmv_launch_moe(int wtype, bool a8, bool quant_x, bool bf16, size_t act_block_bytes, const void* W3d,
@@ -413,10 +415,24 @@ int qmv_matmul(int fmt, const void* W, int64_t rows, int64_t cols, const void* X
     if (!aligned(Y, 4)) return fail(QMV_ERR_ALIGN, "Y must be 4-byte aligned");
     if (!qmv::status_word()) return cuda_fail("qmv_matmul (status word)");
     if (atype == QMV_Q8_K) {
-        // W4A8: exact per-super-block integer dots on the int8 tensor path
-        // (mma.sync), token groups of 16 (Y[m][rows] has the matvec's layout).
-        rc = qmv_gemm_mma_q4_k(pdl, W, rows, cols, X, Y, (int)m, static_cast<cudaStream_t>(stream));
-        if (rc == -2) return fail(QMV_ERR_SHAPE, "cols = %lld needs more shared memory than one SM has", (long long)cols);
+        // W4A8: exact integer block dots on the tensor cores (fp16 operands that
+        // hold the integer codes exactly), after a pre-pass that lays the
+        // activation codes out as fp16 in the workspace.
+        const size_t need = qmv_w4a8_workspace_bytes(cols, m);
+        void* ws = nullptr;
+        size_t have = 0;
+        const int d = qmv::current_device();
+        if (d >= 0 && d < qmv::kMaxDevices) {
+            std::lock_guard<std::mutex> lock(g_ws_mu);
+            ws = g_ws[d].ptr;
+            have = g_ws[d].bytes;
+        }
+        if (!ws || have < need)
+            return fail(QMV_ERR_WORKSPACE,
+                        "qmv_matmul (W4A8) needs %zu bytes of workspace (qmv_workspace_size(QMV_OP_MATMUL, ...)); "
+                        "%zu set", need, have);
+        rc = qmv_launch_gemm_q4k_w4a8(W, rows, cols, X, Y, m, ws, pdl, static_cast<cudaStream_t>(stream));
+        if (rc == -8) return fail(QMV_ERR_CUDA, "qmv_matmul: could not build a TMA tensor map");
         if (rc) return cuda_fail("qmv_matmul");
         return ok();
     }
@@ -451,6 +467,9 @@ size_t qmv_workspace_size(int op, int fmt, int64_t rows, int64_t cols, int64_t n
 {
     if (op == QMV_OP_MOE && rows > 0 && n > 0 && cols >= 0)
         return qmv_moe_workspace_bytes(((fmt >> 8) & 0xff) == QMV_BF16, rows, cols, n);
+    if (op == QMV_OP_MATMUL && (fmt & 0xffff) == QMV_FMT(QMV_Q4_K, QMV_Q8_K) && rows > 0 && n > 0 && cols > 0 &&
+        cols % 256 == 0)
+        return qmv_w4a8_workspace_bytes(cols, n);
     return 0;
 }
 

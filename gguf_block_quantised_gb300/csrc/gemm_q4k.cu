@@ -31,7 +31,7 @@
 #include <cuda.h>
 
 #include "formats.cuh"
-#include "mma_units.cuh"
+#include "q4k_fields.cuh"
 #include "runtime.cuh"
 #include "tc.cuh"
 

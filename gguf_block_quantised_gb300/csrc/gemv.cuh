@@ -55,9 +55,6 @@ struct GemvParams {
     int n_chunks;
     int stages;
     int rpw;            // rows per consumer warp per tile (1, 2 or 4)
-    int wk;             // tensor-core engine: K-splits per 16-row group (1, 2, 4 or 8)
-    int contig;         // whole rows per stage: one bulk copy moves the tile's consecutive rows
-    uint32_t stage_bytes;
     int quant_x;        // A8 only: x is fp32, quantised while staging
     uint32_t seg_cap;   // bytes per row slot of a stage
     uint32_t xhat_bytes;
@@ -69,60 +66,31 @@ __device__ __forceinline__ int64_t ceil16(int64_t v) { return (v + 15) & ~int64_
 
 // Producer warp: arm `bar` and issue the bulk copies of one work item (tile,
 // chunk): lane i copies row i's chunk (its 16-byte aligned superset) into its
-// slot (WIDE: tiles of up to 128 rows, lane i copies rows i, i+32, ...; or,
-// with p.contig, lane 0 copies the tile's consecutive whole rows at once).
-// The ragged end of the matrix past its last 16-byte boundary is stored with
-// plain loads before the arrive, whose release orders them for the consumers.
-// The decode kernels use the narrow form, whose code stays lean.
-template <int BB, bool WIDE = false>
+// slot.  The ragged end of the matrix past its last 16-byte boundary is stored
+// with plain loads before the arrive, whose release orders them for the
+// consumers.
+template <int BB>
 __device__ __forceinline__ void gemv_produce(const GemvParams& p, int64_t tile, int chunk, uint8_t* buf,
-                                             uint64_t* bar, int tr = 0)
+                                             uint64_t* bar)
 {
-    constexpr int RPL = WIDE ? 4 : 1;   // rows per lane
     const int lane = threadIdx.x & 31;
-    if (tr == 0) tr = kConsumerWarps * p.rpw;
+    const int tr = kConsumerWarps * p.rpw;
     const int64_t lim = floor16(p.total);
-    if (WIDE && p.contig) {
-        // Rows r0 .. r1-1 are one byte range: copy its 16-byte aligned superset
-        // at once (the ragged end of the matrix with plain loads).
-        if (lane == 0) {
-            const int64_t r0 = tile * tr;
-            const int64_t r1 = min(p.rows, r0 + tr);
-            const int64_t s0 = r0 * p.rb, e = r1 * p.rb;
-            const int64_t a0 = floor16(s0);
-            const int64_t ea = min(ceil16(e), lim);
-            const uint32_t bytes = ea > a0 ? (uint32_t)(ea - a0) : 0u;
-            for (int64_t k = max(lim, a0); k < e; ++k) buf[k - a0] = p.W[k];
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            mbar_arrive_expect_tx(bar, bytes);
-            if (bytes) bulk_g2s(buf, p.W + a0, bytes, bar);
-        }
-        __syncwarp();
-        return;
-    }
     const int c0 = chunk * p.kb;
     const int c1 = min(p.nb, c0 + p.kb);
-    uint32_t bytes[RPL];
-    int64_t a[RPL];
-#pragma unroll
-    for (int j = 0; j < RPL; ++j) {
-        bytes[j] = 0;
-        a[j] = 0;
-        const int i = lane + 32 * j;
-        const int64_t r = tile * tr + i;
-        if (i < tr && r < p.rows) {
-            const int64_t s = r * p.rb + (int64_t)c0 * BB;
-            const int64_t e = r * p.rb + (int64_t)c1 * BB;
-            a[j] = floor16(s);
-            const int64_t ea = min(ceil16(e), lim);
-            if (ea > a[j]) bytes[j] = (uint32_t)(ea - a[j]);
-            uint8_t* slot = buf + (size_t)i * p.seg_cap;
-            for (int64_t k = max(lim, a[j]); k < e; ++k) slot[k - a[j]] = p.W[k];   // only the matrix's last row
-        }
+    uint32_t bytes = 0;
+    int64_t a = 0;
+    const int64_t r = tile * tr + lane;
+    if (lane < tr && r < p.rows) {
+        const int64_t s = r * p.rb + (int64_t)c0 * BB;
+        const int64_t e = r * p.rb + (int64_t)c1 * BB;
+        a = floor16(s);
+        const int64_t ea = min(ceil16(e), lim);
+        if (ea > a) bytes = (uint32_t)(ea - a);
+        uint8_t* slot = buf + (size_t)lane * p.seg_cap;
+        for (int64_t k = max(lim, a); k < e; ++k) slot[k - a] = p.W[k];   // only the matrix's last row
     }
-    uint32_t total = 0;
-#pragma unroll
-    for (int j = 0; j < RPL; ++j) total += bytes[j];
+    uint32_t total = bytes;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
     // Order this buffer's earlier generic-proxy accesses (consumer reads,
@@ -131,9 +99,7 @@ __device__ __forceinline__ void gemv_produce(const GemvParams& p, int64_t tile, 
     __syncwarp();
     if (lane == 0) mbar_arrive_expect_tx(bar, total);
     __syncwarp();
-#pragma unroll
-    for (int j = 0; j < RPL; ++j)
-        if (bytes[j]) bulk_g2s(buf + (size_t)(lane + 32 * j) * p.seg_cap, p.W + a[j], bytes[j], bar);
+    if (bytes) bulk_g2s(buf + (size_t)lane * p.seg_cap, p.W + a, bytes, bar);
 }
 
 // Consumer: rows r0 + j (j < RIF) of one warp, one K-chunk, all vectors.
@@ -345,8 +311,7 @@ __global__ void __launch_bounds__(kGemvThreads, two_ctas_per_sm<T, A8, NV>() ? 2
 
 // ---- host side -------------------------------------------------------------------
 struct GemvPlan {
-    int kb, n_chunks, stages, group, grid, rpw, wk, contig;
-    uint32_t stage_bytes;
+    int kb, n_chunks, stages, group, grid, rpw;
     uint32_t seg_cap, xhat_bytes, smem;
 };
 

@@ -2,7 +2,6 @@
 #pragma once
 
 #include "gemv.cuh"
-#include "gemv_mma.cuh"
 #include "moe.cuh"
 #include "runtime.cuh"
 
@@ -131,104 +130,6 @@ inline int launch_gemv_group(const GemvParams& p, const GemvPlan& pl, bool pdl, 
     return launch_gemv_nv<T, A8, 16>(p, pl, pdl, st);
 }
 
-// ---- the tensor-core (int8 mma.sync) engine for 8-bit activations -----------------
-// Tile geometry depends on the matrix shape only (never on the vector count), so
-// the reduction order of every output is fixed: wk K-splits per 16-row group,
-// 128/wk rows per tile, K-chunks of kb blocks (about 32 KB per stage).
-template <int T>
-inline bool plan_gemv_mma(int64_t rows, int64_t cols, int n_vec, GemvPlan& pl)
-{
-    using F = Fmt<T>;
-    const int nb = (int)(cols / F::BS);
-    const int64_t rb = (int64_t)nb * F::BB;
-    int tr;
-    if (rb <= 4096) {
-        // Whole rows: a tile's rows are one byte range, moved by one bulk copy.
-        pl.kb = nb;
-        tr = 128;
-        while (tr > 16 && (int64_t)tr * rb > 32768) tr /= 2;
-        while (tr > 16 && (rows + tr - 1) / tr < 2 * num_sms()) tr /= 2;
-        pl.contig = 1;
-    } else {
-        // Long rows: 16-row tiles of ~2 KB row segments.
-        int kb = (2048 + F::BB - 1) / F::BB;
-        pl.kb = kb < nb ? kb : nb;
-        tr = 16;
-        pl.contig = 0;
-    }
-    pl.wk = 128 / tr;
-    pl.n_chunks = (nb + pl.kb - 1) / pl.kb;
-    pl.seg_cap = (uint32_t)(((size_t)pl.kb * F::BB + 48 + 15) & ~size_t(15));
-    pl.rpw = tr / kConsumerWarps;
-    const size_t stage = (size_t)pl.seg_cap * tr;   // covers tr*rb + 32 in the contiguous mode
-    pl.stage_bytes = (uint32_t)stage;
-    int g = n_vec < 16 ? n_vec : 16;
-    if (g < 1) g = 1;
-    for (;; --g) {
-        const size_t xb = xhat_bytes(T, true, g, (int)cols);
-        const size_t base = 256 + 8192 + ((xb + 127) & ~size_t(127));
-        int S = base < kSmemTwoPerSm ? (int)((kSmemTwoPerSm - base) / stage) : 0;
-        if (S < 3) S = base < kSmemOnePerSm ? (int)((kSmemOnePerSm - base) / stage) : 0;
-        if (S >= 2 || g == 1) {
-            if (S < 2) return false;
-            if (S > kMaxStages) S = kMaxStages;
-            pl.group = g;
-            pl.xhat_bytes = (uint32_t)xb;
-            pl.stages = S;
-            pl.smem = (uint32_t)(base + S * stage);
-            return true;
-        }
-    }
-}
-
-template <int T, int NT>
-inline int launch_gemv_mma_nt(const GemvParams& p, const GemvPlan& pl, bool pdl, cudaStream_t st)
-{
-    auto* k = &k_gemv_mma<T, NT>;
-    const int occ = prepare_kernel(k, kGemvThreads, pl.smem);
-    const int64_t tr = 128 / pl.wk;
-    const int64_t n_tiles = (p.rows + tr - 1) / tr;
-    int64_t grid = (int64_t)num_sms() * occ;
-    if (grid > n_tiles) grid = n_tiles;
-    return launch_ex(k, dim3((unsigned)grid), dim3(kGemvThreads), pl.smem, st, pdl, p) == cudaSuccess ? 0 : -6;
-}
-
-template <int T>
-inline int launch_gemv_mma_t(bool quant_x, bool pdl, const void* W, int64_t rows, int64_t cols, const void* x,
-                             float* y, int n_vec, cudaStream_t st)
-{
-    using F = Fmt<T>;
-    GemvPlan pl;
-    if (!plan_gemv_mma<T>(rows, cols, n_vec, pl)) return -2;
-    GemvParams p{};
-    p.W = static_cast<const uint8_t*>(W);
-    p.rows = rows;
-    p.nb = (int)(cols / F::BS);
-    p.rb = (int64_t)p.nb * F::BB;
-    p.total = rows * p.rb;
-    p.cols = (int)cols;
-    p.kb = pl.kb;
-    p.n_chunks = pl.n_chunks;
-    p.stages = pl.stages;
-    p.seg_cap = pl.seg_cap;
-    p.rpw = pl.rpw;
-    p.wk = pl.wk;
-    p.contig = pl.contig;
-    p.stage_bytes = pl.stage_bytes;
-    p.quant_x = quant_x ? 1 : 0;
-    p.xhat_bytes = pl.xhat_bytes;
-    p.status = status_word();
-    const size_t xrow = quant_x ? (size_t)cols * 4 : (size_t)p.nb * act_block_bytes(T);
-    for (int v0 = 0; v0 < n_vec; v0 += pl.group) {
-        p.nv = min(pl.group, n_vec - v0);
-        p.x = static_cast<const uint8_t*>(x) + (size_t)v0 * xrow;
-        p.y = y + (int64_t)v0 * rows;
-        const int rc = p.nv <= 8 ? launch_gemv_mma_nt<T, 1>(p, pl, pdl, st) : launch_gemv_mma_nt<T, 2>(p, pl, pdl, st);
-        if (rc) return rc;
-    }
-    return 0;
-}
-
 // Returns 0, -2 (shape beyond the shared-memory plan) or -6 (launch failure).
 // quant_x: A8 from fp32 activations quantised in the kernel.  pdl: launch as a
 // programmatic dependent of the previous kernel on the stream.
@@ -254,10 +155,8 @@ inline int launch_gemv_t(bool a8, bool quant_x, bool pdl, const void* W, int64_t
     p.stages = pl.stages;
     p.seg_cap = pl.seg_cap;
     p.rpw = pl.rpw;
-    // One bulk copy per row (into its own slot) streams faster here than one
-    // large copy of a whole tile of consecutive rows (measured on the lm_head).
-    p.contig = 0;
-    p.stage_bytes = pl.seg_cap * (uint32_t)(kConsumerWarps * pl.rpw);
+    // One bulk copy per row (into its own slot): measured faster on the lm_head
+    // than one large copy of a whole tile of consecutive rows.
     p.quant_x = quant_x ? 1 : 0;
     p.xhat_bytes = pl.xhat_bytes;
     p.status = status_word();
@@ -317,8 +216,6 @@ inline int launch_moe_t(bool a8, bool quant_x, const void* W3d, int n_expert, in
     p.stages = pl.stages;
     p.seg_cap = pl.seg_cap;
     p.rpw = pl.rpw;
-    p.contig = 0;
-    p.stage_bytes = pl.seg_cap * (uint32_t)(kConsumerWarps * pl.rpw);
     p.quant_x = quant_x ? 1 : 0;
     p.xhat_bytes = pl.xhat_bytes;
     p.status = status_word();
@@ -358,14 +255,6 @@ inline int launch_moe_t(bool a8, bool quant_x, const void* W3d, int n_expert, in
     {                                                                                                           \
         return qmv::launch_moe_t<T>(a8, quant_x, W3d, n_expert, rows, cols, offsets, active, perm, n_pairs, x, \
                                     xrow, kdiv, out, bias, st);                                                 \
-    }
-
-// The W4A8 prefill on the int8 tensor path (mma.sync): token groups of 16.
-#define QMV_GEMM_MMA_INSTANTIATE(T, NAME)                                                                   \
-    int NAME(bool pdl, const void* W, int64_t rows, int64_t cols, const void* X, float* Y, int m,              \
-             cudaStream_t st)                                                                                  \
-    {                                                                                                          \
-        return qmv::launch_gemv_mma_t<T>(false, pdl, W, rows, cols, X, Y, m, st);                              \
     }
 
 #define QMV_GEMV_INSTANTIATE(T, NAME)                                                                     \

@@ -4,4 +4,3 @@
 
 QMV_GEMV_INSTANTIATE(QMV_Q4_K, qmv_gemv_q4_k)
 QMV_MOE_INSTANTIATE(QMV_Q4_K, qmv_moe_q4_k)
-QMV_GEMM_MMA_INSTANTIATE(QMV_Q4_K, qmv_gemm_mma_q4_k)

@@ -51,7 +51,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_moe_gemv(const MoeParams mp
     volatile int* abort_flag = xrow_of + 16;
     uint8_t* xs = smem + 512;
     uint8_t* stage0 = xs + ((p.xhat_bytes + 127) & ~127u);
-    const uint32_t stage_bytes = p.stage_bytes;
+    const uint32_t stage_bytes = p.seg_cap * (uint32_t)(kConsumerWarps * p.rpw);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int my_tiles = (int)((n_tiles - 1 - blockIdx.x) / gridDim.x) + 1;
@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_moe_gemv(const MoeParams mp
                         for (int v = 0; v < NV; ++v) acc[j][v] = 0.f;
                 }
                 gemv_rows<T, A8, NV, RIF>(p, X, buf + (size_t)(warp * p.rpw + g) * p.seg_cap, r0, nrows, c0, c1,
-                                          acc);   // MoE keeps per-row slots (p.contig = 0)
+                                          acc);
                 if (chunk == p.n_chunks - 1) {
                     const int row = RIF == 4 ? (lane >> 3) : (RIF == 2 ? (lane >> 4) : 0);
                     const bool writer = (lane & (32 / RIF - 1)) == 0;

@@ -57,6 +57,23 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(const void* p)
     return d;
 }
 
+// Shared-memory matrix descriptor for a K-major operand whose K extent is one
+// 32-byte row (16 fp16) in the 32-byte swizzled canonical layout: 8-row
+// groups 256 bytes apart, the two 16-byte halves of row r swapped when bit 2
+// of r % 8 is set.  Bits as above, layout 6 (32B swizzle).  The buffer starts
+// on a 256-byte boundary.
+__device__ __forceinline__ uint64_t smem_desc_sw32(const void* p)
+{
+    const uint64_t addr = smem_u32(p);
+    uint64_t d = 0;
+    d |= (addr >> 4) & 0x3fffull;
+    d |= 1ull << 16;
+    d |= (uint64_t)(256 >> 4) << 32;
+    d |= 1ull << 46;
+    d |= 6ull << 61;
+    return d;
+}
+
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B (or fp16
 // when f16 = true), both K-major, M x N.
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool f16 = false)

@@ -27,8 +27,8 @@
  *    stream).  Every call only enqueues work on that stream and returns; none
  *    synchronises.  Inputs must stay valid, and outputs must not be read, until
  *    the stream reaches the call.  Outputs must not alias inputs.
- *  - Calls allocate no device memory.  The mixture-of-experts call needs
- *    scratch, given once through qmv_set_workspace().
+ *  - Calls allocate no device memory.  The mixture-of-experts call and the
+ *    W4A8 prefill need scratch, given once through qmv_set_workspace().
  *  - Errors: every call validates its arguments on the host before launching
  *    and returns a negative qmv_status without launching anything on failure;
  *    qmv_last_error() then names what is supported (the pages' convention of
@@ -219,10 +219,16 @@ int qmv_matvec(int fmt, const void* W, int64_t rows, int64_t cols,
  *         dequantised to bf16 tiles (w rounded once from its fp32 value) and
  *         multiplied on the tensor cores with fp32 accumulation.
  *         QMV_FMT(QMV_Q4_K, QMV_Q8_K): X Q8_K blocks [m][cols/256] (W4A8):
- *         exact int32 sub-block dots on the int8 tensor path (mma.sync
- *         m16n8k32; tcgen05 has no int8 kind on sm_103a), sub-block scales
- *         applied in integers, fp32 accumulation per super-block.  Agrees with
- *         the W4A8 decode of each token within the accuracy bar above.
+ *         per super-block the integers S = sum sc*q*xq and Mn = sum m*bsum
+ *         come out of the tensor cores exactly (sm_103a has no tcgen05
+ *         integer kind; sc*q, xq, m and the sums of 16 are integers that fp16
+ *         holds exactly, so they run as fp16 operands with an fp32
+ *         accumulator), then d_x*(d*S - dmin*Mn) is accumulated in fp32.
+ *         Needs qmv_workspace_size(QMV_OP_MATMUL, fmt, rows, cols, m) bytes
+ *         of workspace (qmv_set_workspace): the activation codes laid out as
+ *         fp16, about m*cols*2.1 bytes; calls that share it must be ordered on
+ *         one stream.  Agrees with the W4A8 decode of each token within the
+ *         accuracy bar above.
  *         Either may be | QMV_FLAG_PDL (the W these kernels read must not be
  *         written by the kernels just before them on the stream).
  *   X   : 16-byte aligned.   Y : fp32 [m][rows], overwritten.
@@ -304,10 +310,13 @@ int qmv_moe_matvec_noalloc(int fmt, const void* W3d, int n_expert, int64_t rows,
 
 /* Workspace for the calls that need scratch. */
 enum { QMV_OP_MATVEC = 1, QMV_OP_MATMUL = 2, QMV_OP_MOE = 3 };
-/* Bytes of workspace `op` needs for these sizes (n = n_tok*k for MoE: the
- * grouping, 2050 + n ints, and n*rows fp32 slot outputs; with BF16
+/* Bytes of workspace `op` needs for these sizes.  QMV_OP_MOE, n = n_tok*k:
+ * the grouping, 2050 + n ints, and n*rows fp32 slot outputs; with BF16
  * activations also the GEMM's slot list, about 2n ints, and the n packed
- * bf16 activation rows, n*cols*2 bytes).  0 if none. */
+ * bf16 activation rows, n*cols*2 bytes.  QMV_OP_MATMUL with
+ * QMV_FMT(QMV_Q4_K, QMV_Q8_K), n = m tokens: the fp16 activation codes
+ * (m*cols*2), sums of 16 (m*cols/8) and scales (about m*cols/64 bytes).
+ * 0 if the call needs none. */
 size_t qmv_workspace_size(int op, int fmt, int64_t rows, int64_t cols, int64_t n);
 /* Register a caller-owned device buffer (256-byte aligned) as the workspace of
  * the current device; NULL/0 clears it.  The library keeps the pointer only. */

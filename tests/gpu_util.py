@@ -26,3 +26,19 @@ def assert_close(y, yref, yabs, tol=TOL, what=""):
         raise AssertionError(f"{what}: {bad.sum()} outputs out of tolerance; first at {tuple(i)}: "
                              f"y={y[tuple(i)]!r} ref={yref[tuple(i)]!r} sum|wx|={yabs[tuple(i)]!r}")
     return float((err / np.maximum(yabs, 1e-300)).max()) if err.size else 0.0
+
+
+class workspace:
+    """Register a device workspace of at least `nbytes` for the calls inside
+    the block (the mixture of experts, the W4A8 prefill); cleared on exit."""
+
+    def __init__(self, qmv, nbytes):
+        self.qmv, self.nbytes = qmv, max(int(nbytes), 256)
+
+    def __enter__(self):
+        self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device="cuda")
+        self.qmv.qmv_set_workspace(self.buf, self.buf.numel())
+        return self.buf
+
+    def __exit__(self, *exc):
+        self.qmv.qmv_set_workspace(None, 0)

@@ -55,44 +55,6 @@ static int check(const char* name, const int64_t* cols_list, int n_cols, int* ac
     return bad;
 }
 
-// The W4A8 prefill engine's plan (Q4_K): tiles of 16..128 rows, whole rows per
-// copy when a row is at most 4 KB.  Without a device num_sms() is 1, which
-// gives the largest tiles; the invariants do not depend on it.
-static int check_mma(int* accepted)
-{
-    using F = Fmt<QMV_Q4_K>;
-    const int64_t cols_list[] = {256, 512, 4096, 14336, 32768};
-    const int64_t rows_list[] = {1, 37, 4096, 14336};
-    const int ms[] = {1, 7, 16, 64, 512};
-    int bad = 0;
-    for (int64_t cols : cols_list)
-        for (int64_t rows : rows_list)
-            for (int m : ms) {
-                GemvPlan pl{};
-                if (!plan_gemv_mma<QMV_Q4_K>(rows, cols, m, pl)) continue;
-                ++*accepted;
-                const int nb = (int)(cols / F::BS);
-                const int64_t rb = (int64_t)nb * F::BB;
-                const int tr = 128 / pl.wk;
-                const size_t base = 256 + 8192 + (((size_t)pl.xhat_bytes + 127) & ~size_t(127));
-                auto fail = [&](const char* what) {
-                    std::printf("mma Q4_K rows=%lld cols=%lld m=%d: %s\n", (long long)rows, (long long)cols, m, what);
-                    ++bad;
-                };
-                if (tr != 16 && tr != 32 && tr != 64 && tr != 128) fail("tile height not 16..128");
-                if (pl.rpw * kConsumerWarps != tr) fail("rows per warp inconsistent with the tile");
-                if (pl.stages < 2 || pl.stages > kMaxStages) fail("stage count outside 2..8");
-                if (pl.smem != base + (size_t)pl.stages * pl.stage_bytes || pl.smem > kSmemOnePerSm)
-                    fail("shared memory wrong or over the limit");
-                if ((int64_t)pl.n_chunks * pl.kb < nb) fail("chunks do not cover the row");
-                if (pl.contig && (int64_t)pl.stage_bytes < (int64_t)tr * rb + 32)
-                    fail("a stage cannot hold a tile's whole rows");
-                if (!pl.contig && pl.seg_cap < (uint32_t)(pl.kb * F::BB + 30)) fail("row segment too small");
-                if (pl.group < 1 || pl.group > 16 || pl.group > m) fail("token group outside 1..16");
-            }
-    return bad;
-}
-
 int main()
 {
     const int64_t c32[] = {32, 96, 896, 2880, 4096, 4864, 8288, 14336, 32768, 65536};
@@ -104,7 +66,6 @@ int main()
     bad += check<QMV_MXFP4>("MXFP4", c32, 10, &accepted);
     bad += check<QMV_Q4_K>("Q4_K", c256, 6, &accepted);
     bad += check<QMV_Q6_K>("Q6_K", c256, 6, &accepted);
-    bad += check_mma(&accepted);
     std::printf("plans accepted %d, violations %d\n", accepted, bad);
     return bad ? 1 : 0;
 }

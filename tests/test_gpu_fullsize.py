@@ -17,7 +17,7 @@ import torch
 
 import oracle_pool as OP
 from gguf_block_quantised_gb300 import synth
-from gpu_util import assert_close, dev, host
+from gpu_util import assert_close, dev, host, workspace
 
 pytestmark = pytest.mark.gpu
 
@@ -75,8 +75,9 @@ def test_prefill_whole_14336x4096_m512(qmv, orc, at):
         x_o = orc.quantize_act(Q8_K, x)
         X = dev(x_o)
     Y = torch.full((m, rows), float("nan"), dtype=torch.float32, device="cuda")
-    qmv.qmv_matmul(qmv.FMT(Q4_K, at), dev(W), rows, cols, X, Y, m)
-    qmv.qmv_get_status()
+    with workspace(qmv, qmv.qmv_workspace_size(qmv.OP_MATMUL, qmv.FMT(Q4_K, at), rows, cols, m)):
+        qmv.qmv_matmul(qmv.FMT(Q4_K, at), dev(W), rows, cols, X, Y, m)
+        qmv.qmv_get_status()
     yref, yabs = OP.matvec(Q4_K, at, W, rows, cols, x_o, m)
     assert_close(host(Y), yref, yabs, what=f"prefill at={at}")
 

@@ -8,7 +8,7 @@ import pytest
 import torch
 
 from gguf_block_quantised_gb300 import synth
-from gpu_util import assert_close, dev, host
+from gpu_util import assert_close, dev, host, workspace
 
 pytestmark = pytest.mark.gpu
 
@@ -113,27 +113,69 @@ def test_matmul_edge_cases(qmv, orc):
 Q8_K = 7
 
 
-@pytest.mark.parametrize("rows,cols,m", [(128, 256, 1), (300, 1024, 37), (14336, 4096, 512)])
+def run_w4a8(qmv, Wd, rows, cols, xq_dev, m):
+    Y = torch.full((m, rows), float("nan"), dtype=torch.float32, device="cuda")
+    need = qmv.qmv_workspace_size(qmv.OP_MATMUL, qmv.FMT(Q4_K, Q8_K), rows, cols, m)
+    with workspace(qmv, need):
+        qmv.qmv_matmul(qmv.FMT(Q4_K, Q8_K), Wd, rows, cols, xq_dev, Y, m)
+        qmv.qmv_get_status()
+    return host(Y)
+
+
+@pytest.mark.parametrize("rows,cols,m", [(128, 256, 1), (300, 1024, 37), (130, 768, 300), (1000, 512, 129),
+                                         (9700, 256, 500)])
 def test_matmul_w4a8_parity(qmv, orc, rows, cols, m):
-    """W4A8 prefill (Q4_K x Q8_K): within 1e-4 of the oracle's exact integer
-    dots, and every token's row within the same bar of its own W4A8 decode
-    (both exact in integers; only the fp32 accumulation order differs)."""
+    """W4A8 prefill (Q4_K x Q8_K) on the tensor cores, every output against the
+    oracle's exact integer dots: ragged row tiles (130, 300, 1000, 9700), ragged
+    token tiles (1, 37, 129, 300, 500), one to four super-blocks per row, and
+    more tiles than SMs (9700 x 500); plus every token's row within the same
+    bar of its own W4A8 decode (both exact in integers; only the fp32
+    accumulation order differs)."""
     W = synth.weights(Q4_K, rows, cols, seed=12, tensor_id=rows)
     Wd = dev(W)
     x = synth.activations(m, cols, seed=12)
     xq = orc.quantize_act(Q8_K, x)
-    Y = torch.full((m, rows), float("nan"), dtype=torch.float32, device="cuda")
-    qmv.qmv_matmul(qmv.FMT(Q4_K, Q8_K), Wd, rows, cols, dev(xq), Y, m)
-    Y = host(Y)
-    g = np.random.default_rng(rows)
-    rids = np.unique(np.concatenate([[0, rows - 1], g.integers(0, rows, 30)])) if rows > 512 else np.arange(rows)
-    toks = np.unique(np.concatenate([[0, m - 1], g.integers(0, m, 14)])) if m > 64 else np.arange(m)
-    yref, yabs = orc.matvec(Q4_K, Q8_K, W, rows, cols, xq[toks], len(toks), row_ids=rids)
-    assert_close(Y[np.ix_(toks, rids)], yref, yabs, what=f"w4a8 {rows}x{cols} m={m}")
+    Y = run_w4a8(qmv, Wd, rows, cols, dev(xq), m)
+    yref, yabs = orc.matvec(Q4_K, Q8_K, W, rows, cols, xq, m)
+    assert_close(Y, yref, yabs, what=f"w4a8 {rows}x{cols} m={m}")
     xqd = dev(xq)
-    _, yabs_all = orc.matvec(Q4_K, Q8_K, W, rows, cols, xq[toks[:3]], 3)
-    for i, t in enumerate(toks[:3]):
+    toks = sorted({0, m // 2, m - 1})
+    for t in toks:
         y1 = torch.empty((1, rows), dtype=torch.float32, device="cuda")
         qmv.qmv_matvec(qmv.FMT(Q4_K, Q8_K), Wd, rows, cols, xqd[t], y1, 1)
-        assert_close(Y[t], host(y1)[0].astype(np.float64), yabs_all[i], what=f"prefill vs decode token {t}")
+        assert_close(Y[t], host(y1)[0].astype(np.float64), yabs[t], what=f"prefill vs decode token {t}")
     qmv.qmv_get_status()
+
+
+def test_matmul_w4a8_integer_exactness(qmv, orc):
+    """The tensor cores return the integer sums exactly.  Weights with d = 1,
+    dmin = 1, every sub-block scale and min 63 and every code 15, against
+    activations whose codes are all +127 in the first half of each super-block
+    and -127 in the second (scale d_x = 1/127 in fp32): each super-block's S is
+    +15.36M - 15.36M and its Mn +/- sums that cancel, so every output is an
+    exact small integer combination that any lost low bit would change.  Plus
+    rows and tokens with mixed codes, compared exactly where the oracle's value
+    is an integer below 2^24."""
+    rows, cols, m = 256, 1024, 130
+    blk = np.zeros(rows * cols // 256, dtype=synth.block_dtype(Q4_K))
+    blk["d"] = np.float16(1.0)
+    blk["dmin"] = np.float16(1.0)
+    blk["scales"] = 0xFF              # every 6-bit scale and min = 63
+    blk["qs"] = 0xFF                  # every code 15
+    g = np.random.default_rng(77)
+    mix = blk.reshape(rows, -1)[rows // 2:]
+    mix["qs"] = g.integers(0, 256, mix["qs"].shape, dtype=np.uint8)
+    mix["scales"] = g.integers(0, 256, mix["scales"].shape, dtype=np.uint8)
+    W = blk.view(np.uint8).reshape(-1)
+    x = np.empty((m, cols), dtype=np.float32)
+    x.reshape(m, -1, 2, 128)[:, :, 0, :] = 1.0
+    x.reshape(m, -1, 2, 128)[:, :, 1, :] = -1.0
+    x[m // 2:] = g.integers(-127, 128, (m - m // 2, cols)).astype(np.float32) / np.float32(127.0)
+    x[m // 2:, 0] = 1.0               # amax = 1, d_x = 1/127
+    xq = orc.quantize_act(Q8_K, x)
+    Y = run_w4a8(qmv, dev(W), rows, cols, dev(xq), m)
+    yref, yabs = orc.matvec(Q4_K, Q8_K, W, rows, cols, xq, m)
+    assert_close(Y, yref, yabs, what="w4a8 adversarial")
+    # the all-maximal quarter: S cancels per super-block, leaving -d_x*dmin*Mn
+    # with Mn = 63 * (sum of the 16 bsums) = 0, so exactly zero
+    assert (Y[: m // 2, : rows // 2] == 0).all() and (yref[: m // 2, : rows // 2] == 0).all()
