@@ -13,6 +13,9 @@
  *   Q5_0  (22 B / 32 w): fp16 d | u32 high-bit mask | 16 bytes of nibbles.
  *         Nibbles as Q4_0; bit i of the mask is bit 4 of element i.  w = d*(q-16).
  *   Q8_0  (34 B / 32 w): fp16 d | 32 int8.  w = d*q.
+ *   Q8_1  (36 B / 32 w): fp16 d | fp16 s | 32 int8.  w = d*q; s is the block's
+ *         code sum times d, which only an activation block uses, so a weight
+ *         ignores it.
  *   Q4_1  (20 B / 32 w): fp16 d | fp16 m | 16 bytes of nibbles, order as Q4_0.
  *         w = d*q + m (carried below as dmin = -m with sub_min = 1).
  *   Q5_1  (24 B / 32 w): fp16 d | fp16 m | u32 high-bit mask | 16 bytes of
@@ -41,6 +44,8 @@
  *   Q6_K  (210 B / 256 w): 128 B low nibbles | 64 B high 2-bit pairs |
  *         int8 scales[16] | fp16 d.  Element i uses scales[i/16].
  *         w = d*sc*(q-32).
+ *   F32, F16, BF16: plain little-endian values, one per element ("Models and
+ *         formats", "Tensor formats": read and accelerated on every backend).
  */
 #include "oracle.h"
 #include <math.h>
@@ -55,7 +60,8 @@ static uint32_t rd_u32(const uint8_t* p)
 int64_t orc_block_elems(int type)
 {
     switch (type) {
-    case ORC_Q4_0: case ORC_Q5_0: case ORC_Q8_0: case ORC_MXFP4: case ORC_Q4_1: case ORC_Q5_1: return 32;
+    case ORC_Q4_0: case ORC_Q5_0: case ORC_Q8_0: case ORC_MXFP4: case ORC_Q4_1: case ORC_Q5_1: case ORC_Q8_1:
+        return 32;
     case ORC_Q4_K: case ORC_Q5_K: case ORC_Q6_K: case ORC_Q8_K: case ORC_Q2_K: case ORC_Q3_K: return 256;
     default: return 0;
     }
@@ -67,6 +73,7 @@ int64_t orc_block_bytes(int type)
     case ORC_Q4_0: return 18;
     case ORC_Q5_0: return 22;
     case ORC_Q8_0: return 34;
+    case ORC_Q8_1: return 36;
     case ORC_Q4_1: return 20;
     case ORC_Q5_1: return 24;
     case ORC_MXFP4: return 17;
@@ -145,6 +152,15 @@ int orc_decode_block(int type, const uint8_t* b, orc_block* out)
         out->d = orc_f16_to_f64((uint16_t)rd_u16(b));
         for (int i = 0; i < 32; i++) {
             out->code[i] = (int8_t)b[2 + i];
+            out->sub_scale[i] = 1;
+        }
+        return ORC_OK;
+    }
+    case ORC_Q8_1: {
+        out->n = 32;
+        out->d = orc_f16_to_f64((uint16_t)rd_u16(b));
+        for (int i = 0; i < 32; i++) {
+            out->code[i] = (int8_t)b[4 + i];
             out->sub_scale[i] = 1;
         }
         return ORC_OK;
@@ -294,8 +310,32 @@ double orc_block_weight(const orc_block* b, int i)
     return a - m;
 }
 
+int64_t orc_plain_bytes(int type)
+{
+    return type == ORC_F32 ? 4 : (type == ORC_F16 || type == ORC_BF16) ? 2 : 0;
+}
+
+/* Element i of a plain weight row, exactly. */
+double orc_plain_weight(int type, const uint8_t* row, int64_t i)
+{
+    if (type == ORC_F32) {
+        float f;
+        memcpy(&f, row + 4 * i, 4);
+        return (double)f;
+    }
+    const uint16_t h = (uint16_t)(row[2 * i] | (row[2 * i + 1] << 8));
+    return type == ORC_F16 ? orc_f16_to_f64(h) : orc_bf16_to_f64(h);
+}
+
 int orc_dequant(int type, const uint8_t* W, int64_t rows, int64_t cols, float* out)
 {
+    if (orc_plain_bytes(type)) {
+        if (rows < 0 || cols < 0) return ORC_EINVAL;
+        for (int64_t r = 0; r < rows; r++)
+            for (int64_t c = 0; c < cols; c++)
+                out[r * cols + c] = (float)orc_plain_weight(type, W + r * cols * orc_plain_bytes(type), c);
+        return ORC_OK;
+    }
     int64_t bs = orc_block_elems(type), bb = orc_block_bytes(type);
     if (bs == 0 || type == ORC_Q8_K) return ORC_EUNSUP;
     if (rows < 0 || cols < 0) return ORC_EINVAL;

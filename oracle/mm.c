@@ -35,7 +35,7 @@
 static int weight_type_ok(int t)
 {
     return t == ORC_Q4_0 || t == ORC_Q5_0 || t == ORC_Q8_0 || t == ORC_MXFP4 || t == ORC_Q4_K || t == ORC_Q6_K ||
-           t == ORC_Q4_1 || t == ORC_Q5_1 || t == ORC_Q5_K || t == ORC_Q2_K || t == ORC_Q3_K;
+           t == ORC_Q4_1 || t == ORC_Q5_1 || t == ORC_Q5_K || t == ORC_Q2_K || t == ORC_Q3_K || t == ORC_Q8_1;
 }
 
 /* The 8-bit activation format that pairs with a weight format: the same block
@@ -75,6 +75,20 @@ int orc_block_dots(int wtype, const uint8_t* W, int64_t rows, int64_t cols,
 static int dot_row(int wtype, int atype, const uint8_t* wrow, int64_t cols, const uint8_t* xv,
                    double* y, double* yabs)
 {
+    if (orc_plain_bytes(wtype)) {
+        /* plain weights against fp32 activations: the definition, in fp64 */
+        double acc = 0.0, aabs = 0.0;
+        for (int64_t c = 0; c < cols; c++) {
+            float xf;
+            memcpy(&xf, xv + 4 * c, 4);
+            const double p = orc_plain_weight(wtype, wrow, c) * (double)xf;
+            acc += p;
+            aabs += fabs(p);
+        }
+        *y = acc;
+        if (yabs) *yabs = aabs;
+        return ORC_OK;
+    }
     int64_t bs = orc_block_elems(wtype), bb = orc_block_bytes(wtype);
     int64_t nb = cols / bs;
     orc_block wb;
@@ -130,8 +144,15 @@ static int64_t act_row_bytes(int atype, int64_t cols)
     return cols / orc_block_elems(atype) * orc_block_bytes(atype);
 }
 
+static int64_t weight_row_bytes(int wtype, int64_t cols)
+{
+    if (orc_plain_bytes(wtype)) return cols * orc_plain_bytes(wtype);
+    return cols / orc_block_elems(wtype) * orc_block_bytes(wtype);
+}
+
 static int check_pair(int wtype, int atype, int64_t cols)
 {
+    if (orc_plain_bytes(wtype)) return (atype == ORC_F32 && cols > 0) ? ORC_OK : ORC_EUNSUP;
     if (!weight_type_ok(wtype)) return ORC_EUNSUP;
     if (atype != ORC_F32 && atype != ORC_BF16 && atype != paired_act(wtype)) return ORC_EUNSUP;
     if (cols <= 0 || cols % orc_block_elems(wtype)) return ORC_ESHAPE;
@@ -146,7 +167,7 @@ int orc_matvec(int wtype, int atype, const uint8_t* W, int64_t rows, int64_t col
     if (rc) return rc;
     if (rows < 0 || n_vec < 0) return ORC_EINVAL;
     if (!row_ids) n_rows = rows;
-    int64_t rb = cols / orc_block_elems(wtype) * orc_block_bytes(wtype);
+    int64_t rb = weight_row_bytes(wtype, cols);
     int64_t xb = act_row_bytes(atype, cols);
     const uint8_t* X = (const uint8_t*)x;
     for (int64_t v = 0; v < n_vec; v++)
@@ -168,7 +189,7 @@ int orc_moe(int wtype, int atype, const uint8_t* W3d, int64_t n_expert,
     int rc = check_pair(wtype, atype, cols);
     if (rc) return rc;
     if (n_expert <= 0 || rows < 0 || k <= 0 || n_tok < 0) return ORC_EINVAL;
-    int64_t rb = cols / orc_block_elems(wtype) * orc_block_bytes(wtype);
+    int64_t rb = weight_row_bytes(wtype, cols);
     int64_t xb = act_row_bytes(atype, cols);
     const uint8_t* X = (const uint8_t*)x;
     for (int64_t t = 0; t < n_tok; t++) {

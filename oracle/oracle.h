@@ -34,7 +34,8 @@
 enum {
     ORC_Q4_0 = 1, ORC_Q5_0 = 2, ORC_Q8_0 = 3, ORC_Q4_K = 4, ORC_Q6_K = 5,
     ORC_MXFP4 = 6, ORC_Q8_K = 7, ORC_F32 = 8, ORC_BF16 = 9,
-    ORC_Q4_1 = 10, ORC_Q5_1 = 11, ORC_Q5_K = 12, ORC_Q2_K = 13, ORC_Q3_K = 14
+    ORC_Q4_1 = 10, ORC_Q5_1 = 11, ORC_Q5_K = 12, ORC_Q2_K = 13, ORC_Q3_K = 14,
+    ORC_Q8_1 = 15, ORC_F16 = 16
 };
 
 /* Return codes. */
@@ -50,7 +51,8 @@ uint16_t orc_f32_to_bf16_rn(float f);
 /* A decoded block.  Every element i satisfies
  *     w_i = d * sub_scale[i] * code[i] - dmin * sub_min[i]
  * exactly (in real arithmetic).  For the 32-element formats sub_scale = 1 and
- * sub_min = 0 (Q4_1 and Q5_1: sub_min = 1 and dmin = -m, their offset);
+ * sub_min = 0 (Q4_1 and Q5_1: sub_min = 1 and dmin = -m, their offset;
+ * Q8_1 is Q8_0's codes and scale, its second field unused);
  * Q4_K and Q5_K carry their 6-bit sub-block scale/min, Q2_K its 4-bit
  * scale/min, Q3_K its 6-bit scale minus 32, Q6_K its int8 sub-block scale.  MXFP4 stores twice the E2M1 value (an integer) in code[]
  * and 2^(e-128) in d. */
@@ -64,13 +66,19 @@ typedef struct {
 } orc_block;
 
 int64_t orc_block_elems(int type);           /* 32 / 256, or 0 if not a block type */
+/* Plain (unblocked) weight types: F32, F16, BF16 -- one value per element,
+ * little-endian, row-major.  Their bytes per element, or 0 for block types. */
+int64_t orc_plain_bytes(int type);
 int64_t orc_block_bytes(int type);           /* bytes per block, or 0 */
 int     orc_decode_block(int type, const uint8_t* blk, orc_block* out);
+/* Element i of a row of a plain weight type (F32, F16, BF16), exactly. */
+double  orc_plain_weight(int type, const uint8_t* row, int64_t i);
 /* Decoded weight of element i as an exact fp64 value. */
 double  orc_block_weight(const orc_block* b, int i);
 /* rows x cols weights -> fp32.  Every format's weight is exactly representable
  * in fp32 except Q4_K's, which is the single rounding RN_fp32(d*sc*q - dmin*m),
- * and Q4_1's and Q5_1's, the single rounding RN_fp32(d*q + m). */
+ * and Q4_1's and Q5_1's, the single rounding RN_fp32(d*q + m).  Plain F16,
+ * BF16 and F32 weights convert exactly. */
 int     orc_dequant(int type, const uint8_t* W, int64_t rows, int64_t cols, float* out);
 
 /* ---- quant.c : the 8-bit activation quantisers ---- */

@@ -24,9 +24,11 @@ LIB_PATH = os.path.join(BUILD_DIR, "liboracle.so")
 SOURCES = ["fp.c", "blocks.c", "quant.c", "wquant.c", "mm.c"]
 
 # The oracle's own type numbers (oracle.h).
-Q4_0, Q5_0, Q8_0, Q4_K, Q6_K, MXFP4, Q8_K, F32, BF16, Q4_1, Q5_1, Q5_K, Q2_K, Q3_K = range(1, 15)
-BLOCK_ELEMS = {Q4_0: 32, Q5_0: 32, Q8_0: 32, MXFP4: 32, Q4_K: 256, Q6_K: 256, Q8_K: 256, Q4_1: 32, Q5_1: 32, Q5_K: 256, Q2_K: 256, Q3_K: 256}
-BLOCK_BYTES = {Q4_0: 18, Q5_0: 22, Q8_0: 34, MXFP4: 17, Q4_K: 144, Q6_K: 210, Q8_K: 292, Q4_1: 20, Q5_1: 24, Q5_K: 176, Q2_K: 84, Q3_K: 110}
+Q4_0, Q5_0, Q8_0, Q4_K, Q6_K, MXFP4, Q8_K, F32, BF16, Q4_1, Q5_1, Q5_K, Q2_K, Q3_K, Q8_1, F16 = range(1, 17)
+BLOCK_ELEMS = {Q4_0: 32, Q5_0: 32, Q8_0: 32, MXFP4: 32, Q4_K: 256, Q6_K: 256, Q8_K: 256, Q4_1: 32, Q5_1: 32,
+               Q5_K: 256, Q2_K: 256, Q3_K: 256, Q8_1: 32, F32: 1, F16: 1, BF16: 1}
+BLOCK_BYTES = {Q4_0: 18, Q5_0: 22, Q8_0: 34, MXFP4: 17, Q4_K: 144, Q6_K: 210, Q8_K: 292, Q4_1: 20, Q5_1: 24,
+               Q5_K: 176, Q2_K: 84, Q3_K: 110, Q8_1: 36, F32: 4, F16: 2, BF16: 2}
 
 _lock = threading.Lock()
 _lib = None
