@@ -33,6 +33,15 @@ QMV_GEMV_DECL(qmv_gemv_q8_0)
 QMV_GEMV_DECL(qmv_gemv_mxfp4)
 QMV_GEMV_DECL(qmv_gemv_q4_k)
 QMV_GEMV_DECL(qmv_gemv_q6_k)
+QMV_GEMV_DECL(qmv_gemv_q4_1)
+QMV_GEMV_DECL(qmv_gemv_q5_1)
+QMV_GEMV_DECL(qmv_gemv_q8_1)
+QMV_GEMV_DECL(qmv_gemv_q2_k)
+QMV_GEMV_DECL(qmv_gemv_q3_k)
+QMV_GEMV_DECL(qmv_gemv_q5_k)
+QMV_GEMV_DECL(qmv_gemv_f32)
+QMV_GEMV_DECL(qmv_gemv_f16)
+QMV_GEMV_DECL(qmv_gemv_bf16)
 size_t qmv_w4a8_workspace_bytes(int64_t cols, int64_t m);
 int qmv_launch_gemm_q4k_w4a8(const void* W, int64_t rows, int64_t cols, const void* X, float* Y, int64_t m,
                              void* ws, bool pdl, cudaStream_t st);
@@ -105,22 +114,36 @@ const char* type_name(int t)
     case QMV_F32: return "F32";
     case QMV_BF16: return "BF16";
     case QMV_MXFP4_R: return "MXFP4_R";
+    case QMV_Q4_1: return "Q4_1";
+    case QMV_Q5_1: return "Q5_1";
+    case QMV_Q8_1: return "Q8_1";
+    case QMV_Q2_K: return "Q2_K";
+    case QMV_Q3_K: return "Q3_K";
+    case QMV_Q5_K: return "Q5_K";
+    case QMV_F16: return "F16";
     default: return "unknown";
     }
 }
 
+bool is_plain(int t) { return t == QMV_F32 || t == QMV_F16 || t == QMV_BF16; }
+
 bool is_weight_type(int t)
 {
-    return t == QMV_Q4_0 || t == QMV_Q5_0 || t == QMV_Q8_0 || t == QMV_MXFP4 || t == QMV_Q4_K || t == QMV_Q6_K;
+    return t == QMV_Q4_0 || t == QMV_Q5_0 || t == QMV_Q8_0 || t == QMV_MXFP4 || t == QMV_Q4_K || t == QMV_Q6_K ||
+           t == QMV_Q4_1 || t == QMV_Q5_1 || t == QMV_Q8_1 || t == QMV_Q2_K || t == QMV_Q3_K || t == QMV_Q5_K ||
+           is_plain(t);
 }
 
-bool is_kquant(int t) { return t == QMV_Q4_K || t == QMV_Q6_K; }
+bool is_kquant(int t) { return qmv::kq_rt(t); }
 
-int paired_act(int wtype) { return is_kquant(wtype) ? QMV_Q8_K : QMV_Q8_0; }
+// The 8-bit activation type a block format pairs with (plain weights: none, F32 only).
+int paired_act(int wtype) { return is_plain(wtype) ? QMV_F32 : is_kquant(wtype) ? QMV_Q8_K : QMV_Q8_0; }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
-const char* kWeightList = "Q4_0, Q5_0, Q8_0, MXFP4 (32-element blocks) and Q4_K, Q6_K (256-element blocks)";
+const char* kWeightList =
+    "Q4_0, Q4_1, Q5_0, Q5_1, Q8_0, Q8_1, MXFP4 (32-element blocks), Q2_K, Q3_K, Q4_K, Q5_K, Q6_K (256-element "
+    "blocks) and plain F32, F16, BF16";
 
 int check_weights(int wtype, const void* W, int64_t rows, int64_t cols)
 {
@@ -129,11 +152,11 @@ int check_weights(int wtype, const void* W, int64_t rows, int64_t cols)
                     type_name(wtype), kWeightList);
     if (rows < 0 || cols <= 0) return fail(QMV_ERR_INVALID_ARG, "rows must be >= 0 and cols > 0 (got %lld x %lld)",
                                            (long long)rows, (long long)cols);
-    const int bs = qmv_block_elems(wtype);
+    const int bs = is_plain(wtype) ? 8 : qmv_block_elems(wtype);
     if (cols % bs)
         return fail(QMV_ERR_SHAPE,
-                    "%s rows hold %d-element blocks; cols = %lld is not a multiple of %d%s", type_name(wtype), bs,
-                    (long long)cols, bs,
+                    "%s rows hold %d-element %s; cols = %lld is not a multiple of %d%s", type_name(wtype), bs,
+                    is_plain(wtype) ? "units" : "blocks", (long long)cols, bs,
                     is_kquant(wtype) ? " (rows whose length is not a multiple of 256 are stored as Q4_0/Q5_0/Q8_0)"
                                      : "");
     if (cols > (int64_t)1 << 24) return fail(QMV_ERR_SHAPE, "cols = %lld is over the limit of 16777216", (long long)cols);
@@ -244,9 +267,10 @@ const char* qmv_last_error(void) { return t_err.c_str(); }
 int qmv_block_elems(int type)
 {
     switch (type) {
-    case QMV_Q4_0: case QMV_Q5_0: case QMV_Q8_0: case QMV_MXFP4: case QMV_MXFP4_R: return 32;
-    case QMV_Q4_K: case QMV_Q6_K: case QMV_Q8_K: return 256;
-    case QMV_F32: case QMV_BF16: return 1;
+    case QMV_Q4_0: case QMV_Q5_0: case QMV_Q8_0: case QMV_MXFP4: case QMV_MXFP4_R: case QMV_Q4_1: case QMV_Q5_1:
+    case QMV_Q8_1: return 32;
+    case QMV_Q4_K: case QMV_Q6_K: case QMV_Q8_K: case QMV_Q2_K: case QMV_Q3_K: case QMV_Q5_K: return 256;
+    case QMV_F32: case QMV_BF16: case QMV_F16: return 1;
     default: return 0;
     }
 }
@@ -261,8 +285,14 @@ size_t qmv_block_bytes(int type)
     case QMV_Q4_K: return 144;
     case QMV_Q6_K: return 210;
     case QMV_Q8_K: return 292;
+    case QMV_Q4_1: return 20;
+    case QMV_Q5_1: return 24;
+    case QMV_Q8_1: return 36;
+    case QMV_Q2_K: return 84;
+    case QMV_Q3_K: return 110;
+    case QMV_Q5_K: return 176;
     case QMV_F32: return 4;
-    case QMV_BF16: return 2;
+    case QMV_BF16: case QMV_F16: return 2;
     default: return 0;
     }
 }
@@ -350,6 +380,9 @@ int qmv_block_dots(int type, const void* W, int64_t rows, int64_t cols, const vo
 {
     int rc = check_weights(type, W, rows, cols);
     if (rc) return rc;
+    if (is_plain(type))
+        return fail(QMV_ERR_UNSUPPORTED, "qmv_block_dots: %s weights have no integer block dots (block formats only)",
+                    type_name(type));
     if (n_vec < 0) return fail(QMV_ERR_INVALID_ARG, "n_vec must be >= 0");
     if (rows == 0 || n_vec == 0) return ok();
     if (!xq || !out) return fail(QMV_ERR_INVALID_ARG, "xq and out must not be NULL");
@@ -389,6 +422,15 @@ int qmv_matvec(int fmt, const void* W, int64_t rows, int64_t cols, const void* x
     case QMV_MXFP4: rc = qmv_gemv_mxfp4(a8, quant_x, pdl, W, rows, cols, x, y, n_vec, st); break;
     case QMV_Q4_K: rc = qmv_gemv_q4_k(a8, quant_x, pdl, W, rows, cols, x, y, n_vec, st); break;
     case QMV_Q6_K: rc = qmv_gemv_q6_k(a8, quant_x, pdl, W, rows, cols, x, y, n_vec, st); break;
+    case QMV_Q4_1: rc = qmv_gemv_q4_1(a8, quant_x, pdl, W, rows, cols, x, y, n_vec, st); break;
+    case QMV_Q5_1: rc = qmv_gemv_q5_1(a8, quant_x, pdl, W, rows, cols, x, y, n_vec, st); break;
+    case QMV_Q8_1: rc = qmv_gemv_q8_1(a8, quant_x, pdl, W, rows, cols, x, y, n_vec, st); break;
+    case QMV_Q2_K: rc = qmv_gemv_q2_k(a8, quant_x, pdl, W, rows, cols, x, y, n_vec, st); break;
+    case QMV_Q3_K: rc = qmv_gemv_q3_k(a8, quant_x, pdl, W, rows, cols, x, y, n_vec, st); break;
+    case QMV_Q5_K: rc = qmv_gemv_q5_k(a8, quant_x, pdl, W, rows, cols, x, y, n_vec, st); break;
+    case QMV_F32: rc = qmv_gemv_f32(a8, quant_x, pdl, W, rows, cols, x, y, n_vec, st); break;
+    case QMV_F16: rc = qmv_gemv_f16(a8, quant_x, pdl, W, rows, cols, x, y, n_vec, st); break;
+    case QMV_BF16: rc = qmv_gemv_bf16(a8, quant_x, pdl, W, rows, cols, x, y, n_vec, st); break;
     }
     if (rc == -2) return fail(QMV_ERR_SHAPE, "cols = %lld needs more shared memory than one SM has", (long long)cols);
     if (rc) return cuda_fail("qmv_matvec");

@@ -22,6 +22,20 @@
 
 namespace qmv {
 
+// Format traits that kernels, launchers and the boundary share.
+__host__ __device__ constexpr bool kq_rt(int T)   // 256-element K-quant (Q8_K activations)
+{
+    return T == QMV_Q4_K || T == QMV_Q6_K || T == QMV_Q5_K || T == QMV_Q2_K || T == QMV_Q3_K;
+}
+__host__ __device__ constexpr bool plain_rt(int T) { return T == QMV_F32 || T == QMV_F16 || T == QMV_BF16; }
+// Run length of the fp32 activation sums the fp32-activation path stages for
+// a format whose weights carry an offset (min) per run: 0 = none.
+__host__ __device__ constexpr int xsum_run_rt(int T)
+{
+    return (T == QMV_Q4_K || T == QMV_Q5_K || T == QMV_Q4_1 || T == QMV_Q5_1) ? 32 : T == QMV_Q2_K ? 16 : 0;
+}
+__host__ __device__ constexpr int block_elems_rt(int T) { return kq_rt(T) ? 256 : plain_rt(T) ? 8 : 32; }
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p)
 {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

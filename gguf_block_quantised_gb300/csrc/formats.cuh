@@ -10,6 +10,13 @@
 //                                                          w = d*sc_j*q - dmin*m_j
 //   Q6_K 210 B / 256 w  128 B low nibbles | 64 B high pairs | int8 sc[16] | fp16 d
 //                                                          w = d*sc*(q-32)
+//   Q4_1  20 B / 32 w   fp16 d | fp16 m | 16 B nibbles     w = d*q + m
+//   Q5_1  24 B / 32 w   fp16 d | fp16 m | u32 fifth bits | 16 B   w = d*q + m
+//   Q8_1  36 B / 32 w   fp16 d | fp16 s (unused) | int8[32]  w = d*q
+//   Q5_K 176 B / 256 w  Q4_K's d, dmin, 12 B sc/m | 32 B fifth bits | 128 B nibbles
+//   Q2_K  84 B / 256 w  16 B sc|m nibbles per 16 | 64 B 2-bit codes | fp16 d | fp16 dmin
+//   Q3_K 110 B / 256 w  32 B high bits | 64 B 2-bit codes | 12 B 6-bit scales | fp16 d
+//   F32, F16, BF16      plain values (fp32 activations only), units of 8
 // Nibble order: element j of a 32-run is the low nibble of byte j, element
 // j+16 its high nibble; Q4_K 32-byte chunk c holds sub-block 2c (low) and
 // 2c+1 (high); Q6_K element i uses scales[i/16].
@@ -67,9 +74,10 @@ constexpr int kBPitch = 48;
 template <int T>
 __host__ __device__ constexpr int kquant_run_pos(int r)
 {
-    if constexpr (T == QMV_Q4_K) return 80 * (r >> 2) + 16 * (r & 3);
-    else return 80 * (2 * (r >> 3) + (r & 1)) + 16 * ((r & 7) >> 1);   // h = r/8, g = (r%8)/2, lh = r%2
+    if constexpr (T == QMV_Q6_K) return 80 * (2 * (r >> 3) + (r & 1)) + 16 * ((r & 7) >> 1);   // h = r/8, g = (r%8)/2, lh = r%2
+    else return 80 * (r >> 2) + 16 * (r & 3);   // unit u = elements 64u .. 64u+63 in order
 }
+
 
 template <int T>
 struct Fmt;
@@ -85,6 +93,7 @@ struct W32 {
 template <int T>
 struct Fmt32Base {
     static constexpr int BS = 32, UE = 32, UPB = 1;
+    static constexpr bool MIN = false;   // a per-block offset m (w = d*q + m)
 
     struct XA8 {
         uint32_t w[8];
@@ -196,6 +205,66 @@ struct Fmt<QMV_MXFP4> : Fmt32Base<QMV_MXFP4> {
             w.c[2 * k + 1] = lut4(q[k] >> 16);
         }
         w.d = e8m0_half(blk[0]);
+    }
+};
+
+// Q4_1 / Q5_1: unsigned codes with a per-block offset, w = d*q + m.  The
+// offset enters through the exact sum of the block's activation codes.
+struct W32M {
+    uint32_t c[8];   // 32 code bytes
+    float d, m;
+};
+
+template <>
+struct Fmt<QMV_Q4_1> : Fmt32Base<QMV_Q4_1> {
+    static constexpr int BB = 20, OFF = 0;
+    static constexpr bool SIGNED = false, MIN = true;
+    using W = W32M;
+    static __device__ __forceinline__ void load(const uint8_t* blk, int, W& w)
+    {
+        uint32_t q[4];
+        load_words<4>(blk + 4, q);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            w.c[k] = q[k] & 0x0f0f0f0fu;
+            w.c[4 + k] = (q[k] >> 4) & 0x0f0f0f0fu;
+        }
+        w.d = half_bits_to_float(ld_u16(blk));
+        w.m = half_bits_to_float(ld_u16(blk + 2));
+    }
+};
+
+template <>
+struct Fmt<QMV_Q5_1> : Fmt32Base<QMV_Q5_1> {
+    static constexpr int BB = 24, OFF = 0;
+    static constexpr bool SIGNED = false, MIN = true;
+    using W = W32M;
+    static __device__ __forceinline__ void load(const uint8_t* blk, int, W& w)
+    {
+        uint32_t q[5];
+        load_words<5>(blk + 4, q);   // q[0] = fifth-bit mask, q[1..4] = nibbles
+        const uint32_t qh = q[0];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            w.c[k] = (q[1 + k] & 0x0f0f0f0fu) | Fmt<QMV_Q5_0>::spread4((qh >> (4 * k)) & 15u);
+            w.c[4 + k] = ((q[1 + k] >> 4) & 0x0f0f0f0fu) | Fmt<QMV_Q5_0>::spread4((qh >> (16 + 4 * k)) & 15u);
+        }
+        w.d = half_bits_to_float(ld_u16(blk));
+        w.m = half_bits_to_float(ld_u16(blk + 2));
+    }
+};
+
+// Q8_1 as a weight: Q8_0's codes and scale; the second fp16 field (the block's
+// code sum times d) serves activation blocks only and is not read.
+template <>
+struct Fmt<QMV_Q8_1> : Fmt32Base<QMV_Q8_1> {
+    static constexpr int BB = 36, OFF = 0;
+    static constexpr bool SIGNED = true;
+    using W = W32;
+    static __device__ __forceinline__ void load(const uint8_t* blk, int, W& w)
+    {
+        load_words<8>(blk + 4, w.c);
+        w.d = half_bits_to_float(ld_u16(blk));
     }
 };
 
@@ -395,28 +464,277 @@ struct Fmt<QMV_Q6_K> {
     }
 };
 
+// ------------------------------------------------------------------------------
+// Q5_K: Q4_K's fields plus a 32-byte field of fifth bits (bit j of byte l is the
+// fifth bit of element 32j + l); units, staging and products are Q4_K's, with
+// 5-bit codes.
+// ------------------------------------------------------------------------------
+template <>
+struct Fmt<QMV_Q5_K> : Fmt<QMV_Q4_K> {
+    static constexpr int BB = 176;
+    // blk is 16-byte aligned (176-byte blocks in a 16-byte aligned staging slot).
+    static __device__ __forceinline__ void load(const uint8_t* blk, int c, W& w)
+    {
+        const uint4 h = *reinterpret_cast<const uint4*>(blk);   // d, dmin, field[0..11]
+        const uint4* hp = reinterpret_cast<const uint4*>(blk + 16);
+        const uint4* qp = reinterpret_cast<const uint4*>(blk + 48 + 32 * c);
+        const uint4 h0 = hp[0], h1 = hp[1], a = qp[0], b = qp[1];
+        const uint32_t q[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        const uint32_t qh[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            w.lo[k] = (q[k] & 0x0f0f0f0fu) | (((qh[k] >> (2 * c)) & 0x01010101u) << 4);
+            w.hi[k] = ((q[k] >> 4) & 0x0f0f0f0fu) | (((qh[k] >> (2 * c + 1)) & 0x01010101u) << 4);
+        }
+        scale_min(h.y, h.z, h.w, 2 * c, w.sc0, w.m0);
+        scale_min(h.y, h.z, h.w, 2 * c + 1, w.sc1, w.m1);
+        w.d = half_bits_to_float(h.x & 0xffffu);
+        w.dmin = half_bits_to_float(h.x >> 16);
+    }
+};
+
+// ------------------------------------------------------------------------------
+// Q2_K and Q3_K: 2-bit code planes.  Element 128n + 32j + l (n < 2, j < 4,
+// l < 32) takes bits 2j..2j+1 of code byte 32n + l.  Unit u = elements
+// 64u .. 64u+63 (n = u/2, j = 2(u%2) + j', j' < 2): four 16-element runs, each
+// with its own scale (run r = 2j' + half, block run 4u + r).
+// ------------------------------------------------------------------------------
+struct WK2 {
+    uint32_t c[2][8];   // codes of elements 64u + 32j' + 4k .. +3 as bytes
+    int sc[4], m[4];    // per run: scale and min (Q3_K: signed scale, no min)
+    float d, dmin;
+};
+
+struct XK2 {
+    uint32_t c[2][8];
+    float d;
+    int s[4];   // sums of the codes of each run
+};
+
+template <int T>
+struct FmtK2Base {
+    static constexpr int BS = 256, UE = 64, UPB = 4;
+    using W = WK2;
+    using XA8 = XK2;
+    static __device__ __forceinline__ void load_x_a8(const XView& X, int v, int b, int u, XA8& x)
+    {
+        const uint4* p = reinterpret_cast<const uint4*>(X.codes + ((size_t)v * X.nb + b) * kKPitch + 80 * u);
+        const uint4 a0 = p[0], a1 = p[1], a2 = p[2], a3 = p[3];
+        x.c[0][0] = a0.x; x.c[0][1] = a0.y; x.c[0][2] = a0.z; x.c[0][3] = a0.w;
+        x.c[0][4] = a1.x; x.c[0][5] = a1.y; x.c[0][6] = a1.z; x.c[0][7] = a1.w;
+        x.c[1][0] = a2.x; x.c[1][1] = a2.y; x.c[1][2] = a2.z; x.c[1][3] = a2.w;
+        x.c[1][4] = a3.x; x.c[1][5] = a3.y; x.c[1][6] = a3.z; x.c[1][7] = a3.w;
+        x.d = X.d[v * X.nb + b];
+        const uint2 bs = *reinterpret_cast<const uint2*>(X.bsum + ((size_t)v * X.nb + b) * 16 + 4 * u);
+        x.s[0] = (int)(int16_t)(bs.x & 0xffffu);
+        x.s[1] = (int)(int16_t)(bs.x >> 16);
+        x.s[2] = (int)(int16_t)(bs.y & 0xffffu);
+        x.s[3] = (int)(int16_t)(bs.y >> 16);
+    }
+    // The integer dot of run r (16 codes) with its activation codes.
+    static __device__ __forceinline__ int run_dot(const W& w, const XA8& x, int r)
+    {
+        int dot = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) dot = dp4a_us(w.c[r >> 1][4 * (r & 1) + k], x.c[r >> 1][4 * (r & 1) + k], dot);
+        return dot;
+    }
+    // sum over run r of (code - off) * x, fp32 in a fixed order
+    template <int OFFC>
+    static __device__ __forceinline__ float run_a32(const W& w, const float* xr, int r)
+    {
+        const float4* xp = reinterpret_cast<const float4*>(xr + 16 * r);
+        float p = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t c = w.c[r >> 1][4 * (r & 1) + k];
+            const float4 xa = xp[k];
+            p = __fmaf_rn(ubyte_to_float_minus(c, 0, 8388608.f + OFFC), xa.x, p);
+            p = __fmaf_rn(ubyte_to_float_minus(c, 1, 8388608.f + OFFC), xa.y, p);
+            p = __fmaf_rn(ubyte_to_float_minus(c, 2, 8388608.f + OFFC), xa.z, p);
+            p = __fmaf_rn(ubyte_to_float_minus(c, 3, 8388608.f + OFFC), xa.w, p);
+        }
+        return p;
+    }
+};
+
+template <>
+struct Fmt<QMV_Q2_K> : FmtK2Base<QMV_Q2_K> {
+    static constexpr int BB = 84;
+    static __device__ __forceinline__ void load(const uint8_t* blk, int u, W& w)
+    {
+        const int n = u >> 1, j0 = 2 * (u & 1);
+        uint32_t q[8], sm[1];
+        load_words<8>(blk + 16 + 32 * n, q);
+        load_words<1>(blk + 8 * n + 2 * j0, sm);   // scale|min bytes of runs 4u .. 4u+3
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            w.c[0][k] = (q[k] >> (2 * j0)) & 0x03030303u;
+            w.c[1][k] = (q[k] >> (2 * j0 + 2)) & 0x03030303u;
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const uint32_t byte = (sm[0] >> (8 * r)) & 0xffu;
+            w.sc[r] = (int)(byte & 15u);
+            w.m[r] = (int)(byte >> 4);
+        }
+        w.d = half_bits_to_float(ld_u16(blk + 80));
+        w.dmin = half_bits_to_float(ld_u16(blk + 82));
+    }
+    static __device__ __forceinline__ void ints(const W& w, const XA8& x, int& S, int& Mn)
+    {
+        S = 0;
+        Mn = 0;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            S += w.sc[r] * run_dot(w, x, r);
+            Mn += w.m[r] * x.s[r];
+        }
+    }
+    static __device__ __forceinline__ void acc_a8(const W& w, const XA8& x, float& acc)
+    {
+        int S, Mn;
+        ints(w, x, S, Mn);
+        acc = __fmaf_rn((float)S, w.d * x.d, acc);
+        acc = __fmaf_rn(-(float)Mn, w.dmin * x.d, acc);
+    }
+    static __device__ __forceinline__ void acc_a32(const W& w, const XView& X, int v, int b, int u, float& acc)
+    {
+        const float* xr = X.xf + (size_t)v * X.cols + (size_t)b * 256 + 64 * u;
+        const float* xs = X.xs32 + (size_t)v * (X.cols / 16) + (size_t)b * 16 + 4 * u;   // sums of 16
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acc = __fmaf_rn(run_a32<0>(w, xr, r), w.d * (float)w.sc[r], acc);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acc = __fmaf_rn(-xs[r], w.dmin * (float)w.m[r], acc);
+    }
+};
+
+template <>
+struct Fmt<QMV_Q3_K> : FmtK2Base<QMV_Q3_K> {
+    static constexpr int BB = 110;
+    // Six-bit scale s (0..15): low 4 bits from byte s (low nibble, s < 8) or
+    // byte s-8 (high nibble), high 2 bits from bits 2*(s/4) of byte 8 + s%4.
+    static __device__ __forceinline__ int scale6(const uint32_t (&f)[3], int s)
+    {
+        const uint32_t lo = s < 8 ? (f[s >> 2] >> (8 * (s & 3))) & 15u : (f[(s - 8) >> 2] >> (8 * ((s - 8) & 3) + 4)) & 15u;
+        const uint32_t hi = (f[2] >> (8 * (s & 3) + 2 * (s >> 2))) & 3u;
+        return (int)(lo | (hi << 4)) - 32;
+    }
+    static __device__ __forceinline__ void load(const uint8_t* blk, int u, W& w)
+    {
+        const int n = u >> 1, j0 = 2 * (u & 1);
+        uint32_t q[8], hm[8], f[3];
+        load_words<8>(blk + 32 + 32 * n, q);
+        load_words<8>(blk, hm);
+        load_words<3>(blk + 96, f);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            // code + 4 = low bits | high bit << 2, in 0..7
+            w.c[0][k] = ((q[k] >> (2 * j0)) & 0x03030303u) | (((hm[k] >> (4 * n + j0)) & 0x01010101u) << 2);
+            w.c[1][k] = ((q[k] >> (2 * j0 + 2)) & 0x03030303u) | (((hm[k] >> (4 * n + j0 + 1)) & 0x01010101u) << 2);
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) w.sc[r] = scale6(f, 4 * u + r);
+        w.d = half_bits_to_float(ld_u16(blk + 108));
+    }
+    static __device__ __forceinline__ void ints(const W& w, const XA8& x, int& S, int& Mn)
+    {
+        S = 0;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) S += w.sc[r] * (run_dot(w, x, r) - 4 * x.s[r]);
+        Mn = 0;
+    }
+    static __device__ __forceinline__ void acc_a8(const W& w, const XA8& x, float& acc)
+    {
+        int S, Mn;
+        ints(w, x, S, Mn);
+        acc = __fmaf_rn((float)S, w.d * x.d, acc);
+    }
+    static __device__ __forceinline__ void acc_a32(const W& w, const XView& X, int v, int b, int u, float& acc)
+    {
+        const float* xr = X.xf + (size_t)v * X.cols + (size_t)b * 256 + 64 * u;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acc = __fmaf_rn(run_a32<4>(w, xr, r), w.d * (float)w.sc[r], acc);
+    }
+};
+
+// ------------------------------------------------------------------------------
+// Plain weights (F32, F16, BF16) with fp32 activations: a unit is 8 weights
+// (16 or 32 bytes, 16-byte aligned when rows are multiples of 8 elements).
+// ------------------------------------------------------------------------------
+struct WP {
+    float w[8];
+};
+
+template <int T>
+struct FmtPlain {
+    static constexpr int BS = 8, UE = 8, UPB = 1;
+    static constexpr int BB = T == QMV_F32 ? 32 : 16;
+    using W = WP;
+    using XA8 = int;   // no 8-bit activation form
+    static __device__ __forceinline__ void load(const uint8_t* blk, int, W& w)
+    {
+        if constexpr (T == QMV_F32) {
+            const float4 a = reinterpret_cast<const float4*>(blk)[0], b = reinterpret_cast<const float4*>(blk)[1];
+            w.w[0] = a.x; w.w[1] = a.y; w.w[2] = a.z; w.w[3] = a.w;
+            w.w[4] = b.x; w.w[5] = b.y; w.w[6] = b.z; w.w[7] = b.w;
+        } else {
+            const uint4 a = *reinterpret_cast<const uint4*>(blk);
+            const uint32_t h[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                if constexpr (T == QMV_F16) {
+                    w.w[2 * k] = half_bits_to_float(h[k] & 0xffffu);
+                    w.w[2 * k + 1] = half_bits_to_float(h[k] >> 16);
+                } else {
+                    w.w[2 * k] = __uint_as_float(h[k] << 16);
+                    w.w[2 * k + 1] = __uint_as_float(h[k] & 0xffff0000u);
+                }
+            }
+        }
+    }
+    static __device__ __forceinline__ void acc_a32(const W& w, const XView& X, int v, int b, int, float& acc)
+    {
+        const float4* xp = reinterpret_cast<const float4*>(X.xf + (size_t)v * X.cols + (size_t)b * 8);
+        const float4 a = xp[0], c = xp[1];
+        float p = __fmul_rn(w.w[0], a.x);
+        p = __fmaf_rn(w.w[1], a.y, p);
+        p = __fmaf_rn(w.w[2], a.z, p);
+        p = __fmaf_rn(w.w[3], a.w, p);
+        p = __fmaf_rn(w.w[4], c.x, p);
+        p = __fmaf_rn(w.w[5], c.y, p);
+        p = __fmaf_rn(w.w[6], c.z, p);
+        p = __fmaf_rn(w.w[7], c.w, p);
+        acc = __fadd_rn(acc, p);
+    }
+};
+template <> struct Fmt<QMV_F32> : FmtPlain<QMV_F32> {};
+template <> struct Fmt<QMV_F16> : FmtPlain<QMV_F16> {};
+template <> struct Fmt<QMV_BF16> : FmtPlain<QMV_BF16> {};
+
 // ---- the 32-element formats' products ------------------------------------------
 template <int T>
-__device__ __forceinline__ void ints32(const W32& w, const typename Fmt<T>::XA8& x, int& S, int& Mn)
+__device__ __forceinline__ void ints32(const typename Fmt<T>::W& w, const typename Fmt<T>::XA8& x, int& S, int& Mn)
 {
     int dot = 0;
 #pragma unroll
     for (int k = 0; k < 8; ++k)
         dot = Fmt<T>::SIGNED ? dp4a_ss(w.c[k], x.w[k], dot) : dp4a_us(w.c[k], x.w[k], dot);
     S = dot - Fmt<T>::OFF * x.sum;
-    Mn = 0;
+    Mn = Fmt<T>::MIN ? x.sum : 0;
 }
 
 template <int T>
-__device__ __forceinline__ void acc32_a8(const W32& w, const typename Fmt<T>::XA8& x, float& acc)
+__device__ __forceinline__ void acc32_a8(const typename Fmt<T>::W& w, const typename Fmt<T>::XA8& x, float& acc)
 {
     int S, Mn;
     ints32<T>(w, x, S, Mn);
     acc = __fmaf_rn((float)S, w.d * x.d, acc);
+    if constexpr (Fmt<T>::MIN) acc = __fmaf_rn((float)Mn, w.m * x.d, acc);
 }
 
 template <int T>
-__device__ __forceinline__ void acc32_a32(const W32& w, const XView& X, int v, int b, float& acc)
+__device__ __forceinline__ void acc32_a32(const typename Fmt<T>::W& w, const XView& X, int v, int b, float& acc)
 {
     // Unsigned codes minus OFF; signed codes are biased by 128 first.
     constexpr float kOff = 8388608.f + (Fmt<T>::SIGNED ? 128.f : (float)Fmt<T>::OFF);
@@ -432,6 +750,7 @@ __device__ __forceinline__ void acc32_a32(const W32& w, const XView& X, int v, i
         p = __fmaf_rn(ubyte_to_float_minus(c, 3, kOff), xa.w, p);
     }
     acc = __fmaf_rn(p, w.d, acc);
+    if constexpr (Fmt<T>::MIN) acc = __fmaf_rn(X.xs32[(size_t)v * (X.cols / 32) + b], w.m, acc);   // m * sum x
 }
 
 // Uniform entry points over all formats.
@@ -443,12 +762,12 @@ struct Ops {
     static __device__ __forceinline__ void ints(const W& w, const XA8& x, int& S, int& Mn)
     {
         if constexpr (F::BS == 32) ints32<T>(w, x, S, Mn);
-        else F::ints(w, x, S, Mn);
+        else if constexpr (F::BS == 256) F::ints(w, x, S, Mn);
     }
     static __device__ __forceinline__ void acc_a8(const W& w, const XA8& x, float& acc)
     {
         if constexpr (F::BS == 32) acc32_a8<T>(w, x, acc);
-        else F::acc_a8(w, x, acc);
+        else if constexpr (F::BS == 256) F::acc_a8(w, x, acc);
     }
     static __device__ __forceinline__ void acc_a32(const W& w, const XView& X, int v, int b, int sub, float& acc)
     {
@@ -469,13 +788,13 @@ __device__ __forceinline__ int staged_pos(int i)
 // Bytes of staged activation codes for g vectors (8-bit staging).
 __host__ __device__ inline size_t xcode_bytes(int T, int g, int cols)
 {
-    return (T == QMV_Q4_K || T == QMV_Q6_K) ? (size_t)g * (cols / 256) * kKPitch : (size_t)g * (cols / 32) * kBPitch;
+    return kq_rt(T) ? (size_t)g * (cols / 256) * kKPitch : (size_t)g * (cols / 32) * kBPitch;
 }
 
 // Bytes of staged activations for g vectors of `cols` elements.
 __host__ __device__ inline size_t xhat_bytes(int T, bool a8, int g, int cols)
 {
-    const int bs = (T == QMV_Q4_K || T == QMV_Q6_K) ? 256 : 32;
+    const int bs = kq_rt(T) ? 256 : 32;
     const size_t nb = (size_t)cols / bs;
     auto r16 = [](size_t v) { return (v + 15) & ~size_t(15); };
     if (a8) {
@@ -484,7 +803,7 @@ __host__ __device__ inline size_t xhat_bytes(int T, bool a8, int g, int cols)
         return s;
     }
     size_t s = r16((size_t)g * cols * 4);
-    if (T == QMV_Q4_K) s += r16((size_t)g * (cols / 32) * 4);
+    if (xsum_run_rt(T)) s += r16((size_t)g * (cols / xsum_run_rt(T)) * 4);
     return s;
 }
 
@@ -773,19 +1092,21 @@ __device__ __forceinline__ void stage_xhat_a8_natural(uint8_t* base, bool quant_
     stage_xhat<T, true>(base, true, quant_x, x, xrow, nullptr, g, cols, tid, nth);
 }
 
-// Per-32 sums of staged fp32 activations (A32 Q4_K), in a fixed order; run
-// after the staging is visible to these threads.
+// Sums of each run of R staged fp32 activations (R = xsum_run_rt(T): the
+// formats whose weights carry a per-run offset), in a fixed order; run after
+// the staging is visible to these threads.
 template <int T>
 __device__ void stage_xsum32(uint8_t* base, int g, int cols, int tid, int nth)
 {
-    if constexpr (T == QMV_Q4_K) {
+    constexpr int R = xsum_run_rt(T);
+    if constexpr (R > 0) {
         auto r16 = [](size_t v) { return (v + 15) & ~size_t(15); };
         const float* xf = reinterpret_cast<const float*>(base);
-        float* xs32 = reinterpret_cast<float*>(base + r16((size_t)g * cols * 4));
-        for (int i = tid; i < g * cols / 32; i += nth) {
+        float* xs = reinterpret_cast<float*>(base + r16((size_t)g * cols * 4));
+        for (int i = tid; i < g * cols / R; i += nth) {
             float s = 0.f;
-            for (int k = 0; k < 32; ++k) s += xf[(size_t)i * 32 + k];
-            xs32[i] = s;
+            for (int k = 0; k < R; ++k) s += xf[(size_t)i * R + k];
+            xs[i] = s;
         }
     }
 }

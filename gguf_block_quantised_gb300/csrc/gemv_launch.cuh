@@ -22,7 +22,7 @@ constexpr size_t kSmemOnePerSm = 227 * 1024;
 
 inline int act_block_bytes(int wtype)
 {
-    return (wtype == QMV_Q4_K || wtype == QMV_Q6_K) ? 292 : 34;
+    return kq_rt(wtype) ? 292 : 34;
 }
 
 // Rows a consumer warp decodes at once: fewer as the vector count (and with
@@ -30,12 +30,12 @@ inline int act_block_bytes(int wtype)
 template <int T, int NV>
 constexpr int rows_in_flight()
 {
-    return Fmt<T>::BS == 32 ? (NV <= 2 ? 4 : 2) : (NV <= 4 ? 2 : 1);
+    return Fmt<T>::BS != 256 ? (NV <= 2 ? 4 : 2) : (NV <= 4 ? 2 : 1);
 }
 
 inline int rows_in_flight_rt(int T, int nv)
 {
-    const bool b32 = !(T == QMV_Q4_K || T == QMV_Q6_K);
+    const bool b32 = !kq_rt(T);
     const int NV = nv <= 1 ? 1 : nv <= 2 ? 2 : nv <= 4 ? 4 : nv <= 8 ? 8 : 16;
     return b32 ? (NV <= 2 ? 4 : 2) : (NV <= 4 ? 2 : 1);
 }
@@ -139,6 +139,9 @@ inline int launch_gemv_t(bool a8, bool quant_x, bool pdl, const void* W, int64_t
 {
     using F = Fmt<T>;
     if (rows == 0 || n_vec == 0) return 0;
+    if constexpr (plain_rt(T)) {
+        if (a8) return -3;   // plain weights take fp32 activations only
+    }
     GemvPlan pl;
     // Small matrices get shorter tiles so that more SMs take part (the tile
     // shape does not enter the arithmetic of any output).
@@ -165,7 +168,9 @@ inline int launch_gemv_t(bool a8, bool quant_x, bool pdl, const void* W, int64_t
         p.nv = min(pl.group, n_vec - v0);
         p.x = static_cast<const uint8_t*>(x) + (size_t)v0 * xrow;
         p.y = y + (int64_t)v0 * rows;
-        const int rc = a8 ? launch_gemv_group<T, true>(p, pl, pdl, st) : launch_gemv_group<T, false>(p, pl, pdl, st);
+        int rc;
+        if constexpr (plain_rt(T)) rc = launch_gemv_group<T, false>(p, pl, pdl, st);
+        else rc = a8 ? launch_gemv_group<T, true>(p, pl, pdl, st) : launch_gemv_group<T, false>(p, pl, pdl, st);
         if (rc) return rc;
     }
     return 0;
@@ -198,6 +203,9 @@ inline int launch_moe_t(bool a8, bool quant_x, const void* W3d, int n_expert, in
 {
     using F = Fmt<T>;
     if (rows == 0 || n_pairs == 0) return 0;
+    if constexpr (plain_rt(T)) {
+        if (a8) return -3;
+    }
     GemvPlan pl;
     // Small tiles (as many rows per warp as the kernel decodes at once) so an
     // expert's rows spread over many SMs; the stage ring is sized for that tile.
@@ -232,12 +240,14 @@ inline int launch_moe_t(bool a8, bool quant_x, const void* W3d, int n_expert, in
     // Grid rows map onto the experts that received pairs (at most this many).
     const int active = n_pairs < n_expert ? n_pairs : n_expert;
     const int g = pl.group;
-    if (a8) {
-        if (g <= 1) return launch_moe_nv<T, true, 1>(mp, pl, active, active, st);
-        if (g <= 2) return launch_moe_nv<T, true, 2>(mp, pl, active, active, st);
-        if (g <= 4) return launch_moe_nv<T, true, 4>(mp, pl, active, active, st);
-        if (g <= 8) return launch_moe_nv<T, true, 8>(mp, pl, active, active, st);
-        return launch_moe_nv<T, true, 16>(mp, pl, active, active, st);
+    if constexpr (!plain_rt(T)) {
+        if (a8) {
+            if (g <= 1) return launch_moe_nv<T, true, 1>(mp, pl, active, active, st);
+            if (g <= 2) return launch_moe_nv<T, true, 2>(mp, pl, active, active, st);
+            if (g <= 4) return launch_moe_nv<T, true, 4>(mp, pl, active, active, st);
+            if (g <= 8) return launch_moe_nv<T, true, 8>(mp, pl, active, active, st);
+            return launch_moe_nv<T, true, 16>(mp, pl, active, active, st);
+        }
     }
     if (g <= 1) return launch_moe_nv<T, false, 1>(mp, pl, active, active, st);
     if (g <= 2) return launch_moe_nv<T, false, 2>(mp, pl, active, active, st);

@@ -98,6 +98,15 @@ QMV_MOE_DECL(qmv_moe_q8_0)
 QMV_MOE_DECL(qmv_moe_mxfp4)
 QMV_MOE_DECL(qmv_moe_q4_k)
 QMV_MOE_DECL(qmv_moe_q6_k)
+QMV_MOE_DECL(qmv_moe_q4_1)
+QMV_MOE_DECL(qmv_moe_q5_1)
+QMV_MOE_DECL(qmv_moe_q8_1)
+QMV_MOE_DECL(qmv_moe_q2_k)
+QMV_MOE_DECL(qmv_moe_q3_k)
+QMV_MOE_DECL(qmv_moe_q5_k)
+QMV_MOE_DECL(qmv_moe_f32)
+QMV_MOE_DECL(qmv_moe_f16)
+QMV_MOE_DECL(qmv_moe_bf16)
 
 size_t qmv_moe_gemm_extra_bytes(int64_t cols, int64_t n_pairs);
 int qmv_launch_moe_gemm_mxfp4(const void* W3d, bool planar, int n_expert, int64_t rows, int64_t cols, const void* x,
@@ -131,7 +140,7 @@ int qmv_launch_moe(int wtype, bool a8, bool quant_x, bool bf16, size_t act_block
     float* part = reinterpret_cast<float*>(w + r256(2050 * 4) + r256((size_t)n_pairs * 4));
     k_moe_group<<<1, 1024, 0, st>>>(ids, (int)n_pairs, n_expert, offsets, active, perm, status_word());
     if (cudaGetLastError() != cudaSuccess) return -6;
-    const size_t xrow = (a8 && !quant_x) ? (size_t)(cols / (wtype == QMV_Q4_K || wtype == QMV_Q6_K ? 256 : 32)) *
+    const size_t xrow = (a8 && !quant_x) ? (size_t)(cols / (kq_rt(wtype) ? 256 : 32)) *
                                                act_block_bytes
                                          : (size_t)cols * 4;
     const int kdiv = gates ? 1 : k;
@@ -154,6 +163,15 @@ int qmv_launch_moe(int wtype, bool a8, bool quant_x, bool bf16, size_t act_block
     case QMV_MXFP4: rc = QMV_MOE_CALL(qmv_moe_mxfp4); break;
     case QMV_Q4_K: rc = QMV_MOE_CALL(qmv_moe_q4_k); break;
     case QMV_Q6_K: rc = QMV_MOE_CALL(qmv_moe_q6_k); break;
+    case QMV_Q4_1: rc = QMV_MOE_CALL(qmv_moe_q4_1); break;
+    case QMV_Q5_1: rc = QMV_MOE_CALL(qmv_moe_q5_1); break;
+    case QMV_Q8_1: rc = QMV_MOE_CALL(qmv_moe_q8_1); break;
+    case QMV_Q2_K: rc = QMV_MOE_CALL(qmv_moe_q2_k); break;
+    case QMV_Q3_K: rc = QMV_MOE_CALL(qmv_moe_q3_k); break;
+    case QMV_Q5_K: rc = QMV_MOE_CALL(qmv_moe_q5_k); break;
+    case QMV_F32: rc = QMV_MOE_CALL(qmv_moe_f32); break;
+    case QMV_F16: rc = QMV_MOE_CALL(qmv_moe_f16); break;
+    case QMV_BF16: rc = QMV_MOE_CALL(qmv_moe_bf16); break;
     }
 #undef QMV_MOE_CALL
     if (rc) return rc;

@@ -47,25 +47,41 @@ __global__ void k_dequant(const uint8_t* __restrict__ W, int64_t rows, int cols,
     for (int sub = 0; sub < F::UPB; ++sub) {
         typename F::W w;
         F::load(buf, sub, w);
-        if constexpr (F::BS == 32) {
+        if constexpr (plain_rt(T)) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) o[k] = w.w[k];
+        } else if constexpr (F::BS == 32) {
 #pragma unroll
             for (int k = 0; k < 8; ++k)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const uint32_t byte = (w.c[k] >> (8 * j)) & 0xffu;
                     const int q = F::SIGNED ? (int)(int8_t)byte : (int)byte - F::OFF;
-                    o[elem_of<T>(sub, k, j)] = w.d * (float)q;   // exact: <= 24 significant bits
+                    if constexpr (F::MIN) o[elem_of<T>(sub, k, j)] = __fmaf_rn(w.d, (float)q, w.m);   // one rounding
+                    else o[elem_of<T>(sub, k, j)] = w.d * (float)q;   // exact: <= 24 significant bits
                 }
-        } else if constexpr (T == QMV_Q4_K) {
+        } else if constexpr (T == QMV_Q4_K || T == QMV_Q5_K) {
+            constexpr uint32_t mask = T == QMV_Q5_K ? 31u : 15u;
             const float D0 = w.d * (float)w.sc0, D1 = w.d * (float)w.sc1;       // exact
             const float M0 = w.dmin * (float)w.m0, M1 = w.dmin * (float)w.m1;   // exact
 #pragma unroll
             for (int k = 0; k < 8; ++k)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    o[64 * sub + 4 * k + j] = __fmaf_rn(D0, (float)((w.lo[k] >> (8 * j)) & 15u), -M0);
-                    o[64 * sub + 32 + 4 * k + j] = __fmaf_rn(D1, (float)((w.hi[k] >> (8 * j)) & 15u), -M1);
+                    o[64 * sub + 4 * k + j] = __fmaf_rn(D0, (float)((w.lo[k] >> (8 * j)) & mask), -M0);
+                    o[64 * sub + 32 + 4 * k + j] = __fmaf_rn(D1, (float)((w.hi[k] >> (8 * j)) & mask), -M1);
                 }
+        } else if constexpr (T == QMV_Q2_K || T == QMV_Q3_K) {
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const float D = w.d * (float)w.sc[r];   // exact
+                const float M = T == QMV_Q2_K ? w.dmin * (float)w.m[r] : 0.f;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int c = (int)((w.c[r >> 1][4 * (r & 1) + (i >> 2)] >> (8 * (i & 3))) & 0xffu);
+                    o[64 * sub + 16 * r + i] = T == QMV_Q2_K ? __fmaf_rn(D, (float)c, -M) : D * (float)(c - 4);
+                }
+            }
         } else {   // Q6_K
             const int h = sub >> 1, lh = sub & 1;
 #pragma unroll
@@ -171,6 +187,15 @@ int qmv_launch_dequant(int t, const void* W, int64_t rows, int64_t cols, float* 
     case QMV_MXFP4: return launch_dequant_t<QMV_MXFP4>(W, rows, cols, out, st);
     case QMV_Q4_K: return launch_dequant_t<QMV_Q4_K>(W, rows, cols, out, st);
     case QMV_Q6_K: return launch_dequant_t<QMV_Q6_K>(W, rows, cols, out, st);
+    case QMV_Q4_1: return launch_dequant_t<QMV_Q4_1>(W, rows, cols, out, st);
+    case QMV_Q5_1: return launch_dequant_t<QMV_Q5_1>(W, rows, cols, out, st);
+    case QMV_Q8_1: return launch_dequant_t<QMV_Q8_1>(W, rows, cols, out, st);
+    case QMV_Q2_K: return launch_dequant_t<QMV_Q2_K>(W, rows, cols, out, st);
+    case QMV_Q3_K: return launch_dequant_t<QMV_Q3_K>(W, rows, cols, out, st);
+    case QMV_Q5_K: return launch_dequant_t<QMV_Q5_K>(W, rows, cols, out, st);
+    case QMV_F32: return launch_dequant_t<QMV_F32>(W, rows, cols, out, st);
+    case QMV_F16: return launch_dequant_t<QMV_F16>(W, rows, cols, out, st);
+    case QMV_BF16: return launch_dequant_t<QMV_BF16>(W, rows, cols, out, st);
     default: return -3;
     }
 }
@@ -186,6 +211,12 @@ int qmv_launch_block_dots(int t, const void* W, int64_t rows, int64_t cols, cons
     case QMV_MXFP4: return launch_dots_t<QMV_MXFP4>(W, rows, cols, xq, n_vec, out, st);
     case QMV_Q4_K: return launch_dots_t<QMV_Q4_K>(W, rows, cols, xq, n_vec, out, st);
     case QMV_Q6_K: return launch_dots_t<QMV_Q6_K>(W, rows, cols, xq, n_vec, out, st);
+    case QMV_Q4_1: return launch_dots_t<QMV_Q4_1>(W, rows, cols, xq, n_vec, out, st);
+    case QMV_Q5_1: return launch_dots_t<QMV_Q5_1>(W, rows, cols, xq, n_vec, out, st);
+    case QMV_Q8_1: return launch_dots_t<QMV_Q8_1>(W, rows, cols, xq, n_vec, out, st);
+    case QMV_Q2_K: return launch_dots_t<QMV_Q2_K>(W, rows, cols, xq, n_vec, out, st);
+    case QMV_Q3_K: return launch_dots_t<QMV_Q3_K>(W, rows, cols, xq, n_vec, out, st);
+    case QMV_Q5_K: return launch_dots_t<QMV_Q5_K>(W, rows, cols, xq, n_vec, out, st);
     default: return -3;
     }
 }

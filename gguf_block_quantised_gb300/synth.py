@@ -11,6 +11,9 @@ Distributions (model-shaped synthetic weights; no trained weights are used):
   Q8_0 codes                : uniform int8 in [-127, 127]
   Q4_K 12-byte scale field  : uniform bytes
   Q6_K int8 sub-block scales: uniform int8 in [-128, 127]
+  Q4_1/Q5_1 offsets m      : fp16(N(0,1) * 0.1)
+  K-quant scale/mask fields: uniform bytes (Q2_K, Q3_K, Q5_K)
+  plain F32/F16/BF16       : N(0,1) * 0.05 (F16 rounded, BF16 its upper 16 bits)
   MXFP4 E8M0 exponent       : uniform in [118, 130]
   activations               : fp32 N(0,1)
   expert biases             : fp32 N(0,1) * 0.02
@@ -23,10 +26,14 @@ from __future__ import annotations
 import numpy as np
 
 Q4_0, Q5_0, Q8_0, Q4_K, Q6_K, MXFP4, Q8_K, F32, BF16 = 1, 2, 3, 4, 5, 6, 7, 8, 9
-BLOCK_ELEMS = {Q4_0: 32, Q5_0: 32, Q8_0: 32, MXFP4: 32, Q4_K: 256, Q6_K: 256, Q8_K: 256}
-BLOCK_BYTES = {Q4_0: 18, Q5_0: 22, Q8_0: 34, MXFP4: 17, Q4_K: 144, Q6_K: 210, Q8_K: 292}
+Q4_1, Q5_1, Q8_1, Q2_K, Q3_K, Q5_K, F16 = 11, 12, 13, 14, 15, 16, 17
+BLOCK_ELEMS = {Q4_0: 32, Q5_0: 32, Q8_0: 32, MXFP4: 32, Q4_K: 256, Q6_K: 256, Q8_K: 256,
+               Q4_1: 32, Q5_1: 32, Q8_1: 32, Q2_K: 256, Q3_K: 256, Q5_K: 256, F32: 1, F16: 1, BF16: 1}
+BLOCK_BYTES = {Q4_0: 18, Q5_0: 22, Q8_0: 34, MXFP4: 17, Q4_K: 144, Q6_K: 210, Q8_K: 292,
+               Q4_1: 20, Q5_1: 24, Q8_1: 36, Q2_K: 84, Q3_K: 110, Q5_K: 176, F32: 4, F16: 2, BF16: 2}
 NAMES = {Q4_0: "Q4_0", Q5_0: "Q5_0", Q8_0: "Q8_0", Q4_K: "Q4_K", Q6_K: "Q6_K",
-         MXFP4: "MXFP4", Q8_K: "Q8_K", F32: "F32", BF16: "BF16"}
+         MXFP4: "MXFP4", Q8_K: "Q8_K", F32: "F32", BF16: "BF16", Q4_1: "Q4_1", Q5_1: "Q5_1",
+         Q8_1: "Q8_1", Q2_K: "Q2_K", Q3_K: "Q3_K", Q5_K: "Q5_K", F16: "F16"}
 
 # Field layouts of one block, in storage order (little-endian).
 _LAYOUT = {
@@ -36,6 +43,12 @@ _LAYOUT = {
     MXFP4: [("e", "u1", ()), ("qs", "u1", (16,))],
     Q4_K: [("d", "<f2", ()), ("dmin", "<f2", ()), ("scales", "u1", (12,)), ("qs", "u1", (128,))],
     Q6_K: [("ql", "u1", (128,)), ("qh", "u1", (64,)), ("scales", "i1", (16,)), ("d", "<f2", ())],
+    Q4_1: [("d", "<f2", ()), ("m", "<f2", ()), ("qs", "u1", (16,))],
+    Q5_1: [("d", "<f2", ()), ("m", "<f2", ()), ("qh", "<u4", ()), ("qs", "u1", (16,))],
+    Q8_1: [("d", "<f2", ()), ("s", "<f2", ()), ("qs", "i1", (32,))],
+    Q5_K: [("d", "<f2", ()), ("dmin", "<f2", ()), ("scales", "u1", (12,)), ("qh", "u1", (32,)), ("qs", "u1", (128,))],
+    Q2_K: [("scales", "u1", (16,)), ("qs", "u1", (64,)), ("d", "<f2", ()), ("dmin", "<f2", ())],
+    Q3_K: [("hmask", "u1", (32,)), ("qs", "u1", (64,)), ("scales", "u1", (12,)), ("d", "<f2", ())],
 }
 
 
@@ -58,7 +71,16 @@ def _fp16_scales(g: np.random.Generator, n: int) -> np.ndarray:
 
 
 def weights(t: int, rows: int, cols: int, seed: int = 0, tensor_id: int = 0) -> np.ndarray:
-    """rows x cols weights of block type t as a flat uint8 array (GGUF row-major blocks)."""
+    """rows x cols weights of block type t as a flat uint8 array (GGUF row-major blocks;
+    plain F32/F16/BF16: N(0,1)*0.05 rounded to the type, row-major values)."""
+    if t in (F32, F16, BF16):
+        w = rng(seed, tensor_id).standard_normal((rows, cols), dtype=np.float32) * np.float32(0.05)
+        if t == F32:
+            return w.view(np.uint8).reshape(-1)
+        if t == F16:
+            return w.astype(np.float16).view(np.uint8).reshape(-1)
+        # bfloat16 values: the upper 16 bits of the fp32 draws
+        return (w.view(np.uint32) >> 16).astype(np.uint16).view(np.uint8).reshape(-1)
     assert cols % BLOCK_ELEMS[t] == 0
     nblk = rows * (cols // BLOCK_ELEMS[t])
     g = rng(seed, tensor_id)
@@ -83,6 +105,32 @@ def weights(t: int, rows: int, cols: int, seed: int = 0, tensor_id: int = 0) -> 
         a["ql"] = g.integers(0, 256, size=(nblk, 128), dtype=np.uint8)
         a["qh"] = g.integers(0, 256, size=(nblk, 64), dtype=np.uint8)
         a["scales"] = g.integers(-128, 128, size=(nblk, 16), dtype=np.int8)
+        a["d"] = _fp16_scales(g, nblk)
+    elif t in (Q4_1, Q5_1):
+        a["d"] = _fp16_scales(g, nblk)
+        a["m"] = (g.standard_normal(nblk, dtype=np.float32) * np.float32(0.1)).astype(np.float16)
+        if t == Q5_1:
+            a["qh"] = g.integers(0, 2**32, size=nblk, dtype=np.uint32)
+        a["qs"] = g.integers(0, 256, size=(nblk, 16), dtype=np.uint8)
+    elif t == Q8_1:
+        a["d"] = _fp16_scales(g, nblk)
+        a["s"] = (g.standard_normal(nblk, dtype=np.float32)).astype(np.float16)   # not read as a weight
+        a["qs"] = g.integers(-127, 128, size=(nblk, 32), dtype=np.int8)
+    elif t == Q5_K:
+        a["d"] = _fp16_scales(g, nblk)
+        a["dmin"] = _fp16_scales(g, nblk)
+        a["scales"] = g.integers(0, 256, size=(nblk, 12), dtype=np.uint8)
+        a["qh"] = g.integers(0, 256, size=(nblk, 32), dtype=np.uint8)
+        a["qs"] = g.integers(0, 256, size=(nblk, 128), dtype=np.uint8)
+    elif t == Q2_K:
+        a["scales"] = g.integers(0, 256, size=(nblk, 16), dtype=np.uint8)
+        a["qs"] = g.integers(0, 256, size=(nblk, 64), dtype=np.uint8)
+        a["d"] = _fp16_scales(g, nblk)
+        a["dmin"] = _fp16_scales(g, nblk)
+    elif t == Q3_K:
+        a["hmask"] = g.integers(0, 256, size=(nblk, 32), dtype=np.uint8)
+        a["qs"] = g.integers(0, 256, size=(nblk, 64), dtype=np.uint8)
+        a["scales"] = g.integers(0, 256, size=(nblk, 12), dtype=np.uint8)
         a["d"] = _fp16_scales(g, nblk)
     else:
         raise ValueError(f"not a weight block type: {t}")

@@ -65,10 +65,22 @@ typedef enum {
     QMV_Q8_K = 7,   /* activations only, 256 w, 292 B: fp32 d | int8[256] | int16 bsums[16]      */
     QMV_F32 = 8,    /* plain fp32 */
     QMV_BF16 = 9,   /* plain bfloat16 */
-    QMV_MXFP4_R = 10 /* MXFP4 rows repacked by qmv_repack: the 16 code bytes of each 32-element
+    QMV_MXFP4_R = 10, /* MXFP4 rows repacked by qmv_repack: the 16 code bytes of each 32-element
                         block in block order, then the row's E8M0 bytes, zero-padded to a
                         multiple of 16 bytes (row bytes = 16*ceil(17*cols/32/16)).  Weights of
                         qmv_moe_matvec with BF16 activations only. */
+    QMV_Q4_1 = 11,  /* 32 w, 20 B: fp16 d | fp16 m | 16 B nibbles;      w = d*q + m            */
+    QMV_Q5_1 = 12,  /* 32 w, 24 B: fp16 d | fp16 m | u32 5th bits | 16 B nibbles; w = d*q + m  */
+    QMV_Q8_1 = 13,  /* 32 w, 36 B: fp16 d | fp16 s (block sum, unused by weights) | int8[32];
+                                                                         w = d*q                */
+    QMV_Q2_K = 14,  /* 256 w, 84 B: 16 B 4-bit sc|m per 16 | 64 B 2-bit codes | fp16 d | fp16 dmin;
+                                                                         w = d*sc*q - dmin*m    */
+    QMV_Q3_K = 15,  /* 256 w, 110 B: 32 B high bits | 64 B 2-bit codes | 12 B 6-bit scales | fp16 d;
+                                                                         w = d*(s-32)*(q-4)     */
+    QMV_Q5_K = 16,  /* 256 w, 176 B: Q4_K's d, dmin, 12 B sc/m | 32 B fifth bits | 128 B nibbles;
+                                                                         w = d*sc*q - dmin*m    */
+    QMV_F16 = 17    /* plain IEEE half (weights) */
+    /* QMV_F32 and QMV_BF16 are also accepted as plain weight types. */
 } qmv_type;
 
 /* A multiply's format is the weight type plus the activation type. */
@@ -194,8 +206,10 @@ int qmv_block_dots(int type, const void* W, int64_t rows, int64_t cols,
  * qmv_matvec -- decode: y[v][r] = sum_c w[r][c] * xhat[v][c] for n_vec
  * vectors sharing one pass over the weights ("The package map", pkg/tensor
  * MatVec; "A request, end to end": N sequences read the weights once).
- *   fmt : QMV_FMT(wtype, atype), wtype in {Q4_0, Q5_0, Q8_0, MXFP4} with atype
- *         in {F32, Q8_0}, or wtype in {Q4_K, Q6_K} with atype in {F32, Q8_K};
+ *   fmt : QMV_FMT(wtype, atype): the 32-element formats {Q4_0, Q4_1, Q5_0,
+ *         Q5_1, Q8_0, Q8_1, MXFP4} with atype in {F32, Q8_0}; the K-quants
+ *         {Q2_K, Q3_K, Q4_K, Q5_K, Q6_K} with atype in {F32, Q8_K}; the plain
+ *         weights {F32, F16, BF16} with atype F32 (cols a multiple of 8);
  *         optionally | QMV_FLAG_QUANTIZE_X (8-bit atype only) | QMV_FLAG_PDL.
  *   x   : F32: fp32 [n_vec][cols], 16-byte aligned, xhat = x.
  *         Q8_0/Q8_K: [n_vec][cols/bs] blocks from qmv_quantize_act,

@@ -6,6 +6,15 @@ import torch
 
 TOL = 1e-4
 
+# The library's type numbers (include/qmv.h) and the oracle's own table
+# (oracle/oracle.h) agree on the original formats; the later ones differ.
+_ORC = {11: 10, 12: 11, 13: 15, 14: 13, 15: 14, 16: 12, 17: 16}
+
+
+def orc_t(t):
+    """The oracle's number for library type t."""
+    return _ORC.get(t, t)
+
 
 def dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()

@@ -9,12 +9,13 @@ import pytest
 import torch
 
 from gguf_block_quantised_gb300 import synth
-from gpu_util import assert_close, dev, host
+from gpu_util import assert_close, dev, host, orc_t
 
 pytestmark = pytest.mark.gpu
 
-W32 = [1, 2, 3, 6]          # Q4_0, Q5_0, Q8_0, MXFP4
-WK = [4, 5]                 # Q4_K, Q6_K
+W32 = [1, 2, 3, 6, 11, 12, 13]   # Q4_0, Q5_0, Q8_0, MXFP4, Q4_1, Q5_1, Q8_1
+WK = [4, 5, 14, 15, 16]          # Q4_K, Q6_K, Q2_K, Q3_K, Q5_K
+PLAIN = [8, 17, 9]               # F32, F16, BF16 weights (fp32 activations only)
 ALLW = W32 + WK
 
 
@@ -78,7 +79,7 @@ def test_quantize_act_scale_below_2_pow_minus_128(qmv, orc, atype):
 def test_dequantize_bit_exact(qmv, orc, t):
     for rows, cols in shapes_for(t)[:3]:
         W = synth.weights(t, rows, cols, seed=1, tensor_id=t)
-        ref = orc.dequant(t, W, rows, cols)
+        ref = orc.dequant(orc_t(t), W, rows, cols)
         out = torch.empty((rows, cols), dtype=torch.float32, device="cuda")
         qmv.qmv_dequantize(t, dev(W), rows, cols, out)
         assert np.array_equal(host(out).view(np.uint32), ref.view(np.uint32)), (t, rows, cols)
@@ -91,7 +92,7 @@ def test_block_dots_bit_exact(qmv, orc, t):
     W = synth.weights(t, rows, cols, seed=2, tensor_id=t)
     x = synth.activations(n_vec, cols, seed=2)
     xq = orc.quantize_act(act_for(t), x)
-    ref = orc.block_dots(t, W, rows, cols, xq, n_vec)
+    ref = orc.block_dots(orc_t(t), W, rows, cols, xq, n_vec)
     assert np.abs(ref).max() < 2 ** 31
     out = torch.empty(ref.shape, dtype=torch.int32, device="cuda")
     qmv.qmv_block_dots(t, dev(W), rows, cols, dev(xq), n_vec, out)
@@ -107,7 +108,7 @@ def test_matvec_parity(qmv, orc, t, a8):
             W = synth.weights(t, rows, cols, seed=3, tensor_id=rows)
             x = synth.activations(n_vec, cols, seed=3, tensor_id=cols)
             xin = orc.quantize_act(at, x) if a8 else x
-            yref, yabs = orc.matvec(t, at, W, rows, cols, xin, n_vec)
+            yref, yabs = orc.matvec(orc_t(t), at, W, rows, cols, xin, n_vec)
             y = torch.full((n_vec, rows), float("nan"), dtype=torch.float32, device="cuda")
             qmv.qmv_matvec(qmv.FMT(t, at), dev(W), rows, cols, dev(xin), y, n_vec)
             assert_close(host(y), yref, yabs, what=f"t={t} a8={a8} {rows}x{cols} n_vec={n_vec}")
@@ -149,7 +150,7 @@ def test_matvec_quantised_pipeline(qmv, orc):
     qmv.qmv_quantize_act(3, dev(x), xq, n_vec * cols)
     y = torch.empty((n_vec, rows), dtype=torch.float32, device="cuda")
     qmv.qmv_matvec(qmv.FMT(t, 3), dev(W), rows, cols, xq, y, n_vec)
-    yref, yabs = orc.matvec(t, 3, W, rows, cols, orc.quantize_act(3, x), n_vec)
+    yref, yabs = orc.matvec(orc_t(t), 3, W, rows, cols, orc.quantize_act(3, x), n_vec)
     assert_close(host(y), yref, yabs)
 
 
@@ -159,7 +160,7 @@ def test_matvec_edge_cases(qmv, orc):
         t, cols = 6, 32
         W = synth.weights(t, rows, cols, seed=rows)
         x = synth.activations(2, cols, seed=rows)
-        yref, yabs = orc.matvec(t, 8, W, rows, cols, x, 2)
+        yref, yabs = orc.matvec(orc_t(t), 8, W, rows, cols, x, 2)
         y = torch.empty((2, rows), dtype=torch.float32, device="cuda")
         qmv.qmv_matvec(qmv.FMT(t, 8), dev(W), rows, cols, dev(x), y, 2)
         assert_close(host(y), yref, yabs, what=f"mxfp4 rows={rows}")
@@ -211,7 +212,7 @@ def test_config_shapes_sampled(qmv, orc, cfg):
             xin = orc.quantize_act(at, x) if a8 else x
             y = torch.empty((n_vec, rows), dtype=torch.float32, device="cuda")
             qmv.qmv_matvec(qmv.FMT(t, at), Wd, rows, cols, dev(xin), y, n_vec)
-            yref, yabs = orc.matvec(t, at, W, rows, cols, xin, n_vec, row_ids=ids)
+            yref, yabs = orc.matvec(orc_t(t), at, W, rows, cols, xin, n_vec, row_ids=ids)
             assert_close(host(y)[:, ids], yref, yabs, what=f"{cfg} a8={a8} n_vec={n_vec}")
     qmv.qmv_get_status()
 
@@ -283,7 +284,7 @@ def test_matvec_degenerate_blocks(qmv, orc, t):
     x = synth.activations(3, cols, seed=61)
     for at in (at8, 8):
         xin = orc.quantize_act(at, x) if at != 8 else x
-        yref, yabs = orc.matvec(t, at, W, rows, cols, xin, 3)
+        yref, yabs = orc.matvec(orc_t(t), at, W, rows, cols, xin, 3)
         y = torch.full((3, rows), float("nan"), dtype=torch.float32, device="cuda")
         qmv.qmv_matvec(qmv.FMT(t, at) | (qmv.FLAG_QUANTIZE_X if at != 8 else 0), dev(W), rows, cols, dev(x), y, 3)
         yh = host(y)
@@ -317,7 +318,7 @@ def test_matvec_many_vectors(qmv, orc, t, at):
     W = synth.weights(t, rows, cols, seed=80 + t)
     x = synth.activations(n_vec, cols, seed=81)
     xin = orc.quantize_act(at, x) if at != 8 else x
-    yref, yabs = orc.matvec(t, at, W, rows, cols, xin, n_vec)
+    yref, yabs = orc.matvec(orc_t(t), at, W, rows, cols, xin, n_vec)
     y = torch.full((n_vec, rows), float("nan"), dtype=torch.float32, device="cuda")
     qmv.qmv_matvec(qmv.FMT(t, at) | (qmv.FLAG_QUANTIZE_X if at != 8 else 0), dev(W), rows, cols, dev(x), y, n_vec)
     assert_close(host(y), yref, yabs, what=f"t={t} at={at}")
@@ -342,3 +343,67 @@ def test_matvec_longest_rows(qmv, orc):
             qmv.qmv_matvec(fmt, big, rows, c, xb, yb, 1)
         assert e.value.code == qmv.ERR_SHAPE and "shared memory" in str(e.value)
     qmv.qmv_get_status()
+
+
+# ---- plain F32 / F16 / BF16 weights (fp32 activations) -------------------------------
+
+@pytest.mark.parametrize("t", PLAIN)
+def test_plain_weights(qmv, orc, t):
+    """Plain weights: dequantisation is the exact conversion; the matvec
+    matches the oracle within the bar on ragged tiles, several K-chunks and
+    16 vectors; decode is batch-invariant bit for bit; 8-bit activations and
+    rows that are not multiples of 8 are refused."""
+    for rows, cols in [(1, 8), (37, 96), (300, 896), (45, 8288)]:
+        W = synth.weights(t, rows, cols, seed=21, tensor_id=rows)
+        out = torch.empty((rows, cols), dtype=torch.float32, device="cuda")
+        qmv.qmv_dequantize(t, dev(W), rows, cols, out)
+        assert np.array_equal(host(out).view(np.uint32), orc.dequant(orc_t(t), W, rows, cols).view(np.uint32))
+        for n_vec in (1, 3, 16):
+            x = synth.activations(n_vec, cols, seed=22, tensor_id=cols)
+            yref, yabs = orc.matvec(orc_t(t), 8, W, rows, cols, x, n_vec)
+            y = torch.full((n_vec, rows), float("nan"), dtype=torch.float32, device="cuda")
+            qmv.qmv_matvec(qmv.FMT(t, 8), dev(W), rows, cols, dev(x), y, n_vec)
+            assert_close(host(y), yref, yabs, what=f"t={t} {rows}x{cols} n_vec={n_vec}")
+            if n_vec == 16:
+                y1 = torch.empty((1, rows), dtype=torch.float32, device="cuda")
+                qmv.qmv_matvec(qmv.FMT(t, 8), dev(W), rows, cols, dev(x[7:8]), y1, 1)
+                assert np.array_equal(host(y1)[0].view(np.uint32), host(y)[7].view(np.uint32))
+    Wd = dev(synth.weights(t, 4, 64, seed=1))
+    y = torch.empty((1, 4), dtype=torch.float32, device="cuda")
+    with pytest.raises(qmv.QmvError) as e:
+        qmv.qmv_matvec(qmv.FMT(t, 3), Wd, 4, 64, Wd, y, 1)
+    assert e.value.code == qmv.ERR_UNSUPPORTED
+    with pytest.raises(qmv.QmvError) as e:
+        qmv.qmv_matvec(qmv.FMT(t, 8), Wd, 4, 60, Wd, y, 1)
+    assert e.value.code == qmv.ERR_SHAPE
+    qmv.qmv_get_status()
+
+
+@pytest.mark.parametrize("t", [11, 12, 13, 14, 15, 16, 17])
+def test_new_formats_in_the_expert_matvec(qmv, orc, t):
+    """The mixture-of-experts matvec over stacked experts of the later formats,
+    up and down forms, against the oracle."""
+    E, rows, k, n_tok = 5, 40, 2, 7
+    cols = 64 if t in (11, 12, 13, 17) else 512
+    W3 = synth.weights(t, E * rows, cols, seed=33, tensor_id=t)
+    ids, gates = synth.router(n_tok, E, k, seed=34)
+    b = synth.bias(E, rows, seed=35)
+    at = 8 if t == 17 else act_for(t)
+    buf = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    qmv.qmv_set_workspace(buf, buf.numel())
+    try:
+        for down in (False, True):
+            x = synth.activations(n_tok * k if down else n_tok, cols, seed=36)
+            if down:
+                x = x.reshape(n_tok, k, cols)
+            fl = qmv.FLAG_QUANTIZE_X if at != 8 else 0
+            shape = (n_tok, rows) if down else (n_tok, k, rows)
+            y = torch.full(shape, float("nan"), dtype=torch.float32, device="cuda")
+            qmv.qmv_moe_matvec(qmv.FMT(t, at) | fl, dev(W3), E, rows, cols, dev(ids), dev(gates) if down else None,
+                               k, dev(x), y, n_tok, dev(b))
+            x_o = orc.quantize_act(at, x) if at != 8 else x
+            yref, yabs = orc.moe(orc_t(t), at, W3, E, rows, cols, ids, gates if down else None, k, x_o, n_tok, bias=b)
+            assert_close(host(y), yref, yabs, what=f"t={t} down={down}")
+        qmv.qmv_get_status()
+    finally:
+        qmv.qmv_set_workspace(None, 0)
