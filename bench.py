@@ -453,7 +453,7 @@ def kquant_decode_leg(q, torch, stream, hbm):
     before it), round robin over enough weight copies to exceed L2 twice, so
     every launch reads its weights from HBM.  Metric: weight GB/s."""
     shapes = [(Q4_K, 4096, 4096), (Q4_K, 1024, 4096), (Q4_K, 14336, 4096), (Q4_K, 4096, 14336),
-              (Q6_K, 128256, 4096)]
+              (Q6_K, 128256, 4096), (16, 14336, 4096)]
     res = {}
     for t, rows, cols in shapes:
         W0 = torch.from_numpy(synth.weights(t, rows, cols, seed=7)).cuda()
@@ -466,11 +466,43 @@ def kquant_decode_leg(q, torch, stream, hbm):
             reps = max(len(copies), 40)
             ms = time_rotating(torch, stream, calls, reps)
             gbs = W0.numel() / (ms / 1e3) / 1e9
-            res[f"{NAMES[t]}_{rows}x{cols}_nv{nv}"] = {"us": ms * 1e3, "weight_gbs": gbs, "frac_of_hbm": gbs / hbm}
+            res[f"{NAMES.get(t, 'Q5_K')}_{rows}x{cols}_nv{nv}"] = {"us": ms * 1e3, "weight_gbs": gbs,
+                                                                 "frac_of_hbm": gbs / hbm}
         del copies, W0
     q.qmv_get_status(stream)
     return {"metric": "decode matvec weight GB/s (K-quants, Q8_K activations quantised in-kernel, PDL chain)",
             "unit": "GB/s", "by_shape": res}
+
+
+ALL_FORMATS = [(Q4_0, "Q4_0"), (11, "Q4_1"), (Q5_0, "Q5_0"), (12, "Q5_1"), (Q8_0, "Q8_0"), (13, "Q8_1"),
+               (MXFP4, "MXFP4"), (14, "Q2_K"), (15, "Q3_K"), (Q4_K, "Q4_K"), (16, "Q5_K"), (Q6_K, "Q6_K"),
+               (F32, "F32"), (17, "F16"), (BF16, "BF16")]
+
+
+def formats_leg(q, torch, stream, hbm, rows=14336, cols=4096):
+    """Every weight format on one Llama-3-8B-shaped matrix (14336x4096), batch
+    1, launched as in a decode step (PDL chain; 8-bit activations quantised in
+    the kernel for the block formats, fp32 for the plain ones), round robin
+    over enough weight copies (> 300 MB) that every launch reads from HBM.
+    Metric: weight bytes of the format / kernel time."""
+    res = {}
+    x = torch.from_numpy(synth.activations(1, cols, seed=8)).cuda()
+    y = torch.empty((1, rows), dtype=torch.float32, device="cuda")
+    for t, name in ALL_FORMATS:
+        W0 = torch.from_numpy(synth.weights(t, rows, cols, seed=7)).cuda()
+        copies = [W0] + [W0.clone() for _ in range(max(1, -(-300_000_000 // W0.numel())) - 1)]
+        plain = t in (F32, 17, BF16)
+        at = F32 if plain else (Q8_K if t in (Q4_K, Q6_K, 14, 15, 16) else Q8_0)
+        fmt = q.FMT(t, at) | q.FLAG_PDL | (0 if plain else q.FLAG_QUANTIZE_X)
+        calls = [lambda s, W=W: q.qmv_matvec(fmt, W, rows, cols, x, y, 1, s.cuda_stream) for W in copies]
+        ms = time_rotating(torch, stream, calls, max(len(copies), 40))
+        gbs = W0.numel() / (ms / 1e3) / 1e9
+        res[name] = {"us": ms * 1e3, "bytes": W0.numel(), "bytes_per_weight": W0.numel() / (rows * cols),
+                     "weight_gbs": gbs, "frac_of_hbm": gbs / hbm}
+        del copies, W0
+    q.qmv_get_status(stream)
+    return {"metric": "decode matvec weight GB/s per format (14336x4096, batch 1, PDL chain)", "unit": "GB/s",
+            "by_format": res}
 
 
 def prefill_leg(q, torch, stream, tflops_peak):
@@ -1097,6 +1129,7 @@ def main():
     tflops_peak = 1900.0 if peak_kind == "fallback" else load_tflops_peak()
     cfg1 = None if args.no_extra else config1_leg(q, torch, stream, hbm)
     kquant = None if args.no_extra else kquant_decode_leg(q, torch, stream, hbm)
+    formats = None if args.no_extra else formats_leg(q, torch, stream, hbm)
     prefill = None if args.no_extra else prefill_leg(q, torch, stream, tflops_peak)
     moe = None if args.no_extra else moe_leg(q, torch, stream, hbm)
     wquant = None if args.no_extra else wquant_leg(q, torch, stream, hbm)
@@ -1176,6 +1209,7 @@ def main():
         "cpu_baseline_all_cores": cpu_all,
         "config1_q4_0_896": cfg1,
         "kquant_decode": kquant,
+        "formats": formats,
         "prefill": prefill,
         "moe": moe,
         "weight_quantiser": wquant,

@@ -86,7 +86,8 @@ int     orc_dequant(int type, const uint8_t* W, int64_t rows, int64_t cols, floa
  * out receives n/bs blocks of ORC_Q8_0 (fp16 d, int8[32]) or ORC_Q8_K
  * (fp32 d, int8[256], int16 bsums[16]). */
 int     orc_quantize_act(int atype, const float* x, int64_t n, uint8_t* out);
-/* fp32 weights (n a multiple of 32) to Q4_0, Q5_0 or Q8_0 blocks (wquant.c). */
+/* fp32 weights to Q4_0, Q4_1, Q5_0, Q5_1, Q8_0 (n a multiple of 32) or Q4_K,
+ * Q5_K, Q6_K blocks (n a multiple of 256) (wquant.c). */
 int     orc_quantize_weights(int wtype, const float* w, int64_t n, uint8_t* out);
 /* Decode one activation block to its integer codes and fp64 scale. */
 int     orc_decode_act_block(int atype, const uint8_t* blk, int32_t* q, double* d, int32_t* bsums);

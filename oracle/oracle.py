@@ -151,9 +151,10 @@ def quantize_act(atype: int, x: np.ndarray) -> np.ndarray:
 
 
 def quantize_weights(wt: int, w: np.ndarray) -> np.ndarray:
-    """w float32 [rows, cols] (cols % 32 == 0) -> Q4_0 / Q5_0 / Q8_0 blocks, uint8 [rows * row_bytes]."""
+    """w float32 [rows, cols] -> Q4_0 / Q4_1 / Q5_0 / Q5_1 / Q8_0 (cols % 32 == 0) or Q4_K / Q5_K / Q6_K
+    (cols % 256 == 0) blocks, uint8 [rows * row_bytes]."""
     w = np.ascontiguousarray(w, dtype=np.float32)
-    out = np.empty(w.size // 32 * BLOCK_BYTES[wt], dtype=np.uint8)
+    out = np.empty(w.size // BLOCK_ELEMS[wt] * BLOCK_BYTES[wt], dtype=np.uint8)
     _check(lib().orc_quantize_weights(wt, _ptr(w), w.size, _ptr(out)), "quantize_weights")
     return out
 
