@@ -128,7 +128,9 @@ def test_q8_0_weights_are_the_symmetric_8bit_form():
 
 def test_refusals():
     with pytest.raises(O.OracleError):
-        O.quantize_weights(O.Q4_K, np.zeros(256, dtype=np.float32))
+        O.quantize_weights(O.Q6_K, np.zeros(200, dtype=np.float32))   # not a whole super-block
+    with pytest.raises(O.OracleError):
+        O.quantize_weights(O.Q8_K, np.zeros(256, dtype=np.float32))   # an activation-only type
     with pytest.raises(O.OracleError):
         O.lib()   # loads
         O._check(O.lib().orc_quantize_weights(O.Q4_0, O._ptr(np.zeros(48, dtype=np.float32)), 48,
