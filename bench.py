@@ -755,36 +755,45 @@ def dist_env():
 
 
 def wquant_leg(q, torch, stream, hbm):
-    """The weight quantiser (qmv_quantize_weights): a 14336x4096 fp32 matrix
-    (235 MB, two copies alternating so each launch reads from HBM) to Q4_0,
-    Q5_0 and Q8_0.  Bytes = the fp32 read plus the blocks written."""
+    """The weight quantiser (qmv_quantize_weights): a 14336x4096 matrix (fp32
+    235 MB, or bf16 117 MB; two copies alternating so each launch reads from
+    HBM) to every block type it writes.  Bytes = the weights read plus the
+    blocks written."""
     rows, cols = 14336, 4096
     n = rows * cols
     g = torch.Generator(device="cuda").manual_seed(7)
     src = [torch.randn(rows, cols, device="cuda", generator=g) * 0.02 for _ in range(2)]
+    srcb = [w.to(torch.bfloat16) for w in src]
     res = {}
-    for t, name in ((Q4_0, "Q4_0"), (Q5_0, "Q5_0"), (Q8_0, "Q8_0")):
+    cases = [(Q4_0, "Q4_0", False), (11, "Q4_1", False), (Q5_0, "Q5_0", False), (12, "Q5_1", False),
+             (Q8_0, "Q8_0", False), (Q4_K, "Q4_K", False), (16, "Q5_K", False), (Q6_K, "Q6_K", False),
+             (Q4_0, "Q4_0_from_bf16", True), (Q4_K, "Q4_K_from_bf16", True)]
+    for t, name, bf in cases:
         out = torch.empty(rows * q.qmv_row_bytes(t, cols), dtype=torch.uint8, device="cuda")
-        nbytes = 4 * n + out.numel()
+        fmt = q.FMT(t, BF16) if bf else t
+        ins = srcb if bf else src
+        nbytes = (2 if bf else 4) * n + out.numel()
         with torch.cuda.stream(stream):
             for i in range(4):
-                q.qmv_quantize_weights(t, src[i % 2], rows, cols, out, stream.cuda_stream)
+                q.qmv_quantize_weights(fmt, ins[i % 2], rows, cols, out, stream.cuda_stream)
             reps = 20
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             for i in range(reps):
-                q.qmv_quantize_weights(t, src[i % 2], rows, cols, out, stream.cuda_stream)
+                q.qmv_quantize_weights(fmt, ins[i % 2], rows, cols, out, stream.cuda_stream)
             e1.record(stream)
         e1.synchronize()
         ms = e0.elapsed_time(e1) / reps
         gbs = nbytes / (ms / 1e3) / 1e9
         res[name] = {"us": 1e3 * ms, "gbs": gbs, "frac_of_hbm": gbs / hbm, "bytes": nbytes}
+        del out
     q.qmv_get_status(stream)
-    del src
+    del src, srcb
     torch.cuda.empty_cache()
-    return {"metric": "weight quantiser GB/s (fp32 read + blocks written)", "unit": "GB/s",
-            "shape": f"{rows}x{cols} fp32", "by_type": res,
-            "kernel": "k_quant_w (Q4_0, Q5_0: eight threads per block); Q8_0 runs the activation quantiser"}
+    return {"metric": "weight quantiser GB/s (weights read + blocks written)", "unit": "GB/s",
+            "shape": f"{rows}x{cols}", "by_type": res,
+            "kernels": "k_quant_w32 (32-element formats: eight threads per block), k_quant_wk (K-quants: one warp "
+                       "per super-block)"}
 
 
 def _oracle_step_workload():

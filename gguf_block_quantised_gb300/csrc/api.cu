@@ -22,7 +22,7 @@
 // Launchers defined in the kernel translation units.
 int qmv_launch_quantize(int atype, const float* x, void* xq, int64_t n, bool pdl, cudaStream_t st);
 int qmv_launch_dequant(int t, const void* W, int64_t rows, int64_t cols, float* out, cudaStream_t st);
-int qmv_launch_quantize_weights(int wtype, const float* W, int64_t n, void* out, cudaStream_t st);
+int qmv_launch_quantize_weights(int wtype, bool bf16, const void* W, int64_t n, void* out, cudaStream_t st);
 int qmv_launch_block_dots(int t, const void* W, int64_t rows, int64_t cols, const void* xq, int n_vec,
                           int32_t* out, cudaStream_t st);
 #define QMV_GEMV_DECL(NAME) \
@@ -325,25 +325,33 @@ int qmv_quantize_act(int fmt, const float* x, void* xq, int64_t n, void* stream)
     return ok();
 }
 
-int qmv_quantize_weights(int type, const float* W, int64_t rows, int64_t cols, void* out, void* stream)
+int qmv_quantize_weights(int type, const void* W, int64_t rows, int64_t cols, void* out, void* stream)
 {
-    if (type != QMV_Q4_0 && type != QMV_Q5_0 && type != QMV_Q8_0)
+    const int wtype = type & 0xff, in = (type >> 8) & 0xff;
+    if (type & ~0xffff) return fail(QMV_ERR_INVALID_ARG, "unknown flags 0x%x", type & ~0xffff);
+    if (in != 0 && in != QMV_F32 && in != QMV_BF16)
+        return fail(QMV_ERR_UNSUPPORTED, "qmv_quantize_weights reads F32 or BF16 weights (got %s)", type_name(in));
+    const bool bf16 = in == QMV_BF16;
+    if (wtype != QMV_Q4_0 && wtype != QMV_Q4_1 && wtype != QMV_Q5_0 && wtype != QMV_Q5_1 && wtype != QMV_Q8_0 &&
+        wtype != QMV_Q4_K && wtype != QMV_Q5_K && wtype != QMV_Q6_K)
         return fail(QMV_ERR_UNSUPPORTED,
-                    "qmv_quantize_weights writes Q4_0, Q5_0 and Q8_0 (got %s); the K-quants' scale search is not "
-                    "part of this library", type_name(type));
+                    "qmv_quantize_weights writes Q4_0, Q4_1, Q5_0, Q5_1, Q8_0, Q4_K, Q5_K and Q6_K (got %s)",
+                    type_name(wtype));
     if (rows < 0 || cols <= 0) return fail(QMV_ERR_INVALID_ARG, "rows must be >= 0 and cols > 0 (got %lld x %lld)",
                                            (long long)rows, (long long)cols);
-    if (cols % 32) return fail(QMV_ERR_SHAPE, "%s rows hold 32-element blocks; cols = %lld is not a multiple of 32",
-                               type_name(type), (long long)cols);
+    const int bs = qmv_block_elems(wtype);
+    if (cols % bs)
+        return fail(QMV_ERR_SHAPE, "%s rows hold %d-element blocks; cols = %lld is not a multiple of %d",
+                    type_name(wtype), bs, (long long)cols, bs);
     if (rows == 0) return ok();
     if (rows > ((int64_t)1 << 40) / cols) return fail(QMV_ERR_SHAPE, "rows * cols must be below 2^40");
     if (!W || !out) return fail(QMV_ERR_INVALID_ARG, "W and out must not be NULL");
     if (!aligned(W, 16)) return fail(QMV_ERR_ALIGN, "W must be 16-byte aligned");
     if (!aligned(out, 2)) return fail(QMV_ERR_ALIGN, "out must be 2-byte aligned");
-    const uintptr_t a0 = reinterpret_cast<uintptr_t>(W), a1 = a0 + (uintptr_t)(rows * cols) * 4;
-    const uintptr_t b0 = reinterpret_cast<uintptr_t>(out), b1 = b0 + (uintptr_t)rows * qmv_row_bytes(type, cols);
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(W), a1 = a0 + (uintptr_t)(rows * cols) * (bf16 ? 2 : 4);
+    const uintptr_t b0 = reinterpret_cast<uintptr_t>(out), b1 = b0 + (uintptr_t)rows * qmv_row_bytes(wtype, cols);
     if (a0 < b1 && b0 < a1) return fail(QMV_ERR_INVALID_ARG, "qmv_quantize_weights: out overlaps W");
-    if (qmv_launch_quantize_weights(type, W, rows * cols, out, static_cast<cudaStream_t>(stream)))
+    if (qmv_launch_quantize_weights(wtype, bf16, W, rows * cols, out, static_cast<cudaStream_t>(stream)))
         return cuda_fail("qmv_quantize_weights");
     return ok();
 }

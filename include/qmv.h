@@ -142,23 +142,37 @@ size_t qmv_row_bytes(int type, int64_t cols);
 int qmv_quantize_act(int fmt, const float* x, void* xq, int64_t n, void* stream);
 
 /* ---------------------------------------------------------------------------
- * qmv_quantize_weights -- fp32 weights to Q4_0, Q5_0 or Q8_0 blocks, the
- * formats the pages' quantiser writes ("Models and formats", "Tensor
- * formats").  The pages do not print the procedure; this is the reading that
- * keeps the files those of the GGUF ecosystem:
- *   Q4_0 / Q5_0: per 32 weights, m = the signed value of largest magnitude
- *     (the first on ties), d = m / -8 (Q4_0) or m / -16 (Q5_0), and each code
- *     is trunc(clamp(w / d + 8.5, 0, 15)) (Q5_0: + 16.5, 0, 31), every step one
- *     fp32 IEEE rounding; fp16(d) is stored.  The largest-magnitude weight
+ * qmv_quantize_weights -- fp32 or bf16 weights to the block formats the pages'
+ * quantiser writes ("Models and formats", "Tensor formats": Q4_0/1, Q5_0/1,
+ * Q8_0 and the K-quants).  The pages do not print the procedure; each format
+ * takes one pass of min/max rules per run, no search:
+ *   Q4_0 / Q5_0: m = the signed value of largest magnitude (the first on
+ *     ties), d = m / -8 (Q4_0) or m / -16 (Q5_0), code = trunc(clamp(w / d +
+ *     8.5, 0, 15)) (Q5_0: + 16.5, 0, 31).  The largest-magnitude weight
  *     decodes exactly to -8 fp16(d) (-16 for Q5_0).
  *   Q8_0: the symmetric 8-bit form, byte for byte qmv_quantize_act(QMV_Q8_0).
- *   W   : fp32 [rows][cols], 16-byte aligned; cols a multiple of 32.
- *   out : rows * qmv_row_bytes(type, cols) bytes, 2-byte aligned, not
- *         overlapping W.
- * Returns QMV_ERR_UNSUPPORTED for other types (the K-quants' scale search is
- * not part of this library), QMV_ERR_SHAPE, QMV_ERR_ALIGN, QMV_ERR_INVALID_ARG.
+ *   Q4_1 / Q5_1: m = min, d = (max - m) / 15 (31), code = trunc(clamp((w -
+ *     m) / d + 0.5, 0, 15 (31))).
+ *   Q4_K / Q5_K: per 32-weight sub-block lo = min(0, min w), s = (max w - lo)
+ *     / 15 (31), z = -lo; d = max s / 63, dmin = max z / 63; six-bit scales
+ *     and mins round(s / d), round(z / dmin); codes round((w + dmin*m) /
+ *     (d*sc)) on the stored fp16 scales.
+ *   Q6_K: per 16-weight run the signed extreme e, s = e / -32; the s of
+ *     largest magnitude s_e, d = s_e / -128; int8 scales round(s / d); codes
+ *     round(w / (d*sc)) + 32.
+ *   Each step is one fp32 rounding, divisions are multiplications by the
+ *   fp32 reciprocal (the quotient when it overflows), ties round away from
+ *   zero; fp16 values are stored rounded to nearest even.
+ *   type : the block type, or QMV_FMT(block type, QMV_BF16) for bf16 weights
+ *          (QMV_FMT(block type, QMV_F32) or the bare type: fp32).
+ *   W    : rows x cols weights, 16-byte aligned; cols a multiple of 32 (256
+ *          for the K-quants).
+ *   out  : rows * qmv_row_bytes(block type, cols) bytes, 2-byte aligned, not
+ *          overlapping W.
+ * Returns QMV_ERR_UNSUPPORTED for other types, QMV_ERR_SHAPE, QMV_ERR_ALIGN,
+ * QMV_ERR_INVALID_ARG.
  * ------------------------------------------------------------------------- */
-int qmv_quantize_weights(int type, const float* W, int64_t rows, int64_t cols, void* out, void* stream);
+int qmv_quantize_weights(int type, const void* W, int64_t rows, int64_t cols, void* out, void* stream);
 
 /* ---------------------------------------------------------------------------
  * qmv_repack -- weights to a layout for the tensor-core kernels, once at load

@@ -74,8 +74,12 @@ def test_refusals(lib):
     assert rc(lib, "qmv_quantize_act", q.Q8_0, 4096, 4096, 0, None) == q.OK
     assert rc(lib, "qmv_quantize_act", q.Q8_0, None, 4096, 32, None) == q.ERR_INVALID_ARG
     # weight quantiser
-    assert rc(lib, "qmv_quantize_weights", q.Q4_K, 4096, 2, 256, 8192, None) == q.ERR_UNSUPPORTED
-    assert "Q4_0" in q.qmv_last_error()
+    assert rc(lib, "qmv_quantize_weights", q.Q2_K, 4096, 2, 256, 8192, None) == q.ERR_UNSUPPORTED   # not written
+    assert "Q4_0" in q.qmv_last_error() and "Q6_K" in q.qmv_last_error()
+    assert rc(lib, "qmv_quantize_weights", q.Q8_K, 4096, 2, 256, 8192, None) == q.ERR_UNSUPPORTED   # activations only
+    assert rc(lib, "qmv_quantize_weights", q.FMT(q.Q4_0, q.Q8_0), 4096, 2, 64, 8192, None) == q.ERR_UNSUPPORTED
+    assert rc(lib, "qmv_quantize_weights", q.Q4_K, 4096, 2, 96, 8192, None) == q.ERR_SHAPE   # K-quant rows of 256
+    assert "256" in q.qmv_last_error()
     assert rc(lib, "qmv_quantize_weights", q.Q4_0, 4096, 2, 48, 8192, None) == q.ERR_SHAPE
     assert rc(lib, "qmv_quantize_weights", q.Q5_0, 4100, 2, 64, 8192, None) == q.ERR_ALIGN
     assert rc(lib, "qmv_quantize_weights", q.Q8_0, 4096, 2, 64, 8193, None) == q.ERR_ALIGN
