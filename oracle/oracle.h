@@ -124,4 +124,16 @@ int     orc_moe(int wtype, int atype, const uint8_t* W3d, int64_t n_expert,
                 int64_t k, const void* x, int64_t n_tok, const float* bias,
                 double* y, double* yabs);
 
+/* ---- moeblock.c : the router and the gated activation of an expert block ---- */
+/* logits[t][e] = x[t] . Wr[e] (+ br[e]) in fp32, in the 32-partial order the
+ * top-k decision is taken in (see moeblock.c). */
+int     orc_router(const float* x, const float* Wr, const float* br, int64_t n_tok, int64_t hidden,
+                   int64_t n_expert, float* logits);
+/* ids[t][s]: the k largest logits (ties to the lower id), descending; gates:
+ * softmax over them in fp64. */
+int     orc_topk_softmax(const float* logits, int64_t n_tok, int64_t n_expert, int64_t k, int32_t* ids,
+                         double* gates);
+/* min(g, limit) * sigmoid(alpha * min(g, limit)) * (clamp(u, -limit, limit) + 1), fp64 */
+double  orc_swiglu(double g, double u, double alpha, double limit);
+
 #endif

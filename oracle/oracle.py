@@ -21,7 +21,7 @@ import numpy as np
 HERE = os.path.dirname(os.path.abspath(__file__))
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "liboracle.so")
-SOURCES = ["fp.c", "blocks.c", "quant.c", "wquant.c", "mm.c"]
+SOURCES = ["fp.c", "blocks.c", "quant.c", "wquant.c", "mm.c", "moeblock.c"]
 
 # The oracle's own type numbers (oracle.h).
 Q4_0, Q5_0, Q8_0, Q4_K, Q6_K, MXFP4, Q8_K, F32, BF16, Q4_1, Q5_1, Q5_K, Q2_K, Q3_K, Q8_1, F16 = range(1, 17)
@@ -77,6 +77,12 @@ def lib():
             L.orc_matvec.argtypes = [I, I, P, I64, I64, P, I64, P, I64, P, P]
             L.orc_moe.argtypes = [I, I, P, I64, I64, I64, P, P, I64, P, I64, P, P, P]
             L.orc_decode_block.argtypes = [I, P, P]
+            L.orc_router.argtypes = [P, P, P, I64, I64, I64, P]
+            L.orc_router.restype = I
+            L.orc_topk_softmax.argtypes = [P, I64, I64, I64, P, P]
+            L.orc_topk_softmax.restype = I
+            L.orc_swiglu.argtypes = [C.c_double, C.c_double, C.c_double, C.c_double]
+            L.orc_swiglu.restype = C.c_double
             for f in ("orc_dequant", "orc_quantize_act", "orc_quantize_weights", "orc_block_dots", "orc_matvec",
                       "orc_moe", "orc_decode_block"):
                 getattr(L, f).restype = I
@@ -200,3 +206,64 @@ def moe(wt: int, at: int, W3d: np.ndarray, n_expert: int, rows: int, cols: int, 
     _check(lib().orc_moe(wt, at, _ptr(W3d), n_expert, rows, cols, _ptr(ids), _ptr(g), k,
                          _ptr(x), n_tok, _ptr(b), _ptr(y), _ptr(ya)), "moe")
     return y, ya
+
+
+# ---- mixture-of-experts block (moeblock.c, composed with moe()) ------------------------
+
+def router(x: np.ndarray, Wr: np.ndarray, br=None) -> np.ndarray:
+    """fp32 logits [n_tok][n_expert] in the order the top-k decision is taken in."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    Wr = np.ascontiguousarray(Wr, dtype=np.float32)
+    n_tok, hidden = x.shape
+    E = Wr.shape[0]
+    b = None if br is None else np.ascontiguousarray(br, dtype=np.float32)
+    out = np.empty((n_tok, E), dtype=np.float32)
+    _check(lib().orc_router(_ptr(x), _ptr(Wr), _ptr(b), n_tok, hidden, E, _ptr(out)), "router")
+    return out
+
+
+def topk_softmax(logits: np.ndarray, k: int):
+    """-> (ids int32 [n_tok][k], gates float64 [n_tok][k])."""
+    logits = np.ascontiguousarray(logits, dtype=np.float32)
+    n_tok, E = logits.shape
+    ids = np.empty((n_tok, k), dtype=np.int32)
+    gates = np.empty((n_tok, k), dtype=np.float64)
+    _check(lib().orc_topk_softmax(_ptr(logits), n_tok, E, k, _ptr(ids), _ptr(gates)), "topk_softmax")
+    return ids, gates
+
+
+def swiglu(g, u, alpha: float, limit: float) -> np.ndarray:
+    """The clipped, offset SwiGLU of each (g, u) pair, fp64."""
+    f = lib().orc_swiglu
+    g = np.asarray(g, dtype=np.float64)
+    u = np.asarray(u, dtype=np.float64)
+    out = np.empty(np.broadcast(g, u).shape, dtype=np.float64)
+    for idx in np.ndindex(out.shape):
+        out[idx] = f(float(g[idx]), float(u[idx]), float(alpha), float(limit))
+    return out
+
+
+def moe_block(wt: int, at: int, x: np.ndarray, Wr, br, Wgu, bgu, Wdown, bdown, n_expert: int, k: int,
+              hidden: int, inter: int, alpha: float, limit: float):
+    """A whole expert block for fp32 hidden states x [n_tok][hidden]:
+    router -> top k -> gate_up (rows [0, inter) gate, [inter, 2 inter) linear)
+    -> clipped SwiGLU -> down, gate-weighted.  at: F32, BF16 or the 8-bit type
+    paired with wt (the activations of both projections, quantised or rounded
+    from fp32 as the library's block does).  Returns (y, yabs, ids, gates)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    n_tok = x.shape[0]
+    ids, gates = topk_softmax(router(x, Wr, br), k)
+
+    def act(v):   # fp32 values -> the activation layout of `at`
+        v = np.ascontiguousarray(v, dtype=np.float32)
+        if at == F32:
+            return v
+        if at == BF16:
+            bits = np.vectorize(f32_to_bf16_rn, otypes=[np.uint16])(v)
+            return bits.view(np.int16)
+        return quantize_act(at, v)
+    y1, _ = moe(wt, at, Wgu, n_expert, 2 * inter, hidden, ids, None, k, act(x), n_tok, bias=bgu)
+    h = swiglu(y1[:, :, :inter], y1[:, :, inter:], alpha, limit)          # [n_tok][k][inter]
+    y, yabs = moe(wt, at, Wdown, n_expert, hidden, inter, ids, gates.astype(np.float32), k,
+                  act(h.astype(np.float32)), n_tok, bias=bdown)
+    return y, yabs, ids, gates
