@@ -577,6 +577,8 @@ def moe_leg(q, torch, stream, hbm):
     Wd_r = torch.empty(E * 2880 * q.qmv_row_bytes(MXFP4_R, 2880), dtype=torch.uint8, device="cuda")
     q.qmv_repack(MXFP4, Wgu, E * 5760, 2880, Wgu_r)
     q.qmv_repack(MXFP4, Wd, E * 2880, 2880, Wd_r)
+    Wr = torch.from_numpy(synth.router_weights(E, 2880, seed=5)).cuda()
+    br = torch.from_numpy(synth.bias(1, E, seed=5, tensor_id=4001)[0]).cuda()
     paths = {"w4a8": (q.FMT(MXFP4, Q8_0) | q.FLAG_QUANTIZE_X, torch.float32, Wgu, Wd),
              "bf16_gemm": (q.FMT(MXFP4, BF16), torch.bfloat16, Wgu, Wd),
              "bf16_gemm_repacked": (q.FMT(MXFP4_R, BF16), torch.bfloat16, Wgu_r, Wd_r)}
@@ -612,15 +614,44 @@ def moe_leg(q, torch, stream, hbm):
                                   "weight_gbs": wbytes / (ms / 1e3) / 1e9,
                                   "frac_of_hbm": wbytes / (ms / 1e3) / 1e9 / hbm,
                                   "tflops": flop / (ms / 1e3) / 1e12}
+            res[f"block_tok{n_tok}"] = block_time(q, torch, stream, fmt, Wgu_p, Wd_p, bgu, bd, Wr, br, n_tok, hbm)
         out[name] = res
     q.qmv_set_workspace(None, 0)
     q.qmv_get_status(stream)
     return {"metric": "MoE layer (gate_up + down) expert weight GB/s", "unit": "GB/s", "by_path": out,
+            "block": "block_tok*: qmv_moe_block, the whole block from fp32 hidden states (router 32x2880 fp32, "
+                     "top 4, gate_up, clipped SwiGLU, down): k_router + k_topk + the path's expert kernels + "
+                     "k_swiglu; four hidden-state batches rotate (each routes its own way)",
             "paths": {"w4a8": "k_moe_group + k_moe_gemv (dp4a, grouped per expert) + k_moe_combine",
                       "bf16_gemm": "k_moe_group + k_moe_tiles + k_moe_gather + k_moe_gemm_mxfp4_bf16 (tcgen05) "
                                    "+ k_moe_combine",
                       "bf16_gemm_repacked": "the same on MXFP4_R experts (qmv_repack once; TMA tensor copies of "
                                             "the codes and exponents)"}}
+
+
+def block_time(q, torch, stream, fmt, Wgu, Wd, bgu, bd, Wr, br, n_tok, hbm, E=32, k=4, hidden=2880, inter=2880):
+    """qmv_moe_block on gpt-oss-shaped experts; fmt's flags are dropped (the block
+    always quantises 8-bit activations itself)."""
+    fmt &= 0xffff
+    xs = [torch.from_numpy(synth.activations(n_tok, hidden, seed=40 + r)).cuda() for r in range(4)]
+    y = torch.empty(n_tok, hidden, device="cuda")
+    ids = torch.empty(n_tok, k, dtype=torch.int32, device="cuda")
+    gates = torch.empty(n_tok, k, device="cuda")
+    ws = torch.empty(q.qmv_moe_block_workspace_size(fmt, E, k, hidden, inter, n_tok), dtype=torch.uint8,
+                     device="cuda")
+    used = []
+    for x in xs:
+        q.qmv_set_workspace(ws, ws.numel())
+        q.qmv_moe_block(fmt, E, k, hidden, inter, Wr, br, Wgu, bgu, Wd, bd, 1.702, 7.0, x, n_tok, y, ids, gates,
+                        stream.cuda_stream)
+        torch.cuda.synchronize()
+        used.append(len(np.unique(ids.cpu().numpy())))
+    calls = [lambda s, x=x: q.qmv_moe_block(fmt, E, k, hidden, inter, Wr, br, Wgu, bgu, Wd, bd, 1.702, 7.0, x,
+                                            n_tok, y, ids, gates, s.cuda_stream) for x in xs]
+    ms = time_rotating(torch, stream, calls, 20 if n_tok >= 1024 else 100)
+    wbytes = float(np.mean(used)) * (2 * inter + hidden) * synth.row_bytes(MXFP4, hidden)
+    return {"ms": ms, "experts_used": float(np.mean(used)), "weight_gbs": wbytes / (ms / 1e3) / 1e9,
+            "frac_of_hbm": wbytes / (ms / 1e3) / 1e9 / hbm}
 
 
 def run_probe(spec):
@@ -629,6 +660,7 @@ def run_probe(spec):
       gemm:rows:cols:m               qmv_matmul, Q4_K x bf16
       gemm8:rows:cols:m              qmv_matmul, Q4_K x Q8_K (W4A8, with its activation pre-pass)
       step[:n_vec]                   one fused decode step of the Qwen2.5-0.5B shape (97 matvecs)
+      block:n_tok[:atype]            qmv_moe_block on the gpt-oss MoE shapes (atype 3 = Q8_0, 8 = fp32, 9 = bf16)
       moe:n_tok[:atype[:repacked]]   one gpt-oss-shaped MoE layer (gate_up + down); atype 3 = Q8_0
                                      quantised in-kernel (default), 9 = bf16 (grouped tensor-core GEMM);
                                      repacked 1: experts repacked to MXFP4_R first (bf16 only)
@@ -675,6 +707,29 @@ def run_probe(spec):
         stream = torch.cuda.current_stream()
         call = lambda: step.run(stream)
         nbytes, what = STEP_WEIGHT_BYTES, "weight GB/s"
+    elif kind == "block":
+        n_tok, at = (a + [Q8_0][len(a) - 1:])[:2]
+        E, k, hid, inter = 32, 4, 2880, 2880
+        Wgu = torch.from_numpy(synth.weights(MXFP4, E * 2 * inter, hid, seed=5, tensor_id=1)).cuda()
+        Wd = torch.from_numpy(synth.weights(MXFP4, E * hid, inter, seed=5, tensor_id=2)).cuda()
+        bgu = torch.from_numpy(synth.bias(E, 2 * inter, seed=5)).cuda()
+        bd = torch.from_numpy(synth.bias(E, hid, seed=5, tensor_id=2001)).cuda()
+        Wr = torch.from_numpy(synth.router_weights(E, hid, seed=5)).cuda()
+        br = torch.from_numpy(synth.bias(1, E, seed=5, tensor_id=4001)[0]).cuda()
+        x = torch.from_numpy(synth.activations(n_tok, hid, seed=40)).cuda()
+        y = torch.empty(n_tok, hid, device="cuda")
+        ids = torch.empty(n_tok, k, dtype=torch.int32, device="cuda")
+        gates = torch.empty(n_tok, k, device="cuda")
+        fmt = q.FMT(MXFP4, at)
+        ws = torch.empty(q.qmv_moe_block_workspace_size(fmt, E, k, hid, inter, n_tok), dtype=torch.uint8,
+                         device="cuda")
+        q.qmv_set_workspace(ws, ws.numel())
+        call = lambda: q.qmv_moe_block(fmt, E, k, hid, inter, Wr, br, Wgu, bgu, Wd, bd, 1.702, 7.0, x, n_tok, y, ids,
+                                       gates)
+        call()
+        torch.cuda.synchronize()
+        nbytes = len(np.unique(ids.cpu().numpy())) * (2 * inter + hid) * synth.row_bytes(MXFP4, hid)
+        what = "expert weight GB/s"
     elif kind == "moe":
         n_tok, at, repacked = (a + [Q8_0, 0][len(a) - 1:])[:3]
         E, k = 32, 4

@@ -61,6 +61,9 @@ _SIGS = {
     "qmv_matmul": (_I, [_I, _P, _I64, _I64, _P, _P, _I64, _P]),
     "qmv_moe_matvec": (_I, [_I, _P, _I, _I64, _I64, _P, _P, _I, _P, _P, _I64, _P, _P]),
     "qmv_moe_matvec_noalloc": (_I, [_I, _P, _I, _I64, _I64, _P, _P, _I, _P, _P, _I64, _P, _P]),
+    "qmv_moe_block": (_I, [_I, _I, _I, _I64, _I64, _P, _P, _P, _P, _P, _P, C.c_float, C.c_float, _P, _I64, _P,
+                           _P, _P, _P]),
+    "qmv_moe_block_workspace_size": (_SZ, [_I, _I, _I, _I64, _I64, _I64]),
     "qmv_workspace_size": (_SZ, [_I, _I, _I64, _I64, _I64]),
     "qmv_set_workspace": (_I, [_P, _SZ]),
     "qmv_get_status": (_I, [_P]),
@@ -175,6 +178,18 @@ def qmv_moe_matvec_noalloc(fmt, W3d, n_expert, rows, cols, ids, gates, k, x, y, 
 
 
 MOE_NOALLOC_MAX_BYTES = 4 << 20
+
+
+def qmv_moe_block(fmt, n_expert, k, hidden, inter, Wr, br, W_gu, b_gu, W_down, b_down, alpha, limit, x, n_tok,
+                  y, ids, gates, stream=None):
+    """Router -> top k -> gate_up -> clipped SwiGLU -> down for fp32 x [n_tok][hidden]."""
+    return _call("qmv_moe_block", fmt, n_expert, k, hidden, inter, _ptr(Wr), _ptr(br), _ptr(W_gu), _ptr(b_gu),
+                 _ptr(W_down), _ptr(b_down), float(alpha), float(limit), _ptr(x), n_tok, _ptr(y), _ptr(ids),
+                 _ptr(gates), _stream(stream))
+
+
+def qmv_moe_block_workspace_size(fmt, n_expert, k, hidden, inter, n_tok) -> int:
+    return load().qmv_moe_block_workspace_size(fmt, n_expert, k, hidden, inter, n_tok)
 
 
 def qmv_workspace_size(op, fmt, rows, cols, n) -> int:

@@ -46,6 +46,11 @@ size_t qmv_w4a8_workspace_bytes(int64_t cols, int64_t m);
 int qmv_launch_gemm_q4k_w4a8(const void* W, int64_t rows, int64_t cols, const void* X, float* Y, int64_t m,
                              void* ws, bool pdl, cudaStream_t st);
 size_t qmv_moe_workspace_bytes(bool bf16, int64_t rows, int64_t cols, int64_t n_pairs);
+size_t qmv_moe_block_workspace_bytes(bool bf16, int n_expert, int64_t hidden, int64_t inter, int64_t n_tok, int k);
+int qmv_launch_moe_block(int wtype, bool a8, bool bf16, size_t act_block_bytes, int n_expert, int k,
+                         int64_t hidden, int64_t inter, const float* Wr, const float* br, const void* Wgu,
+                         const float* bgu, const void* Wd, const float* bd, float alpha, float limit, const float* x,
+                         int64_t n_tok, float* y, int32_t* ids, float* gates, void* ws, cudaStream_t st);
 int qmv_launch_repack_mxfp4(const void* W, int64_t rows, int64_t cols, void* Wout, cudaStream_t st);
 int qmv_launch_moe(int wtype, bool a8, bool quant_x, bool bf16, size_t act_block_bytes, const void* W3d,
                    int n_expert, int64_t rows, int64_t cols, const int32_t* ids, const float* gates, int k,
@@ -511,6 +516,74 @@ int qmv_moe_matvec(int fmt, const void* W3d, int n_expert, int64_t rows, int64_t
                     "qmv_moe_matvec needs %zu bytes of workspace (qmv_workspace_size(QMV_OP_MOE, ...)); %zu set",
                     c.need, have);
     return moe_run("qmv_moe_matvec", c, W3d, n_expert, rows, cols, ids, gates, k, x, y, n_tok, bias, ws, stream);
+}
+
+int qmv_moe_block(int fmt, int n_expert, int k, int64_t hidden, int64_t inter, const float* Wr, const float* br,
+                  const void* W_gu, const float* b_gu, const void* W_down, const float* b_down, float alpha,
+                  float limit, const float* x, int64_t n_tok, float* y, int32_t* ids, float* gates, void* stream)
+{
+    static const char* name = "qmv_moe_block";
+    if (fmt & ~0xffff) return fail(QMV_ERR_INVALID_ARG, "unknown flags 0x%x (8-bit activations are always "
+                                   "quantised inside the block)", fmt & ~0xffff);
+    const int wtype = fmt & 0xff, atype = (fmt >> 8) & 0xff;
+    const bool bf16 = atype == QMV_BF16 && (wtype == QMV_MXFP4 || wtype == QMV_MXFP4_R);
+    if (wtype == QMV_MXFP4_R && !bf16)
+        return fail(QMV_ERR_UNSUPPORTED, "%s: repacked MXFP4_R experts take BF16 activations (got %s)", name,
+                    type_name(atype));
+    if (!is_weight_type(wtype) && wtype != QMV_MXFP4_R)
+        return fail(QMV_ERR_UNSUPPORTED, "%s: %s is not a weight type", name, type_name(wtype));
+    if (atype != QMV_F32 && atype != paired_act(wtype) && !bf16)
+        return fail(QMV_ERR_UNSUPPORTED, "%s: %s experts take F32 or %s activations%s (got %s)", name,
+                    type_name(wtype), type_name(paired_act(wtype)), wtype == QMV_MXFP4 ? " or BF16" : "",
+                    type_name(atype));
+    if (n_expert < 1 || n_expert > 1024) return fail(QMV_ERR_INVALID_ARG, "n_expert must be in 1..1024 (got %d)", n_expert);
+    if (k < 1 || k > 64 || k > n_expert)
+        return fail(QMV_ERR_INVALID_ARG, "k must be in 1..min(64, n_expert) (got %d)", k);
+    if (hidden <= 0 || inter <= 0) return fail(QMV_ERR_INVALID_ARG, "hidden and inter must be > 0");
+    if (n_tok < 0 || n_tok > ((int64_t)1 << 24) / k)
+        return fail(QMV_ERR_INVALID_ARG, "n_tok must be >= 0 with n_tok*k <= 16777216");
+    const int geo = wtype == QMV_MXFP4_R ? QMV_MXFP4 : wtype;
+    int rc = check_weights(geo, W_gu, 2 * inter, hidden);
+    if (rc) return rc;
+    rc = check_weights(geo, W_down, hidden, inter);
+    if (rc) return rc;
+    if (bf16 && (2 * inter > (int64_t)1 << 30 || hidden > (int64_t)1 << 30))
+        return fail(QMV_ERR_SHAPE, "rows must be below 2^30");
+    if (n_tok == 0) return ok();
+    if (!Wr || !x || !y || !ids || !gates)
+        return fail(QMV_ERR_INVALID_ARG, "Wr, x, y, ids and gates must not be NULL");
+    if (!aligned(x, 16)) return fail(QMV_ERR_ALIGN, "x must be 16-byte aligned");
+    if (!aligned(Wr, 4) || !aligned(y, 4) || !aligned(ids, 4) || !aligned(gates, 4) || (br && !aligned(br, 4)) ||
+        (b_gu && !aligned(b_gu, 4)) || (b_down && !aligned(b_down, 4)))
+        return fail(QMV_ERR_ALIGN, "Wr, br, biases, y, ids and gates must be 4-byte aligned");
+    const size_t need = qmv_moe_block_workspace_bytes(bf16, n_expert, hidden, inter, n_tok, k);
+    const int d = qmv::current_device();
+    void* ws = nullptr;
+    size_t have = 0;
+    if (d >= 0 && d < qmv::kMaxDevices) {
+        std::lock_guard<std::mutex> lock(g_ws_mu);
+        ws = g_ws[d].ptr;
+        have = g_ws[d].bytes;
+    }
+    if (!ws || have < need)
+        return fail(QMV_ERR_WORKSPACE, "%s needs %zu bytes of workspace (qmv_moe_block_workspace_size); %zu set",
+                    name, need, have);
+    if (!qmv::status_word()) return cuda_fail(name);
+    rc = qmv_launch_moe_block(wtype, atype != QMV_F32 && !bf16, bf16, qmv_block_bytes(paired_act(wtype)), n_expert,
+                              k, hidden, inter, Wr, br, W_gu, b_gu, W_down, b_down, alpha, limit, x, n_tok, y, ids,
+                              gates, ws, static_cast<cudaStream_t>(stream));
+    if (rc == -2) return fail(QMV_ERR_SHAPE, "%s: a projection needs more shared memory than one SM has", name);
+    if (rc == -8) return fail(QMV_ERR_CUDA, "%s: could not build a TMA tensor map", name);
+    if (rc) return cuda_fail(name);
+    return ok();
+}
+
+size_t qmv_moe_block_workspace_size(int fmt, int n_expert, int k, int64_t hidden, int64_t inter, int64_t n_tok)
+{
+    if (n_expert < 1 || k < 1 || hidden <= 0 || inter <= 0 || n_tok <= 0) return 0;
+    const int wtype = fmt & 0xff, atype = (fmt >> 8) & 0xff;
+    const bool bf16 = atype == QMV_BF16 && (wtype == QMV_MXFP4 || wtype == QMV_MXFP4_R);
+    return qmv_moe_block_workspace_bytes(bf16, n_expert, hidden, inter, n_tok, k);
 }
 
 size_t qmv_workspace_size(int op, int fmt, int64_t rows, int64_t cols, int64_t n)

@@ -124,11 +124,14 @@ size_t qmv_moe_workspace_bytes(bool bf16, int64_t rows, int64_t cols, int64_t n_
 }
 
 // bf16: MXFP4 experts with bf16 activations, through the grouped tensor-core
-// GEMM (moe_gemm.cu); otherwise the expert matvecs of moe.cuh.
+// GEMM (moe_gemm.cu); otherwise the expert matvecs of moe.cuh.  grouped: the
+// workspace already holds the grouping of these ids (an earlier call with the
+// same ids, n_tok and k on this workspace), so it is not rebuilt.
 // Returns 0, -2 (shape beyond the plan), -6 (launch failure), -8 (tensor map).
-int qmv_launch_moe(int wtype, bool a8, bool quant_x, bool bf16, size_t act_block_bytes, const void* W3d,
-                   int n_expert, int64_t rows, int64_t cols, const int32_t* ids, const float* gates, int k,
-                   const void* x, float* y, int64_t n_tok, const float* bias, void* ws, cudaStream_t st)
+int qmv_launch_moe_ex(int wtype, bool a8, bool quant_x, bool bf16, size_t act_block_bytes, const void* W3d,
+                      int n_expert, int64_t rows, int64_t cols, const int32_t* ids, const float* gates, int k,
+                      const void* x, float* y, int64_t n_tok, const float* bias, void* ws, bool grouped,
+                      cudaStream_t st)
 {
     using namespace qmv;
     const int64_t n_pairs = n_tok * k;
@@ -138,8 +141,10 @@ int qmv_launch_moe(int wtype, bool a8, bool quant_x, bool bf16, size_t act_block
     int* active = offsets + 1025;                         // [0] = count, [1..] = expert ids
     int* perm = reinterpret_cast<int*>(w + r256(2050 * 4));
     float* part = reinterpret_cast<float*>(w + r256(2050 * 4) + r256((size_t)n_pairs * 4));
-    k_moe_group<<<1, 1024, 0, st>>>(ids, (int)n_pairs, n_expert, offsets, active, perm, status_word());
-    if (cudaGetLastError() != cudaSuccess) return -6;
+    if (!grouped) {
+        k_moe_group<<<1, 1024, 0, st>>>(ids, (int)n_pairs, n_expert, offsets, active, perm, status_word());
+        if (cudaGetLastError() != cudaSuccess) return -6;
+    }
     const size_t xrow = (a8 && !quant_x) ? (size_t)(cols / (kq_rt(wtype) ? 256 : 32)) *
                                                act_block_bytes
                                          : (size_t)cols * 4;
@@ -181,4 +186,12 @@ int qmv_launch_moe(int wtype, bool a8, bool quant_x, bool bf16, size_t act_block
         if (cudaGetLastError() != cudaSuccess) return -6;
     }
     return 0;
+}
+
+int qmv_launch_moe(int wtype, bool a8, bool quant_x, bool bf16, size_t act_block_bytes, const void* W3d,
+                   int n_expert, int64_t rows, int64_t cols, const int32_t* ids, const float* gates, int k,
+                   const void* x, float* y, int64_t n_tok, const float* bias, void* ws, cudaStream_t st)
+{
+    return qmv_launch_moe_ex(wtype, a8, quant_x, bf16, act_block_bytes, W3d, n_expert, rows, cols, ids, gates, k, x,
+                             y, n_tok, bias, ws, false, st);
 }

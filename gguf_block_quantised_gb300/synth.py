@@ -17,6 +17,7 @@ Distributions (model-shaped synthetic weights; no trained weights are used):
   MXFP4 E8M0 exponent       : uniform in [118, 130]
   activations               : fp32 N(0,1)
   expert biases             : fp32 N(0,1) * 0.02
+  router weights            : fp32 N(0,1) * 0.05 [n_expert][hidden]
   router logits             : N(0,1); top-k by logit (ties to the lower
                               expert id), gates = softmax over the k kept.
 Every tensor draws from its own stream, seeded by (seed, tensor_id).
@@ -143,6 +144,10 @@ def activations(n_vec: int, cols: int, seed: int = 0, tensor_id: int = 1000) -> 
 
 def bias(n_expert: int, rows: int, seed: int = 0, tensor_id: int = 2000) -> np.ndarray:
     return rng(seed, tensor_id).standard_normal((n_expert, rows), dtype=np.float32) * np.float32(0.02)
+
+
+def router_weights(n_expert: int, hidden: int, seed: int = 0, tensor_id: int = 4000) -> np.ndarray:
+    return rng(seed, tensor_id).standard_normal((n_expert, hidden), dtype=np.float32) * np.float32(0.05)
 
 
 def router(n_tok: int, n_expert: int, k: int, seed: int = 0, tensor_id: int = 3000):

@@ -336,6 +336,57 @@ int qmv_moe_matvec_noalloc(int fmt, const void* W3d, int n_expert, int64_t rows,
                            const void* x, float* y, int64_t n_tok, const float* bias,
                            void* stream);
 
+/* ---------------------------------------------------------------------------
+ * qmv_moe_block -- a whole mixture-of-experts block for fp32 hidden states:
+ * router -> top k -> gate_up -> clipped SwiGLU -> down, gate-weighted
+ * ("Models and formats", "Architectures": a router picks k of n experts per
+ * token; stacked 3-D expert tensors; gpt-oss gates with a clipped SwiGLU
+ * whose linear half is offset by one and has a bias on every expert
+ * projection).  The pages print neither the router's arithmetic nor the
+ * clipping constants; this call fixes them as follows.
+ *   Router : logit[t][e] = x_t . Wr[e] + br[e] in fp32, summed as 32 partial
+ *            sums (partial l takes the elements l, l+32, ... by fused
+ *            multiply-add from 0) combined by a butterfly (l + (l xor o),
+ *            o = 16, 8, 4, 2, 1), then the bias: the top-k choice depends on
+ *            this order only, not on the GPU.
+ *   Top k  : the k largest logits, ties to the lower expert id; ids[t][0]
+ *            is the largest.  Gates: softmax over the k kept logits in fp32
+ *            (exp(l_s - l_0), summed in slot order).  If a logit is NaN the
+ *            chosen ids are unspecified (but distinct and in range).
+ *   gate_up: W_gu [n_expert][2*inter][hidden]; rows [0, inter) are the gate
+ *            half g, rows [inter, 2*inter) the linear half u; b_gu
+ *            [n_expert][2*inter] or NULL.
+ *   Gate   : h = min(g, limit) * sigmoid(alpha * min(g, limit))
+ *                * (clamp(u, -limit, limit) + 1), fp32.
+ *   down   : W_down [n_expert][hidden][inter], b_down [n_expert][hidden] or
+ *            NULL; y[t] = sum over slots, in slot order, of
+ *            gates[t][s] * (W_down[ids[t][s]] h_{t,s} + b_down[ids[t][s]]).
+ *   fmt    : QMV_FMT(wtype, atype): atype F32 (fp32 activations), the paired
+ *            8-bit type (x and h are quantised to it inside the expert
+ *            kernels, as QMV_FLAG_QUANTIZE_X does), or, for MXFP4 / MXFP4_R
+ *            experts, BF16 (x and h rounded to bf16, the grouped tensor-core
+ *            GEMM).  No flags.  Each projection gives the results of
+ *            qmv_moe_matvec with the same format.
+ *   Wr     : fp32 [n_expert][hidden]; br fp32 [n_expert] or NULL.
+ *   x      : fp32 [n_tok][hidden], 16-byte aligned.  y : fp32 [n_tok][hidden].
+ *   ids    : int32 [n_tok][k] out.   gates : fp32 [n_tok][k] out.
+ *   n_expert in 1..1024, k in 1..min(64, n_expert), n_tok*k <= 2^24; hidden
+ *   and inter multiples of the weight block length.
+ *   Workspace: qmv_moe_block_workspace_size(...) bytes set by
+ *   qmv_set_workspace(); calls that share it must be ordered on one stream.
+ * ------------------------------------------------------------------------- */
+int qmv_moe_block(int fmt, int n_expert, int k, int64_t hidden, int64_t inter,
+                  const float* Wr, const float* br,
+                  const void* W_gu, const float* b_gu,
+                  const void* W_down, const float* b_down,
+                  float alpha, float limit,
+                  const float* x, int64_t n_tok, float* y,
+                  int32_t* ids, float* gates, void* stream);
+/* Bytes of workspace qmv_moe_block needs (about n_tok*(n_expert + 3*k*inter)*4
+ * plus the expert calls' grouping and slot outputs); 0 for empty sizes. */
+size_t qmv_moe_block_workspace_size(int fmt, int n_expert, int k, int64_t hidden, int64_t inter,
+                                    int64_t n_tok);
+
 /* Workspace for the calls that need scratch. */
 enum { QMV_OP_MATVEC = 1, QMV_OP_MATMUL = 2, QMV_OP_MOE = 3 };
 /* Bytes of workspace `op` needs for these sizes.  QMV_OP_MOE, n = n_tok*k:

@@ -244,12 +244,15 @@ def swiglu(g, u, alpha: float, limit: float) -> np.ndarray:
 
 
 def moe_block(wt: int, at: int, x: np.ndarray, Wr, br, Wgu, bgu, Wdown, bdown, n_expert: int, k: int,
-              hidden: int, inter: int, alpha: float, limit: float):
+              hidden: int, inter: int, alpha: float, limit: float, detail: bool = False):
     """A whole expert block for fp32 hidden states x [n_tok][hidden]:
     router -> top k -> gate_up (rows [0, inter) gate, [inter, 2 inter) linear)
     -> clipped SwiGLU -> down, gate-weighted.  at: F32, BF16 or the 8-bit type
     paired with wt (the activations of both projections, quantised or rounded
-    from fp32 as the library's block does).  Returns (y, yabs, ids, gates)."""
+    from fp32 as the library's block does).  Returns (y, yabs, ids, gates), and
+    with detail=True also a dict of the gate_up outputs y1, their sums of
+    magnitudes y1abs ([n_tok][k][2 inter], fp64) and the activations h
+    ([n_tok][k][inter], fp32)."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     n_tok = x.shape[0]
     ids, gates = topk_softmax(router(x, Wr, br), k)
@@ -262,8 +265,10 @@ def moe_block(wt: int, at: int, x: np.ndarray, Wr, br, Wgu, bgu, Wdown, bdown, n
             bits = np.vectorize(f32_to_bf16_rn, otypes=[np.uint16])(v)
             return bits.view(np.int16)
         return quantize_act(at, v)
-    y1, _ = moe(wt, at, Wgu, n_expert, 2 * inter, hidden, ids, None, k, act(x), n_tok, bias=bgu)
-    h = swiglu(y1[:, :, :inter], y1[:, :, inter:], alpha, limit)          # [n_tok][k][inter]
-    y, yabs = moe(wt, at, Wdown, n_expert, hidden, inter, ids, gates.astype(np.float32), k,
-                  act(h.astype(np.float32)), n_tok, bias=bdown)
+    y1, y1abs = moe(wt, at, Wgu, n_expert, 2 * inter, hidden, ids, None, k, act(x), n_tok, bias=bgu)
+    h = swiglu(y1[:, :, :inter], y1[:, :, inter:], alpha, limit).astype(np.float32)   # [n_tok][k][inter]
+    y, yabs = moe(wt, at, Wdown, n_expert, hidden, inter, ids, gates.astype(np.float32), k, act(h), n_tok,
+                  bias=bdown)
+    if detail:
+        return y, yabs, ids, gates, dict(y1=y1, y1abs=y1abs, h=h)
     return y, yabs, ids, gates

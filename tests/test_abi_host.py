@@ -92,6 +92,33 @@ def test_refusals(lib):
     assert rc(lib, "qmv_set_workspace", 4100, 1024) == q.ERR_ALIGN
 
 
+def test_moe_block_refusals(lib):
+    F = q.FMT
+    A = 4096   # any 16-byte aligned stand-in address: nothing is dereferenced before the checks
+
+    def call(fmt, E=8, k=2, hidden=256, inter=256, n_tok=3, x=A):
+        return rc(lib, "qmv_moe_block", fmt, E, k, hidden, inter, A, None, A, None, A, None, 1.702, 7.0, x, n_tok,
+                  A, A, A, None)
+    assert call(F(q.Q4_0, q.BF16)) == q.ERR_UNSUPPORTED            # BF16 is for MXFP4 experts only
+    assert call(F(q.MXFP4_R, q.F32)) == q.ERR_UNSUPPORTED
+    assert call(F(q.Q4_K, q.Q8_0)) == q.ERR_UNSUPPORTED            # K-quants pair with Q8_K
+    assert call(F(q.Q8_K, q.F32)) == q.ERR_UNSUPPORTED
+    assert call(F(q.Q4_0, q.Q8_0) | q.FLAG_QUANTIZE_X) == q.ERR_INVALID_ARG
+    assert call(F(q.Q4_0, q.F32), E=4, k=5) == q.ERR_INVALID_ARG   # k > n_expert
+    assert call(F(q.Q4_0, q.F32), E=1025, k=2) == q.ERR_INVALID_ARG
+    assert call(F(q.Q4_0, q.F32), inter=40) == q.ERR_SHAPE
+    assert call(F(q.Q4_K, q.F32), hidden=288) == q.ERR_SHAPE
+    assert call(F(q.Q4_0, q.F32), x=4100) == q.ERR_ALIGN
+    assert call(F(q.Q4_0, q.F32), n_tok=0, x=None) == q.OK
+    assert call(F(q.Q4_0, q.F32)) == q.ERR_WORKSPACE               # none registered
+    assert "qmv_moe_block_workspace_size" in q.qmv_last_error()
+    ws = q.qmv_moe_block_workspace_size(F(q.Q4_0, q.F32), 32, 4, 2880, 2880, 1)
+    assert ws >= (32 + 3 * 4 * 2880) * 4
+    assert q.qmv_moe_block_workspace_size(F(q.Q4_0, q.F32), 32, 4, 2880, 2880, 0) == 0
+    assert (q.qmv_moe_block_workspace_size(F(q.MXFP4, q.BF16), 32, 4, 2880, 2880, 8) >
+            q.qmv_moe_block_workspace_size(F(q.MXFP4, q.F32), 32, 4, 2880, 2880, 8))
+
+
 def test_error_strings(lib):
     for code in (0, -1, -2, -3, -4, -5, -6, -7):
         assert q.qmv_strerror(code)
