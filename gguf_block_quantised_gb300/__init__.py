@@ -64,6 +64,7 @@ _SIGS = {
     "qmv_moe_block": (_I, [_I, _I, _I, _I64, _I64, _P, _P, _P, _P, _P, _P, C.c_float, C.c_float, _P, _I64, _P,
                            _P, _P, _P]),
     "qmv_moe_block_workspace_size": (_SZ, [_I, _I, _I, _I64, _I64, _I64]),
+    "qmv_set_wait_limit": (_I, [C.c_uint]),
     "qmv_workspace_size": (_SZ, [_I, _I, _I64, _I64, _I64]),
     "qmv_set_workspace": (_I, [_P, _SZ]),
     "qmv_get_status": (_I, [_P]),
@@ -198,6 +199,11 @@ def qmv_workspace_size(op, fmt, rows, cols, n) -> int:
 
 def qmv_set_workspace(ptr, nbytes, stream=None):
     return _call("qmv_set_workspace", _ptr(ptr), nbytes)
+
+
+def qmv_set_wait_limit(ns):
+    """Diagnostics: the limit of every bounded wait in nanoseconds (0: the default)."""
+    return _call("qmv_set_wait_limit", int(ns))
 
 
 def qmv_get_status(stream=None):

@@ -607,6 +607,14 @@ int qmv_set_workspace(void* ptr, size_t bytes)
     return ok();
 }
 
+int qmv_set_wait_limit(unsigned ns)
+{
+    const int d = qmv::current_device();
+    if (d < 0 || d >= qmv::kMaxDevices) return fail(QMV_ERR_INVALID_ARG, "device %d out of range", d);
+    qmv::set_wait_limit_ns(d, ns);
+    return ok();
+}
+
 int qmv_get_status(void* stream)
 {
     const cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -85,11 +85,42 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
     return ok != 0;
 }
 
+// Waits with a limit under this many nanoseconds (set for diagnostics by
+// qmv_set_wait_limit) poll without blocking and check the clock after every
+// poll, so that they give up even when the phase completes a moment later.
+constexpr uint64_t kShortWaitNs = 1000000ull;
+
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+static __device__ __noinline__ bool mbar_wait_short(uint64_t* bar, uint32_t parity, unsigned* status, uint64_t limit_ns)
+{
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_test_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            atomicOr(status, QMV_DEV_WAIT_TIMEOUT);
+            return false;
+        }
+    }
+}
+
 // Wait for phase `parity` of `bar` to complete; false (and the status word
-// flagged) if it has not after QMV_WAIT_LIMIT_NS.
+// flagged) if it has not after limit_ns.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, unsigned* status,
                                                   uint64_t limit_ns = QMV_WAIT_LIMIT_NS)
 {
+    if (limit_ns < kShortWaitNs) return mbar_wait_short(bar, parity, status, limit_ns);
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {

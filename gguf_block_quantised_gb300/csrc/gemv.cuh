@@ -59,6 +59,7 @@ struct GemvParams {
     uint32_t seg_cap;   // bytes per row slot of a stage
     uint32_t xhat_bytes;
     unsigned* status;
+    unsigned long long wait_ns;   // limit of the pipeline waits (QMV_WAIT_LIMIT_NS unless overridden)
 };
 
 __device__ __forceinline__ int64_t floor16(int64_t v) { return v & ~int64_t(15); }
@@ -248,18 +249,21 @@ __global__ void __launch_bounds__(kGemvThreads, two_ctas_per_sm<T, A8, NV>() ? 2
         bool ok = true;
         int it = S;
         for (; it < n_items; ++it) {
-            ok = mbar_wait_bounded(&empty[s], ph, p.status);
+            ok = mbar_wait_bounded(&empty[s], ph, p.status, p.wait_ns);
             if (!ok) break;
             gemv_produce<F::BB>(p, tile, chunk, stage0 + (size_t)s * stage_bytes, &full[s]);
             if (++chunk == p.n_chunks) { chunk = 0; tile += gridDim.x; }
             if (++s == S) { s = 0; ph ^= 1u; }
         }
-        if (!ok && lane == 0) {
-            // The consumers stopped: let this CTA's copies in flight land
-            // (bounded) before the block leaves.
-            for (int j = max(0, it - S); j < it; ++j)
+        // Let the copies still in flight land (bounded) before the block can
+        // leave: the last S issued items, one per stage and each its stage's
+        // latest phase.  Normally they have landed already; after a consumer
+        // gave up they may not have, whatever the number of items.
+        const int issued = min(it, n_items);
+        if (lane == 0)
+            for (int j = max(0, issued - S); j < issued; ++j)
                 mbar_wait_bounded(&full[j % S], (uint32_t)((j / S) & 1), p.status, 100000000ull);
-        }
+        (void)ok;
         return;
     }
 
@@ -269,7 +273,7 @@ __global__ void __launch_bounds__(kGemvThreads, two_ctas_per_sm<T, A8, NV>() ? 2
     int chunk = 0, s = 0;
     uint32_t ph = 0;
     for (int it = 0; it < n_items; ++it) {
-        if (!mbar_wait_bounded(&full[s], ph, p.status)) return;
+        if (!mbar_wait_bounded(&full[s], ph, p.status, p.wait_ns)) return;
         const uint8_t* buf = stage0 + (size_t)s * stage_bytes;
         const int c0 = chunk * p.kb;
         const int c1 = min(p.nb, c0 + p.kb);

@@ -163,6 +163,7 @@ inline int launch_gemv_t(bool a8, bool quant_x, bool pdl, const void* W, int64_t
     p.quant_x = quant_x ? 1 : 0;
     p.xhat_bytes = pl.xhat_bytes;
     p.status = status_word();
+    p.wait_ns = wait_limit_ns(QMV_WAIT_LIMIT_NS);
     const size_t xrow = (a8 && !quant_x) ? (size_t)p.nb * act_block_bytes(T) : (size_t)cols * 4;
     for (int v0 = 0; v0 < n_vec; v0 += pl.group) {
         p.nv = min(pl.group, n_vec - v0);
@@ -178,14 +179,15 @@ inline int launch_gemv_t(bool a8, bool quant_x, bool pdl, const void* W, int64_t
 
 // ---- mixture of experts -----------------------------------------------------------
 template <int T, bool A8, int NV>
-inline int launch_moe_nv(const MoeParams& mp, const GemvPlan& pl, int grid_y, int active, cudaStream_t st)
+inline int launch_moe_nv(const MoeParams& mp, const GemvPlan& pl, int grid_y, int active, int waves,
+                         cudaStream_t st)
 {
     auto* k = &k_moe_gemv<T, A8, NV, rows_in_flight<T, NV>()>;
     const size_t smem = pl.smem + 256;
     const int occ = prepare_kernel(k, kGemvThreads, smem);
     const int64_t tr = kConsumerWarps * pl.rpw;
     const int64_t n_tiles = (mp.g.rows + tr - 1) / tr;
-    int64_t gx = ((int64_t)num_sms() * occ * 2 + active - 1) / active;
+    int64_t gx = ((int64_t)num_sms() * occ * waves + active - 1) / active;
     if (gx > n_tiles) gx = n_tiles;
     if (gx < 1) gx = 1;
     return launch_ex(k, dim3((unsigned)gx, (unsigned)grid_y), dim3(kGemvThreads), smem, st, false, mp) ==
@@ -198,8 +200,8 @@ inline int launch_moe_nv(const MoeParams& mp, const GemvPlan& pl, int grid_y, in
 // apart; pair p reads row p / kdiv and writes out[p*rows ..].
 template <int T>
 inline int launch_moe_t(bool a8, bool quant_x, const void* W3d, int n_expert, int64_t rows, int64_t cols,
-                        const int* offsets, const int* active_list, const int* perm, int n_pairs, const void* x,
-                        size_t xrow, int kdiv, float* out, const float* bias, cudaStream_t st)
+                        const int* offsets, const int* active_list, const int* perm, int n_pairs, int n_tok,
+                        const void* x, size_t xrow, int kdiv, float* out, const float* bias, cudaStream_t st)
 {
     using F = Fmt<T>;
     if (rows == 0 || n_pairs == 0) return 0;
@@ -209,7 +211,11 @@ inline int launch_moe_t(bool a8, bool quant_x, const void* W3d, int n_expert, in
     GemvPlan pl;
     // Small tiles (as many rows per warp as the kernel decodes at once) so an
     // expert's rows spread over many SMs; the stage ring is sized for that tile.
-    const int gmax = n_pairs < 16 ? n_pairs : 16;
+    // The k slots of a token normally go to k different experts, so an expert
+    // holds at most n_tok pairs: the vector group is sized for that (an expert
+    // with more pairs takes several groups).
+    const int cap = n_tok < n_pairs ? n_tok : n_pairs;
+    const int gmax = cap < 16 ? (cap > 0 ? cap : 1) : 16;
     if (!plan_gemv<T>(a8, rows, cols, gmax, pl, rows_in_flight_rt(T, gmax))) return -2;
     MoeParams mp{};
     GemvParams& p = mp.g;
@@ -227,6 +233,7 @@ inline int launch_moe_t(bool a8, bool quant_x, const void* W3d, int n_expert, in
     p.quant_x = quant_x ? 1 : 0;
     p.xhat_bytes = pl.xhat_bytes;
     p.status = status_word();
+    p.wait_ns = wait_limit_ns(QMV_WAIT_LIMIT_NS);
     p.x = x;
     mp.expert_bytes = p.total;
     mp.offsets = offsets;
@@ -238,33 +245,37 @@ inline int launch_moe_t(bool a8, bool quant_x, const void* W3d, int n_expert, in
     mp.bias = bias;
     mp.group = pl.group;
     // Grid rows map onto the experts that received pairs (at most this many).
+    // When every expert takes one group of pairs (decode) the work per expert
+    // is even and one wave of CTAs covers it; otherwise two waves of smaller
+    // shares balance experts with more pairs.
     const int active = n_pairs < n_expert ? n_pairs : n_expert;
     const int g = pl.group;
+    const int waves = cap <= g ? 1 : 2;
     if constexpr (!plain_rt(T)) {
         if (a8) {
-            if (g <= 1) return launch_moe_nv<T, true, 1>(mp, pl, active, active, st);
-            if (g <= 2) return launch_moe_nv<T, true, 2>(mp, pl, active, active, st);
-            if (g <= 4) return launch_moe_nv<T, true, 4>(mp, pl, active, active, st);
-            if (g <= 8) return launch_moe_nv<T, true, 8>(mp, pl, active, active, st);
-            return launch_moe_nv<T, true, 16>(mp, pl, active, active, st);
+            if (g <= 1) return launch_moe_nv<T, true, 1>(mp, pl, active, active, waves, st);
+            if (g <= 2) return launch_moe_nv<T, true, 2>(mp, pl, active, active, waves, st);
+            if (g <= 4) return launch_moe_nv<T, true, 4>(mp, pl, active, active, waves, st);
+            if (g <= 8) return launch_moe_nv<T, true, 8>(mp, pl, active, active, waves, st);
+            return launch_moe_nv<T, true, 16>(mp, pl, active, active, waves, st);
         }
     }
-    if (g <= 1) return launch_moe_nv<T, false, 1>(mp, pl, active, active, st);
-    if (g <= 2) return launch_moe_nv<T, false, 2>(mp, pl, active, active, st);
-    if (g <= 4) return launch_moe_nv<T, false, 4>(mp, pl, active, active, st);
-    if (g <= 8) return launch_moe_nv<T, false, 8>(mp, pl, active, active, st);
-    return launch_moe_nv<T, false, 16>(mp, pl, active, active, st);
+    if (g <= 1) return launch_moe_nv<T, false, 1>(mp, pl, active, active, waves, st);
+    if (g <= 2) return launch_moe_nv<T, false, 2>(mp, pl, active, active, waves, st);
+    if (g <= 4) return launch_moe_nv<T, false, 4>(mp, pl, active, active, waves, st);
+    if (g <= 8) return launch_moe_nv<T, false, 8>(mp, pl, active, active, waves, st);
+    return launch_moe_nv<T, false, 16>(mp, pl, active, active, waves, st);
 }
 
 }  // namespace qmv
 
 #define QMV_MOE_INSTANTIATE(T, NAME)                                                                        \
     int NAME(bool a8, bool quant_x, const void* W3d, int n_expert, int64_t rows, int64_t cols,                 \
-             const int* offsets, const int* active, const int* perm, int n_pairs, const void* x, size_t xrow,  \
-             int kdiv, float* out, const float* bias, cudaStream_t st)                                          \
+             const int* offsets, const int* active, const int* perm, int n_pairs, int n_tok, const void* x,    \
+             size_t xrow, int kdiv, float* out, const float* bias, cudaStream_t st)                             \
     {                                                                                                           \
-        return qmv::launch_moe_t<T>(a8, quant_x, W3d, n_expert, rows, cols, offsets, active, perm, n_pairs, x, \
-                                    xrow, kdiv, out, bias, st);                                                 \
+        return qmv::launch_moe_t<T>(a8, quant_x, W3d, n_expert, rows, cols, offsets, active, perm, n_pairs,    \
+                                    n_tok, x, xrow, kdiv, out, bias, st);                                       \
     }
 
 #define QMV_GEMV_INSTANTIATE(T, NAME)                                                                     \

@@ -90,8 +90,8 @@ inline size_t r256(size_t v) { return (v + 255) & ~size_t(255); }
 
 #define QMV_MOE_DECL(NAME)                                                                                      \
     int NAME(bool a8, bool quant_x, const void* W3d, int n_expert, int64_t rows, int64_t cols, const int* offsets, \
-             const int* active, const int* perm, int n_pairs, const void* x, size_t xrow, int kdiv, float* out,     \
-             const float* bias, cudaStream_t st);
+             const int* active, const int* perm, int n_pairs, int n_tok, const void* x, size_t xrow, int kdiv,      \
+             float* out, const float* bias, cudaStream_t st);
 QMV_MOE_DECL(qmv_moe_q4_0)
 QMV_MOE_DECL(qmv_moe_q5_0)
 QMV_MOE_DECL(qmv_moe_q8_0)
@@ -160,7 +160,8 @@ int qmv_launch_moe_ex(int wtype, bool a8, bool quant_x, bool bf16, size_t act_bl
                  : -3;
     }
 #define QMV_MOE_CALL(NAME) \
-    NAME(a8, quant_x, W3d, n_expert, rows, cols, offsets, active, perm, (int)n_pairs, x, xrow, kdiv, out, b, st)
+    NAME(a8, quant_x, W3d, n_expert, rows, cols, offsets, active, perm, (int)n_pairs, (int)n_tok, x, xrow, kdiv, out, \
+         b, st)
     if (!bf16) switch (wtype) {
     case QMV_Q4_0: rc = QMV_MOE_CALL(qmv_moe_q4_0); break;
     case QMV_Q5_0: rc = QMV_MOE_CALL(qmv_moe_q5_0); break;

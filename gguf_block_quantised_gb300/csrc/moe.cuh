@@ -29,7 +29,7 @@ struct MoeParams {
 };
 
 template <int T, bool A8, int NV, int RIF>
-__global__ void __launch_bounds__(kGemvThreads, 1) k_moe_gemv(const MoeParams mp)
+__global__ void __launch_bounds__(kGemvThreads, two_ctas_per_sm<T, A8, NV>() ? 2 : 1) k_moe_gemv(const MoeParams mp)
 {
     using F = Fmt<T>;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_moe_gemv(const MoeParams mp
     // so no warp is left waiting on one that gave up.
     auto wait_or_abort = [&](uint64_t* bar, uint32_t parity) {
         if (*abort_flag) return false;
-        if (mbar_wait_bounded(bar, parity, p.status)) return true;
+        if (mbar_wait_bounded(bar, parity, p.status, p.wait_ns)) return true;
         *abort_flag = 1;
         return false;
     };
@@ -96,9 +96,12 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_moe_gemv(const MoeParams mp
             if (++chunk == p.n_chunks) { chunk = 0; tile += gridDim.x; }
             if (++in_group == per_group) { in_group = 0; chunk = 0; tile = blockIdx.x; }
         }
-        if (!ok && lane == 0)
+        // Let the copies still in flight land (bounded) before the block can
+        // leave: the last S issued items, each its stage's latest phase.
+        if (lane == 0)
             for (int j = max(0, it - S); j < it; ++j)
                 mbar_wait_bounded(&full[j % S], (uint32_t)((j / S) & 1), p.status, 100000000ull);
+        (void)ok;
         return;
     }
 

@@ -33,6 +33,23 @@ inline int num_sms()
 // Device address of the library's status word (defined in api.cu).
 unsigned* status_word();
 
+// The limit of the bounded waits of the decode and expert matvec kernels
+// launched on device d: the default, or a diagnostic override
+// (qmv_set_wait_limit; 0 restores the default).
+inline std::atomic<unsigned long long>* wait_limit_slots()
+{
+    static std::atomic<unsigned long long> slots[kMaxDevices];
+    return slots;
+}
+inline void set_wait_limit_ns(int d, unsigned ns) { wait_limit_slots()[d].store(ns, std::memory_order_relaxed); }
+inline unsigned long long wait_limit_ns(unsigned long long dflt)
+{
+    const int d = current_device();
+    const unsigned long long v =
+        (d >= 0 && d < kMaxDevices) ? wait_limit_slots()[d].load(std::memory_order_relaxed) : 0ull;
+    return v ? v : dflt;
+}
+
 // Opt a kernel into `bytes` of dynamic shared memory (once per kernel and
 // device) and return how many of its blocks fit on one SM with that much.
 template <typename K>

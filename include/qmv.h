@@ -401,6 +401,17 @@ size_t qmv_workspace_size(int op, int fmt, int64_t rows, int64_t cols, int64_t n
  * the current device; NULL/0 clears it.  The library keeps the pointer only. */
 int qmv_set_workspace(void* ptr, size_t bytes);
 
+/* Diagnostics: limit the bounded pipeline waits of the decode and expert
+ * matvec kernels (qmv_matvec, qmv_moe_matvec and the block's projections with
+ * F32 or 8-bit activations) launched afterwards on the current device to `ns`
+ * nanoseconds; 0 restores the default of 2 s.  A limit under 1 ms polls without
+ * blocking, so a wait that has to wait at all gives up: it sets the status
+ * word's wait-timeout bit and its kernel stops early -- its outputs are then
+ * incomplete -- after letting its own copies in flight land.  For exercising
+ * that path in tests; calls launched while a short limit is set fail on
+ * purpose.  Host-side setting, read when a call launches its kernels. */
+int qmv_set_wait_limit(unsigned ns);
+
 /* Synchronise `stream`, read and clear the device status word of the current
  * device.  Returns QMV_OK, or QMV_ERR_DEVICE_STATUS with qmv_last_error()
  * describing the fault, or QMV_ERR_CUDA. */
