@@ -61,6 +61,7 @@ int64_t orc_block_elems(int type)
 {
     switch (type) {
     case ORC_Q4_0: case ORC_Q5_0: case ORC_Q8_0: case ORC_MXFP4: case ORC_Q4_1: case ORC_Q5_1: case ORC_Q8_1:
+    case ORC_MXFP8:
         return 32;
     case ORC_Q4_K: case ORC_Q5_K: case ORC_Q6_K: case ORC_Q8_K: case ORC_Q2_K: case ORC_Q3_K: return 256;
     default: return 0;
@@ -77,6 +78,7 @@ int64_t orc_block_bytes(int type)
     case ORC_Q4_1: return 20;
     case ORC_Q5_1: return 24;
     case ORC_MXFP4: return 17;
+    case ORC_MXFP8: return 33;
     case ORC_Q4_K: return 144;
     case ORC_Q5_K: return 176;
     case ORC_Q2_K: return 84;

@@ -93,7 +93,17 @@ static int dot_row(int wtype, int atype, const uint8_t* wrow, int64_t cols, cons
     int64_t nb = cols / bs;
     orc_block wb;
     double acc = 0.0, aabs = 0.0;
-    if (atype == ORC_F32 || atype == ORC_BF16) {
+    if (atype == ORC_MXFP8) {
+        /* block-scaled 8-bit activations: every product is exact in fp64 */
+        for (int64_t b = 0; b < nb; b++) {
+            orc_decode_block(wtype, wrow + b * bb, &wb);
+            for (int i = 0; i < 32; i++) {
+                const double p = orc_block_weight(&wb, i) * orc_mxfp8_value(xv + b * 33, i);
+                acc += p;
+                aabs += fabs(p);
+            }
+        }
+    } else if (atype == ORC_F32 || atype == ORC_BF16) {
         for (int64_t b = 0; b < nb; b++) {
             orc_decode_block(wtype, wrow + b * bb, &wb);
             for (int i = 0; i < bs; i++) {
@@ -154,7 +164,8 @@ static int check_pair(int wtype, int atype, int64_t cols)
 {
     if (orc_plain_bytes(wtype)) return (atype == ORC_F32 && cols > 0) ? ORC_OK : ORC_EUNSUP;
     if (!weight_type_ok(wtype)) return ORC_EUNSUP;
-    if (atype != ORC_F32 && atype != ORC_BF16 && atype != paired_act(wtype)) return ORC_EUNSUP;
+    if (atype == ORC_MXFP8 && orc_block_elems(wtype) != 32) return ORC_EUNSUP;
+    if (atype != ORC_F32 && atype != ORC_BF16 && atype != ORC_MXFP8 && atype != paired_act(wtype)) return ORC_EUNSUP;
     if (cols <= 0 || cols % orc_block_elems(wtype)) return ORC_ESHAPE;
     return ORC_OK;
 }

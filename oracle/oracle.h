@@ -35,7 +35,8 @@ enum {
     ORC_Q4_0 = 1, ORC_Q5_0 = 2, ORC_Q8_0 = 3, ORC_Q4_K = 4, ORC_Q6_K = 5,
     ORC_MXFP4 = 6, ORC_Q8_K = 7, ORC_F32 = 8, ORC_BF16 = 9,
     ORC_Q4_1 = 10, ORC_Q5_1 = 11, ORC_Q5_K = 12, ORC_Q2_K = 13, ORC_Q3_K = 14,
-    ORC_Q8_1 = 15, ORC_F16 = 16
+    ORC_Q8_1 = 15, ORC_F16 = 16,
+    ORC_MXFP8 = 17   /* activations: E8M0 scale | 32 E4M3 codes, 33 bytes (mx.c) */
 };
 
 /* Return codes. */
@@ -105,6 +106,8 @@ int     orc_block_dots(int wtype, const uint8_t* W, int64_t rows, int64_t cols,
  * (row_ids == NULL selects all rows in order).  atype:
  *   ORC_F32  : x is fp32 [n_vec][cols], xhat = x, w exact;
  *   ORC_BF16 : x is bf16 [n_vec][cols], xhat = x, w rounded to bf16 first;
+ *   ORC_MXFP8: x is [n_vec][cols/32] MXFP8 blocks (32-element weight types),
+ *              xhat = E4M3 * 2^(e-127) exactly, products in fp64;
  *   ORC_Q8_0 / ORC_Q8_K : x is [n_vec][cols/bs] blocks, the per-block integer
  *              dots are scaled by the weight and activation scales in fp64.
  * yabs (nullable) receives sum_c |w*xhat| per output, in the same layout. */
@@ -123,6 +126,15 @@ int     orc_moe(int wtype, int atype, const uint8_t* W3d, int64_t n_expert,
                 int64_t rows, int64_t cols, const int32_t* ids, const float* gates,
                 int64_t k, const void* x, int64_t n_tok, const float* bias,
                 double* y, double* yabs);
+
+/* ---- mx.c : MXFP8 activations ---- */
+double  orc_e4m3_to_f64(uint8_t b);
+/* Round to the nearest E4M3 value (ties to even), magnitudes clamped to 448. */
+uint8_t orc_f64_to_e4m3_rn_sat(double v);
+/* n fp32 values (n a multiple of 32, all finite) -> n/32 MXFP8 blocks. */
+int     orc_quantize_mxfp8(const float* x, int64_t n, uint8_t* out);
+/* Element i of an MXFP8 block, exactly. */
+double  orc_mxfp8_value(const uint8_t* blk, int i);
 
 /* ---- moeblock.c : the router and the gated activation of an expert block ---- */
 /* logits[t][e] = x[t] . Wr[e] (+ br[e]) in fp32, in the 32-partial order the

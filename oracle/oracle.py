@@ -21,13 +21,13 @@ import numpy as np
 HERE = os.path.dirname(os.path.abspath(__file__))
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "liboracle.so")
-SOURCES = ["fp.c", "blocks.c", "quant.c", "wquant.c", "mm.c", "moeblock.c"]
+SOURCES = ["fp.c", "blocks.c", "quant.c", "wquant.c", "mm.c", "moeblock.c", "mx.c"]
 
 # The oracle's own type numbers (oracle.h).
-Q4_0, Q5_0, Q8_0, Q4_K, Q6_K, MXFP4, Q8_K, F32, BF16, Q4_1, Q5_1, Q5_K, Q2_K, Q3_K, Q8_1, F16 = range(1, 17)
-BLOCK_ELEMS = {Q4_0: 32, Q5_0: 32, Q8_0: 32, MXFP4: 32, Q4_K: 256, Q6_K: 256, Q8_K: 256, Q4_1: 32, Q5_1: 32,
+Q4_0, Q5_0, Q8_0, Q4_K, Q6_K, MXFP4, Q8_K, F32, BF16, Q4_1, Q5_1, Q5_K, Q2_K, Q3_K, Q8_1, F16, MXFP8 = range(1, 18)
+BLOCK_ELEMS = {MXFP8: 32, Q4_0: 32, Q5_0: 32, Q8_0: 32, MXFP4: 32, Q4_K: 256, Q6_K: 256, Q8_K: 256, Q4_1: 32, Q5_1: 32,
                Q5_K: 256, Q2_K: 256, Q3_K: 256, Q8_1: 32, F32: 1, F16: 1, BF16: 1}
-BLOCK_BYTES = {Q4_0: 18, Q5_0: 22, Q8_0: 34, MXFP4: 17, Q4_K: 144, Q6_K: 210, Q8_K: 292, Q4_1: 20, Q5_1: 24,
+BLOCK_BYTES = {MXFP8: 33, Q4_0: 18, Q5_0: 22, Q8_0: 34, MXFP4: 17, Q4_K: 144, Q6_K: 210, Q8_K: 292, Q4_1: 20, Q5_1: 24,
                Q5_K: 176, Q2_K: 84, Q3_K: 110, Q8_1: 36, F32: 4, F16: 2, BF16: 2}
 
 _lock = threading.Lock()
@@ -83,6 +83,10 @@ def lib():
             L.orc_topk_softmax.restype = I
             L.orc_swiglu.argtypes = [C.c_double, C.c_double, C.c_double, C.c_double]
             L.orc_swiglu.restype = C.c_double
+            L.orc_e4m3_to_f64.argtypes = [C.c_uint8]
+            L.orc_e4m3_to_f64.restype = C.c_double
+            L.orc_f64_to_e4m3_rn_sat.argtypes = [C.c_double]
+            L.orc_f64_to_e4m3_rn_sat.restype = C.c_uint8
             for f in ("orc_dequant", "orc_quantize_act", "orc_quantize_weights", "orc_block_dots", "orc_matvec",
                       "orc_moe", "orc_decode_block"):
                 getattr(L, f).restype = I
@@ -272,3 +276,25 @@ def moe_block(wt: int, at: int, x: np.ndarray, Wr, br, Wgu, bgu, Wdown, bdown, n
     if detail:
         return y, yabs, ids, gates, dict(y1=y1, y1abs=y1abs, h=h)
     return y, yabs, ids, gates
+
+
+# ---- MXFP8 activations (mx.c) -----------------------------------------------------------
+
+def e4m3_to_f64(b: int) -> float:
+    return lib().orc_e4m3_to_f64(int(b))
+
+
+def f64_to_e4m3(v: float) -> int:
+    """Nearest E4M3 code (ties to even), magnitudes clamped to 448."""
+    return lib().orc_f64_to_e4m3_rn_sat(float(v))
+
+
+def mxfp8_values(blocks: np.ndarray) -> np.ndarray:
+    """MXFP8 blocks uint8 [..., nb*33] -> the values they hold, float64 [..., nb*32]."""
+    b = np.ascontiguousarray(blocks, dtype=np.uint8)
+    lead = b.shape[:-1]
+    nb = b.shape[-1] // 33
+    b = b.reshape(-1, nb, 33)
+    tab = np.array([e4m3_to_f64(i) for i in range(256)])
+    v = tab[b[:, :, 1:]] * np.ldexp(1.0, b[:, :, :1].astype(np.int64) - 127)
+    return v.reshape(lead + (nb * 32,))

@@ -50,6 +50,7 @@ static void quantize_block(const float* x, int bs, float* d_out, int8_t* q)
 int orc_quantize_act(int atype, const float* x, int64_t n, uint8_t* out)
 {
     int64_t bs = orc_block_elems(atype), bb = orc_block_bytes(atype);
+    if (atype == ORC_MXFP8) return orc_quantize_mxfp8(x, n, out);
     if (atype != ORC_Q8_0 && atype != ORC_Q8_K) return ORC_EUNSUP;
     if (n < 0) return ORC_EINVAL;
     if (n % bs) return ORC_ESHAPE;
