@@ -17,10 +17,10 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "_build", "libqmv.so")
 
 Q4_0, Q5_0, Q8_0, Q4_K, Q6_K, MXFP4, Q8_K, F32, BF16, MXFP4_R = 1, 2, 3, 4, 5, 6, 7, 8, 9, 10
-Q4_1, Q5_1, Q8_1, Q2_K, Q3_K, Q5_K, F16 = 11, 12, 13, 14, 15, 16, 17
+Q4_1, Q5_1, Q8_1, Q2_K, Q3_K, Q5_K, F16, MXFP8 = 11, 12, 13, 14, 15, 16, 17, 18
 NAMES = {Q4_0: "Q4_0", Q5_0: "Q5_0", Q8_0: "Q8_0", Q4_K: "Q4_K", Q6_K: "Q6_K", MXFP4: "MXFP4",
          Q8_K: "Q8_K", F32: "F32", BF16: "BF16", MXFP4_R: "MXFP4_R", Q4_1: "Q4_1", Q5_1: "Q5_1",
-         Q8_1: "Q8_1", Q2_K: "Q2_K", Q3_K: "Q3_K", Q5_K: "Q5_K", F16: "F16"}
+         Q8_1: "Q8_1", Q2_K: "Q2_K", Q3_K: "Q3_K", Q5_K: "Q5_K", F16: "F16", MXFP8: "MXFP8"}
 OP_MATVEC, OP_MATMUL, OP_MOE = 1, 2, 3
 OK, ERR_INVALID_ARG, ERR_SHAPE, ERR_UNSUPPORTED, ERR_ALIGN, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_STATUS = \
     0, -1, -2, -3, -4, -5, -6, -7

@@ -45,16 +45,18 @@ QMV_GEMV_DECL(qmv_gemv_bf16)
 size_t qmv_w4a8_workspace_bytes(int64_t cols, int64_t m);
 int qmv_launch_gemm_q4k_w4a8(const void* W, int64_t rows, int64_t cols, const void* X, float* Y, int64_t m,
                              void* ws, bool pdl, cudaStream_t st);
-size_t qmv_moe_workspace_bytes(bool bf16, int64_t rows, int64_t cols, int64_t n_pairs);
-size_t qmv_moe_block_workspace_bytes(bool bf16, int n_expert, int64_t hidden, int64_t inter, int64_t n_tok, int k);
-int qmv_launch_moe_block(int wtype, bool a8, bool bf16, size_t act_block_bytes, int n_expert, int k,
+size_t qmv_moe_workspace_bytes(bool bf16, int64_t rows, int64_t cols, int64_t n_pairs, bool mx);
+size_t qmv_moe_block_workspace_bytes(bool bf16, bool mx, int n_expert, int64_t hidden, int64_t inter, int64_t n_tok,
+                                     int k);
+int qmv_launch_moe_block(int wtype, bool a8, bool bf16, bool mx, size_t act_block_bytes, int n_expert, int k,
                          int64_t hidden, int64_t inter, const float* Wr, const float* br, const void* Wgu,
                          const float* bgu, const void* Wd, const float* bd, float alpha, float limit, const float* x,
                          int64_t n_tok, float* y, int32_t* ids, float* gates, void* ws, cudaStream_t st);
 int qmv_launch_repack_mxfp4(const void* W, int64_t rows, int64_t cols, void* Wout, cudaStream_t st);
-int qmv_launch_moe(int wtype, bool a8, bool quant_x, bool bf16, size_t act_block_bytes, const void* W3d,
-                   int n_expert, int64_t rows, int64_t cols, const int32_t* ids, const float* gates, int k,
-                   const void* x, float* y, int64_t n_tok, const float* bias, void* ws, cudaStream_t st);
+int qmv_launch_moe_ex(int wtype, bool a8, bool quant_x, bool bf16, bool mx, size_t act_block_bytes,
+                      const void* W3d, int n_expert, int64_t rows, int64_t cols, const int32_t* ids,
+                      const float* gates, int k, const void* x, float* y, int64_t n_tok, const float* bias, void* ws,
+                      bool grouped, cudaStream_t st);
 int qmv_launch_gemm_q4k_bf16(const void* W, int64_t rows, int64_t cols, const void* X, float* Y, int64_t m, bool pdl,
                              cudaStream_t st);
 
@@ -126,6 +128,7 @@ const char* type_name(int t)
     case QMV_Q3_K: return "Q3_K";
     case QMV_Q5_K: return "Q5_K";
     case QMV_F16: return "F16";
+    case QMV_MXFP8: return "MXFP8";
     default: return "unknown";
     }
 }
@@ -186,7 +189,7 @@ Workspace g_ws[qmv::kMaxDevices];
 // What the argument checks of the MoE calls settle.
 struct MoeCall {
     int wtype = 0;
-    bool a8 = false, quant_x = false, bf16 = false;
+    bool a8 = false, quant_x = false, bf16 = false, mx = false;
     bool empty = false;   // nothing to compute: return QMV_OK
     size_t need = 0;      // bytes of scratch
 };
@@ -203,32 +206,35 @@ int moe_check(const char* name, int fmt, const void* W3d, int n_expert, int64_t 
     c.wtype = fmt & 0xff;
     const int atype = (fmt >> 8) & 0xff;
     c.bf16 = atype == QMV_BF16 && (c.wtype == QMV_MXFP4 || c.wtype == QMV_MXFP4_R);
-    if (c.wtype == QMV_MXFP4_R && !c.bf16)
-        return fail(QMV_ERR_UNSUPPORTED, "%s: repacked MXFP4_R experts take BF16 activations (got %s)", name,
+    c.mx = atype == QMV_MXFP8 && (c.wtype == QMV_MXFP4 || c.wtype == QMV_MXFP4_R);
+    if (c.wtype == QMV_MXFP4_R && !c.bf16 && !c.mx)
+        return fail(QMV_ERR_UNSUPPORTED, "%s: repacked MXFP4_R experts take BF16 or MXFP8 activations (got %s)", name,
                     type_name(atype));
-    if (is_weight_type(c.wtype) && atype != QMV_F32 && atype != paired_act(c.wtype) && !c.bf16)
+    if (is_weight_type(c.wtype) && atype != QMV_F32 && atype != paired_act(c.wtype) && !c.bf16 && !c.mx)
         return fail(QMV_ERR_UNSUPPORTED, "%s: %s experts take F32 or %s activations%s (got %s)", name,
-                    type_name(c.wtype), type_name(paired_act(c.wtype)), c.wtype == QMV_MXFP4 ? " or BF16" : "",
-                    type_name(atype));
+                    type_name(c.wtype), type_name(paired_act(c.wtype)),
+                    c.wtype == QMV_MXFP4 ? ", BF16 or MXFP8" : "", type_name(atype));
     // MXFP4_R has the MXFP4 block geometry (padded rows)
     int rc = check_weights(c.wtype == QMV_MXFP4_R ? QMV_MXFP4 : c.wtype, W3d, rows, cols);
     if (rc) return rc;
-    if (c.quant_x && (atype == QMV_F32 || c.bf16))
+    if (c.quant_x && (atype == QMV_F32 || c.bf16 || c.mx))
         return fail(QMV_ERR_INVALID_ARG, "QMV_FLAG_QUANTIZE_X needs an 8-bit activation type (Q8_0 or Q8_K)");
     if (n_expert < 1 || n_expert > 1024) return fail(QMV_ERR_INVALID_ARG, "n_expert must be in 1..1024 (got %d)", n_expert);
     if (k < 1 || k > 64) return fail(QMV_ERR_INVALID_ARG, "k must be in 1..64 (got %d)", k);
     if (n_tok < 0 || n_tok > ((int64_t)1 << 24) / k)   // range first: n_tok * k must not overflow
         return fail(QMV_ERR_INVALID_ARG, "n_tok must be >= 0 with n_tok*k <= 16777216");
-    if (c.bf16 && rows > (int64_t)1 << 30) return fail(QMV_ERR_SHAPE, "rows must be below 2^30");
+    if ((c.bf16 || c.mx) && rows > (int64_t)1 << 30) return fail(QMV_ERR_SHAPE, "rows must be below 2^30");
+    if (c.mx && cols > 4096)
+        return fail(QMV_ERR_SHAPE, "%s: MXFP8 activations take cols <= 4096 (got %lld)", name, (long long)cols);
     c.empty = n_tok == 0 || rows == 0;
     if (c.empty) return QMV_OK;
     if (!ids || !x || !y) return fail(QMV_ERR_INVALID_ARG, "ids, x and y must not be NULL");
-    c.a8 = atype != QMV_F32 && !c.bf16;
+    c.a8 = atype != QMV_F32 && !c.bf16 && !c.mx;
     const int xal = (c.a8 && !c.quant_x) ? 4 : 16;
     if (!aligned(x, xal)) return fail(QMV_ERR_ALIGN, "x must be %d-byte aligned", xal);
     if (!aligned(ids, 4) || !aligned(y, 4) || (gates && !aligned(gates, 4)) || (bias && !aligned(bias, 4)))
         return fail(QMV_ERR_ALIGN, "ids, gates, bias and y must be 4-byte aligned");
-    c.need = qmv_moe_workspace_bytes(c.bf16, rows, cols, n_tok * k);
+    c.need = qmv_moe_workspace_bytes(c.bf16, rows, cols, n_tok * k, c.mx);
     return QMV_OK;
 }
 
@@ -237,9 +243,9 @@ int moe_run(const char* name, const MoeCall& c, const void* W3d, int n_expert, i
             void* ws, void* stream)
 {
     if (!qmv::status_word()) return cuda_fail(name);
-    const int rc = qmv_launch_moe(c.wtype, c.a8, c.quant_x, c.bf16, qmv_block_bytes(paired_act(c.wtype)), W3d,
-                                  n_expert, rows, cols, ids, gates, k, x, y, n_tok, bias, ws,
-                                  static_cast<cudaStream_t>(stream));
+    const int rc = qmv_launch_moe_ex(c.wtype, c.a8, c.quant_x, c.bf16, c.mx, qmv_block_bytes(paired_act(c.wtype)),
+                                     W3d, n_expert, rows, cols, ids, gates, k, x, y, n_tok, bias, ws, false,
+                                     static_cast<cudaStream_t>(stream));
     if (rc == -2) return fail(QMV_ERR_SHAPE, "cols = %lld needs more shared memory than one SM has", (long long)cols);
     if (rc == -8) return fail(QMV_ERR_CUDA, "%s: could not build a TMA tensor map", name);
     if (rc) return cuda_fail(name);
@@ -273,7 +279,7 @@ int qmv_block_elems(int type)
 {
     switch (type) {
     case QMV_Q4_0: case QMV_Q5_0: case QMV_Q8_0: case QMV_MXFP4: case QMV_MXFP4_R: case QMV_Q4_1: case QMV_Q5_1:
-    case QMV_Q8_1: return 32;
+    case QMV_Q8_1: case QMV_MXFP8: return 32;
     case QMV_Q4_K: case QMV_Q6_K: case QMV_Q8_K: case QMV_Q2_K: case QMV_Q3_K: case QMV_Q5_K: return 256;
     case QMV_F32: case QMV_BF16: case QMV_F16: return 1;
     default: return 0;
@@ -287,6 +293,7 @@ size_t qmv_block_bytes(int type)
     case QMV_Q5_0: return 22;
     case QMV_Q8_0: return 34;
     case QMV_MXFP4: case QMV_MXFP4_R: return 17;
+    case QMV_MXFP8: return 33;
     case QMV_Q4_K: return 144;
     case QMV_Q6_K: return 210;
     case QMV_Q8_K: return 292;
@@ -315,17 +322,18 @@ int qmv_quantize_act(int fmt, const float* x, void* xq, int64_t n, void* stream)
     const bool pdl = (fmt & QMV_FLAG_PDL) != 0;
     if (fmt & ~(0xffff | QMV_FLAG_PDL)) return fail(QMV_ERR_INVALID_ARG, "unknown flags 0x%x", fmt & ~0xffff);
     fmt &= 0xffff;
-    if (fmt != QMV_Q8_0 && fmt != QMV_Q8_K)
-        return fail(QMV_ERR_UNSUPPORTED, "activation format %d (%s) is not supported; supported: Q8_0, Q8_K", fmt,
-                    type_name(fmt));
+    if (fmt != QMV_Q8_0 && fmt != QMV_Q8_K && fmt != QMV_MXFP8)
+        return fail(QMV_ERR_UNSUPPORTED, "activation format %d (%s) is not supported; supported: Q8_0, Q8_K, MXFP8",
+                    fmt, type_name(fmt));
     const int bs = qmv_block_elems(fmt);
     if (n < 0) return fail(QMV_ERR_INVALID_ARG, "n must be >= 0");
     if (n % bs) return fail(QMV_ERR_SHAPE, "%s quantises %d-element blocks; n = %lld is not a multiple of %d",
                             type_name(fmt), bs, (long long)n, bs);
     if (n == 0) return ok();
     if (!x || !xq) return fail(QMV_ERR_INVALID_ARG, "x and xq must not be NULL");
-    if (!aligned(x, fmt == QMV_Q8_K ? 16 : 4)) return fail(QMV_ERR_ALIGN, "x must be %d-byte aligned", fmt == QMV_Q8_K ? 16 : 4);
-    if (!aligned(xq, fmt == QMV_Q8_K ? 4 : 2)) return fail(QMV_ERR_ALIGN, "xq must be %d-byte aligned", fmt == QMV_Q8_K ? 4 : 2);
+    const int xal = fmt == QMV_Q8_0 ? 4 : 16, qal = fmt == QMV_Q8_K ? 4 : fmt == QMV_Q8_0 ? 2 : 1;
+    if (!aligned(x, xal)) return fail(QMV_ERR_ALIGN, "x must be %d-byte aligned", xal);
+    if (!aligned(xq, qal)) return fail(QMV_ERR_ALIGN, "xq must be %d-byte aligned", qal);
     if (qmv_launch_quantize(fmt, x, xq, n, pdl, static_cast<cudaStream_t>(stream))) return cuda_fail("qmv_quantize_act");
     return ok();
 }
@@ -527,15 +535,18 @@ int qmv_moe_block(int fmt, int n_expert, int k, int64_t hidden, int64_t inter, c
                                    "quantised inside the block)", fmt & ~0xffff);
     const int wtype = fmt & 0xff, atype = (fmt >> 8) & 0xff;
     const bool bf16 = atype == QMV_BF16 && (wtype == QMV_MXFP4 || wtype == QMV_MXFP4_R);
-    if (wtype == QMV_MXFP4_R && !bf16)
-        return fail(QMV_ERR_UNSUPPORTED, "%s: repacked MXFP4_R experts take BF16 activations (got %s)", name,
+    const bool mx = atype == QMV_MXFP8 && (wtype == QMV_MXFP4 || wtype == QMV_MXFP4_R);
+    if (wtype == QMV_MXFP4_R && !bf16 && !mx)
+        return fail(QMV_ERR_UNSUPPORTED, "%s: repacked MXFP4_R experts take BF16 or MXFP8 activations (got %s)", name,
                     type_name(atype));
     if (!is_weight_type(wtype) && wtype != QMV_MXFP4_R)
         return fail(QMV_ERR_UNSUPPORTED, "%s: %s is not a weight type", name, type_name(wtype));
-    if (atype != QMV_F32 && atype != paired_act(wtype) && !bf16)
+    if (atype != QMV_F32 && atype != paired_act(wtype) && !bf16 && !mx)
         return fail(QMV_ERR_UNSUPPORTED, "%s: %s experts take F32 or %s activations%s (got %s)", name,
-                    type_name(wtype), type_name(paired_act(wtype)), wtype == QMV_MXFP4 ? " or BF16" : "",
+                    type_name(wtype), type_name(paired_act(wtype)), wtype == QMV_MXFP4 ? ", BF16 or MXFP8" : "",
                     type_name(atype));
+    if (mx && (hidden > 4096 || inter > 4096))
+        return fail(QMV_ERR_SHAPE, "%s: MXFP8 activations take hidden and inter <= 4096", name);
     if (n_expert < 1 || n_expert > 1024) return fail(QMV_ERR_INVALID_ARG, "n_expert must be in 1..1024 (got %d)", n_expert);
     if (k < 1 || k > 64 || k > n_expert)
         return fail(QMV_ERR_INVALID_ARG, "k must be in 1..min(64, n_expert) (got %d)", k);
@@ -547,7 +558,7 @@ int qmv_moe_block(int fmt, int n_expert, int k, int64_t hidden, int64_t inter, c
     if (rc) return rc;
     rc = check_weights(geo, W_down, hidden, inter);
     if (rc) return rc;
-    if (bf16 && (2 * inter > (int64_t)1 << 30 || hidden > (int64_t)1 << 30))
+    if ((bf16 || mx) && (2 * inter > (int64_t)1 << 30 || hidden > (int64_t)1 << 30))
         return fail(QMV_ERR_SHAPE, "rows must be below 2^30");
     if (n_tok == 0) return ok();
     if (!Wr || !x || !y || !ids || !gates)
@@ -556,7 +567,7 @@ int qmv_moe_block(int fmt, int n_expert, int k, int64_t hidden, int64_t inter, c
     if (!aligned(Wr, 4) || !aligned(y, 4) || !aligned(ids, 4) || !aligned(gates, 4) || (br && !aligned(br, 4)) ||
         (b_gu && !aligned(b_gu, 4)) || (b_down && !aligned(b_down, 4)))
         return fail(QMV_ERR_ALIGN, "Wr, br, biases, y, ids and gates must be 4-byte aligned");
-    const size_t need = qmv_moe_block_workspace_bytes(bf16, n_expert, hidden, inter, n_tok, k);
+    const size_t need = qmv_moe_block_workspace_bytes(bf16, mx, n_expert, hidden, inter, n_tok, k);
     const int d = qmv::current_device();
     void* ws = nullptr;
     size_t have = 0;
@@ -569,7 +580,7 @@ int qmv_moe_block(int fmt, int n_expert, int k, int64_t hidden, int64_t inter, c
         return fail(QMV_ERR_WORKSPACE, "%s needs %zu bytes of workspace (qmv_moe_block_workspace_size); %zu set",
                     name, need, have);
     if (!qmv::status_word()) return cuda_fail(name);
-    rc = qmv_launch_moe_block(wtype, atype != QMV_F32 && !bf16, bf16, qmv_block_bytes(paired_act(wtype)), n_expert,
+    rc = qmv_launch_moe_block(wtype, atype != QMV_F32 && !bf16 && !mx, bf16, mx, qmv_block_bytes(paired_act(wtype)), n_expert,
                               k, hidden, inter, Wr, br, W_gu, b_gu, W_down, b_down, alpha, limit, x, n_tok, y, ids,
                               gates, ws, static_cast<cudaStream_t>(stream));
     if (rc == -2) return fail(QMV_ERR_SHAPE, "%s: a projection needs more shared memory than one SM has", name);
@@ -583,13 +594,15 @@ size_t qmv_moe_block_workspace_size(int fmt, int n_expert, int k, int64_t hidden
     if (n_expert < 1 || k < 1 || hidden <= 0 || inter <= 0 || n_tok <= 0) return 0;
     const int wtype = fmt & 0xff, atype = (fmt >> 8) & 0xff;
     const bool bf16 = atype == QMV_BF16 && (wtype == QMV_MXFP4 || wtype == QMV_MXFP4_R);
-    return qmv_moe_block_workspace_bytes(bf16, n_expert, hidden, inter, n_tok, k);
+    const bool mx = atype == QMV_MXFP8 && (wtype == QMV_MXFP4 || wtype == QMV_MXFP4_R);
+    return qmv_moe_block_workspace_bytes(bf16, mx, n_expert, hidden, inter, n_tok, k);
 }
 
 size_t qmv_workspace_size(int op, int fmt, int64_t rows, int64_t cols, int64_t n)
 {
     if (op == QMV_OP_MOE && rows > 0 && n > 0 && cols >= 0)
-        return qmv_moe_workspace_bytes(((fmt >> 8) & 0xff) == QMV_BF16, rows, cols, n);
+        return qmv_moe_workspace_bytes(((fmt >> 8) & 0xff) == QMV_BF16, rows, cols, n,
+                                       ((fmt >> 8) & 0xff) == QMV_MXFP8);
     if (op == QMV_OP_MATMUL && (fmt & 0xffff) == QMV_FMT(QMV_Q4_K, QMV_Q8_K) && rows > 0 && n > 0 && cols > 0 &&
         cols % 256 == 0)
         return qmv_w4a8_workspace_bytes(cols, n);

@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 #include "../../include/qmv.h"
@@ -306,6 +307,31 @@ __device__ __forceinline__ float warp_max(float v)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
     return v;
+}
+
+// ---- MXFP8 activations (OCP Microscaling v1.0) -----------------------------------
+// The scale exponent E of a 32-element block with largest magnitude amax:
+// floor(log2(amax)) - 8 (8: the largest E4M3 exponent), at least -127; -127 for
+// a block of zeros.  Stored as the E8M0 byte E + 127.
+__device__ __forceinline__ int mx_scale_exp(float amax)
+{
+    const uint32_t b = __float_as_uint(amax);
+    const int ef = (int)((b >> 23) & 0xffu);
+    int lg;
+    if (ef) lg = ef - 127;
+    else if (b) lg = (31 - __clz((int)(b & 0x7fffffu))) - 149;   // subnormal amax
+    else return -127;
+    const int E = lg - 8;
+    return E < -127 ? -127 : E;
+}
+
+// E4M3 code of x / 2^E: the scaling by a power of two is exact (a result
+// below 2^-126 is far below half the smallest E4M3 step, so its rounding does
+// not matter), then round to nearest even, magnitudes clamped to 448.
+__device__ __forceinline__ uint32_t mx_e4m3(float x, int E)
+{
+    const float s = __uint_as_float((uint32_t)(127 - E) << 23);   // 2^-E, E in [-127, 119]
+    return (uint32_t)__nv_cvt_float_to_fp8(__fmul_rn(x, s), __NV_SATFINITE, __NV_E4M3);
 }
 
 }  // namespace qmv

@@ -108,30 +108,31 @@ QMV_MOE_DECL(qmv_moe_f32)
 QMV_MOE_DECL(qmv_moe_f16)
 QMV_MOE_DECL(qmv_moe_bf16)
 
-size_t qmv_moe_gemm_extra_bytes(int64_t cols, int64_t n_pairs);
-int qmv_launch_moe_gemm_mxfp4(const void* W3d, bool planar, int n_expert, int64_t rows, int64_t cols, const void* x,
-                              int kdiv, int64_t n_pairs, const int* offsets, const int* active, const int* perm,
-                              void* ws, float* out, const float* bias, cudaStream_t st);
+size_t qmv_moe_gemm_extra_bytes(int64_t cols, int64_t n_pairs, bool mx);
+int qmv_launch_moe_gemm_mxfp4(const void* W3d, bool planar, bool mx, int n_expert, int64_t rows, int64_t cols,
+                              const void* x, int kdiv, int64_t n_pairs, const int* offsets, const int* active,
+                              const int* perm, void* ws, float* out, const float* bias, cudaStream_t st);
 
 // Workspace layout: offsets[1025] + active[1025] | perm[n_pairs] | per-slot
-// outputs [n_pairs][rows] fp32 | (bf16 activations only) the grouped GEMM's
-// slot list and packed activations.
-size_t qmv_moe_workspace_bytes(bool bf16, int64_t rows, int64_t cols, int64_t n_pairs)
+// outputs [n_pairs][rows] fp32 | (the grouped GEMM's activations, bf16 or
+// MXFP8, only) its slot list and packed activations.
+size_t qmv_moe_workspace_bytes(bool bf16, int64_t rows, int64_t cols, int64_t n_pairs, bool mx)
 {
     using qmv::r256;
     const size_t base = r256(2050 * 4) + r256((size_t)n_pairs * 4) + r256((size_t)n_pairs * (size_t)rows * 4);
-    return base + (bf16 ? qmv_moe_gemm_extra_bytes(cols, n_pairs) : 0);
+    return base + ((bf16 || mx) ? qmv_moe_gemm_extra_bytes(cols, n_pairs, mx) : 0);
 }
 
 // bf16: MXFP4 experts with bf16 activations, through the grouped tensor-core
-// GEMM (moe_gemm.cu); otherwise the expert matvecs of moe.cuh.  grouped: the
+// GEMM (moe_gemm.cu); mx: the same with fp32 activations quantised to MXFP8
+// on the block-scaled MMA; otherwise the expert matvecs of moe.cuh.  grouped: the
 // workspace already holds the grouping of these ids (an earlier call with the
 // same ids, n_tok and k on this workspace), so it is not rebuilt.
 // Returns 0, -2 (shape beyond the plan), -6 (launch failure), -8 (tensor map).
-int qmv_launch_moe_ex(int wtype, bool a8, bool quant_x, bool bf16, size_t act_block_bytes, const void* W3d,
-                      int n_expert, int64_t rows, int64_t cols, const int32_t* ids, const float* gates, int k,
-                      const void* x, float* y, int64_t n_tok, const float* bias, void* ws, bool grouped,
-                      cudaStream_t st)
+int qmv_launch_moe_ex(int wtype, bool a8, bool quant_x, bool bf16, bool mx, size_t act_block_bytes,
+                      const void* W3d, int n_expert, int64_t rows, int64_t cols, const int32_t* ids,
+                      const float* gates, int k, const void* x, float* y, int64_t n_tok, const float* bias, void* ws,
+                      bool grouped, cudaStream_t st)
 {
     using namespace qmv;
     const int64_t n_pairs = n_tok * k;
@@ -152,17 +153,17 @@ int qmv_launch_moe_ex(int wtype, bool a8, bool quant_x, bool bf16, size_t act_bl
     float* out = gates ? part : y;
     const float* b = gates ? nullptr : bias;
     int rc = -3;
-    if (bf16) {
+    if (bf16 || mx) {
         void* gws = w + r256(2050 * 4) + r256((size_t)n_pairs * 4) + r256((size_t)n_pairs * (size_t)rows * 4);
         rc = wtype == QMV_MXFP4 || wtype == QMV_MXFP4_R
-                 ? qmv_launch_moe_gemm_mxfp4(W3d, wtype == QMV_MXFP4_R, n_expert, rows, cols, x, kdiv, n_pairs,
+                 ? qmv_launch_moe_gemm_mxfp4(W3d, wtype == QMV_MXFP4_R, mx, n_expert, rows, cols, x, kdiv, n_pairs,
                                              offsets, active, perm, gws, out, b, st)
                  : -3;
     }
 #define QMV_MOE_CALL(NAME) \
     NAME(a8, quant_x, W3d, n_expert, rows, cols, offsets, active, perm, (int)n_pairs, (int)n_tok, x, xrow, kdiv, out, \
          b, st)
-    if (!bf16) switch (wtype) {
+    if (!bf16 && !mx) switch (wtype) {
     case QMV_Q4_0: rc = QMV_MOE_CALL(qmv_moe_q4_0); break;
     case QMV_Q5_0: rc = QMV_MOE_CALL(qmv_moe_q5_0); break;
     case QMV_Q8_0: rc = QMV_MOE_CALL(qmv_moe_q8_0); break;
@@ -193,6 +194,6 @@ int qmv_launch_moe(int wtype, bool a8, bool quant_x, bool bf16, size_t act_block
                    int n_expert, int64_t rows, int64_t cols, const int32_t* ids, const float* gates, int k,
                    const void* x, float* y, int64_t n_tok, const float* bias, void* ws, cudaStream_t st)
 {
-    return qmv_launch_moe_ex(wtype, a8, quant_x, bf16, act_block_bytes, W3d, n_expert, rows, cols, ids, gates, k, x,
-                             y, n_tok, bias, ws, false, st);
+    return qmv_launch_moe_ex(wtype, a8, quant_x, bf16, false, act_block_bytes, W3d, n_expert, rows, cols, ids, gates,
+                             k, x, y, n_tok, bias, ws, false, st);
 }

@@ -189,29 +189,32 @@ inline size_t r256b(size_t v) { return (v + 255) & ~size_t(255); }
 
 }  // namespace qmv
 
-size_t qmv_moe_workspace_bytes(bool bf16, int64_t rows, int64_t cols, int64_t n_pairs);
-int qmv_launch_moe_ex(int wtype, bool a8, bool quant_x, bool bf16, size_t act_block_bytes, const void* W3d,
-                      int n_expert, int64_t rows, int64_t cols, const int32_t* ids, const float* gates, int k,
-                      const void* x, float* y, int64_t n_tok, const float* bias, void* ws, bool grouped,
-                      cudaStream_t st);
+size_t qmv_moe_workspace_bytes(bool bf16, int64_t rows, int64_t cols, int64_t n_pairs, bool mx);
+int qmv_launch_moe_ex(int wtype, bool a8, bool quant_x, bool bf16, bool mx, size_t act_block_bytes,
+                      const void* W3d, int n_expert, int64_t rows, int64_t cols, const int32_t* ids,
+                      const float* gates, int k, const void* x, float* y, int64_t n_tok, const float* bias, void* ws,
+                      bool grouped, cudaStream_t st);
 
 // Workspace: logits [n_tok][n_expert] fp32 | gate_up outputs [n_pairs][2I]
 // fp32 | activations [n_pairs][I] (fp32, or bf16) | (bf16) x [n_tok][hidden]
 // bf16 | the scratch of the two expert calls (shared: they run in order).
-size_t qmv_moe_block_workspace_bytes(bool bf16, int n_expert, int64_t hidden, int64_t inter, int64_t n_tok, int k)
+size_t qmv_moe_block_workspace_bytes(bool bf16, bool mx, int n_expert, int64_t hidden, int64_t inter, int64_t n_tok,
+                                     int k)
 {
     using qmv::r256b;
     const int64_t n_pairs = n_tok * k;
     const int64_t mr = hidden > 2 * inter ? hidden : 2 * inter, mc = hidden > inter ? hidden : inter;
     return r256b((size_t)n_tok * n_expert * 4) + r256b((size_t)n_pairs * 2 * inter * 4) +
            r256b((size_t)n_pairs * inter * (bf16 ? 2 : 4)) + (bf16 ? r256b((size_t)n_tok * hidden * 2) : 0) +
-           qmv_moe_workspace_bytes(bf16, mr, mc, n_pairs);
+           qmv_moe_workspace_bytes(bf16, mr, mc, n_pairs, mx);
 }
 
 // a8: both projections quantise their fp32 inputs to the paired 8-bit blocks
 // inside the expert kernels.  bf16: MXFP4 experts on the grouped GEMM, x and
-// the activations rounded to bf16.  Returns 0, or the codes of qmv_launch_moe.
-int qmv_launch_moe_block(int wtype, bool a8, bool bf16, size_t act_block_bytes, int n_expert, int k,
+// the activations rounded to bf16.  mx: MXFP4 experts on the block-scaled
+// GEMM, x and the activations quantised to MXFP8 by its gather.  Returns 0, or
+// the codes of qmv_launch_moe.
+int qmv_launch_moe_block(int wtype, bool a8, bool bf16, bool mx, size_t act_block_bytes, int n_expert, int k,
                          int64_t hidden, int64_t inter, const float* Wr, const float* br, const void* Wgu,
                          const float* bgu, const void* Wd, const float* bd, float alpha, float limit, const float* x,
                          int64_t n_tok, float* y, int32_t* ids, float* gates, void* ws, cudaStream_t st)
@@ -242,7 +245,7 @@ int qmv_launch_moe_block(int wtype, bool a8, bool bf16, size_t act_block_bytes, 
     if (cudaGetLastError() != cudaSuccess) return -6;
 
     const void* xin = bf16 ? static_cast<const void*>(xb) : static_cast<const void*>(x);
-    int rc = qmv_launch_moe_ex(wtype, a8, a8, bf16, act_block_bytes, Wgu, n_expert, 2 * inter, hidden, ids, nullptr,
+    int rc = qmv_launch_moe_ex(wtype, a8, a8, bf16, mx, act_block_bytes, Wgu, n_expert, 2 * inter, hidden, ids, nullptr,
                                k, xin, y1, n_tok, bgu, inner, false, st);
     if (rc) return rc;
     const int64_t n = n_pairs * inter;
@@ -250,6 +253,6 @@ int qmv_launch_moe_block(int wtype, bool a8, bool bf16, size_t act_block_bytes, 
     if (bf16) k_swiglu<true><<<sg, 256, 0, st>>>(y1, n_pairs, inter, alpha, limit, h);
     else k_swiglu<false><<<sg, 256, 0, st>>>(y1, n_pairs, inter, alpha, limit, h);
     if (cudaGetLastError() != cudaSuccess) return -6;
-    return qmv_launch_moe_ex(wtype, a8, a8, bf16, act_block_bytes, Wd, n_expert, hidden, inter, ids, gates, k, h, y,
+    return qmv_launch_moe_ex(wtype, a8, a8, bf16, mx, act_block_bytes, Wd, n_expert, hidden, inter, ids, gates, k, h, y,
                              n_tok, bd, inner, true, st);
 }

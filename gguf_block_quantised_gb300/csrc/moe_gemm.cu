@@ -13,7 +13,8 @@
 //   k_moe_gather  the routed activation rows, packed per expert in grouped
 //                 order (bf16 [n_valid][cols]) so one TMA tensor map covers
 //                 every expert's token tiles.
-//   k_moe_gemm_mxfp4_bf16   persistent, one CTA per SM, warp-specialised:
+//   k_moe_gemm_mxfp4   persistent, one CTA per SM, warp-specialised (bf16 form;
+//                 the MXFP8 form's differences follow the list):
 //     warp 0      TMA producer of packed token tiles X[128 tokens][128 k]
 //                 (bf16, two 64-k boxes with 128-byte swizzle)
 //     warp 1      TMEM owner and the single-thread MMA issuer
@@ -57,9 +58,8 @@ namespace mg {
 constexpr int BM = 128, BN = 128, BK = 64;   // BK: k of one 128-byte swizzled X row = one TMA box
 constexpr int KSUB = 2;                  // 64-k sub-chunks per k stage (8 MMAs per barrier round)
 constexpr int SK = 4;                    // k stages (X tiles + A tile)
-constexpr int X_BYTES = BN * BK * 2;     // 16384 per sub-chunk
+constexpr int X_BYTES = BN * BK * 2;     // 16384 per sub-chunk (bf16: 64 k; MXFP8: 128 k)
 constexpr int OFF_X = 0;
-constexpr int OFF_R = OFF_X + SK * KSUB * X_BYTES;
 constexpr int DEQ_WARPS = 16;            // warps 4..19: two groups of eight, alternate 128-k stages
 constexpr int EPI_WARP0 = 20;            // warps 20..23
 
@@ -72,15 +72,25 @@ constexpr int SLOT = 176;                // bytes per row per raw stage (>= 16 *
 // tensor copies: two 128-byte-swizzled code boxes [128 rows][128 B] and one
 // exponent box [128 rows][16 B].
 constexpr int RC_BYTES = BM * 128;       // one code box
-template <bool PLANAR>
+// MX (MXFP8 activations): the scale bytes of a token tile's rows, staged whole
+// per tile (double-buffered): rows of at most this many bytes (cols <= 4096).
+constexpr int MX_SPITCH_MAX = 128;
+constexpr int SFBUF = BN * MX_SPITCH_MAX;
+template <bool PLANAR, bool MX = false>
 struct RawCfg {
     static constexpr int BLOCKS = PLANAR ? 16 : 8;                        // blocks per row per raw stage
     static constexpr int SR = PLANAR ? 2 : 4;                             // raw stages
     static constexpr int R_BYTES = PLANAR ? 2 * RC_BYTES + BM * 16 : BM * SLOT;   // 34816 / 22528
     static constexpr int ARRIVALS = PLANAR ? 1 : 192;                     // arrivals that fill a raw stage
-    static constexpr int THREADS = PLANAR ? 768 : 896;                    // + warps 24..27 (GGUF producers)
-    static constexpr int OFF_BAR = OFF_R + SR * R_BYTES;
-    static constexpr int N_BARS = 2 * SK + 2 * SR + 4;
+    // + warps 24..27 (GGUF producers); MX: + four warps that place the token
+    // scales in every TMEM lane quarter (the last four)
+    static constexpr int THREADS = (PLANAR ? 768 : 896) + (MX ? 128 : 0);
+    static constexpr int SF_WARP0 = THREADS / 32 - 4;
+    static constexpr int XS = MX ? X_BYTES : KSUB * X_BYTES;              // X bytes per 128-k stage
+    static constexpr int OFF_R = OFF_X + SK * XS;
+    static constexpr int OFF_SF = OFF_R + SR * R_BYTES;
+    static constexpr int OFF_BAR = OFF_SF + (MX ? 2 * SFBUF : 0);
+    static constexpr int N_BARS = 2 * SK + 2 * SR + 4 + (MX ? 4 : 0);
     static constexpr int SMEM = OFF_BAR + N_BARS * 8 + 16 + 1024;   // + alignment slack
     static_assert(SMEM <= 227 * 1024, "shared memory");
 };
@@ -90,6 +100,15 @@ constexpr uint32_t A_COL = 2 * BN;
 constexpr uint32_t A_STAGE_COLS = KSUB * BK / 2;
 constexpr uint32_t TMEM_COLS = 512;
 static_assert(A_COL + SK * A_STAGE_COLS <= TMEM_COLS, "TMEM budget");
+// MX: SK E4M3 A tiles of 32 columns (128 rows x 128 k, four codes per column),
+// then per stage four columns of weight scales and four of token scales.
+// Weight row m's scale for K step j of a stage sits in lane m, column
+// SFA + m/32, byte j; token n's in lane 32q + n % 32, column SFB + n/32, byte
+// j, for every lane quarter q (the MMA reads the quarter of the output row).
+constexpr uint32_t A_STAGE_COLS_MX = 32;
+constexpr uint32_t SFA_COL = A_COL + SK * A_STAGE_COLS_MX;
+constexpr uint32_t SFB_COL = SFA_COL + SK * 4;
+static_assert(SFB_COL + SK * 4 <= TMEM_COLS, "TMEM budget (MX)");
 }  // namespace mg
 
 // 16-byte asynchronous copy global -> shared (dst, src 16-byte aligned);
@@ -218,6 +237,27 @@ __device__ __forceinline__ void mxfp4_codes_bf16(uint32_t e, const uint32_t (&w)
     }
 }
 
+// Four E2M1 codes (the low nibbles of the bytes of n) -> four E4M3 bytes of
+// the same values: E2M1 magnitudes {0, 0.5, 1, 1.5, 2, 3, 4, 6} are E4M3 0x00,
+// 0x30, 0x38, 0x3C, 0x40, 0x44, 0x48, 0x4C (a prmt table), and the sign bit
+// moves from bit 3 to bit 7.  The block's 2^(e-127) becomes the MMA's scale.
+__device__ __forceinline__ uint32_t e2m1x4_e4m3(uint32_t n)
+{
+    const uint32_t sel = __byte_perm(n | (n >> 4), 0u, 0x0020u) & 0x7777u;
+    return prmt(0x3C383000u, 0x4C484440u, sel) | ((n << 4) & 0x80808080u);
+}
+
+// The 16 code bytes of one MXFP4 block (as four words) -> its 32 codes as E4M3
+// bytes in element order, o[i] = elements 4i..4i+3.
+__device__ __forceinline__ void mxfp4_codes_e4m3(const uint32_t (&w)[4], uint32_t (&o)[8])
+{
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        o[k] = e2m1x4_e4m3(w[k] & 0x0f0f0f0fu);
+        o[4 + k] = e2m1x4_e4m3((w[k] >> 4) & 0x0f0f0f0fu);
+    }
+}
+
 // tiles[0] = number of (expert, token tile) slots; slot i = (tiles[1+2i] =
 // expert, tiles[2+2i] = token tile within the expert's group).
 __global__ void k_moe_tiles(const int* __restrict__ offsets, const int* __restrict__ active, int* __restrict__ tiles)
@@ -261,6 +301,36 @@ __global__ void k_moe_gather(const uint16_t* __restrict__ x, const int* __restri
     reinterpret_cast<uint4*>(Xs + (size_t)j * cols)[c] = reinterpret_cast<const uint4*>(x + (size_t)src * cols)[c];
 }
 
+// MXFP8 operands of the grouped pairs: row j = x row perm[j] / kdiv (fp32),
+// codes to Xc[j][cols] and E8M0 scales to Sf[j][spitch] (bytes past the
+// blocks: 127, a scale of one).  Eight threads per 32-element block.
+__global__ void k_moe_gather_mxfp8(const float* __restrict__ x, const int* __restrict__ perm,
+                                   const int* __restrict__ offsets, int n_expert, int kdiv, int cols, int spitch,
+                                   uint8_t* __restrict__ Xc, uint8_t* __restrict__ Sf)
+{
+    const int n_valid = offsets[n_expert];
+    const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t slot = g >> 3;
+    const int sub = (int)(g & 7);
+    const int j = (int)(slot / spitch), b = (int)(slot % spitch);
+    if (j >= n_valid) return;   // whole groups of eight leave together
+    const int nblk = cols / 32;
+    if (b >= nblk) {
+        if (sub == 0) Sf[(size_t)j * spitch + b] = 127;
+        return;
+    }
+    const float* xr = x + (size_t)(perm[j] / kdiv) * cols + 32 * b;
+    const float4 v = reinterpret_cast<const float4*>(xr)[sub];
+    float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+    const unsigned group = 0xffu << (threadIdx.x & 24);
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(group, m, o, 8));
+    const int E = mx_scale_exp(m);
+    const uint32_t w = mx_e4m3(v.x, E) | (mx_e4m3(v.y, E) << 8) | (mx_e4m3(v.z, E) << 16) | (mx_e4m3(v.w, E) << 24);
+    reinterpret_cast<uint32_t*>(Xc + (size_t)j * cols + 32 * b)[sub] = w;
+    if (sub == 0) Sf[(size_t)j * spitch + b] = (uint8_t)(E + 127);
+}
+
 struct MoeGemmArgs {
     const uint8_t* W3d;   // 16-byte aligned
     int64_t rows;         // rows per expert
@@ -273,18 +343,25 @@ struct MoeGemmArgs {
     const float* bias;    // [n_expert][rows] or NULL
     float* out;           // row of pair p at out + p*rows
     unsigned* status;
+    const uint8_t* sf;    // MX: E8M0 scales of the grouped pairs [sf_rows][spitch]
+    int spitch, sf_rows;
 };
 
 // PLANAR: the experts are MXFP4_R rows (tmC, tmE: code and exponent tensor
 // maps over all experts' rows); otherwise GGUF MXFP4 rows (tmC, tmE unused).
-template <bool PLANAR>
-__global__ void __launch_bounds__(mg::RawCfg<PLANAR>::THREADS, 1)
-    k_moe_gemm_mxfp4_bf16(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmC,
-                          const __grid_constant__ CUtensorMap tmE, const MoeGemmArgs a)
+// MX: MXFP8 activations on kind::mxf8f6f4.block_scale -- the codes of the
+// weights as E4M3 in TMEM with their E8M0 exponents as the weight scales, the
+// tokens' E4M3 codes in shared memory with their scales -- instead of bf16 on
+// kind::f16.
+template <bool PLANAR, bool MX>
+__global__ void __launch_bounds__(mg::RawCfg<PLANAR, MX>::THREADS, 1)
+    k_moe_gemm_mxfp4(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmC,
+                     const __grid_constant__ CUtensorMap tmE, const MoeGemmArgs a)
 {
     using namespace mg;
-    using RC = RawCfg<PLANAR>;
+    using RC = RawCfg<PLANAR, MX>;
     constexpr int SR = RC::SR, R_BYTES = RC::R_BYTES, OFF_BAR = RC::OFF_BAR, SC_BLOCKS = RC::BLOCKS;
+    constexpr int OFF_R = RC::OFF_R, XS = RC::XS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
@@ -298,7 +375,9 @@ __global__ void __launch_bounds__(mg::RawCfg<PLANAR>::THREADS, 1)
     uint64_t* re = rf + SR;
     uint64_t* accf = re + SR;
     uint64_t* acce = accf + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 2);
+    uint64_t* sff = acce + 2;   // MX: the scale rows of a token tile have landed (two buffers)
+    uint64_t* sfe = sff + 2;    // MX: the scale warps are done with a buffer
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 2 + (MX ? 4 : 0));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -309,9 +388,11 @@ __global__ void __launch_bounds__(mg::RawCfg<PLANAR>::THREADS, 1)
     const int nsc = (a.nblk + SC_BLOCKS - 1) / SC_BLOCKS;  // raw stages per row
 
     if (tid == 0) {
-        for (int i = 0; i < SK; ++i) { mbar_init(&full[i], DEQ_WARPS / 2 + 1); mbar_init(&empty[i], 1); }
+        // full: eight dequantising warps and the X copy (MX: and the four scale warps)
+        for (int i = 0; i < SK; ++i) { mbar_init(&full[i], DEQ_WARPS / 2 + (MX ? 5 : 1)); mbar_init(&empty[i], 1); }
         for (int i = 0; i < SR; ++i) { mbar_init(&rf[i], RC::ARRIVALS); mbar_init(&re[i], DEQ_WARPS); }
         for (int i = 0; i < 2; ++i) { mbar_init(&accf[i], 1); mbar_init(&acce[i], 4); }
+        if (MX) for (int i = 0; i < 2; ++i) { mbar_init(&sff[i], 1); mbar_init(&sfe[i], 4); }
         *abort_flag = 0;
         fence_barrier_init();
         prefetch_tmap(&tmX);
@@ -336,7 +417,75 @@ __global__ void __launch_bounds__(mg::RawCfg<PLANAR>::THREADS, 1)
         nt = a.tiles[2 + 2 * slot];
     };
 
-    if (warp == 0) {
+    if (MX && warp == 0) {
+        // ---- token tiles: E4M3 codes, one 128-k box per stage; and once per
+        // tile the tile's scale rows (double-buffered, refilled once the
+        // scale warps are done with the buffer)
+        if (lane == 0) {
+            int s = 0, local = 0, pend = -1;
+            uint32_t ph = 1;
+            for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x, ++local) {
+                int e, nt, rt;
+                tile_of(t, e, nt, rt);
+                const int row0 = a.offsets[e] + nt * BN;
+                const int nsf = min(BN, a.sf_rows - row0);
+                const int sb = local & 1;
+                if (!mbar_wait_backoff(&sfe[sb], (uint32_t)(((local >> 1) & 1) ^ 1), a.status, 128)) { fail(); break; }
+                mbar_arrive_expect_tx(&sff[sb], (uint32_t)(nsf * a.spitch));
+                bulk_g2s(smem + RC::OFF_SF + sb * SFBUF, a.sf + (size_t)row0 * a.spitch, (uint32_t)(nsf * a.spitch),
+                         &sff[sb]);
+                pend = local;
+                bool bad = false;
+                for (int ks = 0; ks < nks; ++ks) {
+                    if (!mbar_wait_backoff(&empty[s], ph, a.status, 128)) { bad = true; break; }
+                    mbar_arrive_expect_tx(&full[s], X_BYTES);
+                    tma_load_2d(smem + OFF_X + s * XS, &tmX, ks * 128, row0, &full[s]);
+                    if (++s == SK) { s = 0; ph ^= 1; }
+                }
+                if (bad) { fail(); break; }
+            }
+            // the last scale copy lands before the block can leave (bounded)
+            if (pend >= 0)
+                mbar_wait_bounded(&sff[pend & 1], (uint32_t)((pend >> 1) & 1), a.status, 100000000ull);
+        }
+    } else if (MX && warp >= RC::SF_WARP0) {
+        // ---- token scales: each of the four warps writes its lane quarter;
+        // lane l holds the words of tokens l, l + 32, l + 64, l + 96 (columns
+        // SFB + 0..3 of the stage)
+        const uint32_t tq = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+        int s = 0, local = 0;
+        uint32_t ph = 1;
+        bool bad = false;
+        for (int t = blockIdx.x; t < n_tiles && !__any_sync(0xffffffffu, *abort_flag); t += gridDim.x, ++local) {
+            int e, nt, rt;
+            tile_of(t, e, nt, rt);
+            const int row0 = a.offsets[e] + nt * BN;
+            const int nsf = min(BN, a.sf_rows - row0);
+            const int sb = local & 1;
+            const uint8_t* sfb = smem + RC::OFF_SF + sb * SFBUF;
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&sff[sb], (uint32_t)((local >> 1) & 1), a.status))) {
+                bad = true;
+            }
+            for (int ks = 0; ks < nks && !bad; ++ks) {
+                if (!__all_sync(0xffffffffu, mbar_wait_backoff(&empty[s], ph, a.status, 128))) { bad = true; break; }
+                uint32_t w[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int j = lane + 32 * c;
+                    w[c] = j < nsf ? *reinterpret_cast<const uint32_t*>(sfb + j * a.spitch + 4 * ks) : 0x7f7f7f7fu;
+                }
+                tmem_st4_async(tq + SFB_COL + 4 * s, w);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&full[s]);
+                if (++s == SK) { s = 0; ph ^= 1; }
+            }
+            if (bad) { fail(); break; }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sfe[sb]);   // done with this tile's scale rows
+        }
+    } else if (warp == 0) {
         // ---- packed token tiles
         if (lane == 0) {
             int s = 0;
@@ -350,8 +499,7 @@ __global__ void __launch_bounds__(mg::RawCfg<PLANAR>::THREADS, 1)
                     mbar_arrive_expect_tx(&full[s], KSUB * X_BYTES);
 #pragma unroll
                     for (int j = 0; j < KSUB; ++j)
-                        tma_load_2d(smem + OFF_X + (s * KSUB + j) * X_BYTES, &tmX, (ks * KSUB + j) * BK, row0,
-                                    &full[s]);
+                        tma_load_2d(smem + OFF_X + s * XS + j * X_BYTES, &tmX, (ks * KSUB + j) * BK, row0, &full[s]);
                     if (++s == SK) { s = 0; ph ^= 1; }
                 }
             }
@@ -376,7 +524,7 @@ __global__ void __launch_bounds__(mg::RawCfg<PLANAR>::THREADS, 1)
                 }
             }
         }
-    } else if (!PLANAR && (warp == 2 || warp == 3 || warp >= EPI_WARP0 + 4)) {   // warps 2, 3, 24..27
+    } else if (!PLANAR && (warp == 2 || warp == 3 || (warp >= EPI_WARP0 + 4 && warp < EPI_WARP0 + 8))) {   // 2, 3, 24..27
         // ---- raw weights: for each row of the tile, the 16-byte-aligned span
         // holding its next (up to) 8 blocks, as 16-byte cp.async pieces spread
         // over the 192 threads of warps 2, 3 and 16..19 (consecutive threads take
@@ -412,6 +560,11 @@ __global__ void __launch_bounds__(mg::RawCfg<PLANAR>::THREADS, 1)
         // ---- MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16(BM, BN);
+            // MX: E4M3 x E4M3, E8M0 scales, M = 128, N = 128; K step j reads byte
+            // j of the scale words
+            auto idesc_mx = [](uint32_t j) {
+                return (j << 4) | ((uint32_t)(BN >> 3) << 17) | (1u << 23) | ((uint32_t)(BM >> 7) << 27) | (j << 29);
+            };
             int s = 0;
             uint32_t pf = 0;
             int local = 0;
@@ -428,13 +581,22 @@ __global__ void __launch_bounds__(mg::RawCfg<PLANAR>::THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t at = tmem + A_COL + s * A_STAGE_COLS;
+                    if constexpr (MX) {
+                        const uint32_t at = tmem + A_COL + s * A_STAGE_COLS_MX;
+                        const uint64_t bdesc = smem_desc_sw128(smem + OFF_X + s * XS);
 #pragma unroll
-                    for (int j = 0; j < KSUB; ++j) {
-                        const uint64_t bdesc = smem_desc_sw128(smem + OFF_X + (s * KSUB + j) * X_BYTES);
+                        for (int j = 0; j < 4; ++j)   // A: 8 TMEM columns, B: 32 bytes per K = 32 step
+                            mma_mx_ts(d, at + 8 * j, bdesc + 2 * j, idesc_mx((uint32_t)j), tmem + SFA_COL + 4 * s,
+                                      tmem + SFB_COL + 4 * s, (ks | j) != 0);
+                    } else {
+                        const uint32_t at = tmem + A_COL + s * A_STAGE_COLS;
 #pragma unroll
-                        for (int k4 = 0; k4 < BK / 16; ++k4)   // A: 8 TMEM columns, B: 32 bytes per K = 16 step
-                            mma_f16_ts(d, at + 32 * j + 8 * k4, bdesc + 2 * k4, idesc, (ks | j | k4) != 0);
+                        for (int j = 0; j < KSUB; ++j) {
+                            const uint64_t bdesc = smem_desc_sw128(smem + OFF_X + s * XS + j * X_BYTES);
+#pragma unroll
+                            for (int k4 = 0; k4 < BK / 16; ++k4)   // A: 8 TMEM columns, B: 32 bytes per K = 16 step
+                                mma_f16_ts(d, at + 32 * j + 8 * k4, bdesc + 2 * k4, idesc, (ks | j | k4) != 0);
+                        }
                     }
                     mma_commit(&empty[s]);
                     if (++s == SK) { s = 0; pf ^= 1; }
@@ -451,7 +613,8 @@ __global__ void __launch_bounds__(mg::RawCfg<PLANAR>::THREADS, 1)
         // lane quarter) and block 2c + t / 128 of each 64-k chunk c, i.e. A
         // tile columns 16 * (t / 128) .. +15
         const int t0 = (tid - 128) & 255, grp = (tid - 128) >> 8, r = t0 & 127, half = t0 >> 7;
-        const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + A_COL + 16 * half;
+        const uint32_t tq = tmem + ((uint32_t)(32 * (warp & 3)) << 16);   // this warp's lane quarter
+        const uint32_t ta = tq + A_COL + 16 * half;
         int sr = 0;
         uint32_t prf = 0;
         uint32_t gk = 0;   // global index of the next 128-k stage
@@ -476,25 +639,62 @@ __global__ void __launch_bounds__(mg::RawCfg<PLANAR>::THREADS, 1)
                     const uint32_t pe = ((gk / SK) & 1) ^ 1;
                     if (!__all_sync(0xffffffffu, mbar_wait_bounded(&empty[s], pe, a.status))) { bad = true; break; }
                     tc_fence_after();
+                    if constexpr (MX) {
+                        // E4M3 codes: block 2j + half of the stage at columns 8 (2j + half)
 #pragma unroll
-                    for (int j = 0; j < KSUB; ++j) {
-                        const int blk = 2 * (KSUB * cs + j) + half;
-                        uint32_t o[16];
-                        if (row < a.rows && blk < nb) {
-                            if constexpr (PLANAR) {
-                                // code box blk / 8, 16-byte chunk (blk % 8) swizzled by the row
-                                const uint4 u = *reinterpret_cast<const uint4*>(
-                                    rbuf + (blk >> 3) * RC_BYTES + r * 128 + (((blk & 7) ^ (r & 7)) << 4));
-                                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-                                mxfp4_codes_bf16(rbuf[2 * RC_BYTES + r * 16 + blk], w, o);
+                        for (int j = 0; j < KSUB; ++j) {
+                            const int blk = 2 * (KSUB * cs + j) + half;
+                            uint32_t o[8];
+                            if (row < a.rows && blk < nb) {
+                                uint32_t w[4];
+                                if constexpr (PLANAR) {
+                                    const uint4 u = *reinterpret_cast<const uint4*>(
+                                        rbuf + (blk >> 3) * RC_BYTES + r * 128 + (((blk & 7) ^ (r & 7)) << 4));
+                                    w[0] = u.x; w[1] = u.y; w[2] = u.z; w[3] = u.w;
+                                } else {
+                                    load_words<4>(slot + off + 17 * blk + 1, w);
+                                }
+                                mxfp4_codes_e4m3(w, o);
                             } else {
-                                mxfp4_block_bf16(slot, off + 17 * blk, o);
-                            }
-                        } else {
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) o[i] = 0u;
+                                for (int i = 0; i < 8; ++i) o[i] = 0u;
+                            }
+                            tmem_st8_async(tq + A_COL + s * A_STAGE_COLS_MX + 16 * j + 8 * half, o);
                         }
-                        tmem_st16_async(ta + s * A_STAGE_COLS + 32 * j, o);
+                        if (half == 0) {
+                            // the row's four block exponents: its scale word (column m / 32)
+                            uint32_t sw = 0;
+#pragma unroll
+                            for (int b = 0; b < 4; ++b) {
+                                const int blk = 4 * cs + b;
+                                uint32_t ev = 127u;
+                                if (row < a.rows && blk < nb)
+                                    ev = PLANAR ? rbuf[2 * RC_BYTES + r * 16 + blk] : slot[off + 17 * blk];
+                                sw |= ev << (8 * b);
+                            }
+                            tmem_st1_async(tq + SFA_COL + 4 * s + (uint32_t)(warp & 3), sw);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < KSUB; ++j) {
+                            const int blk = 2 * (KSUB * cs + j) + half;
+                            uint32_t o[16];
+                            if (row < a.rows && blk < nb) {
+                                if constexpr (PLANAR) {
+                                    // code box blk / 8, 16-byte chunk (blk % 8) swizzled by the row
+                                    const uint4 u = *reinterpret_cast<const uint4*>(
+                                        rbuf + (blk >> 3) * RC_BYTES + r * 128 + (((blk & 7) ^ (r & 7)) << 4));
+                                    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+                                    mxfp4_codes_bf16(rbuf[2 * RC_BYTES + r * 16 + blk], w, o);
+                                } else {
+                                    mxfp4_block_bf16(slot, off + 17 * blk, o);
+                                }
+                            } else {
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) o[i] = 0u;
+                            }
+                            tmem_st16_async(ta + s * A_STAGE_COLS + 32 * j, o);
+                        }
                     }
                     tmem_wait_st();
                     tc_fence_before();
@@ -557,33 +757,62 @@ inline size_t tiles_bytes(int64_t n_pairs)
 
 }  // namespace qmv
 
-// Bytes of workspace beyond the grouping that the grouped GEMM needs: the slot
-// list and the packed bf16 activations.
-size_t qmv_moe_gemm_extra_bytes(int64_t cols, int64_t n_pairs)
+namespace qmv {
+inline int mx_spitch(int64_t cols)   // scale bytes per token row: 4 per 128-k stage, 16-byte multiple
 {
-    return qmv::tiles_bytes(n_pairs) + (size_t)n_pairs * (size_t)cols * 2;
+    const int64_t nks = (cols / 32 + 3) / 4;
+    return (int)((4 * nks + 15) & ~int64_t(15));
+}
+inline size_t r256g(size_t v) { return (v + 255) & ~size_t(255); }
+}  // namespace qmv
+
+// Bytes of workspace beyond the grouping that the grouped GEMM needs: the slot
+// list and the packed activations (bf16, or MXFP8 codes and scales).
+size_t qmv_moe_gemm_extra_bytes(int64_t cols, int64_t n_pairs, bool mx)
+{
+    using namespace qmv;
+    if (mx)
+        return tiles_bytes(n_pairs) + r256g((size_t)n_pairs * (size_t)cols) +
+               r256g((size_t)n_pairs * (size_t)mx_spitch(cols));
+    return tiles_bytes(n_pairs) + (size_t)n_pairs * (size_t)cols * 2;
 }
 
 // Enqueues the slot list, the gather and the grouped GEMM.  ws points at the
 // GEMM's part of the workspace (qmv_moe_gemm_extra_bytes bytes, 256-aligned).
-// planar: W3d holds MXFP4_R rows.  Returns 0, -6 (launch failure) or -8 (tensor
-// map).
-int qmv_launch_moe_gemm_mxfp4(const void* W3d, bool planar, int n_expert, int64_t rows, int64_t cols, const void* x,
-                              int kdiv, int64_t n_pairs, const int* offsets, const int* active, const int* perm,
-                              void* ws, float* out, const float* bias, cudaStream_t st)
+// planar: W3d holds MXFP4_R rows.  mx: x is fp32, quantised to MXFP8 by the
+// gather, and the GEMM runs on kind::mxf8f6f4 (cols <= 4096); otherwise x is
+// bf16.  Returns 0, -2 (shape beyond the plan), -6 (launch failure) or -8
+// (tensor map).
+int qmv_launch_moe_gemm_mxfp4(const void* W3d, bool planar, bool mx, int n_expert, int64_t rows, int64_t cols,
+                              const void* x, int kdiv, int64_t n_pairs, const int* offsets, const int* active,
+                              const int* perm, void* ws, float* out, const float* bias, cudaStream_t st)
 {
     using namespace qmv;
+    const int spitch = mx_spitch(cols);
+    if (mx && spitch > mg::MX_SPITCH_MAX) return -2;
     int* tiles = static_cast<int*>(ws);
-    uint16_t* Xs = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + tiles_bytes(n_pairs));
+    uint8_t* act = static_cast<uint8_t*>(ws) + tiles_bytes(n_pairs);
+    uint8_t* sf = act + r256g((size_t)n_pairs * (size_t)cols);
     k_moe_tiles<<<1, 32, 0, st>>>(offsets, active, tiles);
-    const int64_t per = n_pairs * (cols / 8);
-    k_moe_gather<<<(unsigned)((per + 255) / 256), 256, 0, st>>>(static_cast<const uint16_t*>(x), perm, offsets,
-                                                                  n_expert, kdiv, (int)cols, Xs);
-    if (cudaGetLastError() != cudaSuccess) return -6;
     CUtensorMap tmX, tmC, tmE;
-    if (!make_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Xs, (uint64_t)cols, (uint64_t)n_pairs,
-                      (uint64_t)cols * 2, mg::BK, mg::BN, CU_TENSOR_MAP_SWIZZLE_128B))
-        return -8;
+    if (mx) {
+        const int64_t threads = n_pairs * spitch * 8;
+        k_moe_gather_mxfp8<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(
+            static_cast<const float*>(x), perm, offsets, n_expert, kdiv, (int)cols, spitch, act, sf);
+        if (cudaGetLastError() != cudaSuccess) return -6;
+        if (!make_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_UINT8, act, (uint64_t)cols, (uint64_t)n_pairs,
+                          (uint64_t)cols, 128, mg::BN, CU_TENSOR_MAP_SWIZZLE_128B))
+            return -8;
+    } else {
+        uint16_t* Xs = reinterpret_cast<uint16_t*>(act);
+        const int64_t per = n_pairs * (cols / 8);
+        k_moe_gather<<<(unsigned)((per + 255) / 256), 256, 0, st>>>(static_cast<const uint16_t*>(x), perm, offsets,
+                                                                      n_expert, kdiv, (int)cols, Xs);
+        if (cudaGetLastError() != cudaSuccess) return -6;
+        if (!make_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Xs, (uint64_t)cols, (uint64_t)n_pairs,
+                          (uint64_t)cols * 2, mg::BK, mg::BN, CU_TENSOR_MAP_SWIZZLE_128B))
+            return -8;
+    }
     MoeGemmArgs a;
     a.W3d = static_cast<const uint8_t*>(W3d);
     a.rows = rows;
@@ -596,6 +825,9 @@ int qmv_launch_moe_gemm_mxfp4(const void* W3d, bool planar, int n_expert, int64_
     a.bias = bias;
     a.out = out;
     a.status = status_word();
+    a.sf = sf;
+    a.spitch = spitch;
+    a.sf_rows = (int)n_pairs;
     if (planar) {
         // codes: [all rows][16 * nblk bytes], exponents: [all rows][nblk bytes] at +16*nblk; row pitch rb
         const uint64_t all_rows = (uint64_t)n_expert * (uint64_t)rows;
@@ -604,21 +836,19 @@ int qmv_launch_moe_gemm_mxfp4(const void* W3d, bool planar, int n_expert, int64_
             !make_tmap_2d(&tmE, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<const uint8_t*>(W3d) + (size_t)a.nblk * 16,
                           (uint64_t)a.nblk, all_rows, (uint64_t)a.rb, 16, mg::BM, CU_TENSOR_MAP_SWIZZLE_NONE))
             return -8;
-        auto* k = &k_moe_gemm_mxfp4_bf16<true>;
-        prepare_kernel(k, mg::RawCfg<true>::THREADS, mg::RawCfg<true>::SMEM);
-        return launch_ex(k, dim3(num_sms()), dim3(mg::RawCfg<true>::THREADS), mg::RawCfg<true>::SMEM, st, false, tmX,
-                         tmC, tmE, a) == cudaSuccess
-                   ? 0
-                   : -6;
+    } else {
+        tmC = tmX;   // unused by the GGUF-layout kernel
+        tmE = tmX;
     }
-    tmC = tmX;   // unused by the GGUF-layout kernel
-    tmE = tmX;
-    auto* k = &k_moe_gemm_mxfp4_bf16<false>;
-    prepare_kernel(k, mg::RawCfg<false>::THREADS, mg::RawCfg<false>::SMEM);
-    return launch_ex(k, dim3(num_sms()), dim3(mg::RawCfg<false>::THREADS), mg::RawCfg<false>::SMEM, st, false, tmX,
-                     tmC, tmE, a) == cudaSuccess
-               ? 0
-               : -6;
+    auto launch = [&](auto* k, int threads, int smem) {
+        prepare_kernel(k, threads, smem);
+        return launch_ex(k, dim3(num_sms()), dim3(threads), smem, st, false, tmX, tmC, tmE, a) == cudaSuccess ? 0 : -6;
+    };
+    if (planar)
+        return mx ? launch(&k_moe_gemm_mxfp4<true, true>, mg::RawCfg<true, true>::THREADS, mg::RawCfg<true, true>::SMEM)
+                  : launch(&k_moe_gemm_mxfp4<true, false>, mg::RawCfg<true>::THREADS, mg::RawCfg<true>::SMEM);
+    return mx ? launch(&k_moe_gemm_mxfp4<false, true>, mg::RawCfg<false, true>::THREADS, mg::RawCfg<false, true>::SMEM)
+              : launch(&k_moe_gemm_mxfp4<false, false>, mg::RawCfg<false>::THREADS, mg::RawCfg<false>::SMEM);
 }
 
 // ---- repack: GGUF MXFP4 rows -> MXFP4_R rows --------------------------------------

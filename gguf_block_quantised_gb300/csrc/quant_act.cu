@@ -12,6 +12,7 @@
 // One warp per block.  This kernel moves ~5 bytes per element in total and is
 // a small fraction of any multiply it feeds.
 #include "common.cuh"
+#include "runtime.cuh"
 
 namespace qmv {
 
@@ -70,14 +71,45 @@ __global__ void k_quant_q8_k(const float* __restrict__ x, uint8_t* __restrict__ 
     if (lane == 0) *reinterpret_cast<float*>(o) = d;
 }
 
+// MXFP8: eight threads per 32-element block, four elements each; blocks are
+// 33 bytes (E8M0 scale | 32 E4M3 codes).
+__global__ void k_quant_mxfp8(const float* __restrict__ x, uint8_t* __restrict__ out, int64_t nblk)
+{
+    const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t b = g >> 3;
+    const int sub = (int)(g & 7);
+    pdl_trigger();
+    pdl_wait();
+    if (b >= nblk) return;   // whole groups of eight leave together
+    const float4 v = reinterpret_cast<const float4*>(x + b * 32)[sub];
+    float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+#pragma unroll
+    const unsigned group = 0xffu << (threadIdx.x & 24);   // this block's eight lanes
+    for (int o = 4; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(group, m, o, 8));
+    const int E = mx_scale_exp(m);
+    uint8_t* o = out + b * 33;
+    o[1 + 4 * sub] = (uint8_t)mx_e4m3(v.x, E);
+    o[2 + 4 * sub] = (uint8_t)mx_e4m3(v.y, E);
+    o[3 + 4 * sub] = (uint8_t)mx_e4m3(v.z, E);
+    o[4 + 4 * sub] = (uint8_t)mx_e4m3(v.w, E);
+    if (sub == 0) o[0] = (uint8_t)(E + 127);
+}
+
 }  // namespace qmv
 
 int qmv_launch_quantize(int atype, const float* x, void* xq, int64_t n, bool pdl, cudaStream_t st)
 {
     using namespace qmv;
-    const int bs = atype == QMV_Q8_0 ? 32 : 256;
+    const int bs = atype == QMV_Q8_K ? 256 : 32;
     const int64_t nblk = n / bs;
     if (nblk == 0) return 0;
+    if (atype == QMV_MXFP8) {
+        const int64_t threads = nblk * 8;
+        return launch_ex(k_quant_mxfp8, dim3((unsigned)((threads + 255) / 256)), dim3(256), 0, st, pdl, x,
+                         static_cast<uint8_t*>(xq), nblk) == cudaSuccess
+                   ? 0
+                   : -1;
+    }
     const int warps = 8;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)((nblk + warps - 1) / warps));

@@ -112,6 +112,22 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
         : "memory");
 }
 
+// D[tmem] (+)= (A[tmem] * 2^(sfa-127)) * (B[smem] * 2^(sfb-127))^T with E4M3 A
+// and B, K = 32, one E8M0 scale per row and per 32 k (kind::mxf8f6f4 with
+// block scaling), issued by one thread.  A (M x 32) sits in TMEM: row m in
+// lane m, elements 4j..4j+3 in column a_tmem + j.  The scale words are at
+// sfa_tmem / sfb_tmem; the instruction descriptor's scale ids pick the byte.
+__device__ __forceinline__ void mma_mx_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t sfa_tmem, uint32_t sfb_tmem, bool accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], [%1], %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate ? 1u : 0u)
+        : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar)
@@ -183,6 +199,11 @@ __device__ __forceinline__ void tmem_st8_async(uint32_t taddr, const uint32_t (&
     asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
                  "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
                  : "memory");
+}
+// One 32-bit TMEM column of this thread's lane <- v (complete after tmem_wait_st()).
+__device__ __forceinline__ void tmem_st1_async(uint32_t taddr, uint32_t v)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 

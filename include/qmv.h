@@ -79,7 +79,9 @@ typedef enum {
                                                                          w = d*(s-32)*(q-4)     */
     QMV_Q5_K = 16,  /* 256 w, 176 B: Q4_K's d, dmin, 12 B sc/m | 32 B fifth bits | 128 B nibbles;
                                                                          w = d*sc*q - dmin*m    */
-    QMV_F16 = 17    /* plain IEEE half (weights) */
+    QMV_F16 = 17,   /* plain IEEE half (weights) */
+    QMV_MXFP8 = 18  /* activations only, 32 w, 33 B: E8M0 e | E4M3[32];  x = 2^(e-127)*E4M3(q)
+                       (OCP Microscaling v1.0 MXFP8; see qmv_quantize_act) */
     /* QMV_F32 and QMV_BF16 are also accepted as plain weight types. */
 } qmv_type;
 
@@ -138,6 +140,11 @@ size_t qmv_row_bytes(int type, int64_t cols);
  * clamped to +-127 (q = 0 when amax = 0; when d is below 2^-128 and 1/d
  * overflows, q = round-half-away(x / d)); fp32 arithmetic, one rounding per
  * operation.  Q8_0 stores d rounded to fp16, Q8_K the fp32 d.
+ *   fmt QMV_MXFP8 (x 16-byte aligned, n a multiple of 32, finite values):
+ * the OCP Microscaling v1.0 conversion -- E = floor(log2 amax) - 8 (at least
+ * -127; -127 for a block of zeros), stored as the E8M0 byte E + 127, and
+ * q = E4M3(x / 2^E) rounded to nearest even, magnitudes clamped to 448.  The
+ * MXFP8 mixture-of-experts path quantises its activations the same way.
  * ------------------------------------------------------------------------- */
 int qmv_quantize_act(int fmt, const float* x, void* xq, int64_t n, void* stream);
 
@@ -286,9 +293,14 @@ int qmv_matmul(int fmt, const void* W, int64_t rows, int64_t cols,
  *           | QMV_FLAG_QUANTIZE_X (fp32 rows quantised inside the kernel);
  *           or, for MXFP4 experts only, BF16 (bf16 rows, 16-byte aligned):
  *           the grouped tensor-core GEMM, whose weights 2^(e-127)*E2M1 are
- *           exact in bf16 (fp32 accumulation; rows < 2^30).  The experts may
- *           also be given as QMV_MXFP4_R (qmv_repack output, same results),
- *           which the GEMM moves with TMA tensor copies.
+ *           exact in bf16 (fp32 accumulation; rows < 2^30); or MXFP8 (x fp32
+ *           rows, 16-byte aligned, cols <= 4096): the activations are
+ *           quantised to MXFP8 as qmv_quantize_act does, and the grouped GEMM
+ *           runs on the block-scaled MMA (kind::mxf8f6f4): each MXFP4 code as
+ *           E4M3 with its block's E8M0 exponent as the scale, against the
+ *           tokens' E4M3 codes and scales, products exact, fp32 accumulation.
+ *           The experts may also be given as QMV_MXFP4_R (qmv_repack output,
+ *           same results), which the GEMM moves with TMA tensor copies.
  *   n_expert in 1..1024, k in 1..64, n_tok*k <= 2^24.
  *   Results per (token, slot) are, for F32 and 8-bit activations, those of
  *   qmv_matvec on that expert's matrix (same arithmetic and reduction
@@ -365,8 +377,9 @@ int qmv_moe_matvec_noalloc(int fmt, const void* W3d, int n_expert, int64_t rows,
  *            8-bit type (x and h are quantised to it inside the expert
  *            kernels, as QMV_FLAG_QUANTIZE_X does), or, for MXFP4 / MXFP4_R
  *            experts, BF16 (x and h rounded to bf16, the grouped tensor-core
- *            GEMM).  No flags.  Each projection gives the results of
- *            qmv_moe_matvec with the same format.
+ *            GEMM) or MXFP8 (x and h quantised to MXFP8, the block-scaled
+ *            GEMM; hidden, inter <= 4096).  No flags.  Each projection gives
+ *            the results of qmv_moe_matvec with the same format.
  *   Wr     : fp32 [n_expert][hidden]; br fp32 [n_expert] or NULL.
  *   x      : fp32 [n_tok][hidden], 16-byte aligned.  y : fp32 [n_tok][hidden].
  *   ids    : int32 [n_tok][k] out.   gates : fp32 [n_tok][k] out.

@@ -8,7 +8,7 @@ TOL = 1e-4
 
 # The library's type numbers (include/qmv.h) and the oracle's own table
 # (oracle/oracle.h) agree on the original formats; the later ones differ.
-_ORC = {11: 10, 12: 11, 13: 15, 14: 13, 15: 14, 16: 12, 17: 16}
+_ORC = {11: 10, 12: 11, 13: 15, 14: 13, 15: 14, 16: 12, 17: 16, 18: 17}
 
 
 def orc_t(t):
