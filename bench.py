@@ -560,7 +560,7 @@ def prefill_leg(q, torch, stream, tflops_peak):
                                 "M=128 x N=128, S and Mn drained per super-block)"}}
 
 
-def moe_leg(q, torch, stream, hbm):
+def moe_leg(q, torch, stream, hbm, tflops_peak=None):
     """gpt-oss-20B-shaped MoE layer: 32 MXFP4 experts, gate_up 5760x2880 (up
     form, x shared by the 4 slots) then down 2880x2880 (per-slot inputs,
     gate-weighted), fp32 biases, top-4 of N(0,1) router logits.  Two paths:
@@ -581,7 +581,14 @@ def moe_leg(q, torch, stream, hbm):
     br = torch.from_numpy(synth.bias(1, E, seed=5, tensor_id=4001)[0]).cuda()
     paths = {"w4a8": (q.FMT(MXFP4, Q8_0) | q.FLAG_QUANTIZE_X, torch.float32, Wgu, Wd),
              "bf16_gemm": (q.FMT(MXFP4, BF16), torch.bfloat16, Wgu, Wd),
-             "bf16_gemm_repacked": (q.FMT(MXFP4_R, BF16), torch.bfloat16, Wgu_r, Wd_r)}
+             "bf16_gemm_repacked": (q.FMT(MXFP4_R, BF16), torch.bfloat16, Wgu_r, Wd_r),
+             "mx_gemm": (q.FMT(MXFP4, q.MXFP8), torch.float32, Wgu, Wd),
+             "mx_gemm_repacked": (q.FMT(MXFP4_R, q.MXFP8), torch.float32, Wgu_r, Wd_r)}
+    # the tensor peak of each path's MMA: bf16 (kind::f16) measured; fp8 (the
+    # block-scaled kind) as twice the bf16 figure, the nominal dense ratio
+    peak_of = {"bf16_gemm": tflops_peak, "bf16_gemm_repacked": tflops_peak,
+               "mx_gemm": 2 * tflops_peak if tflops_peak else None,
+               "mx_gemm_repacked": 2 * tflops_peak if tflops_peak else None}
     out = {}
     ws = None
     for name, (fmt, xdt, Wgu_p, Wd_p) in paths.items():
@@ -614,6 +621,8 @@ def moe_leg(q, torch, stream, hbm):
                                   "weight_gbs": wbytes / (ms / 1e3) / 1e9,
                                   "frac_of_hbm": wbytes / (ms / 1e3) / 1e9 / hbm,
                                   "tflops": flop / (ms / 1e3) / 1e12}
+            if peak_of.get(name):
+                res[f"tok{n_tok}"]["frac_of_tensor_peak"] = flop / (ms / 1e3) / 1e12 / peak_of[name]
             res[f"block_tok{n_tok}"] = block_time(q, torch, stream, fmt, Wgu_p, Wd_p, bgu, bd, Wr, br, n_tok, hbm)
         out[name] = res
     q.qmv_set_workspace(None, 0)
@@ -626,7 +635,12 @@ def moe_leg(q, torch, stream, hbm):
                       "bf16_gemm": "k_moe_group + k_moe_tiles + k_moe_gather + k_moe_gemm_mxfp4_bf16 (tcgen05) "
                                    "+ k_moe_combine",
                       "bf16_gemm_repacked": "the same on MXFP4_R experts (qmv_repack once; TMA tensor copies of "
-                                            "the codes and exponents)"}}
+                                            "the codes and exponents)",
+                      "mx_gemm": "k_moe_group + k_moe_tiles + k_moe_gather_mxfp8 (fp32 -> MXFP8) + "
+                                 "k_moe_gemm_mxfp4<MX> (tcgen05 kind::mxf8f6f4.block_scale) + k_moe_combine",
+                      "mx_gemm_repacked": "the same on MXFP4_R experts"},
+            "tensor_peaks_tflops": {"bf16": tflops_peak, "fp8": 2 * tflops_peak if tflops_peak else None,
+                                    "fp8_kind": "twice the measured bf16 burst (nominal dense fp8/bf16 ratio)"}}
 
 
 def block_time(q, torch, stream, fmt, Wgu, Wd, bgu, bd, Wr, br, n_tok, hbm, E=32, k=4, hidden=2880, inter=2880):
@@ -662,8 +676,9 @@ def run_probe(spec):
       step[:n_vec]                   one fused decode step of the Qwen2.5-0.5B shape (97 matvecs)
       block:n_tok[:atype]            qmv_moe_block on the gpt-oss MoE shapes (atype 3 = Q8_0, 8 = fp32, 9 = bf16)
       moe:n_tok[:atype[:repacked]]   one gpt-oss-shaped MoE layer (gate_up + down); atype 3 = Q8_0
-                                     quantised in-kernel (default), 9 = bf16 (grouped tensor-core GEMM);
-                                     repacked 1: experts repacked to MXFP4_R first (bf16 only)
+                                     quantised in-kernel (default), 9 = bf16 (grouped tensor-core GEMM),
+                                     18 = MXFP8 (block-scaled tensor-core GEMM); repacked 1: experts
+                                     repacked to MXFP4_R first (bf16 and MXFP8 only)
     Each runs its call five times and prints the event-timed mean of the last three."""
     import torch
     import gguf_block_quantised_gb300 as q
@@ -744,13 +759,13 @@ def run_probe(spec):
         h = torch.randn(n_tok, k, 2880, device="cuda").to(xdt)
         y1 = torch.empty(n_tok, k, 5760, device="cuda")
         y2 = torch.empty(n_tok, 2880, device="cuda")
-        fmt = q.FMT(MXFP4, BF16) if at == BF16 else q.FMT(MXFP4, Q8_0) | q.FLAG_QUANTIZE_X
-        if repacked and at == BF16:
+        fmt = q.FMT(MXFP4, at) if at in (BF16, q.MXFP8) else q.FMT(MXFP4, Q8_0) | q.FLAG_QUANTIZE_X
+        if repacked and at in (BF16, q.MXFP8):
             Wgu_r = torch.empty(E * 5760 * q.qmv_row_bytes(MXFP4_R, 2880), dtype=torch.uint8, device="cuda")
             Wd_r = torch.empty(E * 2880 * q.qmv_row_bytes(MXFP4_R, 2880), dtype=torch.uint8, device="cuda")
             q.qmv_repack(MXFP4, Wgu, E * 5760, 2880, Wgu_r)
             q.qmv_repack(MXFP4, Wd, E * 2880, 2880, Wd_r)
-            Wgu, Wd, fmt = Wgu_r, Wd_r, q.FMT(MXFP4_R, BF16)
+            Wgu, Wd, fmt = Wgu_r, Wd_r, q.FMT(MXFP4_R, at)
         ws = torch.empty(q.qmv_workspace_size(q.OP_MOE, fmt, 5760, 2880, n_tok * k), dtype=torch.uint8, device="cuda")
         q.qmv_set_workspace(ws, ws.numel())
 
@@ -1195,7 +1210,7 @@ def main():
     kquant = None if args.no_extra else kquant_decode_leg(q, torch, stream, hbm)
     formats = None if args.no_extra else formats_leg(q, torch, stream, hbm)
     prefill = None if args.no_extra else prefill_leg(q, torch, stream, tflops_peak)
-    moe = None if args.no_extra else moe_leg(q, torch, stream, hbm)
+    moe = None if args.no_extra else moe_leg(q, torch, stream, hbm, tflops_peak)
     wquant = None if args.no_extra else wquant_leg(q, torch, stream, hbm)
     value = ws * STEP_WEIGHT_BYTES / (ms1 / 1e3) / 1e9
     if rank != 0:

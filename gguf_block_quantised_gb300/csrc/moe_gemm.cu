@@ -100,7 +100,8 @@ constexpr uint32_t A_COL = 2 * BN;
 constexpr uint32_t A_STAGE_COLS = KSUB * BK / 2;
 constexpr uint32_t TMEM_COLS = 512;
 static_assert(A_COL + SK * A_STAGE_COLS <= TMEM_COLS, "TMEM budget");
-// MX: SK E4M3 A tiles of 32 columns (128 rows x 128 k, four codes per column),
+// MX: SK E2M1 A tiles of 32 columns (128 rows x 128 k, four byte-container
+// codes per column),
 // then per stage four columns of weight scales and four of token scales.
 // Weight row m's scale for K step j of a stage sits in lane m, column
 // SFA + m/32, byte j; token n's in lane 32q + n % 32, column SFB + n/32, byte
@@ -237,24 +238,17 @@ __device__ __forceinline__ void mxfp4_codes_bf16(uint32_t e, const uint32_t (&w)
     }
 }
 
-// Four E2M1 codes (the low nibbles of the bytes of n) -> four E4M3 bytes of
-// the same values: E2M1 magnitudes {0, 0.5, 1, 1.5, 2, 3, 4, 6} are E4M3 0x00,
-// 0x30, 0x38, 0x3C, 0x40, 0x44, 0x48, 0x4C (a prmt table), and the sign bit
-// moves from bit 3 to bit 7.  The block's 2^(e-127) becomes the MMA's scale.
-__device__ __forceinline__ uint32_t e2m1x4_e4m3(uint32_t n)
-{
-    const uint32_t sel = __byte_perm(n | (n >> 4), 0u, 0x0020u) & 0x7777u;
-    return prmt(0x3C383000u, 0x4C484440u, sel) | ((n << 4) & 0x80808080u);
-}
-
-// The 16 code bytes of one MXFP4 block (as four words) -> its 32 codes as E4M3
-// bytes in element order, o[i] = elements 4i..4i+3.
-__device__ __forceinline__ void mxfp4_codes_e4m3(const uint32_t (&w)[4], uint32_t (&o)[8])
+// The 16 code bytes of one MXFP4 block (as four words) -> its 32 E2M1 codes in
+// the MMA's byte containers (the code in bits 5..2 of its byte), in element
+// order: o[i] = elements 4i..4i+3.  Byte j of word k holds element 4k + j in
+// its low nibble and element 16 + 4k + j in its high one.  The block's
+// 2^(e-127) becomes the MMA's weight scale.
+__device__ __forceinline__ void mxfp4_codes_e2m1x8(const uint32_t (&w)[4], uint32_t (&o)[8])
 {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        o[k] = e2m1x4_e4m3(w[k] & 0x0f0f0f0fu);
-        o[4 + k] = e2m1x4_e4m3((w[k] >> 4) & 0x0f0f0f0fu);
+        o[k] = (w[k] & 0x0f0f0f0fu) << 2;
+        o[4 + k] = (w[k] >> 2) & 0x3c3c3c3cu;
     }
 }
 
@@ -349,10 +343,10 @@ struct MoeGemmArgs {
 
 // PLANAR: the experts are MXFP4_R rows (tmC, tmE: code and exponent tensor
 // maps over all experts' rows); otherwise GGUF MXFP4 rows (tmC, tmE unused).
-// MX: MXFP8 activations on kind::mxf8f6f4.block_scale -- the codes of the
-// weights as E4M3 in TMEM with their E8M0 exponents as the weight scales, the
-// tokens' E4M3 codes in shared memory with their scales -- instead of bf16 on
-// kind::f16.
+// MX: MXFP8 activations on kind::mxf8f6f4.block_scale -- the weights' E2M1
+// codes in TMEM byte containers with their E8M0 exponents as the weight
+// scales, the tokens' E4M3 codes in shared memory with their scales --
+// instead of bf16 on kind::f16.
 template <bool PLANAR, bool MX>
 __global__ void __launch_bounds__(mg::RawCfg<PLANAR, MX>::THREADS, 1)
     k_moe_gemm_mxfp4(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmC,
@@ -560,10 +554,11 @@ __global__ void __launch_bounds__(mg::RawCfg<PLANAR, MX>::THREADS, 1)
         // ---- MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16(BM, BN);
-            // MX: E4M3 x E4M3, E8M0 scales, M = 128, N = 128; K step j reads byte
-            // j of the scale words
+            // MX: E2M1 A x E4M3 B, E8M0 scales, M = 128, N = 128; K step j reads
+            // byte j of the scale words
             auto idesc_mx = [](uint32_t j) {
-                return (j << 4) | ((uint32_t)(BN >> 3) << 17) | (1u << 23) | ((uint32_t)(BM >> 7) << 27) | (j << 29);
+                return (j << 4) | (5u << 7) | (0u << 10) | ((uint32_t)(BN >> 3) << 17) | (1u << 23) |
+                       ((uint32_t)(BM >> 7) << 27) | (j << 29);
             };
             int s = 0;
             uint32_t pf = 0;
@@ -640,7 +635,7 @@ __global__ void __launch_bounds__(mg::RawCfg<PLANAR, MX>::THREADS, 1)
                     if (!__all_sync(0xffffffffu, mbar_wait_bounded(&empty[s], pe, a.status))) { bad = true; break; }
                     tc_fence_after();
                     if constexpr (MX) {
-                        // E4M3 codes: block 2j + half of the stage at columns 8 (2j + half)
+                        // E2M1 codes: block 2j + half of the stage at columns 8 (2j + half)
 #pragma unroll
                         for (int j = 0; j < KSUB; ++j) {
                             const int blk = 2 * (KSUB * cs + j) + half;
@@ -654,7 +649,7 @@ __global__ void __launch_bounds__(mg::RawCfg<PLANAR, MX>::THREADS, 1)
                                 } else {
                                     load_words<4>(slot + off + 17 * blk + 1, w);
                                 }
-                                mxfp4_codes_e4m3(w, o);
+                                mxfp4_codes_e2m1x8(w, o);
                             } else {
 #pragma unroll
                                 for (int i = 0; i < 8; ++i) o[i] = 0u;

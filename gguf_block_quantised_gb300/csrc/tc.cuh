@@ -112,11 +112,12 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
         : "memory");
 }
 
-// D[tmem] (+)= (A[tmem] * 2^(sfa-127)) * (B[smem] * 2^(sfb-127))^T with E4M3 A
-// and B, K = 32, one E8M0 scale per row and per 32 k (kind::mxf8f6f4 with
-// block scaling), issued by one thread.  A (M x 32) sits in TMEM: row m in
-// lane m, elements 4j..4j+3 in column a_tmem + j.  The scale words are at
-// sfa_tmem / sfb_tmem; the instruction descriptor's scale ids pick the byte.
+// D[tmem] (+)= (A[tmem] * 2^(sfa-127)) * (B[smem] * 2^(sfb-127))^T, K = 32, one
+// E8M0 scale per row and per 32 k (kind::mxf8f6f4 with block scaling; the
+// element types are in the instruction descriptor), issued by one thread.
+// A (M x 32) sits in TMEM: row m in lane m, elements 4j..4j+3 in the bytes of
+// column a_tmem + j (an E2M1 code in bits 5..2 of its byte).  The scale words
+// are at sfa_tmem / sfb_tmem; the descriptor's scale ids pick the byte.
 __device__ __forceinline__ void mma_mx_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                           uint32_t sfa_tmem, uint32_t sfb_tmem, bool accumulate)
 {

@@ -27,7 +27,7 @@ from gpu_util import TOL, dev, host, orc_t, workspace
 pytestmark = pytest.mark.gpu
 
 Q4_0, Q5_0, Q8_0, Q4_K, Q6_K, MXFP4, Q8_K, F32, BF16, MXFP4_R = 1, 2, 3, 4, 5, 6, 7, 8, 9, 10
-Q5_K = 16
+Q5_K, MXFP8 = 16, 18
 ALPHA, LIMIT = 1.702, 7.0
 EPS_Y1 = 2e-6
 
@@ -112,6 +112,23 @@ def propagation_allowance(orc, wt, at, E, k, hidden, inter, ids, gates, det):
         step = stepb.reshape(h.shape)
         dh = dhb.reshape(h.shape)
         n_flag = int(flip.sum())
+    elif at == MXFP8:
+        hb, dhb = h.reshape(h.shape[:-1] + (-1, 32)), dh.reshape(dh.shape[:-1] + (-1, 32))
+        amax = np.abs(hb).max(axis=-1, keepdims=True)
+        dmax = dhb.max(axis=-1, keepdims=True)
+        lg = np.floor(np.log2(np.where(amax > 0, amax, 1.0)))
+        E = np.maximum(lg - 8, -127)
+        v = np.abs(hb) * np.exp2(-E)
+        sp = np.where(v < 2.0 ** -6, 2.0 ** -9, np.exp2(np.floor(np.log2(np.maximum(v, 2.0 ** -6))) - 3))
+        frac = v / sp
+        near = np.abs(frac - np.floor(frac) - 0.5) * sp * np.exp2(E) <= dhb
+        flip = near & (v < 448)
+        # a block whose largest magnitude is within reach of a power of two may
+        # take the neighbouring scale: then any code may move (clamping included)
+        amb = (amax - np.exp2(lg) <= dmax) | (np.exp2(lg + 1) - amax <= dmax)
+        stepb = np.where(flip, sp * np.exp2(E), 0.0) + np.where(amb, np.abs(hb) * 0.125 + 2 * sp * np.exp2(E), 0.0)
+        step = stepb.reshape(h.shape)
+        n_flag = int(flip.sum()) + int(amb.sum()) * 32
     elif at == BF16:
         hf = h.astype(np.float32)
         lo = (hf.view(np.uint32) & np.uint32(0xFFFF0000)).view(np.float32).astype(np.float64)
@@ -161,7 +178,7 @@ def check_block(qmv, orc, wt, at, E, k, hidden, inter, n_tok, seed=0, inp=None, 
 
 CASES = [(Q4_0, F32), (Q8_0, F32), (Q4_K, F32), (Q6_K, F32), (MXFP4, F32), (Q5_K, F32),
          (Q4_0, Q8_0), (Q5_0, Q8_0), (MXFP4, Q8_0), (Q4_K, Q8_K), (Q6_K, Q8_K),
-         (MXFP4, BF16), (MXFP4_R, BF16)]
+         (MXFP4, BF16), (MXFP4_R, BF16), (MXFP4, MXFP8), (MXFP4_R, MXFP8)]
 
 
 @pytest.mark.parametrize("wt,at", CASES)
@@ -177,7 +194,7 @@ def test_block_without_biases(qmv, orc):
     check_block(qmv, orc, Q8_0, F32, 16, 2, 256, 128, 5, seed=3, biases=False)
 
 
-@pytest.mark.parametrize("at", [F32, Q8_0, BF16])
+@pytest.mark.parametrize("at", [F32, Q8_0, BF16, MXFP8])
 def test_block_gpt_oss_shapes(qmv, orc, at):
     """gpt-oss-sized experts (hidden = inter = 2880, 32 experts, 4 per token)."""
     used, extra, n_flag = check_block(qmv, orc, MXFP4, at, 32, 4, 2880, 2880, 3, seed=9)
