@@ -19,17 +19,26 @@
 
 namespace qmv {
 
-__global__ void __launch_bounds__(1024) k_moe_group(const int32_t* __restrict__ ids, int n_pairs, int n_expert,
+// Expert ids staged in shared memory when they fit (the scans below read each
+// id once per expert a warp handles).
+constexpr int kGroupStageIds = 10240;   // 40 KB: with base[], under the 48 KB of static shared memory
+
+__global__ void __launch_bounds__(1024) k_moe_group(const int32_t* __restrict__ ids_g, int n_pairs, int n_expert,
                                                     int* __restrict__ offsets, int* __restrict__ active,
                                                     int* __restrict__ perm, unsigned* status)
 {
     __shared__ int base[1025];
+    __shared__ int ids_s[kGroupStageIds];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
     pdl_wait();
+    const bool staged = n_pairs <= kGroupStageIds;
     for (int p = tid; p < n_pairs; p += blockDim.x) {
-        const int e = ids[p];
+        const int e = ids_g[p];
         if (e < 0 || e >= n_expert) atomicOr(status, QMV_DEV_BAD_EXPERT);
+        if (staged) ids_s[p] = e;
     }
+    __syncthreads();
+    const int32_t* ids = staged ? ids_s : ids_g;
     for (int e = warp; e < n_expert; e += nw) {
         int c = 0;
         for (int b = 0; b < n_pairs; b += 32) {
