@@ -63,6 +63,7 @@ struct GemmArgs {
     int m;             // tokens
     float* Y;          // [m][rows]
     unsigned* status;
+    int ks;            // K parts: 1, or 2 (each part adds its fp32 sums into a zeroed Y)
 };
 
 // Two fp32 values in one 64-bit register for the packed f32x2 instructions.
@@ -147,9 +148,11 @@ __global__ void __launch_bounds__(gq::THREADS, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n_rt = (int)((a.rows + BM - 1) / BM);
     const int n_nt = (a.m + BN - 1) / BN;
-    const int n_tiles = n_rt * n_nt;
-    const int nks = a.cols / (KSUB * BK);   // k stages per tile
-    const int nsb = a.cols / 256;
+    // work item t: output tile t / ks, K part t % ks (a whole number of
+    // 256-k super-blocks each)
+    const int n_tiles = n_rt * n_nt * a.ks;
+    const int nks = a.cols / (KSUB * BK) / a.ks;   // k stages per item
+    const int nsb = a.cols / 256 / a.ks;
 
     if (tid == 0) {
         for (int i = 0; i < SK; ++i) { mbar_init(&full[i], DEQ_WARPS + 1); mbar_init(&empty[i], 1); }
@@ -179,14 +182,14 @@ __global__ void __launch_bounds__(gq::THREADS, 1)
             int s = 0;
             uint32_t ph = 1;
             for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x) {
-                const int nt = t / n_rt;
+                const int nt = t / a.ks / n_rt, k0 = (t % a.ks) * nks;
                 for (int ks = 0; ks < nks; ++ks) {
                     if (!mbar_wait_backoff(&empty[s], ph, a.status, 64)) { fail(); break; }
                     mbar_arrive_expect_tx(&full[s], KSUB * X_BYTES);
 #pragma unroll
                     for (int j = 0; j < KSUB; ++j)
-                        tma_load_2d(smem + OFF_X + (s * KSUB + j) * X_BYTES, &tmX, (ks * KSUB + j) * BK, nt * BN,
-                                    &full[s]);
+                        tma_load_2d(smem + OFF_X + (s * KSUB + j) * X_BYTES, &tmX, ((k0 + ks) * KSUB + j) * BK,
+                                    nt * BN, &full[s]);
                     if (++s == SK) { s = 0; ph ^= 1; }
                 }
             }
@@ -197,11 +200,11 @@ __global__ void __launch_bounds__(gq::THREADS, 1)
             int s = 0;
             uint32_t ph = 1;
             for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x) {
-                const int rt = t % n_rt;
+                const int rt = (t / a.ks) % n_rt, sb0 = (t % a.ks) * nsb;
                 for (int sb = 0; sb < nsb; ++sb) {
                     if (!mbar_wait_bounded(&re[s], ph, a.status)) { fail(); break; }
                     mbar_arrive_expect_tx(&rf[s], R_BYTES);
-                    tma_load_2d(smem + OFF_R + s * R_BYTES, &tmW, sb * 144, rt * BM, &rf[s]);
+                    tma_load_2d(smem + OFF_R + s * R_BYTES, &tmW, (sb0 + sb) * 144, rt * BM, &rf[s]);
                     if (++s == SR) { s = 0; ph ^= 1; }
                 }
             }
@@ -282,7 +285,7 @@ __global__ void __launch_bounds__(gq::THREADS, 1)
         const int q = warp & 3, ch = (warp - EPI_WARP0) >> 2;
         int local = 0;
         for (int t = blockIdx.x; t < n_tiles && !__any_sync(0xffffffffu, *abort_flag); t += gridDim.x, ++local) {
-            const int rt = t % n_rt, nt = t / n_rt;
+            const int rt = (t / a.ks) % n_rt, nt = t / a.ks / n_rt;
             const int buf = local % NBUF;
             const uint32_t use = (uint32_t)(local / NBUF);
             // warp-uniform: every lane must take part in the tcgen05.ld below
@@ -305,11 +308,23 @@ __global__ void __launch_bounds__(gq::THREADS, 1)
                     if (lane == 0) mbar_arrive(&acce[buf]);
                 }
                 const int tok0 = nt * BN + c0 + rd * 32;
+                if (a.ks == 1) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    if (row_ok && tok0 + i < a.m) a.Y[(int64_t)(tok0 + i) * a.rows + row] = __uint_as_float(v0[i]);
-                    if (row_ok && tok0 + 16 + i < a.m)
-                        a.Y[(int64_t)(tok0 + 16 + i) * a.rows + row] = __uint_as_float(v1[i]);
+                    for (int i = 0; i < 16; ++i) {
+                        if (row_ok && tok0 + i < a.m) a.Y[(int64_t)(tok0 + i) * a.rows + row] = __uint_as_float(v0[i]);
+                        if (row_ok && tok0 + 16 + i < a.m)
+                            a.Y[(int64_t)(tok0 + 16 + i) * a.rows + row] = __uint_as_float(v1[i]);
+                    }
+                } else {
+                    // two parts add into the zeroed Y: 0 + p0 + p1 = 0 + p1 + p0 in
+                    // IEEE arithmetic, so the result does not depend on which lands first
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        if (row_ok && tok0 + i < a.m)
+                            atomicAdd(a.Y + (int64_t)(tok0 + i) * a.rows + row, __uint_as_float(v0[i]));
+                        if (row_ok && tok0 + 16 + i < a.m)
+                            atomicAdd(a.Y + (int64_t)(tok0 + 16 + i) * a.rows + row, __uint_as_float(v1[i]));
+                    }
                 }
             }
         }
@@ -377,11 +392,19 @@ int qmv_launch_gemm_q4k_bf16(const void* W, int64_t rows, int64_t cols, const vo
     a.m = (int)m;
     a.Y = Y;
     a.status = status_word();
-    // 256-token tiles unless they cannot give every SM a tile or pad the
-    // tokens by more than 128-token tiles would (by over 8%).
+    // Rows much shorter than K (cols >= 2 rows, cols >= 8192, whole 512-k
+    // halves): the K range is split in two parts on different SMs, which
+    // doubles the work items and lets 256-token tiles fill the GPU; each
+    // dequantised weight then serves twice as many tokens.  The split follows
+    // the weight's shape alone, so a token's summation order does not depend
+    // on m.
+    a.ks = (cols >= 8192 && cols >= 2 * rows && cols % 512 == 0) ? 2 : 1;
+    // 256-token tiles unless they cannot give half of the SMs a work item or
+    // pad the tokens by more than 128-token tiles would (by over 8%).
     const int64_t n_rt = (rows + gq::BM - 1) / gq::BM;
     const int64_t pad256 = (m + 255) / 256 * 256, pad128 = (m + 127) / 128 * 128;
-    const bool narrow = n_rt * ((m + 255) / 256) < (int64_t)num_sms() || pad256 * 100 > pad128 * 108;
+    const bool narrow = n_rt * ((m + 255) / 256) * a.ks < (int64_t)num_sms() / (a.ks == 2 ? 2 : 1) ||
+                        pad256 * 100 > pad128 * 108;
     const int BN = narrow ? 128 : 256;
     CUtensorMap tmX;
     if (!make_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, (uint64_t)cols, (uint64_t)m, (uint64_t)cols * 2,
@@ -389,7 +412,12 @@ int qmv_launch_gemm_q4k_bf16(const void* W, int64_t rows, int64_t cols, const vo
         return -8;
     auto* k = narrow ? &k_gemm_q4k_bf16<128> : &k_gemm_q4k_bf16<256>;
     prepare_kernel(k, gq::THREADS, gq::SMEM);
-    const int64_t n_tiles = n_rt * ((m + BN - 1) / BN);
+    const int64_t n_tiles = n_rt * ((m + BN - 1) / BN) * a.ks;
     const int grid = (int)std::min<int64_t>(n_tiles, num_sms());
+    if (a.ks == 2) {
+        // the parts add into Y: zero it first (in stream order, so no programmatic overlap)
+        if (cudaMemsetAsync(Y, 0, (size_t)m * (size_t)rows * sizeof(float), st) != cudaSuccess) return -6;
+        pdl = false;
+    }
     return launch_ex(k, dim3(grid), dim3(gq::THREADS), gq::SMEM, st, pdl, tmX, tmW, a) == cudaSuccess ? 0 : -6;
 }

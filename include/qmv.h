@@ -252,7 +252,13 @@ int qmv_matvec(int fmt, const void* W, int64_t rows, int64_t cols,
  * ("The forward pass").
  *   fmt : QMV_FMT(QMV_Q4_K, QMV_BF16): X bf16 [m][cols]; the weights are
  *         dequantised to bf16 tiles (w rounded once from its fp32 value) and
- *         multiplied on the tensor cores with fp32 accumulation.
+ *         multiplied on the tensor cores with fp32 accumulation.  Rows much
+ *         shorter than K (cols >= 8192, cols >= 2*rows, cols a multiple of
+ *         512) run as two K halves on different SMs whose fp32 sums are added
+ *         into Y after zeroing it (cudaMemsetAsync on the stream; two addends
+ *         commute, so Y does not depend on which half lands first; the split
+ *         follows the weight's shape, so a token's result does not depend
+ *         on m).
  *         QMV_FMT(QMV_Q4_K, QMV_Q8_K): X Q8_K blocks [m][cols/256] (W4A8):
  *         per super-block the integers S = sum sc*q*xq and Mn = sum m*bsum
  *         come out of the tensor cores exactly (sm_103a has no tcgen05

@@ -40,6 +40,25 @@ def test_matmul_bf16_parity(qmv, orc, rows, cols, m):
     qmv.qmv_get_status()
 
 
+@pytest.mark.parametrize("rows,cols,m", [(200, 8192, 300), (1024, 8704, 77), (96, 16384, 1)])
+def test_matmul_k_split_parity(qmv, orc, rows, cols, m):
+    """Rows much shorter than K (cols >= 8192 and >= 2 rows) run as two K halves on
+    different SMs that add into a zeroed Y: every output checked, repeated calls
+    bit-identical (two addends commute, whichever lands first), and a token's
+    outputs the same whatever m is (the split follows the weight's shape)."""
+    W = synth.weights(Q4_K, rows, cols, seed=8, tensor_id=rows + cols)
+    Wd = dev(W)
+    xb, xbits = bf16_x(m, cols, 8)
+    Y = run_matmul(qmv, Wd, rows, cols, xb, m)
+    yref, yabs = orc.matvec(Q4_K, BF16, W, rows, cols, xbits, m)
+    assert_close(Y, yref, yabs, what=f"{rows}x{cols} m={m}")
+    for _ in range(3):
+        assert np.array_equal(run_matmul(qmv, Wd, rows, cols, xb, m).view(np.uint32), Y.view(np.uint32))
+    one = run_matmul(qmv, Wd, rows, cols, xb[m - 1:m], 1)
+    assert np.array_equal(one[0].view(np.uint32), Y[m - 1].view(np.uint32))
+    qmv.qmv_get_status()
+
+
 @pytest.mark.parametrize("rows,m", [(9700, 500), (19500, 200)])
 def test_matmul_many_tiles_parity(qmv, orc, rows, m):
     """Enough row tiles that every SM gets at least one: 256-token tiles (the
