@@ -190,7 +190,7 @@ inline int launch_moe_nv(const MoeParams& mp, const GemvPlan& pl, int grid_y, in
     int64_t gx = ((int64_t)num_sms() * occ * waves + active - 1) / active;
     if (gx > n_tiles) gx = n_tiles;
     if (gx < 1) gx = 1;
-    return launch_ex(k, dim3((unsigned)gx, (unsigned)grid_y), dim3(kGemvThreads), smem, st, false, mp) ==
+    return launch_ex(k, dim3((unsigned)gx, (unsigned)grid_y), dim3(kGemvThreads), smem, st, true, mp) ==
                    cudaSuccess
                ? 0
                : -6;

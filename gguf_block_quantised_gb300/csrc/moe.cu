@@ -30,6 +30,7 @@ __global__ void __launch_bounds__(1024) k_moe_group(const int32_t* __restrict__ 
     __shared__ int base[1025];
     __shared__ int ids_s[kGroupStageIds];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
+    pdl_trigger();
     pdl_wait();
     const bool staged = n_pairs <= kGroupStageIds;
     for (int p = tid; p < n_pairs; p += blockDim.x) {
@@ -41,7 +42,15 @@ __global__ void __launch_bounds__(1024) k_moe_group(const int32_t* __restrict__ 
     const int32_t* ids = staged ? ids_s : ids_g;
     for (int e = warp; e < n_expert; e += nw) {
         int c = 0;
-        for (int b = 0; b < n_pairs; b += 32) {
+        int b = 0;
+        for (; b + 96 < n_pairs; b += 128) {   // four independent loads and ballots per round
+            const int v0 = ids[b + lane], v1 = ids[b + 32 + lane], v2 = ids[b + 64 + lane];
+            const int p3 = b + 96 + lane;
+            const int v3 = p3 < n_pairs ? ids[p3] : -1;
+            c += __popc(__ballot_sync(0xffffffffu, v0 == e)) + __popc(__ballot_sync(0xffffffffu, v1 == e)) +
+                 __popc(__ballot_sync(0xffffffffu, v2 == e)) + __popc(__ballot_sync(0xffffffffu, v3 == e));
+        }
+        for (; b < n_pairs; b += 32) {
             const int p = b + lane;
             c += __popc(__ballot_sync(0xffffffffu, p < n_pairs && ids[p] == e));
         }
@@ -64,12 +73,21 @@ __global__ void __launch_bounds__(1024) k_moe_group(const int32_t* __restrict__ 
     const uint32_t lt = (1u << lane) - 1u;
     for (int e = warp; e < n_expert; e += nw) {
         int pos = base[e];
-        for (int b = 0; b < n_pairs; b += 32) {
-            const int p = b + lane;
-            const bool m = p < n_pairs && ids[p] == e;
-            const uint32_t mask = __ballot_sync(0xffffffffu, m);
-            if (m) perm[pos + __popc(mask & lt)] = p;
-            pos += __popc(mask);
+        for (int b = 0; b < n_pairs; b += 128) {   // four chunks of 32 pairs per round, placed in order
+            bool m[4];
+            uint32_t mask[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int p = b + 32 * j + lane;
+                m[j] = p < n_pairs && ids[p] == e;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) mask[j] = __ballot_sync(0xffffffffu, m[j]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (m[j]) perm[pos + __popc(mask[j] & lt)] = b + 32 * j + lane;
+                pos += __popc(mask[j]);
+            }
         }
     }
 }
@@ -78,6 +96,8 @@ __global__ void k_moe_combine(const float* __restrict__ part, const int32_t* __r
                               const float* __restrict__ gates, const float* __restrict__ bias, int k, int64_t rows,
                               int64_t n_tok, int n_expert, float* __restrict__ y)
 {
+    pdl_trigger();
+    pdl_wait();   // the slot outputs come from the kernel before this one
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n_tok * rows) return;
     const int64_t t = i / rows, r = i % rows;
@@ -152,8 +172,12 @@ int qmv_launch_moe_ex(int wtype, bool a8, bool quant_x, bool bf16, bool mx, size
     int* perm = reinterpret_cast<int*>(w + r256(2050 * 4));
     float* part = reinterpret_cast<float*>(w + r256(2050 * 4) + r256((size_t)n_pairs * 4));
     if (!grouped) {
-        k_moe_group<<<1, 1024, 0, st>>>(ids, (int)n_pairs, n_expert, offsets, active, perm, status_word());
-        if (cudaGetLastError() != cudaSuccess) return -6;
+        // every kernel of the chain waits for its predecessor before touching memory,
+        // so each is launched as a programmatic dependent (its launch overlaps the
+        // kernel before it)
+        if (launch_ex(k_moe_group, dim3(1), dim3(1024), 0, st, true, ids, (int)n_pairs, n_expert, offsets, active, perm,
+                      status_word()) != cudaSuccess)
+            return -6;
     }
     const size_t xrow = (a8 && !quant_x) ? (size_t)(cols / (kq_rt(wtype) ? 256 : 32)) *
                                                act_block_bytes
@@ -193,8 +217,9 @@ int qmv_launch_moe_ex(int wtype, bool a8, bool quant_x, bool bf16, bool mx, size
     if (rc) return rc;
     if (gates) {
         const int64_t n = n_tok * rows;
-        k_moe_combine<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(part, ids, gates, bias, k, rows, n_tok, n_expert, y);
-        if (cudaGetLastError() != cudaSuccess) return -6;
+        if (launch_ex(k_moe_combine, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, true, (const float*)part,
+                      ids, gates, bias, k, rows, n_tok, n_expert, y) != cudaSuccess)
+            return -6;
     }
     return 0;
 }

@@ -46,6 +46,8 @@ __global__ void __launch_bounds__(256) k_router(const float* __restrict__ x, con
                                                 float* __restrict__ logits, __nv_bfloat16* __restrict__ xb)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_trigger();
+    pdl_wait();
     const int64_t t0 = (int64_t)blockIdx.x * RT_TOK;
     const int nt = (int)(n_tok - t0 < RT_TOK ? n_tok - t0 : RT_TOK);
     const int e = blockIdx.y * RT_EXP + warp;
@@ -77,15 +79,17 @@ __global__ void __launch_bounds__(256) k_router(const float* __restrict__ x, con
                 for (int j = 0; j < RT_TOK; ++j) acc[j] = __fmaf_rn(xv[u][j], wv[u], acc[j]);
         }
     } else if (nt == 1) {
-        for (; h + (U - 1) * 32 < hidden; h += U * 32) {
-            float wv[U], xv[U];
+        // one token (decode): 24 steps per memory round trip
+        constexpr int U1 = 24;
+        for (; h + (U1 - 1) * 32 < hidden; h += U1 * 32) {
+            float wv[U1], xv[U1];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
+            for (int u = 0; u < U1; ++u) {
                 wv[u] = __ldg(w + h + u * 32);
                 xv[u] = __ldg(xt + h + u * 32);
             }
 #pragma unroll
-            for (int u = 0; u < U; ++u) acc[0] = __fmaf_rn(xv[u], wv[u], acc[0]);
+            for (int u = 0; u < U1; ++u) acc[0] = __fmaf_rn(xv[u], wv[u], acc[0]);
         }
     }
     for (; h < hidden; h += 32) {   // the rest, and partial token tiles of more than one token
@@ -118,6 +122,8 @@ __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, 
 {
     extern __shared__ float sm[];   // per warp: E logits, then 64 kept logits
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_trigger();
+    pdl_wait();
     const int64_t t = (int64_t)blockIdx.x * 8 + warp;
     if (t >= n_tok) return;
     float* L = sm + warp * (E + 64);
@@ -172,6 +178,8 @@ template <bool BF>
 __global__ void __launch_bounds__(256) k_swiglu(const float* __restrict__ y1, int64_t n_pairs, int64_t inter,
                                                 float alpha, float limit, void* __restrict__ h)
 {
+    pdl_trigger();
+    pdl_wait();
     const int64_t n = n_pairs * inter;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t p = i / inter, c = i - p * inter;
@@ -237,12 +245,16 @@ int qmv_launch_moe_block(int wtype, bool a8, bool bf16, bool mx, size_t act_bloc
     void* inner = w;
 
     const dim3 rgrid((unsigned)((n_tok + RT_TOK - 1) / RT_TOK), (unsigned)((n_expert + RT_EXP - 1) / RT_EXP));
-    k_router<<<rgrid, 256, 0, st>>>(x, Wr, br, n_tok, hidden, n_expert, logits, xb);
-    if (cudaGetLastError() != cudaSuccess) return -6;
+    // each kernel waits for its predecessor before touching memory: all are
+    // launched as programmatic dependents
+    if (launch_ex(k_router, rgrid, dim3(256), 0, st, true, x, Wr, br, n_tok, hidden, n_expert, logits, xb) !=
+        cudaSuccess)
+        return -6;
     const size_t tsm = (size_t)8 * (n_expert + 64) * 4;
     prepare_kernel(k_topk, 256, tsm);
-    k_topk<<<(unsigned)((n_tok + 7) / 8), 256, tsm, st>>>(logits, n_tok, n_expert, k, ids, gates);
-    if (cudaGetLastError() != cudaSuccess) return -6;
+    if (launch_ex(k_topk, dim3((unsigned)((n_tok + 7) / 8)), dim3(256), tsm, st, true, (const float*)logits, n_tok,
+                  n_expert, k, ids, gates) != cudaSuccess)
+        return -6;
 
     const void* xin = bf16 ? static_cast<const void*>(xb) : static_cast<const void*>(x);
     int rc = qmv_launch_moe_ex(wtype, a8, a8, bf16, mx, act_block_bytes, Wgu, n_expert, 2 * inter, hidden, ids, nullptr,
@@ -250,9 +262,9 @@ int qmv_launch_moe_block(int wtype, bool a8, bool bf16, bool mx, size_t act_bloc
     if (rc) return rc;
     const int64_t n = n_pairs * inter;
     const unsigned sg = (unsigned)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
-    if (bf16) k_swiglu<true><<<sg, 256, 0, st>>>(y1, n_pairs, inter, alpha, limit, h);
-    else k_swiglu<false><<<sg, 256, 0, st>>>(y1, n_pairs, inter, alpha, limit, h);
-    if (cudaGetLastError() != cudaSuccess) return -6;
+    if (launch_ex(bf16 ? k_swiglu<true> : k_swiglu<false>, dim3(sg), dim3(256), 0, st, true, (const float*)y1, n_pairs,
+                  inter, alpha, limit, h) != cudaSuccess)
+        return -6;
     return qmv_launch_moe_ex(wtype, a8, a8, bf16, mx, act_block_bytes, Wd, n_expert, hidden, inter, ids, gates, k, h, y,
                              n_tok, bd, inner, true, st);
 }

@@ -620,7 +620,7 @@ __global__ void __launch_bounds__(mg::RawCfg<PLANAR, MX>::THREADS, 1)
             const int64_t row_start = ((int64_t)e * a.rows + row) * a.rb;   // byte offset of the row
             bool bad = false;
             for (int sc = 0; sc < nsc && !bad; ++sc) {
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&rf[sr], prf, a.status))) { bad = true; break; }
+                if (!__all_sync(0xffffffffu, mbar_wait_backoff(&rf[sr], prf, a.status, 32))) { bad = true; break; }
                 const uint8_t* rbuf = smem + OFF_R + sr * R_BYTES;
                 const uint8_t* slot = rbuf + r * SLOT;
                 const int off = (int)((row_start + (int64_t)sc * SC_BLOCKS * 17) & 15);
@@ -632,7 +632,7 @@ __global__ void __launch_bounds__(mg::RawCfg<PLANAR, MX>::THREADS, 1)
                     if ((int)(gk & 1) != grp) continue;
                     const int s = (int)(gk % SK);
                     const uint32_t pe = ((gk / SK) & 1) ^ 1;
-                    if (!__all_sync(0xffffffffu, mbar_wait_bounded(&empty[s], pe, a.status))) { bad = true; break; }
+                    if (!__all_sync(0xffffffffu, mbar_wait_backoff(&empty[s], pe, a.status, 32))) { bad = true; break; }
                     tc_fence_after();
                     if constexpr (MX) {
                         // E2M1 codes: block 2j + half of the stage at columns 8 (2j + half)
