@@ -75,8 +75,17 @@ constexpr int RC_BYTES = BM * 128;       // one code box
 // MX (MXFP8 activations): the scale bytes of a token tile's rows, staged whole
 // per tile (double-buffered): rows of at most this many bytes (cols <= 4096).
 constexpr int MX_SPITCH_MAX = 128;
-constexpr int SFBUF = BN * MX_SPITCH_MAX;
-template <bool PLANAR, bool MX = false>
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t A_STAGE_COLS = KSUB * BK / 2;   // bf16 A stage: 128 rows x 128 k, two per column
+constexpr uint32_t A_STAGE_COLS_MX = 32;           // E2M1 A stage: four byte-container codes per column
+// Per variant: TBN tokens per tile (the bf16 form 128; the MX form 128 or, when
+// experts average more than 96 routed tokens, 192 so that one tile covers them),
+// SKV k stages.  TMEM columns: two TBN-column fp32 accumulators, then SKV A
+// stages; MX adds per stage four columns of weight scales and TBN/32 of token
+// scales.  Weight row m's scale for K step j of a stage sits in lane m, column
+// SFA + m/32, byte j; token n's in lane 32q + n % 32, column SFB + n/32, byte j,
+// for every lane quarter q (the MMA reads the quarter of the output row).
+template <bool PLANAR, bool MX = false, int TBN = 128>
 struct RawCfg {
     static constexpr int BLOCKS = PLANAR ? 16 : 8;                        // blocks per row per raw stage
     static constexpr int SR = PLANAR ? 2 : 4;                             // raw stages
@@ -86,30 +95,23 @@ struct RawCfg {
     // scales in every TMEM lane quarter (the last four)
     static constexpr int THREADS = (PLANAR ? 768 : 896) + (MX ? 128 : 0);
     static constexpr int SF_WARP0 = THREADS / 32 - 4;
-    static constexpr int XS = MX ? X_BYTES : KSUB * X_BYTES;              // X bytes per 128-k stage
-    static constexpr int OFF_R = OFF_X + SK * XS;
+    static constexpr int SKV = TBN > 128 ? 3 : SK;
+    static constexpr int XB = MX ? TBN * 128 : X_BYTES;                   // bytes of one X box
+    static constexpr int XS = MX ? XB : KSUB * X_BYTES;                   // X bytes per 128-k stage
+    static constexpr int SFBUF = TBN * MX_SPITCH_MAX;
+    static constexpr int OFF_R = OFF_X + SKV * XS;
     static constexpr int OFF_SF = OFF_R + SR * R_BYTES;
     static constexpr int OFF_BAR = OFF_SF + (MX ? 2 * SFBUF : 0);
-    static constexpr int N_BARS = 2 * SK + 2 * SR + 4 + (MX ? 4 : 0);
+    static constexpr int N_BARS = 2 * SKV + 2 * SR + 4 + (MX ? 4 : 0);
     static constexpr int SMEM = OFF_BAR + N_BARS * 8 + 16 + 1024;   // + alignment slack
+    static constexpr uint32_t A_COL = 2 * TBN;
+    static constexpr uint32_t SFA_COL = A_COL + SKV * A_STAGE_COLS_MX;
+    static constexpr uint32_t SFB_COL = SFA_COL + SKV * 4;
     static_assert(SMEM <= 227 * 1024, "shared memory");
+    static_assert(MX || TBN == 128, "the bf16 form uses 128-token tiles");
+    static_assert(A_COL + SKV * (MX ? A_STAGE_COLS_MX : A_STAGE_COLS) + (MX ? SKV * (4 + TBN / 32) : 0) <= TMEM_COLS,
+                  "TMEM budget");
 };
-// TMEM columns: two 128-column fp32 accumulators, then SK bf16 A tiles of
-// 64 columns each (128 rows x 128 k, two elements per column).
-constexpr uint32_t A_COL = 2 * BN;
-constexpr uint32_t A_STAGE_COLS = KSUB * BK / 2;
-constexpr uint32_t TMEM_COLS = 512;
-static_assert(A_COL + SK * A_STAGE_COLS <= TMEM_COLS, "TMEM budget");
-// MX: SK E2M1 A tiles of 32 columns (128 rows x 128 k, four byte-container
-// codes per column),
-// then per stage four columns of weight scales and four of token scales.
-// Weight row m's scale for K step j of a stage sits in lane m, column
-// SFA + m/32, byte j; token n's in lane 32q + n % 32, column SFB + n/32, byte
-// j, for every lane quarter q (the MMA reads the quarter of the output row).
-constexpr uint32_t A_STAGE_COLS_MX = 32;
-constexpr uint32_t SFA_COL = A_COL + SK * A_STAGE_COLS_MX;
-constexpr uint32_t SFB_COL = SFA_COL + SK * 4;
-static_assert(SFB_COL + SK * 4 <= TMEM_COLS, "TMEM budget (MX)");
 }  // namespace mg
 
 // 16-byte asynchronous copy global -> shared (dst, src 16-byte aligned);
@@ -254,7 +256,8 @@ __device__ __forceinline__ void mxfp4_codes_e2m1x8(const uint32_t (&w)[4], uint3
 
 // tiles[0] = number of (expert, token tile) slots; slot i = (tiles[1+2i] =
 // expert, tiles[2+2i] = token tile within the expert's group).
-__global__ void k_moe_tiles(const int* __restrict__ offsets, const int* __restrict__ active, int* __restrict__ tiles)
+__global__ void k_moe_tiles(const int* __restrict__ offsets, const int* __restrict__ active, int bn,
+                            int* __restrict__ tiles)
 {
     const int lane = threadIdx.x;
     pdl_wait();
@@ -263,7 +266,7 @@ __global__ void k_moe_tiles(const int* __restrict__ offsets, const int* __restri
     for (int i0 = 0; i0 < na; i0 += 32) {
         const int i = i0 + lane;
         const int e = i < na ? active[1 + i] : 0;
-        const int nt = i < na ? (offsets[e + 1] - offsets[e] + mg::BN - 1) / mg::BN : 0;
+        const int nt = i < na ? (offsets[e + 1] - offsets[e] + bn - 1) / bn : 0;
         int pre = nt;   // inclusive prefix sum over the warp
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -347,15 +350,16 @@ struct MoeGemmArgs {
 // codes in TMEM byte containers with their E8M0 exponents as the weight
 // scales, the tokens' E4M3 codes in shared memory with their scales --
 // instead of bf16 on kind::f16.
-template <bool PLANAR, bool MX>
-__global__ void __launch_bounds__(mg::RawCfg<PLANAR, MX>::THREADS, 1)
+template <bool PLANAR, bool MX, int TBN>
+__global__ void __launch_bounds__(mg::RawCfg<PLANAR, MX, TBN>::THREADS, 1)
     k_moe_gemm_mxfp4(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmC,
                      const __grid_constant__ CUtensorMap tmE, const MoeGemmArgs a)
 {
     using namespace mg;
-    using RC = RawCfg<PLANAR, MX>;
+    using RC = RawCfg<PLANAR, MX, TBN>;
     constexpr int SR = RC::SR, R_BYTES = RC::R_BYTES, OFF_BAR = RC::OFF_BAR, SC_BLOCKS = RC::BLOCKS;
-    constexpr int OFF_R = RC::OFF_R, XS = RC::XS;
+    constexpr int OFF_R = RC::OFF_R, XS = RC::XS, SK = RC::SKV, BN = TBN;
+    constexpr uint32_t A_COL = RC::A_COL, SFA_COL = RC::SFA_COL, SFB_COL = RC::SFB_COL;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
@@ -426,13 +430,13 @@ __global__ void __launch_bounds__(mg::RawCfg<PLANAR, MX>::THREADS, 1)
                 const int sb = local & 1;
                 if (!mbar_wait_backoff(&sfe[sb], (uint32_t)(((local >> 1) & 1) ^ 1), a.status, 128)) { fail(); break; }
                 mbar_arrive_expect_tx(&sff[sb], (uint32_t)(nsf * a.spitch));
-                bulk_g2s(smem + RC::OFF_SF + sb * SFBUF, a.sf + (size_t)row0 * a.spitch, (uint32_t)(nsf * a.spitch),
+                bulk_g2s(smem + RC::OFF_SF + sb * RC::SFBUF, a.sf + (size_t)row0 * a.spitch, (uint32_t)(nsf * a.spitch),
                          &sff[sb]);
                 pend = local;
                 bool bad = false;
                 for (int ks = 0; ks < nks; ++ks) {
                     if (!mbar_wait_backoff(&empty[s], ph, a.status, 128)) { bad = true; break; }
-                    mbar_arrive_expect_tx(&full[s], X_BYTES);
+                    mbar_arrive_expect_tx(&full[s], RC::XB);
                     tma_load_2d(smem + OFF_X + s * XS, &tmX, ks * 128, row0, &full[s]);
                     if (++s == SK) { s = 0; ph ^= 1; }
                 }
@@ -456,19 +460,19 @@ __global__ void __launch_bounds__(mg::RawCfg<PLANAR, MX>::THREADS, 1)
             const int row0 = a.offsets[e] + nt * BN;
             const int nsf = min(BN, a.sf_rows - row0);
             const int sb = local & 1;
-            const uint8_t* sfb = smem + RC::OFF_SF + sb * SFBUF;
+            const uint8_t* sfb = smem + RC::OFF_SF + sb * RC::SFBUF;
             if (!__all_sync(0xffffffffu, mbar_wait_bounded(&sff[sb], (uint32_t)((local >> 1) & 1), a.status))) {
                 bad = true;
             }
             for (int ks = 0; ks < nks && !bad; ++ks) {
                 if (!__all_sync(0xffffffffu, mbar_wait_backoff(&empty[s], ph, a.status, 128))) { bad = true; break; }
-                uint32_t w[4];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < TBN / 32; ++c) {
                     const int j = lane + 32 * c;
-                    w[c] = j < nsf ? *reinterpret_cast<const uint32_t*>(sfb + j * a.spitch + 4 * ks) : 0x7f7f7f7fu;
+                    tmem_st1_async(tq + SFB_COL + (TBN / 32) * s + c,
+                                   j < nsf ? *reinterpret_cast<const uint32_t*>(sfb + j * a.spitch + 4 * ks)
+                                           : 0x7f7f7f7fu);
                 }
-                tmem_st4_async(tq + SFB_COL + 4 * s, w);
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
@@ -582,7 +586,7 @@ __global__ void __launch_bounds__(mg::RawCfg<PLANAR, MX>::THREADS, 1)
 #pragma unroll
                         for (int j = 0; j < 4; ++j)   // A: 8 TMEM columns, B: 32 bytes per K = 32 step
                             mma_mx_ts(d, at + 8 * j, bdesc + 2 * j, idesc_mx((uint32_t)j), tmem + SFA_COL + 4 * s,
-                                      tmem + SFB_COL + 4 * s, (ks | j) != 0);
+                                      tmem + SFB_COL + (TBN / 32) * s, (ks | j) != 0);
                     } else {
                         const uint32_t at = tmem + A_COL + s * A_STAGE_COLS;
 #pragma unroll
@@ -746,7 +750,7 @@ __global__ void __launch_bounds__(mg::RawCfg<PLANAR, MX>::THREADS, 1)
 
 inline size_t tiles_bytes(int64_t n_pairs)
 {
-    const size_t slots = (size_t)n_pairs + (size_t)n_pairs / mg::BN + 1;   // >= sum over experts of ceil(count/128)
+    const size_t slots = (size_t)n_pairs + (size_t)n_pairs / mg::BN + 1;   // >= sum over experts of ceil(count/128) (and /192)
     return ((1 + 2 * slots) * 4 + 255) & ~size_t(255);
 }
 
@@ -788,7 +792,10 @@ int qmv_launch_moe_gemm_mxfp4(const void* W3d, bool planar, bool mx, int n_exper
     int* tiles = static_cast<int*>(ws);
     uint8_t* act = static_cast<uint8_t*>(ws) + tiles_bytes(n_pairs);
     uint8_t* sf = act + r256g((size_t)n_pairs * (size_t)cols);
-    k_moe_tiles<<<1, 32, 0, st>>>(offsets, active, tiles);
+    // MX: 192-token tiles when the experts average more than 96 routed pairs, so
+    // that one tile pass over an expert's rows covers its tokens
+    const int tbn = (mx && n_pairs > (int64_t)96 * n_expert) ? 192 : 128;
+    k_moe_tiles<<<1, 32, 0, st>>>(offsets, active, tbn, tiles);
     CUtensorMap tmX, tmC, tmE;
     if (mx) {
         const int64_t threads = n_pairs * spitch * 8;
@@ -796,7 +803,7 @@ int qmv_launch_moe_gemm_mxfp4(const void* W3d, bool planar, bool mx, int n_exper
             static_cast<const float*>(x), perm, offsets, n_expert, kdiv, (int)cols, spitch, act, sf);
         if (cudaGetLastError() != cudaSuccess) return -6;
         if (!make_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_UINT8, act, (uint64_t)cols, (uint64_t)n_pairs,
-                          (uint64_t)cols, 128, mg::BN, CU_TENSOR_MAP_SWIZZLE_128B))
+                          (uint64_t)cols, 128, (uint32_t)tbn, CU_TENSOR_MAP_SWIZZLE_128B))
             return -8;
     } else {
         uint16_t* Xs = reinterpret_cast<uint16_t*>(act);
@@ -839,11 +846,19 @@ int qmv_launch_moe_gemm_mxfp4(const void* W3d, bool planar, bool mx, int n_exper
         prepare_kernel(k, threads, smem);
         return launch_ex(k, dim3(num_sms()), dim3(threads), smem, st, false, tmX, tmC, tmE, a) == cudaSuccess ? 0 : -6;
     };
-    if (planar)
-        return mx ? launch(&k_moe_gemm_mxfp4<true, true>, mg::RawCfg<true, true>::THREADS, mg::RawCfg<true, true>::SMEM)
-                  : launch(&k_moe_gemm_mxfp4<true, false>, mg::RawCfg<true>::THREADS, mg::RawCfg<true>::SMEM);
-    return mx ? launch(&k_moe_gemm_mxfp4<false, true>, mg::RawCfg<false, true>::THREADS, mg::RawCfg<false, true>::SMEM)
-              : launch(&k_moe_gemm_mxfp4<false, false>, mg::RawCfg<false>::THREADS, mg::RawCfg<false>::SMEM);
+    using mg::RawCfg;
+    if (planar) {
+        if (!mx) return launch(&k_moe_gemm_mxfp4<true, false, 128>, RawCfg<true>::THREADS, RawCfg<true>::SMEM);
+        return tbn == 192
+                   ? launch(&k_moe_gemm_mxfp4<true, true, 192>, RawCfg<true, true, 192>::THREADS,
+                            RawCfg<true, true, 192>::SMEM)
+                   : launch(&k_moe_gemm_mxfp4<true, true, 128>, RawCfg<true, true>::THREADS, RawCfg<true, true>::SMEM);
+    }
+    if (!mx) return launch(&k_moe_gemm_mxfp4<false, false, 128>, RawCfg<false>::THREADS, RawCfg<false>::SMEM);
+    return tbn == 192 ? launch(&k_moe_gemm_mxfp4<false, true, 192>, RawCfg<false, true, 192>::THREADS,
+                               RawCfg<false, true, 192>::SMEM)
+                      : launch(&k_moe_gemm_mxfp4<false, true, 128>, RawCfg<false, true>::THREADS,
+                               RawCfg<false, true>::SMEM);
 }
 
 // ---- repack: GGUF MXFP4 rows -> MXFP4_R rows --------------------------------------
