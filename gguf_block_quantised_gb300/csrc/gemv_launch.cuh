@@ -200,8 +200,9 @@ inline int launch_moe_nv(const MoeParams& mp, const GemvPlan& pl, int grid_y, in
 // apart; pair p reads row p / kdiv and writes out[p*rows ..].
 template <int T>
 inline int launch_moe_t(bool a8, bool quant_x, const void* W3d, int n_expert, int64_t rows, int64_t cols,
-                        const int* offsets, const int* active_list, const int* perm, int n_pairs, int n_tok,
-                        const void* x, size_t xrow, int kdiv, float* out, const float* bias, cudaStream_t st)
+                        const int* offsets, const int* active_list, const int* perm, const int32_t* ids,
+                        bool self_group, int n_pairs, int n_tok, const void* x, size_t xrow, int kdiv, float* out,
+                        const float* bias, cudaStream_t st)
 {
     using F = Fmt<T>;
     if (rows == 0 || n_pairs == 0) return 0;
@@ -244,6 +245,10 @@ inline int launch_moe_t(bool a8, bool quant_x, const void* W3d, int n_expert, in
     mp.out = out;
     mp.bias = bias;
     mp.group = pl.group;
+    mp.ids = ids;
+    mp.n_pairs = n_pairs;
+    mp.n_expert = n_expert;
+    mp.self_group = self_group ? 1 : 0;
     // Grid rows map onto the experts that received pairs (at most this many).
     // When every expert takes one group of pairs (decode) the work per expert
     // is even and one wave of CTAs covers it; otherwise two waves of smaller
@@ -271,11 +276,12 @@ inline int launch_moe_t(bool a8, bool quant_x, const void* W3d, int n_expert, in
 
 #define QMV_MOE_INSTANTIATE(T, NAME)                                                                        \
     int NAME(bool a8, bool quant_x, const void* W3d, int n_expert, int64_t rows, int64_t cols,                 \
-             const int* offsets, const int* active, const int* perm, int n_pairs, int n_tok, const void* x,    \
-             size_t xrow, int kdiv, float* out, const float* bias, cudaStream_t st)                             \
+             const int* offsets, const int* active, const int* perm, const int32_t* ids, bool self_group,      \
+             int n_pairs, int n_tok, const void* x, size_t xrow, int kdiv, float* out, const float* bias,       \
+             cudaStream_t st)                                                                                   \
     {                                                                                                           \
-        return qmv::launch_moe_t<T>(a8, quant_x, W3d, n_expert, rows, cols, offsets, active, perm, n_pairs,    \
-                                    n_tok, x, xrow, kdiv, out, bias, st);                                       \
+        return qmv::launch_moe_t<T>(a8, quant_x, W3d, n_expert, rows, cols, offsets, active, perm, ids,        \
+                                    self_group, n_pairs, n_tok, x, xrow, kdiv, out, bias, st);                  \
     }
 
 #define QMV_GEMV_INSTANTIATE(T, NAME)                                                                     \

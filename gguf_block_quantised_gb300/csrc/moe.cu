@@ -119,8 +119,8 @@ inline size_t r256(size_t v) { return (v + 255) & ~size_t(255); }
 
 #define QMV_MOE_DECL(NAME)                                                                                      \
     int NAME(bool a8, bool quant_x, const void* W3d, int n_expert, int64_t rows, int64_t cols, const int* offsets, \
-             const int* active, const int* perm, int n_pairs, int n_tok, const void* x, size_t xrow, int kdiv,      \
-             float* out, const float* bias, cudaStream_t st);
+             const int* active, const int* perm, const int32_t* ids, bool self_group, int n_pairs, int n_tok,       \
+             const void* x, size_t xrow, int kdiv, float* out, const float* bias, cudaStream_t st);
 QMV_MOE_DECL(qmv_moe_q4_0)
 QMV_MOE_DECL(qmv_moe_q5_0)
 QMV_MOE_DECL(qmv_moe_q8_0)
@@ -171,7 +171,10 @@ int qmv_launch_moe_ex(int wtype, bool a8, bool quant_x, bool bf16, bool mx, size
     int* active = offsets + 1025;                         // [0] = count, [1..] = expert ids
     int* perm = reinterpret_cast<int*>(w + r256(2050 * 4));
     float* part = reinterpret_cast<float*>(w + r256(2050 * 4) + r256((size_t)n_pairs * 4));
-    if (!grouped) {
+    // At most 32 pairs on the matvec path (decode): each expert CTA groups the
+    // ids itself, so the grouping kernel is not launched.
+    const bool self_group = !bf16 && !mx && n_pairs <= 32;
+    if (!grouped && !self_group) {
         // every kernel of the chain waits for its predecessor before touching memory,
         // so each is launched as a programmatic dependent (its launch overlaps the
         // kernel before it)
@@ -194,8 +197,8 @@ int qmv_launch_moe_ex(int wtype, bool a8, bool quant_x, bool bf16, bool mx, size
                  : -3;
     }
 #define QMV_MOE_CALL(NAME) \
-    NAME(a8, quant_x, W3d, n_expert, rows, cols, offsets, active, perm, (int)n_pairs, (int)n_tok, x, xrow, kdiv, out, \
-         b, st)
+    NAME(a8, quant_x, W3d, n_expert, rows, cols, offsets, active, perm, ids, self_group, (int)n_pairs, (int)n_tok, x, \
+         xrow, kdiv, out, b, st)
     if (!bf16 && !mx) switch (wtype) {
     case QMV_Q4_0: rc = QMV_MOE_CALL(qmv_moe_q4_0); break;
     case QMV_Q5_0: rc = QMV_MOE_CALL(qmv_moe_q5_0); break;

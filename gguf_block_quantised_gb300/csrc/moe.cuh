@@ -26,18 +26,74 @@ struct MoeParams {
     float* out;              // output row of pair p at out + p*rows
     const float* bias;       // [n_expert][rows] added to every output (NULL: none)
     int group;               // pairs staged at once (<= the kernel's NV, <= 16)
+    // self-grouping (at most 32 pairs, decode): offsets/active/perm are unused;
+    // each CTA sorts the pairs' expert ids itself
+    const int32_t* ids;      // [n_pairs] expert of each pair
+    int n_pairs, n_expert, self_group;
 };
+
+// The grouping of at most 32 pairs by one warp: the experts that received
+// pairs, in id order, and for the y-th of them its pairs in pair order (the
+// stable counting sort of k_moe_group, restricted to one expert).  Ids out of
+// range set the status word and their pairs are left out.
+struct SmallGroup {
+    int n_active, e, cnt;
+    int perm[32];
+};
+
+__device__ __forceinline__ void small_group(const MoeParams& mp, int y, SmallGroup& g)
+{
+    const int lane = threadIdx.x & 31;
+    const int e = lane < mp.n_pairs ? mp.ids[lane] : -1;
+    const bool valid = e >= 0 && e < mp.n_expert;
+    if (lane < mp.n_pairs && !valid) atomicOr(mp.g.status, QMV_DEV_BAD_EXPERT);
+    const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
+    const uint32_t same = __match_any_sync(0xffffffffu, valid ? e : -1) & vmask;
+    const bool first = valid && (__ffs(same) - 1) == lane;   // first pair of its expert
+    const uint32_t firsts = __ballot_sync(0xffffffffu, first);
+    // rank of this lane's expert among the distinct experts, by id
+    int rank = 0;
+    for (uint32_t f = firsts; f; f &= f - 1) {
+        const int q = __ffs(f) - 1;
+        const int eq = __shfl_sync(0xffffffffu, e, q);
+        rank += (valid && eq < e) ? 1 : 0;
+    }
+    const uint32_t mine = __ballot_sync(0xffffffffu, first && rank == y);
+    if (lane == 0) {
+        g.n_active = __popc(firsts);
+        g.e = -1;
+        g.cnt = 0;
+    }
+    __syncwarp();
+    if (mine) {
+        const int leader = __ffs(mine) - 1;
+        const uint32_t pairs = __shfl_sync(0xffffffffu, same, leader);
+        if (lane == leader) {
+            g.e = e;
+            g.cnt = __popc(pairs);
+        }
+        if ((pairs >> lane) & 1u) g.perm[__popc(pairs & ((1u << lane) - 1u))] = lane;
+    }
+}
 
 template <int T, bool A8, int NV, int RIF>
 __global__ void __launch_bounds__(kGemvThreads, two_ctas_per_sm<T, A8, NV>() ? 2 : 1) k_moe_gemv(const MoeParams mp)
 {
     using F = Fmt<T>;
     extern __shared__ __align__(128) uint8_t smem[];
-    pdl_wait();   // the grouping comes from the kernel before this one
-    if ((int)blockIdx.y >= mp.active[0]) return;   // uniform for the whole block
-    const int e = mp.active[1 + blockIdx.y];
-    const int o0 = mp.offsets[e];
-    const int cnt = mp.offsets[e + 1] - o0;
+    // bytes 0..259 hold the barriers, pair_of, xrow_of and the abort flag (below);
+    // the self-grouping result sits in the free bytes before the staged vectors at 512
+    SmallGroup& sg = *reinterpret_cast<SmallGroup*>(smem + 320);
+    static_assert(320 + sizeof(SmallGroup) <= 512, "self-grouping scratch");
+    pdl_wait();   // the grouping (or the ids) comes from the kernel before this one
+    if (mp.self_group) {
+        if (threadIdx.x < 32) small_group(mp, (int)blockIdx.y, sg);
+        __syncthreads();
+    }
+    if ((int)blockIdx.y >= (mp.self_group ? sg.n_active : mp.active[0])) return;   // uniform for the whole block
+    const int e = mp.self_group ? sg.e : mp.active[1 + blockIdx.y];
+    const int o0 = mp.self_group ? 0 : mp.offsets[e];
+    const int cnt = mp.self_group ? sg.cnt : mp.offsets[e + 1] - o0;
     GemvParams p = mp.g;
     const int tr = kConsumerWarps * p.rpw;
     const int64_t n_tiles = (p.rows + tr - 1) / tr;
@@ -114,7 +170,7 @@ __global__ void __launch_bounds__(kGemvThreads, two_ctas_per_sm<T, A8, NV>() ? 2
         const int gv = min(G, cnt - grp * G);
         cbar();   // everyone is done with the previous group's activations
         if (tid < gv) {
-            const int pr = mp.perm[o0 + grp * G + tid];
+            const int pr = mp.self_group ? sg.perm[grp * G + tid] : mp.perm[o0 + grp * G + tid];
             pair_of[tid] = pr;
             xrow_of[tid] = pr / mp.kdiv;
         }
