@@ -671,7 +671,8 @@ def block_time(q, torch, stream, fmt, Wgu, Wd, bgu, bd, Wr, br, n_tok, hbm, E=32
 def run_probe(spec):
     """Single-kernel runs for profiling (ncu captures).  Specs:
       gemv:T:rows:cols:atype:n_vec   qmv_matvec on synthetic weights (atype 8 = fp32)
-      gemm:rows:cols:m               qmv_matmul, Q4_K x bf16
+      gemm:rows:cols:m[:T]           qmv_matmul, weight type T (default Q4_K) x bf16; other types than
+                                     Q4_K run the two-pass product (bf16 dequantisation, then the GEMM)
       gemm8:rows:cols:m              qmv_matmul, Q4_K x Q8_K (W4A8, with its activation pre-pass)
       step[:n_vec]                   one fused decode step of the Qwen2.5-0.5B shape (97 matvecs)
       block:n_tok[:atype]            qmv_moe_block on the gpt-oss MoE shapes (atype 3 = Q8_0, 8 = fp32, 9 = bf16)
@@ -699,11 +700,15 @@ def run_probe(spec):
         call = lambda: q.qmv_matvec(q.FMT(t, at), W, rows, cols, x, y, nv)
         nbytes, what = W.numel(), "weight GB/s"
     elif kind == "gemm":
-        rows, cols, m = a
-        W = torch.from_numpy(synth.weights(Q4_K, rows, cols, seed=1)).cuda()
+        rows, cols, m, t = (a + [Q4_K])[:4]
+        W = torch.from_numpy(synth.weights(t, rows, cols, seed=1)).cuda()
         X = torch.randn(m, cols, device="cuda").to(torch.bfloat16)
         Y = torch.empty(m, rows, device="cuda")
-        call = lambda: q.qmv_matmul(q.FMT(Q4_K, BF16), W, rows, cols, X, Y, m)
+        need = q.qmv_workspace_size(q.OP_MATMUL, q.FMT(t, BF16), rows, cols, m)
+        if need:
+            ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+            q.qmv_set_workspace(ws, ws.numel())
+        call = lambda: q.qmv_matmul(q.FMT(t, BF16), W, rows, cols, X, Y, m)
         nbytes, what = 2 * m * rows * cols / 1e3, "TFLOP/s"
     elif kind == "gemm8":
         rows, cols, m = a

@@ -43,6 +43,9 @@ QMV_GEMV_DECL(qmv_gemv_f32)
 QMV_GEMV_DECL(qmv_gemv_f16)
 QMV_GEMV_DECL(qmv_gemv_bf16)
 size_t qmv_w4a8_workspace_bytes(int64_t cols, int64_t m);
+size_t qmv_bf16_gemm_workspace_bytes(int64_t rows, int64_t cols);
+int qmv_launch_gemm_bf16_two_pass(int t, const void* W, int64_t rows, int64_t cols, const void* X, float* Y, int64_t m,
+                                  void* ws, bool pdl, cudaStream_t st);
 int qmv_launch_gemm_q4k_w4a8(const void* W, int64_t rows, int64_t cols, const void* X, float* Y, int64_t m,
                              void* ws, bool pdl, cudaStream_t st);
 size_t qmv_moe_workspace_bytes(bool bf16, int64_t rows, int64_t cols, int64_t n_pairs, bool mx);
@@ -106,6 +109,19 @@ int ok()
 {
     t_err.clear();
     return QMV_OK;
+}
+
+// Weight types whose rows the bf16 dequantising pass reads (the GGUF block
+// types and the plain F32/F16/BF16 rows; not the repacked QMV_MXFP4_R rows).
+bool dequant_type(int t)
+{
+    switch (t) {
+    case QMV_Q4_0: case QMV_Q5_0: case QMV_Q8_0: case QMV_MXFP4: case QMV_Q4_K: case QMV_Q6_K:
+    case QMV_Q4_1: case QMV_Q5_1: case QMV_Q8_1: case QMV_Q2_K: case QMV_Q3_K: case QMV_Q5_K:
+    case QMV_F32: case QMV_F16: case QMV_BF16:
+        return true;
+    default: return false;
+    }
 }
 
 const char* type_name(int t)
@@ -463,10 +479,11 @@ int qmv_matmul(int fmt, const void* W, int64_t rows, int64_t cols, const void* X
     if (fmt & ~(0xffff | QMV_FLAG_PDL)) return fail(QMV_ERR_INVALID_ARG, "unknown flags 0x%x", fmt & ~0xffff);
     const bool pdl = (fmt & QMV_FLAG_PDL) != 0;
     const int wtype = fmt & 0xff, atype = (fmt >> 8) & 0xff;
-    if (wtype != QMV_Q4_K || (atype != QMV_BF16 && atype != QMV_Q8_K))
+    const bool two_pass = atype == QMV_BF16 && wtype != QMV_Q4_K && dequant_type(wtype);
+    if (!two_pass && (wtype != QMV_Q4_K || (atype != QMV_BF16 && atype != QMV_Q8_K)))
         return fail(QMV_ERR_UNSUPPORTED,
-                    "qmv_matmul: %s weights with %s activations are not provided; supported: QMV_FMT(Q4_K, BF16), "
-                    "QMV_FMT(Q4_K, Q8_K) (other formats: qmv_matvec with n_vec <= 64)",
+                    "qmv_matmul: %s weights with %s activations are not provided; supported: QMV_FMT(Q4_K, Q8_K) "
+                    "and QMV_FMT(t, BF16) for every GGUF block type and F32/F16/BF16 rows t",
                     type_name(wtype), type_name(atype));
     int rc = check_weights(wtype, W, rows, cols);
     if (rc) return rc;
@@ -495,6 +512,29 @@ int qmv_matmul(int fmt, const void* W, int64_t rows, int64_t cols, const void* X
                         "qmv_matmul (W4A8) needs %zu bytes of workspace (qmv_workspace_size(QMV_OP_MATMUL, ...)); "
                         "%zu set", need, have);
         rc = qmv_launch_gemm_q4k_w4a8(W, rows, cols, X, Y, m, ws, pdl, static_cast<cudaStream_t>(stream));
+        if (rc == -8) return fail(QMV_ERR_CUDA, "qmv_matmul: could not build a TMA tensor map");
+        if (rc) return cuda_fail("qmv_matmul");
+        return ok();
+    }
+    if (two_pass) {
+        // dequantise once into bf16 tiles in the workspace, then a bf16 x bf16
+        // tensor-core GEMM over them
+        if (cols % 8) return fail(QMV_ERR_SHAPE, "qmv_matmul: cols = %lld must be a multiple of 8", (long long)cols);
+        const size_t need = qmv_bf16_gemm_workspace_bytes(rows, cols);
+        void* ws = nullptr;
+        size_t have = 0;
+        const int d = qmv::current_device();
+        if (d >= 0 && d < qmv::kMaxDevices) {
+            std::lock_guard<std::mutex> lock(g_ws_mu);
+            ws = g_ws[d].ptr;
+            have = g_ws[d].bytes;
+        }
+        if (!ws || have < need)
+            return fail(QMV_ERR_WORKSPACE,
+                        "qmv_matmul (%s weights) needs %zu bytes of workspace (qmv_workspace_size(QMV_OP_MATMUL, "
+                        "...)); %zu set",
+                        type_name(wtype), need, have);
+        rc = qmv_launch_gemm_bf16_two_pass(wtype, W, rows, cols, X, Y, m, ws, pdl, static_cast<cudaStream_t>(stream));
         if (rc == -8) return fail(QMV_ERR_CUDA, "qmv_matmul: could not build a TMA tensor map");
         if (rc) return cuda_fail("qmv_matmul");
         return ok();
@@ -606,6 +646,9 @@ size_t qmv_workspace_size(int op, int fmt, int64_t rows, int64_t cols, int64_t n
     if (op == QMV_OP_MATMUL && (fmt & 0xffff) == QMV_FMT(QMV_Q4_K, QMV_Q8_K) && rows > 0 && n > 0 && cols > 0 &&
         cols % 256 == 0)
         return qmv_w4a8_workspace_bytes(cols, n);
+    if (op == QMV_OP_MATMUL && ((fmt >> 8) & 0xff) == QMV_BF16 && (fmt & 0xff) != QMV_Q4_K &&
+        dequant_type(fmt & 0xff) && rows > 0 && n > 0 && cols > 0)
+        return qmv_bf16_gemm_workspace_bytes(rows, cols);
     return 0;
 }
 

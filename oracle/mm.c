@@ -76,12 +76,21 @@ static int dot_row(int wtype, int atype, const uint8_t* wrow, int64_t cols, cons
                    double* y, double* yabs)
 {
     if (orc_plain_bytes(wtype)) {
-        /* plain weights against fp32 activations: the definition, in fp64 */
+        /* plain weights against fp32 activations: the definition, in fp64; against
+           bf16 activations (the prefill product) the weight is first rounded to
+           bf16 from its fp32 value, as the bf16 tile holds it */
         double acc = 0.0, aabs = 0.0;
         for (int64_t c = 0; c < cols; c++) {
-            float xf;
-            memcpy(&xf, xv + 4 * c, 4);
-            const double p = orc_plain_weight(wtype, wrow, c) * (double)xf;
+            double p;
+            if (atype == ORC_BF16) {
+                const uint16_t xb = (uint16_t)(xv[2 * c] | (xv[2 * c + 1] << 8));
+                const float wf = (float)orc_plain_weight(wtype, wrow, c);
+                p = orc_bf16_to_f64(orc_f32_to_bf16_rn(wf)) * orc_bf16_to_f64(xb);
+            } else {
+                float xf;
+                memcpy(&xf, xv + 4 * c, 4);
+                p = orc_plain_weight(wtype, wrow, c) * (double)xf;
+            }
             acc += p;
             aabs += fabs(p);
         }
@@ -162,7 +171,7 @@ static int64_t weight_row_bytes(int wtype, int64_t cols)
 
 static int check_pair(int wtype, int atype, int64_t cols)
 {
-    if (orc_plain_bytes(wtype)) return (atype == ORC_F32 && cols > 0) ? ORC_OK : ORC_EUNSUP;
+    if (orc_plain_bytes(wtype)) return ((atype == ORC_F32 || atype == ORC_BF16) && cols > 0) ? ORC_OK : ORC_EUNSUP;
     if (!weight_type_ok(wtype)) return ORC_EUNSUP;
     if (atype == ORC_MXFP8 && orc_block_elems(wtype) != 32) return ORC_EUNSUP;
     if (atype != ORC_F32 && atype != ORC_BF16 && atype != ORC_MXFP8 && atype != paired_act(wtype)) return ORC_EUNSUP;

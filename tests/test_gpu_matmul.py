@@ -121,7 +121,7 @@ def test_matmul_edge_cases(qmv, orc):
     assert (run_matmul(qmv, W, rows, cols, torch.zeros((3, cols), dtype=torch.bfloat16), 3) == 0).all()
     # unsupported pairs and shapes are refused before any launch
     with pytest.raises(qmv.QmvError) as e:
-        qmv.qmv_matmul(qmv.FMT(2, BF16), W, rows, cols, W, Y, 1)
+        qmv.qmv_matmul(qmv.FMT(Q4_K, F32), W, rows, cols, W, Y, 1)
     assert e.value.code == qmv.ERR_UNSUPPORTED
     with pytest.raises(qmv.QmvError) as e:
         qmv.qmv_matmul(qmv.FMT(Q4_K, BF16), W, rows, 300, W, Y, 1)

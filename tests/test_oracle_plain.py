@@ -106,3 +106,32 @@ def test_plain_weights_matvec_dense(orc, t):
     assert np.allclose(yabs, np.abs(x.astype(np.float64)) @ np.abs(wd).T, rtol=1e-12, atol=0)
     with pytest.raises(Exception):
         orc.matvec(t, Q8_0, raw, rows, cols, orc.quantize_act(Q8_0, x), n)   # plain weights pair with F32 only
+
+
+@pytest.mark.parametrize("t", [F32, F16, BF16])
+def test_plain_weights_bf16_activations(orc, t):
+    """Plain rows against bf16 activations (the prefill product): each weight is
+    rounded to bf16 from its fp32 value, nearest-even (torch's conversion), and
+    the products are summed in fp64.  F32 rows include exact halfway cases
+    (1 + 2^-8 rounds down to 1, 1 + 3*2^-8 up to 1 + 2^-6) so a truncating or
+    ties-away rounding fails."""
+    g = np.random.default_rng(70 + t)
+    rows, cols, n = 7, 64, 3
+    w32 = g.standard_normal((rows, cols)).astype(np.float32)
+    w32[0, :4] = [1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, -(1 + 2.0 ** -8), 3.0 * (1 + 2.0 ** -8)]
+    if t == F32:
+        raw, wf = w32.view(np.uint8).reshape(-1), w32
+    elif t == F16:
+        w16 = w32.astype(np.float16)
+        raw, wf = w16.view(np.uint8).reshape(-1), w16.astype(np.float32)
+    else:
+        wb = torch.from_numpy(w32).to(torch.bfloat16)
+        raw, wf = wb.view(torch.int16).numpy().view(np.uint8).reshape(-1), wb.float().numpy()
+    wd = torch.from_numpy(wf).to(torch.bfloat16).double().numpy()
+    if t == F32:
+        assert wd[0, 0] == 1.0 and wd[0, 1] == 1 + 2.0 ** -6 and wd[0, 2] == -1.0
+    xb = torch.from_numpy(g.standard_normal((n, cols)).astype(np.float32)).to(torch.bfloat16)
+    y, yabs = orc.matvec(t, BF16, raw, rows, cols, xb.view(torch.int16).numpy(), n)
+    xd = xb.double().numpy()
+    assert np.allclose(y, xd @ wd.T, rtol=0, atol=1e-12)
+    assert np.allclose(yabs, np.abs(xd) @ np.abs(wd).T, rtol=1e-12, atol=0)
