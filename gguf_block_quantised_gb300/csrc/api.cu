@@ -44,8 +44,10 @@ QMV_GEMV_DECL(qmv_gemv_f16)
 QMV_GEMV_DECL(qmv_gemv_bf16)
 size_t qmv_w4a8_workspace_bytes(int64_t cols, int64_t m);
 size_t qmv_bf16_gemm_workspace_bytes(int64_t rows, int64_t cols);
-int qmv_launch_gemm_bf16_two_pass(int t, const void* W, int64_t rows, int64_t cols, const void* X, float* Y, int64_t m,
-                                  void* ws, bool pdl, cudaStream_t st);
+int qmv_launch_gemm_two_pass_bf16(int t, const void* W, int64_t rows, int64_t cols, const void* X, float* Y, int64_t m,
+                               void* ws, bool pdl, cudaStream_t st);
+int qmv_launch_gemm_deq_bf16(int t, const void* W, int64_t rows, int64_t cols, const void* X, float* Y, int64_t m,
+                             bool pdl, cudaStream_t st);
 int qmv_launch_gemm_q4k_w4a8(const void* W, int64_t rows, int64_t cols, const void* X, float* Y, int64_t m,
                              void* ws, bool pdl, cudaStream_t st);
 size_t qmv_moe_workspace_bytes(bool bf16, int64_t rows, int64_t cols, int64_t n_pairs, bool mx);
@@ -122,6 +124,16 @@ bool dequant_type(int t)
         return true;
     default: return false;
     }
+}
+
+// Block types and row lengths whose prefill GEMM dequantises tiles into TMEM
+// itself (besides Q4_K's own kernel): the raw tiles are TMA boxes, which need
+// rows of a whole number of 16 bytes.
+bool fused_tile(int t, int64_t cols)
+{
+    if (t != QMV_Q4_0 && t != QMV_Q5_0 && t != QMV_Q8_0 && t != QMV_Q6_K) return false;
+    const int64_t bs = qmv_block_elems(t);
+    return cols > 0 && cols % bs == 0 && (cols / bs) * (int64_t)qmv_block_bytes(t) % 16 == 0;
 }
 
 const char* type_name(int t)
@@ -516,25 +528,33 @@ int qmv_matmul(int fmt, const void* W, int64_t rows, int64_t cols, const void* X
         if (rc) return cuda_fail("qmv_matmul");
         return ok();
     }
+    if (two_pass && fused_tile(wtype, cols)) {
+        // tiles dequantised into TMEM inside the GEMM
+        rc = qmv_launch_gemm_deq_bf16(wtype, W, rows, cols, X, Y, m, pdl, static_cast<cudaStream_t>(stream));
+        if (rc == -8) return fail(QMV_ERR_CUDA, "qmv_matmul: could not build a TMA tensor map");
+        if (rc) return cuda_fail("qmv_matmul");
+        return ok();
+    }
     if (two_pass) {
-        // dequantise once into bf16 tiles in the workspace, then a bf16 x bf16
-        // tensor-core GEMM over them
-        if (cols % 8) return fail(QMV_ERR_SHAPE, "qmv_matmul: cols = %lld must be a multiple of 8", (long long)cols);
-        const size_t need = qmv_bf16_gemm_workspace_bytes(rows, cols);
+        // BF16 rows as they are; the other types converted to bf16 tiles in
+        // the workspace first
         void* ws = nullptr;
-        size_t have = 0;
-        const int d = qmv::current_device();
-        if (d >= 0 && d < qmv::kMaxDevices) {
-            std::lock_guard<std::mutex> lock(g_ws_mu);
-            ws = g_ws[d].ptr;
-            have = g_ws[d].bytes;
+        if (wtype != QMV_BF16) {
+            const size_t need = qmv_bf16_gemm_workspace_bytes(rows, cols);
+            size_t have = 0;
+            const int d = qmv::current_device();
+            if (d >= 0 && d < qmv::kMaxDevices) {
+                std::lock_guard<std::mutex> lock(g_ws_mu);
+                ws = g_ws[d].ptr;
+                have = g_ws[d].bytes;
+            }
+            if (!ws || have < need)
+                return fail(QMV_ERR_WORKSPACE,
+                            "qmv_matmul (%s weights) needs %zu bytes of workspace (qmv_workspace_size(QMV_OP_MATMUL, "
+                            "...)); %zu set",
+                            type_name(wtype), need, have);
         }
-        if (!ws || have < need)
-            return fail(QMV_ERR_WORKSPACE,
-                        "qmv_matmul (%s weights) needs %zu bytes of workspace (qmv_workspace_size(QMV_OP_MATMUL, "
-                        "...)); %zu set",
-                        type_name(wtype), need, have);
-        rc = qmv_launch_gemm_bf16_two_pass(wtype, W, rows, cols, X, Y, m, ws, pdl, static_cast<cudaStream_t>(stream));
+        rc = qmv_launch_gemm_two_pass_bf16(wtype, W, rows, cols, X, Y, m, ws, pdl, static_cast<cudaStream_t>(stream));
         if (rc == -8) return fail(QMV_ERR_CUDA, "qmv_matmul: could not build a TMA tensor map");
         if (rc) return cuda_fail("qmv_matmul");
         return ok();
@@ -646,8 +666,8 @@ size_t qmv_workspace_size(int op, int fmt, int64_t rows, int64_t cols, int64_t n
     if (op == QMV_OP_MATMUL && (fmt & 0xffff) == QMV_FMT(QMV_Q4_K, QMV_Q8_K) && rows > 0 && n > 0 && cols > 0 &&
         cols % 256 == 0)
         return qmv_w4a8_workspace_bytes(cols, n);
-    if (op == QMV_OP_MATMUL && ((fmt >> 8) & 0xff) == QMV_BF16 && (fmt & 0xff) != QMV_Q4_K &&
-        dequant_type(fmt & 0xff) && rows > 0 && n > 0 && cols > 0)
+    if (op == QMV_OP_MATMUL && ((fmt >> 8) & 0xff) == QMV_BF16 && dequant_type(fmt & 0xff) && (fmt & 0xff) != QMV_Q4_K &&
+        (fmt & 0xff) != QMV_BF16 && !fused_tile(fmt & 0xff, cols) && rows > 0 && n > 0 && cols > 0)
         return qmv_bf16_gemm_workspace_bytes(rows, cols);
     return 0;
 }

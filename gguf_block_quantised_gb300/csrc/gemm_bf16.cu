@@ -1,16 +1,15 @@
-// gemm_bf16.cu -- prefill GEMM for the weight formats without a fused tile
-// dequantiser: Y[m][r] = sum_k X[m][k] * bf16(w[r][k]) on the 5th-generation
-// tensor cores (tcgen05, sm_103a).
+// gemm_bf16.cu -- prefill GEMM for plain weight rows: Y[m][r] = sum_k X[m][k] *
+// bf16(w[r][k]) on the 5th-generation tensor cores (tcgen05, sm_103a).
 //
 // "Architecture" page, "The package map": pkg/tensor MatMul is the prefill
-// multiply; "The two phases": prefill is bound by arithmetic.  The pages' own
-// prefill workload mixes Q5_0, Q8_0, Q6_K and Q4_K matrices.  Q4_K has a fused
-// kernel (gemm_q4k.cu) whose dequantising warps feed TMEM directly; every other
-// weight format runs in two passes here: the weights are dequantised once into
-// bf16 tiles in the workspace (verify.cu, w rounded to bf16 from its fp32 value,
-// as in the fused kernel), then multiplied by this plain bf16 x bf16 GEMM.  At
-// prefill sizes the GEMM is bound by the tensor cores, and the extra pass is a
-// stream over the weights.
+// multiply; "The two phases": prefill is bound by arithmetic.  BF16 weight rows
+// are the GEMM's A operand as they are.  F32 and F16 rows, and the block
+// formats without a tile dequantiser inside a GEMM (Q4_1, Q5_1, Q8_1, MXFP4,
+// Q2_K, Q3_K, Q5_K, and Q4_0 / Q5_0 / Q8_0 / Q6_K rows whose byte length is not
+// a multiple of 16), are first converted to bf16 (w's fp32 value rounded to
+// nearest even) in the workspace by a streaming pass, then multiplied.  (Q4_K
+// and the other Q4_0, Q5_0, Q8_0, Q6_K rows dequantise tile by tile inside
+// their GEMMs: gemm_q4k.cu, gemm_deq.cu.)
 //
 // One persistent CTA per SM, 12 warps:
 //   warp 0      TMA producer: per 128-k stage two boxes of weight rows
@@ -29,7 +28,7 @@
 #include <cuda_bf16.h>
 
 #include "common.cuh"
-#include "formats.cuh"
+#include "dequant_unit.cuh"
 #include "runtime.cuh"
 #include "tc.cuh"
 
@@ -213,74 +212,6 @@ __global__ void __launch_bounds__(gb::THREADS, 1)
 // writes it with 16-byte stores.  Blocks are row-major and rows have whole
 // blocks, so block i's elements land at i*BS in the [rows][cols] bf16 tiles.
 
-// Element index of byte j of code word k of a 32-element unit (MXFP4 keeps its
-// nibble pairs: low nibble = element p/2, high = 16 + p/2).
-template <int T>
-__device__ __forceinline__ constexpr int unit_elem(int k, int j)
-{
-    if constexpr (T == QMV_MXFP4) {
-        const int p = 4 * k + j;
-        return (p & 1) ? 16 + (p >> 1) : (p >> 1);
-    } else {
-        return 4 * k + j;
-    }
-}
-
-// The UE values of unit `s` of the block at blk, in the unit's own element
-// order (Q6_K: group g's 16 elements at 16g..16g+15).
-template <int T>
-__device__ __forceinline__ void unit_values(const uint8_t* blk, int s, float (&v)[Fmt<T>::UE])
-{
-    using F = Fmt<T>;
-    typename F::W w;
-    F::load(blk, s, w);
-    if constexpr (plain_rt(T)) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) v[k] = w.w[k];
-    } else if constexpr (F::BS == 32) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t byte = (w.c[k] >> (8 * j)) & 0xffu;
-                const int q = F::SIGNED ? (int)(int8_t)byte : (int)byte - F::OFF;
-                if constexpr (F::MIN) v[unit_elem<T>(k, j)] = __fmaf_rn(w.d, (float)q, w.m);   // one rounding
-                else v[unit_elem<T>(k, j)] = w.d * (float)q;   // exact: <= 24 significant bits
-            }
-    } else if constexpr (T == QMV_Q4_K || T == QMV_Q5_K) {
-        constexpr uint32_t mask = T == QMV_Q5_K ? 31u : 15u;
-        const float D0 = w.d * (float)w.sc0, D1 = w.d * (float)w.sc1;       // exact
-        const float M0 = w.dmin * (float)w.m0, M1 = w.dmin * (float)w.m1;   // exact
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                v[4 * k + j] = __fmaf_rn(D0, (float)((w.lo[k] >> (8 * j)) & mask), -M0);
-                v[32 + 4 * k + j] = __fmaf_rn(D1, (float)((w.hi[k] >> (8 * j)) & mask), -M1);
-            }
-    } else if constexpr (T == QMV_Q2_K || T == QMV_Q3_K) {
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const float D = w.d * (float)w.sc[r];   // exact
-            const float M = T == QMV_Q2_K ? w.dmin * (float)w.m[r] : 0.f;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int c = (int)((w.c[r >> 1][4 * (r & 1) + (i >> 2)] >> (8 * (i & 3))) & 0xffu);
-                v[16 * r + i] = T == QMV_Q2_K ? __fmaf_rn(D, (float)c, -M) : D * (float)(c - 4);
-            }
-        }
-    } else {   // Q6_K
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-            const float D = w.d * (float)w.sc[g];   // exact
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) v[16 * g + 4 * k + j] = D * (float)((int)((w.g[g][k] >> (8 * j)) & 63u) - 32);
-        }
-    }
-}
-
 // Eight values -> eight bf16 (round to nearest even) in one 16-byte store.
 __device__ __forceinline__ void store_bf16x8(__nv_bfloat16* p, const float* v)
 {
@@ -348,9 +279,8 @@ static int launch_dequant_bf16(int t, const void* W, int64_t rows, int64_t cols,
     case QMV_Q4_0: return launch_dequant_bf16_t<QMV_Q4_0>(W, rows, cols, out, st);
     case QMV_Q5_0: return launch_dequant_bf16_t<QMV_Q5_0>(W, rows, cols, out, st);
     case QMV_Q8_0: return launch_dequant_bf16_t<QMV_Q8_0>(W, rows, cols, out, st);
-    case QMV_MXFP4: return launch_dequant_bf16_t<QMV_MXFP4>(W, rows, cols, out, st);
-    case QMV_Q4_K: return launch_dequant_bf16_t<QMV_Q4_K>(W, rows, cols, out, st);
     case QMV_Q6_K: return launch_dequant_bf16_t<QMV_Q6_K>(W, rows, cols, out, st);
+    case QMV_MXFP4: return launch_dequant_bf16_t<QMV_MXFP4>(W, rows, cols, out, st);
     case QMV_Q4_1: return launch_dequant_bf16_t<QMV_Q4_1>(W, rows, cols, out, st);
     case QMV_Q5_1: return launch_dequant_bf16_t<QMV_Q5_1>(W, rows, cols, out, st);
     case QMV_Q8_1: return launch_dequant_bf16_t<QMV_Q8_1>(W, rows, cols, out, st);
@@ -359,7 +289,6 @@ static int launch_dequant_bf16(int t, const void* W, int64_t rows, int64_t cols,
     case QMV_Q5_K: return launch_dequant_bf16_t<QMV_Q5_K>(W, rows, cols, out, st);
     case QMV_F32: return launch_dequant_bf16_t<QMV_F32>(W, rows, cols, out, st);
     case QMV_F16: return launch_dequant_bf16_t<QMV_F16>(W, rows, cols, out, st);
-    case QMV_BF16: return launch_dequant_bf16_t<QMV_BF16>(W, rows, cols, out, st);
     default: return -3;
     }
 }
@@ -372,17 +301,16 @@ size_t qmv_bf16_gemm_workspace_bytes(int64_t rows, int64_t cols)
     return ((size_t)rows * (size_t)cols * 2 + 255) & ~size_t(255);
 }
 
-// Dequantises W (weight type t) to bf16 in ws, then Y = X * Wb^T.  Returns 0,
-// -3 (type), -6 (launch failure) or -8 (tensor map).
-int qmv_launch_gemm_bf16_two_pass(int t, const void* W, int64_t rows, int64_t cols, const void* X, float* Y, int64_t m,
-                                  void* ws, bool pdl, cudaStream_t st)
+namespace qmv {
+
+// Y = X * Wb^T with Wb bf16 [rows][cols] (16-byte rows).  as_dependent: launch
+// as a programmatic dependent of the kernel before it on the stream (the GEMM
+// waits for it before its first copy).
+static int launch_gemm_bf16(const void* Wb, int64_t rows, int64_t cols, const void* X, float* Y, int64_t m,
+                            bool as_dependent, cudaStream_t st)
 {
-    using namespace qmv;
-    if (rows == 0 || m == 0) return 0;
-    const int rc = launch_dequant_bf16(t, W, rows, cols, ws, st);
-    if (rc) return rc;
     CUtensorMap tmW, tmX;
-    if (!make_tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws, (uint64_t)cols, (uint64_t)rows, (uint64_t)cols * 2,
+    if (!make_tmap_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Wb, (uint64_t)cols, (uint64_t)rows, (uint64_t)cols * 2,
                       gb::BK, gb::BM, CU_TENSOR_MAP_SWIZZLE_128B))
         return -8;
     GemmBf16Args a;
@@ -402,20 +330,32 @@ int qmv_launch_gemm_bf16_two_pass(int t, const void* W, int64_t rows, int64_t co
         return -8;
     const int64_t n_tiles = n_rt * ((m + BN - 1) / BN);
     const int grid = (int)std::min<int64_t>(n_tiles, num_sms());
-    // the dequantising pass just before: a programmatic dependent of it (the GEMM
-    // waits for it before its first copy); pdl: the dequantising pass itself is
-    // an ordinary launch after the caller's kernels
-    (void)pdl;
     if (narrow) {
         prepare_kernel(&k_gemm_bf16<128>, gb::THREADS, gb::Cfg<128>::SMEM);
-        return launch_ex(&k_gemm_bf16<128>, dim3(grid), dim3(gb::THREADS), gb::Cfg<128>::SMEM, st, true, tmX, tmW, a) ==
-                       cudaSuccess
+        return launch_ex(&k_gemm_bf16<128>, dim3(grid), dim3(gb::THREADS), gb::Cfg<128>::SMEM, st, as_dependent, tmX,
+                         tmW, a) == cudaSuccess
                    ? 0
                    : -6;
     }
     prepare_kernel(&k_gemm_bf16<256>, gb::THREADS, gb::Cfg<256>::SMEM);
-    return launch_ex(&k_gemm_bf16<256>, dim3(grid), dim3(gb::THREADS), gb::Cfg<256>::SMEM, st, true, tmX, tmW, a) ==
-                   cudaSuccess
+    return launch_ex(&k_gemm_bf16<256>, dim3(grid), dim3(gb::THREADS), gb::Cfg<256>::SMEM, st, as_dependent, tmX, tmW,
+                     a) == cudaSuccess
                ? 0
                : -6;
+}
+
+}  // namespace qmv
+
+// BF16 weights multiply as they are; the other types here are first converted
+// to bf16 tiles in ws (qmv_bf16_gemm_workspace_bytes).  Returns 0, -3 (type), -6
+// (launch failure) or -8 (tensor map).
+int qmv_launch_gemm_two_pass_bf16(int t, const void* W, int64_t rows, int64_t cols, const void* X, float* Y, int64_t m,
+                               void* ws, bool pdl, cudaStream_t st)
+{
+    using namespace qmv;
+    if (rows == 0 || m == 0) return 0;
+    if (t == QMV_BF16) return launch_gemm_bf16(W, rows, cols, X, Y, m, pdl, st);
+    const int rc = launch_dequant_bf16(t, W, rows, cols, ws, st);
+    if (rc) return rc;
+    return launch_gemm_bf16(ws, rows, cols, X, Y, m, true, st);
 }

@@ -30,7 +30,7 @@
 // unwinds and frees its TMEM.
 #include <cuda.h>
 
-#include "formats.cuh"
+#include "dequant_unit.cuh"
 #include "q4k_fields.cuh"
 #include "runtime.cuh"
 #include "tc.cuh"
@@ -65,27 +65,6 @@ struct GemmArgs {
     unsigned* status;
     int ks;            // K parts: 1, or 2 (each part adds its fp32 sums into a zeroed Y)
 };
-
-// Two fp32 values in one 64-bit register for the packed f32x2 instructions.
-__device__ __forceinline__ uint64_t pk2(float lo, float hi)
-{
-    return ((uint64_t)__float_as_uint(hi) << 32) | __float_as_uint(lo);
-}
-
-// (D*q - M) for the two codes packed in bytes j0, j1 of `codes` (each 0..15),
-// exactly as two fp32 fused multiply-adds: 0x4B0000qq is the float 2^23 + q,
-// so subtracting 2^23 gives q exactly.
-__device__ __forceinline__ uint32_t dq2_bf16(uint32_t codes, uint32_t sel, uint64_t D2, uint64_t negM2)
-{
-    const uint32_t f0 = __byte_perm(codes, 0x4B000000u, sel & 0xffffu);          // bytes: code, 0, 0, 0x4B
-    const uint32_t f1 = __byte_perm(codes, 0x4B000000u, sel >> 16);
-    uint64_t v = ((uint64_t)f1 << 32) | f0, q, w;
-    const uint64_t two23 = pk2(-8388608.f, -8388608.f);
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(q) : "l"(v), "l"(two23));
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(w) : "l"(D2), "l"(q), "l"(negM2));
-    const __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float((uint32_t)w), __uint_as_float((uint32_t)(w >> 32)));
-    return *reinterpret_cast<const uint32_t*>(&b);
-}
 
 // Dequantise this thread's part of sub-blocks 2c, 2c+1 of the raw super-block
 // tile: w = RN_fp32(d*sc*q - dmin*m) (d*sc and dmin*m are exact products),

@@ -272,15 +272,18 @@ int qmv_matvec(int fmt, const void* W, int64_t rows, int64_t cols,
  *         accuracy bar above.
  *         QMV_FMT(t, QMV_BF16) for every other weight type t (Q4_0, Q5_0,
  *         Q8_0, Q6_K, MXFP4, Q4_1, Q5_1, Q8_1, Q2_K, Q3_K, Q5_K and plain
- *         F32/F16/BF16 rows; not QMV_MXFP4_R): two passes on the stream, a
- *         dequantising kernel writes bf16(w) (rounded once from w's fp32
- *         value) into the workspace, then a bf16 x bf16 tensor-core GEMM with
- *         fp32 accumulation reads it.  cols must be a multiple of 8 (and of
- *         the block).  Needs qmv_workspace_size(QMV_OP_MATMUL, fmt, rows,
- *         cols, m) bytes of workspace: rows*cols*2 (the bf16 weights, rounded
- *         up to 256), QMV_ERR_WORKSPACE otherwise; calls that share it must be
- *         ordered on one stream.  No K split: a token's result does not
- *         depend on m, and repeated calls are bit-identical.
+ *         F32/F16/BF16 rows; not QMV_MXFP4_R): the same product, bf16(w)
+ *         rounded once from w's fp32 value.  Q4_0, Q5_0, Q8_0 and Q6_K rows
+ *         of a whole number of 16 bytes (cols a multiple of 256, or of 2048
+ *         for Q6_K) are dequantised tile by tile into the tensor cores'
+ *         operand memory inside the GEMM (with the same two-K-halves rule as
+ *         Q4_K); BF16 rows are the operand as they are; the other types and
+ *         row lengths (Q4_1, Q5_1, Q8_1, MXFP4, Q2_K, Q3_K, Q5_K, F32, F16,
+ *         and e.g. Q8_0 with cols = 896) are converted to bf16 in the
+ *         workspace first, which needs qmv_workspace_size(QMV_OP_MATMUL, fmt,
+ *         rows, cols, m) bytes (rows*cols*2 rounded up to 256;
+ *         QMV_ERR_WORKSPACE otherwise; calls that share it must be ordered on
+ *         one stream).
  *         Any of these may be | QMV_FLAG_PDL (the W these kernels read must
  *         not be written by the kernels just before them on the stream).
  *   X   : 16-byte aligned.   Y : fp32 [m][rows], overwritten.
@@ -425,8 +428,9 @@ enum { QMV_OP_MATVEC = 1, QMV_OP_MATMUL = 2, QMV_OP_MOE = 3 };
  * bf16 activation rows, n*cols*2 bytes.  QMV_OP_MATMUL with
  * QMV_FMT(QMV_Q4_K, QMV_Q8_K), n = m tokens: the fp16 activation codes
  * (m*cols*2), sums of 16 (m*cols/8) and scales (about m*cols/64 bytes).
- * QMV_OP_MATMUL with QMV_FMT(t, QMV_BF16), t not Q4_K: the bf16 weights,
- * rows*cols*2 bytes rounded up to 256.  0 if the call needs none. */
+ * QMV_OP_MATMUL with QMV_FMT(t, QMV_BF16) converted in two passes (see
+ * qmv_matmul): the bf16 weights, rows*cols*2 bytes rounded up to 256.  0 if
+ * the call needs none. */
 size_t qmv_workspace_size(int op, int fmt, int64_t rows, int64_t cols, int64_t n);
 /* Register a caller-owned device buffer (256-byte aligned) as the workspace of
  * the current device; NULL/0 clears it.  The library keeps the pointer only. */

@@ -1,8 +1,10 @@
-"""GPU parity of the prefill product for every weight format without a fused
-tile dequantiser (all GGUF block types but Q4_K, and plain F32/F16/BF16 rows)
-with bf16 activations: one pass writes bf16(w) tiles into the workspace, a
-bf16 x bf16 tcgen05 GEMM multiplies them.  The oracle multiplies bf16(w), w
-rounded from its fp32 value, by the bf16 activations in fp64.  Bar:
+"""GPU parity of the prefill product for the weight formats other than Q4_K
+(Q4_0, Q5_0, Q8_0 and Q6_K rows of a whole number of 16 bytes dequantised
+tile by tile into TMEM inside a tcgen05 GEMM; BF16 rows multiplied as they
+are; the other types and row lengths converted to bf16 in the workspace
+first), with bf16 activations.  The oracle
+multiplies bf16(w), w rounded from its fp32 value, by the bf16 activations in
+fp64.  Bar:
 |Y - Y_oracle| <= 1e-4 * sum|bf16(w) x| for every output checked
 ("Architecture" page, "The two phases": prefill multiplies a whole prompt)."""
 import numpy as np
@@ -17,7 +19,19 @@ pytestmark = pytest.mark.gpu
 Q4_0, Q5_0, Q8_0, Q4_K, Q6_K, MXFP4, F32, BF16, MXFP4_R = 1, 2, 3, 4, 5, 6, 8, 9, 10
 Q4_1, Q5_1, Q8_1, Q2_K, Q3_K, Q5_K, F16 = 11, 12, 13, 14, 15, 16, 17
 TYPES = [Q4_0, Q5_0, Q8_0, Q6_K, MXFP4, Q4_1, Q5_1, Q8_1, Q2_K, Q3_K, Q5_K, F32, F16, BF16]
-K_TYPES = {Q6_K, Q2_K, Q3_K, Q5_K}
+BB = {Q4_0: (32, 18), Q5_0: (32, 22), Q8_0: (32, 34), Q6_K: (256, 210)}
+
+
+def two_pass(t, cols):
+    """Whether the product converts the weights to bf16 in the workspace first
+    (every type but Q4_K and BF16 rows, except Q4_0 / Q5_0 / Q8_0 / Q6_K rows of
+    a whole number of 16 bytes, which are dequantised inside the GEMM)."""
+    if t in (Q4_K, BF16):
+        return False
+    if t in BB:
+        bs, bb = BB[t]
+        return (cols // bs) * bb % 16 != 0
+    return True
 
 
 def bf16_x(m, cols, seed):
@@ -29,7 +43,7 @@ def bf16_x(m, cols, seed):
 def run(qmv, t, Wd, rows, cols, xb, m):
     Y = torch.full((m, rows), float("nan"), dtype=torch.float32, device="cuda")
     need = qmv.qmv_workspace_size(qmv.OP_MATMUL, qmv.FMT(t, BF16), rows, cols, m)
-    assert need >= rows * cols * 2
+    assert need == ((rows * cols * 2 + 255) // 256 * 256 if two_pass(t, cols) else 0)
     with workspace(qmv, need):
         qmv.qmv_matmul(qmv.FMT(t, BF16), Wd, rows, cols, xb.cuda(), Y, m)
         qmv.qmv_get_status()
@@ -46,30 +60,41 @@ def check(qmv, orc, t, rows, cols, m, seed):
 
 @pytest.mark.parametrize("t", TYPES)
 @pytest.mark.parametrize("rows,cols,m", [(130, 512, 300), (300, 768, 1), (256, 1024, 129)])
-def test_two_pass_parity(qmv, orc, t, rows, cols, m):
+def test_formats_parity(qmv, orc, t, rows, cols, m):
     """Ragged row tiles (130, 300), ragged token tiles (1, 129, 300), several
     128-k stages per tile; every output checked."""
     check(qmv, orc, t, rows, cols, m, 21)
 
 
-@pytest.mark.parametrize("t,cols", [(Q8_0, 32), (Q4_0, 96), (MXFP4, 160), (F32, 8), (BF16, 40), (F16, 1032),
-                                    (Q6_K, 256), (Q3_K, 1280)])
-def test_two_pass_ragged_k(qmv, orc, t, cols):
+@pytest.mark.parametrize("t,cols", [(Q8_0, 32), (Q4_0, 96), (Q5_0, 224), (Q8_0, 4064), (MXFP4, 160), (F32, 8),
+                                    (BF16, 40), (F16, 1032), (Q6_K, 256), (Q3_K, 1280)])
+def test_formats_ragged_k(qmv, orc, t, cols):
     """K that is not a multiple of the 128-k stage (and for the plain rows not
     of a 64-k box): the tensor maps fill the missing k with zeros."""
     check(qmv, orc, t, 200, cols, 77, 22)
 
 
-@pytest.mark.parametrize("t,rows,m", [(Q8_0, 9700, 500), (Q5_0, 19500, 200), (Q6_K, 4000, 1100)])
-def test_two_pass_many_tiles(qmv, orc, t, rows, m):
+@pytest.mark.parametrize("t,rows,cols,m", [(Q8_0, 9700, 256, 500), (Q5_0, 19500, 256, 200), (Q6_K, 4000, 256, 1100),
+                                           (Q6_K, 5000, 2048, 300), (Q4_0, 4000, 512, 1100)])
+def test_formats_many_tiles(qmv, orc, t, rows, cols, m):
     """More tiles than SMs with 256-token tiles (9700 x 500, 4000 x 1100) and
-    with 128-token tiles (19500 x 200), ragged in both directions."""
-    check(qmv, orc, t, rows, 256, m, 23)
+    with 128-token tiles (19500 x 200, 5000 x 300), ragged in both directions;
+    Q6_K both in two passes (256 k: 210-byte rows) and inside the GEMM."""
+    check(qmv, orc, t, rows, cols, m, 23)
+
+
+@pytest.mark.parametrize("t,rows,cols,m", [(Q6_K, 130, 2048, 300), (Q6_K, 300, 4096, 1), (Q6_K, 256, 6144, 129),
+                                           (Q8_0, 129, 2304, 257), (Q5_0, 257, 1280, 33), (Q4_0, 1, 256, 5)])
+def test_formats_fused_tiles(qmv, orc, t, rows, cols, m):
+    """The tile dequantisers inside the GEMM: Q6_K rows of whole 16 bytes
+    (cols a multiple of 2048; two A stages per super-block) and odd numbers of
+    128-k stages for the 32-element formats, ragged rows and tokens."""
+    check(qmv, orc, t, rows, cols, m, 29)
 
 
 @pytest.mark.parametrize("t,rows,cols,m", [(Q5_0, 4864, 896, 512), (Q8_0, 896, 4864, 512), (Q8_0, 151936, 896, 64),
                                            (Q5_0, 896, 896, 2048), (Q6_K, 4096, 14336, 512)])
-def test_two_pass_model_shapes_sampled(qmv, orc, t, rows, cols, m):
+def test_formats_model_shapes_sampled(qmv, orc, t, rows, cols, m):
     """Qwen2-0.5B-shaped matrices in its GGUF formats (the layers in Q5_0, the
     vocabulary projection in Q8_0: 896 is not a multiple of the 256-element
     K-quant super-block) and a 14336-wide Q6_K down projection: 40 sampled rows
@@ -86,9 +111,9 @@ def test_two_pass_model_shapes_sampled(qmv, orc, t, rows, cols, m):
     assert_close(Y[np.ix_(toks, rids)], yref, yabs, what=f"type {t} {rows}x{cols} m={m}")
 
 
-def test_two_pass_deterministic_and_token_independent(qmv):
+def test_formats_deterministic_and_token_independent(qmv):
     """Repeated calls are bit-identical, and a token's outputs do not depend on
-    how many tokens share the call (no split of K, one accumulation order)."""
+    how many tokens share the call (one accumulation order per output)."""
     rows, cols, m = 1000, 1536, 300
     Wd = dev(synth.weights(Q5_0, rows, cols, seed=25))
     xb, _ = bf16_x(m, cols, 25)
@@ -100,7 +125,25 @@ def test_two_pass_deterministic_and_token_independent(qmv):
         assert np.array_equal(part.view(np.uint32), Y[t0:t0 + n].view(np.uint32))
 
 
-def test_two_pass_equals_rowwise_decode(qmv, orc):
+@pytest.mark.parametrize("t,rows,cols,m", [(Q8_0, 200, 8192, 300), (Q6_K, 96, 16384, 1), (Q5_0, 1024, 8704, 77)])
+def test_formats_k_split(qmv, orc, t, rows, cols, m):
+    """Rows much shorter than K (cols >= 8192 and >= 2 rows, an even number of
+    raw stages) run as two K halves that add into a zeroed Y: every output
+    checked, repeated calls bit-identical, and the last token's outputs the same
+    when it is multiplied alone (the split follows the weight's shape)."""
+    W = synth.weights(t, rows, cols, seed=28, tensor_id=rows + cols)
+    Wd = dev(W)
+    xb, xbits = bf16_x(m, cols, 28)
+    Y = run(qmv, t, Wd, rows, cols, xb, m)
+    yref, yabs = orc.matvec(orc_t(t), BF16, W, rows, cols, xbits, m)
+    assert_close(Y, yref, yabs, what=f"type {t} {rows}x{cols} m={m}")
+    for _ in range(2):
+        assert np.array_equal(run(qmv, t, Wd, rows, cols, xb, m).view(np.uint32), Y.view(np.uint32))
+    one = run(qmv, t, Wd, rows, cols, xb[m - 1:m], 1)
+    assert np.array_equal(one[0].view(np.uint32), Y[m - 1].view(np.uint32))
+
+
+def test_formats_equals_rowwise_decode(qmv, orc):
     """Prefill against sequential fp32 decode of the same bf16 token values: the
     GEMM multiplies bf16-rounded weights and the A32 matvec exact ones, so they
     differ by at most the weight rounding, 2^-9 * sum|w x| (plus fp32 noise)."""
@@ -118,7 +161,7 @@ def test_two_pass_equals_rowwise_decode(qmv, orc):
     assert (np.abs(Y - yv) <= (2.0 ** -9 + 2e-6) * yabs).all()
 
 
-def test_two_pass_edge_cases_and_refusals(qmv):
+def test_formats_edge_cases_and_refusals(qmv):
     rows, cols = 128, 256
     W = dev(synth.weights(Q8_0, rows, cols, seed=27))
     Y = torch.full((1, rows), 5.0, device="cuda")
@@ -129,13 +172,15 @@ def test_two_pass_edge_cases_and_refusals(qmv):
     assert (host(Y) == 5).all()
     # zero activations give exact zeros
     assert (run(qmv, Q8_0, W, rows, cols, torch.zeros((3, cols), dtype=torch.bfloat16), 3) == 0).all()
-    # no workspace, or too little, is refused before any launch
+    # F32 / F16 rows without workspace, or with too little, are refused
+    # before any launch; block types and BF16 rows need none
+    Wf32 = dev(synth.weights(F32, rows, cols, seed=27))
     with pytest.raises(qmv.QmvError) as e:
-        qmv.qmv_matmul(qmv.FMT(Q8_0, BF16), W, rows, cols, x1, Y, 1)
+        qmv.qmv_matmul(qmv.FMT(F32, BF16), Wf32, rows, cols, x1, Y, 1)
     assert e.value.code == qmv.ERR_WORKSPACE
     with workspace(qmv, rows * cols * 2 - 512):
         with pytest.raises(qmv.QmvError) as e:
-            qmv.qmv_matmul(qmv.FMT(Q8_0, BF16), W, rows, cols, x1, Y, 1)
+            qmv.qmv_matmul(qmv.FMT(F32, BF16), Wf32, rows, cols, x1, Y, 1)
         assert e.value.code == qmv.ERR_WORKSPACE
     with workspace(qmv, 1 << 20):
         # plain rows must be 16-byte rows of bf16 tiles: cols a multiple of 8
@@ -150,6 +195,11 @@ def test_two_pass_edge_cases_and_refusals(qmv):
             with pytest.raises(qmv.QmvError) as e:
                 qmv.qmv_matmul(fmt, W, rows, cols, x1, Y, 1)
             assert e.value.code == qmv.ERR_UNSUPPORTED
-    assert qmv.qmv_workspace_size(qmv.OP_MATMUL, qmv.FMT(Q8_0, BF16), rows, cols, 1) >= rows * cols * 2
-    assert qmv.qmv_workspace_size(qmv.OP_MATMUL, qmv.FMT(Q4_K, BF16), rows, cols, 1) == 0
+    assert qmv.qmv_workspace_size(qmv.OP_MATMUL, qmv.FMT(F16, BF16), rows, cols, 1) == rows * cols * 2
+    for t in (Q4_0, Q5_0, Q8_0, BF16, Q4_K):
+        assert qmv.qmv_workspace_size(qmv.OP_MATMUL, qmv.FMT(t, BF16), rows, cols, 1) == 0
+    for t in (Q4_1, MXFP4, Q5_K, Q6_K):   # Q6_K: 256 k = 210 bytes per row
+        assert qmv.qmv_workspace_size(qmv.OP_MATMUL, qmv.FMT(t, BF16), rows, cols, 1) == rows * cols * 2
+    assert qmv.qmv_workspace_size(qmv.OP_MATMUL, qmv.FMT(Q6_K, BF16), rows, 2048, 1) == 0
+    assert qmv.qmv_workspace_size(qmv.OP_MATMUL, qmv.FMT(Q8_0, BF16), rows, 896, 1) == rows * 896 * 2
     qmv.qmv_get_status()
