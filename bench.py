@@ -551,10 +551,11 @@ def prefill_leg(q, torch, stream, tflops_peak):
         del Ws
     q.qmv_get_status(stream)
     agg = {k: tot[k][0] / (tot[k][1] / 1e3) / 1e12 for k in tot}
+    formats = prefill_formats(q, torch, stream, tflops_peak)
     return {"metric": "prefill GEMM TFLOP/s (Q4_K weights; bf16 and W4A8 activations, fp32 accumulate)",
             "unit": "TFLOP/s", "value": agg["bf16"], "frac": agg["bf16"] / tflops_peak,
             "w4a8_value": agg["w4a8"], "w4a8_frac": agg["w4a8"] / tflops_peak, "peak": tflops_peak,
-            "shapes": out["bf16"], "w4a8": out["w4a8"],
+            "shapes": out["bf16"], "w4a8": out["w4a8"], "formats": formats,
             "kernels": {"bf16": "k_gemm_q4k_bf16 (tcgen05.mma kind::f16 bf16, M=128 rows x N=256 tokens, A in TMEM)",
                         "w4a8": "k_w4a8_prep + k_gemm_q4k_w4a8 (tcgen05.mma kind::f16 on fp16 integer operands, "
                                 "M=128 x N=128, S and Mn drained per super-block)"}}
@@ -666,6 +667,40 @@ def block_time(q, torch, stream, fmt, Wgu, Wd, bgu, bd, Wr, br, n_tok, hbm, E=32
     wbytes = float(np.mean(used)) * (2 * inter + hidden) * synth.row_bytes(MXFP4, hidden)
     return {"ms": ms, "experts_used": float(np.mean(used)), "weight_gbs": wbytes / (ms / 1e3) / 1e9,
             "frac_of_hbm": wbytes / (ms / 1e3) / 1e9 / hbm}
+
+
+def prefill_formats(q, torch, stream, tflops_peak):
+    """The prefill product for the other formats of the pages' prefill mix (and
+    Q4_0) on the same shapes, bf16 activations: Q4_0 / Q5_0 / Q8_0 / Q6_K rows of
+    whole 16 bytes dequantise tiles into TMEM inside the GEMM (k_gemm_deq_bf16);
+    the Qwen2-0.5B layer shapes whose rows are not (896 columns: 616-byte Q5_0
+    rows) convert to bf16 in the workspace first (k_dequant_bf16 + k_gemm_bf16),
+    timed whole.  Four (W, X) copies rotate, as for Q4_K."""
+    out = {}
+    cases = [(t, rows, cols, m) for t in (Q8_0, Q5_0, Q6_K, Q4_0) for rows, cols in ((14336, 4096), (4096, 14336))
+             for m in (512, 2048)] + [(Q5_0, 4864, 896, 512), (Q5_0, 896, 4864, 512)]
+    names = {Q4_0: "Q4_0", Q5_0: "Q5_0", Q8_0: "Q8_0", Q6_K: "Q6_K"}
+    ws = None
+    for t, rows, cols, m in cases:
+        flop = 2.0 * m * rows * cols
+        Ws = [torch.from_numpy(synth.weights(t, rows, cols, seed=4, tensor_id=rows + i)).cuda() for i in range(4)]
+        Xs = [torch.randn(m, cols, device="cuda").to(torch.bfloat16) for _ in range(4)]
+        Y = torch.empty(m, rows, device="cuda")
+        need = q.qmv_workspace_size(q.OP_MATMUL, q.FMT(t, BF16), rows, cols, m)
+        if need and (ws is None or ws.numel() < need):
+            ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+        if need:
+            q.qmv_set_workspace(ws, ws.numel())
+        calls = [(lambda s, W=W, X=X: q.qmv_matmul(q.FMT(t, BF16), W, rows, cols, X, Y, m, s.cuda_stream))
+                 for W, X in zip(Ws, Xs)]
+        ms = time_rotating(torch, stream, calls, 40)
+        q.qmv_set_workspace(None, 0)
+        out[f"{names[t]}_{rows}x{cols}_m{m}"] = {
+            "ms": ms, "tflops": flop / (ms / 1e3) / 1e12, "frac_of_peak": flop / (ms / 1e3) / 1e12 / tflops_peak,
+            "path": "two passes (bf16 in the workspace)" if need else "tiles dequantised inside the GEMM"}
+        del Ws, Xs, Y
+    q.qmv_get_status(stream)
+    return out
 
 
 def run_probe(spec):
