@@ -78,9 +78,8 @@ constexpr int MX_SPITCH_MAX = 128;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t A_STAGE_COLS = KSUB * BK / 2;   // bf16 A stage: 128 rows x 128 k, two per column
 constexpr uint32_t A_STAGE_COLS_MX = 32;           // E2M1 A stage: four byte-container codes per column
-// Per variant: TBN tokens per tile (the bf16 form 128; the MX form 128 or, when
-// experts average more than 96 routed tokens, 192 so that one tile covers them),
-// SKV k stages.  TMEM columns: two TBN-column fp32 accumulators, then SKV A
+// Per variant: TBN tokens per tile (128 or, when experts average more than 96
+// routed tokens, 192 so that one tile covers them), SKV k stages.  TMEM columns: two TBN-column fp32 accumulators, then SKV A
 // stages; MX adds per stage four columns of weight scales and TBN/32 of token
 // scales.  Weight row m's scale for K step j of a stage sits in lane m, column
 // SFA + m/32, byte j; token n's in lane 32q + n % 32, column SFB + n/32, byte j,
@@ -95,9 +94,12 @@ struct RawCfg {
     // scales in every TMEM lane quarter (the last four)
     static constexpr int THREADS = (PLANAR ? 768 : 896) + (MX ? 128 : 0);
     static constexpr int SF_WARP0 = THREADS / 32 - 4;
-    static constexpr int SKV = TBN > 128 ? 3 : SK;
-    static constexpr int XB = MX ? TBN * 128 : X_BYTES;                   // bytes of one X box
-    static constexpr int XS = MX ? XB : KSUB * X_BYTES;                   // X bytes per 128-k stage
+    // 192-token tiles: three k stages (MX) or two (bf16, whose 64-column A
+    // stages leave room for two next to two 192-column accumulators)
+    static constexpr int SKV = TBN > 128 ? (MX ? 3 : 2) : SK;
+    static constexpr int XBF = TBN * BK * 2;                              // bf16: bytes of one 64-k X box
+    static constexpr int XB = MX ? TBN * 128 : XBF;                       // bytes of one X box
+    static constexpr int XS = MX ? XB : KSUB * XBF;                       // X bytes per 128-k stage
     static constexpr int SFBUF = TBN * MX_SPITCH_MAX;
     static constexpr int OFF_R = OFF_X + SKV * XS;
     static constexpr int OFF_SF = OFF_R + SR * R_BYTES;
@@ -108,7 +110,6 @@ struct RawCfg {
     static constexpr uint32_t SFA_COL = A_COL + SKV * A_STAGE_COLS_MX;
     static constexpr uint32_t SFB_COL = SFA_COL + SKV * 4;
     static_assert(SMEM <= 227 * 1024, "shared memory");
-    static_assert(MX || TBN == 128, "the bf16 form uses 128-token tiles");
     static_assert(A_COL + SKV * (MX ? A_STAGE_COLS_MX : A_STAGE_COLS) + (MX ? SKV * (4 + TBN / 32) : 0) <= TMEM_COLS,
                   "TMEM budget");
 };
@@ -494,10 +495,10 @@ __global__ void __launch_bounds__(mg::RawCfg<PLANAR, MX, TBN>::THREADS, 1)
                 const int row0 = a.offsets[e] + nt * BN;
                 for (int ks = 0; ks < nks; ++ks) {
                     if (!mbar_wait_backoff(&empty[s], ph, a.status, 128)) { fail(); break; }
-                    mbar_arrive_expect_tx(&full[s], KSUB * X_BYTES);
+                    mbar_arrive_expect_tx(&full[s], KSUB * RC::XBF);
 #pragma unroll
                     for (int j = 0; j < KSUB; ++j)
-                        tma_load_2d(smem + OFF_X + s * XS + j * X_BYTES, &tmX, (ks * KSUB + j) * BK, row0, &full[s]);
+                        tma_load_2d(smem + OFF_X + s * XS + j * RC::XBF, &tmX, (ks * KSUB + j) * BK, row0, &full[s]);
                     if (++s == SK) { s = 0; ph ^= 1; }
                 }
             }
@@ -591,7 +592,7 @@ __global__ void __launch_bounds__(mg::RawCfg<PLANAR, MX, TBN>::THREADS, 1)
                         const uint32_t at = tmem + A_COL + s * A_STAGE_COLS;
 #pragma unroll
                         for (int j = 0; j < KSUB; ++j) {
-                            const uint64_t bdesc = smem_desc_sw128(smem + OFF_X + s * XS + j * X_BYTES);
+                            const uint64_t bdesc = smem_desc_sw128(smem + OFF_X + s * XS + j * RC::XBF);
 #pragma unroll
                             for (int k4 = 0; k4 < BK / 16; ++k4)   // A: 8 TMEM columns, B: 32 bytes per K = 16 step
                                 mma_f16_ts(d, at + 32 * j + 8 * k4, bdesc + 2 * k4, idesc, (ks | j | k4) != 0);
@@ -792,9 +793,10 @@ int qmv_launch_moe_gemm_mxfp4(const void* W3d, bool planar, bool mx, int n_exper
     int* tiles = static_cast<int*>(ws);
     uint8_t* act = static_cast<uint8_t*>(ws) + tiles_bytes(n_pairs);
     uint8_t* sf = act + r256g((size_t)n_pairs * (size_t)cols);
-    // MX: 192-token tiles when the experts average more than 96 routed pairs, so
-    // that one tile pass over an expert's rows covers its tokens
-    const int tbn = (mx && n_pairs > (int64_t)96 * n_expert) ? 192 : 128;
+    // 192-token tiles when the experts average more than 96 routed pairs, so
+    // that one tile pass over an expert's rows (one dequantisation of them)
+    // covers its tokens
+    const int tbn = n_pairs > (int64_t)96 * n_expert ? 192 : 128;
     k_moe_tiles<<<1, 32, 0, st>>>(offsets, active, tbn, tiles);
     CUtensorMap tmX, tmC, tmE;
     if (mx) {
@@ -812,7 +814,7 @@ int qmv_launch_moe_gemm_mxfp4(const void* W3d, bool planar, bool mx, int n_exper
                                                                       n_expert, kdiv, (int)cols, Xs);
         if (cudaGetLastError() != cudaSuccess) return -6;
         if (!make_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Xs, (uint64_t)cols, (uint64_t)n_pairs,
-                          (uint64_t)cols * 2, mg::BK, mg::BN, CU_TENSOR_MAP_SWIZZLE_128B))
+                          (uint64_t)cols * 2, mg::BK, (uint32_t)tbn, CU_TENSOR_MAP_SWIZZLE_128B))
             return -8;
     }
     MoeGemmArgs a;
@@ -848,13 +850,19 @@ int qmv_launch_moe_gemm_mxfp4(const void* W3d, bool planar, bool mx, int n_exper
     };
     using mg::RawCfg;
     if (planar) {
-        if (!mx) return launch(&k_moe_gemm_mxfp4<true, false, 128>, RawCfg<true>::THREADS, RawCfg<true>::SMEM);
+        if (!mx)
+            return tbn == 192 ? launch(&k_moe_gemm_mxfp4<true, false, 192>, RawCfg<true, false, 192>::THREADS,
+                                       RawCfg<true, false, 192>::SMEM)
+                              : launch(&k_moe_gemm_mxfp4<true, false, 128>, RawCfg<true>::THREADS, RawCfg<true>::SMEM);
         return tbn == 192
                    ? launch(&k_moe_gemm_mxfp4<true, true, 192>, RawCfg<true, true, 192>::THREADS,
                             RawCfg<true, true, 192>::SMEM)
                    : launch(&k_moe_gemm_mxfp4<true, true, 128>, RawCfg<true, true>::THREADS, RawCfg<true, true>::SMEM);
     }
-    if (!mx) return launch(&k_moe_gemm_mxfp4<false, false, 128>, RawCfg<false>::THREADS, RawCfg<false>::SMEM);
+    if (!mx)
+        return tbn == 192 ? launch(&k_moe_gemm_mxfp4<false, false, 192>, RawCfg<false, false, 192>::THREADS,
+                                   RawCfg<false, false, 192>::SMEM)
+                          : launch(&k_moe_gemm_mxfp4<false, false, 128>, RawCfg<false>::THREADS, RawCfg<false>::SMEM);
     return tbn == 192 ? launch(&k_moe_gemm_mxfp4<false, true, 192>, RawCfg<false, true, 192>::THREADS,
                                RawCfg<false, true, 192>::SMEM)
                       : launch(&k_moe_gemm_mxfp4<false, true, 128>, RawCfg<false, true>::THREADS,
