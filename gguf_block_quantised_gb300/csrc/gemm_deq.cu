@@ -491,10 +491,11 @@ static int launch_gemm_deq_t(const void* W, int64_t rows, int64_t cols, const vo
     // of raw stages each), as in the Q4_K GEMM; the split follows the shape
     const int nrs_all = (a.nb + C::BPR - 1) / C::BPR;
     a.ks = (cols >= 8192 && cols >= 2 * rows && nrs_all % 2 == 0) ? 2 : 1;
+    // 256-token tiles unless they cannot give half of the SMs a work item (a
+    // tile's cost is mostly dequantising its weight rows: partly empty 256-token
+    // tiles beat twice as many 128-token ones)
     const int64_t n_rt = (rows + gd::BM - 1) / gd::BM;
-    const int64_t pad256 = (m + 255) / 256 * 256, pad128 = (m + 127) / 128 * 128;
-    const bool narrow = n_rt * ((m + 255) / 256) * a.ks < (int64_t)num_sms() / (a.ks == 2 ? 2 : 1) ||
-                        pad256 * 100 > pad128 * 108;
+    const bool narrow = n_rt * ((m + 255) / 256) * a.ks < (int64_t)num_sms() / (a.ks == 2 ? 2 : 1);
     const int BN = narrow ? 128 : 256;
     CUtensorMap tmX, tmW;
     if (!make_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, (uint64_t)cols, (uint64_t)m, (uint64_t)cols * 2,

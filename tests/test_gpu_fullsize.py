@@ -3,8 +3,8 @@
 The sampled-row tests elsewhere reach every code path on small shapes; these
 compare whole outputs at the model shapes the bench runs -- the Qwen2.5-0.5B
 lm_head (151936 x 896 Q8_0) and layer matrices, the Llama-3-8B K-quant
-shapes at 16 vectors, the prefill GEMM at 14336 x 4096 with 512 tokens (bf16
-and W4A8), and the gpt-oss-20B experts at 64 tokens on both MoE paths -- so a
+shapes at 16 vectors, the prefill GEMM at 14336 x 4096 with 512 tokens (Q4_K
+with bf16 and W4A8 activations, Q8_0 and Q6_K with bf16), and the gpt-oss-20B experts at 64 tokens on both MoE paths -- so a
 fault confined to one tile, K-chunk or expert deep inside a large launch
 cannot pass.  The oracle runs on every host core (rows or tokens split over
 spawned processes, tests/oracle_pool.py).
@@ -62,11 +62,13 @@ def test_kquant_whole_16_vectors(qmv, orc, t, rows, cols):
     assert_close(y, yref, yabs, what=f"t={t} {rows}x{cols} n_vec=16")
 
 
-@pytest.mark.parametrize("at", [BF16, Q8_K], ids=["bf16", "w4a8"])
-def test_prefill_whole_14336x4096_m512(qmv, orc, at):
-    """The prefill GEMM on Q4_K 14336 x 4096 with 512 tokens, every output."""
+@pytest.mark.parametrize("t,at", [(Q4_K, BF16), (Q4_K, Q8_K), (Q8_0, BF16), (Q6_K, BF16)],
+                         ids=["bf16", "w4a8", "q8_0_bf16", "q6_k_bf16"])
+def test_prefill_whole_14336x4096_m512(qmv, orc, t, at):
+    """The prefill GEMM on 14336 x 4096 with 512 tokens, every output: Q4_K with
+    bf16 and Q8_K activations, and Q8_0 / Q6_K tiles dequantised inside the GEMM."""
     rows, cols, m = 14336, 4096, 512
-    W = synth.weights(Q4_K, rows, cols, seed=14, tensor_id=1)
+    W = synth.weights(t, rows, cols, seed=14, tensor_id=1)
     x = synth.activations(m, cols, seed=14)
     if at == BF16:
         xb = torch.from_numpy(x).to(torch.bfloat16)
@@ -75,11 +77,11 @@ def test_prefill_whole_14336x4096_m512(qmv, orc, at):
         x_o = orc.quantize_act(Q8_K, x)
         X = dev(x_o)
     Y = torch.full((m, rows), float("nan"), dtype=torch.float32, device="cuda")
-    with workspace(qmv, qmv.qmv_workspace_size(qmv.OP_MATMUL, qmv.FMT(Q4_K, at), rows, cols, m)):
-        qmv.qmv_matmul(qmv.FMT(Q4_K, at), dev(W), rows, cols, X, Y, m)
+    with workspace(qmv, qmv.qmv_workspace_size(qmv.OP_MATMUL, qmv.FMT(t, at), rows, cols, m)):
+        qmv.qmv_matmul(qmv.FMT(t, at), dev(W), rows, cols, X, Y, m)
         qmv.qmv_get_status()
-    yref, yabs = OP.matvec(Q4_K, at, W, rows, cols, x_o, m)
-    assert_close(host(Y), yref, yabs, what=f"prefill at={at}")
+    yref, yabs = OP.matvec(t, at, W, rows, cols, x_o, m)
+    assert_close(host(Y), yref, yabs, what=f"prefill t={t} at={at}")
 
 
 @pytest.mark.parametrize("path", ["w4a8", "bf16", "bf16_repacked"])

@@ -59,12 +59,13 @@ def test_matmul_k_split_parity(qmv, orc, rows, cols, m):
     qmv.qmv_get_status()
 
 
-@pytest.mark.parametrize("rows,m", [(9700, 500), (19500, 200)])
+@pytest.mark.parametrize("rows,m", [(9700, 500), (19500, 200), (9600, 300)])
 def test_matmul_many_tiles_parity(qmv, orc, rows, m):
-    """Enough row tiles that every SM gets at least one: 256-token tiles (the
-    wide tile of the large prefill shapes; 9700 x 500) and several 128-token
-    tiles per SM (19500 x 200), each with a ragged last row tile and a ragged
-    last token tile; every output checked."""
+    """More tiles than SMs: 256-token tiles (the wide tile of the large prefill
+    shapes; 9700 x 500, and 19500 x 200 in partly empty 256-token tiles) and
+    128-token tiles with two per CTA on some SMs (9600 x 300: 75 row tiles give
+    fewer than one 256-token tile per SM, so 225 tiles of 128 tokens), each with a
+    ragged last row tile and a ragged last token tile; every output checked."""
     cols = 256
     W = synth.weights(Q4_K, rows, cols, seed=8, tensor_id=rows)
     xb, xbits = bf16_x(m, cols, 8)

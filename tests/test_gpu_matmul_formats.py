@@ -74,12 +74,13 @@ def test_formats_ragged_k(qmv, orc, t, cols):
     check(qmv, orc, t, 200, cols, 77, 22)
 
 
-@pytest.mark.parametrize("t,rows,cols,m", [(Q8_0, 9700, 256, 500), (Q5_0, 19500, 256, 200), (Q6_K, 4000, 256, 1100),
-                                           (Q6_K, 5000, 2048, 300), (Q4_0, 4000, 512, 1100)])
+@pytest.mark.parametrize("t,rows,cols,m", [(Q8_0, 9700, 256, 500), (Q5_0, 19500, 256, 200), (Q5_0, 9600, 256, 300),
+                                           (Q6_K, 4000, 256, 1100), (Q6_K, 5000, 2048, 300), (Q4_0, 4000, 512, 1100)])
 def test_formats_many_tiles(qmv, orc, t, rows, cols, m):
-    """More tiles than SMs with 256-token tiles (9700 x 500, 4000 x 1100) and
-    with 128-token tiles (19500 x 200, 5000 x 300), ragged in both directions;
-    Q6_K both in two passes (256 k: 210-byte rows) and inside the GEMM."""
+    """More tiles than SMs with 256-token tiles (9700 x 500, 19500 x 200,
+    4000 x 1100) and with 128-token tiles (9600 x 300: 225 tiles, two on some
+    CTAs; 5000 x 300), ragged in both directions; Q6_K both in two passes
+    (256 k: 210-byte rows) and inside the GEMM."""
     check(qmv, orc, t, rows, cols, m, 23)
 
 
