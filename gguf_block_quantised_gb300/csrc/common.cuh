@@ -154,6 +154,28 @@ __device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity
     }
 }
 
+// ---- thread-block clusters: distributed shared memory and the barrier --------
+// The address of this shared-memory location in the CTA of the cluster with
+// rank `rank` (the same offset in its shared memory).
+__device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank)
+{
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+    return a;
+}
+
+__device__ __forceinline__ void dsmem_st_u32(uint32_t a, uint32_t v)
+{
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+
+// All threads of all CTAs of the cluster; the stores before it (also into
+// other CTAs' shared memory) are visible to every thread of the cluster after.
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // ---- bulk copy global -> shared (TMA, 1-D) ------------------------------------
 // dst and src 16-byte aligned, bytes a multiple of 16.  Completion is signalled
 // as transaction bytes on `bar`.

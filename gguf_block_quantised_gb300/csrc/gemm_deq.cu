@@ -25,8 +25,9 @@
 // A raw stage is 128 k of the 32-element formats (4 blocks per row) or one
 // 256-k super-block (two A stages).  Rows whose byte length is not a multiple
 // of 16 are not taken here (the caller converts them in two passes).  Blocks past the end of a row (cols not a
-// multiple of 128) decode as zeros.  Rows much shorter than K run as two K
-// halves that add into a zeroed Y, as in the Q4_K GEMM.  Every mbarrier wait is
+// multiple of 128) decode as zeros.  Rows much shorter than K run as 2 or 4 K
+// parts on the CTAs of a thread-block cluster, whose partial tiles are summed
+// in part order through distributed shared memory.  Every mbarrier wait is
 // bounded; on a timeout the kernel flags the status word, unwinds and frees
 // its TMEM.
 #include <cuda.h>
@@ -85,7 +86,9 @@ struct GemmDeqArgs {
     int m;                // tokens
     float* Y;             // [m][rows]
     unsigned* status;
-    int ks;               // K parts: 1 or 2
+    int ks;               // K parts: 1, 2 (adding into a zeroed Y) or 4 (a cluster, one tile per CTA)
+    int cluster;          // 1: the K parts are the CTAs of a cluster, reduced through its shared memory
+    int nrs_all;          // raw stages of a whole row
 };
 
 // NC 16-byte chunks of shared memory from p (16-byte aligned) as 4*NC words;
@@ -287,8 +290,10 @@ __global__ void __launch_bounds__(gd::THREADS, 1)
     const int n_rt = (int)((a.rows + BM - 1) / BM);
     const int n_nt = (a.m + BN - 1) / BN;
     const int n_tiles = n_rt * n_nt * a.ks;
-    const int nrs = (a.nb + C::BPR - 1) / C::BPR / a.ks;   // raw stages per work item
-    const int nks = nrs * C::AST;                          // k stages per work item
+    // work item t: tile t / ks, K part t % ks (with a cluster: the CTA's rank in
+    // it, the grid one item per CTA); part p takes raw stages
+    // [p * nrs_all / ks, (p + 1) * nrs_all / ks)
+    auto rs_begin = [&](int part) { return part * a.nrs_all / a.ks; };
 
     if (tid == 0) {
         for (int i = 0; i < SK; ++i) { mbar_init(&full[i], DEQ_WARPS + 1); mbar_init(&empty[i], 1); }
@@ -318,7 +323,8 @@ __global__ void __launch_bounds__(gd::THREADS, 1)
             int s = 0;
             uint32_t ph = 1;
             for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x) {
-                const int nt = t / a.ks / n_rt, k0 = (t % a.ks) * nks;
+                const int nt = t / a.ks / n_rt, part = t % a.ks;
+                const int k0 = rs_begin(part) * C::AST, nks = (rs_begin(part + 1) - rs_begin(part)) * C::AST;
                 for (int ks = 0; ks < nks; ++ks) {
                     if (!mbar_wait_backoff(&empty[s], ph, a.status, 64)) { fail(); break; }
                     mbar_arrive_expect_tx(&full[s], KSUB * X_BYTES);
@@ -338,8 +344,8 @@ __global__ void __launch_bounds__(gd::THREADS, 1)
             for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x) {
                 const int rt = (t / a.ks) % n_rt, part = t % a.ks;
                 bool bad = false;
-                for (int rs = 0; rs < nrs; ++rs) {
-                    const int kb = (part * nrs + rs) * C::BPR;
+                for (int rs = rs_begin(part); rs < rs_begin(part + 1); ++rs) {
+                    const int kb = rs * C::BPR;
                     if (!mbar_wait_backoff(&re[sr], ph, a.status, 64)) { bad = true; break; }
                     mbar_arrive_expect_tx(&rf[sr], BM * C::BOXW);
                     tma_load_2d(smem + OFF_R + sr * C::R_BYTES, &tmW, (kb * F::BB) & ~15, rt * BM, &rf[sr]);
@@ -361,6 +367,7 @@ __global__ void __launch_bounds__(gd::THREADS, 1)
                 if (!mbar_wait_bounded(&acce[buf], (use & 1) ^ 1, a.status)) { fail(); break; }
                 tc_fence_after();
                 const uint32_t d = tmem + buf * BN;
+                const int part = t % a.ks, nks = (rs_begin(part + 1) - rs_begin(part)) * C::AST;
                 bool bad = false;
                 for (int ks = 0; ks < nks; ++ks) {
                     if (!mbar_wait_bounded(&full[s], pf, a.status)) { bad = true; break; }
@@ -390,8 +397,8 @@ __global__ void __launch_bounds__(gd::THREADS, 1)
         for (int t = blockIdx.x; t < n_tiles && !__any_sync(0xffffffffu, *abort_flag); t += gridDim.x) {
             const int part = t % a.ks;
             bool bad = false;
-            for (int rs = 0; rs < nrs && !bad; ++rs) {
-                const int kb = (part * nrs + rs) * C::BPR;
+            for (int rs = rs_begin(part); rs < rs_begin(part + 1) && !bad; ++rs) {
+                const int kb = rs * C::BPR;
                 const int nblk = min(C::BPR, a.nb - kb);
                 if (!__all_sync(0xffffffffu, mbar_wait_bounded(&rf[sr], prf, a.status))) { bad = true; break; }
                 // rows past the end of the matrix read the box's zero fill, never stored
@@ -427,6 +434,7 @@ __global__ void __launch_bounds__(gd::THREADS, 1)
             // warp-uniform: every lane must take part in the tcgen05.ld below
             if (!__all_sync(0xffffffffu, mbar_wait_bounded(&accf[buf], use & 1, a.status))) { fail(); break; }
             tc_fence_after();
+            if (a.cluster) break;   // a K part: reduced through the cluster below
             const int64_t row = (int64_t)rt * BM + 32 * q + lane;
             const bool row_ok = row < a.rows;
             const int c0 = ch * BN / 2, nr = BN / 64;
@@ -465,6 +473,55 @@ __global__ void __launch_bounds__(gd::THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
+    if (a.cluster) {
+        // K parts of one tile, one per CTA of the cluster: each lane quarter of
+        // the tile (32 rows) has an owner CTA (quarter q -> rank q * ks / 4),
+        // which gathers the ks partial sums of its quarters in its X stage area
+        // as [quarter][part][column][row] fp32 and adds them in part order:
+        // ((p0 + p1) + p2) + p3, the same bits whichever part finishes first.
+        // The first cluster barrier orders every CTA's last MMA before the
+        // others' stores into its X area; the second, the stores before the sums.
+        cluster_sync();
+        const int t = blockIdx.x, part = t % a.ks;
+        const int rt = (t / a.ks) % n_rt, nt = t / a.ks / n_rt;
+        const int qpr = 4 / a.ks;   // lane quarters per owner
+        float* red = reinterpret_cast<float*>(smem);
+        if (warp >= EPI_WARP0) {
+            const int q = warp & 3, ch = (warp - EPI_WARP0) >> 2;
+            const uint32_t owner = (uint32_t)(q / qpr), qo = (uint32_t)(q % qpr);
+            tc_fence_after();
+            const int c0 = ch * BN / 2, nr = BN / 64;
+            for (int rd = 0; rd < nr; ++rd) {
+                uint32_t v0[16], v1[16];
+                const uint32_t tc = tmem + ((uint32_t)(32 * q) << 16) + c0 + rd * 32;
+                tmem_ld16_async(tc, v0);
+                tmem_ld16_async(tc + 16, v1);
+                tmem_wait_ld();
+                const int col0 = c0 + rd * 32;
+                float* dst = red + ((size_t)(qo * a.ks + part) * BN + col0) * 32 + lane;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    dsmem_st_u32(dsmem_addr(dst + 32 * i, owner), v0[i]);
+                    dsmem_st_u32(dsmem_addr(dst + 32 * (16 + i), owner), v1[i]);
+                }
+            }
+        }
+        cluster_sync();
+        if (warp >= EPI_WARP0) {
+            const int rank = part;
+            for (int idx = warp - EPI_WARP0; idx < qpr * BN; idx += EPI_WARPS) {
+                const int qo = idx / BN, col = idx % BN;
+                const int64_t row = (int64_t)rt * BM + 32 * (rank * qpr + qo) + lane;
+                const int tok = nt * BN + col;
+                const float* src = red + ((size_t)(qo * a.ks) * BN + col) * 32 + lane;
+                float sum = src[0];
+                for (int p = 1; p < a.ks; ++p) sum += src[(size_t)p * BN * 32];
+                if (row < a.rows && tok < a.m) a.Y[(int64_t)tok * a.rows + row] = sum;
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+    }
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
@@ -489,13 +546,27 @@ static int launch_gemm_deq_t(const void* W, int64_t rows, int64_t cols, const vo
     a.status = status_word();
     // rows much shorter than K: two K halves on different SMs (a whole number
     // of raw stages each), as in the Q4_K GEMM; the split follows the shape
-    const int nrs_all = (a.nb + C::BPR - 1) / C::BPR;
-    a.ks = (cols >= 8192 && cols >= 2 * rows && nrs_all % 2 == 0) ? 2 : 1;
+    a.nrs_all = (a.nb + C::BPR - 1) / C::BPR;
+    const int64_t n_rt = (rows + gd::BM - 1) / gd::BM;
+    // Rows much shorter than K run as K parts; the split follows the weight's
+    // shape alone, so a token's summation order does not depend on m.  Few row
+    // tiles (four parts stay within half of the SMs) and at least 16 raw stages:
+    // four parts on the CTAs of a cluster, one tile each, summed in part order
+    // through its shared memory.  Else cols >= 8192 and >= 2 rows: two parts on
+    // the persistent grid adding into a zeroed Y (a cluster of two, one tile per
+    // CTA, measured slower there: 4096 x 14336 at 2048 tokens 0.208 -> 0.259 ms).
+    a.ks = 1;
+    a.cluster = 0;
+    if (cols >= 2048 && n_rt * 4 <= (int64_t)num_sms() / 2 && a.nrs_all >= 16) {
+        a.ks = 4;
+        a.cluster = 1;
+    } else if (cols >= 8192 && cols >= 2 * rows && a.nrs_all % 2 == 0) {
+        a.ks = 2;
+    }
     // 256-token tiles unless they cannot give half of the SMs a work item (a
     // tile's cost is mostly dequantising its weight rows: partly empty 256-token
     // tiles beat twice as many 128-token ones)
-    const int64_t n_rt = (rows + gd::BM - 1) / gd::BM;
-    const bool narrow = n_rt * ((m + 255) / 256) * a.ks < (int64_t)num_sms() / (a.ks == 2 ? 2 : 1);
+    const bool narrow = n_rt * ((m + 255) / 256) * a.ks < (int64_t)num_sms() / (a.ks == 1 ? 1 : 2);
     const int BN = narrow ? 128 : 256;
     CUtensorMap tmX, tmW;
     if (!make_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, (uint64_t)cols, (uint64_t)m, (uint64_t)cols * 2,
@@ -506,14 +577,19 @@ static int launch_gemm_deq_t(const void* W, int64_t rows, int64_t cols, const vo
         return -8;
     auto* k = narrow ? &k_gemm_deq_bf16<T, 128> : &k_gemm_deq_bf16<T, 256>;
     prepare_kernel(k, gd::THREADS, C::SMEM);
-    const int64_t n_tiles = n_rt * ((m + BN - 1) / BN) * a.ks;
-    const int grid = (int)std::min<int64_t>(n_tiles, num_sms());
+    const int64_t n_items = n_rt * ((m + BN - 1) / BN) * a.ks;
+    if (n_items > INT32_MAX) return -6;
     if (a.ks == 2) {
         // the parts add into Y: zero it first (in stream order, so no programmatic overlap)
         if (cudaMemsetAsync(Y, 0, (size_t)m * (size_t)rows * sizeof(float), st) != cudaSuccess) return -6;
         pdl = false;
     }
-    return launch_ex(k, dim3(grid), dim3(gd::THREADS), C::SMEM, st, pdl, tmX, tmW, a) == cudaSuccess ? 0 : -6;
+    // persistent over the work items, or (a cluster per tile) one item per CTA
+    const int grid = a.cluster ? (int)n_items : (int)std::min<int64_t>(n_items, num_sms());
+    return launch_ex_cluster(k, dim3(grid), dim3(gd::THREADS), C::SMEM, st, pdl, a.cluster ? a.ks : 1, tmX, tmW, a) ==
+                   cudaSuccess
+               ? 0
+               : -6;
 }
 
 }  // namespace qmv

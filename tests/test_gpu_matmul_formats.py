@@ -126,12 +126,16 @@ def test_formats_deterministic_and_token_independent(qmv):
         assert np.array_equal(part.view(np.uint32), Y[t0:t0 + n].view(np.uint32))
 
 
-@pytest.mark.parametrize("t,rows,cols,m", [(Q8_0, 200, 8192, 300), (Q6_K, 96, 16384, 1), (Q5_0, 1024, 8704, 77)])
+@pytest.mark.parametrize("t,rows,cols,m", [(Q8_0, 200, 8192, 300), (Q6_K, 96, 16384, 1), (Q5_0, 1024, 8704, 77),
+                                           (Q5_0, 896, 4864, 130), (Q8_0, 2600, 8192, 40)])
 def test_formats_k_split(qmv, orc, t, rows, cols, m):
-    """Rows much shorter than K (cols >= 8192 and >= 2 rows, an even number of
-    raw stages) run as two K halves that add into a zeroed Y: every output
-    checked, repeated calls bit-identical, and the last token's outputs the same
-    when it is multiplied alone (the split follows the weight's shape)."""
+    """Rows much shorter than K: few row tiles run as four K parts on the CTAs
+    of a thread-block cluster, summed in part order through its shared memory
+    (200 x 8192, 96 x 16384, 1024 x 8704, the Qwen2-0.5B down projection 896 x
+    4864 with unequal parts); more row tiles with cols >= 8192 and >= 2 rows as
+    two halves adding into a zeroed Y (2600 x 8192).  Every output checked,
+    repeated calls bit-identical, and the last token's outputs the same when it
+    is multiplied alone (the split follows the weight's shape)."""
     W = synth.weights(t, rows, cols, seed=28, tensor_id=rows + cols)
     Wd = dev(W)
     xb, xbits = bf16_x(m, cols, 28)
