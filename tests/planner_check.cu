@@ -32,7 +32,7 @@ static int check(const char* name, const int64_t* cols_list, int n_cols, int* ac
                     const int g16 = nv < 16 ? nv : 16;
                     GemvPlan pl{};
                     const bool ok = a < 2 ? plan_gemv<T>(a8, rows, cols, nv, pl, 4, 152)
-                                          : plan_gemv<T>(a8, rows, cols, g16, pl, rows_in_flight_rt(T, g16));
+                                          : plan_gemv<T>(a8, rows, cols, g16, pl, rows_in_flight_rt(T, g16, false));
                     if (!ok) continue;   // refused: shared memory
                     ++*accepted;
                     const int nb = (int)(cols / F::BS);
@@ -49,7 +49,7 @@ static int check(const char* name, const int64_t* cols_list, int n_cols, int* ac
                     if (pl.xhat_bytes != xhat_bytes(T, a8, pl.group, (int)cols)) fail("staged activations mis-sized", rows, cols, nv, a8);
                     if (pl.group > 1 && pl.xhat_bytes > kXhatMaxBytes) fail("staged activations over the limit", rows, cols, nv, a8);
                     if (pl.rpw != 1 && pl.rpw != 2 && pl.rpw != 4) fail("rows per warp not 1, 2 or 4", rows, cols, nv, a8);
-                    if (pl.n_chunks > 1 && pl.rpw > rows_in_flight_rt(T, pl.group))
+                    if (pl.n_chunks > 1 && pl.rpw > rows_in_flight_rt(T, pl.group, true))
                         fail("a multi-chunk row group wider than the decode width", rows, cols, nv, a8);
                 }
     return bad;
