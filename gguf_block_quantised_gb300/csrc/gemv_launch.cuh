@@ -16,7 +16,7 @@ constexpr int chunk_target_bytes()
 {
     return T == QMV_Q4_K ? 2560 : 4096;
 }
-constexpr size_t kXhatMaxBytes = 96 * 1024;      // staged activations per CTA
+constexpr size_t kXhatMaxBytes = 176 * 1024;     // staged activations per CTA
 constexpr size_t kSmemTwoPerSm = 112 * 1024;     // two CTAs per SM
 constexpr size_t kSmemOnePerSm = 227 * 1024;
 
