@@ -796,7 +796,10 @@ int qmv_launch_moe_gemm_mxfp4(const void* W3d, bool planar, bool mx, int n_exper
     // 192-token tiles when the experts average more than 96 routed pairs, so
     // that one tile pass over an expert's rows (one dequantisation of them)
     // covers its tokens
-    const int tbn = n_pairs > (int64_t)96 * n_expert ? 192 : 128;
+    // MX with at most 32 routed pairs per expert on average: 64-token tiles
+    // (the E2M1 operands cost little to form, so the MMA's padded columns are
+    // what a mostly empty 128-token tile wastes)
+    const int tbn = n_pairs > (int64_t)96 * n_expert ? 192 : (mx && n_pairs <= (int64_t)32 * n_expert) ? 64 : 128;
     k_moe_tiles<<<1, 32, 0, st>>>(offsets, active, tbn, tiles);
     CUtensorMap tmX, tmC, tmE;
     if (mx) {
@@ -854,6 +857,9 @@ int qmv_launch_moe_gemm_mxfp4(const void* W3d, bool planar, bool mx, int n_exper
             return tbn == 192 ? launch(&k_moe_gemm_mxfp4<true, false, 192>, RawCfg<true, false, 192>::THREADS,
                                        RawCfg<true, false, 192>::SMEM)
                               : launch(&k_moe_gemm_mxfp4<true, false, 128>, RawCfg<true>::THREADS, RawCfg<true>::SMEM);
+        if (tbn == 64)
+            return launch(&k_moe_gemm_mxfp4<true, true, 64>, RawCfg<true, true, 64>::THREADS,
+                          RawCfg<true, true, 64>::SMEM);
         return tbn == 192
                    ? launch(&k_moe_gemm_mxfp4<true, true, 192>, RawCfg<true, true, 192>::THREADS,
                             RawCfg<true, true, 192>::SMEM)
@@ -863,6 +869,9 @@ int qmv_launch_moe_gemm_mxfp4(const void* W3d, bool planar, bool mx, int n_exper
         return tbn == 192 ? launch(&k_moe_gemm_mxfp4<false, false, 192>, RawCfg<false, false, 192>::THREADS,
                                    RawCfg<false, false, 192>::SMEM)
                           : launch(&k_moe_gemm_mxfp4<false, false, 128>, RawCfg<false>::THREADS, RawCfg<false>::SMEM);
+    if (tbn == 64)
+        return launch(&k_moe_gemm_mxfp4<false, true, 64>, RawCfg<false, true, 64>::THREADS,
+                      RawCfg<false, true, 64>::SMEM);
     return tbn == 192 ? launch(&k_moe_gemm_mxfp4<false, true, 192>, RawCfg<false, true, 192>::THREADS,
                                RawCfg<false, true, 192>::SMEM)
                       : launch(&k_moe_gemm_mxfp4<false, true, 128>, RawCfg<false, true>::THREADS,
