@@ -221,7 +221,7 @@ inline int launch_moe_t(bool a8, bool quant_x, const void* W3d, int n_expert, in
     // holds at most n_tok pairs: the vector group is sized for that (an expert
     // with more pairs takes several groups).
     const int cap = n_tok < n_pairs ? n_tok : n_pairs;
-    const int gmax = cap < 16 ? (cap > 0 ? cap : 1) : 16;
+    const int gmax = cap < 8 ? (cap > 0 ? cap : 1) : 8;
     if (!plan_gemv<T>(a8, rows, cols, gmax, pl, rows_in_flight_rt(T, gmax, false))) return -2;
     MoeParams mp{};
     GemvParams& p = mp.g;
