@@ -69,21 +69,17 @@ __device__ __forceinline__ float scaled(float v, float s, float id)
 }
 
 // ---- the 32-element formats: eight threads per block --------------------------------
-template <int T, bool BF>
-__global__ void __launch_bounds__(256) k_quant_w32(const void* __restrict__ x, uint8_t* __restrict__ out,
-                                                   int64_t nblk)
+// One block's share of thread `part` (weights 4*part .. +3 in v); every lane of
+// the warp calls it (the reductions are shuffles over the block's eight lanes).
+template <int T>
+__device__ __forceinline__ void quant_w32_item(float (&v)[4], int64_t blk, int part, bool valid,
+                                               uint8_t* __restrict__ out)
 {
     constexpr bool Q0 = T == QMV_Q4_0 || T == QMV_Q5_0, Q1 = T == QMV_Q4_1 || T == QMV_Q5_1, Q8 = T == QMV_Q8_0;
     constexpr int BITS = (T == QMV_Q4_0 || T == QMV_Q4_1) ? 4 : 5;
     constexpr int BB = T == QMV_Q4_0 ? 18 : T == QMV_Q5_0 ? 22 : T == QMV_Q4_1 ? 20 : T == QMV_Q5_1 ? 24 : 34;
     constexpr float kHalf = (float)(1 << (BITS - 1));
     constexpr float kTop = (float)((1 << BITS) - 1);
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t blk = i >> 3;
-    const int part = (int)(i & 7);
-    const bool valid = blk < nblk;           // the same for the eight lanes of a block
-    float v[4] = {0.f, 0.f, 0.f, 0.f};
-    if (valid) load4<BF>(x, i, v);
 
     float d = 0.f, id = 0.f, mn = 0.f;
     uint32_t codes = 0, hi_bits = 0;
@@ -192,6 +188,31 @@ __global__ void __launch_bounds__(256) k_quant_w32(const void* __restrict__ x, u
             qs[0] = (uint16_t)(b & 0xffffu);
             qs[1] = (uint16_t)(b >> 16);
         }
+    }
+}
+
+// Each thread takes ITEMS blocks a grid apart, all its loads issued first (more
+// bytes in flight per thread: a bf16 thread reads only 8 bytes per block).
+template <int T, bool BF, int ITEMS>
+__global__ void __launch_bounds__(256) k_quant_w32(const void* __restrict__ x, uint8_t* __restrict__ out,
+                                                   int64_t nblk)
+{
+    const int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;   // a multiple of 8: blocks stay whole
+    float v[ITEMS][4];
+    bool valid[ITEMS];
+#pragma unroll
+    for (int j = 0; j < ITEMS; ++j) {
+        const int64_t i = i0 + j * stride;
+        valid[j] = (i >> 3) < nblk;   // the same for the eight lanes of a block
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[j][k] = 0.f;
+        if (valid[j]) load4<BF>(x, i, v[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < ITEMS; ++j) {
+        const int64_t i = i0 + j * stride;
+        quant_w32_item<T>(v[j], i >> 3, (int)(i & 7), valid[j], out);
     }
 }
 
@@ -346,8 +367,10 @@ static int launch_w32(const void* W, int64_t n, void* out, cudaStream_t st)
 {
     const int64_t nblk = n / 32;
     if (nblk == 0) return 0;
-    const int64_t threads = nblk * 8;
-    k_quant_w32<T, BF><<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(W, static_cast<uint8_t*>(out), nblk);
+    constexpr int ITEMS = BF ? 4 : 2;
+    const int64_t threads = (nblk * 8 + ITEMS - 1) / ITEMS;
+    k_quant_w32<T, BF, ITEMS><<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(W, static_cast<uint8_t*>(out),
+                                                                                nblk);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
