@@ -39,7 +39,7 @@ __device__ __forceinline__ void unit_values(const uint8_t* blk, int s, float (&v
         for (int k = 0; k < 8; ++k)
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const uint32_t byte = (w.c[k] >> (8 * j)) & 0xffu;
+                const uint32_t byte = (w.code(k) >> (8 * j)) & 0xffu;
                 const int q = F::SIGNED ? (int)(int8_t)byte : (int)byte - F::OFF;
                 if constexpr (F::MIN) v[unit_elem<T>(k, j)] = __fmaf_rn(w.d, (float)q, w.m);   // one rounding
                 else v[unit_elem<T>(k, j)] = w.d * (float)q;   // exact: <= 24 significant bits

@@ -133,7 +133,7 @@ __device__ __forceinline__ void gemv_rows(const GemvParams& p, const XView& X, c
                     F::load_x_a8(X, v, b, sub, xu);
 #pragma unroll
                     for (int j = 0; j < RIF; ++j)
-                        if (j < nrows) O::acc_a8(w[j], xu, acc[j][v]);
+                        if (j < nrows) O::template acc_a8<(NV <= 2)>(w[j], xu, acc[j][v]);
                 } else {
 #pragma unroll
                     for (int j = 0; j < RIF; ++j)

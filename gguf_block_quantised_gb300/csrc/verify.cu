@@ -55,7 +55,7 @@ __global__ void k_dequant(const uint8_t* __restrict__ W, int64_t rows, int cols,
             for (int k = 0; k < 8; ++k)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const uint32_t byte = (w.c[k] >> (8 * j)) & 0xffu;
+                    const uint32_t byte = (w.code(k) >> (8 * j)) & 0xffu;
                     const int q = F::SIGNED ? (int)(int8_t)byte : (int)byte - F::OFF;
                     if constexpr (F::MIN) o[elem_of<T>(sub, k, j)] = __fmaf_rn(w.d, (float)q, w.m);   // one rounding
                     else o[elem_of<T>(sub, k, j)] = w.d * (float)q;   // exact: <= 24 significant bits
