@@ -20,7 +20,9 @@
 //               memory, M = 128 rows, N = BN tokens, K = 16, fp32 accumulator
 //   warps 4-11  epilogue: TMEM -> registers -> Y, two warps per TMEM lane
 //               quarter, each half of the columns; the accumulator is released
-//               as soon as its last columns are in registers
+//               as soon as its last columns are in registers.  Two accumulators
+//               (all 512 TMEM columns at 256 tokens): one tile's epilogue
+//               overlaps the next tile's MMAs.
 // K beyond cols reads zeros (the tensor maps' out-of-bounds fill), so cols need
 // only be a multiple of 8 (16-byte rows).  Every mbarrier wait is bounded; on a
 // timeout the kernel flags the status word, unwinds and frees its TMEM.
@@ -42,13 +44,13 @@ constexpr int BM = 128, BK = 64;           // BK: k of one 128-byte swizzled row
 constexpr int A_BOX = BM * BK * 2;         // 16384
 constexpr int EPI_WARP0 = 4, EPI_WARPS = 8;
 constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);   // 384
-constexpr uint32_t TMEM_COLS = 256;
+constexpr uint32_t TMEM_COLS = 512;   // two accumulators of up to 256 columns (A and B are in shared memory)
 template <int BN>
 struct Cfg {
     static constexpr int X_BOX = BN * BK * 2;                     // 16384 / 32768
     static constexpr int STAGE = 2 * A_BOX + 2 * X_BOX;           // one 128-k stage
     static constexpr int SK = BN == 256 ? 2 : 3;                  // stages
-    static constexpr int NBUF = BN == 256 ? 1 : 2;                // accumulators
+    static constexpr int NBUF = 2;   // accumulators: one tile's epilogue overlaps the next tile's MMAs
     static constexpr int OFF_BAR = SK * STAGE;
     static constexpr int SMEM = OFF_BAR + (2 * SK + 4) * 8 + 16 + 1024;   // + alignment slack
     static_assert(SMEM <= 227 * 1024, "shared memory");
