@@ -75,12 +75,15 @@ def test_formats_ragged_k(qmv, orc, t, cols):
 
 
 @pytest.mark.parametrize("t,rows,cols,m", [(Q8_0, 9700, 256, 500), (Q5_0, 19500, 256, 200), (Q5_0, 9600, 256, 300),
-                                           (Q6_K, 4000, 256, 1100), (Q6_K, 5000, 2048, 300), (Q4_0, 4000, 512, 1100)])
+                                           (Q6_K, 4000, 256, 1100), (Q6_K, 5000, 2048, 300), (Q4_0, 4000, 512, 1100),
+                                           (BF16, 9700, 256, 600), (F16, 5000, 512, 700)])
 def test_formats_many_tiles(qmv, orc, t, rows, cols, m):
     """More tiles than SMs with 256-token tiles (9700 x 500, 19500 x 200,
     4000 x 1100) and with 128-token tiles (9600 x 300: 225 tiles, two on some
     CTAs; 5000 x 300), ragged in both directions; Q6_K both in two passes
-    (256 k: 210-byte rows) and inside the GEMM."""
+    (256 k: 210-byte rows) and inside the GEMM; the plain bf16 GEMM's two
+    accumulators over several tiles per CTA (BF16 rows as they are, F16 rows
+    through the workspace)."""
     check(qmv, orc, t, rows, cols, m, 23)
 
 
