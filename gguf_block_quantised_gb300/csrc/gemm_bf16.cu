@@ -83,8 +83,15 @@ __global__ void __launch_bounds__(gb::THREADS, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // Tile t covers token tile t % n_nt of row tile t / n_nt: the CTAs running
+    // at once share few weight row tiles, read from DRAM once and then from L2
+    // by each of their token tiles, while the (smaller) activations stay in L2
+    // for every row tile.  (Token tiles outermost streamed all the weights
+    // once per token tile: 5.4 times the operands' bytes at 14336 x 4096 x
+    // 2048.)
     const int n_rt = (int)((a.rows + BM - 1) / BM);
-    const int n_tiles = n_rt * ((a.m + BN - 1) / BN);
+    const int n_nt = (a.m + BN - 1) / BN;
+    const int n_tiles = n_rt * n_nt;
     const int nks = (a.cols + 2 * BK - 1) / (2 * BK);   // 128-k stages per tile
 
     if (tid == 0) {
@@ -113,7 +120,7 @@ __global__ void __launch_bounds__(gb::THREADS, 1)
             int s = 0;
             uint32_t ph = 1;
             for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x) {
-                const int rt = t % n_rt, nt = t / n_rt;
+                const int rt = t / n_nt, nt = t % n_nt;
                 for (int ks = 0; ks < nks; ++ks) {
                     if (!mbar_wait_backoff(&empty[s], ph, a.status, 64)) { fail(); break; }
                     uint8_t* st = smem + s * C::STAGE;
@@ -165,7 +172,7 @@ __global__ void __launch_bounds__(gb::THREADS, 1)
         const int q = warp & 3, ch = (warp - EPI_WARP0) >> 2;
         int local = 0;
         for (int t = blockIdx.x; t < n_tiles && !__any_sync(0xffffffffu, *abort_flag); t += gridDim.x, ++local) {
-            const int rt = t % n_rt, nt = t / n_rt;
+            const int rt = t / n_nt, nt = t % n_nt;
             const int buf = local % NBUF;
             const uint32_t use = (uint32_t)(local / NBUF);
             // warp-uniform: every lane must take part in the tcgen05.ld below

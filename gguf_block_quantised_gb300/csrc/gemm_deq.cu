@@ -323,7 +323,7 @@ __global__ void __launch_bounds__(gd::THREADS, 1)
             int s = 0;
             uint32_t ph = 1;
             for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x) {
-                const int nt = t / a.ks / n_rt, part = t % a.ks;
+                const int nt = (t / a.ks) % n_nt, part = t % a.ks;
                 const int k0 = rs_begin(part) * C::AST, nks = (rs_begin(part + 1) - rs_begin(part)) * C::AST;
                 for (int ks = 0; ks < nks; ++ks) {
                     if (!mbar_wait_backoff(&empty[s], ph, a.status, 64)) { fail(); break; }
@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(gd::THREADS, 1)
             int sr = 0;
             uint32_t ph = 1;
             for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x) {
-                const int rt = (t / a.ks) % n_rt, part = t % a.ks;
+                const int rt = t / a.ks / n_nt, part = t % a.ks;
                 bool bad = false;
                 for (int rs = rs_begin(part); rs < rs_begin(part + 1); ++rs) {
                     const int kb = rs * C::BPR;
@@ -428,7 +428,7 @@ __global__ void __launch_bounds__(gd::THREADS, 1)
         const int q = warp & 3, ch = (warp - EPI_WARP0) >> 2;
         int local = 0;
         for (int t = blockIdx.x; t < n_tiles && !__any_sync(0xffffffffu, *abort_flag); t += gridDim.x, ++local) {
-            const int rt = (t / a.ks) % n_rt, nt = t / a.ks / n_rt;
+            const int rt = t / a.ks / n_nt, nt = (t / a.ks) % n_nt;
             const int buf = local % NBUF;
             const uint32_t use = (uint32_t)(local / NBUF);
             // warp-uniform: every lane must take part in the tcgen05.ld below
@@ -483,7 +483,7 @@ __global__ void __launch_bounds__(gd::THREADS, 1)
         // others' stores into its X area; the second, the stores before the sums.
         cluster_sync();
         const int t = blockIdx.x, part = t % a.ks;
-        const int rt = (t / a.ks) % n_rt, nt = t / a.ks / n_rt;
+        const int rt = t / a.ks / n_nt, nt = (t / a.ks) % n_nt;
         const int qpr = 4 / a.ks;   // lane quarters per owner
         float* red = reinterpret_cast<float*>(smem);
         if (warp >= EPI_WARP0) {

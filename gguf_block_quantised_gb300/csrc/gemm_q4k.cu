@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(gq::THREADS, 1)
             int s = 0;
             uint32_t ph = 1;
             for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x) {
-                const int nt = t / a.ks / n_rt, k0 = (t % a.ks) * nks;
+                const int nt = (t / a.ks) % n_nt, k0 = (t % a.ks) * nks;
                 for (int ks = 0; ks < nks; ++ks) {
                     if (!mbar_wait_backoff(&empty[s], ph, a.status, 64)) { fail(); break; }
                     mbar_arrive_expect_tx(&full[s], KSUB * X_BYTES);
@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(gq::THREADS, 1)
             int s = 0;
             uint32_t ph = 1;
             for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x) {
-                const int rt = (t / a.ks) % n_rt, sb0 = (t % a.ks) * nsb;
+                const int rt = t / a.ks / n_nt, sb0 = (t % a.ks) * nsb;
                 for (int sb = 0; sb < nsb; ++sb) {
                     if (!mbar_wait_bounded(&re[s], ph, a.status)) { fail(); break; }
                     mbar_arrive_expect_tx(&rf[s], R_BYTES);
@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(gq::THREADS, 1)
         const int q = warp & 3, ch = (warp - EPI_WARP0) >> 2;
         int local = 0;
         for (int t = blockIdx.x; t < n_tiles && !__any_sync(0xffffffffu, *abort_flag); t += gridDim.x, ++local) {
-            const int rt = (t / a.ks) % n_rt, nt = t / a.ks / n_rt;
+            const int rt = t / a.ks / n_nt, nt = (t / a.ks) % n_nt;
             const int buf = local % NBUF;
             const uint32_t use = (uint32_t)(local / NBUF);
             // warp-uniform: every lane must take part in the tcgen05.ld below

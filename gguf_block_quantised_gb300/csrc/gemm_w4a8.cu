@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(w8::THREADS, 1)
             int xs = 0, cs = 0;
             uint32_t xph = 1, cph = 1;
             for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x) {
-                const int nt = t / n_rt;
+                const int nt = t % n_nt;
                 bool bad = false;
                 for (int sb = 0; sb < nsb && !bad; ++sb) {
                     if (!mbar_wait_backoff(&cempty[cs], cph, a.status, 64)) { bad = true; break; }
@@ -248,7 +248,7 @@ __global__ void __launch_bounds__(w8::THREADS, 1)
             int rs = 0;
             uint32_t ph = 1;
             for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x) {
-                const int rt = t % n_rt;
+                const int rt = t / n_nt;
                 bool bad = false;
                 for (int sb = 0; sb < nsb; ++sb) {
                     if (!mbar_wait_backoff(&rempty[rs], ph, a.status, 64)) { bad = true; break; }
@@ -383,7 +383,7 @@ __global__ void __launch_bounds__(w8::THREADS, 1)
         int cs = 0;
         uint32_t cph = 0;
         for (int t = blockIdx.x; t < n_tiles && !__any_sync(0xffffffffu, *abort_flag); t += gridDim.x) {
-            const int rt = t % n_rt, nt = t / n_rt;
+            const int rt = t / n_nt, nt = t % n_nt;
             float acc[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) acc[i] = 0.f;
