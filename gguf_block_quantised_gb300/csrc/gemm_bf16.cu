@@ -328,11 +328,20 @@ static int launch_gemm_bf16(const void* Wb, int64_t rows, int64_t cols, const vo
     a.m = (int)m;
     a.Y = Y;
     a.status = status_word();
-    // 256-token tiles unless they cannot give every SM a tile or pad the tokens
-    // by more than 128-token tiles would (by over 8%)
+    // The token tile width with the larger expected throughput: the useful
+    // fraction of the padded tokens, times the fraction of the SMs busy over
+    // the waves of tiles, times 0.9 for 128-token tiles (their measured
+    // throughput against 256-token tiles when both fill whole waves).  Against
+    // A/B runs of both widths (14336 x 4096 at 512, 768, 1024, 1536 and 2048
+    // tokens; 4096 x 14336 at 512 and 1024) it picks the faster one, or one
+    // within 2% of it.
     const int64_t n_rt = (rows + gb::BM - 1) / gb::BM;
-    const int64_t pad256 = (m + 255) / 256 * 256, pad128 = (m + 127) / 128 * 128;
-    const bool narrow = n_rt * ((m + 255) / 256) < (int64_t)num_sms() || pad256 * 100 > pad128 * 108;
+    auto score = [&](int64_t bn) {
+        const int64_t nt = (m + bn - 1) / bn, tiles = n_rt * nt, sms = num_sms();
+        const int64_t waves = (tiles + sms - 1) / sms;
+        return (double)m / (double)(nt * bn) * (double)tiles / (double)(waves * sms) * (bn == 128 ? 0.9 : 1.0);
+    };
+    const bool narrow = score(128) > score(256);
     const int BN = narrow ? 128 : 256;
     if (!make_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, (uint64_t)cols, (uint64_t)m, (uint64_t)cols * 2,
                       gb::BK, (uint32_t)BN, CU_TENSOR_MAP_SWIZZLE_128B))
