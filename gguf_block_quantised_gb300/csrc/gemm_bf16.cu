@@ -12,8 +12,8 @@
 // their GEMMs: gemm_q4k.cu, gemm_deq.cu.)
 //
 // One persistent CTA per SM, 12 warps:
-//   warp 0      TMA producer: per 128-k stage two boxes of weight rows
-//               W[128 rows][64 k] and two of tokens X[BN][64 k] (bf16,
+//   warp 0      TMA producer: per stage one or two 64-k boxes of weight rows
+//               W[128 rows][64 k] and as many of tokens X[BN][64 k] (bf16,
 //               128-byte swizzle, the UMMA K-major canonical layout)
 //   warp 1      TMEM owner (alloc/free) and the single-thread MMA issuer:
 //               tcgen05.mma.cta_group::1.kind::f16, A and B from shared
@@ -45,11 +45,17 @@ constexpr int A_BOX = BM * BK * 2;         // 16384
 constexpr int EPI_WARP0 = 4, EPI_WARPS = 8;
 constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);   // 384
 constexpr uint32_t TMEM_COLS = 512;   // two accumulators of up to 256 columns (A and B are in shared memory)
+// Stages: four of 64 k at 256 tokens, three of 128 k at 128 tokens (192 KB
+// either way).  A/B at 256 tokens against two 128-k stages: BF16 14336 x 4096
+// x 2048 tokens 1372 -> 1545 TFLOP/s, 4096 x 14336 x 2048 1196 -> 1379; at
+// 128 tokens six 64-k stages measured slower than three of 128 k (958 -> 903
+// at 14336 x 4096 x 512).
 template <int BN>
 struct Cfg {
     static constexpr int X_BOX = BN * BK * 2;                     // 16384 / 32768
-    static constexpr int STAGE = 2 * A_BOX + 2 * X_BOX;           // one 128-k stage
-    static constexpr int SK = BN == 256 ? 2 : 3;                  // stages
+    static constexpr int KSUB = BN == 256 ? 1 : 2;                // 64-k boxes of each operand per stage
+    static constexpr int STAGE = KSUB * (A_BOX + X_BOX);
+    static constexpr int SK = BN == 256 ? 4 : 3;                  // stages
     static constexpr int NBUF = 2;   // accumulators: one tile's epilogue overlaps the next tile's MMAs
     static constexpr int OFF_BAR = SK * STAGE;
     static constexpr int SMEM = OFF_BAR + (2 * SK + 4) * 8 + 16 + 1024;   // + alignment slack
@@ -92,7 +98,8 @@ __global__ void __launch_bounds__(gb::THREADS, 1)
     const int n_rt = (int)((a.rows + BM - 1) / BM);
     const int n_nt = (a.m + BN - 1) / BN;
     const int n_tiles = n_rt * n_nt;
-    const int nks = (a.cols + 2 * BK - 1) / (2 * BK);   // 128-k stages per tile
+    constexpr int KSUB = C::KSUB;
+    const int nks = (a.cols + KSUB * BK - 1) / (KSUB * BK);   // stages per tile
 
     if (tid == 0) {
         for (int i = 0; i < SK; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
@@ -126,9 +133,9 @@ __global__ void __launch_bounds__(gb::THREADS, 1)
                     uint8_t* st = smem + s * C::STAGE;
                     mbar_arrive_expect_tx(&full[s], C::STAGE);
 #pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        tma_load_2d(st + j * A_BOX, &tmW, (2 * ks + j) * BK, rt * BM, &full[s]);
-                        tma_load_2d(st + 2 * A_BOX + j * C::X_BOX, &tmX, (2 * ks + j) * BK, nt * BN, &full[s]);
+                    for (int j = 0; j < KSUB; ++j) {
+                        tma_load_2d(st + j * A_BOX, &tmW, (KSUB * ks + j) * BK, rt * BM, &full[s]);
+                        tma_load_2d(st + KSUB * A_BOX + j * C::X_BOX, &tmX, (KSUB * ks + j) * BK, nt * BN, &full[s]);
                     }
                     if (++s == SK) { s = 0; ph ^= 1; }
                 }
@@ -153,9 +160,9 @@ __global__ void __launch_bounds__(gb::THREADS, 1)
                     tc_fence_after();
                     const uint8_t* st = smem + s * C::STAGE;
 #pragma unroll
-                    for (int j = 0; j < 2; ++j) {
+                    for (int j = 0; j < KSUB; ++j) {
                         const uint64_t adesc = smem_desc_sw128(st + j * A_BOX);
-                        const uint64_t bdesc = smem_desc_sw128(st + 2 * A_BOX + j * C::X_BOX);
+                        const uint64_t bdesc = smem_desc_sw128(st + KSUB * A_BOX + j * C::X_BOX);
 #pragma unroll
                         for (int k4 = 0; k4 < BK / 16; ++k4)   // 32 bytes per K = 16 step in both operands
                             mma_f16(d, adesc + 2 * k4, bdesc + 2 * k4, idesc, (ks | j | k4) != 0);
@@ -330,16 +337,14 @@ static int launch_gemm_bf16(const void* Wb, int64_t rows, int64_t cols, const vo
     a.status = status_word();
     // The token tile width with the larger expected throughput: the useful
     // fraction of the padded tokens, times the fraction of the SMs busy over
-    // the waves of tiles, times 0.9 for 128-token tiles (their measured
-    // throughput against 256-token tiles when both fill whole waves).  Against
-    // A/B runs of both widths (14336 x 4096 at 512, 768, 1024, 1536 and 2048
-    // tokens; 4096 x 14336 at 512 and 1024) it picks the faster one, or one
-    // within 2% of it.
+    // the waves of tiles, times 0.8 for 128-token tiles (their measured
+    // throughput against 256-token tiles when both fill whole waves: 1241
+    // against 1545 TFLOP/s at 14336 x 4096 x 2048).
     const int64_t n_rt = (rows + gb::BM - 1) / gb::BM;
     auto score = [&](int64_t bn) {
         const int64_t nt = (m + bn - 1) / bn, tiles = n_rt * nt, sms = num_sms();
         const int64_t waves = (tiles + sms - 1) / sms;
-        return (double)m / (double)(nt * bn) * (double)tiles / (double)(waves * sms) * (bn == 128 ? 0.9 : 1.0);
+        return (double)m / (double)(nt * bn) * (double)tiles / (double)(waves * sms) * (bn == 128 ? 0.8 : 1.0);
     };
     const bool narrow = score(128) > score(256);
     const int BN = narrow ? 128 : 256;
