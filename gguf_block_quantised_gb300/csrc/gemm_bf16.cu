@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(gb::THREADS, 1)
     auto fail = [&]() { *abort_flag = 1; };
 
     if (warp == 0) {
-        // ---- weight rows and token tiles, two 64-k boxes of each per stage
+        // ---- weight rows and token tiles, KSUB 64-k boxes of each per stage
         if (lane == 0) {
             int s = 0;
             uint32_t ph = 1;
