@@ -675,11 +675,14 @@ def prefill_formats(q, torch, stream, tflops_peak):
     whole 16 bytes dequantise tiles into TMEM inside the GEMM (k_gemm_deq_bf16);
     the Qwen2-0.5B layer shapes whose rows are not (896 columns: 616-byte Q5_0
     rows) convert to bf16 in the workspace first (k_dequant_bf16 + k_gemm_bf16),
-    timed whole.  Four (W, X) copies rotate, as for Q4_K."""
+    timed whole.  BF16 rows go straight into the plain bf16 GEMM (k_gemm_bf16),
+    and MXFP4 rows (no tile dequantiser) take the two passes.  Four (W, X)
+    copies rotate, as for Q4_K."""
     out = {}
     cases = [(t, rows, cols, m) for t in (Q8_0, Q5_0, Q6_K, Q4_0) for rows, cols in ((14336, 4096), (4096, 14336))
              for m in (512, 2048)] + [(Q5_0, 4864, 896, 512), (Q5_0, 896, 4864, 512)]
-    names = {Q4_0: "Q4_0", Q5_0: "Q5_0", Q8_0: "Q8_0", Q6_K: "Q6_K"}
+    cases += [(t, 14336, 4096, m) for t in (BF16, MXFP4) for m in (512, 2048)]
+    names = {Q4_0: "Q4_0", Q5_0: "Q5_0", Q8_0: "Q8_0", Q6_K: "Q6_K", BF16: "BF16", MXFP4: "MXFP4"}
     ws = None
     for t, rows, cols, m in cases:
         flop = 2.0 * m * rows * cols
@@ -697,7 +700,8 @@ def prefill_formats(q, torch, stream, tflops_peak):
         q.qmv_set_workspace(None, 0)
         out[f"{names[t]}_{rows}x{cols}_m{m}"] = {
             "ms": ms, "tflops": flop / (ms / 1e3) / 1e12, "frac_of_peak": flop / (ms / 1e3) / 1e12 / tflops_peak,
-            "path": "two passes (bf16 in the workspace)" if need else "tiles dequantised inside the GEMM"}
+            "path": "two passes (bf16 in the workspace)" if need else
+                    ("bf16 rows as they are" if t == BF16 else "tiles dequantised inside the GEMM")}
         del Ws, Xs, Y
     q.qmv_get_status(stream)
     return out
