@@ -97,13 +97,17 @@ def test_formats_fused_tiles(qmv, orc, t, rows, cols, m):
 
 
 @pytest.mark.parametrize("t,rows,cols,m", [(Q5_0, 4864, 896, 512), (Q8_0, 896, 4864, 512), (Q8_0, 151936, 896, 64),
-                                           (Q5_0, 896, 896, 2048), (Q6_K, 4096, 14336, 512)])
+                                           (Q5_0, 896, 896, 2048), (Q6_K, 4096, 14336, 512),
+                                           (BF16, 14336, 4096, 2048), (BF16, 4096, 14336, 512),
+                                           (MXFP4, 14336, 4096, 512)])
 def test_formats_model_shapes_sampled(qmv, orc, t, rows, cols, m):
     """Qwen2-0.5B-shaped matrices in its GGUF formats (the layers in Q5_0, the
     vocabulary projection in Q8_0: 896 is not a multiple of the 256-element
-    K-quant super-block) and a 14336-wide Q6_K down projection: 40 sampled rows
-    for 64 sampled tokens checked by the oracle, first and last of each
-    included."""
+    K-quant super-block), a 14336-wide Q6_K down projection, and the
+    configuration's full-size shapes as BF16 rows (the plain GEMM's 64-k stages
+    at 256-token tiles, its 128-k stages at 128-token tiles) and as MXFP4 rows
+    (two passes): 40 sampled rows for 64 sampled tokens checked by the oracle,
+    first and last of each included."""
     W = synth.weights(t, rows, cols, seed=24, tensor_id=rows * 3 + cols)
     xb, xbits = bf16_x(m, cols, 24)
     Y = run(qmv, t, dev(W), rows, cols, xb, m)
