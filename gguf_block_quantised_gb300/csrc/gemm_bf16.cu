@@ -335,18 +335,9 @@ static int launch_gemm_bf16(const void* Wb, int64_t rows, int64_t cols, const vo
     a.m = (int)m;
     a.Y = Y;
     a.status = status_word();
-    // The token tile width with the larger expected throughput: the useful
-    // fraction of the padded tokens, times the fraction of the SMs busy over
-    // the waves of tiles, times 0.8 for 128-token tiles (their measured
-    // throughput against 256-token tiles when both fill whole waves: 1241
-    // against 1545 TFLOP/s at 14336 x 4096 x 2048).
+    // 128- or 256-token tiles by the wave model of gemm_bf16_narrow
     const int64_t n_rt = (rows + gb::BM - 1) / gb::BM;
-    auto score = [&](int64_t bn) {
-        const int64_t nt = (m + bn - 1) / bn, tiles = n_rt * nt, sms = num_sms();
-        const int64_t waves = (tiles + sms - 1) / sms;
-        return (double)m / (double)(nt * bn) * (double)tiles / (double)(waves * sms) * (bn == 128 ? 0.8 : 1.0);
-    };
-    const bool narrow = score(128) > score(256);
+    const bool narrow = gemm_bf16_narrow(rows, m, num_sms());
     const int BN = narrow ? 128 : 256;
     if (!make_tmap_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, (uint64_t)cols, (uint64_t)m, (uint64_t)cols * 2,
                       gb::BK, (uint32_t)BN, CU_TENSOR_MAP_SWIZZLE_128B))

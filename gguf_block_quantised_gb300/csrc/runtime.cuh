@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <cstdint>
 #include <atomic>
 #include <mutex>
 #include <utility>
@@ -28,6 +29,23 @@ inline int num_sms()
         if (d >= 0 && d < kMaxDevices) cache[d].store(v, std::memory_order_relaxed);
     }
     return v;
+}
+
+// Token tile width of the plain bf16 prefill GEMM (k_gemm_bf16): true for
+// 128-token tiles, false for 256.  The width with the larger expected
+// throughput: the useful fraction of the padded tokens, times the fraction of
+// the SMs busy over the waves of tiles, times 0.8 for 128-token tiles (their
+// measured throughput against 256-token tiles when both fill whole waves: 1241
+// against 1545 TFLOP/s at 14336 x 4096 x 2048).
+inline bool gemm_bf16_narrow(int64_t rows, int64_t m, int64_t sms)
+{
+    const int64_t n_rt = (rows + 127) / 128;
+    auto score = [&](int64_t bn) {
+        const int64_t nt = (m + bn - 1) / bn, tiles = n_rt * nt;
+        const int64_t waves = (tiles + sms - 1) / sms;
+        return (double)m / (double)(nt * bn) * (double)tiles / (double)(waves * sms) * (bn == 128 ? 0.8 : 1.0);
+    };
+    return score(128) > score(256);
 }
 
 // Device address of the library's status word (defined in api.cu).

@@ -55,6 +55,29 @@ static int check(const char* name, const int64_t* cols_list, int n_cols, int* ac
     return bad;
 }
 
+// The plain bf16 GEMM's tile width model against the faster width of A/B runs
+// of both widths on a 152-SM GB300 (BF16 rows), and two limits: a single
+// 128-token tile for at most 128 tokens, 256-token tiles when they fill whole
+// waves without padding.
+static int check_gemm_bf16_width()
+{
+    struct Case { int64_t rows, m; bool narrow; };
+    const Case cases[] = {{14336, 512, true},  {14336, 768, false}, {14336, 1024, false}, {14336, 1536, false},
+                          {14336, 2048, false}, {4096, 512, true},   {4096, 1024, false}};
+    int bad = 0;
+    for (const Case& c : cases)
+        if (gemm_bf16_narrow(c.rows, c.m, 152) != c.narrow) {
+            std::printf("bf16 GEMM width: rows=%lld m=%lld picks %d tokens\n", (long long)c.rows, (long long)c.m,
+                        gemm_bf16_narrow(c.rows, c.m, 152) ? 128 : 256);
+            ++bad;
+        }
+    for (int64_t rows : {128, 4096, 14336, 151936})
+        for (int64_t m : {1, 64, 127, 128})
+            if (!gemm_bf16_narrow(rows, m, 152)) { std::printf("bf16 GEMM width: m=%lld not 128\n", (long long)m); ++bad; }
+    if (gemm_bf16_narrow(152 * 128, 256 * 3, 152)) { std::printf("bf16 GEMM width: whole waves not 256\n"); ++bad; }
+    return bad;
+}
+
 int main()
 {
     const int64_t c32[] = {32, 96, 896, 2880, 4096, 4864, 8288, 14336, 32768, 65536};
@@ -66,6 +89,7 @@ int main()
     bad += check<QMV_MXFP4>("MXFP4", c32, 10, &accepted);
     bad += check<QMV_Q4_K>("Q4_K", c256, 6, &accepted);
     bad += check<QMV_Q6_K>("Q6_K", c256, 6, &accepted);
+    bad += check_gemm_bf16_width();
     std::printf("plans accepted %d, violations %d\n", accepted, bad);
     return bad ? 1 : 0;
 }
