@@ -129,3 +129,26 @@ def test_binding_raises_with_message(lib):
     with pytest.raises(q.QmvError) as e:
         q.qmv_matvec(q.FMT(q.Q4_K, q.F32), 4096, 8, 300, 4096, 4096, 1, stream=0)
     assert e.value.code == q.ERR_SHAPE and "multiple of 256" in str(e.value)
+
+
+def test_matmul_workspace_follows_the_prefill_route(lib):
+    """qmv_workspace_size(QMV_OP_MATMUL, ...) names the route qmv_matmul takes:
+    none for Q4_K, for BF16 rows, and for Q4_0 / Q5_0 / Q8_0 / Q6_K rows that
+    are a whole number of 16 bytes (tiles dequantised inside the GEMM); the bf16
+    weight tiles (rows x cols x 2 bytes) for every other type and row length;
+    the W4A8 form's codes, sums and scales for Q4_K x Q8_K."""
+    F = q.FMT
+    rows = 1000
+    for t, cols in [(q.Q4_0, 4096), (q.Q5_0, 4096), (q.Q8_0, 4096), (q.Q6_K, 2048), (q.Q6_K, 14336),
+                    (q.Q4_K, 4096), (q.BF16, 896), (q.BF16, 4096)]:
+        assert q.qmv_workspace_size(q.OP_MATMUL, F(t, q.BF16), rows, cols, 512) == 0, (t, cols)
+    # rows not a whole number of 16 bytes: 896 columns of Q4_0 / Q5_0 / Q8_0 (504 / 616 / 952
+    # bytes), one Q6_K super-block (210 bytes)
+    two_pass = [(q.Q4_0, 896), (q.Q5_0, 896), (q.Q8_0, 896), (q.Q6_K, 256)]
+    two_pass += [(t, 4096) for t in (q.Q4_1, q.Q5_1, q.Q8_1, q.MXFP4, q.Q2_K, q.Q3_K, q.Q5_K, q.F32, q.F16)]
+    for t, cols in two_pass:
+        need = q.qmv_workspace_size(q.OP_MATMUL, F(t, q.BF16), rows, cols, 512)
+        assert need >= rows * cols * 2 and need < rows * cols * 2 + 256, (t, cols, need)
+    w4a8 = q.qmv_workspace_size(q.OP_MATMUL, F(q.Q4_K, q.Q8_K), rows, 4096, 512)
+    assert w4a8 >= 512 * 4096 * 2    # the activation codes as fp16, at least
+    assert q.qmv_workspace_size(q.OP_MATMUL, F(q.Q4_K, q.BF16), rows, 4096, 0) == 0
